@@ -1,0 +1,214 @@
+"""Plain, slow CPU oracle of the HashAttention sparse-decode path.
+
+TEST INFRASTRUCTURE ONLY. This module is imported by the tests, by
+``__graft_entry__.smoke()`` and by ``bench.py``'s CPU-baseline / reference arm,
+and by nothing else. The product path (the CUDA library and its Python binding)
+never imports, links or calls it, and it shares no code, table or helper with
+that path.
+
+Everything is NumPy in float64 (signature work in Python/NumPy integers), one
+(batch, query head) at a time, written straight from the definitions:
+
+* HashAttention: Semantic Sparsity for Faster Inference (Desai et al., ICML 2025,
+  arXiv:2412.14468v2)
+    - "Only selection is approximate; selected KV stay in full form" (Sec. 4):
+      z_i = <q, k_i>/sqrt(d); o_hat = sum_{i in I} e^{z_i} v_i / sum_{j in I} e^{z_j};
+      three stages SCORE / TOPK / GATHER-ATT.
+    - "A 32-bit signature makes scoring cheap" (Eqs. (1)-(2), Sec. 4.1):
+      SCORE(k_i, q) = -popcount(h_i XOR h_q).
+    - "Token-level sparsity still needs a careful kernel" (Sec. 4.4, budget
+      accounting): the retrieval budget m is joined by the first and the most
+      recent tokens of the context.
+* Nectar: Neural Estimation of Cached-Token Attention via Regression
+  (arXiv:2605.09778v2)
+    - Sec. 3, Eq. (3.1): alpha(q) = log sum_j e^{s_j} (log attention mass),
+      A(q) = sum_j e^{s_j} v_j / sum_j e^{s_j}.
+    - Eqs. (3.4)-(3.5): ATT_full = (e^alpha A + N_loc) / (e^alpha + Z_loc); the
+      split of the softmax sum is exact; gate form g = sigmoid(a - log Z_loc).
+
+Readings where the pages are silent (each is listed in the design notes):
+  * keep the m SMALLEST Hamming distances (SCORE is the negated distance);
+  * ties are broken by token index ascending, so the selected set is unique;
+  * T (top-min(m, n) over all n tokens) is UNIONED with the windows
+    [0, min(S, n)) and [max(0, n - Lw), n); duplicates are counted once;
+  * the softmax scale is 1/sqrt(d); lse is the natural log of the sum over I;
+  * an empty selected set gives out = 0 and lse = -inf;
+  * the query head h reads KV head h // G (contiguous GQA groups).
+
+Pins: ``tests/test_oracle_pins.py`` ties every function here to something
+other than itself (the worked examples printed on the pages, closed forms,
+brute force on tiny inputs, extended-precision arithmetic, and an independent
+library routine); ``tests/test_oracle_mutations.py`` plants plausible mistakes
+in copies of these functions and shows that a pin fails for each.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+N_BINS = 33  # a 32-bit Hamming distance takes the values 0..32
+
+
+# ---------------------------------------------------------------------------
+# SCORE -- HashAttention, Eq. (2): SCORE(k_i, q) = -popcount(h_i XOR h_q)
+# ---------------------------------------------------------------------------
+
+def popcount32(x) -> np.ndarray:
+    """Number of set bits of each 32-bit word, as the plain sum of its 32 bits."""
+    w = np.asarray(x).astype(np.int64) & 0xFFFFFFFF
+    total = np.zeros(w.shape, dtype=np.int64)
+    for j in range(32):
+        total += (w >> j) & 1
+    return total
+
+
+def hamming_distances(q_code, k_codes) -> np.ndarray:
+    """popcount(h_q XOR h_i) for every key code h_i (the negated SCORE)."""
+    q = np.int64(int(q_code) & 0xFFFFFFFF)
+    k = np.asarray(k_codes).astype(np.int64) & 0xFFFFFFFF
+    return popcount32(k ^ q)
+
+
+def distance_histogram(dist) -> np.ndarray:
+    """Count of tokens at each distance 0..32."""
+    return np.bincount(np.asarray(dist, dtype=np.int64), minlength=N_BINS)[:N_BINS]
+
+
+# ---------------------------------------------------------------------------
+# TOPK -- HashAttention, Sec. 4 (three stages) and Sec. 4.4 (fixed windows)
+# ---------------------------------------------------------------------------
+
+def top_m_by_score(dist, m: int) -> np.ndarray:
+    """Indices of the min(m, n) tokens with the highest SCORE, ascending.
+
+    Highest SCORE = smallest distance; ties go to the smaller token index.
+    """
+    dist = np.asarray(dist, dtype=np.int64)
+    n = dist.shape[0]
+    k = max(0, min(int(m), n))
+    order = np.lexsort((np.arange(n), dist))  # last key is primary: distance, then index
+    return np.sort(order[:k]).astype(np.int64)
+
+
+def window_positions(n: int, n_sink: int, n_local: int) -> np.ndarray:
+    """The first n_sink and the most recent n_local positions of an n-token context."""
+    sink = np.arange(0, max(0, min(int(n_sink), n)), dtype=np.int64)
+    local = np.arange(max(0, n - int(n_local)), n, dtype=np.int64)
+    return np.union1d(sink, local).astype(np.int64)
+
+
+def selected_set(q_code, k_codes, n: int, m: int, n_sink: int, n_local: int) -> np.ndarray:
+    """I = top-m by SCORE over all n tokens, joined with the sink/local windows."""
+    dist = hamming_distances(q_code, np.asarray(k_codes)[:n])
+    top = top_m_by_score(dist, m)
+    win = window_positions(n, n_sink, n_local)
+    return np.union1d(top, win).astype(np.int64)
+
+
+def max_reads(n: int, m: int, n_sink: int, n_local: int) -> int:
+    """Upper bound on |I|: the budget plus every fixed window position, capped at n."""
+    return min(n, m + n_sink + n_local)
+
+
+# ---------------------------------------------------------------------------
+# GATHER-ATT -- HashAttention, Sec. 4; log-normaliser from Nectar, Eq. (3.1)
+# ---------------------------------------------------------------------------
+
+def attend(q, K, V, idx):
+    """Softmax attention of one query over the rows ``idx`` of K/V, in float64.
+
+    Returns (out, lse): out = sum_i e^{z_i} v_i / sum_j e^{z_j} and
+    lse = log sum_j e^{z_j}, z_i = <q, k_i>/sqrt(d), i, j over idx.
+    Empty idx gives (zeros, -inf).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    d = q.shape[-1]
+    idx = np.asarray(idx, dtype=np.int64)
+    if idx.size == 0:
+        return np.zeros(np.asarray(V).shape[-1], dtype=np.float64), -math.inf
+    k_rows = np.asarray(K)[idx].astype(np.float64)
+    v_rows = np.asarray(V)[idx].astype(np.float64)
+    z = k_rows @ q / math.sqrt(d)
+    z_max = z.max()
+    w = np.exp(z - z_max)
+    total = w.sum()
+    lse = z_max + math.log(total)
+    out = (w / total) @ v_rows
+    return out, lse
+
+
+def merge(out_a, lse_a, out_b, lse_b):
+    """Exact merge of two partial attentions over disjoint token sets.
+
+    Nectar, Eq. (3.4): with e^{lse_a} the mass of part a and N_b = e^{lse_b} out_b,
+    ATT = (e^{lse_a} out_a + e^{lse_b} out_b) / (e^{lse_a} + e^{lse_b});
+    the merged log-normaliser is log(e^{lse_a} + e^{lse_b}).
+    """
+    out_a = np.asarray(out_a, dtype=np.float64)
+    out_b = np.asarray(out_b, dtype=np.float64)
+    if lse_a == -math.inf and lse_b == -math.inf:
+        return np.zeros_like(out_a), -math.inf
+    top = max(lse_a, lse_b)
+    wa = math.exp(lse_a - top)
+    wb = math.exp(lse_b - top)
+    out = (wa * out_a + wb * out_b) / (wa + wb)
+    return out, top + math.log(wa + wb)
+
+
+def merge_gate(out_a, lse_a, out_loc, lse_loc):
+    """Nectar, Eq. (3.5) gate form: g = sigmoid(lse_a - lse_loc); g*A + (1-g)*A_loc."""
+    g = 1.0 / (1.0 + math.exp(-(lse_a - lse_loc)))
+    return g * np.asarray(out_a, dtype=np.float64) + (1.0 - g) * np.asarray(out_loc, dtype=np.float64)
+
+
+# ---------------------------------------------------------------------------
+# The whole path, one (batch, query head) at a time
+# ---------------------------------------------------------------------------
+
+def decode_head(q, q_code, k_codes, K, V, n: int, m: int, n_sink: int, n_local: int,
+                dense: bool = False):
+    """One query head's sparse decode: SCORE -> TOPK -> GATHER-ATT.
+
+    K, V: [n_cap, d] rows of the query's KV head (any float dtype; widened to
+    float64 on the selected rows). ``dense`` attends over every token (the
+    m >= n reading of Sec. 4: the estimator equals full attention when I is all
+    tokens). Returns (idx, dist, out, lse).
+    """
+    if dense:
+        idx = np.arange(n, dtype=np.int64)
+        dist = None
+    else:
+        dist = hamming_distances(q_code, np.asarray(k_codes)[:n])
+        top = top_m_by_score(dist, m)
+        idx = np.union1d(top, window_positions(n, n_sink, n_local)).astype(np.int64)
+    out, lse = attend(q, K, V, idx)
+    return idx, dist, out, lse
+
+
+def decode_batch(q, q_sig, k_sig, K, V, seq_lens, m, n_sink, n_local,
+                 m_per_seq=None, dense=False, heads=None):
+    """Run ``decode_head`` over (b, h) pairs.
+
+    Layouts (NumPy arrays): q [B, Hq, d]; q_sig [B, Hq] (32-bit words);
+    k_sig [B, Hkv, n_cap]; K, V [B, Hkv, n_cap, d] (a batch extent of 1 is shared
+    by every batch entry); seq_lens [B]. ``heads`` restricts the work to a list of
+    (b, h) pairs. Returns {(b, h): (idx, dist, out, lse)}.
+    """
+    B, Hq = q.shape[0], q.shape[1]
+    Hkv = K.shape[1]
+    G = Hq // Hkv
+    pairs = heads if heads is not None else [(b, h) for b in range(B) for h in range(Hq)]
+    res = {}
+    for b, h in pairs:
+        g = h // G
+        kb = 0 if K.shape[0] == 1 else b
+        sb = 0 if (k_sig is None or k_sig.shape[0] == 1) else b
+        n = int(seq_lens[b])
+        mb = int(m_per_seq[b]) if m_per_seq is not None else int(m)
+        codes = None if dense else k_sig[sb, g]
+        qc = None if dense else int(q_sig[b, h])
+        res[(b, h)] = decode_head(q[b, h], qc, codes, K[kb, g], V[kb, g], n, mb,
+                                  n_sink, n_local, dense=dense)
+    return res
