@@ -1,0 +1,466 @@
+#!/usr/bin/env python3
+"""Sparse-decode benchmark: query-heads/s at 128K context and achieved HBM GB/s.
+
+One step = one hash_attn_decode call (SCORE -> TOPK -> GATHER-ATT + merge) over
+the batch-16 x 131,072-token workload (32 query / 8 KV heads, d=128, bf16 KV,
+m=4096, 128 sink + 256 local tokens), inputs resident in HBM. Prints one JSON
+line. ``--impl reference`` times the CPU oracle instead (the reference arm).
+
+Multi-GPU (torchrun): every rank decodes its own independent batch (weak
+scaling, no collective on the data path); the time is the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse-decode query-heads/sec at 128K ctx; achieved HBM GB/s vs peak"
+UNIT = "query-heads/s"
+WORKLOAD = 3
+WORKLOAD_DESC = ("batch16-128k: B=16 sequences x 131072 cached tokens, 32 query / 8 KV heads, d=128, "
+                 "bf16 K/V ~ N(0,1), 32-bit sign(W x) codes per KV head, m=4096 (32x token sparsity), "
+                 "n_sink=128, n_local=256")
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_FILE = os.path.join(ROOT, "profiles", "k_gather_att_batch16_128k.md")
+GATHER_SOURCE = os.path.join(ROOT, "long_context_sparse_score_gb300", "csrc", "k_gather_att.cu")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-heads", type=int, default=192,
+                    help="query heads of the workload the CPU oracle baseline runs")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=16,
+                    help="sequences per GPU (16 = the workload; fewer only for small profiling cases)")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- distributed plumbing
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def dist_max(world, x: float, device) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- peaks, clocks, profiles
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            v = float(json.load(fh)["hbm_gbs"])
+        return v, "measured"
+    except Exception:  # noqa: BLE001
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling (100 ms) of SM clocks and throttle reasons while running."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.tmp = tempfile.NamedTemporaryFile(prefix="clk", suffix=".csv", delete=False)
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        self.t_start = self.t_end = None
+
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_end(self):
+        self.t_end = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.close()
+        rows = []
+        with open(self.tmp.name) as fh:
+            for r in csv.reader(fh):
+                if len(r) < 10:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(r[0].strip().split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    rows.append((ts, float(r[2]), float(r[3]), [x.strip() for x in r[6:10]]))
+                except ValueError:
+                    continue
+        os.unlink(self.tmp.name)
+        if not rows:
+            return None
+        lo = (self.t_start or 0) - 1.0
+        hi = (self.t_end or 1e30) + 1.0
+        win = [r for r in rows if lo <= r[0] <= hi] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in win for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in win), "sm_max_mhz": max(r[2] for r in win),
+                "reasons": reasons, "samples": len(win)}
+
+
+def profiled_traffic():
+    """DRAM bytes per GATHER-ATT launch from the committed ncu summary, if the kernel
+    source is unchanged since the capture (else None)."""
+    try:
+        text = open(PROFILE_FILE).read()
+        sha = hashlib.sha256(open(GATHER_SOURCE, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    got = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            got[k.strip()] = v.strip().strip("`")
+    if got.get("kernel_source_sha256") != sha:
+        return None
+    try:
+        return float(got["traffic_bytes_per_launch_full_workload"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------- workload helpers
+
+def algorithmic_bytes(w, sel_idx, sel_cnt):
+    """(score_bytes, gather_bytes): signature words once per (sequence, KV head); the
+    union of selected K/V rows per KV-head storage; q, q_sig, out, lse."""
+    import torch
+    B, Hq, d = w.q.shape
+    Hkv = w.Hkv
+    G = Hq // Hkv
+    Bk = w.K.shape[0]
+    lens = w.seq_lens.to(torch.int64)
+    code_words = int(lens.sum().item()) * Hkv if Bk == B else int(w.seq_lens[0].item()) * Hkv
+    score = 4 * code_words + 4 * B * Hq + 4 * B
+    cap = sel_idx.shape[-1]
+    valid = torch.arange(cap, device=sel_idx.device).view(1, 1, cap) < sel_cnt.unsqueeze(-1)
+    bi = torch.arange(B, device=sel_idx.device).view(B, 1, 1).expand(B, Hq, cap)
+    if Bk == 1 and B > 1:
+        bi = torch.zeros_like(bi)
+    gi = (torch.arange(Hq, device=sel_idx.device) // G).view(1, Hq, 1).expand(B, Hq, cap)
+    mask = torch.zeros((Bk, Hkv, w.n_cap), dtype=torch.bool, device=sel_idx.device)
+    mask[bi[valid], gi[valid], sel_idx[valid].to(torch.int64)] = True
+    rows = int(mask.sum().item())
+    es = w.K.element_size()
+    gather = rows * 2 * d * es + B * Hq * d * w.q.element_size() + B * Hq * (d + 1) * 4
+    return score, gather, rows
+
+
+def run_cpu_oracle(w, n_heads: int):
+    """Time the oracle (single thread) on the first n_heads query heads, pair by pair;
+    returns (seconds, heads, parity summary vs the given GPU outputs)."""
+    import numpy as np
+    from oracle import hashattn_oracle as O
+    B, Hq, d = w.q.shape
+    G = Hq // w.Hkv
+    q = w.q.float().cpu().numpy()
+    qs = w.q_sig.cpu().numpy().astype(np.int64)
+    lens = w.seq_lens.cpu().numpy()
+    pairs = [(b, g) for b in range(B) for g in range(w.Hkv)]
+    spent, done, results = 0.0, 0, {}
+    for b, g in pairs:
+        if done >= n_heads:
+            break
+        Kh = w.K[b, g].float().cpu().numpy()
+        Vh = w.V[b, g].float().cpu().numpy()
+        codes = w.k_sig[b, g].cpu().numpy().astype(np.int64)
+        for hh in range(G):
+            if done >= n_heads:
+                break
+            h = g * G + hh
+            t0 = time.perf_counter()
+            r = O.decode_head(q[b, h], int(qs[b, h]), codes, Kh, Vh, int(lens[b]), w.m, w.n_sink,
+                              w.n_local)
+            spent += time.perf_counter() - t0
+            results[(b, h)] = r
+            done += 1
+    return spent, done, results
+
+
+def build_lib():
+    from long_context_sparse_score_gb300 import _build
+    _build.build()
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+    from long_context_sparse_score_gb300 import hashattn as H, workloads as W
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build_lib()
+    if rank == 0 and args.batch == 16:
+        w = W.make_workload(WORKLOAD, dev)
+    else:  # same recipe; other ranks draw independent batches (seeds offset by the rank)
+        w = W.make_gqa(WORKLOAD + 100 * rank, B=args.batch, Hq=32, Hkv=8, d=128, n_cap=131072,
+                       seq_lens=131072, m=4096, n_sink=128, n_local=256, device=dev)
+    B, Hq, d = w.q.shape
+    shape = H.make_shape(w.q, w.K, w.V, w.k_sig)
+    ws = torch.empty(H.hash_attn_workspace_size(shape, w.m, w.n_sink, w.n_local), dtype=torch.uint8,
+                     device=dev)
+    H.hash_attn_workspace_init(ws)
+    out = torch.empty((B, Hq, d), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    cap = H.hash_attn_select_capacity(w.n_cap, w.m, w.n_sink, w.n_local)
+    sel = torch.empty((B, Hq, cap), dtype=torch.int32, device=dev)
+    cnt = torch.empty((B, Hq), dtype=torch.int32, device=dev)
+
+    def step(events=None, with_sel=False):
+        s_idx, s_cnt = (sel, cnt) if with_sel else (None, None)
+        if events is None:
+            H.hash_attn_decode(shape, w.q, w.q_sig, w.k_sig, w.K, w.V, w.seq_lens, None, w.m,
+                               w.n_sink, w.n_local, out, lse, s_idx, s_cnt, workspace=ws)
+        else:
+            H.hash_attn_decode_timed(shape, w.q, w.q_sig, w.k_sig, w.K, w.V, w.seq_lens, None, w.m,
+                                     w.n_sink, w.n_local, out, lse, events, s_idx, s_cnt, workspace=ws)
+
+    # one call that also returns the selected sets: the algorithmic byte count
+    step(with_sel=True)
+    st, flags = H.hash_attn_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st} flags {flags:#x}")
+    score_bytes, gather_bytes, uniq_rows = algorithmic_bytes(w, sel, cnt)
+    path_bytes = score_bytes + gather_bytes
+
+    K, Wm = args.steps, args.warmup
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    for row in evs:  # torch creates the CUDA event on its first record
+        for e in row:
+            e.record()
+    for _ in range(Wm):
+        step()
+    sampler = ClockSampler(local) if rank == 0 else None
+    torch.cuda.synchronize()
+    time.sleep(0.3)
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if sampler:
+        sampler.mark_start()
+    t_start.record()
+    for k in range(K):
+        step(evs[k])
+    t_end.record()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark_end()
+    dist_barrier(world)
+    elapsed_ms = t_start.elapsed_time(t_end)
+    elapsed_ms = dist_max(world, elapsed_ms, dev)
+    clocks = sampler.stop() if sampler else None
+    st, flags = H.hash_attn_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st} flags {flags:#x} after the timed loop")
+
+    t_score = [evs[k][0].elapsed_time(evs[k][1]) for k in range(K)]
+    t_topk = [evs[k][1].elapsed_time(evs[k][2]) for k in range(K)]
+    t_gath = [evs[k][2].elapsed_time(evs[k][3]) for k in range(K)]
+    ms_step = elapsed_ms / K
+    heads_total = world * B * Hq * K
+    value = heads_total / (elapsed_ms / 1e3)
+
+    # e2e: per-step query inputs from pinned host memory, results back to the host
+    q_h = w.q.cpu().pin_memory()
+    qs_h = w.q_sig.cpu().pin_memory()
+    sl_h = w.seq_lens.cpu().pin_memory()
+    out_h = torch.empty_like(out, device="cpu").pin_memory()
+    lse_h = torch.empty_like(lse, device="cpu").pin_memory()
+    q_d, qs_d, sl_d = torch.empty_like(w.q), torch.empty_like(w.q_sig), torch.empty_like(w.seq_lens)
+    h2d = q_h.numel() * q_h.element_size() + qs_h.numel() * 4 + sl_h.numel() * 4
+    d2h = out_h.numel() * 4 + lse_h.numel() * 4
+    e2e_steps = max(3, min(K, 500))
+
+    def e2e_step():
+        q_d.copy_(q_h, non_blocking=True)
+        qs_d.copy_(qs_h, non_blocking=True)
+        sl_d.copy_(sl_h, non_blocking=True)
+        H.hash_attn_decode(shape, q_d, qs_d, w.k_sig, w.K, w.V, sl_d, None, w.m, w.n_sink,
+                           w.n_local, out, lse, None, None, workspace=ws)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    dist_barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = dist_max(world, time.perf_counter() - t0, dev)
+    e2e_value = world * B * Hq * e2e_steps / e2e_s
+    if not torch.allclose(out_h, out.cpu()):
+        raise RuntimeError("e2e output mismatch")
+
+    if rank != 0:
+        return None
+    peak, peak_kind = hbm_peak()
+    g_ms = statistics.mean(t_gath)
+    achieved = gather_bytes / (g_ms * 1e-3) / 1e9
+    path_gbs = path_bytes / (ms_step * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": Wm,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 KV, sign-projection codes; no dataset or weights)",
+        "config": {"workload": WORKLOAD_DESC if B == 16 else WORKLOAD_DESC.replace("B=16", f"B={B}"),
+                   "global_batch_query_heads": world * B * Hq,
+                   "seq_len": w.n_cap, "parallelism": f"replicas x{world} (independent batches)",
+                   "l2": "no flush: inputs larger than L2 (8.6 GB KV + 67 MB codes per GPU; "
+                         f"{path_bytes / 1e9:.2f} GB algorithmic reads per step > 126 MB L2)"},
+        "roofline": {"kernel": "k_gather_att", "bound": "hbm", "achieved": achieved, "peak": peak,
+                     "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": profiled_traffic(), "algorithmic_bytes_per_launch": gather_bytes,
+                     "unique_kv_rows": uniq_rows, "avg_launch_ms": g_ms},
+        "pipeline": {"achieved_gbs": path_gbs, "frac": path_gbs / peak,
+                     "algorithmic_bytes_per_step": path_bytes,
+                     "stage_ms": {"score": statistics.mean(t_score), "topk": statistics.mean(t_topk),
+                                  "gather_att": g_ms}},
+        "gpu_launches": 3 * K,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps,
+                "note": "per step: q, q_sig, seq_lens host->device, decode, out+lse device->host, "
+                        "stream sync; KV cache and key codes are device-resident state"},
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        cpu_s, cpu_heads, res = run_cpu_oracle(w, args.cpu_heads)
+        o = out.cpu().numpy()
+        lz = lse.cpu().numpy()
+        worst = max(float(np.max(np.abs(o[b, h] - r[2]) / (1 + np.abs(r[2])))) for (b, h), r in res.items())
+        worst_l = max(abs(float(lz[b, h]) - r[3]) / (1 + abs(r[3])) for (b, h), r in res.items())
+        sel_ok = all(int(cnt[b, h]) == len(r[0]) and
+                     np.array_equal(sel[b, h, :int(cnt[b, h])].cpu().numpy(), r[0])
+                     for (b, h), r in res.items())
+        line["cpu_baseline"] = {
+            "value": cpu_heads / cpu_s, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{cpu_heads} query heads (all 4 heads of the first {math.ceil(cpu_heads / 4)} "
+                      f"(sequence, KV head) pairs) of the same workload, NumPy float64, one thread",
+            "seconds": cpu_s,
+            "parity_on_sample": {"selected_sets_exact": sel_ok, "max_out_err_rel": worst,
+                                 "max_lse_err_rel": worst_l}}
+    return line
+
+
+# ---------------------------------------------------------------- reference arm (the oracle)
+
+def run_reference(args, world, rank, local):
+    import numpy as np
+    import torch
+    from long_context_sparse_score_gb300 import workloads as W
+    from oracle import hashattn_oracle as O
+
+    if rank != 0:
+        return None
+    dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
+    w = W.make_workload(WORKLOAD, dev)
+    B, Hq, d = w.q.shape
+    G = Hq // w.Hkv
+    q = w.q.float().cpu().numpy()
+    qs = w.q_sig.cpu().numpy().astype(np.int64)
+    lens = w.seq_lens.cpu().numpy()
+    pool = []
+    for b, g in [(0, 0), (5, 3), (11, 6), (15, 7)]:
+        Kh = w.K[b, g].float().cpu().numpy()
+        Vh = w.V[b, g].float().cpu().numpy()
+        codes = w.k_sig[b, g].cpu().numpy().astype(np.int64)
+        for hh in range(G):
+            pool.append((b, g * G + hh, Kh, Vh, codes))
+
+    def one(i):
+        b, h, Kh, Vh, codes = pool[i % len(pool)]
+        O.decode_head(q[b, h], int(qs[b, h]), codes, Kh, Vh, int(lens[b]), w.m, w.n_sink, w.n_local)
+
+    for i in range(args.warmup):
+        one(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        one(i)
+    sec = time.perf_counter() - t0
+    value = args.steps / sec
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16 KV, sign-projection codes; no dataset or weights)",
+        "config": {"workload": WORKLOAD_DESC, "global_batch_query_heads": B * Hq, "seq_len": w.n_cap,
+                   "parallelism": "host cores (one thread)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"one query head per step, cycling over {len(pool)} heads of 4 "
+                                   "(sequence, KV head) pairs of the workload"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        line = run_reference(args, world, rank, local)
+    else:
+        line = run_ours(args, world, rank, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

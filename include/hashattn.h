@@ -1,0 +1,224 @@
+/*
+ * hashattn.h -- C ABI of the GB300 (sm_103a) sparse-decode library.
+ *
+ * One decode step of HashAttention sparse attention, per (batch entry b, query
+ * head h), with g = h / (h_q / h_kv) the KV head h reads:
+ *
+ *   SCORE       dist_i = popcount(q_sig[b,h] XOR k_sig[b,g,i]),  i < n = seq_lens[b]
+ *               (HashAttention: Semantic Sparsity for Faster Inference, Eq. (2):
+ *                SCORE = -dist, so the best tokens have the smallest distance)
+ *   TOPK        T = the min(m, n) tokens of smallest dist, ties to the smaller
+ *               index; I = T u [0, min(S, n)) u [max(0, n - Lw), n), ascending
+ *               (same page, Sec. 4 "three stages" and Sec. 4.4 fixed windows)
+ *   GATHER-ATT  z_i = <q, K_i> / sqrt(d) over i in I, read in place (page size 1);
+ *               out = sum_i e^{z_i} V_i / sum_j e^{z_j},  lse = log sum_j e^{z_j}
+ *               (same page, Sec. 4 estimator; lse is the log attention mass of
+ *                Nectar: Neural Estimation of Cached-Token Attention via
+ *                Regression, Sec. 3 Eq. (3.1))
+ *   merge       partial results over disjoint token sets combine exactly through
+ *               their log-normalisers (Nectar, Eqs. (3.4)-(3.5))
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor pointers are DEVICE pointers unless stated; the caller owns every
+ *    buffer. The library allocates no device memory and keeps no global state
+ *    other than a thread-local last-error string.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream). All work is enqueued on it; no call synchronises except
+ *    hash_attn_device_status and hash_attn_workspace_init's caller-visible copy.
+ *  - Argument errors are found on the host and returned BEFORE anything is
+ *    enqueued. Errors that only the device can see (a seq_len outside
+ *    [0, n_cap], a per-sequence budget above the bound, an index outside
+ *    [0, seq_len)) set a flag in the workspace's error word; the affected
+ *    (b, h) results are defined (empty set: out = 0, lse = -inf, or the bad
+ *    index is skipped) and the flag is read with hash_attn_device_status.
+ *  - Kernel-launch failures return HA_ERR_CUDA. hash_attn_last_error() returns a
+ *    human-readable detail of the last failure on the calling thread.
+ *  - Layouts are given as element strides (not bytes). The innermost (d / token)
+ *    dimension of every tensor is contiguous.
+ */
+#ifndef HASHATTN_H
+#define HASHATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    HA_OK = 0,
+    HA_ERR_INVALID_ARG = -1,  /* null pointer, bad size, stride or alignment   */
+    HA_ERR_UNSUPPORTED = -2,  /* d not in {64, 128}, dtype not supported        */
+    HA_ERR_WORKSPACE = -3,    /* workspace null, unaligned or too small         */
+    HA_ERR_CUDA = -4,         /* a CUDA runtime call or kernel launch failed    */
+    HA_ERR_DEVICE = -5,       /* a device-side check failed (see the error word) */
+    HA_ERR_TIMEOUT = -6       /* a bounded device wait ran out                  */
+} ha_status;
+
+typedef enum { HA_F32 = 0, HA_BF16 = 1 } ha_dtype;
+
+/* Device error-word flags (OR-ed together, read by hash_attn_device_status). */
+#define HA_DEVERR_SEQLEN   0x1u  /* seq_lens[b] < 0 or > n_cap: b treated as empty */
+#define HA_DEVERR_BUDGET   0x2u  /* m_per_seq[b] < 0 or > the bound m: clamped     */
+#define HA_DEVERR_INDEX    0x4u  /* a given index outside [0, seq_len): skipped     */
+#define HA_DEVERR_COUNT    0x8u  /* a given count outside [0, idx_cap]: clamped     */
+#define HA_DEVERR_TIMEOUT  0x10u /* a bounded pipeline wait gave up                 */
+#define HA_DEVERR_STATE    0x20u /* workspace counters were not in their reset state */
+
+/* Number of Hamming-distance bins of a 32-bit code (distances 0..32). */
+#define HA_NBINS 33
+
+/*
+ * Problem shape and strides (in elements).
+ *   q      [batch, h_q, d]              q[b,h,:]     at q     + b*q_sb  + h*q_sh
+ *   K, V   [batch, h_kv, n_cap, d]      K[b,g,i,:]   at K     + b*k_sb  + g*k_sh + i*k_sn
+ *   k_sig  [batch, h_kv, n_cap] uint32  k_sig[b,g,i] at k_sig + b*ks_sb + g*ks_sh + i
+ * k_sb, v_sb and ks_sb may be 0: every batch entry then reads the same cache
+ * (one shared document). q_sig is [batch, h_q] contiguous; seq_lens [batch].
+ * Requirements: batch, h_q, h_kv >= 1; h_q % h_kv == 0; d in {64, 128};
+ * n_cap >= 1; K/V rows start on 16-byte boundaries (pointer and k_sn/k_sh/k_sb,
+ * v_* strides times the element size multiples of 16); k_sig 16-byte aligned
+ * with ks_sh and ks_sb multiples of 4.
+ */
+typedef struct {
+    int32_t batch, h_q, h_kv, d, n_cap;
+    int32_t q_dtype, kv_dtype;              /* ha_dtype values */
+    int64_t q_sb, q_sh;
+    int64_t k_sb, k_sh, k_sn;
+    int64_t v_sb, v_sh, v_sn;
+    int64_t ks_sb, ks_sh;
+} ha_shape;
+
+/*
+ * Bytes of workspace that hash_attn_decode / _select / _score / _gather_att need
+ * for this shape and a budget bound m_max with windows n_sink / n_local
+ * (m_max >= n_cap selects the dense layout). Written to *bytes.
+ * Errors: HA_ERR_INVALID_ARG / HA_ERR_UNSUPPORTED for a bad shape or negative
+ * m_max / n_sink / n_local.
+ */
+ha_status hash_attn_workspace_size(const ha_shape* shape, int32_t m_max, int32_t n_sink,
+                                   int32_t n_local, size_t* bytes);
+
+/*
+ * Zero a workspace (enqueued on `stream`). A workspace must be zeroed once
+ * before its first use; every call leaves its counters back at zero.
+ * The workspace pointer must be 256-byte aligned.
+ */
+ha_status hash_attn_workspace_init(void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Capacity of the per-head selected-index list for (n_cap, m, n_sink, n_local):
+ * min(n_cap, m + n_sink + n_local) (HashAttention Sec. 4.4: the budget plus the
+ * fixed positions bounds the number of reads). n_cap when m >= n_cap.
+ */
+int32_t hash_attn_select_capacity(int32_t n_cap, int32_t m, int32_t n_sink, int32_t n_local);
+
+/*
+ * The whole path: SCORE -> TOPK -> GATHER-ATT (split-K) -> merge.
+ *   q          [batch, h_q, d] of shape->q_dtype
+ *   q_sig      [batch, h_q] uint32 query codes
+ *   k_sig      key codes (see ha_shape)
+ *   K, V       cache rows of shape->kv_dtype (see ha_shape)
+ *   seq_lens   [batch] int32, valid tokens per entry, 0 <= seq_lens[b] <= n_cap
+ *   m_per_seq  [batch] int32 budgets, or NULL for the scalar m. When given, m is
+ *              the bound every entry obeys (larger entries are clamped to m and
+ *              flagged HA_DEVERR_BUDGET).
+ *   m, n_sink, n_local  budget and window sizes (>= 0).
+ *              With m >= n_cap and m_per_seq NULL the dense path runs (I is every
+ *              token), SCORE/TOPK are skipped, and q_sig / k_sig may be NULL.
+ *   out        [batch, h_q, d] float32, lse [batch, h_q] float32 (natural log;
+ *              an empty I gives out = 0 and lse = -inf)
+ *   sel_idx    optional [batch, h_q, cap] int32, cap = hash_attn_select_capacity,
+ *              receives I ascending, padded with -1; sel_cnt optional [batch, h_q]
+ *              int32 receives |I|. Both NULL to skip. Ignored by the dense path.
+ *   workspace  >= hash_attn_workspace_size(shape, m, n_sink, n_local) bytes,
+ *              256-byte aligned, zeroed once before first use.
+ * Errors: HA_ERR_INVALID_ARG, HA_ERR_UNSUPPORTED, HA_ERR_WORKSPACE before
+ * launch; HA_ERR_CUDA on a failed launch.
+ */
+ha_status hash_attn_decode(const ha_shape* shape, const void* q, const uint32_t* q_sig,
+                           const uint32_t* k_sig, const void* K, const void* V,
+                           const int32_t* seq_lens, const int32_t* m_per_seq, int32_t m,
+                           int32_t n_sink, int32_t n_local, float* out, float* lse,
+                           int32_t* sel_idx, int32_t* sel_cnt, void* workspace,
+                           size_t ws_bytes, void* stream);
+
+/*
+ * hash_attn_decode with CUDA events recorded between its stages (for the cost
+ * model T = T_scan + T_TOPK + T_att of HashAttention Sec. 4.4). `events` points
+ * to 4 cudaEvent_t (as void*): recorded before SCORE, before TOPK, before
+ * GATHER-ATT and after the last kernel. The dense path records all four around
+ * its single kernel. Same arguments and errors as hash_attn_decode.
+ */
+ha_status hash_attn_decode_timed(const ha_shape* shape, const void* q, const uint32_t* q_sig,
+                                 const uint32_t* k_sig, const void* K, const void* V,
+                                 const int32_t* seq_lens, const int32_t* m_per_seq, int32_t m,
+                                 int32_t n_sink, int32_t n_local, float* out, float* lse,
+                                 int32_t* sel_idx, int32_t* sel_cnt, void* workspace,
+                                 size_t ws_bytes, void* stream, void* const* events);
+
+/*
+ * SCORE alone (HashAttention Eq. (2)).
+ *   dist  optional [batch, h_q, n_cap] uint8: dist[b,h,i] for i < seq_lens[b]
+ *         (entries at i >= seq_lens[b] are not written)
+ *   hist  optional [batch, h_q, 33] uint32: number of tokens at each distance
+ * At least one of dist / hist must be non-NULL. Errors as hash_attn_decode.
+ */
+ha_status hash_attn_score(const ha_shape* shape, const uint32_t* q_sig, const uint32_t* k_sig,
+                          const int32_t* seq_lens, uint8_t* dist, uint32_t* hist,
+                          void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * SCORE + TOPK (the selected set I of hash_attn_decode, same tie rule and
+ * windows), written to sel_idx [batch, h_q, cap] (ascending, -1 padded) and
+ * sel_cnt [batch, h_q]; cap = hash_attn_select_capacity(n_cap, m, n_sink, n_local).
+ * m >= n_cap is allowed here (every token is then selected).
+ */
+ha_status hash_attn_select(const ha_shape* shape, const uint32_t* q_sig, const uint32_t* k_sig,
+                           const int32_t* seq_lens, const int32_t* m_per_seq, int32_t m,
+                           int32_t n_sink, int32_t n_local, int32_t* sel_idx, int32_t* sel_cnt,
+                           void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * GATHER-ATT + merge over caller-given index lists (page size 1, read in place):
+ *   idx  [batch, h_q, idx_cap] int32 token indices (any order, no duplicates
+ *        expected; each must lie in [0, seq_lens[b]) or it is skipped and
+ *        HA_DEVERR_INDEX is flagged), cnt [batch, h_q] int32 valid entries.
+ * idx_cap <= hash_attn_select_capacity(n_cap, m_max, n_sink, n_local) of the
+ * workspace's sizing. Outputs as hash_attn_decode.
+ */
+ha_status hash_attn_gather_att(const ha_shape* shape, const void* q, const void* K,
+                               const void* V, const int32_t* seq_lens, const int32_t* idx,
+                               int32_t idx_cap, const int32_t* cnt, float* out, float* lse,
+                               void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Exact merge of two partial attentions over disjoint token sets, row by row
+ * (Nectar Eq. (3.4)): L = log(e^{lse_a} + e^{lse_b}),
+ * out = e^{lse_a - L} out_a + e^{lse_b - L} out_b. Rows with both lse = -inf
+ * give out = 0, lse = -inf. out/lse may alias out_a/lse_a or out_b/lse_b.
+ *   out_a, out_b, out [rows, d] float32; lse_a, lse_b, lse [rows] float32.
+ */
+ha_status hash_attn_merge(const float* out_a, const float* lse_a, const float* out_b,
+                          const float* lse_b, float* out, float* lse, int32_t rows, int32_t d,
+                          void* stream);
+
+/*
+ * Synchronise `stream`, read and clear the workspace's device error word.
+ * Returns HA_OK, HA_ERR_TIMEOUT (timeout flag set) or HA_ERR_DEVICE (any other
+ * flag); *flags (optional) receives the raw HA_DEVERR_* bits.
+ */
+ha_status hash_attn_device_status(void* workspace, void* stream, uint32_t* flags);
+
+/* Static description of a status code. */
+const char* hash_attn_status_string(ha_status status);
+
+/* Detail of the last failure on the calling thread ("" if none). */
+const char* hash_attn_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HASHATTN_H */

@@ -1,0 +1,230 @@
+// Internal declarations shared by the library's translation units: workspace
+// layout, kernel parameter blocks, launch helpers and small device primitives
+// (mbarrier waits with a time limit, bulk global->shared copies).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "hashattn.h"
+
+namespace ha {
+
+// ------------------------------------------------------------------ constants
+
+constexpr int kScoreThreads = 256;        // SCORE / TOPK block size
+constexpr int kMaxHeadsPerPass = 4;       // query heads of one KV head handled per code pass
+constexpr int kTargetCtas = 2 * 152;      // two CTAs per SM of a GB300 (152 SMs)
+constexpr int kTileRows = 32;             // GATHER-ATT rows per pipeline stage
+constexpr int kGatherThreads = 160;       // 1 producer warp + 4 consumer warps
+constexpr int kMaxSegments = 4096;        // TOPK chunks per head (bounds the prefix table)
+constexpr int64_t kMaxCap = int64_t(1) << 24;  // largest n_cap accepted
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per pipeline wait
+
+// ------------------------------------------------------------------ workspace
+//
+// [0, 256)                 error word (uint32) + padding
+// counters   uint32[heads]  split-K arrival counters of GATHER-ATT (self-resetting)
+// chunk_hist uint32[heads][nchunks][33]  SCORE histogram of every chunk
+// seg_cnt    int32 [heads][nchunks]      selected tokens of every chunk
+// seg_idx    int32 [heads][nchunks*chunk] selected token indices, chunk c's
+//                                          entries at [c*chunk, c*chunk + seg_cnt)
+// part       float [heads][splits][2 + d] split-K partials (max, sum, o[d])
+struct Layout {
+    int heads = 0;
+    int chunk = 0;           // tokens per SCORE/TOPK chunk (0: no selection regions)
+    int nchunks = 0;
+    int rows_cap = 0;        // most rows one head attends to
+    int splits = 1;          // GATHER-ATT CTAs per head
+    int rows_per_split = 0;  // multiple of kTileRows
+    size_t off_err = 0, off_counter = 0, off_hist = 0, off_segcnt = 0, off_seg = 0, off_part = 0;
+    size_t total = 0;
+};
+
+// Chunk of tokens per SCORE/TOPK CTA for a shape: the largest of 8192..1024 that
+// still gives kTargetCtas CTAs, else 1024.
+int choose_chunk(int64_t batch_hkv, int64_t n_cap);
+// Split-K policy for GATHER-ATT.
+void choose_splits(int64_t heads, int64_t rows_cap, int* splits, int* rows_per_split);
+// Full layout; with_selection=false leaves out the chunk_hist / seg regions.
+Layout make_layout(const ha_shape& s, int64_t rows_cap, bool with_selection);
+
+// ------------------------------------------------------------------ parameters
+
+struct ScoreParams {
+    const uint32_t* q_sig;   // [B, Hq]
+    const uint32_t* k_sig;
+    int64_t ks_sb, ks_sh;
+    const int32_t* seq_lens;
+    int B, Hq, Hkv, G, n_cap;
+    int chunk, nchunks;
+    uint32_t* chunk_hist;    // [heads][nchunks][33]
+    uint32_t* counters;      // reset to zero for the heads of this KV head (may be null)
+    uint8_t* dist;           // optional [B, Hq, n_cap]
+    uint32_t* err;
+};
+
+struct SelectParams {
+    const uint32_t* q_sig;
+    const uint32_t* k_sig;
+    int64_t ks_sb, ks_sh;
+    const int32_t* seq_lens;
+    const int32_t* m_per_seq;  // may be null
+    int m, n_sink, n_local;
+    int B, Hq, Hkv, G, n_cap;
+    int chunk, nchunks;
+    const uint32_t* chunk_hist;
+    int32_t* seg_cnt;        // [heads][nchunks]
+    int32_t* seg_idx;        // [heads][nchunks*chunk]
+    uint32_t* err;
+};
+
+struct CompactParams {
+    const int32_t* seq_lens;
+    int Hq, n_cap, chunk, nchunks, cap;
+    const int32_t* seg_cnt;
+    const int32_t* seg_idx;
+    int32_t* sel_idx;        // [heads][cap]
+    int32_t* sel_cnt;        // [heads]
+    uint32_t* err;
+};
+
+struct HistParams {
+    const int32_t* seq_lens;
+    int Hq, n_cap, chunk, nchunks;
+    const uint32_t* chunk_hist;
+    uint32_t* hist;          // [heads][33]
+};
+
+enum IndexMode : int { kIdentity = 0, kSegmented = 1, kList = 2 };
+
+struct GatherParams {
+    const void* q;
+    int64_t q_sb, q_sh;
+    int q_bf16;
+    const char* K;
+    const char* V;
+    int64_t k_sb, k_sh, k_sn, v_sb, v_sh, v_sn;  // elements
+    const int32_t* seq_lens;
+    int B, Hq, Hkv, G, n_cap;
+    int mode;
+    // kSegmented
+    const int32_t* seg_cnt;
+    const int32_t* seg_idx;
+    int chunk, nchunks;
+    // kList
+    const int32_t* list_idx;
+    const int32_t* list_cnt;
+    int list_cap;
+    int splits, rows_per_split;
+    float* part;
+    uint32_t* counters;
+    uint32_t* err;
+    float* out;
+    float* lse;
+    float qscale;            // log2(e) / sqrt(d)
+};
+
+struct MergeParams {
+    const float* out_a; const float* lse_a;
+    const float* out_b; const float* lse_b;
+    float* out; float* lse;
+    int rows, d;
+};
+
+// Launchers (each returns cudaGetLastError() of its launch).
+cudaError_t launch_score(const ScoreParams& p, int batch_hkv, cudaStream_t st);
+cudaError_t launch_select(const SelectParams& p, int batch_hkv, cudaStream_t st);
+cudaError_t launch_compact(const CompactParams& p, int heads, cudaStream_t st);
+cudaError_t launch_hist(const HistParams& p, int heads, cudaStream_t st);
+cudaError_t launch_gather(const GatherParams& p, int d, int kv_bf16, cudaStream_t st);
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t st);
+
+// ------------------------------------------------------------------ device helpers
+
+#ifdef __CUDACC__
+
+__device__ __forceinline__ void flag_error(uint32_t* err, uint32_t f) {
+    if (err) atomicOr(err, f);
+}
+
+// Valid length of batch entry b, or 0 (flagged) when outside [0, n_cap].
+__device__ __forceinline__ int checked_len(const int32_t* seq_lens, int b, int n_cap, uint32_t* err,
+                                           bool report) {
+    int n = seq_lens[b];
+    if (n < 0 || n > n_cap) {
+        if (report) flag_error(err, HA_DEVERR_SEQLEN);
+        return 0;
+    }
+    return n;
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase of `bar` with the given parity; gives up after
+// kWaitLimitNs (returns false) or as soon as *abort becomes non-zero.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  const volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0u) {
+            if (*abort) return false;
+            if (global_ns() - t0 > kWaitLimitNs) return false;
+        }
+    }
+}
+
+// 1-D bulk copy global -> shared (TMA engine), completion counted in bytes on `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+#endif  // __CUDACC__
+
+}  // namespace ha

@@ -1,0 +1,523 @@
+// C ABI of the sparse-decode library: argument checks, workspace layout and the
+// stream-ordered launch sequence SCORE -> TOPK -> GATHER-ATT (+ merge).
+// Every check that the host can make happens before anything is enqueued.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "ha_internal.cuh"
+
+namespace ha {
+
+namespace {
+
+thread_local std::string g_last_error;
+
+ha_status fail(ha_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+ha_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(HA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elem_size(int dtype) { return dtype == HA_F32 ? 4 : 2; }
+
+ha_status check_shape(const ha_shape* s) {
+    if (s == nullptr) return fail(HA_ERR_INVALID_ARG, "shape is NULL");
+    if (s->batch < 1 || s->h_q < 1 || s->h_kv < 1)
+        return fail(HA_ERR_INVALID_ARG, "batch, h_q and h_kv must be >= 1 (got %d, %d, %d)", s->batch,
+                    s->h_q, s->h_kv);
+    if (s->h_q % s->h_kv != 0)
+        return fail(HA_ERR_INVALID_ARG, "h_q (%d) must be a multiple of h_kv (%d)", s->h_q, s->h_kv);
+    if (s->d != 64 && s->d != 128) return fail(HA_ERR_UNSUPPORTED, "d must be 64 or 128 (got %d)", s->d);
+    if ((s->q_dtype != HA_F32 && s->q_dtype != HA_BF16) || (s->kv_dtype != HA_F32 && s->kv_dtype != HA_BF16))
+        return fail(HA_ERR_UNSUPPORTED, "dtypes must be HA_F32 or HA_BF16 (got q %d, kv %d)", s->q_dtype,
+                    s->kv_dtype);
+    if (s->n_cap < 1 || (int64_t)s->n_cap > kMaxCap)
+        return fail(HA_ERR_INVALID_ARG, "n_cap must be in [1, %lld] (got %d)", (long long)kMaxCap, s->n_cap);
+    if ((int64_t)s->batch * s->h_q > (int64_t)1 << 26)
+        return fail(HA_ERR_INVALID_ARG, "batch * h_q too large");
+    if (s->q_sb < 0 || s->q_sh < 0 || s->k_sb < 0 || s->k_sh < 0 || s->k_sn < 1 || s->v_sb < 0 ||
+        s->v_sh < 0 || s->v_sn < 1 || s->ks_sb < 0 || s->ks_sh < 0)
+        return fail(HA_ERR_INVALID_ARG, "strides must be >= 0 (token strides >= 1)");
+    return HA_OK;
+}
+
+ha_status check_kv(const ha_shape* s, const void* K, const void* V) {
+    if (K == nullptr || V == nullptr) return fail(HA_ERR_INVALID_ARG, "K or V is NULL");
+    const int64_t es = elem_size(s->kv_dtype);
+    if (!aligned16(K) || !aligned16(V)) return fail(HA_ERR_INVALID_ARG, "K and V must be 16-byte aligned");
+    const int64_t strides[6] = {s->k_sb, s->k_sh, s->k_sn, s->v_sb, s->v_sh, s->v_sn};
+    for (int64_t st : strides)
+        if ((st * es) % 16 != 0)
+            return fail(HA_ERR_INVALID_ARG, "K/V strides times the element size must be multiples of 16 bytes");
+    return HA_OK;
+}
+
+ha_status check_codes(const ha_shape* s, const uint32_t* q_sig, const uint32_t* k_sig) {
+    if (q_sig == nullptr || k_sig == nullptr) return fail(HA_ERR_INVALID_ARG, "q_sig or k_sig is NULL");
+    if (!aligned16(k_sig) || s->ks_sh % 4 != 0 || s->ks_sb % 4 != 0)
+        return fail(HA_ERR_INVALID_ARG, "k_sig rows must start on 16-byte boundaries (pointer, ks_sh, ks_sb)");
+    return HA_OK;
+}
+
+ha_status check_window(int32_t m, int32_t n_sink, int32_t n_local) {
+    if (m < 0 || n_sink < 0 || n_local < 0)
+        return fail(HA_ERR_INVALID_ARG, "m, n_sink and n_local must be >= 0 (got %d, %d, %d)", m, n_sink,
+                    n_local);
+    return HA_OK;
+}
+
+ha_status check_ws(const Layout& lay, void* ws, size_t ws_bytes) {
+    if (ws == nullptr) return fail(HA_ERR_WORKSPACE, "workspace is NULL");
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return fail(HA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if (ws_bytes < lay.total)
+        return fail(HA_ERR_WORKSPACE, "workspace too small: %zu bytes given, %zu needed", ws_bytes, lay.total);
+    return HA_OK;
+}
+
+int64_t rows_cap_of(int32_t n_cap, int64_t m, int64_t n_sink, int64_t n_local) {
+    const int64_t r = m + n_sink + n_local;
+    return r < n_cap ? r : n_cap;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+    return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+struct Views {
+    uint32_t* err;
+    uint32_t* counters;
+    uint32_t* chunk_hist;
+    int32_t* seg_cnt;
+    int32_t* seg_idx;
+    float* part;
+};
+
+Views views(const Layout& lay, void* ws) {
+    Views v;
+    v.err = at<uint32_t>(ws, lay.off_err);
+    v.counters = at<uint32_t>(ws, lay.off_counter);
+    v.chunk_hist = lay.chunk ? at<uint32_t>(ws, lay.off_hist) : nullptr;
+    v.seg_cnt = lay.chunk ? at<int32_t>(ws, lay.off_segcnt) : nullptr;
+    v.seg_idx = lay.chunk ? at<int32_t>(ws, lay.off_seg) : nullptr;
+    v.part = at<float>(ws, lay.off_part);
+    return v;
+}
+
+ScoreParams score_params(const ha_shape* s, const Layout& lay, const Views& v, const uint32_t* q_sig,
+                         const uint32_t* k_sig, const int32_t* seq_lens) {
+    ScoreParams p{};
+    p.q_sig = q_sig;
+    p.k_sig = k_sig;
+    p.ks_sb = s->ks_sb;
+    p.ks_sh = s->ks_sh;
+    p.seq_lens = seq_lens;
+    p.B = s->batch;
+    p.Hq = s->h_q;
+    p.Hkv = s->h_kv;
+    p.G = s->h_q / s->h_kv;
+    p.n_cap = s->n_cap;
+    p.chunk = lay.chunk;
+    p.nchunks = lay.nchunks;
+    p.chunk_hist = v.chunk_hist;
+    p.counters = v.counters;
+    p.dist = nullptr;
+    p.err = v.err;
+    return p;
+}
+
+SelectParams select_params(const ha_shape* s, const Layout& lay, const Views& v, const uint32_t* q_sig,
+                           const uint32_t* k_sig, const int32_t* seq_lens, const int32_t* m_per_seq,
+                           int32_t m, int32_t n_sink, int32_t n_local) {
+    SelectParams p{};
+    p.q_sig = q_sig;
+    p.k_sig = k_sig;
+    p.ks_sb = s->ks_sb;
+    p.ks_sh = s->ks_sh;
+    p.seq_lens = seq_lens;
+    p.m_per_seq = m_per_seq;
+    p.m = m;
+    p.n_sink = n_sink;
+    p.n_local = n_local;
+    p.B = s->batch;
+    p.Hq = s->h_q;
+    p.Hkv = s->h_kv;
+    p.G = s->h_q / s->h_kv;
+    p.n_cap = s->n_cap;
+    p.chunk = lay.chunk;
+    p.nchunks = lay.nchunks;
+    p.chunk_hist = v.chunk_hist;
+    p.seg_cnt = v.seg_cnt;
+    p.seg_idx = v.seg_idx;
+    p.err = v.err;
+    return p;
+}
+
+GatherParams gather_params(const ha_shape* s, const Layout& lay, const Views& v, const void* q,
+                           const void* K, const void* V, const int32_t* seq_lens, float* out, float* lse) {
+    GatherParams p{};
+    p.q = q;
+    p.q_sb = s->q_sb;
+    p.q_sh = s->q_sh;
+    p.q_bf16 = s->q_dtype == HA_BF16;
+    p.K = static_cast<const char*>(K);
+    p.V = static_cast<const char*>(V);
+    p.k_sb = s->k_sb;
+    p.k_sh = s->k_sh;
+    p.k_sn = s->k_sn;
+    p.v_sb = s->v_sb;
+    p.v_sh = s->v_sh;
+    p.v_sn = s->v_sn;
+    p.seq_lens = seq_lens;
+    p.B = s->batch;
+    p.Hq = s->h_q;
+    p.Hkv = s->h_kv;
+    p.G = s->h_q / s->h_kv;
+    p.n_cap = s->n_cap;
+    p.mode = kIdentity;
+    p.chunk = lay.chunk;
+    p.nchunks = lay.nchunks;
+    p.seg_cnt = v.seg_cnt;
+    p.seg_idx = v.seg_idx;
+    p.splits = lay.splits;
+    p.rows_per_split = lay.rows_per_split;
+    p.part = v.part;
+    p.counters = v.counters;
+    p.err = v.err;
+    p.out = out;
+    p.lse = lse;
+    p.qscale = (float)(1.4426950408889634 / std::sqrt((double)s->d));
+    return p;
+}
+
+ha_status record(void* const* events, int i, cudaStream_t st) {
+    if (events == nullptr) return HA_OK;
+    cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st);
+    return e == cudaSuccess ? HA_OK : cuda_fail(e, "cudaEventRecord");
+}
+
+#define HA_TRY(expr)                      \
+    do {                                  \
+        const ha_status _st = (expr);     \
+        if (_st != HA_OK) return _st;     \
+    } while (0)
+
+#define HA_LAUNCH(expr, what)                              \
+    do {                                                   \
+        const cudaError_t _e = (expr);                     \
+        if (_e != cudaSuccess) return cuda_fail(_e, what); \
+    } while (0)
+
+ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, const uint32_t* k_sig,
+                      const void* K, const void* V, const int32_t* seq_lens, const int32_t* m_per_seq,
+                      int32_t m, int32_t n_sink, int32_t n_local, float* out, float* lse, int32_t* sel_idx,
+                      int32_t* sel_cnt, void* ws, size_t ws_bytes, void* stream, void* const* events) {
+    HA_TRY(check_shape(s));
+    HA_TRY(check_window(m, n_sink, n_local));
+    if (q == nullptr || seq_lens == nullptr || out == nullptr || lse == nullptr)
+        return fail(HA_ERR_INVALID_ARG, "q, seq_lens, out and lse must not be NULL");
+    HA_TRY(check_kv(s, K, V));
+    const bool dense = (m >= s->n_cap) && (m_per_seq == nullptr);
+    if (!dense) HA_TRY(check_codes(s, q_sig, k_sig));
+    if ((sel_idx == nullptr) != (sel_cnt == nullptr))
+        return fail(HA_ERR_INVALID_ARG, "sel_idx and sel_cnt must both be given or both be NULL");
+    const int64_t rows_cap = dense ? s->n_cap : rows_cap_of(s->n_cap, m, n_sink, n_local);
+    const Layout lay = make_layout(*s, rows_cap, !dense);
+    HA_TRY(check_ws(lay, ws, ws_bytes));
+    const Views v = views(lay, ws);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int bhkv = s->batch * s->h_kv;
+    const int heads = s->batch * s->h_q;
+
+    GatherParams gp = gather_params(s, lay, v, q, K, V, seq_lens, out, lse);
+    if (dense) {
+        HA_TRY(record(events, 0, st));
+        HA_TRY(record(events, 1, st));
+        HA_TRY(record(events, 2, st));
+        gp.mode = kIdentity;
+        HA_LAUNCH(launch_gather(gp, s->d, s->kv_dtype == HA_BF16, st), "GATHER-ATT launch");
+        HA_TRY(record(events, 3, st));
+        return HA_OK;
+    }
+    HA_TRY(record(events, 0, st));
+    HA_LAUNCH(launch_score(score_params(s, lay, v, q_sig, k_sig, seq_lens), bhkv, st), "SCORE launch");
+    HA_TRY(record(events, 1, st));
+    HA_LAUNCH(launch_select(select_params(s, lay, v, q_sig, k_sig, seq_lens, m_per_seq, m, n_sink, n_local),
+                            bhkv, st),
+              "TOPK launch");
+    HA_TRY(record(events, 2, st));
+    gp.mode = kSegmented;
+    HA_LAUNCH(launch_gather(gp, s->d, s->kv_dtype == HA_BF16, st), "GATHER-ATT launch");
+    HA_TRY(record(events, 3, st));
+    if (sel_idx != nullptr) {
+        CompactParams cp{};
+        cp.seq_lens = seq_lens;
+        cp.Hq = s->h_q;
+        cp.n_cap = s->n_cap;
+        cp.chunk = lay.chunk;
+        cp.nchunks = lay.nchunks;
+        cp.cap = (int)rows_cap;
+        cp.seg_cnt = v.seg_cnt;
+        cp.seg_idx = v.seg_idx;
+        cp.sel_idx = sel_idx;
+        cp.sel_cnt = sel_cnt;
+        cp.err = v.err;
+        HA_LAUNCH(launch_compact(cp, heads, st), "compaction launch");
+    }
+    return HA_OK;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- layout policy
+
+int choose_chunk(int64_t batch_hkv, int64_t n_cap) {
+    for (int c = 8192; c > 1024; c >>= 1)
+        if (batch_hkv * ceil_div(n_cap, c) >= kTargetCtas) return c;
+    return 1024;
+}
+
+void choose_splits(int64_t heads, int64_t rows_cap, int* splits, int* rows_per_split) {
+    if (rows_cap <= 0) {
+        *splits = 1;
+        *rows_per_split = kTileRows;
+        return;
+    }
+    int64_t sp = ceil_div(rows_cap, 1024);
+    const int64_t fill = ceil_div(kTargetCtas, heads);       // enough CTAs for small batches
+    if (fill > sp) sp = fill;
+    const int64_t most = ceil_div(rows_cap, 2 * kTileRows);  // at least two tiles per CTA
+    if (sp > most) sp = most;
+    if (sp < 1) sp = 1;
+    int64_t rps = ceil_div(ceil_div(rows_cap, sp), kTileRows) * kTileRows;
+    sp = ceil_div(rows_cap, rps);
+    *splits = (int)sp;
+    *rows_per_split = (int)rps;
+}
+
+Layout make_layout(const ha_shape& s, int64_t rows_cap, bool with_selection) {
+    Layout L;
+    L.heads = s.batch * s.h_q;
+    L.rows_cap = (int)rows_cap;
+    choose_splits(L.heads, rows_cap, &L.splits, &L.rows_per_split);
+    size_t off = 256;  // error word + padding
+    L.off_err = 0;
+    L.off_counter = off;
+    off = align_up(off + (size_t)L.heads * 4, 256);
+    if (with_selection) {
+        L.chunk = choose_chunk((int64_t)s.batch * s.h_kv, s.n_cap);
+        L.nchunks = (int)ceil_div(s.n_cap, L.chunk);
+        L.off_hist = off;
+        off = align_up(off + (size_t)L.heads * L.nchunks * HA_NBINS * 4, 256);
+        L.off_segcnt = off;
+        off = align_up(off + (size_t)L.heads * L.nchunks * 4, 256);
+        L.off_seg = off;
+        off = align_up(off + (size_t)L.heads * L.nchunks * L.chunk * 4, 256);
+    }
+    L.off_part = off;
+    off = align_up(off + (size_t)L.heads * L.splits * (s.d + 2) * 4, 256);
+    L.total = off;
+    return L;
+}
+
+}  // namespace ha
+
+using namespace ha;
+
+extern "C" {
+
+ha_status hash_attn_workspace_size(const ha_shape* shape, int32_t m_max, int32_t n_sink, int32_t n_local,
+                                   size_t* bytes) {
+    HA_TRY(check_shape(shape));
+    HA_TRY(check_window(m_max, n_sink, n_local));
+    if (bytes == nullptr) return fail(HA_ERR_INVALID_ARG, "bytes is NULL");
+    const bool dense = m_max >= shape->n_cap;
+    // the selection regions are always included so that hash_attn_select and
+    // hash_attn_score work with any budget on the same workspace
+    const int64_t rows_cap = dense ? shape->n_cap : rows_cap_of(shape->n_cap, m_max, n_sink, n_local);
+    const Layout sparse = make_layout(*shape, rows_cap, true);
+    *bytes = sparse.total;
+    return HA_OK;
+}
+
+ha_status hash_attn_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
+    if (workspace == nullptr) return fail(HA_ERR_WORKSPACE, "workspace is NULL");
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(HA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    const cudaError_t e = cudaMemsetAsync(workspace, 0, ws_bytes, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? HA_OK : cuda_fail(e, "cudaMemsetAsync");
+}
+
+int32_t hash_attn_select_capacity(int32_t n_cap, int32_t m, int32_t n_sink, int32_t n_local) {
+    if (n_cap < 0 || m < 0 || n_sink < 0 || n_local < 0) return 0;
+    return (int32_t)rows_cap_of(n_cap, m, n_sink, n_local);
+}
+
+ha_status hash_attn_decode(const ha_shape* shape, const void* q, const uint32_t* q_sig, const uint32_t* k_sig,
+                           const void* K, const void* V, const int32_t* seq_lens, const int32_t* m_per_seq,
+                           int32_t m, int32_t n_sink, int32_t n_local, float* out, float* lse, int32_t* sel_idx,
+                           int32_t* sel_cnt, void* workspace, size_t ws_bytes, void* stream) {
+    return decode_impl(shape, q, q_sig, k_sig, K, V, seq_lens, m_per_seq, m, n_sink, n_local, out, lse, sel_idx,
+                       sel_cnt, workspace, ws_bytes, stream, nullptr);
+}
+
+ha_status hash_attn_decode_timed(const ha_shape* shape, const void* q, const uint32_t* q_sig,
+                                 const uint32_t* k_sig, const void* K, const void* V, const int32_t* seq_lens,
+                                 const int32_t* m_per_seq, int32_t m, int32_t n_sink, int32_t n_local, float* out,
+                                 float* lse, int32_t* sel_idx, int32_t* sel_cnt, void* workspace, size_t ws_bytes,
+                                 void* stream, void* const* events) {
+    if (events == nullptr) return fail(HA_ERR_INVALID_ARG, "events is NULL");
+    for (int i = 0; i < 4; ++i)
+        if (events[i] == nullptr) return fail(HA_ERR_INVALID_ARG, "events[%d] is NULL", i);
+    return decode_impl(shape, q, q_sig, k_sig, K, V, seq_lens, m_per_seq, m, n_sink, n_local, out, lse, sel_idx,
+                       sel_cnt, workspace, ws_bytes, stream, events);
+}
+
+ha_status hash_attn_score(const ha_shape* shape, const uint32_t* q_sig, const uint32_t* k_sig,
+                          const int32_t* seq_lens, uint8_t* dist, uint32_t* hist, void* workspace,
+                          size_t ws_bytes, void* stream) {
+    HA_TRY(check_shape(shape));
+    HA_TRY(check_codes(shape, q_sig, k_sig));
+    if (seq_lens == nullptr) return fail(HA_ERR_INVALID_ARG, "seq_lens is NULL");
+    if (dist == nullptr && hist == nullptr) return fail(HA_ERR_INVALID_ARG, "dist and hist are both NULL");
+    const Layout lay = make_layout(*shape, 0, true);
+    HA_TRY(check_ws(lay, workspace, ws_bytes));
+    const Views v = views(lay, workspace);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    ScoreParams sp = score_params(shape, lay, v, q_sig, k_sig, seq_lens);
+    sp.counters = nullptr;
+    sp.dist = dist;
+    HA_LAUNCH(launch_score(sp, shape->batch * shape->h_kv, st), "SCORE launch");
+    if (hist != nullptr) {
+        HistParams hp{};
+        hp.seq_lens = seq_lens;
+        hp.Hq = shape->h_q;
+        hp.n_cap = shape->n_cap;
+        hp.chunk = lay.chunk;
+        hp.nchunks = lay.nchunks;
+        hp.chunk_hist = v.chunk_hist;
+        hp.hist = hist;
+        HA_LAUNCH(launch_hist(hp, shape->batch * shape->h_q, st), "histogram launch");
+    }
+    return HA_OK;
+}
+
+ha_status hash_attn_select(const ha_shape* shape, const uint32_t* q_sig, const uint32_t* k_sig,
+                           const int32_t* seq_lens, const int32_t* m_per_seq, int32_t m, int32_t n_sink,
+                           int32_t n_local, int32_t* sel_idx, int32_t* sel_cnt, void* workspace, size_t ws_bytes,
+                           void* stream) {
+    HA_TRY(check_shape(shape));
+    HA_TRY(check_window(m, n_sink, n_local));
+    HA_TRY(check_codes(shape, q_sig, k_sig));
+    if (seq_lens == nullptr || sel_idx == nullptr || sel_cnt == nullptr)
+        return fail(HA_ERR_INVALID_ARG, "seq_lens, sel_idx and sel_cnt must not be NULL");
+    const int64_t rows_cap = rows_cap_of(shape->n_cap, m, n_sink, n_local);
+    const Layout lay = make_layout(*shape, rows_cap, true);
+    HA_TRY(check_ws(lay, workspace, ws_bytes));
+    const Views v = views(lay, workspace);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int bhkv = shape->batch * shape->h_kv;
+    HA_LAUNCH(launch_score(score_params(shape, lay, v, q_sig, k_sig, seq_lens), bhkv, st), "SCORE launch");
+    HA_LAUNCH(launch_select(select_params(shape, lay, v, q_sig, k_sig, seq_lens, m_per_seq, m, n_sink, n_local),
+                            bhkv, st),
+              "TOPK launch");
+    CompactParams cp{};
+    cp.seq_lens = seq_lens;
+    cp.Hq = shape->h_q;
+    cp.n_cap = shape->n_cap;
+    cp.chunk = lay.chunk;
+    cp.nchunks = lay.nchunks;
+    cp.cap = (int)rows_cap;
+    cp.seg_cnt = v.seg_cnt;
+    cp.seg_idx = v.seg_idx;
+    cp.sel_idx = sel_idx;
+    cp.sel_cnt = sel_cnt;
+    cp.err = v.err;
+    HA_LAUNCH(launch_compact(cp, shape->batch * shape->h_q, st), "compaction launch");
+    return HA_OK;
+}
+
+ha_status hash_attn_gather_att(const ha_shape* shape, const void* q, const void* K, const void* V,
+                               const int32_t* seq_lens, const int32_t* idx, int32_t idx_cap, const int32_t* cnt,
+                               float* out, float* lse, void* workspace, size_t ws_bytes, void* stream) {
+    HA_TRY(check_shape(shape));
+    if (q == nullptr || seq_lens == nullptr || out == nullptr || lse == nullptr || cnt == nullptr)
+        return fail(HA_ERR_INVALID_ARG, "q, seq_lens, cnt, out and lse must not be NULL");
+    if (idx_cap < 0 || idx_cap > shape->n_cap)
+        return fail(HA_ERR_INVALID_ARG, "idx_cap must be in [0, n_cap] (got %d)", idx_cap);
+    if (idx == nullptr && idx_cap > 0) return fail(HA_ERR_INVALID_ARG, "idx is NULL");
+    HA_TRY(check_kv(shape, K, V));
+    const Layout lay = make_layout(*shape, idx_cap, false);
+    HA_TRY(check_ws(lay, workspace, ws_bytes));
+    const Views v = views(lay, workspace);
+    GatherParams gp = gather_params(shape, lay, v, q, K, V, seq_lens, out, lse);
+    gp.mode = kList;
+    gp.list_idx = idx;
+    gp.list_cnt = cnt;
+    gp.list_cap = idx_cap;
+    HA_LAUNCH(launch_gather(gp, shape->d, shape->kv_dtype == HA_BF16, static_cast<cudaStream_t>(stream)),
+              "GATHER-ATT launch");
+    return HA_OK;
+}
+
+ha_status hash_attn_merge(const float* out_a, const float* lse_a, const float* out_b, const float* lse_b,
+                          float* out, float* lse, int32_t rows, int32_t d, void* stream) {
+    if (rows < 0 || d < 1) return fail(HA_ERR_INVALID_ARG, "rows must be >= 0 and d >= 1");
+    if (rows == 0) return HA_OK;
+    if (!out_a || !lse_a || !out_b || !lse_b || !out || !lse)
+        return fail(HA_ERR_INVALID_ARG, "merge pointers must not be NULL");
+    MergeParams p{out_a, lse_a, out_b, lse_b, out, lse, rows, d};
+    HA_LAUNCH(launch_merge(p, static_cast<cudaStream_t>(stream)), "merge launch");
+    return HA_OK;
+}
+
+ha_status hash_attn_device_status(void* workspace, void* stream, uint32_t* flags) {
+    if (workspace == nullptr) return fail(HA_ERR_WORKSPACE, "workspace is NULL");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    cudaError_t e = cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the error word");
+    if (word != 0) {
+        e = cudaMemsetAsync(workspace, 0, sizeof(word), st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the error word");
+    }
+    if (flags) *flags = word;
+    if (word == 0) return HA_OK;
+    if (word & HA_DEVERR_TIMEOUT) return fail(HA_ERR_TIMEOUT, "device error word 0x%x (wait timed out)", word);
+    return fail(HA_ERR_DEVICE, "device error word 0x%x", word);
+}
+
+const char* hash_attn_status_string(ha_status status) {
+    switch (status) {
+        case HA_OK: return "ok";
+        case HA_ERR_INVALID_ARG: return "invalid argument";
+        case HA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case HA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case HA_ERR_CUDA: return "CUDA error";
+        case HA_ERR_DEVICE: return "device-side check failed";
+        case HA_ERR_TIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}
+
+const char* hash_attn_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,446 @@
+// GATHER-ATT and merge kernels of the sparse-decode path.
+//
+// HashAttention: Semantic Sparsity for Faster Inference, Sec. 4: attention over
+// the selected set I only, o = sum_{i in I} e^{z_i} v_i / sum_{j in I} e^{z_j},
+// z_i = <q, k_i>/sqrt(d); Sec. 4.4: paged attention with a page of one token, the
+// selected indices used directly, no gathered copy of the KV rows.
+// Nectar: Neural Estimation of Cached-Token Attention via Regression, Eq. (3.1)
+// and Eqs. (3.4)-(3.5): the log-normaliser lse = log sum_j e^{z_j} is returned
+// with o, and partial results over disjoint token sets merge exactly.
+//
+// k_gather_att: one CTA per (query head, split of I). Warp 0 is the producer: it
+// turns list positions into token indices and has the TMA engine copy each
+// selected K row and V row (one 1-D bulk copy per row, straight from the cache)
+// into a ring of shared-memory stages, completion counted on an mbarrier per
+// stage. Warps 1-4 consume: 8 rows per warp per 32-row stage, 4 lanes per row.
+// Scores are fp32 (q pre-scaled by log2(e)/sqrt(d), packed fp32x2 FMAs), the
+// softmax is online in base 2, and P.V accumulates per lane over its rows.
+// Splits write (max, sum, o) partials; the last CTA of a head to finish merges
+// them (no waiting: an arrival counter decides who is last).
+#include "ha_internal.cuh"
+
+#include <math_constants.h>
+
+namespace ha {
+namespace {
+
+template <int D, typename KT>
+struct Cfg {
+    static constexpr int ES = sizeof(KT);
+    static constexpr int RB = D * ES;                 // bytes of one K or V row
+    static constexpr int PITCH = RB + 16;             // shared row pitch: rows land on distinct banks
+    static constexpr int STAGES = RB <= 256 ? 4 : 2;
+    static constexpr int NCH = RB / 16;               // 16-byte chunks per row
+    static constexpr int CPL = NCH / 4;               // chunks per lane (4 lanes per row)
+    static constexpr int EPC = 16 / ES;               // elements per chunk
+    static constexpr int DPL = CPL * EPC;             // dims per lane (= D / 4)
+    static constexpr int STAGE_BYTES = 2 * kTileRows * PITCH;
+    static constexpr int DATA_BYTES = STAGES * STAGE_BYTES;
+    // shared layout after the stage ring
+    static constexpr int OFF_TOK = DATA_BYTES;                            // int [STAGES][32]
+    static constexpr int OFF_BAR = OFF_TOK + STAGES * kTileRows * 4;      // u64 full[S], empty[S]
+    static constexpr int OFF_CMB = OFF_BAR + 2 * STAGES * 8;              // float wm[4], wl[4], wo[4][D]
+    static constexpr int OFF_PRE = OFF_CMB + (8 + 4 * D) * 4;             // int pre[nchunks + 1]
+};
+
+template <typename KT>
+__device__ __forceinline__ void chunk_to_float(const uint4 w, float* f);
+
+template <>
+__device__ __forceinline__ void chunk_to_float<__nv_bfloat16>(const uint4 w, float* f) {
+    f[0] = bf16lo(w.x); f[1] = bf16hi(w.x);
+    f[2] = bf16lo(w.y); f[3] = bf16hi(w.y);
+    f[4] = bf16lo(w.z); f[5] = bf16hi(w.z);
+    f[6] = bf16lo(w.w); f[7] = bf16hi(w.w);
+}
+
+template <>
+__device__ __forceinline__ void chunk_to_float<float>(const uint4 w, float* f) {
+    f[0] = __uint_as_float(w.x); f[1] = __uint_as_float(w.y);
+    f[2] = __uint_as_float(w.z); f[3] = __uint_as_float(w.w);
+}
+
+__device__ __forceinline__ float load_q(const void* q, int64_t off, int bf16) {
+    if (bf16) {
+        const uint16_t raw = reinterpret_cast<const uint16_t*>(q)[off];
+        return __uint_as_float(((uint32_t)raw) << 16);
+    }
+    return reinterpret_cast<const float*>(q)[off];
+}
+
+template <int D, typename KT>
+__global__ void __launch_bounds__(kGatherThreads) k_gather_att(const GatherParams p) {
+    using C = Cfg<D, KT>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    int* rowtok = reinterpret_cast<int*>(smem + C::OFF_TOK);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    float* wm = reinterpret_cast<float*>(smem + C::OFF_CMB);
+    float* wl = wm + 4;
+    float* wo = wm + 8;
+    int* pre = reinterpret_cast<int*>(smem + C::OFF_PRE);
+    __shared__ int s_L, s_issued, s_last;
+    __shared__ volatile int s_abort;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int lin = blockIdx.x;
+    const int split = lin % p.splits;
+    lin /= p.splits;
+    const int hh = lin % p.G;
+    lin /= p.G;
+    const int b = lin % p.B;
+    const int g = lin / p.B;
+    const int head = b * p.Hq + g * p.G + hh;
+    const bool report = (p.mode != kSegmented) && split == 0 && hh == 0 && g == 0 && tid == 0;
+    const int n = checked_len(p.seq_lens, b, p.n_cap, p.err, report);
+
+    // ---- setup: list length (and segment prefix table) by warp 0; barriers
+    if (warp == 0) {
+        int L = 0;
+        if (p.mode == kIdentity) {
+            L = n;
+        } else if (p.mode == kList) {
+            L = p.list_cnt[head];
+            if (L < 0 || L > p.list_cap) {
+                if (lane == 0) flag_error(p.err, HA_DEVERR_COUNT);
+                L = min(max(L, 0), p.list_cap);
+            }
+        } else {
+            const int nch = (n + p.chunk - 1) / p.chunk;
+            const int32_t* cnt = p.seg_cnt + (int64_t)head * p.nchunks;
+            int carry = 0;
+            if (lane == 0) pre[0] = 0;
+            for (int base = 0; base < nch; base += 32) {
+                const int cc = base + lane;
+                int v = (cc < nch) ? cnt[cc] : 0;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, v, o);
+                    if (lane >= o) v += y;
+                }
+                if (cc < nch) pre[cc + 1] = carry + v;
+                carry += __shfl_sync(0xffffffffu, v, 31);
+            }
+            L = carry;
+        }
+        if (lane == 0) {
+            s_L = L;
+            s_abort = 0;
+            s_issued = 0;
+            for (int s = 0; s < C::STAGES; ++s) {
+                mbar_init(smem_addr(&bars[s]), 1);
+                mbar_init(smem_addr(&bars[C::STAGES + s]), 4);
+            }
+            mbar_fence_init();
+        }
+    }
+    __syncthreads();
+
+    const int L = s_L;
+    const int r0 = split * p.rows_per_split;
+    const int r1 = min(L, r0 + p.rows_per_split);
+    const int ntiles = (r1 > r0) ? (r1 - r0 + kTileRows - 1) / kTileRows : 0;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        const char* Kb = p.K + ((int64_t)b * p.k_sb + (int64_t)g * p.k_sh) * C::ES;
+        const char* Vb = p.V + ((int64_t)b * p.v_sb + (int64_t)g * p.v_sh) * C::ES;
+        const int nch = (p.mode == kSegmented) ? (n + p.chunk - 1) / p.chunk : 0;
+        const int32_t* seg = (p.mode == kSegmented)
+                                 ? p.seg_idx + (int64_t)head * p.nchunks * p.chunk
+                                 : nullptr;
+        const int32_t* lst = (p.mode == kList) ? p.list_idx + (int64_t)head * p.list_cap : nullptr;
+        int issued = 0;
+        for (int t = 0; t < ntiles; ++t) {
+            const int s = t % C::STAGES;
+            if (t >= C::STAGES) {
+                bool ok = true;
+                if (lane == 0) ok = mbar_wait_bounded(smem_addr(&bars[C::STAGES + s]),
+                                                      ((t / C::STAGES) - 1) & 1, &s_abort);
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                if (!ok) {
+                    if (lane == 0) {
+                        flag_error(p.err, HA_DEVERR_TIMEOUT);
+                        s_abort = 1;
+                    }
+                    break;
+                }
+            }
+            const int pp = r0 + t * kTileRows + lane;
+            int tok = -1;
+            if (pp < r1) {
+                if (p.mode == kIdentity) {
+                    tok = pp;
+                } else if (p.mode == kSegmented) {
+                    int lo = 0, hi = nch - 1;
+                    while (lo < hi) {
+                        const int mid = (lo + hi + 1) >> 1;
+                        if (pre[mid] <= pp) lo = mid; else hi = mid - 1;
+                    }
+                    tok = seg[(int64_t)lo * p.chunk + (pp - pre[lo])];
+                } else {
+                    tok = lst[pp];
+                    if (tok < 0 || tok >= n) {
+                        flag_error(p.err, HA_DEVERR_INDEX);
+                        tok = -1;
+                    }
+                }
+            }
+            rowtok[s * kTileRows + lane] = tok;
+            const unsigned vm = __ballot_sync(0xffffffffu, tok >= 0);
+            __syncwarp();
+            const uint32_t full = smem_addr(&bars[s]);
+            if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)__popc(vm) * 2u * C::RB);
+            __syncwarp();
+            if (tok >= 0) {
+                unsigned char* ks = smem + s * C::STAGE_BYTES + lane * C::PITCH;
+                unsigned char* vs = ks + kTileRows * C::PITCH;
+                bulk_g2s(smem_addr(ks), Kb + (int64_t)tok * p.k_sn * C::ES, C::RB, full);
+                bulk_g2s(smem_addr(vs), Vb + (int64_t)tok * p.v_sn * C::ES, C::RB, full);
+            }
+            issued = t + 1;
+        }
+        if (lane == 0) s_issued = issued;
+    } else {
+        // ------------------------------------------------------------ consumers
+        const int cw = warp - 1;
+        const int r = lane & 7, qt = lane >> 3;
+        float qv[C::DPL];
+        {
+            const int64_t qoff = (int64_t)b * p.q_sb + (int64_t)(g * p.G + hh) * p.q_sh;
+#pragma unroll
+            for (int jc = 0; jc < C::CPL; ++jc) {
+                const int dim0 = (jc * 4 + qt) * C::EPC;
+#pragma unroll
+                for (int e = 0; e < C::EPC; ++e)
+                    qv[jc * C::EPC + e] = load_q(p.q, qoff + dim0 + e, p.q_bf16) * p.qscale;
+            }
+        }
+        float2 ov[C::DPL / 2];
+#pragma unroll
+        for (int i = 0; i < C::DPL / 2; ++i) ov[i] = make_float2(0.f, 0.f);
+        float mrun = -CUDART_INF_F, lrun = 0.f;
+
+        for (int t = 0; t < ntiles; ++t) {
+            const int s = t % C::STAGES;
+            const bool ok = mbar_wait_bounded(smem_addr(&bars[s]), (t / C::STAGES) & 1, &s_abort);
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (lane == 0) {
+                    flag_error(p.err, HA_DEVERR_TIMEOUT);
+                    s_abort = 1;
+                }
+                break;
+            }
+            const int row = cw * 8 + r;
+            const int tok = rowtok[s * kTileRows + row];
+            const unsigned char* kr = smem + s * C::STAGE_BYTES + row * C::PITCH;
+            const unsigned char* vr = kr + kTileRows * C::PITCH;
+
+            float part = 0.f;
+            if (tok >= 0) {
+                float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int jc = 0; jc < C::CPL; ++jc) {
+                    const uint4 w = *reinterpret_cast<const uint4*>(kr + (jc * 4 + qt) * 16);
+                    float f[C::EPC];
+                    chunk_to_float<KT>(w, f);
+#pragma unroll
+                    for (int e = 0; e < C::EPC; e += 4) {
+                        a0 = __ffma2_rn(make_float2(qv[jc * C::EPC + e], qv[jc * C::EPC + e + 1]),
+                                        make_float2(f[e], f[e + 1]), a0);
+                        a1 = __ffma2_rn(make_float2(qv[jc * C::EPC + e + 2], qv[jc * C::EPC + e + 3]),
+                                        make_float2(f[e + 2], f[e + 3]), a1);
+                    }
+                }
+                part = (a0.x + a0.y) + (a1.x + a1.y);
+            }
+            part += __shfl_xor_sync(0xffffffffu, part, 8);
+            part += __shfl_xor_sync(0xffffffffu, part, 16);
+            const float sc = (tok >= 0) ? part : -CUDART_INF_F;
+            float mx = sc;
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            const float mnew = fmaxf(mrun, mx);
+            if (mnew != -CUDART_INF_F) {
+                if (mnew > mrun) {
+                    const float alpha = exp2f(mrun - mnew);
+                    lrun *= alpha;
+#pragma unroll
+                    for (int i = 0; i < C::DPL / 2; ++i) ov[i] = __fmul2_rn(ov[i], make_float2(alpha, alpha));
+                    mrun = mnew;
+                }
+                const float pr = exp2f(sc - mnew);
+                float ps = pr;
+                ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+                ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+                ps += __shfl_xor_sync(0xffffffffu, ps, 4);
+                lrun += ps;
+                if (tok >= 0) {
+                    const float2 pp2 = make_float2(pr, pr);
+#pragma unroll
+                    for (int jc = 0; jc < C::CPL; ++jc) {
+                        const uint4 w = *reinterpret_cast<const uint4*>(vr + (jc * 4 + qt) * 16);
+                        float f[C::EPC];
+                        chunk_to_float<KT>(w, f);
+#pragma unroll
+                        for (int e = 0; e < C::EPC; e += 2)
+                            ov[(jc * C::EPC + e) / 2] = __ffma2_rn(pp2, make_float2(f[e], f[e + 1]),
+                                                                   ov[(jc * C::EPC + e) / 2]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&bars[C::STAGES + s]));
+        }
+        // reduce the 8 row-lanes of each dim group; lanes r == 0 hold the sums
+#pragma unroll
+        for (int i = 0; i < C::DPL / 2; ++i) {
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) {
+                ov[i].x += __shfl_xor_sync(0xffffffffu, ov[i].x, o);
+                ov[i].y += __shfl_xor_sync(0xffffffffu, ov[i].y, o);
+            }
+        }
+        if (r == 0) {
+#pragma unroll
+            for (int jc = 0; jc < C::CPL; ++jc) {
+                const int dim0 = (jc * 4 + qt) * C::EPC;
+#pragma unroll
+                for (int e = 0; e < C::EPC; e += 2) {
+                    wo[cw * D + dim0 + e] = ov[(jc * C::EPC + e) / 2].x;
+                    wo[cw * D + dim0 + e + 1] = ov[(jc * C::EPC + e) / 2].y;
+                }
+            }
+        }
+        if (lane == 0) {
+            wm[cw] = mrun;
+            wl[cw] = lrun;
+        }
+    }
+    __syncthreads();
+
+    // ---- after a timeout: wait (bounded) for copies still in flight before exit
+    if (s_abort && tid == 0) {
+        const int issued = s_issued;
+        const int zero = 0;
+        for (int s = 0; s < C::STAGES; ++s) {
+            int last = -1;
+            for (int t = s; t < issued; t += C::STAGES) last = t;
+            if (last >= 0)
+                (void)mbar_wait_bounded(smem_addr(&bars[s]), (last / C::STAGES) & 1,
+                                        reinterpret_cast<const volatile int*>(&zero));
+        }
+    }
+
+    // ---- combine the 4 consumer warps: (M, Lsum, O[d]) in base-2 units
+    constexpr float kLn2 = 0.69314718055994530942f;
+    if (tid < D) {
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, wm[w]);
+        float Ls = 0.f, O = 0.f;
+        if (M != -CUDART_INF_F) {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                if (wm[w] != -CUDART_INF_F) {
+                    const float sc = exp2f(wm[w] - M);
+                    Ls += wl[w] * sc;
+                    O += wo[w * D + tid] * sc;
+                }
+            }
+        }
+        if (p.splits == 1) {
+            p.out[(int64_t)head * D + tid] = (Ls > 0.f) ? O / Ls : 0.f;
+            if (tid == 0) p.lse[head] = (Ls > 0.f) ? (M + log2f(Ls)) * kLn2 : -CUDART_INF_F;
+        } else {
+            float* pt = p.part + ((int64_t)head * p.splits + split) * (D + 2);
+            pt[2 + tid] = O;
+            if (tid == 0) {
+                pt[0] = M;
+                pt[1] = Ls;
+            }
+        }
+    }
+    if (p.splits == 1) return;
+
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const unsigned prev = atomicAdd(&p.counters[head], 1u);
+        if (prev >= (unsigned)p.splits) flag_error(p.err, HA_DEVERR_STATE);
+        s_last = (prev == (unsigned)(p.splits - 1)) ? 1 : 0;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (tid < D) {
+        const float* pt = p.part + (int64_t)head * p.splits * (D + 2);
+        float M = -CUDART_INF_F;
+        for (int s = 0; s < p.splits; ++s) M = fmaxf(M, __ldcg(pt + (int64_t)s * (D + 2)));
+        float Ls = 0.f, O = 0.f;
+        if (M != -CUDART_INF_F) {
+            for (int s = 0; s < p.splits; ++s) {
+                const float ms = __ldcg(pt + (int64_t)s * (D + 2));
+                if (ms != -CUDART_INF_F) {
+                    const float sc = exp2f(ms - M);
+                    Ls += __ldcg(pt + (int64_t)s * (D + 2) + 1) * sc;
+                    O += __ldcg(pt + (int64_t)s * (D + 2) + 2 + tid) * sc;
+                }
+            }
+        }
+        p.out[(int64_t)head * D + tid] = (Ls > 0.f) ? O / Ls : 0.f;
+        if (tid == 0) p.lse[head] = (Ls > 0.f) ? (M + log2f(Ls)) * kLn2 : -CUDART_INF_F;
+    }
+    if (tid == 0) p.counters[head] = 0u;
+}
+
+// Exact merge of two partial attentions (Nectar Eq. (3.4)); one warp per row.
+__global__ void __launch_bounds__(256) k_merge(const MergeParams p) {
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= p.rows) return;
+    const float la = p.lse_a[row], lb = p.lse_b[row];
+    const float M = fmaxf(la, lb);
+    const bool empty = (M == -CUDART_INF_F);
+    const float wa = empty ? 0.f : expf(la - M);
+    const float wb = empty ? 0.f : expf(lb - M);
+    const float S = wa + wb;
+    const float ca = empty ? 0.f : wa / S, cb = empty ? 0.f : wb / S;
+    const int64_t base = (int64_t)row * p.d;
+    for (int k = lane; k < p.d; k += 32) {
+        const float oa = p.out_a[base + k], ob = p.out_b[base + k];
+        p.out[base + k] = empty ? 0.f : ca * oa + cb * ob;
+    }
+    __syncwarp();
+    if (lane == 0) p.lse[row] = empty ? -CUDART_INF_F : M + logf(S);
+}
+
+template <int D, typename KT>
+cudaError_t launch_gather_t(const GatherParams& p, cudaStream_t st) {
+    using C = Cfg<D, KT>;
+    const size_t smem = (size_t)C::OFF_PRE + (size_t)(p.nchunks + 1) * sizeof(int);
+    cudaError_t e = cudaFuncSetAttribute(k_gather_att<D, KT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = (unsigned)(p.B * p.Hq) * (unsigned)p.splits;
+    k_gather_att<D, KT><<<grid, kGatherThreads, smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gather(const GatherParams& p, int d, int kv_bf16, cudaStream_t st) {
+    if (d == 128 && kv_bf16) return launch_gather_t<128, __nv_bfloat16>(p, st);
+    if (d == 64 && kv_bf16) return launch_gather_t<64, __nv_bfloat16>(p, st);
+    if (d == 128 && !kv_bf16) return launch_gather_t<128, float>(p, st);
+    if (d == 64 && !kv_bf16) return launch_gather_t<64, float>(p, st);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t st) {
+    if (p.rows <= 0) return cudaSuccess;
+    k_merge<<<(p.rows + 7) / 8, 256, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace ha

@@ -1,0 +1,240 @@
+"""Python binding of libhashattn.so (ctypes; argument marshalling only).
+
+Every function here has the name of the C entry point it calls and forwards
+device pointers taken from torch tensors plus the current CUDA stream. No step
+of the computation runs in Python or torch. Loading fails loudly when the
+library has not been built: there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+from ._build import LIB_PATH
+
+HA_OK = 0
+HA_ERR_INVALID_ARG = -1
+HA_ERR_UNSUPPORTED = -2
+HA_ERR_WORKSPACE = -3
+HA_ERR_CUDA = -4
+HA_ERR_DEVICE = -5
+HA_ERR_TIMEOUT = -6
+
+HA_F32 = 0
+HA_BF16 = 1
+
+HA_DEVERR_SEQLEN = 0x1
+HA_DEVERR_BUDGET = 0x2
+HA_DEVERR_INDEX = 0x4
+HA_DEVERR_COUNT = 0x8
+HA_DEVERR_TIMEOUT = 0x10
+HA_DEVERR_STATE = 0x20
+
+HA_NBINS = 33
+
+# Entry points declared in include/hashattn.h (checked by the tests).
+EXPORTED = [
+    "hash_attn_workspace_size", "hash_attn_workspace_init", "hash_attn_select_capacity",
+    "hash_attn_decode", "hash_attn_decode_timed", "hash_attn_score", "hash_attn_select",
+    "hash_attn_gather_att", "hash_attn_merge", "hash_attn_device_status",
+    "hash_attn_status_string", "hash_attn_last_error",
+]
+
+
+class HAShape(ctypes.Structure):
+    """Mirror of ``ha_shape`` (all strides in elements)."""
+
+    _fields_ = [
+        ("batch", ctypes.c_int32), ("h_q", ctypes.c_int32), ("h_kv", ctypes.c_int32),
+        ("d", ctypes.c_int32), ("n_cap", ctypes.c_int32),
+        ("q_dtype", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
+        ("q_sb", ctypes.c_int64), ("q_sh", ctypes.c_int64),
+        ("k_sb", ctypes.c_int64), ("k_sh", ctypes.c_int64), ("k_sn", ctypes.c_int64),
+        ("v_sb", ctypes.c_int64), ("v_sh", ctypes.c_int64), ("v_sn", ctypes.c_int64),
+        ("ks_sb", ctypes.c_int64), ("ks_sh", ctypes.c_int64),
+    ]
+
+
+class HashAttnError(RuntimeError):
+    def __init__(self, status: int, detail: str):
+        super().__init__(f"{status_string(status)} ({status}): {detail}")
+        self.status = status
+        self.detail = detail
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I32 = ctypes.c_int32
+_SZ = ctypes.c_size_t
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if libhashattn.so has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libhashattn.so not built at {LIB_PATH}; run __graft_entry__.build() "
+                          "or python long_context_sparse_score_gb300/_build.py")
+    L = ctypes.CDLL(LIB_PATH)
+    SP = ctypes.POINTER(HAShape)
+    L.hash_attn_workspace_size.argtypes = [SP, _I32, _I32, _I32, ctypes.POINTER(_SZ)]
+    L.hash_attn_workspace_init.argtypes = [_P, _SZ, _P]
+    L.hash_attn_select_capacity.argtypes = [_I32, _I32, _I32, _I32]
+    L.hash_attn_select_capacity.restype = _I32
+    dec = [SP, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _SZ, _P]
+    L.hash_attn_decode.argtypes = dec
+    L.hash_attn_decode_timed.argtypes = dec + [ctypes.POINTER(_P)]
+    L.hash_attn_score.argtypes = [SP, _P, _P, _P, _P, _P, _P, _SZ, _P]
+    L.hash_attn_select.argtypes = [SP, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _SZ, _P]
+    L.hash_attn_gather_att.argtypes = [SP, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P, _SZ, _P]
+    L.hash_attn_merge.argtypes = [_P, _P, _P, _P, _P, _P, _I32, _I32, _P]
+    L.hash_attn_device_status.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_uint32)]
+    L.hash_attn_status_string.argtypes = [_I32]
+    L.hash_attn_status_string.restype = ctypes.c_char_p
+    L.hash_attn_last_error.argtypes = []
+    L.hash_attn_last_error.restype = ctypes.c_char_p
+    for name in EXPORTED:
+        if name not in ("hash_attn_select_capacity", "hash_attn_status_string", "hash_attn_last_error"):
+            getattr(L, name).restype = _I32
+    _lib = L
+    return L
+
+
+def status_string(status: int) -> str:
+    return lib().hash_attn_status_string(status).decode()
+
+
+def last_error() -> str:
+    return lib().hash_attn_last_error().decode()
+
+
+def _check(status: int) -> None:
+    if status != HA_OK:
+        raise HashAttnError(status, last_error())
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return HA_F32
+    if t.dtype == torch.bfloat16:
+        return HA_BF16
+    raise ValueError(f"unsupported dtype {t.dtype}")
+
+
+def make_shape(q, K, V, k_sig=None, *, n_cap=None, batch=None, share_kv=None) -> HAShape:
+    """ha_shape from tensors: q [B, Hq, d], K/V [Bk, Hkv, n_cap, d], k_sig [Bk, Hkv, n_cap].
+
+    A batch extent of 1 in K/V/k_sig with B > 1 is read as one cache shared by
+    every batch entry (batch stride 0).
+    """
+    B, Hq, d = q.shape
+    Bk, Hkv, ncap, dk = K.shape
+    assert dk == d and V.shape == K.shape
+    s = HAShape()
+    s.batch, s.h_q, s.h_kv, s.d, s.n_cap = B, Hq, Hkv, d, ncap if n_cap is None else n_cap
+    s.q_dtype, s.kv_dtype = _dtype_code(q), _dtype_code(K)
+    s.q_sb, s.q_sh = q.stride(0), q.stride(1)
+    shared = (Bk == 1 and B > 1) if share_kv is None else share_kv
+    s.k_sb = 0 if shared else K.stride(0)
+    s.k_sh, s.k_sn = K.stride(1), K.stride(2)
+    s.v_sb = 0 if shared else V.stride(0)
+    s.v_sh, s.v_sn = V.stride(1), V.stride(2)
+    if k_sig is not None:
+        s.ks_sb = 0 if (k_sig.shape[0] == 1 and B > 1) else k_sig.stride(0)
+        s.ks_sh = k_sig.stride(1)
+    return s
+
+
+def hash_attn_workspace_size(shape: HAShape, m_max: int, n_sink: int, n_local: int) -> int:
+    out = _SZ(0)
+    _check(lib().hash_attn_workspace_size(ctypes.byref(shape), m_max, n_sink, n_local, ctypes.byref(out)))
+    return out.value
+
+
+def hash_attn_workspace_init(workspace, stream=None) -> None:
+    _check(lib().hash_attn_workspace_init(_ptr(workspace), workspace.numel() * workspace.element_size(),
+                                          _stream(stream)))
+
+
+def hash_attn_select_capacity(n_cap: int, m: int, n_sink: int, n_local: int) -> int:
+    return lib().hash_attn_select_capacity(n_cap, m, n_sink, n_local)
+
+
+def _ws(workspace):
+    return _ptr(workspace), workspace.numel() * workspace.element_size()
+
+
+def hash_attn_decode(shape, q, q_sig, k_sig, K, V, seq_lens, m_per_seq, m, n_sink, n_local,
+                     out, lse, sel_idx=None, sel_cnt=None, *, workspace, stream=None) -> None:
+    ws, nb = _ws(workspace)
+    _check(lib().hash_attn_decode(ctypes.byref(shape), _ptr(q), _ptr(q_sig), _ptr(k_sig), _ptr(K),
+                                  _ptr(V), _ptr(seq_lens), _ptr(m_per_seq), m, n_sink, n_local,
+                                  _ptr(out), _ptr(lse), _ptr(sel_idx), _ptr(sel_cnt), ws, nb,
+                                  _stream(stream)))
+
+
+def hash_attn_decode_timed(shape, q, q_sig, k_sig, K, V, seq_lens, m_per_seq, m, n_sink, n_local,
+                           out, lse, events, sel_idx=None, sel_cnt=None, *, workspace,
+                           stream=None) -> None:
+    """``events``: four torch.cuda.Event(enable_timing=True)."""
+    ws, nb = _ws(workspace)
+    arr = (_P * 4)(*[e.cuda_event for e in events])
+    _check(lib().hash_attn_decode_timed(ctypes.byref(shape), _ptr(q), _ptr(q_sig), _ptr(k_sig),
+                                        _ptr(K), _ptr(V), _ptr(seq_lens), _ptr(m_per_seq), m,
+                                        n_sink, n_local, _ptr(out), _ptr(lse), _ptr(sel_idx),
+                                        _ptr(sel_cnt), ws, nb, _stream(stream), arr))
+
+
+def hash_attn_score(shape, q_sig, k_sig, seq_lens, dist=None, hist=None, *, workspace,
+                    stream=None) -> None:
+    ws, nb = _ws(workspace)
+    _check(lib().hash_attn_score(ctypes.byref(shape), _ptr(q_sig), _ptr(k_sig), _ptr(seq_lens),
+                                 _ptr(dist), _ptr(hist), ws, nb, _stream(stream)))
+
+
+def hash_attn_select(shape, q_sig, k_sig, seq_lens, m_per_seq, m, n_sink, n_local, sel_idx, sel_cnt,
+                     *, workspace, stream=None) -> None:
+    ws, nb = _ws(workspace)
+    _check(lib().hash_attn_select(ctypes.byref(shape), _ptr(q_sig), _ptr(k_sig), _ptr(seq_lens),
+                                  _ptr(m_per_seq), m, n_sink, n_local, _ptr(sel_idx), _ptr(sel_cnt),
+                                  ws, nb, _stream(stream)))
+
+
+def hash_attn_gather_att(shape, q, K, V, seq_lens, idx, idx_cap, cnt, out, lse, *, workspace,
+                         stream=None) -> None:
+    ws, nb = _ws(workspace)
+    _check(lib().hash_attn_gather_att(ctypes.byref(shape), _ptr(q), _ptr(K), _ptr(V), _ptr(seq_lens),
+                                      _ptr(idx), idx_cap, _ptr(cnt), _ptr(out), _ptr(lse), ws, nb,
+                                      _stream(stream)))
+
+
+def hash_attn_merge(out_a, lse_a, out_b, lse_b, out, lse, rows: int, d: int, stream=None) -> None:
+    _check(lib().hash_attn_merge(_ptr(out_a), _ptr(lse_a), _ptr(out_b), _ptr(lse_b), _ptr(out),
+                                 _ptr(lse), rows, d, _stream(stream)))
+
+
+def hash_attn_device_status(workspace, stream=None) -> tuple[int, int]:
+    """(status, raw flags); synchronises the stream and clears the error word."""
+    flags = ctypes.c_uint32(0)
+    st = lib().hash_attn_device_status(_ptr(workspace), _stream(stream), ctypes.byref(flags))
+    return st, flags.value

@@ -1,0 +1,377 @@
+"""CUDA path (through the C ABI) against the CPU oracle on the same seeded inputs.
+
+Selected index sets and Hamming distances/histograms must match bit for bit;
+outputs within 2e-3 * (1 + |ref|) and lse within 1e-4 * (1 + |ref|).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import gpu_helpers as GH
+from oracle import hashattn_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from long_context_sparse_score_gb300 import _build
+    _build.build()
+    from long_context_sparse_score_gb300 import hashattn
+    hashattn.lib()
+
+
+def W():
+    from long_context_sparse_score_gb300 import workloads
+    return workloads
+
+
+def all_heads(w):
+    return [(b, h) for b in range(w.B) for h in range(w.Hq)]
+
+
+# ---------------------------------------------------------------- small shapes, many edge cases
+
+SMALL = [
+    # name, B, Hq, Hkv, d, n_cap, lens, m, S, Lw, kv dtype
+    ("g1_d64_bf16", 1, 2, 2, 64, 1500, [1500], 64, 4, 16, torch.bfloat16),
+    ("g4_ragged_tail", 2, 8, 2, 128, 5000, [5000, 3333], 300, 32, 64, torch.bfloat16),
+    ("g8_two_passes", 1, 8, 1, 128, 3000, [2999], 100, 8, 8, torch.bfloat16),
+    ("g2_d64", 3, 4, 2, 64, 2100, [2100, 1, 1025], 50, 3, 5, torch.bfloat16),
+    ("fp32_d128", 1, 4, 1, 128, 1200, [1200], 77, 5, 9, torch.float32),
+    ("fp32_d64", 1, 1, 1, 64, 1024, [1024], 64, 4, 16, torch.float32),
+    ("windows_overlap", 2, 4, 1, 128, 200, [200, 150], 64, 128, 128, torch.bfloat16),
+    ("budget_zero", 1, 4, 2, 128, 900, [900], 0, 16, 16, torch.bfloat16),
+    ("empty_everything", 2, 4, 2, 128, 900, [900, 0], 0, 0, 0, torch.bfloat16),
+    ("budget_at_n", 1, 4, 2, 128, 704, [700], 700, 0, 0, torch.bfloat16),
+    ("budget_above_n", 2, 4, 2, 128, 704, [500, 704], 600, 8, 8, torch.bfloat16),
+    ("chunk_edges", 3, 4, 1, 128, 8196, [8192, 8193, 1024], 512, 1, 1, torch.bfloat16),
+    ("long_rows_many_splits", 1, 4, 1, 128, 40000, [40000], 9000, 64, 64, torch.bfloat16),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
+def test_small_shapes(case):
+    name, B, Hq, Hkv, d, n_cap, lens, m, S, Lw, kvdt = case
+    w = W().make_gqa(7, B=B, Hq=Hq, Hkv=Hkv, d=d, n_cap=n_cap, seq_lens=lens, m=m, n_sink=S,
+                     n_local=Lw, device="cuda", kv_dtype=kvdt, name=name)
+    if kvdt == torch.float32:
+        w.q = w.q.float()
+    res = GH.run_decode(w)
+    assert res["status"] == 0, res["flags"]
+    hc = GH.HostCopy(w)
+    GH.check_selection(res, hc, all_heads(w), m)
+    GH.check_attention(res, hc, all_heads(w), m)
+
+
+def test_tie_heavy_codes():
+    """Few distinct codes: the threshold bin holds most tokens; the index tie rule decides."""
+    w = W().make_gqa(8, B=2, Hq=8, Hkv=2, d=128, n_cap=20000, seq_lens=[20000, 17001], m=1500,
+                     n_sink=16, n_local=16, device="cuda")
+    gen = torch.Generator(device="cuda").manual_seed(99)
+    pool = torch.tensor([0x0F0F0F0F, 0x0F0F0F0E, 0x7F0F0F0F], dtype=torch.int64, device="cuda")
+    pool = torch.where(pool >= 2**31, pool - 2**32, pool).to(torch.int32)
+    pick = torch.randint(0, 3, w.k_sig.shape, generator=gen, device="cuda")
+    w.k_sig = pool[pick].contiguous()
+    w.q_sig = torch.full_like(w.q_sig, 0x0F0F0F0F)
+    res = GH.run_decode(w)
+    assert res["status"] == 0
+    hc = GH.HostCopy(w)
+    GH.check_selection(res, hc, all_heads(w), w.m)
+    GH.check_attention(res, hc, all_heads(w), w.m)
+
+
+def test_all_codes_equal_take_first_m():
+    w = W().make_gqa(9, B=1, Hq=4, Hkv=1, d=128, n_cap=5000, seq_lens=[5000], m=333, n_sink=0,
+                     n_local=0, device="cuda")
+    w.k_sig = torch.full_like(w.k_sig, 12345)
+    res = GH.run_decode(w)
+    idx = res["sel_idx"].cpu().numpy()
+    for h in range(4):
+        assert int(res["sel_cnt"][0, h]) == 333
+        assert np.array_equal(idx[0, h, :333], np.arange(333))
+
+
+def test_ragged_per_sequence_budget():
+    lens = [4096, 9000, 1, 0, 12000, 6000]
+    wl = W()
+    mb = wl.ragged_budget(torch.tensor(lens, dtype=torch.int32))
+    w = wl.make_gqa(5, B=6, Hq=8, Hkv=2, d=128, n_cap=12000, seq_lens=lens, m=int(mb.max()),
+                    n_sink=64, n_local=128, device="cuda", m_per_seq=mb)
+    res = GH.run_decode(w)
+    assert res["status"] == 0
+    hc = GH.HostCopy(w)
+    GH.check_selection(res, hc, all_heads(w), w.m)
+    GH.check_attention(res, hc, all_heads(w), w.m)
+    lse = res["lse"].cpu().numpy()
+    assert np.all(lse[3] == -math.inf) and np.all(res["out"][3].cpu().numpy() == 0)
+
+
+def test_shared_cache_batch_stride_zero():
+    w = W().make_gqa(4, B=5, Hq=8, Hkv=2, d=128, n_cap=6000, seq_lens=6000, m=512, n_sink=128,
+                     n_local=0, device="cuda", shared=True)
+    assert w.K.shape[0] == 1
+    res = GH.run_decode(w)
+    hc = GH.HostCopy(w)
+    GH.check_selection(res, hc, all_heads(w), w.m)
+    GH.check_attention(res, hc, all_heads(w), w.m)
+
+
+def test_strided_views():
+    """K/V and codes as views into larger buffers (padded token and head strides)."""
+    base = W().make_gqa(10, B=2, Hq=4, Hkv=2, d=128, n_cap=3000, seq_lens=[2900, 3000], m=200,
+                        n_sink=8, n_local=8, device="cuda")
+    Kb = torch.zeros((2, 2, 3100, 136), dtype=torch.bfloat16, device="cuda")
+    Vb = torch.zeros((2, 2, 3072, 128), dtype=torch.bfloat16, device="cuda")
+    Kb[:, :, :3000, :128] = base.K
+    Vb[:, :, :3000] = base.V
+    Cb = torch.zeros((2, 2, 3004), dtype=torch.int32, device="cuda")
+    Cb[:, :, :3000] = base.k_sig
+    K = Kb[:, :, :3000, :128]
+    V = Vb[:, :, :3000]
+    base.k_sig = Cb[:, :, :3000]
+    res = GH.run_decode(base, K=K, V=V)
+    assert res["status"] == 0
+    hc = GH.HostCopy(base, K=K, V=V)
+    GH.check_selection(res, hc, all_heads(base), base.m)
+    GH.check_attention(res, hc, all_heads(base), base.m)
+
+
+def test_dense_path_equals_full_attention():
+    w = W().make_gqa(11, B=2, Hq=8, Hkv=2, d=128, n_cap=3000, seq_lens=[3000, 2222], m=0,
+                     n_sink=0, n_local=0, device="cuda")
+    res = GH.run_decode(w, m=3000, dense=True, m_per_seq=None)
+    assert res["status"] == 0
+    hc = GH.HostCopy(w)
+    GH.check_attention(res, hc, all_heads(w), 3000, dense=True)
+
+
+def test_repeated_calls_are_identical():
+    w = W().make_gqa(12, B=2, Hq=8, Hkv=2, d=128, n_cap=9000, seq_lens=[9000, 8000], m=700,
+                     n_sink=16, n_local=16, device="cuda")
+    a = GH.run_decode(w)
+    b = GH.run_decode(w, ws=a["ws"])
+    c = GH.run_decode(w, ws=a["ws"])
+    for r in (b, c):
+        assert torch.equal(a["out"], r["out"]) and torch.equal(a["lse"], r["lse"])
+        assert torch.equal(a["sel_idx"], r["sel_idx"])
+
+
+# ---------------------------------------------------------------- stage entry points
+
+def test_score_entry_point():
+    H = GH.ha()
+    w = W().make_gqa(13, B=2, Hq=8, Hkv=2, d=128, n_cap=7000, seq_lens=[7000, 4321], m=64,
+                     n_sink=0, n_local=0, device="cuda")
+    shape = H.make_shape(w.q, w.K, w.V, w.k_sig)
+    ws = GH.workspace(shape, w.m, 0, 0)
+    dist = torch.full((2, 8, 7000), 255, dtype=torch.uint8, device="cuda")
+    hist = torch.zeros((2, 8, 33), dtype=torch.int32, device="cuda")
+    H.hash_attn_score(shape, w.q_sig, w.k_sig, w.seq_lens, dist, hist, workspace=ws)
+    torch.cuda.synchronize()
+    dist = dist.cpu().numpy()
+    hist = hist.cpu().numpy()
+    qs = w.q_sig.cpu().numpy()
+    for b, n in [(0, 7000), (1, 4321)]:
+        for h in range(8):
+            ref = O.hamming_distances(int(qs[b, h]), w.k_sig[b, h // 4, :n].cpu().numpy())
+            assert np.array_equal(dist[b, h, :n], ref)
+            assert np.all(dist[b, h, n:] == 255)
+            assert np.array_equal(hist[b, h], O.distance_histogram(ref))
+
+
+def test_select_entry_point_matches_decode():
+    H = GH.ha()
+    w = W().make_gqa(14, B=2, Hq=8, Hkv=2, d=128, n_cap=10000, seq_lens=[10000, 7777], m=600,
+                     n_sink=32, n_local=48, device="cuda")
+    shape = H.make_shape(w.q, w.K, w.V, w.k_sig)
+    ws = GH.workspace(shape, w.m, w.n_sink, w.n_local)
+    cap = H.hash_attn_select_capacity(10000, 600, 32, 48)
+    sel = torch.empty((2, 8, cap), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((2, 8), dtype=torch.int32, device="cuda")
+    H.hash_attn_select(shape, w.q_sig, w.k_sig, w.seq_lens, None, 600, 32, 48, sel, cnt, workspace=ws)
+    res = {"sel_idx": sel, "sel_cnt": cnt}
+    GH.check_selection(res, GH.HostCopy(w), all_heads(w), 600)
+    dec = GH.run_decode(w)
+    assert torch.equal(dec["sel_idx"], sel) and torch.equal(dec["sel_cnt"], cnt)
+
+
+def test_gather_att_entry_point_with_given_lists():
+    H = GH.ha()
+    w = W().make_gqa(15, B=2, Hq=4, Hkv=2, d=128, n_cap=5000, seq_lens=[5000, 3000], m=0,
+                     n_sink=0, n_local=0, device="cuda")
+    rng = np.random.default_rng(0)
+    cap = 700
+    idx = np.full((2, 4, cap), -1, dtype=np.int32)
+    cnt = np.zeros((2, 4), dtype=np.int32)
+    lists = {}
+    for b, n in [(0, 5000), (1, 3000)]:
+        for h in range(4):
+            k = int(rng.integers(0, cap + 1))
+            sel = rng.choice(n, size=k, replace=False)       # unsorted on purpose
+            idx[b, h, :k] = sel
+            cnt[b, h] = k
+            lists[(b, h)] = np.sort(sel)
+    shape = H.make_shape(w.q, w.K, w.V)
+    ws = GH.workspace(shape, cap, 0, 0)
+    out = torch.empty((2, 4, 128), device="cuda")
+    lse = torch.empty((2, 4), device="cuda")
+    H.hash_attn_gather_att(shape, w.q, w.K, w.V, w.seq_lens, torch.from_numpy(idx).cuda(), cap,
+                           torch.from_numpy(cnt).cuda(), out, lse, workspace=ws)
+    st, flags = H.hash_attn_device_status(ws)
+    assert st == 0, flags
+    hc = GH.HostCopy(w)
+    for (b, h), sel in lists.items():
+        Kh, Vh = hc.kv(b, h // 2)
+        ro, rl = O.attend(hc.q[b, h], Kh, Vh, sel)
+        GH.assert_out_close(out[b, h].cpu().numpy(), ro, f"({b},{h})")
+        GH.assert_lse_close(float(lse[b, h]), rl, f"({b},{h})")
+    # an index outside [0, seq_len) is skipped and flagged
+    idx[1, 0, 0] = 3000
+    cnt[1, 0] = max(cnt[1, 0], 1)
+    H.hash_attn_gather_att(shape, w.q, w.K, w.V, w.seq_lens, torch.from_numpy(idx).cuda(), cap,
+                           torch.from_numpy(cnt).cuda(), out, lse, workspace=ws)
+    st, flags = H.hash_attn_device_status(ws)
+    assert st == H.HA_ERR_DEVICE and flags & H.HA_DEVERR_INDEX
+
+
+def test_merge_entry_point():
+    H = GH.ha()
+    rng = np.random.default_rng(1)
+    rows, d = 37, 128
+    oa = rng.standard_normal((rows, d)).astype(np.float32)
+    ob = rng.standard_normal((rows, d)).astype(np.float32)
+    la = (rng.standard_normal(rows) * 3).astype(np.float32)
+    lb = (rng.standard_normal(rows) * 3).astype(np.float32)
+    la[3] = -np.inf
+    lb[5] = -np.inf
+    la[7] = lb[7] = -np.inf
+    t = lambda a: torch.from_numpy(a).cuda()
+    out = torch.empty((rows, d), device="cuda")
+    lse = torch.empty(rows, device="cuda")
+    H.hash_attn_merge(t(oa), t(la), t(ob), t(lb), out, lse, rows, d)
+    torch.cuda.synchronize()
+    for r in range(rows):
+        ro, rl = O.merge(oa[r], float(la[r]), ob[r], float(lb[r]))
+        GH.assert_out_close(out[r].cpu().numpy(), ro, f"row {r}")
+        GH.assert_lse_close(float(lse[r]), rl, f"row {r}")
+    # in place (out aliases out_a)
+    A, LA = t(oa.copy()), t(la.copy())
+    H.hash_attn_merge(A, LA, t(ob), t(lb), A, LA, rows, d)
+    torch.cuda.synchronize()
+    assert torch.allclose(A, out) and torch.equal(LA.isinf(), lse.isinf())
+
+
+def test_device_errors_are_flagged_not_faulted():
+    H = GH.ha()
+    w = W().make_gqa(16, B=3, Hq=4, Hkv=2, d=128, n_cap=2000, seq_lens=[2000, 1500, 2000], m=100,
+                     n_sink=4, n_local=4, device="cuda")
+    w.seq_lens = torch.tensor([2000, 2001, -5], dtype=torch.int32, device="cuda")  # 2 bad entries
+    res = GH.run_decode(w)
+    assert res["status"] == H.HA_ERR_DEVICE and res["flags"] & H.HA_DEVERR_SEQLEN
+    assert torch.all(res["lse"][1:].isneginf()) and torch.all(res["out"][1:] == 0)
+    assert torch.all(res["sel_cnt"][1:] == 0)
+    hc = GH.HostCopy(w)
+    GH.check_attention(res, hc, [(0, h) for h in range(4)], w.m)
+    # a per-sequence budget above the bound is clamped and flagged
+    w.seq_lens = torch.tensor([2000, 1500, 2000], dtype=torch.int32, device="cuda")
+    w.m_per_seq = torch.tensor([100, 150, 50], dtype=torch.int32, device="cuda")
+    res = GH.run_decode(w, m=100)
+    assert res["status"] == H.HA_ERR_DEVICE and res["flags"] & H.HA_DEVERR_BUDGET
+    assert int(res["sel_cnt"][1, 0]) == len(O.selected_set(int(w.q_sig[1, 0]),
+                                                              w.k_sig[1, 0].cpu().numpy(), 1500, 100, 4, 4))
+    # the next call on the same workspace reports clean
+    w.m_per_seq = None
+    res = GH.run_decode(w, ws=res["ws"])
+    assert res["status"] == 0
+
+
+# ---------------------------------------------------------------- the five workloads at full size
+
+def test_workload1_tiny_full():
+    w = W().make_workload(1, "cuda")
+    res = GH.run_decode(w)
+    assert res["status"] == 0
+    hc = GH.HostCopy(w)
+    GH.check_selection(res, hc, all_heads(w), w.m)
+    GH.check_attention(res, hc, all_heads(w), w.m)
+
+
+def test_workload2_gqa_32k_full():
+    w = W().make_workload(2, "cuda")
+    res = GH.run_decode(w)
+    assert res["status"] == 0
+    hc = GH.HostCopy(w)
+    GH.check_selection(res, hc, all_heads(w), w.m)
+    GH.check_attention(res, hc, all_heads(w), w.m)
+
+
+def _sample_heads(w, k, seed):
+    rng = np.random.default_rng(seed)
+    pairs = all_heads(w)
+    pick = rng.choice(len(pairs), size=min(k, len(pairs)), replace=False)
+    return sorted(pairs[i] for i in pick)
+
+
+def test_workload3_batch16_128k_sampled():
+    w = W().make_workload(3, "cuda")
+    res = GH.run_decode(w)
+    assert res["status"] == 0
+    hc = GH.HostCopy(w)
+    heads = _sample_heads(w, 24, 3)
+    GH.check_selection(res, hc, heads, w.m)
+    GH.check_attention(res, hc, heads[:12], w.m)
+    # properties that hold for every head: |I| within [min(n, m), m + S + Lw], ascending, windows in
+    cnt = res["sel_cnt"].cpu().numpy()
+    assert cnt.min() >= 4096 and cnt.max() <= 4096 + 128 + 256
+    idx = res["sel_idx"].cpu().numpy()
+    assert np.all(np.diff(idx[:, :, :4096], axis=-1) > 0)
+    assert np.all(idx[:, :, :128] == np.arange(128))
+    del w, res
+
+
+def test_workload4_shared_document_full():
+    H = GH.ha()
+    w = W().make_workload(4, "cuda")
+    doc = GH.run_decode(w)
+    assert doc["status"] == 0
+    B, Hq, d = w.q.shape
+    from types import SimpleNamespace
+    loc_w = SimpleNamespace(q=w.q, q_sig=None, k_sig=None, K=w.K_loc, V=w.V_loc, B=B, Hq=Hq,
+                            Hkv=8, m=512, n_sink=0, n_local=0, m_per_seq=None,
+                            seq_lens=torch.full((B,), 512, dtype=torch.int32, device="cuda"))
+    loc = GH.run_decode(loc_w, dense=True, m_per_seq=None)
+    assert loc["status"] == 0
+    out = torch.empty_like(doc["out"])
+    lse = torch.empty_like(doc["lse"])
+    H.hash_attn_merge(doc["out"], doc["lse"], loc["out"], loc["lse"], out, lse, B * Hq, d)
+    torch.cuda.synchronize()
+    hc = GH.HostCopy(w)
+    heads = _sample_heads(w, 16, 4)
+    GH.check_selection(doc, hc, heads, w.m)
+    q = w.q.float().cpu().numpy()
+    for b, h in heads[:8]:
+        _, _, od, ld = hc.head(b, h, w.m)
+        Kl = w.K_loc[b, h // 4].float().cpu().numpy()
+        Vl = w.V_loc[b, h // 4].float().cpu().numpy()
+        ol, ll = O.attend(q[b, h], Kl, Vl, np.arange(512))
+        ro, rl = O.merge(od, ld, ol, ll)
+        GH.assert_out_close(out[b, h].cpu().numpy(), ro, f"merged ({b},{h})")
+        GH.assert_lse_close(float(lse[b, h]), rl, f"merged ({b},{h})")
+
+
+def test_workload5_ragged_full_sparse_and_dense():
+    w = W().make_workload(5, "cuda")
+    res = GH.run_decode(w)
+    assert res["status"] == 0
+    hc = GH.HostCopy(w)
+    heads = _sample_heads(w, 24, 5)
+    GH.check_selection(res, hc, heads, w.m)
+    GH.check_attention(res, hc, heads[:12], w.m)
+    dense = GH.run_decode(w, m=w.n_cap, m_per_seq=None, dense=True, sel=False)
+    assert dense["status"] == 0
+    GH.check_attention(dense, hc, heads[:6], w.n_cap, dense=True)

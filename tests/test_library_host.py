@@ -1,0 +1,138 @@
+"""Host-side tests of the C ABI that need no GPU.
+
+The library must build, load and export every entry point that
+include/hashattn.h declares; argument errors must come back as status codes
+before anything is enqueued (so these calls never touch a device).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def ha():
+    from long_context_sparse_score_gb300 import _build
+    _build.build()
+    from long_context_sparse_score_gb300 import hashattn
+    return hashattn
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "hashattn.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:ha_status|size_t|int32_t|const char\*)\s+(hash_attn_\w+)\(",
+                                 text, re.M)))
+
+
+def test_header_declares_the_binding_names(ha):
+    assert _declared() == sorted(ha.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(ha):
+    L = ha.lib()
+    for name in _declared():
+        assert hasattr(L, name), name
+
+
+def _shape(ha, **kw):
+    s = ha.HAShape()
+    s.batch, s.h_q, s.h_kv, s.d, s.n_cap = 2, 8, 2, 128, 4096
+    s.q_dtype = s.kv_dtype = ha.HA_BF16
+    s.q_sb, s.q_sh = 8 * 128, 128
+    s.k_sb, s.k_sh, s.k_sn = 2 * 4096 * 128, 4096 * 128, 128
+    s.v_sb, s.v_sh, s.v_sn = s.k_sb, s.k_sh, s.k_sn
+    s.ks_sb, s.ks_sh = 2 * 4096, 4096
+    for k, v in kw.items():
+        setattr(s, k, v)
+    return s
+
+
+def _ws_size(ha, s, m=256, S=16, L=16):
+    out = ctypes.c_size_t(0)
+    st = ha.lib().hash_attn_workspace_size(ctypes.byref(s), m, S, L, ctypes.byref(out))
+    return st, out.value
+
+
+def test_workspace_size_and_capacity(ha):
+    st, nbytes = _ws_size(ha, _shape(ha))
+    assert st == ha.HA_OK and nbytes > 0 and nbytes % 256 == 0
+    # the budget arithmetic of the pages: 16,384 tokens, m=1,024, 128 + 128 -> 1,280 reads
+    assert ha.hash_attn_select_capacity(16384, 1024, 128, 128) == 1280
+    assert ha.hash_attn_select_capacity(1000, 1024, 128, 128) == 1000
+    assert ha.hash_attn_select_capacity(4096, 0, 0, 0) == 0
+    # a dense-sized workspace (m >= n_cap) is at least as large as a sparse one
+    assert _ws_size(ha, _shape(ha), m=4096)[1] >= nbytes
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("d", 96, -2), ("d", 256, -2), ("h_q", 7, -1), ("h_kv", 0, -1), ("batch", 0, -1),
+    ("n_cap", 0, -1), ("kv_dtype", 5, -2), ("q_dtype", -1, -2), ("k_sn", 0, -1), ("q_sh", -3, -1),
+])
+def test_bad_shape_is_rejected(ha, field, value, status):
+    st, _ = _ws_size(ha, _shape(ha, **{field: value}))
+    assert st == status
+    assert ha.last_error() != ""
+
+
+def _decode(ha, s, *, q=512, q_sig=512, k_sig=512, K=512, V=512, seq=512, m=256, S=16, L=16,
+            out=512, lse=512, ws=1024, ws_bytes=None, sel=None, cnt=None):
+    if ws_bytes is None:
+        ws_bytes = 1 << 40
+    return ha.lib().hash_attn_decode(ctypes.byref(s), q, q_sig, k_sig, K, V, seq, None, m, S, L,
+                                     out, lse, sel, cnt, ws, ws_bytes, None)
+
+
+def test_decode_argument_errors_before_launch(ha):
+    s = _shape(ha)
+    assert _decode(ha, s, q=None) == ha.HA_ERR_INVALID_ARG
+    assert _decode(ha, s, K=None) == ha.HA_ERR_INVALID_ARG
+    assert _decode(ha, s, out=None) == ha.HA_ERR_INVALID_ARG
+    assert _decode(ha, s, k_sig=None) == ha.HA_ERR_INVALID_ARG          # sparse path needs codes
+    assert _decode(ha, s, k_sig=516) == ha.HA_ERR_INVALID_ARG           # unaligned codes
+    assert _decode(ha, s, K=520) == ha.HA_ERR_INVALID_ARG               # unaligned rows
+    assert _decode(ha, s, m=-1) == ha.HA_ERR_INVALID_ARG
+    assert _decode(ha, s, S=-4) == ha.HA_ERR_INVALID_ARG
+    assert _decode(ha, s, ws=None) == ha.HA_ERR_WORKSPACE
+    assert _decode(ha, s, ws=1024 + 16) == ha.HA_ERR_WORKSPACE           # not 256-aligned
+    assert _decode(ha, s, ws_bytes=1024) == ha.HA_ERR_WORKSPACE          # too small
+    assert _decode(ha, s, sel=512) == ha.HA_ERR_INVALID_ARG              # sel_idx without sel_cnt
+    assert _decode(ha, _shape(ha, ks_sh=4095)) == ha.HA_ERR_INVALID_ARG  # code rows unaligned
+    assert _decode(ha, _shape(ha, k_sn=100)) == ha.HA_ERR_INVALID_ARG    # 200-byte row stride
+    assert _decode(ha, _shape(ha, d=80)) == ha.HA_ERR_UNSUPPORTED
+    assert "workspace" in ha.last_error() or ha.last_error() != ""
+
+
+def test_other_entry_points_reject_bad_arguments(ha):
+    L = ha.lib()
+    s = _shape(ha)
+    sp = ctypes.byref(s)
+    assert L.hash_attn_score(sp, 512, 512, 512, None, None, 1024, 1 << 40, None) == ha.HA_ERR_INVALID_ARG
+    assert L.hash_attn_select(sp, 512, 512, 512, None, 8, 0, 0, None, 512, 1024, 1 << 40,
+                              None) == ha.HA_ERR_INVALID_ARG
+    assert L.hash_attn_gather_att(sp, 512, 512, 512, 512, 512, 5000, 512, 512, 512, 1024, 1 << 40,
+                                  None) == ha.HA_ERR_INVALID_ARG     # idx_cap > n_cap
+    assert L.hash_attn_merge(512, 512, 512, 512, 512, 512, -1, 128, None) == ha.HA_ERR_INVALID_ARG
+    assert L.hash_attn_merge(None, 512, 512, 512, 512, 512, 4, 128, None) == ha.HA_ERR_INVALID_ARG
+    assert L.hash_attn_merge(None, None, None, None, None, None, 0, 128, None) == ha.HA_OK  # nothing to do
+    assert L.hash_attn_device_status(None, None, None) == ha.HA_ERR_WORKSPACE
+    assert L.hash_attn_workspace_init(None, 16, None) == ha.HA_ERR_WORKSPACE
+    events = (ctypes.c_void_p * 4)(None, None, None, None)
+    assert L.hash_attn_decode_timed(sp, 512, 512, 512, 512, 512, 512, None, 8, 0, 0, 512, 512, None,
+                                    None, 1024, 1 << 40, None, events) == ha.HA_ERR_INVALID_ARG
+
+
+def test_status_strings(ha):
+    for code in range(0, -7, -1):
+        assert ha.status_string(code) not in ("", "unknown status")
+    assert ha.status_string(-99) == "unknown status"
+
+
+def test_product_path_fails_loudly_without_the_library(ha, monkeypatch, tmp_path):
+    from long_context_sparse_score_gb300 import hashattn
+    monkeypatch.setattr(hashattn, "_lib", None)
+    monkeypatch.setattr(hashattn, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        hashattn.lib()
