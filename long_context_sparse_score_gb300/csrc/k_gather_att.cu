@@ -8,11 +8,13 @@
 // and Eqs. (3.4)-(3.5): the log-normaliser lse = log sum_j e^{z_j} is returned
 // with o, and partial results over disjoint token sets merge exactly.
 //
-// k_gather_att: one CTA per (query head, split of I). Warp 0 is the producer: it
-// turns list positions into token indices and has the TMA engine copy each
-// selected K row and V row (one 1-D bulk copy per row, straight from the cache)
-// into a ring of shared-memory stages, completion counted on an mbarrier per
-// stage. Warps 1-4 consume: 8 rows per warp per 32-row stage, 4 lanes per row.
+// k_gather_att: one CTA per (query head, split of I). The CTA first turns its
+// range of list positions into token indices in shared memory. Warp 0 is the
+// producer: per 32-row stage it copies each selected K row and V row straight
+// from the cache with 16-byte asynchronous copies (one warp instruction moves a
+// 256-byte K row and its 256-byte V row), and an mbarrier per stage completes
+// when they have landed. Warps 1-4 consume: 8 rows per warp per stage, 4 lanes
+// per row.
 // Scores are fp32 (q pre-scaled by log2(e)/sqrt(d), packed fp32x2 FMAs), the
 // softmax is online in base 2, and P.V accumulates per lane over its rows.
 // Splits write (max, sum, o) partials; the last CTA of a head to finish merges
@@ -40,7 +42,7 @@ struct Cfg {
     static constexpr int OFF_TOK = DATA_BYTES;                            // int [STAGES][32]
     static constexpr int OFF_BAR = OFF_TOK + STAGES * kTileRows * 4;      // u64 full[S], empty[S]
     static constexpr int OFF_CMB = OFF_BAR + 2 * STAGES * 8;              // float wm[4], wl[4], wo[4][D]
-    static constexpr int OFF_PRE = OFF_CMB + (8 + 4 * D) * 4;             // int pre[nchunks + 1]
+    static constexpr int OFF_TOKL = OFF_CMB + (8 + 4 * D) * 4;            // int tokl[rows_per_split]
 };
 
 template <typename KT>
@@ -77,7 +79,8 @@ __global__ void __launch_bounds__(kGatherThreads) k_gather_att(const GatherParam
     float* wm = reinterpret_cast<float*>(smem + C::OFF_CMB);
     float* wl = wm + 4;
     float* wo = wm + 8;
-    int* pre = reinterpret_cast<int*>(smem + C::OFF_PRE);
+    int* tokl = reinterpret_cast<int*>(smem + C::OFF_TOKL);
+    int* pre = tokl + p.rows_per_split;   // [nchunks + 1] (segmented lists only)
     __shared__ int s_L, s_issued, s_last;
     __shared__ volatile int s_abort;
 
@@ -127,8 +130,8 @@ __global__ void __launch_bounds__(kGatherThreads) k_gather_att(const GatherParam
             s_abort = 0;
             s_issued = 0;
             for (int s = 0; s < C::STAGES; ++s) {
-                mbar_init(smem_addr(&bars[s]), 1);
-                mbar_init(smem_addr(&bars[C::STAGES + s]), 4);
+                mbar_init(smem_addr(&bars[s]), 1);               // producer lane 0 (+ copy tracking)
+                mbar_init(smem_addr(&bars[C::STAGES + s]), 4);   // one arrival per consumer warp
             }
             mbar_fence_init();
         }
@@ -138,17 +141,44 @@ __global__ void __launch_bounds__(kGatherThreads) k_gather_att(const GatherParam
     const int L = s_L;
     const int r0 = split * p.rows_per_split;
     const int r1 = min(L, r0 + p.rows_per_split);
-    const int ntiles = (r1 > r0) ? (r1 - r0 + kTileRows - 1) / kTileRows : 0;
+    const int nrows = max(0, r1 - r0);
+    const int ntiles = (nrows + kTileRows - 1) / kTileRows;
+
+    // ---- this CTA's token indices, list positions [r0, r1), into shared memory
+    {
+        const int nch = (p.mode == kSegmented) ? (n + p.chunk - 1) / p.chunk : 0;
+        const int32_t* seg = (p.mode == kSegmented) ? p.seg_idx + (int64_t)head * p.nchunks * p.chunk
+                                                    : nullptr;
+        const int32_t* lst = (p.mode == kList) ? p.list_idx + (int64_t)head * p.list_cap : nullptr;
+        for (int i = tid; i < nrows; i += kGatherThreads) {
+            const int pp = r0 + i;
+            int tok;
+            if (p.mode == kIdentity) {
+                tok = pp;
+            } else if (p.mode == kSegmented) {
+                int lo = 0, hi = nch - 1;
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (pre[mid] <= pp) lo = mid; else hi = mid - 1;
+                }
+                tok = seg[(int64_t)lo * p.chunk + (pp - pre[lo])];
+            } else {
+                tok = lst[pp];
+                if (tok < 0 || tok >= n) {
+                    flag_error(p.err, HA_DEVERR_INDEX);
+                    tok = -1;
+                }
+            }
+            tokl[i] = tok;
+        }
+    }
+    __syncthreads();
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         const char* Kb = p.K + ((int64_t)b * p.k_sb + (int64_t)g * p.k_sh) * C::ES;
         const char* Vb = p.V + ((int64_t)b * p.v_sb + (int64_t)g * p.v_sh) * C::ES;
-        const int nch = (p.mode == kSegmented) ? (n + p.chunk - 1) / p.chunk : 0;
-        const int32_t* seg = (p.mode == kSegmented)
-                                 ? p.seg_idx + (int64_t)head * p.nchunks * p.chunk
-                                 : nullptr;
-        const int32_t* lst = (p.mode == kList) ? p.list_idx + (int64_t)head * p.list_cap : nullptr;
+        const int64_t kstep = p.k_sn * C::ES, vstep = p.v_sn * C::ES;
         int issued = 0;
         for (int t = 0; t < ntiles; ++t) {
             const int s = t % C::STAGES;
@@ -165,38 +195,29 @@ __global__ void __launch_bounds__(kGatherThreads) k_gather_att(const GatherParam
                     break;
                 }
             }
-            const int pp = r0 + t * kTileRows + lane;
-            int tok = -1;
-            if (pp < r1) {
-                if (p.mode == kIdentity) {
-                    tok = pp;
-                } else if (p.mode == kSegmented) {
-                    int lo = 0, hi = nch - 1;
-                    while (lo < hi) {
-                        const int mid = (lo + hi + 1) >> 1;
-                        if (pre[mid] <= pp) lo = mid; else hi = mid - 1;
-                    }
-                    tok = seg[(int64_t)lo * p.chunk + (pp - pre[lo])];
-                } else {
-                    tok = lst[pp];
-                    if (tok < 0 || tok >= n) {
-                        flag_error(p.err, HA_DEVERR_INDEX);
-                        tok = -1;
-                    }
+            const int row0 = t * kTileRows;
+            const int tok = (row0 + lane < nrows) ? tokl[row0 + lane] : -1;
+            int* rt = rowtok + s * kTileRows;
+            rt[lane] = tok;
+            __syncwarp();
+            unsigned char* stage = smem + s * C::STAGE_BYTES;
+            // (row, K or V, 16-byte chunk) triples of the stage, 32 per warp instruction
+#pragma unroll 4
+            for (int it = lane; it < kTileRows * 2 * C::NCH; it += 32) {
+                const int row = it / (2 * C::NCH);
+                const int rem = it - row * (2 * C::NCH);
+                const int isv = rem >= C::NCH ? 1 : 0;
+                const int ch = rem - isv * C::NCH;
+                const int tr = rt[row];
+                if (tr >= 0) {
+                    const char* src = (isv ? Vb + (int64_t)tr * vstep : Kb + (int64_t)tr * kstep) + ch * 16;
+                    cp_async16(smem_addr(stage + (isv * kTileRows + row) * C::PITCH + ch * 16), src);
                 }
             }
-            rowtok[s * kTileRows + lane] = tok;
-            const unsigned vm = __ballot_sync(0xffffffffu, tok >= 0);
-            __syncwarp();
             const uint32_t full = smem_addr(&bars[s]);
-            if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)__popc(vm) * 2u * C::RB);
+            cp_async_arrive(full);
             __syncwarp();
-            if (tok >= 0) {
-                unsigned char* ks = smem + s * C::STAGE_BYTES + lane * C::PITCH;
-                unsigned char* vs = ks + kTileRows * C::PITCH;
-                bulk_g2s(smem_addr(ks), Kb + (int64_t)tok * p.k_sn * C::ES, C::RB, full);
-                bulk_g2s(smem_addr(vs), Vb + (int64_t)tok * p.v_sn * C::ES, C::RB, full);
-            }
+            if (lane == 0) mbar_arrive(full);
             issued = t + 1;
         }
         if (lane == 0) s_issued = issued;
@@ -418,7 +439,7 @@ __global__ void __launch_bounds__(256) k_merge(const MergeParams p) {
 template <int D, typename KT>
 cudaError_t launch_gather_t(const GatherParams& p, cudaStream_t st) {
     using C = Cfg<D, KT>;
-    const size_t smem = (size_t)C::OFF_PRE + (size_t)(p.nchunks + 1) * sizeof(int);
+    const size_t smem = (size_t)C::OFF_TOKL + (size_t)(p.rows_per_split + p.nchunks + 1) * sizeof(int);
     cudaError_t e = cudaFuncSetAttribute(k_gather_att<D, KT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;

@@ -42,6 +42,28 @@ __device__ __forceinline__ void load_codes(const uint32_t* __restrict__ row, int
     }
 }
 
+// Codes of this thread in SCORE: groups of 4 consecutive tokens, the warp's 32
+// lanes reading 512 contiguous bytes per load; token of slot j is
+// c0 + (j / 4) * (4 * kScoreThreads) + 4 * threadIdx.x + j % 4.
+template <int TPT>
+__device__ __forceinline__ void load_codes_coalesced(const uint32_t* __restrict__ row, int c0, int n,
+                                                     uint32_t (&c)[TPT]) {
+#pragma unroll
+    for (int j = 0; j < TPT / 4; ++j) {
+        const int i = c0 + j * 4 * kScoreThreads + 4 * threadIdx.x;
+        if (i + 4 <= n) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(row + i));
+            c[4 * j + 0] = v.x;
+            c[4 * j + 1] = v.y;
+            c[4 * j + 2] = v.z;
+            c[4 * j + 3] = v.w;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) c[4 * j + e] = (i + e < n) ? __ldg(row + i + e) : 0u;
+        }
+    }
+}
+
 __device__ __forceinline__ uint32_t warp_sum(uint32_t v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -94,7 +116,7 @@ __device__ __forceinline__ uint32_t field(uint32_t w01, uint32_t w23, int e) {
 // ---------------------------------------------------------------- SCORE
 
 template <int TPT>
-__global__ void __launch_bounds__(kScoreThreads) k_score(const ScoreParams p) {
+__global__ void __launch_bounds__(kScoreThreads, 3) k_score(const ScoreParams p) {
     constexpr int C = kScoreThreads * TPT;
     // Per-thread histogram columns: hist[bin][thread], the counts of up to four
     // heads packed one byte each (a thread sees at most TPT <= 32 tokens).
@@ -112,10 +134,9 @@ __global__ void __launch_bounds__(kScoreThreads) k_score(const ScoreParams p) {
     if (c0 >= n) return;
 
     const uint32_t* row = p.k_sig + (int64_t)b * p.ks_sb + (int64_t)g * p.ks_sh;
-    const int i0 = c0 + tid * TPT;
     uint32_t code[TPT];
-    load_codes<TPT>(row, i0, n, code);
-    const int nvalid = max(0, min(TPT, n - i0));
+    load_codes_coalesced<TPT>(row, c0, n, code);
+    const int nin = n - c0;  // tokens of this chunk are valid below this offset
 
     for (int hp = 0; hp < p.G; hp += kMaxHeadsPerPass) {
         const int nh = min(kMaxHeadsPerPass, p.G - hp);
@@ -126,7 +147,8 @@ __global__ void __launch_bounds__(kScoreThreads) k_score(const ScoreParams p) {
         for (int u = 0; u < HA_NBINS; ++u) hist[u][tid] = 0u;
 #pragma unroll
         for (int j = 0; j < TPT; ++j) {
-            if (j < nvalid) {
+            const int off = (j >> 2) * 4 * kScoreThreads + 4 * tid + (j & 3);
+            if (off < nin) {
 #pragma unroll
                 for (int e = 0; e < kMaxHeadsPerPass; ++e) {
                     if (e < nh) {
@@ -140,10 +162,12 @@ __global__ void __launch_bounds__(kScoreThreads) k_score(const ScoreParams p) {
 #pragma unroll
             for (int e = 0; e < kMaxHeadsPerPass; ++e) {
                 if (e < nh) {
-                    uint8_t* drow = p.dist + (int64_t)(head0 + hp + e) * p.n_cap + i0;
+                    uint8_t* drow = p.dist + (int64_t)(head0 + hp + e) * p.n_cap + c0;
 #pragma unroll
-                    for (int j = 0; j < TPT; ++j)
-                        if (j < nvalid) drow[j] = (uint8_t)__popc(qs[e] ^ code[j]);
+                    for (int j = 0; j < TPT; ++j) {
+                        const int off = (j >> 2) * 4 * kScoreThreads + 4 * tid + (j & 3);
+                        if (off < nin) drow[off] = (uint8_t)__popc(qs[e] ^ code[j]);
+                    }
                 }
             }
         }
@@ -169,10 +193,12 @@ __global__ void __launch_bounds__(kScoreThreads) k_score(const ScoreParams p) {
 // ---------------------------------------------------------------- TOPK
 
 template <int TPT>
-__global__ void __launch_bounds__(kScoreThreads) k_select(const SelectParams p) {
+__global__ void __launch_bounds__(kScoreThreads, 3) k_select(const SelectParams p) {
     constexpr int C = kScoreThreads * TPT;
     __shared__ int s_t[kMaxHeadsPerPass];
     __shared__ int s_quota[kMaxHeadsPerPass];
+    __shared__ uint32_t s_tot[kMaxHeadsPerPass][HA_NBINS];
+    __shared__ uint32_t s_pre[kMaxHeadsPerPass][HA_NBINS];
     __shared__ uint32_t s_w1[kWarps][2];
     __shared__ uint32_t s_w2[kWarps][2];
 
@@ -206,13 +232,47 @@ __global__ void __launch_bounds__(kScoreThreads) k_select(const SelectParams p) 
 
     for (int hp = 0; hp < p.G; hp += kMaxHeadsPerPass) {
         const int nh = min(kMaxHeadsPerPass, p.G - hp);
-        // ---- threshold bin t and this chunk's tie quota, one warp per head
+        // ---- threshold bin t and this chunk's tie quota: the histograms of all
+        // chunks (totals) and of the chunks before this one (prefix), per head
+        for (int i = tid; i < kMaxHeadsPerPass * HA_NBINS; i += kScoreThreads) {
+            (&s_tot[0][0])[i] = 0u;
+            (&s_pre[0][0])[i] = 0u;
+        }
+        __syncthreads();
+        {
+            const int per = nch * HA_NBINS;
+            const int total = nh * per;
+            const uint32_t* H0 = p.chunk_hist + (int64_t)(head0 + hp) * p.nchunks * HA_NBINS;
+            constexpr int kBatch = 8;
+            for (int i0 = 0; i0 < total; i0 += kBatch * kScoreThreads) {
+                uint32_t v[kBatch];
+#pragma unroll
+                for (int k2 = 0; k2 < kBatch; ++k2) {
+                    const int i = i0 + k2 * kScoreThreads + tid;
+                    v[k2] = 0u;
+                    if (i < total) {
+                        const int e = i / per;
+                        v[k2] = H0[(int64_t)e * p.nchunks * HA_NBINS + (i - e * per)];
+                    }
+                }
+#pragma unroll
+                for (int k2 = 0; k2 < kBatch; ++k2) {
+                    const int i = i0 + k2 * kScoreThreads + tid;
+                    if (v[k2] != 0u) {
+                        const int e = i / per;
+                        const int rem = i - e * per;
+                        const int cc = rem / HA_NBINS;
+                        const int u = rem - cc * HA_NBINS;
+                        atomicAdd(&s_tot[e][u], v[k2]);
+                        if (cc < c) atomicAdd(&s_pre[e][u], v[k2]);
+                    }
+                }
+            }
+        }
+        __syncthreads();
         if (warp < nh) {
-            const uint32_t* H = p.chunk_hist + (int64_t)(head0 + hp + warp) * p.nchunks * HA_NBINS;
             // bins 0..31 (bin 32 is implied: the cumulative count reaches n there)
-            uint32_t tot = 0;
-            for (int cc = 0; cc < nch; ++cc) tot += H[cc * HA_NBINS + lane];
-            uint32_t incl = tot;
+            uint32_t incl = s_tot[warp][lane];
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
@@ -222,12 +282,9 @@ __global__ void __launch_bounds__(kScoreThreads) k_select(const SelectParams p) 
             const int t = reach ? (__ffs(reach) - 1) : 32;
             const uint32_t below = __shfl_sync(0xffffffffu, incl, (t == 0 ? 0 : t - 1) & 31);
             const int r = k - (t == 0 ? 0 : (int)below);
-            uint32_t tb = 0;
-            for (int cc = lane; cc < c; cc += 32) tb += H[cc * HA_NBINS + t];
-            tb = warp_sum(tb);
             if (lane == 0) {
                 s_t[warp] = t;
-                s_quota[warp] = r - (int)tb;
+                s_quota[warp] = r - (int)s_pre[warp][t];
             }
         }
         __syncthreads();

@@ -194,7 +194,7 @@ def test_select_entry_point_matches_decode():
     sel = torch.empty((2, 8, cap), dtype=torch.int32, device="cuda")
     cnt = torch.empty((2, 8), dtype=torch.int32, device="cuda")
     H.hash_attn_select(shape, w.q_sig, w.k_sig, w.seq_lens, None, 600, 32, 48, sel, cnt, workspace=ws)
-    res = {"sel_idx": sel, "sel_cnt": cnt}
+    res = {"sel_idx": sel, "sel_cnt": cnt, "cap": cap}
     GH.check_selection(res, GH.HostCopy(w), all_heads(w), 600)
     dec = GH.run_decode(w)
     assert torch.equal(dec["sel_idx"], sel) and torch.equal(dec["sel_cnt"], cnt)
