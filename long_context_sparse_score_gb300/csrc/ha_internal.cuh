@@ -17,8 +17,9 @@ constexpr int kScoreThreads = 256;        // SCORE / TOPK block size
 constexpr int kMaxHeadsPerPass = 4;       // query heads of one KV head handled per code pass
 constexpr int kTargetCtas = 2 * 152;      // two CTAs per SM of a GB300 (152 SMs)
 constexpr int kTileRows = 32;             // GATHER-ATT rows per pipeline stage
-constexpr int kGatherThreads = 160;       // 1 producer warp + 4 consumer warps
-constexpr int kMaxSegments = 4096;        // TOPK chunks per head (bounds the prefix table)
+constexpr int kGatherThreads = 128;       // 4 warps, each with its own copy pipeline
+constexpr int kSegPerChunk = kScoreThreads / 32;  // TOPK writes one segment per warp
+constexpr int kMaxSegments = 4096;        // segments per head (bounds GATHER-ATT's prefix table)
 constexpr int64_t kMaxCap = int64_t(1) << 24;  // largest n_cap accepted
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per pipeline wait
 
@@ -27,14 +28,17 @@ constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per pipeline 
 // [0, 256)                 error word (uint32) + padding
 // counters   uint32[heads]  split-K arrival counters of GATHER-ATT (self-resetting)
 // chunk_hist uint32[heads][nchunks][33]  SCORE histogram of every chunk
-// seg_cnt    int32 [heads][nchunks]      selected tokens of every chunk
-// seg_idx    int32 [heads][nchunks*chunk] selected token indices, chunk c's
-//                                          entries at [c*chunk, c*chunk + seg_cnt)
+// seg_cnt    int32 [heads][nseg]         selected tokens of every segment (one
+//                                          per warp sub-chunk of seg_cap tokens)
+// seg_idx    int32 [heads][nseg*seg_cap] selected token indices, segment s's
+//                                          entries at [s*seg_cap, s*seg_cap + seg_cnt)
 // part       float [heads][splits][2 + d] split-K partials (max, sum, o[d])
 struct Layout {
     int heads = 0;
     int chunk = 0;           // tokens per SCORE/TOPK chunk (0: no selection regions)
     int nchunks = 0;
+    int seg_cap = 0;         // tokens per TOPK segment (chunk / kSegPerChunk)
+    int nseg = 0;            // segments per head
     int rows_cap = 0;        // most rows one head attends to
     int splits = 1;          // GATHER-ATT CTAs per head
     int rows_per_split = 0;  // multiple of kTileRows
@@ -82,7 +86,7 @@ struct SelectParams {
 
 struct CompactParams {
     const int32_t* seq_lens;
-    int Hq, n_cap, chunk, nchunks, cap;
+    int Hq, n_cap, seg_cap, nseg, cap;
     const int32_t* seg_cnt;
     const int32_t* seg_idx;
     int32_t* sel_idx;        // [heads][cap]
@@ -112,7 +116,7 @@ struct GatherParams {
     // kSegmented
     const int32_t* seg_cnt;
     const int32_t* seg_idx;
-    int chunk, nchunks;
+    int seg_cap, nseg;
     // kList
     const int32_t* list_idx;
     const int32_t* list_cnt;

@@ -90,6 +90,13 @@ ha_status check_ws(const Layout& lay, void* ws, size_t ws_bytes) {
     return HA_OK;
 }
 
+ha_status check_segments(const Layout& lay) {
+    if (lay.nseg > kMaxSegments)
+        return fail(HA_ERR_UNSUPPORTED, "n_cap too large for this batch: %d selection segments per head (limit %d)",
+                    lay.nseg, kMaxSegments);
+    return HA_OK;
+}
+
 int64_t rows_cap_of(int32_t n_cap, int64_t m, int64_t n_sink, int64_t n_local) {
     const int64_t r = m + n_sink + n_local;
     return r < n_cap ? r : n_cap;
@@ -191,8 +198,8 @@ GatherParams gather_params(const ha_shape* s, const Layout& lay, const Views& v,
     p.G = s->h_q / s->h_kv;
     p.n_cap = s->n_cap;
     p.mode = kIdentity;
-    p.chunk = lay.chunk;
-    p.nchunks = lay.nchunks;
+    p.seg_cap = lay.seg_cap;
+    p.nseg = lay.nseg;
     p.seg_cnt = v.seg_cnt;
     p.seg_idx = v.seg_idx;
     p.splits = lay.splits;
@@ -239,6 +246,7 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
         return fail(HA_ERR_INVALID_ARG, "sel_idx and sel_cnt must both be given or both be NULL");
     const int64_t rows_cap = dense ? s->n_cap : rows_cap_of(s->n_cap, m, n_sink, n_local);
     const Layout lay = make_layout(*s, rows_cap, !dense);
+    HA_TRY(check_segments(lay));
     HA_TRY(check_ws(lay, ws, ws_bytes));
     const Views v = views(lay, ws);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -270,8 +278,8 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
         cp.seq_lens = seq_lens;
         cp.Hq = s->h_q;
         cp.n_cap = s->n_cap;
-        cp.chunk = lay.chunk;
-        cp.nchunks = lay.nchunks;
+        cp.seg_cap = lay.seg_cap;
+        cp.nseg = lay.nseg;
         cp.cap = (int)rows_cap;
         cp.seg_cnt = v.seg_cnt;
         cp.seg_idx = v.seg_idx;
@@ -323,12 +331,14 @@ Layout make_layout(const ha_shape& s, int64_t rows_cap, bool with_selection) {
     if (with_selection) {
         L.chunk = choose_chunk((int64_t)s.batch * s.h_kv, s.n_cap);
         L.nchunks = (int)ceil_div(s.n_cap, L.chunk);
+        L.seg_cap = L.chunk / kSegPerChunk;
+        L.nseg = L.nchunks * kSegPerChunk;
         L.off_hist = off;
         off = align_up(off + (size_t)L.heads * L.nchunks * HA_NBINS * 4, 256);
         L.off_segcnt = off;
-        off = align_up(off + (size_t)L.heads * L.nchunks * 4, 256);
+        off = align_up(off + (size_t)L.heads * L.nseg * 4, 256);
         L.off_seg = off;
-        off = align_up(off + (size_t)L.heads * L.nchunks * L.chunk * 4, 256);
+        off = align_up(off + (size_t)L.heads * L.nseg * L.seg_cap * 4, 256);
     }
     L.off_part = off;
     off = align_up(off + (size_t)L.heads * L.splits * (s.d + 2) * 4, 256);
@@ -352,6 +362,7 @@ ha_status hash_attn_workspace_size(const ha_shape* shape, int32_t m_max, int32_t
     // hash_attn_score work with any budget on the same workspace
     const int64_t rows_cap = dense ? shape->n_cap : rows_cap_of(shape->n_cap, m_max, n_sink, n_local);
     const Layout sparse = make_layout(*shape, rows_cap, true);
+    HA_TRY(check_segments(sparse));
     *bytes = sparse.total;
     return HA_OK;
 }
@@ -397,6 +408,7 @@ ha_status hash_attn_score(const ha_shape* shape, const uint32_t* q_sig, const ui
     if (seq_lens == nullptr) return fail(HA_ERR_INVALID_ARG, "seq_lens is NULL");
     if (dist == nullptr && hist == nullptr) return fail(HA_ERR_INVALID_ARG, "dist and hist are both NULL");
     const Layout lay = make_layout(*shape, 0, true);
+    HA_TRY(check_segments(lay));
     HA_TRY(check_ws(lay, workspace, ws_bytes));
     const Views v = views(lay, workspace);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -429,6 +441,7 @@ ha_status hash_attn_select(const ha_shape* shape, const uint32_t* q_sig, const u
         return fail(HA_ERR_INVALID_ARG, "seq_lens, sel_idx and sel_cnt must not be NULL");
     const int64_t rows_cap = rows_cap_of(shape->n_cap, m, n_sink, n_local);
     const Layout lay = make_layout(*shape, rows_cap, true);
+    HA_TRY(check_segments(lay));
     HA_TRY(check_ws(lay, workspace, ws_bytes));
     const Views v = views(lay, workspace);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -441,8 +454,8 @@ ha_status hash_attn_select(const ha_shape* shape, const uint32_t* q_sig, const u
     cp.seq_lens = seq_lens;
     cp.Hq = shape->h_q;
     cp.n_cap = shape->n_cap;
-    cp.chunk = lay.chunk;
-    cp.nchunks = lay.nchunks;
+    cp.seg_cap = lay.seg_cap;
+    cp.nseg = lay.nseg;
     cp.cap = (int)rows_cap;
     cp.seg_cnt = v.seg_cnt;
     cp.seg_idx = v.seg_idx;

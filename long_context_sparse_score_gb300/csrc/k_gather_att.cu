@@ -9,16 +9,18 @@
 // with o, and partial results over disjoint token sets merge exactly.
 //
 // k_gather_att: one CTA per (query head, split of I). The CTA first turns its
-// range of list positions into token indices in shared memory. Warp 0 is the
-// producer: per 32-row stage it copies each selected K row and V row straight
-// from the cache with 16-byte asynchronous copies (one warp instruction moves a
-// 256-byte K row and its 256-byte V row), and an mbarrier per stage completes
-// when they have landed. Warps 1-4 consume: 8 rows per warp per stage, 4 lanes
-// per row.
-// Scores are fp32 (q pre-scaled by log2(e)/sqrt(d), packed fp32x2 FMAs), the
-// softmax is online in base 2, and P.V accumulates per lane over its rows.
-// Splits write (max, sum, o) partials; the last CTA of a head to finish merges
-// them (no waiting: an arrival counter decides who is last).
+// range of list positions into token indices in shared memory. Then each warp
+// runs its own pipeline over 8-row tiles (tiles w, w + W, w + 2W, ... of the
+// CTA): it copies the K and V rows of a tile straight from the cache with
+// 16-byte asynchronous copies (one warp instruction moves a 256-byte K row and
+// its 256-byte V row) into a private ring of P shared-memory stages, keeping
+// P - 1 tiles in flight while it computes the oldest one. Waits are on the
+// warp's own copy groups only: no barrier couples warps until the final combine.
+// In a tile, 4 lanes share a row: scores are fp32 (q pre-scaled by
+// log2(e)/sqrt(d), packed fp32x2 FMAs), the softmax is online in base 2 and P.V
+// accumulates per lane over its rows. Splits write (max, sum, o) partials; the
+// last CTA of a head to finish merges them (an arrival counter decides who is
+// last; nothing waits).
 #include "ha_internal.cuh"
 
 #include <math_constants.h>
@@ -26,23 +28,24 @@
 namespace ha {
 namespace {
 
+constexpr int kWarpsG = kGatherThreads / 32;
+
 template <int D, typename KT>
 struct Cfg {
     static constexpr int ES = sizeof(KT);
     static constexpr int RB = D * ES;                 // bytes of one K or V row
     static constexpr int PITCH = RB + 16;             // shared row pitch: rows land on distinct banks
-    static constexpr int STAGES = RB <= 256 ? 4 : 2;
+    static constexpr int R = 8;                       // rows per warp tile
+    static constexpr int P = 2;                       // stages per warp (more warps beat deeper rings)
     static constexpr int NCH = RB / 16;               // 16-byte chunks per row
     static constexpr int CPL = NCH / 4;               // chunks per lane (4 lanes per row)
     static constexpr int EPC = 16 / ES;               // elements per chunk
     static constexpr int DPL = CPL * EPC;             // dims per lane (= D / 4)
-    static constexpr int STAGE_BYTES = 2 * kTileRows * PITCH;
-    static constexpr int DATA_BYTES = STAGES * STAGE_BYTES;
-    // shared layout after the stage ring
-    static constexpr int OFF_TOK = DATA_BYTES;                            // int [STAGES][32]
-    static constexpr int OFF_BAR = OFF_TOK + STAGES * kTileRows * 4;      // u64 full[S], empty[S]
-    static constexpr int OFF_CMB = OFF_BAR + 2 * STAGES * 8;              // float wm[4], wl[4], wo[4][D]
-    static constexpr int OFF_TOKL = OFF_CMB + (8 + 4 * D) * 4;            // int tokl[rows_per_split]
+    static constexpr int STAGE_BYTES = 2 * R * PITCH; // K rows, then V rows
+    static constexpr int WARP_BYTES = P * STAGE_BYTES;
+    static constexpr int DATA_BYTES = kWarpsG * WARP_BYTES;
+    static constexpr int OFF_CMB = DATA_BYTES;                            // float wm[W], wl[W], wo[W][D]
+    static constexpr int OFF_TOKL = OFF_CMB + (2 * kWarpsG + kWarpsG * D) * 4;  // int tokl[rows_per_split]
 };
 
 template <typename KT>
@@ -70,19 +73,42 @@ __device__ __forceinline__ float load_q(const void* q, int64_t off, int bf16) {
     return reinterpret_cast<const float*>(q)[off];
 }
 
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Token of list position pp (kSegmented: the prefix table `pre` of the head's
+// segments; kList: the caller's list, checked against [0, n)).
+__device__ __forceinline__ int token_at(const GatherParams& p, int pp, int n, const int* pre, int nused,
+                                        const int32_t* seg, const int32_t* lst) {
+    if (p.mode == kIdentity) return pp;
+    if (p.mode == kSegmented) {
+        int lo = 0, hi = nused - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (pre[mid] <= pp) lo = mid; else hi = mid - 1;
+        }
+        return seg[(int64_t)lo * p.seg_cap + (pp - pre[lo])];
+    }
+    const int tok = lst[pp];
+    if (tok < 0 || tok >= n) {
+        flag_error(p.err, HA_DEVERR_INDEX);
+        return -1;
+    }
+    return tok;
+}
+
 template <int D, typename KT>
-__global__ void __launch_bounds__(kGatherThreads) k_gather_att(const GatherParams p) {
+__global__ void __launch_bounds__(kGatherThreads, 3) k_gather_att(const GatherParams p) {
     using C = Cfg<D, KT>;
     extern __shared__ __align__(128) unsigned char smem[];
-    int* rowtok = reinterpret_cast<int*>(smem + C::OFF_TOK);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     float* wm = reinterpret_cast<float*>(smem + C::OFF_CMB);
-    float* wl = wm + 4;
-    float* wo = wm + 8;
+    float* wl = wm + kWarpsG;
+    float* wo = wl + kWarpsG;
     int* tokl = reinterpret_cast<int*>(smem + C::OFF_TOKL);
-    int* pre = tokl + p.rows_per_split;   // [nchunks + 1] (segmented lists only)
-    __shared__ int s_L, s_issued, s_last;
-    __shared__ volatile int s_abort;
+    int* pre = tokl + p.rows_per_split;   // [nseg + 1] (segmented lists only)
+    __shared__ int s_L, s_last;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int lin = blockIdx.x;
@@ -95,8 +121,9 @@ __global__ void __launch_bounds__(kGatherThreads) k_gather_att(const GatherParam
     const int head = b * p.Hq + g * p.G + hh;
     const bool report = (p.mode != kSegmented) && split == 0 && hh == 0 && g == 0 && tid == 0;
     const int n = checked_len(p.seq_lens, b, p.n_cap, p.err, report);
+    const int nused = (p.mode == kSegmented) ? (n + p.seg_cap - 1) / p.seg_cap : 0;
 
-    // ---- setup: list length (and segment prefix table) by warp 0; barriers
+    // ---- list length (and the segment prefix table), warp 0
     if (warp == 0) {
         int L = 0;
         if (p.mode == kIdentity) {
@@ -108,275 +135,219 @@ __global__ void __launch_bounds__(kGatherThreads) k_gather_att(const GatherParam
                 L = min(max(L, 0), p.list_cap);
             }
         } else {
-            const int nch = (n + p.chunk - 1) / p.chunk;
-            const int32_t* cnt = p.seg_cnt + (int64_t)head * p.nchunks;
+            const int32_t* cnt = p.seg_cnt + (int64_t)head * p.nseg;
             int carry = 0;
             if (lane == 0) pre[0] = 0;
-            for (int base = 0; base < nch; base += 32) {
+            for (int base = 0; base < nused; base += 32) {
                 const int cc = base + lane;
-                int v = (cc < nch) ? cnt[cc] : 0;
+                int v = (cc < nused) ? cnt[cc] : 0;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
                     const int y = __shfl_up_sync(0xffffffffu, v, o);
                     if (lane >= o) v += y;
                 }
-                if (cc < nch) pre[cc + 1] = carry + v;
+                if (cc < nused) pre[cc + 1] = carry + v;
                 carry += __shfl_sync(0xffffffffu, v, 31);
             }
             L = carry;
         }
-        if (lane == 0) {
-            s_L = L;
-            s_abort = 0;
-            s_issued = 0;
-            for (int s = 0; s < C::STAGES; ++s) {
-                mbar_init(smem_addr(&bars[s]), 1);               // producer lane 0 (+ copy tracking)
-                mbar_init(smem_addr(&bars[C::STAGES + s]), 4);   // one arrival per consumer warp
-            }
-            mbar_fence_init();
-        }
+        if (lane == 0) s_L = L;
     }
     __syncthreads();
 
     const int L = s_L;
     const int r0 = split * p.rows_per_split;
-    const int r1 = min(L, r0 + p.rows_per_split);
-    const int nrows = max(0, r1 - r0);
-    const int ntiles = (nrows + kTileRows - 1) / kTileRows;
+    const int nrows = max(0, min(L, r0 + p.rows_per_split) - r0);
 
-    // ---- this CTA's token indices, list positions [r0, r1), into shared memory
+    // ---- this CTA's token indices (list positions [r0, r0 + nrows)) into shared memory
     {
-        const int nch = (p.mode == kSegmented) ? (n + p.chunk - 1) / p.chunk : 0;
-        const int32_t* seg = (p.mode == kSegmented) ? p.seg_idx + (int64_t)head * p.nchunks * p.chunk
-                                                    : nullptr;
+        const int32_t* seg = (p.mode == kSegmented) ? p.seg_idx + (int64_t)head * p.nseg * p.seg_cap : nullptr;
         const int32_t* lst = (p.mode == kList) ? p.list_idx + (int64_t)head * p.list_cap : nullptr;
-        for (int i = tid; i < nrows; i += kGatherThreads) {
-            const int pp = r0 + i;
-            int tok;
-            if (p.mode == kIdentity) {
-                tok = pp;
-            } else if (p.mode == kSegmented) {
-                int lo = 0, hi = nch - 1;
-                while (lo < hi) {
-                    const int mid = (lo + hi + 1) >> 1;
-                    if (pre[mid] <= pp) lo = mid; else hi = mid - 1;
-                }
-                tok = seg[(int64_t)lo * p.chunk + (pp - pre[lo])];
-            } else {
-                tok = lst[pp];
-                if (tok < 0 || tok >= n) {
-                    flag_error(p.err, HA_DEVERR_INDEX);
-                    tok = -1;
-                }
+        constexpr int kB = 4;
+        for (int i0 = 0; i0 < nrows; i0 += kB * kGatherThreads) {
+            int tk[kB];
+#pragma unroll
+            for (int u = 0; u < kB; ++u) {
+                const int i = i0 + u * kGatherThreads + tid;
+                tk[u] = (i < nrows) ? token_at(p, r0 + i, n, pre, nused, seg, lst) : -1;
             }
-            tokl[i] = tok;
+#pragma unroll
+            for (int u = 0; u < kB; ++u) {
+                const int i = i0 + u * kGatherThreads + tid;
+                if (i < nrows) tokl[i] = tk[u];
+            }
         }
     }
     __syncthreads();
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        const char* Kb = p.K + ((int64_t)b * p.k_sb + (int64_t)g * p.k_sh) * C::ES;
-        const char* Vb = p.V + ((int64_t)b * p.v_sb + (int64_t)g * p.v_sh) * C::ES;
-        const int64_t kstep = p.k_sn * C::ES, vstep = p.v_sn * C::ES;
-        int issued = 0;
-        for (int t = 0; t < ntiles; ++t) {
-            const int s = t % C::STAGES;
-            if (t >= C::STAGES) {
-                bool ok = true;
-                if (lane == 0) ok = mbar_wait_bounded(smem_addr(&bars[C::STAGES + s]),
-                                                      ((t / C::STAGES) - 1) & 1, &s_abort);
-                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-                if (!ok) {
-                    if (lane == 0) {
-                        flag_error(p.err, HA_DEVERR_TIMEOUT);
-                        s_abort = 1;
-                    }
-                    break;
-                }
-            }
-            const int row0 = t * kTileRows;
-            const int tok = (row0 + lane < nrows) ? tokl[row0 + lane] : -1;
-            int* rt = rowtok + s * kTileRows;
-            rt[lane] = tok;
-            __syncwarp();
-            unsigned char* stage = smem + s * C::STAGE_BYTES;
-            // (row, K or V, 16-byte chunk) triples of the stage, 32 per warp instruction
-#pragma unroll 4
-            for (int it = lane; it < kTileRows * 2 * C::NCH; it += 32) {
-                const int row = it / (2 * C::NCH);
-                const int rem = it - row * (2 * C::NCH);
-                const int isv = rem >= C::NCH ? 1 : 0;
-                const int ch = rem - isv * C::NCH;
-                const int tr = rt[row];
+    // ---- per-warp pipeline over 8-row tiles
+    const char* Kb = p.K + ((int64_t)b * p.k_sb + (int64_t)g * p.k_sh) * C::ES;
+    const char* Vb = p.V + ((int64_t)b * p.v_sb + (int64_t)g * p.v_sh) * C::ES;
+    const int64_t kstep = p.k_sn * C::ES, vstep = p.v_sn * C::ES;
+    unsigned char* wbuf = smem + warp * C::WARP_BYTES;
+    const int ntiles = (nrows + C::R - 1) / C::R;
+    const int ntw = (ntiles > warp) ? (ntiles - warp + kWarpsG - 1) / kWarpsG : 0;
+
+    auto issue = [&](int k) {
+        const int row0 = (warp + k * kWarpsG) * C::R;
+        unsigned char* st = wbuf + (k % C::P) * C::STAGE_BYTES;
+#pragma unroll
+        for (int it = lane; it < C::R * 2 * C::NCH; it += 32) {
+            const int row = it / (2 * C::NCH);
+            const int rem = it - row * (2 * C::NCH);
+            const int isv = rem >= C::NCH ? 1 : 0;
+            const int ch = rem - isv * C::NCH;
+            const int rr = row0 + row;
+            if (rr < nrows) {
+                const int tr = tokl[rr];
                 if (tr >= 0) {
                     const char* src = (isv ? Vb + (int64_t)tr * vstep : Kb + (int64_t)tr * kstep) + ch * 16;
-                    cp_async16(smem_addr(stage + (isv * kTileRows + row) * C::PITCH + ch * 16), src);
+                    cp_async16(smem_addr(st + (isv * C::R + row) * C::PITCH + ch * 16), src);
                 }
             }
-            const uint32_t full = smem_addr(&bars[s]);
-            cp_async_arrive(full);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(full);
-            issued = t + 1;
         }
-        if (lane == 0) s_issued = issued;
-    } else {
-        // ------------------------------------------------------------ consumers
-        const int cw = warp - 1;
-        const int r = lane & 7, qt = lane >> 3;
-        float qv[C::DPL];
-        {
-            const int64_t qoff = (int64_t)b * p.q_sb + (int64_t)(g * p.G + hh) * p.q_sh;
+    };
+
+    const int r = lane & 7, qt = lane >> 3;
+    float qv[C::DPL];
+    {
+        const int64_t qoff = (int64_t)b * p.q_sb + (int64_t)(g * p.G + hh) * p.q_sh;
+#pragma unroll
+        for (int jc = 0; jc < C::CPL; ++jc) {
+            const int dim0 = (jc * 4 + qt) * C::EPC;
+#pragma unroll
+            for (int e = 0; e < C::EPC; ++e)
+                qv[jc * C::EPC + e] = load_q(p.q, qoff + dim0 + e, p.q_bf16) * p.qscale;
+        }
+    }
+    float2 ov[C::DPL / 2];
+#pragma unroll
+    for (int i = 0; i < C::DPL / 2; ++i) ov[i] = make_float2(0.f, 0.f);
+    float mrun = -CUDART_INF_F, lrun = 0.f;
+
+#pragma unroll
+    for (int k = 0; k < C::P - 1; ++k) {
+        if (k < ntw) issue(k);
+        cp_async_commit();
+    }
+    for (int k = 0; k < ntw; ++k) {
+        if (k + C::P - 1 < ntw) issue(k + C::P - 1);
+        cp_async_commit();
+        cp_async_wait<C::P - 1>();
+        __syncwarp();
+        const int rr = (warp + k * kWarpsG) * C::R + r;
+        const int tok = (rr < nrows) ? tokl[rr] : -1;
+        const unsigned char* kr = wbuf + (k % C::P) * C::STAGE_BYTES + r * C::PITCH;
+        const unsigned char* vr = kr + C::R * C::PITCH;
+
+        float part = 0.f;
+        if (tok >= 0) {
+            float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int jc = 0; jc < C::CPL; ++jc) {
-                const int dim0 = (jc * 4 + qt) * C::EPC;
+                const uint4 w = *reinterpret_cast<const uint4*>(kr + (jc * 4 + qt) * 16);
+                float f[C::EPC];
+                chunk_to_float<KT>(w, f);
 #pragma unroll
-                for (int e = 0; e < C::EPC; ++e)
-                    qv[jc * C::EPC + e] = load_q(p.q, qoff + dim0 + e, p.q_bf16) * p.qscale;
-            }
-        }
-        float2 ov[C::DPL / 2];
-#pragma unroll
-        for (int i = 0; i < C::DPL / 2; ++i) ov[i] = make_float2(0.f, 0.f);
-        float mrun = -CUDART_INF_F, lrun = 0.f;
-
-        for (int t = 0; t < ntiles; ++t) {
-            const int s = t % C::STAGES;
-            const bool ok = mbar_wait_bounded(smem_addr(&bars[s]), (t / C::STAGES) & 1, &s_abort);
-            if (!__all_sync(0xffffffffu, ok)) {
-                if (lane == 0) {
-                    flag_error(p.err, HA_DEVERR_TIMEOUT);
-                    s_abort = 1;
+                for (int e = 0; e < C::EPC; e += 4) {
+                    a0 = __ffma2_rn(make_float2(qv[jc * C::EPC + e], qv[jc * C::EPC + e + 1]),
+                                    make_float2(f[e], f[e + 1]), a0);
+                    a1 = __ffma2_rn(make_float2(qv[jc * C::EPC + e + 2], qv[jc * C::EPC + e + 3]),
+                                    make_float2(f[e + 2], f[e + 3]), a1);
                 }
-                break;
             }
-            const int row = cw * 8 + r;
-            const int tok = rowtok[s * kTileRows + row];
-            const unsigned char* kr = smem + s * C::STAGE_BYTES + row * C::PITCH;
-            const unsigned char* vr = kr + kTileRows * C::PITCH;
-
-            float part = 0.f;
+            part = (a0.x + a0.y) + (a1.x + a1.y);
+        }
+        part += __shfl_xor_sync(0xffffffffu, part, 8);
+        part += __shfl_xor_sync(0xffffffffu, part, 16);
+        const float sc = (tok >= 0) ? part : -CUDART_INF_F;
+        float mx = sc;
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        const float mnew = fmaxf(mrun, mx);
+        if (mnew != -CUDART_INF_F) {
+            if (mnew > mrun) {
+                const float alpha = exp2f(mrun - mnew);
+                lrun *= alpha;
+#pragma unroll
+                for (int i = 0; i < C::DPL / 2; ++i) ov[i] = __fmul2_rn(ov[i], make_float2(alpha, alpha));
+                mrun = mnew;
+            }
+            const float pr = exp2f(sc - mnew);
+            float ps = pr;
+            ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+            ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+            ps += __shfl_xor_sync(0xffffffffu, ps, 4);
+            lrun += ps;
             if (tok >= 0) {
-                float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+                const float2 pp2 = make_float2(pr, pr);
 #pragma unroll
                 for (int jc = 0; jc < C::CPL; ++jc) {
-                    const uint4 w = *reinterpret_cast<const uint4*>(kr + (jc * 4 + qt) * 16);
+                    const uint4 w = *reinterpret_cast<const uint4*>(vr + (jc * 4 + qt) * 16);
                     float f[C::EPC];
                     chunk_to_float<KT>(w, f);
 #pragma unroll
-                    for (int e = 0; e < C::EPC; e += 4) {
-                        a0 = __ffma2_rn(make_float2(qv[jc * C::EPC + e], qv[jc * C::EPC + e + 1]),
-                                        make_float2(f[e], f[e + 1]), a0);
-                        a1 = __ffma2_rn(make_float2(qv[jc * C::EPC + e + 2], qv[jc * C::EPC + e + 3]),
-                                        make_float2(f[e + 2], f[e + 3]), a1);
-                    }
-                }
-                part = (a0.x + a0.y) + (a1.x + a1.y);
-            }
-            part += __shfl_xor_sync(0xffffffffu, part, 8);
-            part += __shfl_xor_sync(0xffffffffu, part, 16);
-            const float sc = (tok >= 0) ? part : -CUDART_INF_F;
-            float mx = sc;
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-            const float mnew = fmaxf(mrun, mx);
-            if (mnew != -CUDART_INF_F) {
-                if (mnew > mrun) {
-                    const float alpha = exp2f(mrun - mnew);
-                    lrun *= alpha;
-#pragma unroll
-                    for (int i = 0; i < C::DPL / 2; ++i) ov[i] = __fmul2_rn(ov[i], make_float2(alpha, alpha));
-                    mrun = mnew;
-                }
-                const float pr = exp2f(sc - mnew);
-                float ps = pr;
-                ps += __shfl_xor_sync(0xffffffffu, ps, 1);
-                ps += __shfl_xor_sync(0xffffffffu, ps, 2);
-                ps += __shfl_xor_sync(0xffffffffu, ps, 4);
-                lrun += ps;
-                if (tok >= 0) {
-                    const float2 pp2 = make_float2(pr, pr);
-#pragma unroll
-                    for (int jc = 0; jc < C::CPL; ++jc) {
-                        const uint4 w = *reinterpret_cast<const uint4*>(vr + (jc * 4 + qt) * 16);
-                        float f[C::EPC];
-                        chunk_to_float<KT>(w, f);
-#pragma unroll
-                        for (int e = 0; e < C::EPC; e += 2)
-                            ov[(jc * C::EPC + e) / 2] = __ffma2_rn(pp2, make_float2(f[e], f[e + 1]),
-                                                                   ov[(jc * C::EPC + e) / 2]);
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&bars[C::STAGES + s]));
-        }
-        // reduce the 8 row-lanes of each dim group; lanes r == 0 hold the sums
-#pragma unroll
-        for (int i = 0; i < C::DPL / 2; ++i) {
-#pragma unroll
-            for (int o = 1; o < 8; o <<= 1) {
-                ov[i].x += __shfl_xor_sync(0xffffffffu, ov[i].x, o);
-                ov[i].y += __shfl_xor_sync(0xffffffffu, ov[i].y, o);
-            }
-        }
-        if (r == 0) {
-#pragma unroll
-            for (int jc = 0; jc < C::CPL; ++jc) {
-                const int dim0 = (jc * 4 + qt) * C::EPC;
-#pragma unroll
-                for (int e = 0; e < C::EPC; e += 2) {
-                    wo[cw * D + dim0 + e] = ov[(jc * C::EPC + e) / 2].x;
-                    wo[cw * D + dim0 + e + 1] = ov[(jc * C::EPC + e) / 2].y;
+                    for (int e = 0; e < C::EPC; e += 2)
+                        ov[(jc * C::EPC + e) / 2] =
+                            __ffma2_rn(pp2, make_float2(f[e], f[e + 1]), ov[(jc * C::EPC + e) / 2]);
                 }
             }
         }
-        if (lane == 0) {
-            wm[cw] = mrun;
-            wl[cw] = lrun;
+        __syncwarp();
+    }
+    cp_async_wait<0>();
+
+    // ---- per warp: reduce the 8 row-lanes of each dim group (lanes r == 0 hold the sums)
+#pragma unroll
+    for (int i = 0; i < C::DPL / 2; ++i) {
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            ov[i].x += __shfl_xor_sync(0xffffffffu, ov[i].x, o);
+            ov[i].y += __shfl_xor_sync(0xffffffffu, ov[i].y, o);
         }
+    }
+    if (r == 0) {
+#pragma unroll
+        for (int jc = 0; jc < C::CPL; ++jc) {
+            const int dim0 = (jc * 4 + qt) * C::EPC;
+#pragma unroll
+            for (int e = 0; e < C::EPC; e += 2) {
+                wo[warp * D + dim0 + e] = ov[(jc * C::EPC + e) / 2].x;
+                wo[warp * D + dim0 + e + 1] = ov[(jc * C::EPC + e) / 2].y;
+            }
+        }
+    }
+    if (lane == 0) {
+        wm[warp] = mrun;
+        wl[warp] = lrun;
     }
     __syncthreads();
 
-    // ---- after a timeout: wait (bounded) for copies still in flight before exit
-    if (s_abort && tid == 0) {
-        const int issued = s_issued;
-        const int zero = 0;
-        for (int s = 0; s < C::STAGES; ++s) {
-            int last = -1;
-            for (int t = s; t < issued; t += C::STAGES) last = t;
-            if (last >= 0)
-                (void)mbar_wait_bounded(smem_addr(&bars[s]), (last / C::STAGES) & 1,
-                                        reinterpret_cast<const volatile int*>(&zero));
-        }
-    }
-
-    // ---- combine the 4 consumer warps: (M, Lsum, O[d]) in base-2 units
+    // ---- combine the warps: (M, Lsum, O[d]) in base-2 units
     constexpr float kLn2 = 0.69314718055994530942f;
-    if (tid < D) {
+    for (int dd = tid; dd < D; dd += kGatherThreads) {
         float M = -CUDART_INF_F;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) M = fmaxf(M, wm[w]);
+        for (int w = 0; w < kWarpsG; ++w) M = fmaxf(M, wm[w]);
         float Ls = 0.f, O = 0.f;
         if (M != -CUDART_INF_F) {
 #pragma unroll
-            for (int w = 0; w < 4; ++w) {
+            for (int w = 0; w < kWarpsG; ++w) {
                 if (wm[w] != -CUDART_INF_F) {
-                    const float sc = exp2f(wm[w] - M);
-                    Ls += wl[w] * sc;
-                    O += wo[w * D + tid] * sc;
+                    const float s = exp2f(wm[w] - M);
+                    Ls += wl[w] * s;
+                    O += wo[w * D + dd] * s;
                 }
             }
         }
         if (p.splits == 1) {
-            p.out[(int64_t)head * D + tid] = (Ls > 0.f) ? O / Ls : 0.f;
-            if (tid == 0) p.lse[head] = (Ls > 0.f) ? (M + log2f(Ls)) * kLn2 : -CUDART_INF_F;
+            p.out[(int64_t)head * D + dd] = (Ls > 0.f) ? O / Ls : 0.f;
+            if (dd == 0) p.lse[head] = (Ls > 0.f) ? (M + log2f(Ls)) * kLn2 : -CUDART_INF_F;
         } else {
             float* pt = p.part + ((int64_t)head * p.splits + split) * (D + 2);
-            pt[2 + tid] = O;
-            if (tid == 0) {
+            pt[2 + dd] = O;
+            if (dd == 0) {
                 pt[0] = M;
                 pt[1] = Ls;
             }
@@ -394,7 +365,7 @@ __global__ void __launch_bounds__(kGatherThreads) k_gather_att(const GatherParam
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    if (tid < D) {
+    for (int dd = tid; dd < D; dd += kGatherThreads) {
         const float* pt = p.part + (int64_t)head * p.splits * (D + 2);
         float M = -CUDART_INF_F;
         for (int s = 0; s < p.splits; ++s) M = fmaxf(M, __ldcg(pt + (int64_t)s * (D + 2)));
@@ -405,12 +376,12 @@ __global__ void __launch_bounds__(kGatherThreads) k_gather_att(const GatherParam
                 if (ms != -CUDART_INF_F) {
                     const float sc = exp2f(ms - M);
                     Ls += __ldcg(pt + (int64_t)s * (D + 2) + 1) * sc;
-                    O += __ldcg(pt + (int64_t)s * (D + 2) + 2 + tid) * sc;
+                    O += __ldcg(pt + (int64_t)s * (D + 2) + 2 + dd) * sc;
                 }
             }
         }
-        p.out[(int64_t)head * D + tid] = (Ls > 0.f) ? O / Ls : 0.f;
-        if (tid == 0) p.lse[head] = (Ls > 0.f) ? (M + log2f(Ls)) * kLn2 : -CUDART_INF_F;
+        p.out[(int64_t)head * D + dd] = (Ls > 0.f) ? O / Ls : 0.f;
+        if (dd == 0) p.lse[head] = (Ls > 0.f) ? (M + log2f(Ls)) * kLn2 : -CUDART_INF_F;
     }
     if (tid == 0) p.counters[head] = 0u;
 }
@@ -439,7 +410,7 @@ __global__ void __launch_bounds__(256) k_merge(const MergeParams p) {
 template <int D, typename KT>
 cudaError_t launch_gather_t(const GatherParams& p, cudaStream_t st) {
     using C = Cfg<D, KT>;
-    const size_t smem = (size_t)C::OFF_TOKL + (size_t)(p.rows_per_split + p.nchunks + 1) * sizeof(int);
+    const size_t smem = (size_t)C::OFF_TOKL + (size_t)(p.rows_per_split + p.nseg + 1) * sizeof(int);
     cudaError_t e = cudaFuncSetAttribute(k_gather_att<D, KT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;

@@ -5,15 +5,23 @@
 // the query code; Sec. 4 keeps the m best tokens, Sec. 4.4 adds the first
 // n_sink and the most recent n_local tokens.
 //
-// Work decomposition: a CTA owns one chunk of `chunk` consecutive tokens of one
-// (batch entry, KV head) and serves every query head of that KV head from a
-// single read of the chunk's codes (the GQA sharing of Nectar Sec. 3).
-//   k_score   per-chunk 33-bin distance histograms (and, for the SCORE entry
+// Work decomposition. A CTA owns one chunk of kScoreThreads * TPT consecutive
+// tokens of one (batch entry, KV head) and serves every query head of that KV
+// head from one read of the chunk's codes (the GQA sharing of Nectar Sec. 3).
+// Inside the chunk, warp w owns the sub-chunk of 32 * TPT consecutive tokens
+// starting at w * 32 * TPT; in round r its lane l holds the 4 tokens
+// 128 r + 4 l + {0..3} of the sub-chunk (one 16-byte load; 512 contiguous bytes
+// per warp load).
+//   k_score   33-bin distance histogram of every chunk (and, for the SCORE entry
 //             point, the distances themselves)
-//   k_select  threshold bin t and tie quota r per head from the chunk
-//             histograms; then, with two block-wide prefix sums in token order,
-//             the deterministic selection (distance, then index) joined with
-//             the windows, written as one ascending segment per chunk
+//   k_select  per head: the threshold bin t (smallest t whose cumulative count
+//             reaches min(m, n)) and the chunk's tie quota from the chunk
+//             histograms; then each warp selects its sub-chunk in token order
+//             with ballots and writes it as one ascending segment. Only the one
+//             chunk per head where the quota of tied tokens runs out needs the
+//             per-warp tie ranks; elsewhere a token is selected iff its distance
+//             is at most t (quota left) or below t (quota spent), or it lies in
+//             a window.
 //   k_compact gathers the segments into the caller's [heads, cap] list
 //   k_hist    sums the chunk histograms (SCORE entry point)
 #include "ha_internal.cuh"
@@ -23,43 +31,23 @@ namespace {
 
 constexpr int kWarps = kScoreThreads / 32;
 
+// Codes of this thread (see the decomposition above); tokens at or beyond n read 0.
 template <int TPT>
-__device__ __forceinline__ void load_codes(const uint32_t* __restrict__ row, int i0, int n,
+__device__ __forceinline__ void load_codes(const uint32_t* __restrict__ row, int sbase, int n,
                                            uint32_t (&c)[TPT]) {
-    if (i0 + TPT <= n) {
-        const uint4* p = reinterpret_cast<const uint4*>(row + i0);
+    const int lane = threadIdx.x & 31;
 #pragma unroll
-        for (int j = 0; j < TPT / 4; ++j) {
-            const uint4 v = __ldg(p + j);
-            c[4 * j + 0] = v.x;
-            c[4 * j + 1] = v.y;
-            c[4 * j + 2] = v.z;
-            c[4 * j + 3] = v.w;
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < TPT; ++j) c[j] = (i0 + j < n) ? __ldg(row + i0 + j) : 0u;
-    }
-}
-
-// Codes of this thread in SCORE: groups of 4 consecutive tokens, the warp's 32
-// lanes reading 512 contiguous bytes per load; token of slot j is
-// c0 + (j / 4) * (4 * kScoreThreads) + 4 * threadIdx.x + j % 4.
-template <int TPT>
-__device__ __forceinline__ void load_codes_coalesced(const uint32_t* __restrict__ row, int c0, int n,
-                                                     uint32_t (&c)[TPT]) {
-#pragma unroll
-    for (int j = 0; j < TPT / 4; ++j) {
-        const int i = c0 + j * 4 * kScoreThreads + 4 * threadIdx.x;
+    for (int r = 0; r < TPT / 4; ++r) {
+        const int i = sbase + 128 * r + 4 * lane;
         if (i + 4 <= n) {
             const uint4 v = __ldg(reinterpret_cast<const uint4*>(row + i));
-            c[4 * j + 0] = v.x;
-            c[4 * j + 1] = v.y;
-            c[4 * j + 2] = v.z;
-            c[4 * j + 3] = v.w;
+            c[4 * r + 0] = v.x;
+            c[4 * r + 1] = v.y;
+            c[4 * r + 2] = v.z;
+            c[4 * r + 3] = v.w;
         } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) c[4 * j + e] = (i + e < n) ? __ldg(row + i + e) : 0u;
+            for (int e = 0; e < 4; ++e) c[4 * r + e] = (i + e < n) ? __ldg(row + i + e) : 0u;
         }
     }
 }
@@ -70,42 +58,8 @@ __device__ __forceinline__ uint32_t warp_sum(uint32_t v) {
     return v;
 }
 
-// Block-wide exclusive prefix sum of two packed words (16-bit fields each; every
-// field total stays below 2^16). `wsum` is [kWarps][2] shared scratch used by
-// this scan only.
-__device__ __forceinline__ void block_scan2(uint32_t a, uint32_t b, uint32_t& ex_a, uint32_t& ex_b,
-                                            uint32_t& tot_a, uint32_t& tot_b, uint32_t (*wsum)[2]) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint32_t ia = a, ib = b;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t ya = __shfl_up_sync(0xffffffffu, ia, o);
-        const uint32_t yb = __shfl_up_sync(0xffffffffu, ib, o);
-        if (lane >= o) {
-            ia += ya;
-            ib += yb;
-        }
-    }
-    if (lane == 31) {
-        wsum[warp][0] = ia;
-        wsum[warp][1] = ib;
-    }
-    __syncthreads();
-    uint32_t pa = 0, pb = 0, sa = 0, sb = 0;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-        const uint32_t va = wsum[w][0], vb = wsum[w][1];
-        if (w < warp) {
-            pa += va;
-            pb += vb;
-        }
-        sa += va;
-        sb += vb;
-    }
-    ex_a = pa + ia - a;
-    ex_b = pb + ib - b;
-    tot_a = sa;
-    tot_b = sb;
+__device__ __forceinline__ void red_shared_add(uint32_t addr, uint32_t v) {
+    asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ uint32_t field(uint32_t w01, uint32_t w23, int e) {
@@ -113,12 +67,15 @@ __device__ __forceinline__ uint32_t field(uint32_t w01, uint32_t w23, int e) {
     return (e & 1) ? (w >> 16) : (w & 0xffffu);
 }
 
+__device__ __forceinline__ int popc_lt(unsigned m, unsigned lt) { return __popc(m & lt); }
+
 // ---------------------------------------------------------------- SCORE
 
 template <int TPT>
 __global__ void __launch_bounds__(kScoreThreads, 3) k_score(const ScoreParams p) {
     constexpr int C = kScoreThreads * TPT;
-    // Per-thread histogram columns: hist[bin][thread], the counts of up to four
+    constexpr int SC = 32 * TPT;
+    // Per-thread histogram columns hist[bin][thread]: the counts of up to four
     // heads packed one byte each (a thread sees at most TPT <= 32 tokens).
     __shared__ uint32_t hist[HA_NBINS][kScoreThreads];
 
@@ -134,9 +91,10 @@ __global__ void __launch_bounds__(kScoreThreads, 3) k_score(const ScoreParams p)
     if (c0 >= n) return;
 
     const uint32_t* row = p.k_sig + (int64_t)b * p.ks_sb + (int64_t)g * p.ks_sh;
+    const int sbase = c0 + warp * SC;
     uint32_t code[TPT];
-    load_codes_coalesced<TPT>(row, c0, n, code);
-    const int nin = n - c0;  // tokens of this chunk are valid below this offset
+    load_codes<TPT>(row, sbase, n, code);
+    const uint32_t col = smem_addr(&hist[0][tid]);
 
     for (int hp = 0; hp < p.G; hp += kMaxHeadsPerPass) {
         const int nh = min(kMaxHeadsPerPass, p.G - hp);
@@ -147,13 +105,13 @@ __global__ void __launch_bounds__(kScoreThreads, 3) k_score(const ScoreParams p)
         for (int u = 0; u < HA_NBINS; ++u) hist[u][tid] = 0u;
 #pragma unroll
         for (int j = 0; j < TPT; ++j) {
-            const int off = (j >> 2) * 4 * kScoreThreads + 4 * tid + (j & 3);
-            if (off < nin) {
+            const int i = sbase + 128 * (j >> 2) + 4 * lane + (j & 3);
+            if (i < n) {
 #pragma unroll
                 for (int e = 0; e < kMaxHeadsPerPass; ++e) {
                     if (e < nh) {
-                        const int d = __popc(qs[e] ^ code[j]);
-                        hist[d][tid] += 1u << (8 * e);
+                        const uint32_t d = (uint32_t)__popc(qs[e] ^ code[j]);
+                        red_shared_add(col + d * (kScoreThreads * 4), 1u << (8 * e));
                     }
                 }
             }
@@ -162,11 +120,11 @@ __global__ void __launch_bounds__(kScoreThreads, 3) k_score(const ScoreParams p)
 #pragma unroll
             for (int e = 0; e < kMaxHeadsPerPass; ++e) {
                 if (e < nh) {
-                    uint8_t* drow = p.dist + (int64_t)(head0 + hp + e) * p.n_cap + c0;
+                    uint8_t* drow = p.dist + (int64_t)(head0 + hp + e) * p.n_cap;
 #pragma unroll
                     for (int j = 0; j < TPT; ++j) {
-                        const int off = (j >> 2) * 4 * kScoreThreads + 4 * tid + (j & 3);
-                        if (off < nin) drow[off] = (uint8_t)__popc(qs[e] ^ code[j]);
+                        const int i = sbase + 128 * (j >> 2) + 4 * lane + (j & 3);
+                        if (i < n) drow[i] = (uint8_t)__popc(qs[e] ^ code[j]);
                     }
                 }
             }
@@ -192,15 +150,81 @@ __global__ void __launch_bounds__(kScoreThreads, 3) k_score(const ScoreParams p)
 
 // ---------------------------------------------------------------- TOPK
 
+// One warp selects its sub-chunk for one head and writes the selected token
+// indices ascending to `seg`; returns how many (warp-uniform).
+//   mode 0: no tied token (distance == t) of this sub-chunk is taken
+//   mode 1: every tied token is taken
+//   mode 2: the first qw tied tokens (token order) are taken
+template <int TPT>
+__device__ __forceinline__ int select_subchunk(const uint32_t (&code)[TPT], uint32_t qs, int t, int mode,
+                                               int qw, int sbase, int n, int wlo, int whi,
+                                               int32_t* __restrict__ seg) {
+    const int lane = threadIdx.x & 31;
+    const unsigned lt = (1u << lane) - 1u;
+    const int t_eff = (mode == 1) ? t : t - 1;
+    int pos = 0, tie_run = 0;
+#pragma unroll
+    for (int r = 0; r < TPT / 4; ++r) {
+        const int rb = sbase + 128 * r;
+        if (rb >= n) break;
+        const int i0 = rb + 4 * lane;
+        unsigned sel = 0;
+        const bool slow = (mode == 2) || (rb < wlo) || (rb + 128 > whi) || (rb + 128 > n);
+        if (!slow) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sel |= ((int)__popc(qs ^ code[4 * r + e]) <= t_eff ? 1u : 0u) << e;
+        } else {
+            unsigned tie = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = i0 + e;
+                const int d = __popc(qs ^ code[4 * r + e]);
+                const bool valid = i < n;
+                const bool inw = (i < wlo) || (i >= whi);
+                const bool take = (mode == 2) ? (d < t) : (d <= t_eff);
+                if (valid && (inw || take)) sel |= 1u << e;
+                if (valid && d == t) tie |= 1u << e;
+            }
+            if (mode == 2) {
+                const unsigned b0 = __ballot_sync(0xffffffffu, tie & 1u);
+                const unsigned b1 = __ballot_sync(0xffffffffu, (tie >> 1) & 1u);
+                const unsigned b2 = __ballot_sync(0xffffffffu, (tie >> 2) & 1u);
+                const unsigned b3 = __ballot_sync(0xffffffffu, (tie >> 3) & 1u);
+                int rk = tie_run + popc_lt(b0, lt) + popc_lt(b1, lt) + popc_lt(b2, lt) + popc_lt(b3, lt);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if ((tie >> e) & 1u) {
+                        if (rk < qw) sel |= 1u << e;
+                        ++rk;
+                    }
+                }
+                tie_run += __popc(b0) + __popc(b1) + __popc(b2) + __popc(b3);
+            }
+        }
+        const unsigned m0 = __ballot_sync(0xffffffffu, sel & 1u);
+        const unsigned m1 = __ballot_sync(0xffffffffu, (sel >> 1) & 1u);
+        const unsigned m2 = __ballot_sync(0xffffffffu, (sel >> 2) & 1u);
+        const unsigned m3 = __ballot_sync(0xffffffffu, (sel >> 3) & 1u);
+        int w = pos + popc_lt(m0, lt) + popc_lt(m1, lt) + popc_lt(m2, lt) + popc_lt(m3, lt);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if ((sel >> e) & 1u) seg[w++] = i0 + e;
+        pos += __popc(m0) + __popc(m1) + __popc(m2) + __popc(m3);
+    }
+    return pos;
+}
+
 template <int TPT>
 __global__ void __launch_bounds__(kScoreThreads, 3) k_select(const SelectParams p) {
     constexpr int C = kScoreThreads * TPT;
+    constexpr int SC = 32 * TPT;
     __shared__ int s_t[kMaxHeadsPerPass];
     __shared__ int s_quota[kMaxHeadsPerPass];
+    __shared__ int s_mode[kMaxHeadsPerPass];
     __shared__ uint32_t s_tot[kMaxHeadsPerPass][HA_NBINS];
     __shared__ uint32_t s_pre[kMaxHeadsPerPass][HA_NBINS];
-    __shared__ uint32_t s_w1[kWarps][2];
-    __shared__ uint32_t s_w2[kWarps][2];
+    __shared__ uint32_t s_own[kMaxHeadsPerPass][HA_NBINS];
+    __shared__ int s_wt[kMaxHeadsPerPass][kWarps];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int c = blockIdx.x % p.nchunks;
@@ -222,21 +246,22 @@ __global__ void __launch_bounds__(kScoreThreads, 3) k_select(const SelectParams 
     const int wlo = min(p.n_sink, n);          // sink window [0, wlo)
     const int whi = max(0, n - p.n_local);     // local window [whi, n)
     const int head0 = b * p.Hq + g * p.G;
-    const int64_t seg_stride = (int64_t)p.nchunks * p.chunk;
+    const int nseg = p.nchunks * kWarps;
+    const int64_t seg_stride = (int64_t)nseg * SC;
+    const int sc = c * kWarps + warp;          // this warp's segment
+    const int sbase = c * C + warp * SC;
 
     const uint32_t* row = p.k_sig + (int64_t)b * p.ks_sb + (int64_t)g * p.ks_sh;
-    const int i0 = c * C + tid * TPT;
     uint32_t code[TPT];
-    load_codes<TPT>(row, i0, n, code);
-    const int nvalid = max(0, min(TPT, n - i0));
+    load_codes<TPT>(row, sbase, n, code);
 
     for (int hp = 0; hp < p.G; hp += kMaxHeadsPerPass) {
         const int nh = min(kMaxHeadsPerPass, p.G - hp);
-        // ---- threshold bin t and this chunk's tie quota: the histograms of all
-        // chunks (totals) and of the chunks before this one (prefix), per head
+        // ---- histogram totals, the prefix before this chunk and this chunk's own
         for (int i = tid; i < kMaxHeadsPerPass * HA_NBINS; i += kScoreThreads) {
             (&s_tot[0][0])[i] = 0u;
             (&s_pre[0][0])[i] = 0u;
+            (&s_own[0][0])[i] = 0u;
         }
         __syncthreads();
         {
@@ -265,11 +290,13 @@ __global__ void __launch_bounds__(kScoreThreads, 3) k_select(const SelectParams 
                         const int u = rem - cc * HA_NBINS;
                         atomicAdd(&s_tot[e][u], v[k2]);
                         if (cc < c) atomicAdd(&s_pre[e][u], v[k2]);
+                        if (cc == c) atomicAdd(&s_own[e][u], v[k2]);
                     }
                 }
             }
         }
         __syncthreads();
+        // ---- threshold bin t, this chunk's quota of tied tokens and its mode
         if (warp < nh) {
             // bins 0..31 (bin 32 is implied: the cumulative count reaches n there)
             uint32_t incl = s_tot[warp][lane];
@@ -283,84 +310,60 @@ __global__ void __launch_bounds__(kScoreThreads, 3) k_select(const SelectParams 
             const uint32_t below = __shfl_sync(0xffffffffu, incl, (t == 0 ? 0 : t - 1) & 31);
             const int r = k - (t == 0 ? 0 : (int)below);
             if (lane == 0) {
+                const int quota = r - (int)s_pre[warp][t];
+                const int ties = (int)s_own[warp][t];
                 s_t[warp] = t;
-                s_quota[warp] = r - (int)s_pre[warp][t];
+                s_quota[warp] = quota;
+                s_mode[warp] = (quota <= 0) ? 0 : (quota >= ties ? 1 : 2);
             }
         }
         __syncthreads();
         uint32_t qs[kMaxHeadsPerPass];
-        int t[kMaxHeadsPerPass], quota[kMaxHeadsPerPass];
+        int t[kMaxHeadsPerPass], mode[kMaxHeadsPerPass], qw[kMaxHeadsPerPass];
+        bool boundary = false;
 #pragma unroll
         for (int e = 0; e < kMaxHeadsPerPass; ++e) {
             qs[e] = (e < nh) ? p.q_sig[head0 + hp + e] : 0u;
-            t[e] = (e < nh) ? s_t[e] : -1;
-            quota[e] = (e < nh) ? s_quota[e] : 0;
+            t[e] = (e < nh) ? s_t[e] : 0;
+            mode[e] = (e < nh) ? s_mode[e] : 0;
+            qw[e] = (e < nh) ? s_quota[e] : 0;
+            boundary = boundary || (mode[e] == 2);
         }
-        // ---- pass 1: ties (distance == t) per head, prefix over the chunk
-        uint32_t tie01 = 0, tie23 = 0;
+        // ---- the chunk where the tie quota runs out: per-warp tie counts
+        if (boundary) {
 #pragma unroll
-        for (int j = 0; j < TPT; ++j) {
-            if (j < nvalid) {
+            for (int e = 0; e < kMaxHeadsPerPass; ++e) {
+                if (mode[e] == 2) {
+                    uint32_t cnt = 0;
 #pragma unroll
-                for (int e = 0; e < kMaxHeadsPerPass; ++e) {
-                    const uint32_t hit = (__popc(qs[e] ^ code[j]) == t[e]) ? 1u : 0u;
-                    if (e == 0) tie01 += hit;
-                    if (e == 1) tie01 += hit << 16;
-                    if (e == 2) tie23 += hit;
-                    if (e == 3) tie23 += hit << 16;
+                    for (int j = 0; j < TPT; ++j) {
+                        const int i = sbase + 128 * (j >> 2) + 4 * lane + (j & 3);
+                        cnt += (i < n && (int)__popc(qs[e] ^ code[j]) == t[e]) ? 1u : 0u;
+                    }
+                    cnt = __reduce_add_sync(0xffffffffu, cnt);
+                    if (lane == 0) s_wt[e][warp] = (int)cnt;
+                }
+            }
+            __syncthreads();
+#pragma unroll
+            for (int e = 0; e < kMaxHeadsPerPass; ++e) {
+                if (mode[e] == 2) {
+                    int q = qw[e];
+                    for (int w2 = 0; w2 < warp; ++w2) q -= s_wt[e][w2];
+                    qw[e] = q;
+                    mode[e] = (q <= 0) ? 0 : (q >= s_wt[e][warp] ? 1 : 2);
                 }
             }
         }
-        uint32_t tb01, tb23, tt01, tt23;
-        block_scan2(tie01, tie23, tb01, tb23, tt01, tt23, s_w1);
-        // ---- pass 2: selection flags in token order
-        int run[kMaxHeadsPerPass];
-        uint32_t selmask[kMaxHeadsPerPass];
-        uint32_t sel01 = 0, sel23 = 0;
-#pragma unroll
-        for (int e = 0; e < kMaxHeadsPerPass; ++e) {
-            run[e] = (int)field(tb01, tb23, e);
-            selmask[e] = 0u;
-        }
-#pragma unroll
-        for (int j = 0; j < TPT; ++j) {
-            if (j < nvalid) {
-                const int i = i0 + j;
-                const bool inw = (i < wlo) || (i >= whi);
-#pragma unroll
-                for (int e = 0; e < kMaxHeadsPerPass; ++e) {
-                    const int d = __popc(qs[e] ^ code[j]);
-                    const bool tie = (d == t[e]);
-                    const bool s = inw || (d < t[e]) || (tie && run[e] < quota[e]);
-                    run[e] += tie ? 1 : 0;
-                    if (s) selmask[e] |= 1u << j;
-                }
-            }
-        }
-#pragma unroll
-        for (int e = 0; e < kMaxHeadsPerPass; ++e) {
-            if (e >= nh) selmask[e] = 0u;
-            const uint32_t cnt = (uint32_t)__popc(selmask[e]);
-            if (e == 0) sel01 += cnt;
-            if (e == 1) sel01 += cnt << 16;
-            if (e == 2) sel23 += cnt;
-            if (e == 3) sel23 += cnt << 16;
-        }
-        uint32_t sb01, sb23, st01, st23;
-        block_scan2(sel01, sel23, sb01, sb23, st01, st23, s_w2);
-        // ---- pass 3: write this chunk's ascending segment per head
+        // ---- select and write this warp's segment, head by head
 #pragma unroll
         for (int e = 0; e < kMaxHeadsPerPass; ++e) {
             if (e < nh) {
-                int32_t* seg = p.seg_idx + (int64_t)(head0 + hp + e) * seg_stride + (int64_t)c * p.chunk;
-                int pos = (int)field(sb01, sb23, e);
-                uint32_t msk = selmask[e];
-                while (msk) {
-                    const int j = __ffs(msk) - 1;
-                    msk &= msk - 1;
-                    seg[pos++] = i0 + j;
-                }
-                if (tid == 0) p.seg_cnt[(int64_t)(head0 + hp + e) * p.nchunks + c] = (int)field(st01, st23, e);
+                const int64_t h = head0 + hp + e;
+                int32_t* seg = p.seg_idx + h * seg_stride + (int64_t)sc * SC;
+                const int cnt = select_subchunk<TPT>(code, qs[e], t[e], mode[e], qw[e], sbase, n, wlo,
+                                                     whi, seg);
+                if (lane == 0) p.seg_cnt[h * nseg + sc] = cnt;
             }
         }
         __syncthreads();
@@ -373,15 +376,15 @@ __global__ void __launch_bounds__(256) k_compact(const CompactParams p) {
     const int head = blockIdx.x;
     const int b = head / p.Hq;
     const int n = checked_len(p.seq_lens, b, p.n_cap, p.err, false);
-    const int nch = (n + p.chunk - 1) / p.chunk;
-    const int32_t* cnt = p.seg_cnt + (int64_t)head * p.nchunks;
-    const int32_t* seg = p.seg_idx + (int64_t)head * p.nchunks * p.chunk;
+    const int nused = (n + p.seg_cap - 1) / p.seg_cap;
+    const int32_t* cnt = p.seg_cnt + (int64_t)head * p.nseg;
+    const int32_t* seg = p.seg_idx + (int64_t)head * p.nseg * p.seg_cap;
     int32_t* dst = p.sel_idx + (int64_t)head * p.cap;
     int base = 0;
-    for (int cc = 0; cc < nch; ++cc) {
-        int k = cnt[cc];
+    for (int s = 0; s < nused; ++s) {
+        int k = cnt[s];
         if (base + k > p.cap) k = p.cap - base;  // cannot happen for |I| <= cap
-        for (int t = threadIdx.x; t < k; t += blockDim.x) dst[base + t] = seg[(int64_t)cc * p.chunk + t];
+        for (int t = threadIdx.x; t < k; t += blockDim.x) dst[base + t] = seg[(int64_t)s * p.seg_cap + t];
         base += k;
     }
     for (int t = base + threadIdx.x; t < p.cap; t += blockDim.x) dst[t] = -1;
