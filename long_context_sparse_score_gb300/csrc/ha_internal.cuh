@@ -33,6 +33,9 @@ constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per pipeline 
 // seg_idx    int32 [heads][nseg*seg_cap] selected token indices, segment s's
 //                                          entries at [s*seg_cap, s*seg_cap + seg_cnt)
 // part       float [heads][splits][2 + d] split-K partials (max, sum, o[d])
+// score_cnt  uint32[batch*h_kv]          SCORE arrival counters (self-resetting)
+// meta_t     int32 [heads]                threshold bin t of every head
+// meta_qt    int2  [heads][nchunks]       per chunk: (tie quota left, ties in chunk)
 struct Layout {
     int heads = 0;
     int chunk = 0;           // tokens per SCORE/TOPK chunk (0: no selection regions)
@@ -43,6 +46,7 @@ struct Layout {
     int splits = 1;          // GATHER-ATT CTAs per head
     int rows_per_split = 0;  // multiple of kTileRows
     size_t off_err = 0, off_counter = 0, off_hist = 0, off_segcnt = 0, off_seg = 0, off_part = 0;
+    size_t off_scnt = 0, off_meta_t = 0, off_meta_qt = 0;
     size_t total = 0;
 };
 
@@ -67,6 +71,13 @@ struct ScoreParams {
     uint32_t* counters;      // reset to zero for the heads of this KV head (may be null)
     uint8_t* dist;           // optional [B, Hq, n_cap]
     uint32_t* err;
+    // selection thresholds (null: histograms only): the last CTA of a
+    // (batch entry, KV head) derives t and every chunk's tie quota
+    const int32_t* m_per_seq;
+    int m;
+    uint32_t* score_cnt;     // [B * Hkv]
+    int32_t* meta_t;         // [heads]
+    int2* meta_qt;           // [heads][nchunks]
 };
 
 struct SelectParams {
@@ -74,13 +85,13 @@ struct SelectParams {
     const uint32_t* k_sig;
     int64_t ks_sb, ks_sh;
     const int32_t* seq_lens;
-    const int32_t* m_per_seq;  // may be null
-    int m, n_sink, n_local;
+    int n_sink, n_local;
     int B, Hq, Hkv, G, n_cap;
     int chunk, nchunks;
-    const uint32_t* chunk_hist;
-    int32_t* seg_cnt;        // [heads][nchunks]
-    int32_t* seg_idx;        // [heads][nchunks*chunk]
+    const int32_t* meta_t;   // [heads]
+    const int2* meta_qt;     // [heads][nchunks]
+    int32_t* seg_cnt;        // [heads][nseg]
+    int32_t* seg_idx;        // [heads][nseg * seg_cap]
     uint32_t* err;
 };
 

@@ -114,6 +114,9 @@ struct Views {
     int32_t* seg_cnt;
     int32_t* seg_idx;
     float* part;
+    uint32_t* score_cnt;
+    int32_t* meta_t;
+    int2* meta_qt;
 };
 
 Views views(const Layout& lay, void* ws) {
@@ -124,11 +127,15 @@ Views views(const Layout& lay, void* ws) {
     v.seg_cnt = lay.chunk ? at<int32_t>(ws, lay.off_segcnt) : nullptr;
     v.seg_idx = lay.chunk ? at<int32_t>(ws, lay.off_seg) : nullptr;
     v.part = at<float>(ws, lay.off_part);
+    v.score_cnt = lay.chunk ? at<uint32_t>(ws, lay.off_scnt) : nullptr;
+    v.meta_t = lay.chunk ? at<int32_t>(ws, lay.off_meta_t) : nullptr;
+    v.meta_qt = lay.chunk ? at<int2>(ws, lay.off_meta_qt) : nullptr;
     return v;
 }
 
 ScoreParams score_params(const ha_shape* s, const Layout& lay, const Views& v, const uint32_t* q_sig,
-                         const uint32_t* k_sig, const int32_t* seq_lens) {
+                         const uint32_t* k_sig, const int32_t* seq_lens, const int32_t* m_per_seq,
+                         int32_t m, bool thresholds) {
     ScoreParams p{};
     p.q_sig = q_sig;
     p.k_sig = k_sig;
@@ -146,20 +153,22 @@ ScoreParams score_params(const ha_shape* s, const Layout& lay, const Views& v, c
     p.counters = v.counters;
     p.dist = nullptr;
     p.err = v.err;
+    p.m_per_seq = m_per_seq;
+    p.m = m;
+    p.score_cnt = thresholds ? v.score_cnt : nullptr;
+    p.meta_t = thresholds ? v.meta_t : nullptr;
+    p.meta_qt = thresholds ? v.meta_qt : nullptr;
     return p;
 }
 
 SelectParams select_params(const ha_shape* s, const Layout& lay, const Views& v, const uint32_t* q_sig,
-                           const uint32_t* k_sig, const int32_t* seq_lens, const int32_t* m_per_seq,
-                           int32_t m, int32_t n_sink, int32_t n_local) {
+                           const uint32_t* k_sig, const int32_t* seq_lens, int32_t n_sink, int32_t n_local) {
     SelectParams p{};
     p.q_sig = q_sig;
     p.k_sig = k_sig;
     p.ks_sb = s->ks_sb;
     p.ks_sh = s->ks_sh;
     p.seq_lens = seq_lens;
-    p.m_per_seq = m_per_seq;
-    p.m = m;
     p.n_sink = n_sink;
     p.n_local = n_local;
     p.B = s->batch;
@@ -169,7 +178,8 @@ SelectParams select_params(const ha_shape* s, const Layout& lay, const Views& v,
     p.n_cap = s->n_cap;
     p.chunk = lay.chunk;
     p.nchunks = lay.nchunks;
-    p.chunk_hist = v.chunk_hist;
+    p.meta_t = v.meta_t;
+    p.meta_qt = v.meta_qt;
     p.seg_cnt = v.seg_cnt;
     p.seg_idx = v.seg_idx;
     p.err = v.err;
@@ -264,9 +274,9 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
         return HA_OK;
     }
     HA_TRY(record(events, 0, st));
-    HA_LAUNCH(launch_score(score_params(s, lay, v, q_sig, k_sig, seq_lens), bhkv, st), "SCORE launch");
+    HA_LAUNCH(launch_score(score_params(s, lay, v, q_sig, k_sig, seq_lens, m_per_seq, m, true), bhkv, st), "SCORE launch");
     HA_TRY(record(events, 1, st));
-    HA_LAUNCH(launch_select(select_params(s, lay, v, q_sig, k_sig, seq_lens, m_per_seq, m, n_sink, n_local),
+    HA_LAUNCH(launch_select(select_params(s, lay, v, q_sig, k_sig, seq_lens, n_sink, n_local),
                             bhkv, st),
               "TOPK launch");
     HA_TRY(record(events, 2, st));
@@ -339,6 +349,12 @@ Layout make_layout(const ha_shape& s, int64_t rows_cap, bool with_selection) {
         off = align_up(off + (size_t)L.heads * L.nseg * 4, 256);
         L.off_seg = off;
         off = align_up(off + (size_t)L.heads * L.nseg * L.seg_cap * 4, 256);
+        L.off_scnt = off;
+        off = align_up(off + (size_t)s.batch * s.h_kv * 4, 256);
+        L.off_meta_t = off;
+        off = align_up(off + (size_t)L.heads * 4, 256);
+        L.off_meta_qt = off;
+        off = align_up(off + (size_t)L.heads * L.nchunks * 8, 256);
     }
     L.off_part = off;
     off = align_up(off + (size_t)L.heads * L.splits * (s.d + 2) * 4, 256);
@@ -412,7 +428,7 @@ ha_status hash_attn_score(const ha_shape* shape, const uint32_t* q_sig, const ui
     HA_TRY(check_ws(lay, workspace, ws_bytes));
     const Views v = views(lay, workspace);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    ScoreParams sp = score_params(shape, lay, v, q_sig, k_sig, seq_lens);
+    ScoreParams sp = score_params(shape, lay, v, q_sig, k_sig, seq_lens, nullptr, 0, false);
     sp.counters = nullptr;
     sp.dist = dist;
     HA_LAUNCH(launch_score(sp, shape->batch * shape->h_kv, st), "SCORE launch");
@@ -446,8 +462,8 @@ ha_status hash_attn_select(const ha_shape* shape, const uint32_t* q_sig, const u
     const Views v = views(lay, workspace);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int bhkv = shape->batch * shape->h_kv;
-    HA_LAUNCH(launch_score(score_params(shape, lay, v, q_sig, k_sig, seq_lens), bhkv, st), "SCORE launch");
-    HA_LAUNCH(launch_select(select_params(shape, lay, v, q_sig, k_sig, seq_lens, m_per_seq, m, n_sink, n_local),
+    HA_LAUNCH(launch_score(score_params(shape, lay, v, q_sig, k_sig, seq_lens, m_per_seq, m, true), bhkv, st), "SCORE launch");
+    HA_LAUNCH(launch_select(select_params(shape, lay, v, q_sig, k_sig, seq_lens, n_sink, n_local),
                             bhkv, st),
               "TOPK launch");
     CompactParams cp{};

@@ -71,13 +71,14 @@ __device__ __forceinline__ int popc_lt(unsigned m, unsigned lt) { return __popc(
 
 // ---------------------------------------------------------------- SCORE
 
-template <int TPT>
+template <int TPT, bool WRITE_DIST>
 __global__ void __launch_bounds__(kScoreThreads, 3) k_score(const ScoreParams p) {
     constexpr int C = kScoreThreads * TPT;
     constexpr int SC = 32 * TPT;
     // Per-thread histogram columns hist[bin][thread]: the counts of up to four
     // heads packed one byte each (a thread sees at most TPT <= 32 tokens).
     __shared__ uint32_t hist[HA_NBINS][kScoreThreads];
+    __shared__ int s_last;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int c = blockIdx.x % p.nchunks;
@@ -116,7 +117,7 @@ __global__ void __launch_bounds__(kScoreThreads, 3) k_score(const ScoreParams p)
                 }
             }
         }
-        if (p.dist != nullptr) {
+        if (WRITE_DIST) {
 #pragma unroll
             for (int e = 0; e < kMaxHeadsPerPass; ++e) {
                 if (e < nh) {
@@ -146,9 +147,110 @@ __global__ void __launch_bounds__(kScoreThreads, 3) k_score(const ScoreParams p)
         }
         __syncthreads();
     }
+
+    // ---- the last CTA of this (batch entry, KV head) to finish turns the chunk
+    // histograms into the threshold bin t of every head and, per chunk, the
+    // number of tied tokens (distance == t) still to take and the chunk's ties
+    if (p.meta_t == nullptr) return;
+    const int nch = (n + C - 1) / C;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const unsigned prev = atomicAdd(&p.score_cnt[bg], 1u);
+        if (prev >= (unsigned)nch) flag_error(p.err, HA_DEVERR_STATE);
+        s_last = (prev == (unsigned)(nch - 1)) ? 1 : 0;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    int mb = p.m;
+    if (p.m_per_seq != nullptr) {
+        mb = p.m_per_seq[b];
+        if (mb < 0 || mb > p.m) {
+            if (g == 0 && tid == 0) flag_error(p.err, HA_DEVERR_BUDGET);
+            mb = min(max(mb, 0), p.m);
+        }
+    }
+    const int k = min(mb, n);  // tokens taken by score
+    for (int e = warp; e < p.G; e += kWarps) {
+        const int64_t h = head0 + e;
+        const uint32_t* H = p.chunk_hist + h * p.nchunks * HA_NBINS;
+        // bins 0..31 (bin 32 is implied: the cumulative count reaches n there)
+        uint32_t tot = 0;
+        for (int c0b = 0; c0b < nch; c0b += 8) {
+            uint32_t v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = (c0b + u < nch) ? __ldcg(H + (c0b + u) * HA_NBINS + lane) : 0u;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) tot += v[u];
+        }
+        uint32_t incl = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const unsigned reach = __ballot_sync(0xffffffffu, incl >= (uint32_t)k);
+        const int t = reach ? (__ffs(reach) - 1) : 32;
+        const uint32_t below = __shfl_sync(0xffffffffu, incl, (t == 0 ? 0 : t - 1) & 31);
+        const int r = k - (t == 0 ? 0 : (int)below);
+        int carry = 0;  // tied tokens in the chunks before
+        for (int base = 0; base < nch; base += 32) {
+            const int cc = base + lane;
+            const int v = (cc < nch) ? (int)__ldcg(H + cc * HA_NBINS + t) : 0;
+            int in = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, in, o);
+                if (lane >= o) in += y;
+            }
+            if (cc < nch) p.meta_qt[h * p.nchunks + cc] = make_int2(r - (carry + in - v), v);
+            carry += __shfl_sync(0xffffffffu, in, 31);
+        }
+        if (lane == 0) p.meta_t[h] = t;
+    }
+    if (tid == 0) p.score_cnt[bg] = 0u;
 }
 
 // ---------------------------------------------------------------- TOPK
+
+// Selection bits of one round (4 tokens per lane) on the rare path: the round
+// touches a window or the end of the sequence, or the sub-chunk holds the point
+// where the tie quota runs out (mode 2). Returns the 4 selection bits in bits
+// 0..3 and the number of tied tokens of the whole round in bits 8..15.
+__device__ __noinline__ unsigned slow_round(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t qs,
+                                            int t, int t_eff, int mode, int qw, int tie_run, int i0, int n,
+                                            int wlo, int whi) {
+    const unsigned lt = (1u << (threadIdx.x & 31)) - 1u;
+    const uint32_t cw[4] = {c0, c1, c2, c3};
+    unsigned sel = 0, tie = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int i = i0 + e;
+        const int d = __popc(qs ^ cw[e]);
+        const bool valid = i < n;
+        const bool inw = (i < wlo) || (i >= whi);
+        const bool take = (mode == 2) ? (d < t) : (d <= t_eff);
+        if (valid && (inw || take)) sel |= 1u << e;
+        if (valid && d == t) tie |= 1u << e;
+    }
+    const unsigned b0 = __ballot_sync(0xffffffffu, tie & 1u);
+    const unsigned b1 = __ballot_sync(0xffffffffu, (tie >> 1) & 1u);
+    const unsigned b2 = __ballot_sync(0xffffffffu, (tie >> 2) & 1u);
+    const unsigned b3 = __ballot_sync(0xffffffffu, (tie >> 3) & 1u);
+    if (mode == 2) {
+        int rk = tie_run + popc_lt(b0, lt) + popc_lt(b1, lt) + popc_lt(b2, lt) + popc_lt(b3, lt);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if ((tie >> e) & 1u) {
+                if (rk < qw) sel |= 1u << e;
+                ++rk;
+            }
+        }
+    }
+    const unsigned ties = (unsigned)(__popc(b0) + __popc(b1) + __popc(b2) + __popc(b3));
+    return sel | (ties << 8);
+}
 
 // One warp selects its sub-chunk for one head and writes the selected token
 // indices ascending to `seg`; returns how many (warp-uniform).
@@ -174,32 +276,10 @@ __device__ __forceinline__ int select_subchunk(const uint32_t (&code)[TPT], uint
 #pragma unroll
             for (int e = 0; e < 4; ++e) sel |= ((int)__popc(qs ^ code[4 * r + e]) <= t_eff ? 1u : 0u) << e;
         } else {
-            unsigned tie = 0;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int i = i0 + e;
-                const int d = __popc(qs ^ code[4 * r + e]);
-                const bool valid = i < n;
-                const bool inw = (i < wlo) || (i >= whi);
-                const bool take = (mode == 2) ? (d < t) : (d <= t_eff);
-                if (valid && (inw || take)) sel |= 1u << e;
-                if (valid && d == t) tie |= 1u << e;
-            }
-            if (mode == 2) {
-                const unsigned b0 = __ballot_sync(0xffffffffu, tie & 1u);
-                const unsigned b1 = __ballot_sync(0xffffffffu, (tie >> 1) & 1u);
-                const unsigned b2 = __ballot_sync(0xffffffffu, (tie >> 2) & 1u);
-                const unsigned b3 = __ballot_sync(0xffffffffu, (tie >> 3) & 1u);
-                int rk = tie_run + popc_lt(b0, lt) + popc_lt(b1, lt) + popc_lt(b2, lt) + popc_lt(b3, lt);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    if ((tie >> e) & 1u) {
-                        if (rk < qw) sel |= 1u << e;
-                        ++rk;
-                    }
-                }
-                tie_run += __popc(b0) + __popc(b1) + __popc(b2) + __popc(b3);
-            }
+            const unsigned res = slow_round(code[4 * r], code[4 * r + 1], code[4 * r + 2], code[4 * r + 3], qs,
+                                            t, t_eff, mode, qw, tie_run, i0, n, wlo, whi);
+            sel = res & 15u;
+            tie_run += (int)(res >> 8);
         }
         const unsigned m0 = __ballot_sync(0xffffffffu, sel & 1u);
         const unsigned m1 = __ballot_sync(0xffffffffu, (sel >> 1) & 1u);
@@ -218,12 +298,6 @@ template <int TPT>
 __global__ void __launch_bounds__(kScoreThreads, 3) k_select(const SelectParams p) {
     constexpr int C = kScoreThreads * TPT;
     constexpr int SC = 32 * TPT;
-    __shared__ int s_t[kMaxHeadsPerPass];
-    __shared__ int s_quota[kMaxHeadsPerPass];
-    __shared__ int s_mode[kMaxHeadsPerPass];
-    __shared__ uint32_t s_tot[kMaxHeadsPerPass][HA_NBINS];
-    __shared__ uint32_t s_pre[kMaxHeadsPerPass][HA_NBINS];
-    __shared__ uint32_t s_own[kMaxHeadsPerPass][HA_NBINS];
     __shared__ int s_wt[kMaxHeadsPerPass][kWarps];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -234,15 +308,6 @@ __global__ void __launch_bounds__(kScoreThreads, 3) k_select(const SelectParams 
     const int nch = (n + C - 1) / C;
     if (c >= nch) return;
 
-    int mb = p.m;
-    if (p.m_per_seq != nullptr) {
-        mb = p.m_per_seq[b];
-        if (mb < 0 || mb > p.m) {
-            if (c == 0 && g == 0 && tid == 0) flag_error(p.err, HA_DEVERR_BUDGET);
-            mb = min(max(mb, 0), p.m);
-        }
-    }
-    const int k = min(mb, n);                  // tokens taken by score
     const int wlo = min(p.n_sink, n);          // sink window [0, wlo)
     const int whi = max(0, n - p.n_local);     // local window [whi, n)
     const int head0 = b * p.Hq + g * p.G;
@@ -257,76 +322,24 @@ __global__ void __launch_bounds__(kScoreThreads, 3) k_select(const SelectParams 
 
     for (int hp = 0; hp < p.G; hp += kMaxHeadsPerPass) {
         const int nh = min(kMaxHeadsPerPass, p.G - hp);
-        // ---- histogram totals, the prefix before this chunk and this chunk's own
-        for (int i = tid; i < kMaxHeadsPerPass * HA_NBINS; i += kScoreThreads) {
-            (&s_tot[0][0])[i] = 0u;
-            (&s_pre[0][0])[i] = 0u;
-            (&s_own[0][0])[i] = 0u;
-        }
-        __syncthreads();
-        {
-            const int per = nch * HA_NBINS;
-            const int total = nh * per;
-            const uint32_t* H0 = p.chunk_hist + (int64_t)(head0 + hp) * p.nchunks * HA_NBINS;
-            constexpr int kBatch = 8;
-            for (int i0 = 0; i0 < total; i0 += kBatch * kScoreThreads) {
-                uint32_t v[kBatch];
-#pragma unroll
-                for (int k2 = 0; k2 < kBatch; ++k2) {
-                    const int i = i0 + k2 * kScoreThreads + tid;
-                    v[k2] = 0u;
-                    if (i < total) {
-                        const int e = i / per;
-                        v[k2] = H0[(int64_t)e * p.nchunks * HA_NBINS + (i - e * per)];
-                    }
-                }
-#pragma unroll
-                for (int k2 = 0; k2 < kBatch; ++k2) {
-                    const int i = i0 + k2 * kScoreThreads + tid;
-                    if (v[k2] != 0u) {
-                        const int e = i / per;
-                        const int rem = i - e * per;
-                        const int cc = rem / HA_NBINS;
-                        const int u = rem - cc * HA_NBINS;
-                        atomicAdd(&s_tot[e][u], v[k2]);
-                        if (cc < c) atomicAdd(&s_pre[e][u], v[k2]);
-                        if (cc == c) atomicAdd(&s_own[e][u], v[k2]);
-                    }
-                }
-            }
-        }
-        __syncthreads();
-        // ---- threshold bin t, this chunk's quota of tied tokens and its mode
-        if (warp < nh) {
-            // bins 0..31 (bin 32 is implied: the cumulative count reaches n there)
-            uint32_t incl = s_tot[warp][lane];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            const unsigned reach = __ballot_sync(0xffffffffu, incl >= (uint32_t)k);
-            const int t = reach ? (__ffs(reach) - 1) : 32;
-            const uint32_t below = __shfl_sync(0xffffffffu, incl, (t == 0 ? 0 : t - 1) & 31);
-            const int r = k - (t == 0 ? 0 : (int)below);
-            if (lane == 0) {
-                const int quota = r - (int)s_pre[warp][t];
-                const int ties = (int)s_own[warp][t];
-                s_t[warp] = t;
-                s_quota[warp] = quota;
-                s_mode[warp] = (quota <= 0) ? 0 : (quota >= ties ? 1 : 2);
-            }
-        }
-        __syncthreads();
+        // ---- threshold bin t and this chunk's tie quota (from SCORE), per head
         uint32_t qs[kMaxHeadsPerPass];
         int t[kMaxHeadsPerPass], mode[kMaxHeadsPerPass], qw[kMaxHeadsPerPass];
         bool boundary = false;
 #pragma unroll
         for (int e = 0; e < kMaxHeadsPerPass; ++e) {
-            qs[e] = (e < nh) ? p.q_sig[head0 + hp + e] : 0u;
-            t[e] = (e < nh) ? s_t[e] : 0;
-            mode[e] = (e < nh) ? s_mode[e] : 0;
-            qw[e] = (e < nh) ? s_quota[e] : 0;
+            qs[e] = 0u;
+            t[e] = 0;
+            mode[e] = 0;
+            qw[e] = 0;
+            if (e < nh) {
+                const int64_t h = head0 + hp + e;
+                const int2 qt = p.meta_qt[h * p.nchunks + c];
+                qs[e] = p.q_sig[h];
+                t[e] = p.meta_t[h];
+                qw[e] = qt.x;
+                mode[e] = (qt.x <= 0) ? 0 : (qt.x >= qt.y ? 1 : 2);
+            }
             boundary = boundary || (mode[e] == 2);
         }
         // ---- the chunk where the tie quota runs out: per-warp tie counts
@@ -403,18 +416,23 @@ __global__ void __launch_bounds__(64) k_hist(const HistParams p) {
     p.hist[(int64_t)head * HA_NBINS + u] = s;
 }
 
-}  // namespace
-
-cudaError_t launch_score(const ScoreParams& p, int batch_hkv, cudaStream_t st) {
+template <bool WD>
+cudaError_t launch_score_t(const ScoreParams& p, int batch_hkv, cudaStream_t st) {
     const dim3 grid((unsigned)batch_hkv * (unsigned)p.nchunks);
     switch (p.chunk / kScoreThreads) {
-        case 4: k_score<4><<<grid, kScoreThreads, 0, st>>>(p); break;
-        case 8: k_score<8><<<grid, kScoreThreads, 0, st>>>(p); break;
-        case 16: k_score<16><<<grid, kScoreThreads, 0, st>>>(p); break;
-        case 32: k_score<32><<<grid, kScoreThreads, 0, st>>>(p); break;
+        case 4: k_score<4, WD><<<grid, kScoreThreads, 0, st>>>(p); break;
+        case 8: k_score<8, WD><<<grid, kScoreThreads, 0, st>>>(p); break;
+        case 16: k_score<16, WD><<<grid, kScoreThreads, 0, st>>>(p); break;
+        case 32: k_score<32, WD><<<grid, kScoreThreads, 0, st>>>(p); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_score(const ScoreParams& p, int batch_hkv, cudaStream_t st) {
+    return p.dist != nullptr ? launch_score_t<true>(p, batch_hkv, st) : launch_score_t<false>(p, batch_hkv, st);
 }
 
 cudaError_t launch_select(const SelectParams& p, int batch_hkv, cudaStream_t st) {
