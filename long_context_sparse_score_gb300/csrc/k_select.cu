@@ -214,84 +214,84 @@ __global__ void __launch_bounds__(kScoreThreads, 3) k_score(const ScoreParams p)
 
 // ---------------------------------------------------------------- TOPK
 
-// Selection bits of one round (4 tokens per lane) on the rare path: the round
-// touches a window or the end of the sequence, or the sub-chunk holds the point
-// where the tie quota runs out (mode 2). Returns the 4 selection bits in bits
-// 0..3 and the number of tied tokens of the whole round in bits 8..15.
-__device__ __noinline__ unsigned slow_round(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t qs,
-                                            int t, int t_eff, int mode, int qw, int tie_run, int i0, int n,
-                                            int wlo, int whi) {
-    const unsigned lt = (1u << (threadIdx.x & 31)) - 1u;
-    const uint32_t cw[4] = {c0, c1, c2, c3};
-    unsigned sel = 0, tie = 0;
+// Codes of this lane in TOPK: TPT consecutive tokens starting at lbase (a lane's
+// selected tokens are then consecutive in its segment); tokens >= n read 0.
+template <int TPT>
+__device__ __forceinline__ void load_codes_contig(const uint32_t* __restrict__ row, int lbase, int n,
+                                                  uint32_t (&c)[TPT]) {
+    if (lbase + TPT <= n) {
+        const uint4* p = reinterpret_cast<const uint4*>(row + lbase);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const int i = i0 + e;
-        const int d = __popc(qs ^ cw[e]);
-        const bool valid = i < n;
-        const bool inw = (i < wlo) || (i >= whi);
-        const bool take = (mode == 2) ? (d < t) : (d <= t_eff);
-        if (valid && (inw || take)) sel |= 1u << e;
-        if (valid && d == t) tie |= 1u << e;
-    }
-    const unsigned b0 = __ballot_sync(0xffffffffu, tie & 1u);
-    const unsigned b1 = __ballot_sync(0xffffffffu, (tie >> 1) & 1u);
-    const unsigned b2 = __ballot_sync(0xffffffffu, (tie >> 2) & 1u);
-    const unsigned b3 = __ballot_sync(0xffffffffu, (tie >> 3) & 1u);
-    if (mode == 2) {
-        int rk = tie_run + popc_lt(b0, lt) + popc_lt(b1, lt) + popc_lt(b2, lt) + popc_lt(b3, lt);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            if ((tie >> e) & 1u) {
-                if (rk < qw) sel |= 1u << e;
-                ++rk;
-            }
+        for (int j = 0; j < TPT / 4; ++j) {
+            const uint4 v = __ldg(p + j);
+            c[4 * j + 0] = v.x;
+            c[4 * j + 1] = v.y;
+            c[4 * j + 2] = v.z;
+            c[4 * j + 3] = v.w;
         }
+    } else {
+#pragma unroll
+        for (int j = 0; j < TPT; ++j) c[j] = (lbase + j < n) ? __ldg(row + lbase + j) : 0u;
     }
-    const unsigned ties = (unsigned)(__popc(b0) + __popc(b1) + __popc(b2) + __popc(b3));
-    return sel | (ties << 8);
 }
 
-// One warp selects its sub-chunk for one head and writes the selected token
-// indices ascending to `seg`; returns how many (warp-uniform).
-//   mode 0: no tied token (distance == t) of this sub-chunk is taken
-//   mode 1: every tied token is taken
-//   mode 2: the first qw tied tokens (token order) are taken
-template <int TPT>
-__device__ __forceinline__ int select_subchunk(const uint32_t (&code)[TPT], uint32_t qs, int t, int mode,
-                                               int qw, int sbase, int n, int wlo, int whi,
-                                               int32_t* __restrict__ seg) {
+// Warp-inclusive prefix sum.
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
     const int lane = threadIdx.x & 31;
-    const unsigned lt = (1u << lane) - 1u;
-    const int t_eff = (mode == 1) ? t : t - 1;
-    int pos = 0, tie_run = 0;
 #pragma unroll
-    for (int r = 0; r < TPT / 4; ++r) {
-        const int rb = sbase + 128 * r;
-        if (rb >= n) break;
-        const int i0 = rb + 4 * lane;
-        unsigned sel = 0;
-        const bool slow = (mode == 2) || (rb < wlo) || (rb + 128 > whi) || (rb + 128 > n);
-        if (!slow) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sel |= ((int)__popc(qs ^ code[4 * r + e]) <= t_eff ? 1u : 0u) << e;
-        } else {
-            const unsigned res = slow_round(code[4 * r], code[4 * r + 1], code[4 * r + 2], code[4 * r + 3], qs,
-                                            t, t_eff, mode, qw, tie_run, i0, n, wlo, whi);
-            sel = res & 15u;
-            tie_run += (int)(res >> 8);
-        }
-        const unsigned m0 = __ballot_sync(0xffffffffu, sel & 1u);
-        const unsigned m1 = __ballot_sync(0xffffffffu, (sel >> 1) & 1u);
-        const unsigned m2 = __ballot_sync(0xffffffffu, (sel >> 2) & 1u);
-        const unsigned m3 = __ballot_sync(0xffffffffu, (sel >> 3) & 1u);
-        int w = pos + popc_lt(m0, lt) + popc_lt(m1, lt) + popc_lt(m2, lt) + popc_lt(m3, lt);
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            if ((sel >> e) & 1u) seg[w++] = i0 + e;
-        pos += __popc(m0) + __popc(m1) + __popc(m2) + __popc(m3);
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
     }
-    return pos;
+    return v;
+}
+
+// Selection mask (bit j = token lbase + j, j < tpt) of one lane for one head on
+// the rare path: the lane's tokens touch a window or the end of the sequence, or
+// the sub-chunk holds the point where the tie quota runs out (mode 2, where the
+// whole warp calls this together to rank ties across lanes). Codes are re-read.
+__device__ __noinline__ uint32_t lane_mask_slow(const uint32_t* __restrict__ row, uint32_t qs, int t, int mode,
+                                                int qw, int lbase, int tpt, int n, int wlo, int whi) {
+    const int teff = (mode == 1) ? t : t - 1;
+    uint32_t m = 0u, tie = 0u;
+    for (int j = 0; j < tpt; ++j) {
+        const int i = lbase + j;
+        if (i >= n) break;
+        const int d = __popc(qs ^ __ldg(row + i));
+        const bool inw = (i < wlo) || (i >= whi);
+        const bool take = (mode == 2) ? (d < t) : (d <= teff);
+        if (inw || take) m |= 1u << j;
+        if (d == t) tie |= 1u << j;
+    }
+    if (mode == 2) {
+        const uint32_t c = (uint32_t)__popc(tie);
+        const int before = (int)(warp_incl_scan(c) - c);  // ties in the lanes before
+        int left = qw - before;
+        uint32_t x = tie;
+        while (x != 0u && left > 0) {
+            const uint32_t low = x & (0u - x);
+            m |= low;
+            x ^= low;
+            --left;
+        }
+    }
+    return m;
+}
+
+// Selection mask of one lane for one head.
+//   mode 0: no tied token (distance == t) of the sub-chunk is taken
+//   mode 1: every tied token is taken
+//   mode 2: the first qw tied tokens of the sub-chunk (token order) are taken
+template <int TPT>
+__device__ __forceinline__ uint32_t lane_mask(const uint32_t (&code)[TPT], const uint32_t* row, uint32_t qs,
+                                              int t, int mode, int qw, int lbase, int n, int wlo, int whi) {
+    const bool edge = (lbase < wlo) || (lbase + TPT > whi) || (lbase + TPT > n);
+    if (edge || mode == 2) return lane_mask_slow(row, qs, t, mode, qw, lbase, TPT, n, wlo, whi);
+    const int teff = (mode == 1) ? t : t - 1;
+    uint32_t m = 0u;
+#pragma unroll
+    for (int j = 0; j < TPT; ++j) m |= ((int)__popc(qs ^ code[j]) <= teff ? 1u : 0u) << j;
+    return m;
 }
 
 template <int TPT>
@@ -316,9 +316,10 @@ __global__ void __launch_bounds__(kScoreThreads, 3) k_select(const SelectParams 
     const int sc = c * kWarps + warp;          // this warp's segment
     const int sbase = c * C + warp * SC;
 
+    const int lbase = sbase + lane * TPT;      // this lane's first token
     const uint32_t* row = p.k_sig + (int64_t)b * p.ks_sb + (int64_t)g * p.ks_sh;
     uint32_t code[TPT];
-    load_codes<TPT>(row, sbase, n, code);
+    load_codes_contig<TPT>(row, lbase, n, code);
 
     for (int hp = 0; hp < p.G; hp += kMaxHeadsPerPass) {
         const int nh = min(kMaxHeadsPerPass, p.G - hp);
@@ -349,10 +350,8 @@ __global__ void __launch_bounds__(kScoreThreads, 3) k_select(const SelectParams 
                 if (mode[e] == 2) {
                     uint32_t cnt = 0;
 #pragma unroll
-                    for (int j = 0; j < TPT; ++j) {
-                        const int i = sbase + 128 * (j >> 2) + 4 * lane + (j & 3);
-                        cnt += (i < n && (int)__popc(qs[e] ^ code[j]) == t[e]) ? 1u : 0u;
-                    }
+                    for (int j = 0; j < TPT; ++j)
+                        cnt += (lbase + j < n && (int)__popc(qs[e] ^ code[j]) == t[e]) ? 1u : 0u;
                     cnt = __reduce_add_sync(0xffffffffu, cnt);
                     if (lane == 0) s_wt[e][warp] = (int)cnt;
                 }
@@ -368,15 +367,36 @@ __global__ void __launch_bounds__(kScoreThreads, 3) k_select(const SelectParams 
                 }
             }
         }
-        // ---- select and write this warp's segment, head by head
+        // ---- selection masks, then one prefix sum per head pair places every
+        // lane's selected tokens (consecutive in the segment)
+        uint32_t msk[kMaxHeadsPerPass];
+        uint32_t c01 = 0u, c23 = 0u;  // per-lane counts, 16-bit fields
+#pragma unroll
+        for (int e = 0; e < kMaxHeadsPerPass; ++e) {
+            msk[e] = (e < nh) ? lane_mask<TPT>(code, row, qs[e], t[e], mode[e], qw[e], lbase, n, wlo, whi) : 0u;
+            const uint32_t c = (uint32_t)__popc(msk[e]);
+            if (e == 0) c01 |= c;
+            if (e == 1) c01 |= c << 16;
+            if (e == 2) c23 |= c;
+            if (e == 3) c23 |= c << 16;
+        }
+        const uint32_t i01 = warp_incl_scan(c01);
+        const uint32_t i23 = (nh > 2) ? warp_incl_scan(c23) : 0u;
+        const uint32_t x01 = i01 - c01, x23 = i23 - c23;
+        const uint32_t t01 = __shfl_sync(0xffffffffu, i01, 31), t23 = __shfl_sync(0xffffffffu, i23, 31);
 #pragma unroll
         for (int e = 0; e < kMaxHeadsPerPass; ++e) {
             if (e < nh) {
                 const int64_t h = head0 + hp + e;
                 int32_t* seg = p.seg_idx + h * seg_stride + (int64_t)sc * SC;
-                const int cnt = select_subchunk<TPT>(code, qs[e], t[e], mode[e], qw[e], sbase, n, wlo,
-                                                     whi, seg);
-                if (lane == 0) p.seg_cnt[h * nseg + sc] = cnt;
+                int w = (int)field(x01, x23, e);
+                uint32_t x = msk[e];
+                while (x != 0u) {
+                    const int j = __ffs(x) - 1;
+                    x &= x - 1u;
+                    seg[w++] = lbase + j;
+                }
+                if (lane == 0) p.seg_cnt[h * nseg + sc] = (int)field(t01, t23, e);
             }
         }
         __syncthreads();
