@@ -50,8 +50,8 @@ struct Layout {
     size_t total = 0;
 };
 
-// Chunk of tokens per SCORE/TOPK CTA for a shape: the largest of 8192..1024 that
-// still gives kTargetCtas CTAs, else 1024.
+// Chunk of tokens per SCORE/TOPK CTA for a shape: kScoreThreads * TPT for the
+// largest TPT in {32, 16, 8, 4} that still gives kTargetCtas CTAs, else TPT = 4.
 int choose_chunk(int64_t batch_hkv, int64_t n_cap);
 // Split-K policy for GATHER-ATT.
 void choose_splits(int64_t heads, int64_t rows_cap, int* splits, int* rows_per_split);

@@ -306,9 +306,10 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
 // ---------------------------------------------------------------- layout policy
 
 int choose_chunk(int64_t batch_hkv, int64_t n_cap) {
-    for (int c = 8192; c > 1024; c >>= 1)
-        if (batch_hkv * ceil_div(n_cap, c) >= kTargetCtas) return c;
-    return 1024;
+    // kScoreThreads * TPT with TPT in {32, 16, 8, 4} (the instantiated kernels)
+    for (int tpt = 32; tpt > 4; tpt >>= 1)
+        if (batch_hkv * ceil_div(n_cap, (int64_t)kScoreThreads * tpt) >= kTargetCtas) return kScoreThreads * tpt;
+    return kScoreThreads * 4;
 }
 
 void choose_splits(int64_t heads, int64_t rows_cap, int* splits, int* rows_per_split) {

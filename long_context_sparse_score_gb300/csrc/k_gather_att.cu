@@ -355,9 +355,9 @@ __global__ void __launch_bounds__(kGatherThreads, 3) k_gather_att(const GatherPa
     }
     if (p.splits == 1) return;
 
-    __threadfence();
-    __syncthreads();
+    __syncthreads();  // every partial store of this CTA precedes thread 0's fence
     if (tid == 0) {
+        __threadfence();
         const unsigned prev = atomicAdd(&p.counters[head], 1u);
         if (prev >= (unsigned)p.splits) flag_error(p.err, HA_DEVERR_STATE);
         s_last = (prev == (unsigned)(p.splits - 1)) ? 1 : 0;

@@ -153,9 +153,9 @@ __global__ void __launch_bounds__(kScoreThreads, 3) k_score(const ScoreParams p)
     // number of tied tokens (distance == t) still to take and the chunk's ties
     if (p.meta_t == nullptr) return;
     const int nch = (n + C - 1) / C;
-    __threadfence();
-    __syncthreads();
+    __syncthreads();  // every histogram store of this CTA precedes thread 0's fence
     if (tid == 0) {
+        __threadfence();
         const unsigned prev = atomicAdd(&p.score_cnt[bg], 1u);
         if (prev >= (unsigned)nch) flag_error(p.err, HA_DEVERR_STATE);
         s_last = (prev == (unsigned)(nch - 1)) ? 1 : 0;
