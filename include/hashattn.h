@@ -21,7 +21,8 @@
  * Conventions shared by every entry point:
  *  - All tensor pointers are DEVICE pointers unless stated; the caller owns every
  *    buffer. The library allocates no device memory and keeps no global state
- *    other than a thread-local last-error string.
+ *    other than a thread-local last-error string and the fixed scratch array of
+ *    hash_attn_gather_att_noalloc.
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *    stream). All work is enqueued on it; no call synchronises except
  *    hash_attn_device_status and hash_attn_workspace_init's caller-visible copy.
@@ -192,6 +193,33 @@ ha_status hash_attn_gather_att(const ha_shape* shape, const void* q, const void*
                                const void* V, const int32_t* seq_lens, const int32_t* idx,
                                int32_t idx_cap, const int32_t* cnt, float* out, float* lse,
                                void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * GATHER-ATT + merge over caller-given index lists, like hash_attn_gather_att,
+ * but with no workspace argument and no device allocation anywhere: its scratch
+ * (error word, split counters, split-K partials) is a fixed array compiled into
+ * the library, HA_NOALLOC_SCRATCH_BYTES long, that every GPU which loads the
+ * library keeps until the process exits. The paper has no counterpart; this is
+ * for callers that are not allowed to allocate device memory, for instance a
+ * plugin whose host application owns every device allocation through its own
+ * pool, or a latency-critical path where cudaMalloc's implicit synchronisation
+ * with the device would stall other work.
+ *   dev_flags  optional device pointer to one uint32 that receives this call's
+ *              HA_DEVERR_* bits (0 = clean) in stream order; NULL to skip.
+ * Shapes whose scratch would exceed HA_NOALLOC_SCRATCH_BYTES are rejected with
+ * HA_ERR_WORKSPACE before anything is enqueued (the scratch holds
+ * 256 + 4 * batch * h_q plus 4 * batch * h_q * splits * (d + 2) bytes, rounded).
+ * The first call on a device looks up the array's device address and clears it
+ * (a synchronous memset); make that first call before any stream capture. All
+ * calls share the one array, which keeps the last call's contents: calls that
+ * overlap on the GPU (other streams, other host threads) race and must not be
+ * issued. Other arguments, layouts and errors as hash_attn_gather_att.
+ */
+#define HA_NOALLOC_SCRATCH_BYTES (16u << 20)
+ha_status hash_attn_gather_att_noalloc(const ha_shape* shape, const void* q, const void* K,
+                                       const void* V, const int32_t* seq_lens, const int32_t* idx,
+                                       int32_t idx_cap, const int32_t* cnt, float* out, float* lse,
+                                       uint32_t* dev_flags, void* stream);
 
 /*
  * Exact merge of two partial attentions over disjoint token sets, row by row

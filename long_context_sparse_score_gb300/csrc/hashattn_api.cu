@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <mutex>
 #include <string>
 
 #include "ha_internal.cuh"
@@ -551,3 +552,80 @@ const char* hash_attn_status_string(ha_status status) {
 const char* hash_attn_last_error(void) { return g_last_error.c_str(); }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- allocation-free GATHER-ATT
+//
+// Scratch for hash_attn_gather_att_noalloc: a fixed device array of the library
+// module. Host code must not hand the array's name to a kernel (on the host it
+// only stands in for the symbol); the device address is looked up per device.
+
+namespace ha {
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[HA_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kNoallocMaxDevices = 128;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kNoallocMaxDevices] = {};
+
+// Device address of the scratch on the current device; the first call per
+// device looks it up and clears the array.
+ha_status noalloc_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kNoallocMaxDevices)
+        return fail(HA_ERR_UNSUPPORTED, "device ordinal %d beyond %d", dev, kNoallocMaxDevices);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the built-in scratch");
+        e = cudaMemset(ptr, 0, HA_NOALLOC_SCRATCH_BYTES);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the built-in scratch");
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = g_noalloc_ptr[dev];
+    return HA_OK;
+}
+
+}  // namespace
+}  // namespace ha
+
+extern "C" ha_status hash_attn_gather_att_noalloc(const ha_shape* shape, const void* q, const void* K,
+                                                  const void* V, const int32_t* seq_lens, const int32_t* idx,
+                                                  int32_t idx_cap, const int32_t* cnt, float* out, float* lse,
+                                                  uint32_t* dev_flags, void* stream) {
+    HA_TRY(check_shape(shape));
+    if (q == nullptr || seq_lens == nullptr || out == nullptr || lse == nullptr || cnt == nullptr)
+        return fail(HA_ERR_INVALID_ARG, "q, seq_lens, cnt, out and lse must not be NULL");
+    if (idx_cap < 0 || idx_cap > shape->n_cap)
+        return fail(HA_ERR_INVALID_ARG, "idx_cap must be in [0, n_cap] (got %d)", idx_cap);
+    if (idx == nullptr && idx_cap > 0) return fail(HA_ERR_INVALID_ARG, "idx is NULL");
+    HA_TRY(check_kv(shape, K, V));
+    const Layout lay = make_layout(*shape, idx_cap, false);
+    if (lay.total > HA_NOALLOC_SCRATCH_BYTES)
+        return fail(HA_ERR_WORKSPACE,
+                    "this shape needs %zu bytes of scratch; the built-in scratch holds %u bytes "
+                    "(use hash_attn_gather_att with a caller workspace)",
+                    lay.total, (unsigned)HA_NOALLOC_SCRATCH_BYTES);
+    void* ws = nullptr;
+    HA_TRY(noalloc_scratch(&ws));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // the error word starts clean for every call; the counters are left at zero by
+    // the previous call (and by the clearing at set-up)
+    cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), st);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the error word");
+    const Views v = views(lay, ws);
+    GatherParams gp = gather_params(shape, lay, v, q, K, V, seq_lens, out, lse);
+    gp.mode = kList;
+    gp.list_idx = idx;
+    gp.list_cnt = cnt;
+    gp.list_cap = idx_cap;
+    HA_LAUNCH(launch_gather(gp, shape->d, shape->kv_dtype == HA_BF16, st), "GATHER-ATT launch");
+    if (dev_flags != nullptr) {
+        e = cudaMemcpyAsync(dev_flags, ws, sizeof(uint32_t), cudaMemcpyDeviceToDevice, st);
+        if (e != cudaSuccess) return cuda_fail(e, "copying the error word");
+    }
+    return HA_OK;
+}

@@ -32,12 +32,13 @@ HA_DEVERR_TIMEOUT = 0x10
 HA_DEVERR_STATE = 0x20
 
 HA_NBINS = 33
+HA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 # Entry points declared in include/hashattn.h (checked by the tests).
 EXPORTED = [
     "hash_attn_workspace_size", "hash_attn_workspace_init", "hash_attn_select_capacity",
     "hash_attn_decode", "hash_attn_decode_timed", "hash_attn_score", "hash_attn_select",
-    "hash_attn_gather_att", "hash_attn_merge", "hash_attn_device_status",
+    "hash_attn_gather_att", "hash_attn_gather_att_noalloc", "hash_attn_merge", "hash_attn_device_status",
     "hash_attn_status_string", "hash_attn_last_error",
 ]
 
@@ -89,6 +90,7 @@ def lib() -> ctypes.CDLL:
     L.hash_attn_score.argtypes = [SP, _P, _P, _P, _P, _P, _P, _SZ, _P]
     L.hash_attn_select.argtypes = [SP, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _SZ, _P]
     L.hash_attn_gather_att.argtypes = [SP, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P, _SZ, _P]
+    L.hash_attn_gather_att_noalloc.argtypes = [SP, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P, _P]
     L.hash_attn_merge.argtypes = [_P, _P, _P, _P, _P, _P, _I32, _I32, _P]
     L.hash_attn_device_status.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_uint32)]
     L.hash_attn_status_string.argtypes = [_I32]
@@ -226,6 +228,15 @@ def hash_attn_gather_att(shape, q, K, V, seq_lens, idx, idx_cap, cnt, out, lse, 
     _check(lib().hash_attn_gather_att(ctypes.byref(shape), _ptr(q), _ptr(K), _ptr(V), _ptr(seq_lens),
                                       _ptr(idx), idx_cap, _ptr(cnt), _ptr(out), _ptr(lse), ws, nb,
                                       _stream(stream)))
+
+
+def hash_attn_gather_att_noalloc(shape, q, K, V, seq_lens, idx, idx_cap, cnt, out, lse, dev_flags=None,
+                                 stream=None) -> None:
+    """hash_attn_gather_att without a workspace: the library's built-in scratch
+    serves (for callers that may not allocate device memory)."""
+    _check(lib().hash_attn_gather_att_noalloc(ctypes.byref(shape), _ptr(q), _ptr(K), _ptr(V),
+                                              _ptr(seq_lens), _ptr(idx), idx_cap, _ptr(cnt), _ptr(out),
+                                              _ptr(lse), _ptr(dev_flags), _stream(stream)))
 
 
 def hash_attn_merge(out_a, lse_a, out_b, lse_b, out, lse, rows: int, d: int, stream=None) -> None:
