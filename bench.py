@@ -82,6 +82,12 @@ def dist_max(world, x: float, device) -> float:
     return float(t.item())
 
 
+def throughput(world: int, heads_per_rank: int, steps: int, elapsed_ms: float) -> float:
+    """Query heads per second of the whole job: every rank decodes its own batch
+    (weak scaling); elapsed_ms is the slowest rank's time for `steps` steps."""
+    return world * heads_per_rank * steps / (elapsed_ms / 1e3)
+
+
 # ---------------------------------------------------------------- peaks, clocks, profiles
 
 def hbm_peak():
@@ -313,8 +319,7 @@ def run_ours(args, world, rank, local):
     t_topk = [evs[k][1].elapsed_time(evs[k][2]) for k in range(K)]
     t_gath = [evs[k][2].elapsed_time(evs[k][3]) for k in range(K)]
     ms_step = elapsed_ms / K
-    heads_total = world * B * Hq * K
-    value = heads_total / (elapsed_ms / 1e3)
+    value = throughput(world, B * Hq, K, elapsed_ms)
 
     # e2e: per-step query inputs from pinned host memory, results back to the host
     q_h = w.q.cpu().pin_memory()
