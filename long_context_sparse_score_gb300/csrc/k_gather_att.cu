@@ -17,7 +17,7 @@
 // P - 1 tiles in flight while it computes the oldest one. Waits are on the
 // warp's own copy groups only: no barrier couples warps until the final combine.
 // In a tile, 4 lanes share a row: scores are fp32 (q pre-scaled by
-// log2(e)/sqrt(d), packed fp32x2 FMAs), the softmax is online in base 2 and P.V
+// log2(e)/sqrt(d) and kept in shared memory, packed fp32x2 FMAs), the softmax is online in base 2 and P.V
 // accumulates per lane over its rows. Splits write (max, sum, o) partials; the
 // last CTA of a head to finish merges them (an arrival counter decides who is
 // last; nothing waits).
@@ -99,8 +99,11 @@ __device__ __forceinline__ int token_at(const GatherParams& p, int pp, int n, co
     return tok;
 }
 
+// Five CTAs per SM for rows of up to 256 bytes (20 warps of copy pipelines);
+// the 512-byte-row instantiation keeps three to avoid spills.
 template <int D, typename KT>
-__global__ void __launch_bounds__(kGatherThreads, 3) k_gather_att(const GatherParams p) {
+__global__ void __launch_bounds__(kGatherThreads, (D * sizeof(KT) <= 256) ? 5 : 3)
+    k_gather_att(const GatherParams p) {
     using C = Cfg<D, KT>;
     extern __shared__ __align__(128) unsigned char smem[];
     float* wm = reinterpret_cast<float*>(smem + C::OFF_CMB);
@@ -109,6 +112,7 @@ __global__ void __launch_bounds__(kGatherThreads, 3) k_gather_att(const GatherPa
     int* tokl = reinterpret_cast<int*>(smem + C::OFF_TOKL);
     int* pre = tokl + p.rows_per_split;   // [nseg + 1] (segmented lists only)
     __shared__ int s_L, s_last;
+    __shared__ __align__(16) float s_q[D];   // q * log2(e) / sqrt(d), shared by the CTA's warps
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int lin = blockIdx.x;
@@ -159,7 +163,12 @@ __global__ void __launch_bounds__(kGatherThreads, 3) k_gather_att(const GatherPa
     const int r0 = split * p.rows_per_split;
     const int nrows = max(0, min(L, r0 + p.rows_per_split) - r0);
 
-    // ---- this CTA's token indices (list positions [r0, r0 + nrows)) into shared memory
+    // ---- the scaled query, then this CTA's token indices (list positions
+    // [r0, r0 + nrows)) into shared memory
+    {
+        const int64_t qoff = (int64_t)b * p.q_sb + (int64_t)(g * p.G + hh) * p.q_sh;
+        for (int dd = tid; dd < D; dd += kGatherThreads) s_q[dd] = load_q(p.q, qoff + dd, p.q_bf16) * p.qscale;
+    }
     {
         const int32_t* seg = (p.mode == kSegmented) ? p.seg_idx + (int64_t)head * p.nseg * p.seg_cap : nullptr;
         const int32_t* lst = (p.mode == kList) ? p.list_idx + (int64_t)head * p.list_cap : nullptr;
@@ -209,17 +218,6 @@ __global__ void __launch_bounds__(kGatherThreads, 3) k_gather_att(const GatherPa
     };
 
     const int r = lane & 7, qt = lane >> 3;
-    float qv[C::DPL];
-    {
-        const int64_t qoff = (int64_t)b * p.q_sb + (int64_t)(g * p.G + hh) * p.q_sh;
-#pragma unroll
-        for (int jc = 0; jc < C::CPL; ++jc) {
-            const int dim0 = (jc * 4 + qt) * C::EPC;
-#pragma unroll
-            for (int e = 0; e < C::EPC; ++e)
-                qv[jc * C::EPC + e] = load_q(p.q, qoff + dim0 + e, p.q_bf16) * p.qscale;
-        }
-    }
     float2 ov[C::DPL / 2];
 #pragma unroll
     for (int i = 0; i < C::DPL / 2; ++i) ov[i] = make_float2(0.f, 0.f);
@@ -250,10 +248,9 @@ __global__ void __launch_bounds__(kGatherThreads, 3) k_gather_att(const GatherPa
                 chunk_to_float<KT>(w, f);
 #pragma unroll
                 for (int e = 0; e < C::EPC; e += 4) {
-                    a0 = __ffma2_rn(make_float2(qv[jc * C::EPC + e], qv[jc * C::EPC + e + 1]),
-                                    make_float2(f[e], f[e + 1]), a0);
-                    a1 = __ffma2_rn(make_float2(qv[jc * C::EPC + e + 2], qv[jc * C::EPC + e + 3]),
-                                    make_float2(f[e + 2], f[e + 3]), a1);
+                    const float4 q4 = *reinterpret_cast<const float4*>(s_q + (jc * 4 + qt) * C::EPC + e);
+                    a0 = __ffma2_rn(make_float2(q4.x, q4.y), make_float2(f[e], f[e + 1]), a0);
+                    a1 = __ffma2_rn(make_float2(q4.z, q4.w), make_float2(f[e + 2], f[e + 3]), a1);
                 }
             }
             part = (a0.x + a0.y) + (a1.x + a1.y);
