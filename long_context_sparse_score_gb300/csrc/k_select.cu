@@ -67,8 +67,6 @@ __device__ __forceinline__ uint32_t field(uint32_t w01, uint32_t w23, int e) {
     return (e & 1) ? (w >> 16) : (w & 0xffffu);
 }
 
-__device__ __forceinline__ int popc_lt(unsigned m, unsigned lt) { return __popc(m & lt); }
-
 // ---------------------------------------------------------------- SCORE
 
 template <int TPT, bool WRITE_DIST>
@@ -216,22 +214,36 @@ __global__ void __launch_bounds__(kScoreThreads, 3) k_score(const ScoreParams p)
 
 // Codes of this lane in TOPK: TPT consecutive tokens starting at lbase (a lane's
 // selected tokens are then consecutive in its segment); tokens >= n read 0.
+// The warp loads its 32 * TPT codes with 512-byte coalesced loads and hands
+// them to their owner lanes through a shared tile (row pitch TPT + 4 words keeps
+// both the stores and the per-lane reads free of bank conflicts).
 template <int TPT>
-__device__ __forceinline__ void load_codes_contig(const uint32_t* __restrict__ row, int lbase, int n,
-                                                  uint32_t (&c)[TPT]) {
-    if (lbase + TPT <= n) {
-        const uint4* p = reinterpret_cast<const uint4*>(row + lbase);
+__device__ __forceinline__ void load_codes_contig(const uint32_t* __restrict__ row, int sbase, int n,
+                                                  uint32_t (*tile)[TPT + 4], uint32_t (&c)[TPT]) {
+    const int lane = threadIdx.x & 31;
 #pragma unroll
-        for (int j = 0; j < TPT / 4; ++j) {
-            const uint4 v = __ldg(p + j);
-            c[4 * j + 0] = v.x;
-            c[4 * j + 1] = v.y;
-            c[4 * j + 2] = v.z;
-            c[4 * j + 3] = v.w;
+    for (int j = 0; j < TPT / 4; ++j) {
+        const int o = 128 * j + 4 * lane;  // offset in the warp's sub-chunk
+        const int i = sbase + o;
+        uint4 v;
+        if (i + 4 <= n) {
+            v = __ldg(reinterpret_cast<const uint4*>(row + i));
+        } else {
+            v.x = (i < n) ? __ldg(row + i) : 0u;
+            v.y = (i + 1 < n) ? __ldg(row + i + 1) : 0u;
+            v.z = (i + 2 < n) ? __ldg(row + i + 2) : 0u;
+            v.w = (i + 3 < n) ? __ldg(row + i + 3) : 0u;
         }
-    } else {
+        *reinterpret_cast<uint4*>(&tile[o / TPT][o % TPT]) = v;
+    }
+    __syncwarp();
 #pragma unroll
-        for (int j = 0; j < TPT; ++j) c[j] = (lbase + j < n) ? __ldg(row + lbase + j) : 0u;
+    for (int j = 0; j < TPT / 4; ++j) {
+        const uint4 v = *reinterpret_cast<const uint4*>(&tile[lane][4 * j]);
+        c[4 * j + 0] = v.x;
+        c[4 * j + 1] = v.y;
+        c[4 * j + 2] = v.z;
+        c[4 * j + 3] = v.w;
     }
 }
 
@@ -249,15 +261,16 @@ __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
 // Selection mask (bit j = token lbase + j, j < tpt) of one lane for one head on
 // the rare path: the lane's tokens touch a window or the end of the sequence, or
 // the sub-chunk holds the point where the tie quota runs out (mode 2, where the
-// whole warp calls this together to rank ties across lanes). Codes are re-read.
-__device__ __noinline__ uint32_t lane_mask_slow(const uint32_t* __restrict__ row, uint32_t qs, int t, int mode,
+// whole warp calls this together to rank ties across lanes). `codes` are the
+// lane's codes in the shared tile.
+__device__ __noinline__ uint32_t lane_mask_slow(const uint32_t* codes, uint32_t qs, int t, int mode,
                                                 int qw, int lbase, int tpt, int n, int wlo, int whi) {
     const int teff = (mode == 1) ? t : t - 1;
     uint32_t m = 0u, tie = 0u;
     for (int j = 0; j < tpt; ++j) {
         const int i = lbase + j;
         if (i >= n) break;
-        const int d = __popc(qs ^ __ldg(row + i));
+        const int d = __popc(qs ^ codes[j]);
         const bool inw = (i < wlo) || (i >= whi);
         const bool take = (mode == 2) ? (d < t) : (d <= teff);
         if (inw || take) m |= 1u << j;
@@ -283,10 +296,10 @@ __device__ __noinline__ uint32_t lane_mask_slow(const uint32_t* __restrict__ row
 //   mode 1: every tied token is taken
 //   mode 2: the first qw tied tokens of the sub-chunk (token order) are taken
 template <int TPT>
-__device__ __forceinline__ uint32_t lane_mask(const uint32_t (&code)[TPT], const uint32_t* row, uint32_t qs,
+__device__ __forceinline__ uint32_t lane_mask(const uint32_t (&code)[TPT], const uint32_t* tile_row, uint32_t qs,
                                               int t, int mode, int qw, int lbase, int n, int wlo, int whi) {
     const bool edge = (lbase < wlo) || (lbase + TPT > whi) || (lbase + TPT > n);
-    if (edge || mode == 2) return lane_mask_slow(row, qs, t, mode, qw, lbase, TPT, n, wlo, whi);
+    if (edge || mode == 2) return lane_mask_slow(tile_row, qs, t, mode, qw, lbase, TPT, n, wlo, whi);
     const int teff = (mode == 1) ? t : t - 1;
     uint32_t m = 0u;
 #pragma unroll
@@ -299,6 +312,7 @@ __global__ void __launch_bounds__(kScoreThreads, 3) k_select(const SelectParams 
     constexpr int C = kScoreThreads * TPT;
     constexpr int SC = 32 * TPT;
     __shared__ int s_wt[kMaxHeadsPerPass][kWarps];
+    __shared__ __align__(16) uint32_t s_codes[kWarps][32][TPT + 4];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int c = blockIdx.x % p.nchunks;
@@ -319,7 +333,7 @@ __global__ void __launch_bounds__(kScoreThreads, 3) k_select(const SelectParams 
     const int lbase = sbase + lane * TPT;      // this lane's first token
     const uint32_t* row = p.k_sig + (int64_t)b * p.ks_sb + (int64_t)g * p.ks_sh;
     uint32_t code[TPT];
-    load_codes_contig<TPT>(row, lbase, n, code);
+    load_codes_contig<TPT>(row, sbase, n, s_codes[warp], code);
 
     for (int hp = 0; hp < p.G; hp += kMaxHeadsPerPass) {
         const int nh = min(kMaxHeadsPerPass, p.G - hp);
@@ -373,7 +387,9 @@ __global__ void __launch_bounds__(kScoreThreads, 3) k_select(const SelectParams 
         uint32_t c01 = 0u, c23 = 0u;  // per-lane counts, 16-bit fields
 #pragma unroll
         for (int e = 0; e < kMaxHeadsPerPass; ++e) {
-            msk[e] = (e < nh) ? lane_mask<TPT>(code, row, qs[e], t[e], mode[e], qw[e], lbase, n, wlo, whi) : 0u;
+            msk[e] = (e < nh) ? lane_mask<TPT>(code, &s_codes[warp][lane][0], qs[e], t[e], mode[e], qw[e], lbase, n,
+                                                 wlo, whi)
+                               : 0u;
             const uint32_t c = (uint32_t)__popc(msk[e]);
             if (e == 0) c01 |= c;
             if (e == 1) c01 |= c << 16;
