@@ -142,16 +142,26 @@ __global__ void __launch_bounds__(kGatherThreads, (D * sizeof(KT) <= 256) ? 5 : 
             const int32_t* cnt = p.seg_cnt + (int64_t)head * p.nseg;
             int carry = 0;
             if (lane == 0) pre[0] = 0;
-            for (int base = 0; base < nused; base += 32) {
-                const int cc = base + lane;
-                int v = (cc < nused) ? cnt[cc] : 0;
+            // counts in batches of 4 x 32 loads in flight, then the scans
+            for (int base = 0; base < nused; base += 128) {
+                int v4[4];
 #pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int y = __shfl_up_sync(0xffffffffu, v, o);
-                    if (lane >= o) v += y;
+                for (int k = 0; k < 4; ++k) {
+                    const int cc = base + 32 * k + lane;
+                    v4[k] = (cc < nused) ? cnt[cc] : 0;
                 }
-                if (cc < nused) pre[cc + 1] = carry + v;
-                carry += __shfl_sync(0xffffffffu, v, 31);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int cc = base + 32 * k + lane;
+                    int v = v4[k];
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const int y = __shfl_up_sync(0xffffffffu, v, o);
+                        if (lane >= o) v += y;
+                    }
+                    if (cc < nused) pre[cc + 1] = carry + v;
+                    carry += __shfl_sync(0xffffffffu, v, 31);
+                }
             }
             L = carry;
         }

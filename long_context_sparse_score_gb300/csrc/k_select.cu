@@ -308,7 +308,7 @@ __device__ __forceinline__ uint32_t lane_mask(const uint32_t (&code)[TPT], const
 }
 
 template <int TPT>
-__global__ void __launch_bounds__(kScoreThreads, 3) k_select(const SelectParams p) {
+__global__ void __launch_bounds__(kScoreThreads, 4) k_select(const SelectParams p) {
     constexpr int C = kScoreThreads * TPT;
     constexpr int SC = 32 * TPT;
     __shared__ int s_wt[kMaxHeadsPerPass][kWarps];
