@@ -73,9 +73,11 @@ template <int TPT, bool WRITE_DIST>
 __global__ void __launch_bounds__(kScoreThreads, 3) k_score(const ScoreParams p) {
     constexpr int C = kScoreThreads * TPT;
     constexpr int SC = 32 * TPT;
-    // Per-thread histogram columns hist[bin][thread]: the counts of up to four
-    // heads packed one byte each (a thread sees at most TPT <= 32 tokens).
-    __shared__ uint32_t hist[HA_NBINS][kScoreThreads];
+    // Histogram columns hist[bin][pair][lane], shared by the CTA's warps: lane l
+    // of every warp adds into column l (no bank conflict inside an instruction),
+    // heads 2*pair and 2*pair+1 in the low and high 16-bit field (a column sees at
+    // most kWarps * TPT <= 256 tokens per bin).
+    __shared__ uint32_t hist[HA_NBINS][2][32];
     __shared__ int s_last;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -93,15 +95,15 @@ __global__ void __launch_bounds__(kScoreThreads, 3) k_score(const ScoreParams p)
     const int sbase = c0 + warp * SC;
     uint32_t code[TPT];
     load_codes<TPT>(row, sbase, n, code);
-    const uint32_t col = smem_addr(&hist[0][tid]);
+    const uint32_t col = smem_addr(&hist[0][0][lane]);
 
     for (int hp = 0; hp < p.G; hp += kMaxHeadsPerPass) {
         const int nh = min(kMaxHeadsPerPass, p.G - hp);
         uint32_t qs[kMaxHeadsPerPass];
 #pragma unroll
         for (int e = 0; e < kMaxHeadsPerPass; ++e) qs[e] = (e < nh) ? p.q_sig[head0 + hp + e] : 0u;
-#pragma unroll
-        for (int u = 0; u < HA_NBINS; ++u) hist[u][tid] = 0u;
+        for (int x = tid; x < HA_NBINS * 2 * 32; x += kScoreThreads) (&hist[0][0][0])[x] = 0u;
+        __syncthreads();
 #pragma unroll
         for (int j = 0; j < TPT; ++j) {
             const int i = sbase + 128 * (j >> 2) + 4 * lane + (j & 3);
@@ -110,7 +112,7 @@ __global__ void __launch_bounds__(kScoreThreads, 3) k_score(const ScoreParams p)
                 for (int e = 0; e < kMaxHeadsPerPass; ++e) {
                     if (e < nh) {
                         const uint32_t d = (uint32_t)__popc(qs[e] ^ code[j]);
-                        red_shared_add(col + d * (kScoreThreads * 4), 1u << (8 * e));
+                        red_shared_add(col + (d * 2 + (e >> 1)) * (32 * 4), 1u << (16 * (e & 1)));
                     }
                 }
             }
@@ -130,15 +132,8 @@ __global__ void __launch_bounds__(kScoreThreads, 3) k_score(const ScoreParams p)
         }
         __syncthreads();
         for (int u = warp; u < HA_NBINS; u += kWarps) {
-            uint32_t s01 = 0, s23 = 0;  // 16-bit fields: heads (0,1) and (2,3)
-#pragma unroll
-            for (int k = lane; k < kScoreThreads; k += 32) {
-                const uint32_t w = hist[u][k];
-                s01 += (w & 0xffu) | ((w & 0xff00u) << 8);
-                s23 += ((w >> 16) & 0xffu) | ((w >> 8) & 0xff0000u);
-            }
-            s01 = warp_sum(s01);
-            s23 = warp_sum(s23);
+            const uint32_t s01 = warp_sum(hist[u][0][lane]);  // 16-bit fields: heads (0,1)
+            const uint32_t s23 = warp_sum(hist[u][1][lane]);  // and (2,3)
             if (lane < nh)
                 p.chunk_hist[((int64_t)(head0 + hp + lane) * p.nchunks + c) * HA_NBINS + u] =
                     field(s01, s23, lane);
