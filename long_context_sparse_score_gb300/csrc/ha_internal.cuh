@@ -7,6 +7,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "hashattn.h"
 
 namespace ha {
@@ -148,12 +150,29 @@ struct MergeParams {
     int rows, d;
 };
 
+// Launch with (pdl = true) or without programmatic stream serialization.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                      Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 // Launchers (each returns cudaGetLastError() of its launch).
 cudaError_t launch_score(const ScoreParams& p, int batch_hkv, cudaStream_t st);
-cudaError_t launch_select(const SelectParams& p, int batch_hkv, cudaStream_t st);
+cudaError_t launch_select(const SelectParams& p, int batch_hkv, cudaStream_t st, bool pdl = false);
 cudaError_t launch_compact(const CompactParams& p, int heads, cudaStream_t st);
 cudaError_t launch_hist(const HistParams& p, int heads, cudaStream_t st);
-cudaError_t launch_gather(const GatherParams& p, int d, int kv_bf16, cudaStream_t st);
+cudaError_t launch_gather(const GatherParams& p, int d, int kv_bf16, cudaStream_t st, bool pdl = false);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t st);
 
 // ------------------------------------------------------------------ device helpers
@@ -247,6 +266,13 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
     asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
+
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while its predecessor drains; it must wait here
+// before touching the predecessor's outputs. launch_dependents lets the next
+// such kernel start early (it changes only when it may start, not what it sees).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }

@@ -277,12 +277,14 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
     HA_TRY(record(events, 0, st));
     HA_LAUNCH(launch_score(score_params(s, lay, v, q_sig, k_sig, seq_lens, m_per_seq, m, true), bhkv, st), "SCORE launch");
     HA_TRY(record(events, 1, st));
+    // TOPK and GATHER-ATT may start while their predecessor drains (they wait in
+    // the kernel before reading its output)
     HA_LAUNCH(launch_select(select_params(s, lay, v, q_sig, k_sig, seq_lens, n_sink, n_local),
-                            bhkv, st),
+                            bhkv, st, true),
               "TOPK launch");
     HA_TRY(record(events, 2, st));
     gp.mode = kSegmented;
-    HA_LAUNCH(launch_gather(gp, s->d, s->kv_dtype == HA_BF16, st), "GATHER-ATT launch");
+    HA_LAUNCH(launch_gather(gp, s->d, s->kv_dtype == HA_BF16, st, true), "GATHER-ATT launch");
     HA_TRY(record(events, 3, st));
     if (sel_idx != nullptr) {
         CompactParams cp{};

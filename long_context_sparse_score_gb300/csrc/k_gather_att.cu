@@ -127,6 +127,14 @@ __global__ void __launch_bounds__(kGatherThreads, (D * sizeof(KT) <= 256) ? 5 : 
     const int n = checked_len(p.seq_lens, b, p.n_cap, p.err, report);
     const int nused = (p.mode == kSegmented) ? (n + p.seg_cap - 1) / p.seg_cap : 0;
 
+    // ---- the scaled query (an input: read before waiting for TOPK's output)
+    {
+        const int64_t qoff = (int64_t)b * p.q_sb + (int64_t)(g * p.G + hh) * p.q_sh;
+        for (int dd = tid; dd < D; dd += kGatherThreads) s_q[dd] = load_q(p.q, qoff + dd, p.q_bf16) * p.qscale;
+    }
+    pdl_launch_dependents();
+    pdl_wait();
+
     // ---- list length (and the segment prefix table), warp 0
     if (warp == 0) {
         int L = 0;
@@ -173,12 +181,7 @@ __global__ void __launch_bounds__(kGatherThreads, (D * sizeof(KT) <= 256) ? 5 : 
     const int r0 = split * p.rows_per_split;
     const int nrows = max(0, min(L, r0 + p.rows_per_split) - r0);
 
-    // ---- the scaled query, then this CTA's token indices (list positions
-    // [r0, r0 + nrows)) into shared memory
-    {
-        const int64_t qoff = (int64_t)b * p.q_sb + (int64_t)(g * p.G + hh) * p.q_sh;
-        for (int dd = tid; dd < D; dd += kGatherThreads) s_q[dd] = load_q(p.q, qoff + dd, p.q_bf16) * p.qscale;
-    }
+    // ---- this CTA's token indices (list positions [r0, r0 + nrows)) into shared memory
     {
         const int32_t* seg = (p.mode == kSegmented) ? p.seg_idx + (int64_t)head * p.nseg * p.seg_cap : nullptr;
         const int32_t* lst = (p.mode == kList) ? p.list_idx + (int64_t)head * p.list_cap : nullptr;
@@ -415,24 +418,23 @@ __global__ void __launch_bounds__(256) k_merge(const MergeParams p) {
 }
 
 template <int D, typename KT>
-cudaError_t launch_gather_t(const GatherParams& p, cudaStream_t st) {
+cudaError_t launch_gather_t(const GatherParams& p, cudaStream_t st, bool pdl) {
     using C = Cfg<D, KT>;
     const size_t smem = (size_t)C::OFF_TOKL + (size_t)(p.rows_per_split + p.nseg + 1) * sizeof(int);
     cudaError_t e = cudaFuncSetAttribute(k_gather_att<D, KT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)(p.B * p.Hq) * (unsigned)p.splits;
-    k_gather_att<D, KT><<<grid, kGatherThreads, smem, st>>>(p);
-    return cudaGetLastError();
+    return launch_ex(k_gather_att<D, KT>, dim3(grid), dim3(kGatherThreads), smem, st, pdl, p);
 }
 
 }  // namespace
 
-cudaError_t launch_gather(const GatherParams& p, int d, int kv_bf16, cudaStream_t st) {
-    if (d == 128 && kv_bf16) return launch_gather_t<128, __nv_bfloat16>(p, st);
-    if (d == 64 && kv_bf16) return launch_gather_t<64, __nv_bfloat16>(p, st);
-    if (d == 128 && !kv_bf16) return launch_gather_t<128, float>(p, st);
-    if (d == 64 && !kv_bf16) return launch_gather_t<64, float>(p, st);
+cudaError_t launch_gather(const GatherParams& p, int d, int kv_bf16, cudaStream_t st, bool pdl) {
+    if (d == 128 && kv_bf16) return launch_gather_t<128, __nv_bfloat16>(p, st, pdl);
+    if (d == 64 && kv_bf16) return launch_gather_t<64, __nv_bfloat16>(p, st, pdl);
+    if (d == 128 && !kv_bf16) return launch_gather_t<128, float>(p, st, pdl);
+    if (d == 64 && !kv_bf16) return launch_gather_t<64, float>(p, st, pdl);
     return cudaErrorInvalidValue;
 }
 

@@ -70,7 +70,7 @@ __device__ __forceinline__ uint32_t field(uint32_t w01, uint32_t w23, int e) {
 // ---------------------------------------------------------------- SCORE
 
 template <int TPT, bool WRITE_DIST>
-__global__ void __launch_bounds__(kScoreThreads, 3) k_score(const ScoreParams p) {
+__global__ void __launch_bounds__(kScoreThreads, 5) k_score(const ScoreParams p) {
     constexpr int C = kScoreThreads * TPT;
     constexpr int SC = 32 * TPT;
     // Histogram columns hist[bin][pair][lane], shared by the CTA's warps: lane l
@@ -86,6 +86,7 @@ __global__ void __launch_bounds__(kScoreThreads, 3) k_score(const ScoreParams p)
     const int b = bg / p.Hkv, g = bg % p.Hkv;
     const int n = checked_len(p.seq_lens, b, p.n_cap, p.err, c == 0 && g == 0 && tid == 0);
     const int head0 = b * p.Hq + g * p.G;
+    pdl_launch_dependents();
     if (c == 0 && p.counters != nullptr)
         for (int e = tid; e < p.G; e += kScoreThreads) p.counters[head0 + e] = 0u;
     const int c0 = c * C;
@@ -329,6 +330,8 @@ __global__ void __launch_bounds__(kScoreThreads, 4) k_select(const SelectParams 
     const uint32_t* row = p.k_sig + (int64_t)b * p.ks_sb + (int64_t)g * p.ks_sh;
     uint32_t code[TPT];
     load_codes_contig<TPT>(row, sbase, n, s_codes[warp], code);
+    pdl_launch_dependents();
+    pdl_wait();  // SCORE's thresholds are read below
 
     for (int hp = 0; hp < p.G; hp += kMaxHeadsPerPass) {
         const int nh = min(kMaxHeadsPerPass, p.G - hp);
@@ -466,16 +469,16 @@ cudaError_t launch_score(const ScoreParams& p, int batch_hkv, cudaStream_t st) {
     return p.dist != nullptr ? launch_score_t<true>(p, batch_hkv, st) : launch_score_t<false>(p, batch_hkv, st);
 }
 
-cudaError_t launch_select(const SelectParams& p, int batch_hkv, cudaStream_t st) {
+cudaError_t launch_select(const SelectParams& p, int batch_hkv, cudaStream_t st, bool pdl) {
     const dim3 grid((unsigned)batch_hkv * (unsigned)p.nchunks);
+    const dim3 block(kScoreThreads);
     switch (p.chunk / kScoreThreads) {
-        case 4: k_select<4><<<grid, kScoreThreads, 0, st>>>(p); break;
-        case 8: k_select<8><<<grid, kScoreThreads, 0, st>>>(p); break;
-        case 16: k_select<16><<<grid, kScoreThreads, 0, st>>>(p); break;
-        case 32: k_select<32><<<grid, kScoreThreads, 0, st>>>(p); break;
+        case 4: return launch_ex(k_select<4>, grid, block, 0, st, pdl, p);
+        case 8: return launch_ex(k_select<8>, grid, block, 0, st, pdl, p);
+        case 16: return launch_ex(k_select<16>, grid, block, 0, st, pdl, p);
+        case 32: return launch_ex(k_select<32>, grid, block, 0, st, pdl, p);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_compact(const CompactParams& p, int heads, cudaStream_t st) {
