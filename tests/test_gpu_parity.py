@@ -96,6 +96,42 @@ def test_all_codes_equal_take_first_m():
         assert np.array_equal(idx[0, h, :333], np.arange(333))
 
 
+WINDOW_CASES = [
+    # name, n, m, S, Lw, code pattern
+    ("quota_ends_in_sink_window", 5000, 700, 1000, 300, "equal"),
+    ("quota_ends_in_local_window", 5000, 900, 8, 300, "far_then_equal"),
+    ("windows_span_many_chunks", 20000, 500, 7000, 9000, "random"),
+    ("windows_meet_exactly", 6000, 100, 2500, 3500, "random"),
+    ("windows_and_ties_random_pool", 9000, 1200, 1500, 2500, "pool"),
+]
+
+
+@pytest.mark.parametrize("case", WINDOW_CASES, ids=[c[0] for c in WINDOW_CASES])
+def test_windows_across_chunks_and_tie_boundary(case):
+    """Windows that cover several chunks, and a tie quota that runs out inside a
+    chunk the sink or the local window reaches (chunks are 1,024 tokens here)."""
+    name, n, m, S, Lw, pattern = case
+    w = W().make_gqa(17, B=2, Hq=4, Hkv=1, d=128, n_cap=n, seq_lens=[n, n - 333], m=m, n_sink=S,
+                     n_local=Lw, device="cuda", name=name)
+    q0 = 0x0F0F0F0F
+    w.q_sig = torch.full_like(w.q_sig, q0)
+    if pattern == "equal":
+        w.k_sig = torch.full_like(w.k_sig, q0)
+    elif pattern == "far_then_equal":
+        ks = torch.full_like(w.k_sig, q0)
+        ks[..., :4000] = ~torch.tensor(q0, dtype=torch.int32)
+        w.k_sig = ks.contiguous()
+    elif pattern == "pool":
+        gen = torch.Generator(device="cuda").manual_seed(5)
+        pool = torch.tensor([q0, q0 ^ 1, q0 ^ 3, q0 ^ 0x70000000], dtype=torch.int32, device="cuda")
+        w.k_sig = pool[torch.randint(0, 4, w.k_sig.shape, generator=gen, device="cuda")].contiguous()
+    res = GH.run_decode(w)
+    assert res["status"] == 0, res["flags"]
+    hc = GH.HostCopy(w)
+    GH.check_selection(res, hc, all_heads(w), m)
+    GH.check_attention(res, hc, all_heads(w)[:4], m)
+
+
 def test_ragged_per_sequence_budget():
     lens = [4096, 9000, 1, 0, 12000, 6000]
     wl = W()
