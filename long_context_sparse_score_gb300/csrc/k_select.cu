@@ -419,23 +419,71 @@ __global__ void __launch_bounds__(kScoreThreads, 4) k_select(const SelectParams 
 
 // ---------------------------------------------------------------- compaction / histogram
 
-__global__ void __launch_bounds__(256) k_compact(const CompactParams p) {
+// One CTA per head: the segment counts are loaded together and scanned into a
+// prefix table in shared memory, then every output position finds its segment
+// by binary search (all loads independent), and the tail is padded with -1.
+constexpr int kCompactThreads = 256;
+
+__global__ void __launch_bounds__(kCompactThreads) k_compact(const CompactParams p) {
+    __shared__ int s_pre[kMaxSegments + 1];
+    __shared__ int s_wsum[kCompactThreads / 32];
     const int head = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int b = head / p.Hq;
     const int n = checked_len(p.seq_lens, b, p.n_cap, p.err, false);
     const int nused = (n + p.seg_cap - 1) / p.seg_cap;
     const int32_t* cnt = p.seg_cnt + (int64_t)head * p.nseg;
     const int32_t* seg = p.seg_idx + (int64_t)head * p.nseg * p.seg_cap;
     int32_t* dst = p.sel_idx + (int64_t)head * p.cap;
-    int base = 0;
-    for (int s = 0; s < nused; ++s) {
-        int k = cnt[s];
-        if (base + k > p.cap) k = p.cap - base;  // cannot happen for |I| <= cap
-        for (int t = threadIdx.x; t < k; t += blockDim.x) dst[base + t] = seg[(int64_t)s * p.seg_cap + t];
-        base += k;
+    int carry = 0;
+    for (int base = 0; base < nused; base += kCompactThreads) {
+        const int i = base + tid;
+        const int v = (i < nused) ? min(max(cnt[i], 0), p.seg_cap) : 0;
+        int x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) s_wsum[warp] = x;
+        __syncthreads();
+        int before = 0, total = 0;
+#pragma unroll
+        for (int w2 = 0; w2 < kCompactThreads / 32; ++w2) {
+            before += (w2 < warp) ? s_wsum[w2] : 0;
+            total += s_wsum[w2];
+        }
+        if (i < nused) s_pre[i] = carry + before + x - v;
+        carry += total;
+        __syncthreads();
     }
-    for (int t = base + threadIdx.x; t < p.cap; t += blockDim.x) dst[t] = -1;
-    if (threadIdx.x == 0) p.sel_cnt[head] = base;
+    if (tid == 0) s_pre[nused] = carry;
+    __syncthreads();
+    const int total = min(carry, p.cap);  // entries beyond cap cannot occur for |I| <= cap
+    constexpr int kB = 4;
+    for (int t0 = 0; t0 < total; t0 += kB * kCompactThreads) {
+        int tok[kB];
+#pragma unroll
+        for (int u = 0; u < kB; ++u) {
+            const int t = t0 + u * kCompactThreads + tid;
+            tok[u] = -1;
+            if (t < total) {
+                int lo = 0, hi = nused - 1;
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (s_pre[mid] <= t) lo = mid; else hi = mid - 1;
+                }
+                tok[u] = seg[(int64_t)lo * p.seg_cap + (t - s_pre[lo])];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kB; ++u) {
+            const int t = t0 + u * kCompactThreads + tid;
+            if (t < total) dst[t] = tok[u];
+        }
+    }
+    for (int t = total + tid; t < p.cap; t += kCompactThreads) dst[t] = -1;
+    if (tid == 0) p.sel_cnt[head] = total;
 }
 
 __global__ void __launch_bounds__(64) k_hist(const HistParams p) {
@@ -482,7 +530,7 @@ cudaError_t launch_select(const SelectParams& p, int batch_hkv, cudaStream_t st,
 }
 
 cudaError_t launch_compact(const CompactParams& p, int heads, cudaStream_t st) {
-    k_compact<<<heads, 256, 0, st>>>(p);
+    k_compact<<<heads, kCompactThreads, 0, st>>>(p);
     return cudaGetLastError();
 }
 
