@@ -324,26 +324,37 @@ def run_ours(args, world, rank, local):
     ms_step = elapsed_ms / K
     value = throughput(world, B * Hq, K, elapsed_ms)
 
-    # e2e: per-step query inputs from pinned host memory, results back to the host
-    q_h = w.q.cpu().pin_memory()
-    qs_h = w.q_sig.cpu().pin_memory()
-    sl_h = w.seq_lens.cpu().pin_memory()
-    out_h = torch.empty_like(out, device="cpu").pin_memory()
-    lse_h = torch.empty_like(lse, device="cpu").pin_memory()
-    q_d, qs_d, sl_d = torch.empty_like(w.q), torch.empty_like(w.q_sig), torch.empty_like(w.seq_lens)
-    h2d = q_h.numel() * q_h.element_size() + qs_h.numel() * 4 + sl_h.numel() * 4
-    d2h = out_h.numel() * 4 + lse_h.numel() * 4
+    # e2e: per-step query inputs from pinned host memory, results back to the host.
+    # The step's inputs travel as one packed buffer (q | q codes | sequence lengths:
+    # one host->device copy) and the results as one (out | lse: one device->host
+    # copy); the C entry point gets its arguments marshalled once.
+    qn, qsn, sln = w.q.numel() * w.q.element_size(), w.q_sig.numel() * 4, w.seq_lens.numel() * 4
+    in_h = torch.empty(qn + qsn + sln, dtype=torch.uint8).pin_memory()
+    in_h[:qn].copy_(w.q.cpu().contiguous().view(torch.uint8).view(-1))
+    in_h[qn:qn + qsn].copy_(w.q_sig.cpu().contiguous().view(torch.uint8).view(-1))
+    in_h[qn + qsn:].copy_(w.seq_lens.cpu().contiguous().view(torch.uint8).view(-1))
+    in_d = torch.empty_like(in_h, device=dev)
+    q_d = in_d[:qn].view(w.q.dtype).view(w.q.shape)
+    qs_d = in_d[qn:qn + qsn].view(torch.int32).view(w.q_sig.shape)
+    sl_d = in_d[qn + qsn:].view(torch.int32)
+    on, ln = out.numel() * 4, lse.numel() * 4
+    res_d = torch.empty(on + ln, dtype=torch.uint8, device=dev)
+    out_d = res_d[:on].view(torch.float32).view(out.shape)
+    lse_d = res_d[on:].view(torch.float32).view(lse.shape)
+    res_h = torch.empty_like(res_d, device="cpu").pin_memory()
+    h2d, d2h = in_h.numel(), res_h.numel()
     e2e_steps = max(3, min(K, 500))
+    stream = torch.cuda.current_stream()
+    in_ptrs = [t.data_ptr() for t in (q_d, qs_d, w.k_sig, w.K, w.V, sl_d)]
+    outs = [out_d.data_ptr(), lse_d.data_ptr()]
+    st_ptr = stream.cuda_stream
 
     def e2e_step():
-        q_d.copy_(q_h, non_blocking=True)
-        qs_d.copy_(qs_h, non_blocking=True)
-        sl_d.copy_(sl_h, non_blocking=True)
-        H.hash_attn_decode(shape, q_d, qs_d, w.k_sig, w.K, w.V, sl_d, None, w.m, w.n_sink,
-                           w.n_local, out, lse, None, None, workspace=ws)
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+        in_d.copy_(in_h, non_blocking=True)
+        H.hash_attn_decode(shape, *in_ptrs, None, w.m, w.n_sink, w.n_local, *outs, None, None, workspace=ws,
+                           stream=st_ptr)
+        res_h.copy_(res_d, non_blocking=True)
+        stream.synchronize()
 
     for _ in range(3):
         e2e_step()
@@ -353,7 +364,9 @@ def run_ours(args, world, rank, local):
         e2e_step()
     e2e_s = dist_max(world, time.perf_counter() - t0, dev)
     e2e_value = world * B * Hq * e2e_steps / e2e_s
-    if not torch.allclose(out_h, out.cpu()):
+    out_h = res_h[:on].view(torch.float32).view(out.shape)
+    lse_h = res_h[on:].view(torch.float32).view(lse.shape)
+    if not (torch.equal(out_h, out.cpu()) and torch.equal(lse_h, lse.cpu())):
         raise RuntimeError("e2e output mismatch")
 
     if rank != 0:
@@ -384,7 +397,7 @@ def run_ours(args, world, rank, local):
         "gpu_launches": 3 * K,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps,
-                "note": "per step: q, q_sig, seq_lens host->device, decode, out+lse device->host, "
+                "note": "per step: q, q_sig, seq_lens host->device (one packed pinned buffer), decode, out+lse device->host (one buffer), "
                         "stream sync; KV cache and key codes are device-resident state"},
         "clocks": clocks,
     }
