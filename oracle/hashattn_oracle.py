@@ -25,6 +25,8 @@ Everything is NumPy in float64 (signature work in Python/NumPy integers), one
       A(q) = sum_j e^{s_j} v_j / sum_j e^{s_j}.
     - Eqs. (3.4)-(3.5): ATT_full = (e^alpha A + N_loc) / (e^alpha + Z_loc); the
       split of the softmax sum is exact; gate form g = sigmoid(a - log Z_loc).
+    - Sec. 3 (virtual logit/value pair): any number of segments merge the same
+      way (``merge_segments``).
 
 Readings where the pages are silent (each is listed in the design notes):
   * keep the m SMALLEST Hamming distances (SCORE is the negated distance);
@@ -161,6 +163,27 @@ def merge_gate(out_a, lse_a, out_loc, lse_loc):
     """Nectar, Eq. (3.5) gate form: g = sigmoid(lse_a - lse_loc); g*A + (1-g)*A_loc."""
     g = 1.0 / (1.0 + math.exp(-(lse_a - lse_loc)))
     return g * np.asarray(out_a, dtype=np.float64) + (1.0 - g) * np.asarray(out_loc, dtype=np.float64)
+
+
+def merge_segments(outs, lses):
+    """Exact merge of any number of partial attentions over disjoint token sets.
+
+    Nectar, Sec. 3: a segment whose scores are not materialised enters the
+    softmax as one virtual logit lse_s with value out_s; with Eq. (3.4) applied to
+    every segment, L = log sum_s e^{lse_s} and out = sum_s e^{lse_s - L} out_s.
+    ``outs`` [k, d] (k >= 1), ``lses`` [k]; segments with lse = -inf contribute
+    nothing, and if all are empty the result is (zeros, -inf).
+    """
+    outs = np.asarray(outs, dtype=np.float64)
+    lse_list = [float(x) for x in np.asarray(lses, dtype=np.float64).reshape(-1)]
+    live = [s for s, l in enumerate(lse_list) if l != -math.inf]
+    if not live:
+        return np.zeros(outs.shape[-1], dtype=np.float64), -math.inf
+    peak = max(lse_list[s] for s in live)
+    mass = [math.exp(lse_list[s] - peak) for s in live]
+    norm = sum(mass)
+    merged = sum(m_s * outs[s] for m_s, s in zip(mass, live)) / norm
+    return merged, peak + math.log(norm)
 
 
 # ---------------------------------------------------------------------------

@@ -321,6 +321,34 @@ def check_merge_partition(o):
     assert lm == -math.inf and np.all(om == 0)
 
 
+def check_merge_segments(o):
+    """Nectar Sec. 3 / Eq. (3.4) over k segments: merging the parts of any partition
+    of I (some parts empty) gives attention over I; segment order does not matter."""
+    rng = np.random.default_rng(41)
+    for trial in range(25):
+        n, d = int(rng.integers(1, 160)), 16
+        q, K, V = _rand_qkv(rng, n, d)
+        q *= 1.5
+        k = int(rng.integers(1, 7))
+        label = rng.integers(0, k, n)  # a part may get no token
+        parts = [np.flatnonzero(label == s) for s in range(k)]
+        res = [o.attend(q, K, V, p) for p in parts]
+        outs = np.stack([r[0] for r in res])
+        lses = np.array([r[1] for r in res])
+        o_all, l_all = o.attend(q, K, V, np.arange(n))
+        om, lm = o.merge_segments(outs, lses)
+        assert np.allclose(om, o_all, rtol=1e-12, atol=1e-12)
+        assert abs(lm - l_all) < 1e-12 * max(1.0, abs(l_all))
+        perm = rng.permutation(k)
+        om2, lm2 = o.merge_segments(outs[perm], lses[perm])
+        assert np.allclose(om2, om, rtol=1e-12, atol=1e-12) and abs(lm2 - lm) < 1e-12 * max(1.0, abs(lm))
+    # one segment is returned as it is; all-empty segments give (0, -inf)
+    om, lm = o.merge_segments(outs[:1], lses[:1])
+    assert np.allclose(om, outs[0]) and lm == lses[0]
+    om, lm = o.merge_segments(np.ones((3, d)), np.full(3, -math.inf))
+    assert lm == -math.inf and np.all(om == 0)
+
+
 def check_decode_composition(o):
     """decode_head = attend over selected_set, and decode_batch maps h to KV head h // G."""
     rng = np.random.default_rng(37)
@@ -353,7 +381,7 @@ ALL_CHECKS = [
     check_topm_bruteforce, check_topm_ties, check_windows, check_budget,
     check_dense_vs_sdpa, check_decimal, check_weighted_sum, check_lse_bounds,
     check_lse_gradient, check_low_temperature, check_empty,
-    check_merge_partition, check_decode_composition,
+    check_merge_partition, check_merge_segments, check_decode_composition,
 ]
 
 

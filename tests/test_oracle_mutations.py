@@ -41,6 +41,9 @@ MUTATIONS = [
     ("gate_sign_flipped", "g = 1.0 / (1.0 + math.exp(-(lse_a - lse_loc)))",
      "g = 1.0 / (1.0 + math.exp(lse_a - lse_loc))"),
     ("gqa_head_modulo", "g = h // G", "g = h % Hkv"),
+    ("merge_segments_mean_not_mass", "merged = sum(m_s * outs[s] for m_s, s in zip(mass, live)) / norm",
+     "merged = sum(outs[s] for s in live) / len(live)"),
+    ("merge_segments_lse_without_peak", "return merged, peak + math.log(norm)", "return merged, math.log(norm)"),
 ]
 
 
