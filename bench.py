@@ -178,6 +178,37 @@ def profiled_traffic():
         return None
 
 
+# ---------------------------------------------------------------- next rows
+
+def measure_merge_n(dev, peak):
+    """The multi-segment (out, lse) merge on a size larger than L2: 4 segments of
+    65,536 rows x d=128 (any partition of heads' token sets); algorithmic bytes =
+    every segment read once + the result written once."""
+    import torch
+    from long_context_sparse_score_gb300 import hashattn as H
+    nseg, rows, d = 4, 65536, 128
+    g = torch.Generator(device=dev).manual_seed(77)
+    outs = torch.randn((nseg, rows, d), generator=g, device=dev)
+    lses = torch.randn((nseg, rows), generator=g, device=dev) * 4
+    out = torch.empty((rows, d), device=dev)
+    lse = torch.empty(rows, device=dev)
+    for _ in range(3):
+        H.hash_attn_merge_n(outs, lses, out, lse)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 20
+    e0.record()
+    for _ in range(reps):
+        H.hash_attn_merge_n(outs, lses, out, lse)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    nbytes = (nseg + 1) * rows * (d + 1) * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"kernel": "k_merge_n", "segments": nseg, "rows": rows, "d": d, "bytes_per_launch": nbytes,
+            "ms_per_launch": ms, "achieved_gbs": gbs, "frac_of_peak": gbs / peak, "bound": "hbm"}
+
+
 # ---------------------------------------------------------------- workload helpers
 
 def algorithmic_bytes(w, sel_idx, sel_cnt):
@@ -400,6 +431,7 @@ def run_ours(args, world, rank, local):
                 "note": "per step: q, q_sig, seq_lens host->device (one packed pinned buffer), decode, out+lse device->host (one buffer), "
                         "stream sync; KV cache and key codes are device-resident state"},
         "clocks": clocks,
+        "next": {"merge_n": measure_merge_n(dev, peak)},
     }
     if not args.no_cpu_baseline:
         cpu_s, cpu_heads, res = run_cpu_oracle(w, args.cpu_heads)

@@ -233,6 +233,27 @@ ha_status hash_attn_merge(const float* out_a, const float* lse_a, const float* o
                           void* stream);
 
 /*
+ * Exact merge of nseg partial attentions over disjoint token sets, row by row
+ * (Nectar Sec. 3: each segment enters the softmax as one virtual logit lse_s
+ * with value out_s; Eq. (3.4) applied to every segment):
+ * L = log sum_s e^{lse_s}, out = sum_s e^{lse_s - L} out_s. Segments with
+ * lse = -inf contribute nothing; rows where all are -inf give out = 0,
+ * lse = -inf. Composes a sparse document segment, a dense local segment and
+ * generated-token segments in one call.
+ *   outs  float32, segment s row r dim k at outs[s * out_seg_stride + r * d + k]
+ *   lses  float32, segment s row r at lses[s * lse_seg_stride + r]
+ *   out [rows, d], lse [rows] float32 (device). out may alias the rows of one
+ *   segment (each element is read before it is written); lse likewise.
+ *   nseg >= 1; out_seg_stride >= rows * d and lse_seg_stride >= rows.
+ * Errors: HA_ERR_INVALID_ARG (null pointers, nseg < 1, rows < 0, d < 1,
+ * strides that overlap segments) before anything is enqueued; rows == 0 does
+ * nothing.
+ */
+ha_status hash_attn_merge_n(const float* outs, int64_t out_seg_stride, const float* lses,
+                            int64_t lse_seg_stride, int32_t nseg, float* out, float* lse, int32_t rows,
+                            int32_t d, void* stream);
+
+/*
  * Synchronise `stream`, read and clear the workspace's device error word.
  * Returns HA_OK, HA_ERR_TIMEOUT (timeout flag set) or HA_ERR_DEVICE (any other
  * flag); *flags (optional) receives the raw HA_DEVERR_* bits.

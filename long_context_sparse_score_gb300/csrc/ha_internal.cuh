@@ -150,6 +150,14 @@ struct MergeParams {
     int rows, d;
 };
 
+struct MergeNParams {
+    const float* outs; int64_t out_seg_stride;
+    const float* lses; int64_t lse_seg_stride;
+    int nseg;
+    float* out; float* lse;
+    int rows, d;
+};
+
 // Launch with (pdl = true) or without programmatic stream serialization.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
@@ -174,6 +182,7 @@ cudaError_t launch_compact(const CompactParams& p, int heads, cudaStream_t st);
 cudaError_t launch_hist(const HistParams& p, int heads, cudaStream_t st);
 cudaError_t launch_gather(const GatherParams& p, int d, int kv_bf16, cudaStream_t st, bool pdl = false);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t st);
+cudaError_t launch_merge_n(const MergeNParams& p, cudaStream_t st);
 
 // ------------------------------------------------------------------ device helpers
 

@@ -520,6 +520,19 @@ ha_status hash_attn_merge(const float* out_a, const float* lse_a, const float* o
     return HA_OK;
 }
 
+ha_status hash_attn_merge_n(const float* outs, int64_t out_seg_stride, const float* lses, int64_t lse_seg_stride,
+                            int32_t nseg, float* out, float* lse, int32_t rows, int32_t d, void* stream) {
+    if (nseg < 1 || rows < 0 || d < 1) return fail(HA_ERR_INVALID_ARG, "nseg must be >= 1, rows >= 0 and d >= 1");
+    if (rows == 0) return HA_OK;
+    if (!outs || !lses || !out || !lse) return fail(HA_ERR_INVALID_ARG, "merge pointers must not be NULL");
+    if (nseg > 1 && (out_seg_stride < (int64_t)rows * d || lse_seg_stride < rows))
+        return fail(HA_ERR_INVALID_ARG, "segment strides overlap (out %lld < %lld or lse %lld < %d)",
+                    (long long)out_seg_stride, (long long)rows * d, (long long)lse_seg_stride, rows);
+    MergeNParams p{outs, out_seg_stride, lses, lse_seg_stride, nseg, out, lse, rows, d};
+    HA_LAUNCH(launch_merge_n(p, static_cast<cudaStream_t>(stream)), "merge launch");
+    return HA_OK;
+}
+
 ha_status hash_attn_device_status(void* workspace, void* stream, uint32_t* flags) {
     if (workspace == nullptr) return fail(HA_ERR_WORKSPACE, "workspace is NULL");
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -38,7 +38,8 @@ HA_NOALLOC_SCRATCH_BYTES = 16 << 20
 EXPORTED = [
     "hash_attn_workspace_size", "hash_attn_workspace_init", "hash_attn_select_capacity",
     "hash_attn_decode", "hash_attn_decode_timed", "hash_attn_score", "hash_attn_select",
-    "hash_attn_gather_att", "hash_attn_gather_att_noalloc", "hash_attn_merge", "hash_attn_device_status",
+    "hash_attn_gather_att", "hash_attn_gather_att_noalloc", "hash_attn_merge", "hash_attn_merge_n",
+    "hash_attn_device_status",
     "hash_attn_status_string", "hash_attn_last_error",
 ]
 
@@ -92,6 +93,7 @@ def lib() -> ctypes.CDLL:
     L.hash_attn_gather_att.argtypes = [SP, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P, _SZ, _P]
     L.hash_attn_gather_att_noalloc.argtypes = [SP, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P, _P]
     L.hash_attn_merge.argtypes = [_P, _P, _P, _P, _P, _P, _I32, _I32, _P]
+    L.hash_attn_merge_n.argtypes = [_P, ctypes.c_int64, _P, ctypes.c_int64, _I32, _P, _P, _I32, _I32, _P]
     L.hash_attn_device_status.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_uint32)]
     L.hash_attn_status_string.argtypes = [_I32]
     L.hash_attn_status_string.restype = ctypes.c_char_p
@@ -242,6 +244,16 @@ def hash_attn_gather_att_noalloc(shape, q, K, V, seq_lens, idx, idx_cap, cnt, ou
 def hash_attn_merge(out_a, lse_a, out_b, lse_b, out, lse, rows: int, d: int, stream=None) -> None:
     _check(lib().hash_attn_merge(_ptr(out_a), _ptr(lse_a), _ptr(out_b), _ptr(lse_b), _ptr(out),
                                  _ptr(lse), rows, d, _stream(stream)))
+
+
+def hash_attn_merge_n(outs, lses, out, lse, stream=None) -> None:
+    """``outs`` [nseg, rows, d] and ``lses`` [nseg, rows] float32 (rows contiguous
+    within a segment; any segment stride); ``out`` [rows, d], ``lse`` [rows]."""
+    nseg, rows, d = outs.shape
+    if tuple(lses.shape) != (nseg, rows) or outs.stride(1) != d or outs.stride(2) != 1 or lses.stride(1) != 1:
+        raise ValueError("outs must be [nseg, rows, d] with contiguous rows and lses [nseg, rows]")
+    _check(lib().hash_attn_merge_n(_ptr(outs), outs.stride(0), _ptr(lses), lses.stride(0), nseg, _ptr(out),
+                                   _ptr(lse), rows, d, _stream(stream)))
 
 
 def hash_attn_device_status(workspace, stream=None) -> tuple[int, int]:

@@ -302,6 +302,37 @@ def test_merge_entry_point():
     assert torch.allclose(A, out) and torch.equal(LA.isinf(), lse.isinf())
 
 
+@pytest.mark.parametrize("nseg,d", [(1, 128), (2, 64), (3, 128), (5, 128)])
+def test_merge_n_entry_point(nseg, d):
+    """Multi-segment merge against the oracle: empty segments and empty rows, a
+    padded segment stride, and the output aliasing segment 0."""
+    H = GH.ha()
+    rng = np.random.default_rng(10 + nseg)
+    rows = 41
+    outs = rng.standard_normal((nseg, rows + 3, d)).astype(np.float32)  # 3 padding rows per segment
+    lses = (rng.standard_normal((nseg, rows + 5)) * 4).astype(np.float32)
+    lses[0, 2] = -np.inf
+    lses[:, 9] = -np.inf
+    if nseg > 1:
+        lses[nseg - 1, 11:20] = -np.inf
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    O_d, L_d = t(outs), t(lses)
+    ov, lv = O_d[:, :rows], L_d[:, :rows]   # views with segment strides (rows + 3) * d and rows + 5
+    out = torch.empty((rows, d), device="cuda")
+    lse = torch.empty(rows, device="cuda")
+    H.hash_attn_merge_n(ov, lv, out, lse)
+    torch.cuda.synchronize()
+    for r in range(rows):
+        ro, rl = O.merge_segments(outs[:, r], lses[:, r])
+        GH.assert_out_close(out[r].cpu().numpy(), ro, f"row {r}")
+        GH.assert_lse_close(float(lse[r]), rl, f"row {r}")
+    assert torch.all(out[9] == 0) and bool(lse[9].isneginf())
+    # in place: the result overwrites segment 0
+    H.hash_attn_merge_n(ov, lv, ov[0], lv[0])
+    torch.cuda.synchronize()
+    assert torch.allclose(ov[0], out) and torch.equal(lv[0].isinf(), lse.isinf())
+
+
 def test_device_errors_are_flagged_not_faulted():
     H = GH.ha()
     w = W().make_gqa(16, B=3, Hq=4, Hkv=2, d=128, n_cap=2000, seq_lens=[2000, 1500, 2000], m=100,

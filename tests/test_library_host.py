@@ -117,6 +117,13 @@ def test_other_entry_points_reject_bad_arguments(ha):
     assert L.hash_attn_merge(512, 512, 512, 512, 512, 512, -1, 128, None) == ha.HA_ERR_INVALID_ARG
     assert L.hash_attn_merge(None, 512, 512, 512, 512, 512, 4, 128, None) == ha.HA_ERR_INVALID_ARG
     assert L.hash_attn_merge(None, None, None, None, None, None, 0, 128, None) == ha.HA_OK  # nothing to do
+    # multi-segment merge: segment count, row/dim bounds, overlapping strides, nulls
+    assert L.hash_attn_merge_n(512, 512, 512, 512, 0, 512, 512, 4, 128, None) == ha.HA_ERR_INVALID_ARG
+    assert L.hash_attn_merge_n(512, 4 * 128 - 1, 512, 4, 3, 512, 512, 4, 128, None) == ha.HA_ERR_INVALID_ARG
+    assert L.hash_attn_merge_n(512, 4 * 128, 512, 3, 3, 512, 512, 4, 128, None) == ha.HA_ERR_INVALID_ARG
+    assert L.hash_attn_merge_n(None, 512, 512, 4, 3, 512, 512, 4, 128, None) == ha.HA_ERR_INVALID_ARG
+    assert L.hash_attn_merge_n(512, 512, 512, 4, 2, 512, 512, 4, 0, None) == ha.HA_ERR_INVALID_ARG
+    assert L.hash_attn_merge_n(None, 0, None, 0, 2, None, None, 0, 128, None) == ha.HA_OK  # nothing to do
     assert L.hash_attn_device_status(None, None, None) == ha.HA_ERR_WORKSPACE
     assert L.hash_attn_workspace_init(None, 16, None) == ha.HA_ERR_WORKSPACE
     events = (ctypes.c_void_p * 4)(None, None, None, None)
