@@ -16,6 +16,8 @@ Everything is NumPy in float64 (signature work in Python/NumPy integers), one
       three stages SCORE / TOPK / GATHER-ATT.
     - "A 32-bit signature makes scoring cheap" (Eqs. (1)-(2), Sec. 4.1):
       SCORE(k_i, q) = -popcount(h_i XOR h_q).
+    - Sec. 4.1: the signature is ReLU(sign(.)) of a projection of q or k
+      (``encode``; bit j set iff projection j is positive).
     - "Token-level sparsity still needs a careful kernel" (Sec. 4.4, budget
       accounting): the retrieval budget m is joined by the first and the most
       recent tokens of the context.
@@ -71,6 +73,37 @@ def hamming_distances(q_code, k_codes) -> np.ndarray:
     q = np.int64(int(q_code) & 0xFFFFFFFF)
     k = np.asarray(k_codes).astype(np.int64) & 0xFFFFFFFF
     return popcount32(k ^ q)
+
+
+def encode(x, W) -> int:
+    """32-bit code of vector x under the projection W [32, d].
+
+    HashAttention, Sec. 4.1: the signature is ReLU(sign(F(x))), so bit j is 1 iff
+    the j-th projection is positive (0 maps to bit 0). F is the learned map on the
+    pages; a given linear W (sign random projection) stands in for it here.
+    Decided in float64.
+    """
+    proj = np.asarray(W, dtype=np.float64) @ np.asarray(x, dtype=np.float64)
+    code = 0
+    for j in range(32):
+        if proj[j] > 0.0:
+            code |= 1 << j
+    return code
+
+
+def encode_ambiguous(x, W, eps: float = 2.0 ** -22) -> int:
+    """Bits of ``encode`` that float32 arithmetic may decide either way: those whose
+    projection lies within d * eps * sum_k |W_jk x_k| of zero (a bound on the
+    rounding error of any float32 summation order)."""
+    W = np.asarray(W, dtype=np.float64)
+    x = np.asarray(x, dtype=np.float64)
+    proj = W @ x
+    bound = W.shape[1] * eps * (np.abs(W) @ np.abs(x))
+    mask = 0
+    for j in range(32):
+        if abs(proj[j]) <= bound[j]:
+            mask |= 1 << j
+    return mask
 
 
 def distance_histogram(dist) -> np.ndarray:

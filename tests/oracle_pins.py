@@ -349,6 +349,37 @@ def check_merge_segments(o):
     assert lm == -math.inf and np.all(om == 0)
 
 
+def check_encode(o):
+    """Sign-projection codes: a worked 2-d example, identity projections (bit j is
+    the sign of x_j), x = 0 gives 0 (sign(0) maps to bit 0), sign symmetry, positive
+    scaling, and row permutations of W permuting the bits."""
+    W2 = np.zeros((32, 2))
+    W2[0] = (1.0, 1.0)
+    W2[1] = (1.0, -1.0)
+    assert o.encode(np.array([1.0, 0.5]), W2) == 0b11       # projections (1.5, 0.5)
+    assert o.encode(np.array([0.5, 1.0]), W2) == 0b01       # projections (1.5, -0.5)
+    rng = np.random.default_rng(43)
+    d = 32
+    x = rng.standard_normal(d)
+    want = sum(1 << j for j in range(32) if x[j] > 0)
+    assert o.encode(x, np.eye(32)) == want
+    W = rng.standard_normal((32, 48))
+    assert o.encode(np.zeros(48), W) == 0
+    for _ in range(20):
+        v = rng.standard_normal(48)
+        c = o.encode(v, W)
+        assert o.encode(-v, W) == (~c) & 0xFFFFFFFF          # no projection is exactly 0 here
+        assert o.encode(3.7 * v, W) == c
+        perm = rng.permutation(32)
+        cp = o.encode(v, W[perm])
+        assert all(((cp >> j) & 1) == ((c >> perm[j]) & 1) for j in range(32))
+    # the ambiguity mask flags exactly the bits whose projection is (near) zero
+    Wz = np.eye(32)
+    xz = np.ones(32)
+    xz[5] = 0.0
+    assert o.encode_ambiguous(xz, Wz) == 1 << 5
+
+
 def check_decode_composition(o):
     """decode_head = attend over selected_set, and decode_batch maps h to KV head h // G."""
     rng = np.random.default_rng(37)
@@ -381,7 +412,7 @@ ALL_CHECKS = [
     check_topm_bruteforce, check_topm_ties, check_windows, check_budget,
     check_dense_vs_sdpa, check_decimal, check_weighted_sum, check_lse_bounds,
     check_lse_gradient, check_low_temperature, check_empty,
-    check_merge_partition, check_merge_segments, check_decode_composition,
+    check_merge_partition, check_merge_segments, check_encode, check_decode_composition,
 ]
 
 
