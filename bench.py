@@ -209,6 +209,43 @@ def measure_merge_n(dev, peak):
             "ms_per_launch": ms, "achieved_gbs": gbs, "frac_of_peak": gbs / peak, "bound": "hbm"}
 
 
+def measure_encode(w, shape, dev):
+    """Sign-projection codes of the step's queries (B x Hq vectors) and of one
+    appended key per (sequence, KV head), at the bench shape."""
+    import torch
+    from long_context_sparse_score_gb300 import hashattn as H
+    g = torch.Generator(device=dev).manual_seed(78)
+    W = torch.randn((w.Hkv, 32, w.d), generator=g, device=dev)
+    q_sig = torch.empty_like(w.q_sig)
+    k_sig = w.k_sig.clone()
+    pos = (w.seq_lens - 1).to(torch.int32)
+    reps = 50
+    graphs = []
+    for call in (lambda: H.hash_attn_encode_queries(shape, w.q, W, q_sig),
+                 lambda: H.hash_attn_encode_keys(shape, w.K, W, pos, k_sig)):
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()  # the launches replay without host overhead: device time per call
+        with torch.cuda.graph(gr):
+            for _ in range(reps):
+                call()
+        graphs.append(gr)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    for gr in graphs:
+        gr.replay()
+    torch.cuda.synchronize()
+    ev[0].record()
+    graphs[0].replay()
+    ev[1].record()
+    graphs[1].replay()
+    ev[2].record()
+    torch.cuda.synchronize()
+    return {"kernel": "k_encode", "query_vectors": w.B * w.Hq, "key_vectors": w.B * w.Hkv, "d": w.d,
+            "queries_us": ev[0].elapsed_time(ev[1]) * 1e3 / reps, "keys_us": ev[1].elapsed_time(ev[2]) * 1e3 / reps,
+            "bound": "latency (32 x d GEMV per vector)", "timing": "CUDA graph of 50 launches"}
+
+
 # ---------------------------------------------------------------- workload helpers
 
 def algorithmic_bytes(w, sel_idx, sel_cnt):
@@ -431,7 +468,7 @@ def run_ours(args, world, rank, local):
                 "note": "per step: q, q_sig, seq_lens host->device (one packed pinned buffer), decode, out+lse device->host (one buffer), "
                         "stream sync; KV cache and key codes are device-resident state"},
         "clocks": clocks,
-        "next": {"merge_n": measure_merge_n(dev, peak)},
+        "next": {"merge_n": measure_merge_n(dev, peak), "encode": measure_encode(w, shape, dev)},
     }
     if not args.no_cpu_baseline:
         cpu_s, cpu_heads, res = run_cpu_oracle(w, args.cpu_heads)

@@ -233,6 +233,37 @@ ha_status hash_attn_merge(const float* out_a, const float* lse_a, const float* o
                           void* stream);
 
 /*
+ * Codes of the decode step's queries by sign projection (HashAttention Sec. 4.1:
+ * the signature is ReLU(sign(.)) of a projection, so bit j is 1 iff projection j
+ * is positive; a given 32 x d projection per KV head stands in for the learned
+ * map): q_sig[b, h] = code of q[b, h, :] under W[h / G].
+ *   q      per shape (q_dtype, q_sb, q_sh), device
+ *   W      float32 [h_kv, 32, d] contiguous, device
+ *   q_sig  uint32 [batch, h_q] contiguous, device (written)
+ * Projections accumulate in float32 (four interleaved partial sums over the
+ * dims, a fixed order, so results are reproducible).
+ * Errors: HA_ERR_INVALID_ARG / HA_ERR_UNSUPPORTED (shape, NULL pointers) before
+ * anything is enqueued.
+ */
+ha_status hash_attn_encode_queries(const ha_shape* shape, const void* q, const float* W, uint32_t* q_sig,
+                                   void* stream);
+
+/*
+ * Append the newly cached tokens' key codes: for every batch entry b and KV head
+ * g with 0 <= pos[b] < n_cap, k_sig[b, g, pos[b]] = code of K[b, g, pos[b], :]
+ * under W[g] (same rule as hash_attn_encode_queries). Nothing else of k_sig is
+ * touched; an entry with pos[b] outside [0, n_cap) is skipped and, when
+ * dev_flags is given, HA_DEVERR_INDEX is OR-ed into *dev_flags (device uint32).
+ *   K      per shape (kv_dtype, k_sb, k_sh, k_sn), device
+ *   W      float32 [h_kv, 32, d] contiguous, device
+ *   pos    int32 [batch], device
+ *   k_sig  per shape (ks_sb, ks_sh), device
+ * Errors: HA_ERR_INVALID_ARG / HA_ERR_UNSUPPORTED before anything is enqueued.
+ */
+ha_status hash_attn_encode_keys(const ha_shape* shape, const void* K, const float* W, const int32_t* pos,
+                                uint32_t* k_sig, uint32_t* dev_flags, void* stream);
+
+/*
  * Exact merge of nseg partial attentions over disjoint token sets, row by row
  * (Nectar Sec. 3: each segment enters the softmax as one virtual logit lse_s
  * with value out_s; Eq. (3.4) applied to every segment):

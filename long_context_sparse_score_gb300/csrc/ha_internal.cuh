@@ -150,6 +150,22 @@ struct MergeParams {
     int rows, d;
 };
 
+// Sign-projection codes of query vectors (keys == 0: codes[b * Hq + h] from
+// x[b, h] under W[h / G]) or of appended keys (keys == 1: codes[b, g, pos[b]]
+// from x[b, g, pos[b]] under W[g]; element strides x_sb/x_sh/x_sn, code strides
+// c_sb/c_sh).
+struct EncodeParams {
+    const void* x;
+    int x_bf16;
+    int64_t x_sb, x_sh, x_sn;
+    const float* W;          // [Hkv][32][d]
+    uint32_t* codes;
+    int64_t c_sb, c_sh;
+    const int32_t* pos;      // keys only
+    uint32_t* flags;         // optional (keys): HA_DEVERR_INDEX for a position outside [0, n_cap)
+    int B, Hq, Hkv, G, d, n_cap, keys;
+};
+
 struct MergeNParams {
     const float* outs; int64_t out_seg_stride;
     const float* lses; int64_t lse_seg_stride;
@@ -183,6 +199,7 @@ cudaError_t launch_hist(const HistParams& p, int heads, cudaStream_t st);
 cudaError_t launch_gather(const GatherParams& p, int d, int kv_bf16, cudaStream_t st, bool pdl = false);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t st);
 cudaError_t launch_merge_n(const MergeNParams& p, cudaStream_t st);
+cudaError_t launch_encode(const EncodeParams& p, cudaStream_t st);
 
 // ------------------------------------------------------------------ device helpers
 

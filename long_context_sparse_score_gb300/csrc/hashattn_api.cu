@@ -533,6 +533,57 @@ ha_status hash_attn_merge_n(const float* outs, int64_t out_seg_stride, const flo
     return HA_OK;
 }
 
+ha_status hash_attn_encode_queries(const ha_shape* shape, const void* q, const float* W, uint32_t* q_sig,
+                                   void* stream) {
+    HA_TRY(check_shape(shape));
+    if (q == nullptr || W == nullptr || q_sig == nullptr)
+        return fail(HA_ERR_INVALID_ARG, "q, W and q_sig must not be NULL");
+    EncodeParams p{};
+    p.x = q;
+    p.x_bf16 = shape->q_dtype == HA_BF16;
+    p.x_sb = shape->q_sb;
+    p.x_sh = shape->q_sh;
+    p.W = W;
+    p.codes = q_sig;
+    p.B = shape->batch;
+    p.Hq = shape->h_q;
+    p.Hkv = shape->h_kv;
+    p.G = shape->h_q / shape->h_kv;
+    p.d = shape->d;
+    p.n_cap = shape->n_cap;
+    p.keys = 0;
+    HA_LAUNCH(launch_encode(p, static_cast<cudaStream_t>(stream)), "query encode launch");
+    return HA_OK;
+}
+
+ha_status hash_attn_encode_keys(const ha_shape* shape, const void* K, const float* W, const int32_t* pos,
+                                uint32_t* k_sig, uint32_t* dev_flags, void* stream) {
+    HA_TRY(check_shape(shape));
+    if (K == nullptr || W == nullptr || pos == nullptr || k_sig == nullptr)
+        return fail(HA_ERR_INVALID_ARG, "K, W, pos and k_sig must not be NULL");
+    EncodeParams p{};
+    p.x = K;
+    p.x_bf16 = shape->kv_dtype == HA_BF16;
+    p.x_sb = shape->k_sb;
+    p.x_sh = shape->k_sh;
+    p.x_sn = shape->k_sn;
+    p.W = W;
+    p.codes = k_sig;
+    p.c_sb = shape->ks_sb;
+    p.c_sh = shape->ks_sh;
+    p.pos = pos;
+    p.flags = dev_flags;
+    p.B = shape->batch;
+    p.Hq = shape->h_q;
+    p.Hkv = shape->h_kv;
+    p.G = shape->h_q / shape->h_kv;
+    p.d = shape->d;
+    p.n_cap = shape->n_cap;
+    p.keys = 1;
+    HA_LAUNCH(launch_encode(p, static_cast<cudaStream_t>(stream)), "key encode launch");
+    return HA_OK;
+}
+
 ha_status hash_attn_device_status(void* workspace, void* stream, uint32_t* flags) {
     if (workspace == nullptr) return fail(HA_ERR_WORKSPACE, "workspace is NULL");
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -39,6 +39,7 @@ EXPORTED = [
     "hash_attn_workspace_size", "hash_attn_workspace_init", "hash_attn_select_capacity",
     "hash_attn_decode", "hash_attn_decode_timed", "hash_attn_score", "hash_attn_select",
     "hash_attn_gather_att", "hash_attn_gather_att_noalloc", "hash_attn_merge", "hash_attn_merge_n",
+    "hash_attn_encode_queries", "hash_attn_encode_keys",
     "hash_attn_device_status",
     "hash_attn_status_string", "hash_attn_last_error",
 ]
@@ -94,6 +95,8 @@ def lib() -> ctypes.CDLL:
     L.hash_attn_gather_att_noalloc.argtypes = [SP, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P, _P]
     L.hash_attn_merge.argtypes = [_P, _P, _P, _P, _P, _P, _I32, _I32, _P]
     L.hash_attn_merge_n.argtypes = [_P, ctypes.c_int64, _P, ctypes.c_int64, _I32, _P, _P, _I32, _I32, _P]
+    L.hash_attn_encode_queries.argtypes = [SP, _P, _P, _P, _P]
+    L.hash_attn_encode_keys.argtypes = [SP, _P, _P, _P, _P, _P, _P]
     L.hash_attn_device_status.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_uint32)]
     L.hash_attn_status_string.argtypes = [_I32]
     L.hash_attn_status_string.restype = ctypes.c_char_p
@@ -254,6 +257,17 @@ def hash_attn_merge_n(outs, lses, out, lse, stream=None) -> None:
         raise ValueError("outs must be [nseg, rows, d] with contiguous rows and lses [nseg, rows]")
     _check(lib().hash_attn_merge_n(_ptr(outs), outs.stride(0), _ptr(lses), lses.stride(0), nseg, _ptr(out),
                                    _ptr(lse), rows, d, _stream(stream)))
+
+
+def hash_attn_encode_queries(shape, q, W, q_sig, stream=None) -> None:
+    """q_sig[b, h] = sign-projection code of q[b, h] under W[h // G] (W float32 [h_kv, 32, d])."""
+    _check(lib().hash_attn_encode_queries(ctypes.byref(shape), _ptr(q), _ptr(W), _ptr(q_sig), _stream(stream)))
+
+
+def hash_attn_encode_keys(shape, K, W, pos, k_sig, dev_flags=None, stream=None) -> None:
+    """k_sig[b, g, pos[b]] = code of K[b, g, pos[b]] under W[g], for pos[b] in [0, n_cap)."""
+    _check(lib().hash_attn_encode_keys(ctypes.byref(shape), _ptr(K), _ptr(W), _ptr(pos), _ptr(k_sig),
+                                       _ptr(dev_flags), _stream(stream)))
 
 
 def hash_attn_device_status(workspace, stream=None) -> tuple[int, int]:

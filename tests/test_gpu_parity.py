@@ -333,6 +333,50 @@ def test_merge_n_entry_point(nseg, d):
     assert torch.allclose(ov[0], out) and torch.equal(lv[0].isinf(), lse.isinf())
 
 
+@pytest.mark.parametrize("d,q_dtype", [(128, torch.float32), (128, torch.bfloat16), (64, torch.bfloat16)])
+def test_encode_queries_and_keys(d, q_dtype):
+    """Sign-projection codes against the oracle: every bit that float32 rounding
+    cannot flip must match; appended keys land at their positions only."""
+    H = GH.ha()
+    B, Hq, Hkv, n_cap = 3, 8, 2, 64
+    gen = torch.Generator(device="cuda").manual_seed(19 + d)
+    q = torch.randn((B, Hq, d), generator=gen, device="cuda").to(q_dtype)
+    K = torch.randn((B, Hkv, n_cap, d), generator=gen, device="cuda").to(torch.bfloat16)
+    V = torch.zeros_like(K)
+    W = torch.randn((Hkv, 32, d), generator=gen, device="cuda")
+    k_sig = torch.full((B, Hkv, n_cap), 0x5A5A5A5A, dtype=torch.int32, device="cuda")
+    shape = H.make_shape(q, K, V, k_sig)
+    q_sig = torch.zeros((B, Hq), dtype=torch.int32, device="cuda")
+    H.hash_attn_encode_queries(shape, q, W, q_sig)
+    pos = torch.tensor([17, -1, n_cap - 1], dtype=torch.int32, device="cuda")
+    flags = torch.zeros(1, dtype=torch.int32, device="cuda")
+    before = k_sig.clone()
+    H.hash_attn_encode_keys(shape, K, W, pos, k_sig, flags)
+    torch.cuda.synchronize()
+    Wn = W.cpu().numpy().astype(np.float64)
+    qn = q.float().cpu().numpy()
+    Kn = K.float().cpu().numpy()
+    G = Hq // Hkv
+    got_q = q_sig.cpu().numpy().astype(np.int64) & 0xFFFFFFFF
+    for b in range(B):
+        for h in range(Hq):
+            ref = O.encode(qn[b, h], Wn[h // G])
+            amb = O.encode_ambiguous(qn[b, h], Wn[h // G])
+            assert (int(got_q[b, h]) ^ ref) & ~amb & 0xFFFFFFFF == 0, (b, h, hex(int(got_q[b, h])), hex(ref))
+    got_k = k_sig.cpu().numpy().astype(np.int64) & 0xFFFFFFFF
+    exp_k = before.cpu().numpy().astype(np.int64) & 0xFFFFFFFF
+    for b, p_ in enumerate([17, -1, n_cap - 1]):
+        for g in range(Hkv):
+            if p_ < 0:
+                continue
+            ref = O.encode(Kn[b, g, p_], Wn[g])
+            amb = O.encode_ambiguous(Kn[b, g, p_], Wn[g])
+            assert (int(got_k[b, g, p_]) ^ ref) & ~amb & 0xFFFFFFFF == 0, (b, g)
+            exp_k[b, g, p_] = got_k[b, g, p_]
+    assert np.array_equal(got_k, exp_k), "codes outside the appended positions changed"
+    assert int(flags.item()) & H.HA_DEVERR_INDEX
+
+
 def test_device_errors_are_flagged_not_faulted():
     H = GH.ha()
     w = W().make_gqa(16, B=3, Hq=4, Hkv=2, d=128, n_cap=2000, seq_lens=[2000, 1500, 2000], m=100,
