@@ -16,6 +16,8 @@ Everything is NumPy in float64 (signature work in Python/NumPy integers), one
       three stages SCORE / TOPK / GATHER-ATT.
     - "A 32-bit signature makes scoring cheap" (Eqs. (1)-(2), Sec. 4.1):
       SCORE(k_i, q) = -popcount(h_i XOR h_q).
+    - Sec. 5: the selection is compared with the exact top-k by attention score
+      (``top_m_by_dot``) through its recall (``recall``).
     - Sec. 4.1: the signature is ReLU(sign(.)) of a projection of q or k
       (``encode``; bit j set iff projection j is positive).
     - "Token-level sparsity still needs a careful kernel" (Sec. 4.4, budget
@@ -145,6 +147,50 @@ def selected_set(q_code, k_codes, n: int, m: int, n_sink: int, n_local: int) -> 
 def max_reads(n: int, m: int, n_sink: int, n_local: int) -> int:
     """Upper bound on |I|: the budget plus every fixed window position, capped at n."""
     return min(n, m + n_sink + n_local)
+
+
+# ---------------------------------------------------------------------------
+# The exact comparator of the selection -- HashAttention, Sec. 5 (oracle top-k
+# by attention score) and the recall of the hashed selection against it
+# ---------------------------------------------------------------------------
+
+def dot_scores(q, K, n: int) -> np.ndarray:
+    """<q, k_i> for the first n rows of K, in float64 (the ranking is that of z_i)."""
+    return np.asarray(K, dtype=np.float64)[:n] @ np.asarray(q, dtype=np.float64)
+
+
+def top_m_by_dot(q, K, n: int, m: int) -> np.ndarray:
+    """Indices of the min(m, n) largest <q, k_i>, ascending; ties go to the smaller index."""
+    z = dot_scores(q, K, n)
+    k = max(0, min(int(m), n))
+    order = np.lexsort((np.arange(n), -z))  # score descending, then index ascending
+    return np.sort(order[:k]).astype(np.int64)
+
+
+def top_m_band(q, K, n: int, m: int, eps: float = 2.0 ** -22):
+    """(sure, band): the tokens certainly in the top min(m, n) and those whose score
+    lies within the float32 rounding bound d * eps * sum_k |q_k k_ik| of the
+    min(m, n)-th largest score (either decision is valid for them)."""
+    q = np.asarray(q, dtype=np.float64)
+    Kf = np.asarray(K, dtype=np.float64)[:n]
+    z = Kf @ q
+    k = max(0, min(int(m), n))
+    if k == 0 or k == n:
+        return np.arange(k, dtype=np.int64), np.zeros(0, dtype=np.int64)
+    bound = Kf.shape[1] * eps * (np.abs(Kf) @ np.abs(q))
+    zk = np.sort(z)[::-1][k - 1]
+    band = np.flatnonzero(np.abs(z - zk) <= bound + bound.max())
+    sure = np.flatnonzero(z - bound - bound.max() > zk)
+    return sure.astype(np.int64), band.astype(np.int64)
+
+
+def recall(selected, reference) -> float:
+    """|selected & reference| / |reference| (1.0 when the reference is empty)."""
+    ref = np.unique(np.asarray(reference, dtype=np.int64))
+    if ref.size == 0:
+        return 1.0
+    hit = np.intersect1d(np.unique(np.asarray(selected, dtype=np.int64)), ref).size
+    return hit / ref.size
 
 
 # ---------------------------------------------------------------------------

@@ -380,6 +380,31 @@ def check_encode(o):
     assert o.encode_ambiguous(xz, Wz) == 1 << 5
 
 
+def check_exact_topm_and_recall(o):
+    """Exact top-m by dot score against an O(n^2) rank, ties by index, m >= n; the
+    rounding band brackets the boundary; recall on worked examples."""
+    rng = np.random.default_rng(47)
+    for trial in range(30):
+        n, d = int(rng.integers(1, 70)), 8
+        K = rng.standard_normal((n, d))
+        if trial % 3 == 0:                    # repeated rows: exact ties
+            K[rng.integers(0, n, n // 2)] = K[0]
+        q = rng.standard_normal(d)
+        m = int(rng.integers(0, n + 3))
+        z = [float(np.dot(K[i], q)) for i in range(n)]
+        rank = [sum(1 for j in range(n) if z[j] > z[i] or (z[j] == z[i] and j < i)) for i in range(n)]
+        want = sorted(i for i in range(n) if rank[i] < m)
+        got = o.top_m_by_dot(q, K, n, m)
+        assert list(got) == want, (n, m)
+        sure, band = o.top_m_band(q, K, n, m)
+        assert set(sure) <= set(want) and set(want) <= set(sure) | set(band)
+    K = np.tile(rng.standard_normal((1, 4)), (10, 1))  # all scores equal: the first m
+    assert list(o.top_m_by_dot(rng.standard_normal(4), K, 10, 3)) == [0, 1, 2]
+    assert o.recall([1, 2, 3], [2, 3, 4, 5]) == 0.5
+    assert o.recall([7, 9], [7, 9]) == 1.0 and o.recall([1], [2]) == 0.0 and o.recall([], []) == 1.0
+    assert abs(o.recall(np.arange(10), np.arange(5, 20)) - 5 / 15) < 1e-15
+
+
 def check_decode_composition(o):
     """decode_head = attend over selected_set, and decode_batch maps h to KV head h // G."""
     rng = np.random.default_rng(37)
@@ -412,7 +437,8 @@ ALL_CHECKS = [
     check_topm_bruteforce, check_topm_ties, check_windows, check_budget,
     check_dense_vs_sdpa, check_decimal, check_weighted_sum, check_lse_bounds,
     check_lse_gradient, check_low_temperature, check_empty,
-    check_merge_partition, check_merge_segments, check_encode, check_decode_composition,
+    check_merge_partition, check_merge_segments, check_encode, check_exact_topm_and_recall,
+    check_decode_composition,
 ]
 
 

@@ -44,6 +44,11 @@ MUTATIONS = [
     ("merge_segments_mean_not_mass", "merged = sum(m_s * outs[s] for m_s, s in zip(mass, live)) / norm",
      "merged = sum(outs[s] for s in live) / len(live)"),
     ("merge_segments_lse_without_peak", "return merged, peak + math.log(norm)", "return merged, math.log(norm)"),
+    ("exact_topm_smallest_scores", "order = np.lexsort((np.arange(n), -z))  # score descending",
+     "order = np.lexsort((np.arange(n), z))  # score descending"),
+    ("exact_topm_ties_to_larger_index", "order = np.lexsort((np.arange(n), -z))  # score descending",
+     "order = np.lexsort((-np.arange(n), -z))  # score descending"),
+    ("recall_over_selected", "    return hit / ref.size", "    return hit / max(1, np.unique(np.asarray(selected)).size)"),
     ("encode_zero_sets_bit", "        if proj[j] > 0.0:", "        if proj[j] >= 0.0:"),
     ("encode_bit_order_reversed", "            code |= 1 << j", "            code |= 1 << (31 - j)"),
     ("encode_transposed_projection", "proj = np.asarray(W, dtype=np.float64) @ np.asarray(x, dtype=np.float64)",
