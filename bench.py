@@ -246,6 +246,39 @@ def measure_encode(w, shape, dev):
             "bound": "latency (32 x d GEMV per vector)", "timing": "CUDA graph of 50 launches"}
 
 
+def measure_exact(w, shape, sel, cnt, dev):
+    """The exact comparator on the bench workload: top-m (m = the decode budget)
+    by dot score over every cached token, and the recall of the decode's own
+    selection (top-m by Hamming distance joined with the windows) against it."""
+    import torch
+    from long_context_sparse_score_gb300 import hashattn as H
+    ws = torch.empty(H.hash_attn_topk_exact_workspace_size(shape), dtype=torch.uint8, device=dev)
+    idx = torch.empty((w.B, w.Hq, w.m), dtype=torch.int32, device=dev)
+    ecnt = torch.empty((w.B, w.Hq), dtype=torch.int32, device=dev)
+    rec = torch.empty(w.B * w.Hq, device=dev)
+    H.hash_attn_topk_exact(shape, w.q, w.K, w.seq_lens, w.m, idx, ecnt, workspace=ws)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    ev[0].record()
+    H.hash_attn_topk_exact(shape, w.q, w.K, w.seq_lens, w.m, idx, ecnt, workspace=ws)
+    ev[1].record()
+    H.hash_attn_recall(sel, cnt, idx, ecnt, rec)
+    ev[2].record()
+    torch.cuda.synchronize()
+    st, flags = H.hash_attn_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"exact top-k device status {st} flags {flags:#x}")
+    kv_bytes = w.B * w.Hkv * w.n_cap * w.d * w.K.element_size()
+    ms = ev[0].elapsed_time(ev[1])
+    del ws
+    return {"kernels": "k_dot_scores + k_topk_exact", "m": w.m, "ms": ms,
+            "key_read_gbs": kv_bytes / (ms * 1e-3) / 1e9,
+            "recall_mean": float(rec.mean()), "recall_min": float(rec.min()),
+            "recall_kernel_us": ev[1].elapsed_time(ev[2]) * 1e3,
+            "recall_note": "hashed selection (top-m by Hamming distance + windows) vs exact top-m by <q, k>; "
+                           "synthetic queries near random cached keys, codes by sign random projection"}
+
+
 # ---------------------------------------------------------------- workload helpers
 
 def algorithmic_bytes(w, sel_idx, sel_cnt):
@@ -468,7 +501,8 @@ def run_ours(args, world, rank, local):
                 "note": "per step: q, q_sig, seq_lens host->device (one packed pinned buffer), decode, out+lse device->host (one buffer), "
                         "stream sync; KV cache and key codes are device-resident state"},
         "clocks": clocks,
-        "next": {"merge_n": measure_merge_n(dev, peak), "encode": measure_encode(w, shape, dev)},
+        "next": {"merge_n": measure_merge_n(dev, peak), "encode": measure_encode(w, shape, dev),
+                 "exact_topk": measure_exact(w, shape, sel, cnt, dev)},
     }
     if not args.no_cpu_baseline:
         cpu_s, cpu_heads, res = run_cpu_oracle(w, args.cpu_heads)

@@ -264,6 +264,38 @@ ha_status hash_attn_encode_keys(const ha_shape* shape, const void* K, const floa
                                 uint32_t* k_sig, uint32_t* dev_flags, void* stream);
 
 /*
+ * The exact comparator of the hashed selection (HashAttention Sec. 5 measures
+ * against the top-k by attention score): for every (b, h), the k = min(m, n)
+ * tokens with the largest z_i = <q[b, h], K[b, h / G, i]> (float32, i < n =
+ * seq_lens[b]; ties go to the smaller index), written ascending to
+ * idx[b, h, 0..k) and padded with -1 to idx_cap; cnt[b, h] = k.
+ *   q, K     per shape (K rows 16-byte aligned, as for hash_attn_decode)
+ *   idx      int32 [batch, h_q, idx_cap], min(m, n_cap) <= idx_cap <= n_cap
+ *   cnt      int32 [batch, h_q]
+ *   workspace >= hash_attn_topk_exact_workspace_size bytes, 256-byte aligned
+ *            (no zeroing needed: every call clears its first word, the device
+ *            error word read by hash_attn_device_status; the scores of all
+ *            heads live after it)
+ * Errors: HA_ERR_INVALID_ARG / HA_ERR_UNSUPPORTED / HA_ERR_WORKSPACE before
+ * anything is enqueued; bad seq_lens are flagged in the error word.
+ */
+ha_status hash_attn_topk_exact_workspace_size(const ha_shape* shape, size_t* bytes);
+ha_status hash_attn_topk_exact(const ha_shape* shape, const void* q, const void* K, const int32_t* seq_lens,
+                               int32_t m, int32_t* idx, int32_t idx_cap, int32_t* cnt, void* workspace,
+                               size_t ws_bytes, void* stream);
+
+/*
+ * Recall of one selection against a reference, per head:
+ * recall[h] = |sel_h & ref_h| / |ref_h| (1 for an empty reference), with sel_h =
+ * sel_idx[h, 0..sel_cnt[h]) and ref_h = ref_idx[h, 0..ref_cnt[h]) ascending
+ * lists (counts clamped to [0, cap]); e.g. hashed selection vs exact top-k.
+ *   sel_idx [heads, sel_cap], ref_idx [heads, ref_cap] int32; recall float32 [heads].
+ * Errors: HA_ERR_INVALID_ARG before anything is enqueued; heads == 0 does nothing.
+ */
+ha_status hash_attn_recall(const int32_t* sel_idx, const int32_t* sel_cnt, int32_t sel_cap, const int32_t* ref_idx,
+                           const int32_t* ref_cnt, int32_t ref_cap, int32_t heads, float* recall, void* stream);
+
+/*
  * Exact merge of nseg partial attentions over disjoint token sets, row by row
  * (Nectar Sec. 3: each segment enters the softmax as one virtual logit lse_s
  * with value out_s; Eq. (3.4) applied to every segment):

@@ -166,6 +166,29 @@ struct EncodeParams {
     int B, Hq, Hkv, G, d, n_cap, keys;
 };
 
+// Exact top-m by dot score (the comparator of the hashed selection).
+struct ExactParams {
+    const void* q;
+    int64_t q_sb, q_sh;
+    int q_bf16;
+    const char* K;
+    int64_t k_sb, k_sh, k_sn;  // elements
+    const int32_t* seq_lens;
+    int B, Hq, Hkv, G, n_cap, m;
+    float* scores;             // [B * Hq][n_cap] (workspace)
+    int32_t* idx;              // [B * Hq][idx_cap]
+    int idx_cap;
+    int32_t* cnt;              // [B * Hq]
+    uint32_t* err;
+};
+
+struct RecallParams {
+    const int32_t* sel_idx; const int32_t* sel_cnt; int sel_cap;
+    const int32_t* ref_idx; const int32_t* ref_cnt; int ref_cap;
+    int heads;
+    float* recall;
+};
+
 struct MergeNParams {
     const float* outs; int64_t out_seg_stride;
     const float* lses; int64_t lse_seg_stride;
@@ -200,6 +223,8 @@ cudaError_t launch_gather(const GatherParams& p, int d, int kv_bf16, cudaStream_
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t st);
 cudaError_t launch_merge_n(const MergeNParams& p, cudaStream_t st);
 cudaError_t launch_encode(const EncodeParams& p, cudaStream_t st);
+cudaError_t launch_topk_exact(const ExactParams& p, int d, int kv_bf16, cudaStream_t st);
+cudaError_t launch_recall(const RecallParams& p, cudaStream_t st);
 
 // ------------------------------------------------------------------ device helpers
 

@@ -584,6 +584,68 @@ ha_status hash_attn_encode_keys(const ha_shape* shape, const void* K, const floa
     return HA_OK;
 }
 
+ha_status hash_attn_topk_exact_workspace_size(const ha_shape* shape, size_t* bytes) {
+    HA_TRY(check_shape(shape));
+    if (bytes == nullptr) return fail(HA_ERR_INVALID_ARG, "bytes is NULL");
+    *bytes = 256 + align_up((size_t)shape->batch * shape->h_q * (size_t)shape->n_cap * sizeof(float), 256);
+    return HA_OK;
+}
+
+ha_status hash_attn_topk_exact(const ha_shape* shape, const void* q, const void* K, const int32_t* seq_lens,
+                               int32_t m, int32_t* idx, int32_t idx_cap, int32_t* cnt, void* workspace,
+                               size_t ws_bytes, void* stream) {
+    HA_TRY(check_shape(shape));
+    if (q == nullptr || seq_lens == nullptr || idx == nullptr || cnt == nullptr)
+        return fail(HA_ERR_INVALID_ARG, "q, seq_lens, idx and cnt must not be NULL");
+    HA_TRY(check_kv(shape, K, K));
+    if (m < 0) return fail(HA_ERR_INVALID_ARG, "m must be >= 0 (got %d)", m);
+    const int32_t need = m < shape->n_cap ? m : shape->n_cap;
+    if (idx_cap < need || idx_cap > shape->n_cap)
+        return fail(HA_ERR_INVALID_ARG, "idx_cap must be in [min(m, n_cap), n_cap] (got %d)", idx_cap);
+    size_t nbytes = 0;
+    HA_TRY(hash_attn_topk_exact_workspace_size(shape, &nbytes));
+    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 || ws_bytes < nbytes)
+        return fail(HA_ERR_WORKSPACE, "workspace must be 256-byte aligned and hold %zu bytes", nbytes);
+    ExactParams p{};
+    p.q = q;
+    p.q_sb = shape->q_sb;
+    p.q_sh = shape->q_sh;
+    p.q_bf16 = shape->q_dtype == HA_BF16;
+    p.K = static_cast<const char*>(K);
+    p.k_sb = shape->k_sb;
+    p.k_sh = shape->k_sh;
+    p.k_sn = shape->k_sn;
+    p.seq_lens = seq_lens;
+    p.B = shape->batch;
+    p.Hq = shape->h_q;
+    p.Hkv = shape->h_kv;
+    p.G = shape->h_q / shape->h_kv;
+    p.n_cap = shape->n_cap;
+    p.m = m;
+    p.err = static_cast<uint32_t*>(workspace);
+    p.scores = reinterpret_cast<float*>(static_cast<char*>(workspace) + 256);
+    p.idx = idx;
+    p.idx_cap = idx_cap;
+    p.cnt = cnt;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // every call starts with a clean error word (the rest of the workspace is scratch)
+    const cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(uint32_t), st);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the error word");
+    HA_LAUNCH(launch_topk_exact(p, shape->d, shape->kv_dtype == HA_BF16, st), "exact top-k launch");
+    return HA_OK;
+}
+
+ha_status hash_attn_recall(const int32_t* sel_idx, const int32_t* sel_cnt, int32_t sel_cap, const int32_t* ref_idx,
+                           const int32_t* ref_cnt, int32_t ref_cap, int32_t heads, float* recall, void* stream) {
+    if (heads < 0 || sel_cap < 0 || ref_cap < 0) return fail(HA_ERR_INVALID_ARG, "heads and caps must be >= 0");
+    if (heads == 0) return HA_OK;
+    if (!sel_cnt || !ref_cnt || !recall || (!sel_idx && sel_cap > 0) || (!ref_idx && ref_cap > 0))
+        return fail(HA_ERR_INVALID_ARG, "recall pointers must not be NULL");
+    RecallParams p{sel_idx, sel_cnt, sel_cap, ref_idx, ref_cnt, ref_cap, heads, recall};
+    HA_LAUNCH(launch_recall(p, static_cast<cudaStream_t>(stream)), "recall launch");
+    return HA_OK;
+}
+
 ha_status hash_attn_device_status(void* workspace, void* stream, uint32_t* flags) {
     if (workspace == nullptr) return fail(HA_ERR_WORKSPACE, "workspace is NULL");
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -1,0 +1,290 @@
+// The exact comparator of the hashed selection and its recall.
+//
+// HashAttention: Semantic Sparsity for Faster Inference, Sec. 5 measures the
+// hashed selection against the oracle top-k by attention score. Here:
+//   k_dot_scores   z[head, i] = <q[b, h], k_i> (float32) for every cached token
+//                  i < n; one read of a KV head's rows serves its G query heads
+//                  (4 lanes share a row, 16-byte loads, q in shared memory).
+//   k_topk_exact   per head, the min(m, n) largest z (ties: smaller index):
+//                  radix select over order-preserving 32-bit keys, 8 bits per
+//                  pass, then one compaction pass in token order writes the
+//                  ascending list (-1 padded).
+//   k_recall       per head, |selected & reference| / |reference|: the
+//                  reference list is staged in shared memory in tiles and every
+//                  selected index is looked up by binary search.
+#include "ha_internal.cuh"
+
+#include <math_constants.h>
+
+namespace ha {
+namespace {
+
+constexpr int kScoreRowsPerCta = 1024;
+constexpr int kTopkThreads = 1024;
+constexpr int kRecallThreads = 256;
+constexpr int kRecallTile = 8192;
+
+template <typename KT>
+__device__ __forceinline__ void to_float8(const uint4 w, float* f);
+
+template <>
+__device__ __forceinline__ void to_float8<__nv_bfloat16>(const uint4 w, float* f) {
+    f[0] = bf16lo(w.x); f[1] = bf16hi(w.x);
+    f[2] = bf16lo(w.y); f[3] = bf16hi(w.y);
+    f[4] = bf16lo(w.z); f[5] = bf16hi(w.z);
+    f[6] = bf16lo(w.w); f[7] = bf16hi(w.w);
+}
+
+template <>
+__device__ __forceinline__ void to_float8<float>(const uint4 w, float* f) {
+    f[0] = __uint_as_float(w.x); f[1] = __uint_as_float(w.y);
+    f[2] = __uint_as_float(w.z); f[3] = __uint_as_float(w.w);
+}
+
+// grid: (B * Hkv, token blocks of kScoreRowsPerCta); 256 threads; dynamic
+// shared memory G * D floats (the group's queries).
+template <int D, typename KT>
+__global__ void __launch_bounds__(256) k_dot_scores(const ExactParams p) {
+    constexpr int ES = sizeof(KT);
+    constexpr int NCH = D * ES / 16;  // 16-byte chunks per row
+    constexpr int CPL = NCH / 4;      // chunks per lane (4 lanes per row)
+    constexpr int EPC = 16 / ES;      // elements per chunk
+    extern __shared__ float s_q[];    // [G][D]
+    const int bg = blockIdx.x;
+    const int b = bg / p.Hkv, g = bg % p.Hkv;
+    const int n = checked_len(p.seq_lens, b, p.n_cap, p.err, blockIdx.y == 0 && g == 0 && threadIdx.x == 0);
+    for (int i = threadIdx.x; i < p.G * D; i += blockDim.x) {
+        const int hh = i / D, k = i - hh * D;
+        const int64_t off = (int64_t)b * p.q_sb + (int64_t)(g * p.G + hh) * p.q_sh + k;
+        s_q[i] = p.q_bf16 ? __uint_as_float(((uint32_t) reinterpret_cast<const uint16_t*>(p.q)[off]) << 16)
+                          : reinterpret_cast<const float*>(p.q)[off];
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r = lane & 7, qt = lane >> 3;
+    const char* Kb = p.K + ((int64_t)b * p.k_sb + (int64_t)g * p.k_sh) * ES;
+    const int row_end = min(n, (int)(blockIdx.y + 1) * kScoreRowsPerCta);
+    for (int row0 = blockIdx.y * kScoreRowsPerCta + warp * 8; row0 < row_end; row0 += 8 * 8) {
+        const int row = row0 + r;
+        uint4 w[CPL];
+#pragma unroll
+        for (int jc = 0; jc < CPL; ++jc)
+            w[jc] = (row < row_end) ? __ldg(reinterpret_cast<const uint4*>(Kb + (int64_t)row * p.k_sn * ES +
+                                                                          (jc * 4 + qt) * 16))
+                                    : make_uint4(0u, 0u, 0u, 0u);
+        for (int hh = 0; hh < p.G; ++hh) {
+            const float* qh = s_q + hh * D;
+            float acc = 0.f;
+#pragma unroll
+            for (int jc = 0; jc < CPL; ++jc) {
+                float f[EPC];
+                to_float8<KT>(w[jc], f);
+#pragma unroll
+                for (int e = 0; e < EPC; ++e) acc = fmaf(qh[(jc * 4 + qt) * EPC + e], f[e], acc);
+            }
+            acc += __shfl_xor_sync(0xffffffffu, acc, 8);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 16);
+            if (qt == 0 && row < row_end)
+                p.scores[((int64_t)b * p.Hq + g * p.G + hh) * p.n_cap + row] = acc;
+        }
+    }
+}
+
+// Order-preserving key of a float: larger float, larger key.
+__device__ __forceinline__ uint32_t fkey(float x) {
+    const uint32_t u = __float_as_uint(x);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Block-wide exclusive prefix sum of one int per thread; returns the exclusive
+// value and writes the block total to *total (every thread).
+__device__ __forceinline__ int block_excl_scan(int v, int* s_warp, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = blockDim.x >> 5;
+        int y = (lane < nw) ? s_warp[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int z = __shfl_up_sync(0xffffffffu, y, o);
+            if (lane >= o) y += z;
+        }
+        if (lane < nw) s_warp[lane] = y;  // inclusive over warps
+    }
+    __syncthreads();
+    const int before = (warp > 0 ? s_warp[warp - 1] : 0) + x - v;
+    *total = s_warp[(blockDim.x >> 5) - 1];
+    __syncthreads();
+    return before;
+}
+
+// One CTA (kTopkThreads) per query head.
+__global__ void __launch_bounds__(kTopkThreads) k_topk_exact(const ExactParams p) {
+    __shared__ unsigned s_hist[256];
+    __shared__ int s_warp[kTopkThreads / 32];
+    __shared__ uint32_t s_prefix;
+    __shared__ int s_need;
+    const int head = blockIdx.x;
+    const int b = head / p.Hq;
+    const int tid = threadIdx.x;
+    const int n = checked_len(p.seq_lens, b, p.n_cap, nullptr, false);
+    const int k = max(0, min(p.m, n));
+    const float* z = p.scores + (int64_t)head * p.n_cap;
+    int32_t* dst = p.idx + (int64_t)head * p.idx_cap;
+
+    // ---- radix select: the k-th largest key T, and how many keys equal to T to take
+    uint32_t prefix = 0u, mask = 0u;
+    int need = k;
+    if (k > 0 && k < n) {
+        if (tid == 0) {  // kept if no bin matches (cannot happen for finite keys; the count check flags it)
+            s_prefix = 0u;
+            s_need = need;
+        }
+        for (int shift = 24; shift >= 0; shift -= 8) {
+            for (int i = tid; i < 256; i += kTopkThreads) s_hist[i] = 0u;
+            __syncthreads();
+            for (int i = tid; i < n; i += kTopkThreads) {
+                const uint32_t key = fkey(z[i]);
+                if ((key & mask) == prefix) atomicAdd(&s_hist[(key >> shift) & 0xFFu], 1u);
+            }
+            __syncthreads();
+            if (tid < 32) {
+                // bins from the top: lane l holds bins 255 - 8l ... 248 - 8l
+                unsigned c[8], sum = 0u;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    c[u] = s_hist[255 - 8 * tid - u];
+                    sum += c[u];
+                }
+                unsigned incl = sum;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (tid >= o) incl += y;
+                }
+                unsigned above = incl - sum;  // keys in the bins above this lane's
+                const unsigned hit = __ballot_sync(0xffffffffu, above < (unsigned)need && (unsigned)need <= incl);
+                if (tid == __ffs(hit) - 1) {
+                    int bin = 255 - 8 * tid;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        if (above + c[u] >= (unsigned)need) {
+                            bin = 255 - 8 * tid - u;
+                            break;
+                        }
+                        above += c[u];
+                    }
+                    s_prefix = prefix | ((uint32_t)bin << shift);
+                    s_need = need - (int)above;
+                }
+            }
+            __syncthreads();
+            prefix = s_prefix;
+            need = s_need;
+            mask |= 0xFFu << shift;
+            __syncthreads();
+        }
+    }
+    // ---- compaction in token order: keys above T, and the first `need` keys equal to T
+    const bool all = (k >= n);
+    int out_base = 0, ties_seen = 0;
+    for (int i0 = 0; i0 < n && k > 0; i0 += kTopkThreads) {
+        const int i = i0 + tid;
+        bool take = false, tie = false;
+        if (i < n) {
+            if (all) {
+                take = true;
+            } else {
+                const uint32_t key = fkey(z[i]);
+                take = key > prefix;
+                tie = key == prefix;
+            }
+        }
+        int ties_total;
+        const int tie_before = block_excl_scan(tie ? 1 : 0, s_warp, &ties_total);
+        if (tie && ties_seen + tie_before < need) take = true;
+        ties_seen += ties_total;
+        int taken_total;
+        const int pos = block_excl_scan(take ? 1 : 0, s_warp, &taken_total);
+        if (take && out_base + pos < p.idx_cap) dst[out_base + pos] = i;
+        out_base += taken_total;
+    }
+    for (int t = k + tid; t < p.idx_cap; t += kTopkThreads) dst[t] = -1;
+    if (tid == 0) {
+        p.cnt[head] = k;
+        if (out_base != k) flag_error(p.err, HA_DEVERR_STATE);
+    }
+}
+
+// One CTA per head: recall[head] = |selected & reference| / |reference|.
+__global__ void __launch_bounds__(kRecallThreads) k_recall(const RecallParams p) {
+    __shared__ int s_ref[kRecallTile];
+    __shared__ int s_sum[kRecallThreads / 32];
+    const int head = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int na = min(max(p.sel_cnt[head], 0), p.sel_cap);
+    const int nb = min(max(p.ref_cnt[head], 0), p.ref_cap);
+    const int32_t* A = p.sel_idx + (int64_t)head * p.sel_cap;
+    const int32_t* Bv = p.ref_idx + (int64_t)head * p.ref_cap;
+    int hits = 0;
+    for (int t0 = 0; t0 < nb; t0 += kRecallTile) {
+        const int tn = min(kRecallTile, nb - t0);
+        __syncthreads();
+        for (int i = tid; i < tn; i += kRecallThreads) s_ref[i] = Bv[t0 + i];
+        __syncthreads();
+        for (int i = tid; i < na; i += kRecallThreads) {
+            const int x = A[i];
+            int lo = 0, hi = tn - 1;
+            while (lo < hi) {  // the reference list is ascending
+                const int mid = (lo + hi) >> 1;
+                if (s_ref[mid] < x) lo = mid + 1; else hi = mid;
+            }
+            hits += (s_ref[lo] == x) ? 1 : 0;
+        }
+    }
+    int v = hits;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if ((tid & 31) == 0) s_sum[tid >> 5] = v;
+    __syncthreads();
+    if (tid == 0) {
+        int total = 0;
+        for (int w = 0; w < kRecallThreads / 32; ++w) total += s_sum[w];
+        p.recall[head] = (nb == 0) ? 1.f : (float)total / (float)nb;
+    }
+}
+
+template <int D, typename KT>
+cudaError_t launch_scores_t(const ExactParams& p, cudaStream_t st) {
+    const dim3 grid((unsigned)(p.B * p.Hkv), (unsigned)((p.n_cap + kScoreRowsPerCta - 1) / kScoreRowsPerCta));
+    k_dot_scores<D, KT><<<grid, 256, (size_t)p.G * D * sizeof(float), st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_topk_exact(const ExactParams& p, int d, int kv_bf16, cudaStream_t st) {
+    cudaError_t e = cudaErrorInvalidValue;
+    if (d == 128 && kv_bf16) e = launch_scores_t<128, __nv_bfloat16>(p, st);
+    if (d == 64 && kv_bf16) e = launch_scores_t<64, __nv_bfloat16>(p, st);
+    if (d == 128 && !kv_bf16) e = launch_scores_t<128, float>(p, st);
+    if (d == 64 && !kv_bf16) e = launch_scores_t<64, float>(p, st);
+    if (e != cudaSuccess) return e;
+    k_topk_exact<<<p.B * p.Hq, kTopkThreads, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_recall(const RecallParams& p, cudaStream_t st) {
+    if (p.heads <= 0) return cudaSuccess;
+    k_recall<<<p.heads, kRecallThreads, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace ha

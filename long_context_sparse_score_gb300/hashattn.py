@@ -39,7 +39,8 @@ EXPORTED = [
     "hash_attn_workspace_size", "hash_attn_workspace_init", "hash_attn_select_capacity",
     "hash_attn_decode", "hash_attn_decode_timed", "hash_attn_score", "hash_attn_select",
     "hash_attn_gather_att", "hash_attn_gather_att_noalloc", "hash_attn_merge", "hash_attn_merge_n",
-    "hash_attn_encode_queries", "hash_attn_encode_keys",
+    "hash_attn_encode_queries", "hash_attn_encode_keys", "hash_attn_topk_exact_workspace_size",
+    "hash_attn_topk_exact", "hash_attn_recall",
     "hash_attn_device_status",
     "hash_attn_status_string", "hash_attn_last_error",
 ]
@@ -97,6 +98,9 @@ def lib() -> ctypes.CDLL:
     L.hash_attn_merge_n.argtypes = [_P, ctypes.c_int64, _P, ctypes.c_int64, _I32, _P, _P, _I32, _I32, _P]
     L.hash_attn_encode_queries.argtypes = [SP, _P, _P, _P, _P]
     L.hash_attn_encode_keys.argtypes = [SP, _P, _P, _P, _P, _P, _P]
+    L.hash_attn_topk_exact_workspace_size.argtypes = [SP, ctypes.POINTER(_SZ)]
+    L.hash_attn_topk_exact.argtypes = [SP, _P, _P, _P, _I32, _P, _I32, _P, _P, _SZ, _P]
+    L.hash_attn_recall.argtypes = [_P, _P, _I32, _P, _P, _I32, _I32, _P, _P]
     L.hash_attn_device_status.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_uint32)]
     L.hash_attn_status_string.argtypes = [_I32]
     L.hash_attn_status_string.restype = ctypes.c_char_p
@@ -268,6 +272,26 @@ def hash_attn_encode_keys(shape, K, W, pos, k_sig, dev_flags=None, stream=None) 
     """k_sig[b, g, pos[b]] = code of K[b, g, pos[b]] under W[g], for pos[b] in [0, n_cap)."""
     _check(lib().hash_attn_encode_keys(ctypes.byref(shape), _ptr(K), _ptr(W), _ptr(pos), _ptr(k_sig),
                                        _ptr(dev_flags), _stream(stream)))
+
+
+def hash_attn_topk_exact_workspace_size(shape) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().hash_attn_topk_exact_workspace_size(ctypes.byref(shape), ctypes.byref(out)))
+    return out.value
+
+
+def hash_attn_topk_exact(shape, q, K, seq_lens, m, idx, cnt, *, workspace, stream=None) -> None:
+    """idx [B, Hq, cap] / cnt [B, Hq]: the min(m, n) largest <q, k_i> per head, ascending."""
+    ws, nb = _ws(workspace)
+    _check(lib().hash_attn_topk_exact(ctypes.byref(shape), _ptr(q), _ptr(K), _ptr(seq_lens), m, _ptr(idx),
+                                      idx.shape[-1], _ptr(cnt), ws, nb, _stream(stream)))
+
+
+def hash_attn_recall(sel_idx, sel_cnt, ref_idx, ref_cnt, recall, stream=None) -> None:
+    """recall[h] = |sel_h & ref_h| / |ref_h| over [heads, cap] index lists (any leading shape)."""
+    heads = sel_cnt.numel()
+    _check(lib().hash_attn_recall(_ptr(sel_idx), _ptr(sel_cnt), sel_idx.shape[-1], _ptr(ref_idx), _ptr(ref_cnt),
+                                  ref_idx.shape[-1], heads, _ptr(recall), _stream(stream)))
 
 
 def hash_attn_device_status(workspace, stream=None) -> tuple[int, int]:

@@ -377,6 +377,62 @@ def test_encode_queries_and_keys(d, q_dtype):
     assert int(flags.item()) & H.HA_DEVERR_INDEX
 
 
+@pytest.mark.parametrize("d,kv_dtype,m", [(128, torch.bfloat16, 100), (128, torch.bfloat16, 2500),
+                                           (64, torch.float32, 37), (128, torch.bfloat16, 5000)])
+def test_topk_exact_and_recall(d, kv_dtype, m):
+    """Exact top-m by dot score against the oracle (tokens inside the float32 band
+    around the boundary may go either way, the count is exact), then the recall of
+    the hashed selection against it."""
+    H = GH.ha()
+    w = W().make_gqa(21, B=2, Hq=8, Hkv=2, d=d, n_cap=3000, seq_lens=[3000, 2222], m=300, n_sink=16,
+                     n_local=16, device="cuda", kv_dtype=kv_dtype)
+    if kv_dtype == torch.float32:
+        w.q = w.q.float()
+    shape = H.make_shape(w.q, w.K, w.V, w.k_sig)
+    ws = torch.empty(H.hash_attn_topk_exact_workspace_size(shape), dtype=torch.uint8, device="cuda")
+    cap = min(m, 3000)
+    idx = torch.full((2, 8, cap), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.full((2, 8), -7, dtype=torch.int32, device="cuda")
+    H.hash_attn_topk_exact(shape, w.q, w.K, w.seq_lens, m, idx, cnt, workspace=ws)
+    st, flags = H.hash_attn_device_status(ws)
+    assert st == 0, flags
+    qn, Kn = w.q.float().cpu().numpy(), w.K.float().cpu().numpy()
+    idx_h, cnt_h = idx.cpu().numpy(), cnt.cpu().numpy()
+    for b, n in enumerate([3000, 2222]):
+        for h in range(8):
+            k = min(m, n)
+            assert int(cnt_h[b, h]) == k
+            got = idx_h[b, h, :k]
+            assert np.all(np.diff(got) > 0) and np.all(idx_h[b, h, k:] == -1)
+            sure, band = O.top_m_band(qn[b, h], Kn[b, h // 4], n, m)
+            assert set(sure) <= set(got) <= set(sure) | set(band), (b, h)
+    # recall of the hashed selection against the exact top-m
+    res = GH.run_decode(w)
+    rec = torch.empty(16, device="cuda")
+    H.hash_attn_recall(res["sel_idx"], res["sel_cnt"], idx, cnt, rec)
+    torch.cuda.synchronize()
+    sel_h, scnt_h = res["sel_idx"].cpu().numpy(), res["sel_cnt"].cpu().numpy()
+    for b in range(2):
+        for h in range(8):
+            want = O.recall(sel_h[b, h, :scnt_h[b, h]], idx_h[b, h, :cnt_h[b, h]])
+            assert abs(float(rec[b * 8 + h]) - want) < 1e-6
+
+
+def test_topk_exact_ties_take_smaller_indices():
+    H = GH.ha()
+    w = W().make_gqa(22, B=1, Hq=4, Hkv=1, d=128, n_cap=2048, seq_lens=[2048], m=64, n_sink=0, n_local=0,
+                     device="cuda")
+    w.K[:] = w.K[:, :, :1]                       # every row equal: every score ties
+    shape = H.make_shape(w.q, w.K, w.V, w.k_sig)
+    ws = torch.empty(H.hash_attn_topk_exact_workspace_size(shape), dtype=torch.uint8, device="cuda")
+    idx = torch.empty((1, 4, 300), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((1, 4), dtype=torch.int32, device="cuda")
+    H.hash_attn_topk_exact(shape, w.q, w.K, w.seq_lens, 300, idx, cnt, workspace=ws)
+    torch.cuda.synchronize()
+    for h in range(4):
+        assert int(cnt[0, h]) == 300 and torch.equal(idx[0, h].cpu(), torch.arange(300, dtype=torch.int32))
+
+
 def test_device_errors_are_flagged_not_faulted():
     H = GH.ha()
     w = W().make_gqa(16, B=3, Hq=4, Hkv=2, d=128, n_cap=2000, seq_lens=[2000, 1500, 2000], m=100,
