@@ -36,7 +36,10 @@ Readings where the pages are silent (each is listed in the design notes):
   * keep the m SMALLEST Hamming distances (SCORE is the negated distance);
   * ties are broken by token index ascending, so the selected set is unique;
   * T (top-min(m, n) over all n tokens) is UNIONED with the windows
-    [0, min(S, n)) and [max(0, n - Lw), n); duplicates are counted once;
+    [0, min(S, n)) and [max(0, n - Lw), n); duplicates are counted once (the
+    other reading, T over the tokens outside the windows with |I| fixed at
+    min(n, m + |W|), is available as ``exclusive``);
+  * a budget may be given per sequence or per query head (each <= m);
   * the softmax scale is 1/sqrt(d); lse is the natural log of the sum over I;
   * an empty selected set gives out = 0 and lse = -inf;
   * the query head h reads KV head h // G (contiguous GQA groups).
@@ -136,11 +139,22 @@ def window_positions(n: int, n_sink: int, n_local: int) -> np.ndarray:
     return np.union1d(sink, local).astype(np.int64)
 
 
-def selected_set(q_code, k_codes, n: int, m: int, n_sink: int, n_local: int) -> np.ndarray:
-    """I = top-m by SCORE over all n tokens, joined with the sink/local windows."""
+def selected_set(q_code, k_codes, n: int, m: int, n_sink: int, n_local: int,
+                 exclusive: bool = False) -> np.ndarray:
+    """I = top-m by SCORE joined with the sink/local windows.
+
+    Default reading: the top-m is taken over all n tokens (windows may repeat some
+    of them, so |I| <= m + |windows|). ``exclusive``: the other reading of the
+    budget arithmetic (HashAttention Sec. 4.4, m plus the fixed positions): the
+    top-m is taken over the tokens outside the windows, so |I| = min(n, m + |W|).
+    """
     dist = hamming_distances(q_code, np.asarray(k_codes)[:n])
-    top = top_m_by_score(dist, m)
     win = window_positions(n, n_sink, n_local)
+    if exclusive:
+        outside = np.setdiff1d(np.arange(n, dtype=np.int64), win)
+        top = outside[top_m_by_score(dist[outside], m)]
+    else:
+        top = top_m_by_score(dist, m)
     return np.union1d(top, win).astype(np.int64)
 
 
@@ -270,7 +284,7 @@ def merge_segments(outs, lses):
 # ---------------------------------------------------------------------------
 
 def decode_head(q, q_code, k_codes, K, V, n: int, m: int, n_sink: int, n_local: int,
-                dense: bool = False):
+                dense: bool = False, exclusive: bool = False):
     """One query head's sparse decode: SCORE -> TOPK -> GATHER-ATT.
 
     K, V: [n_cap, d] rows of the query's KV head (any float dtype; widened to
@@ -283,20 +297,20 @@ def decode_head(q, q_code, k_codes, K, V, n: int, m: int, n_sink: int, n_local: 
         dist = None
     else:
         dist = hamming_distances(q_code, np.asarray(k_codes)[:n])
-        top = top_m_by_score(dist, m)
-        idx = np.union1d(top, window_positions(n, n_sink, n_local)).astype(np.int64)
+        idx = selected_set(q_code, k_codes, n, m, n_sink, n_local, exclusive=exclusive)
     out, lse = attend(q, K, V, idx)
     return idx, dist, out, lse
 
 
 def decode_batch(q, q_sig, k_sig, K, V, seq_lens, m, n_sink, n_local,
-                 m_per_seq=None, dense=False, heads=None):
+                 m_per_seq=None, dense=False, heads=None, m_per_head=None, exclusive=False):
     """Run ``decode_head`` over (b, h) pairs.
 
     Layouts (NumPy arrays): q [B, Hq, d]; q_sig [B, Hq] (32-bit words);
     k_sig [B, Hkv, n_cap]; K, V [B, Hkv, n_cap, d] (a batch extent of 1 is shared
-    by every batch entry); seq_lens [B]. ``heads`` restricts the work to a list of
-    (b, h) pairs. Returns {(b, h): (idx, dist, out, lse)}.
+    by every batch entry); seq_lens [B]; m_per_head [B, Hq] overrides the
+    budgets. ``heads`` restricts the work to a list of (b, h) pairs. Returns
+    {(b, h): (idx, dist, out, lse)}.
     """
     B, Hq = q.shape[0], q.shape[1]
     Hkv = K.shape[1]
@@ -309,8 +323,10 @@ def decode_batch(q, q_sig, k_sig, K, V, seq_lens, m, n_sink, n_local,
         sb = 0 if (k_sig is None or k_sig.shape[0] == 1) else b
         n = int(seq_lens[b])
         mb = int(m_per_seq[b]) if m_per_seq is not None else int(m)
+        if m_per_head is not None:
+            mb = int(m_per_head[b, h])
         codes = None if dense else k_sig[sb, g]
         qc = None if dense else int(q_sig[b, h])
         res[(b, h)] = decode_head(q[b, h], qc, codes, K[kb, g], V[kb, g], n, mb,
-                                  n_sink, n_local, dense=dense)
+                                  n_sink, n_local, dense=dense, exclusive=exclusive)
     return res

@@ -405,6 +405,37 @@ def check_exact_topm_and_recall(o):
     assert abs(o.recall(np.arange(10), np.arange(5, 20)) - 5 / 15) < 1e-15
 
 
+def check_exclusive_windows(o):
+    """Exclusive reading: |I| = min(n, m + |W|), W inside I, and I minus W is the
+    brute-force top-m of the tokens outside the windows; with no windows both
+    readings agree. Per-head budgets reach every head."""
+    rng = np.random.default_rng(53)
+    for trial in range(40):
+        n = int(rng.integers(1, 60))
+        codes = rng.integers(0, 16, n) * 0x1111  # few distinct codes: many ties
+        q = int(rng.integers(0, 2 ** 32))
+        m, S, L = int(rng.integers(0, n + 4)), int(rng.integers(0, 6)), int(rng.integers(0, 6))
+        I = o.selected_set(q, codes, n, m, S, L, exclusive=True)
+        W = set(range(min(S, n))) | set(range(max(0, n - L), n))
+        assert len(I) == min(n, m + len(W)) and W <= set(I)
+        outside = [i for i in range(n) if i not in W]
+        d = [_py_popcount(q ^ int(codes[i])) for i in outside]
+        rank = _rank_bruteforce(d)
+        assert set(I) - W == {outside[j] for j in range(len(outside)) if rank[j] < m}
+        assert np.array_equal(o.selected_set(q, codes, n, m, 0, 0, exclusive=True),
+                              o.selected_set(q, codes, n, m, 0, 0))
+    B, Hq, Hkv, n_cap, dd = 2, 4, 2, 40, 4
+    qv = rng.standard_normal((B, Hq, dd))
+    Kv = rng.standard_normal((B, Hkv, n_cap, dd))
+    q_sig = rng.integers(0, 2 ** 32, (B, Hq))
+    k_sig = rng.integers(0, 2 ** 32, (B, Hkv, n_cap))
+    mph = rng.integers(0, 20, (B, Hq))
+    res = o.decode_batch(qv, q_sig, k_sig, Kv, Kv, np.array([40, 33]), 20, 2, 3, m_per_head=mph, exclusive=True)
+    for (b, h), (idx, _, _, _) in res.items():
+        want = o.selected_set(int(q_sig[b, h]), k_sig[b, h // 2], [40, 33][b], int(mph[b, h]), 2, 3, exclusive=True)
+        assert np.array_equal(idx, want)
+
+
 def check_decode_composition(o):
     """decode_head = attend over selected_set, and decode_batch maps h to KV head h // G."""
     rng = np.random.default_rng(37)
@@ -438,7 +469,7 @@ ALL_CHECKS = [
     check_dense_vs_sdpa, check_decimal, check_weighted_sum, check_lse_bounds,
     check_lse_gradient, check_low_temperature, check_empty,
     check_merge_partition, check_merge_segments, check_encode, check_exact_topm_and_recall,
-    check_decode_composition,
+    check_exclusive_windows, check_decode_composition,
 ]
 
 

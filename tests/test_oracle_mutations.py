@@ -28,8 +28,10 @@ MUTATIONS = [
      "sink = np.arange(0, int(n_sink), dtype=np.int64)"),
     ("intersection_not_union", "return np.union1d(top, win).astype(np.int64)",
      "return np.intersect1d(top, win).astype(np.int64)"),
-    ("windows_dropped", "idx = np.union1d(top, window_positions(n, n_sink, n_local)).astype(np.int64)",
-     "idx = top"),
+    ("windows_dropped", "    win = window_positions(n, n_sink, n_local)\n    if exclusive:",
+     "    win = np.zeros(0, dtype=np.int64)\n    if exclusive:"),
+    ("exclusive_ignores_windows", "top = outside[top_m_by_score(dist[outside], m)]", "top = top_m_by_score(dist, m)"),
+    ("per_head_budget_ignored", "            mb = int(m_per_head[b, h])", "            mb = mb"),
     ("missing_sqrt_d_scale", "z = k_rows @ q / math.sqrt(d)", "z = k_rows @ q"),
     ("scale_by_d", "z = k_rows @ q / math.sqrt(d)", "z = k_rows @ q / d"),
     ("lse_drops_max", "lse = z_max + math.log(total)", "lse = math.log(total)"),
