@@ -279,6 +279,36 @@ def measure_exact(w, shape, sel, cnt, dev):
                            "synthetic queries near random cached keys, codes by sign random projection"}
 
 
+def measure_variants(w, shape, ws, out, lse, dev):
+    """The decode step with the selection variants on the bench workload:
+    exclusive windows (top-m over the tokens outside the windows) and per-head
+    budgets (uniform in [m/2, m])."""
+    import torch
+    from long_context_sparse_score_gb300 import hashattn as H
+    g = torch.Generator(device=dev).manual_seed(79)
+    mph = torch.randint(w.m // 2, w.m + 1, (w.B, w.Hq), generator=g, device=dev, dtype=torch.int32)
+    res = {}
+    for name, opts in (("exclusive_windows", H.select_opts(None, True)), ("per_head_budgets", H.select_opts(mph))):
+        call = lambda: H.hash_attn_decode_ex(shape, w.q, w.q_sig, w.k_sig, w.K, w.V, w.seq_lens, None, w.m,
+                                             w.n_sink, w.n_local, opts, out, lse, workspace=ws)
+        for _ in range(5):
+            call()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 100
+        e0.record()
+        for _ in range(reps):
+            call()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        res[name] = {"ms_per_step": ms, "query_heads_per_s": w.B * w.Hq / (ms * 1e-3)}
+    st, flags = H.hash_attn_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"selection variants: device status {st} flags {flags:#x}")
+    return res
+
+
 # ---------------------------------------------------------------- workload helpers
 
 def algorithmic_bytes(w, sel_idx, sel_cnt):
@@ -502,7 +532,8 @@ def run_ours(args, world, rank, local):
                         "stream sync; KV cache and key codes are device-resident state"},
         "clocks": clocks,
         "next": {"merge_n": measure_merge_n(dev, peak), "encode": measure_encode(w, shape, dev),
-                 "exact_topk": measure_exact(w, shape, sel, cnt, dev)},
+                 "exact_topk": measure_exact(w, shape, sel, cnt, dev),
+                 "selection_variants": measure_variants(w, shape, ws, out, lse, dev)},
     }
     if not args.no_cpu_baseline:
         cpu_s, cpu_heads, res = run_cpu_oracle(w, args.cpu_heads)

@@ -160,6 +160,35 @@ ha_status hash_attn_decode_timed(const ha_shape* shape, const void* q, const uin
                                  size_t ws_bytes, void* stream, void* const* events);
 
 /*
+ * Selection variants (HashAttention Sec. 4.4 budget accounting; adaptive
+ * budgets). Zero-initialise and set what is needed:
+ *   m_per_head         device int32 [batch, h_q] budget of every query head (each
+ *                      in [0, m]; outside values are clamped and flagged
+ *                      HA_DEVERR_BUDGET), overriding m_per_seq; NULL: none.
+ *   exclusive_windows  0: the top-m is taken over all n tokens and joined with
+ *                      the windows (|I| <= m + windows). 1: the top-m is taken
+ *                      over the tokens outside the windows, so
+ *                      |I| = min(n, m + |windows|) exactly.
+ *   reserved           must be zero.
+ */
+typedef struct {
+    const int32_t* m_per_head;
+    int32_t exclusive_windows;
+    int32_t reserved[3];
+} ha_select_opts;
+
+/*
+ * hash_attn_decode with selection options (opts may be NULL: the defaults of
+ * hash_attn_decode). The workspace size and the sel_idx capacity are those of
+ * hash_attn_decode for the same m, n_sink, n_local.
+ */
+ha_status hash_attn_decode_ex(const ha_shape* shape, const void* q, const uint32_t* q_sig, const uint32_t* k_sig,
+                              const void* K, const void* V, const int32_t* seq_lens, const int32_t* m_per_seq,
+                              int32_t m, int32_t n_sink, int32_t n_local, const ha_select_opts* opts, float* out,
+                              float* lse, int32_t* sel_idx, int32_t* sel_cnt, void* workspace, size_t ws_bytes,
+                              void* stream);
+
+/*
  * SCORE alone (HashAttention Eq. (2)).
  *   dist  optional [batch, h_q, n_cap] uint8: dist[b,h,i] for i < seq_lens[b]
  *         (entries at i >= seq_lens[b] are not written)
@@ -180,6 +209,12 @@ ha_status hash_attn_select(const ha_shape* shape, const uint32_t* q_sig, const u
                            const int32_t* seq_lens, const int32_t* m_per_seq, int32_t m,
                            int32_t n_sink, int32_t n_local, int32_t* sel_idx, int32_t* sel_cnt,
                            void* workspace, size_t ws_bytes, void* stream);
+
+/* hash_attn_select with selection options (see ha_select_opts; NULL = defaults). */
+ha_status hash_attn_select_ex(const ha_shape* shape, const uint32_t* q_sig, const uint32_t* k_sig,
+                              const int32_t* seq_lens, const int32_t* m_per_seq, int32_t m, int32_t n_sink,
+                              int32_t n_local, const ha_select_opts* opts, int32_t* sel_idx, int32_t* sel_cnt,
+                              void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * GATHER-ATT + merge over caller-given index lists (page size 1, read in place):

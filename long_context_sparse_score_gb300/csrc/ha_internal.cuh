@@ -76,7 +76,10 @@ struct ScoreParams {
     // selection thresholds (null: histograms only): the last CTA of a
     // (batch entry, KV head) derives t and every chunk's tie quota
     const int32_t* m_per_seq;
+    const int32_t* m_per_head;   // [B * Hq] or null: budgets per query head (override m_per_seq)
     int m;
+    int excl;                // 1: the top-m is taken over the tokens outside the windows
+    int n_sink, n_local;
     uint32_t* score_cnt;     // [B * Hkv]
     int32_t* meta_t;         // [heads]
     int2* meta_qt;           // [heads][nchunks]
@@ -92,6 +95,7 @@ struct SelectParams {
     int chunk, nchunks;
     const int32_t* meta_t;   // [heads]
     const int2* meta_qt;     // [heads][nchunks]
+    int excl;                // window tokens are never ties (exclusive windows)
     int32_t* seg_cnt;        // [heads][nseg]
     int32_t* seg_idx;        // [heads][nseg * seg_cap]
     uint32_t* err;

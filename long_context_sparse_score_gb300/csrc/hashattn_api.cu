@@ -242,16 +242,36 @@ ha_status record(void* const* events, int i, cudaStream_t st) {
         if (_e != cudaSuccess) return cuda_fail(_e, what); \
     } while (0)
 
+ha_status check_opts(const ha_select_opts* o) {
+    if (o == nullptr) return HA_OK;
+    if (o->exclusive_windows != 0 && o->exclusive_windows != 1)
+        return fail(HA_ERR_INVALID_ARG, "exclusive_windows must be 0 or 1 (got %d)", o->exclusive_windows);
+    for (int i = 0; i < 3; ++i)
+        if (o->reserved[i] != 0) return fail(HA_ERR_INVALID_ARG, "ha_select_opts.reserved must be zero");
+    return HA_OK;
+}
+
+// The selection options into the SCORE/TOPK parameter blocks.
+void apply_opts(const ha_select_opts* o, int32_t n_sink, int32_t n_local, ScoreParams* sp, SelectParams* tp) {
+    sp->n_sink = n_sink;
+    sp->n_local = n_local;
+    sp->m_per_head = o ? o->m_per_head : nullptr;
+    sp->excl = o ? o->exclusive_windows : 0;
+    tp->excl = sp->excl;
+}
+
 ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, const uint32_t* k_sig,
                       const void* K, const void* V, const int32_t* seq_lens, const int32_t* m_per_seq,
-                      int32_t m, int32_t n_sink, int32_t n_local, float* out, float* lse, int32_t* sel_idx,
-                      int32_t* sel_cnt, void* ws, size_t ws_bytes, void* stream, void* const* events) {
+                      int32_t m, int32_t n_sink, int32_t n_local, const ha_select_opts* opts, float* out,
+                      float* lse, int32_t* sel_idx, int32_t* sel_cnt, void* ws, size_t ws_bytes, void* stream,
+                      void* const* events) {
     HA_TRY(check_shape(s));
     HA_TRY(check_window(m, n_sink, n_local));
+    HA_TRY(check_opts(opts));
     if (q == nullptr || seq_lens == nullptr || out == nullptr || lse == nullptr)
         return fail(HA_ERR_INVALID_ARG, "q, seq_lens, out and lse must not be NULL");
     HA_TRY(check_kv(s, K, V));
-    const bool dense = (m >= s->n_cap) && (m_per_seq == nullptr);
+    const bool dense = (m >= s->n_cap) && (m_per_seq == nullptr) && (opts == nullptr || opts->m_per_head == nullptr);
     if (!dense) HA_TRY(check_codes(s, q_sig, k_sig));
     if ((sel_idx == nullptr) != (sel_cnt == nullptr))
         return fail(HA_ERR_INVALID_ARG, "sel_idx and sel_cnt must both be given or both be NULL");
@@ -274,14 +294,15 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
         HA_TRY(record(events, 3, st));
         return HA_OK;
     }
+    ScoreParams sp = score_params(s, lay, v, q_sig, k_sig, seq_lens, m_per_seq, m, true);
+    SelectParams tp = select_params(s, lay, v, q_sig, k_sig, seq_lens, n_sink, n_local);
+    apply_opts(opts, n_sink, n_local, &sp, &tp);
     HA_TRY(record(events, 0, st));
-    HA_LAUNCH(launch_score(score_params(s, lay, v, q_sig, k_sig, seq_lens, m_per_seq, m, true), bhkv, st), "SCORE launch");
+    HA_LAUNCH(launch_score(sp, bhkv, st), "SCORE launch");
     HA_TRY(record(events, 1, st));
     // TOPK and GATHER-ATT may start while their predecessor drains (they wait in
     // the kernel before reading its output)
-    HA_LAUNCH(launch_select(select_params(s, lay, v, q_sig, k_sig, seq_lens, n_sink, n_local),
-                            bhkv, st, true),
-              "TOPK launch");
+    HA_LAUNCH(launch_select(tp, bhkv, st, true), "TOPK launch");
     HA_TRY(record(events, 2, st));
     gp.mode = kSegmented;
     HA_LAUNCH(launch_gather(gp, s->d, s->kv_dtype == HA_BF16, st, true), "GATHER-ATT launch");
@@ -404,8 +425,17 @@ ha_status hash_attn_decode(const ha_shape* shape, const void* q, const uint32_t*
                            const void* K, const void* V, const int32_t* seq_lens, const int32_t* m_per_seq,
                            int32_t m, int32_t n_sink, int32_t n_local, float* out, float* lse, int32_t* sel_idx,
                            int32_t* sel_cnt, void* workspace, size_t ws_bytes, void* stream) {
-    return decode_impl(shape, q, q_sig, k_sig, K, V, seq_lens, m_per_seq, m, n_sink, n_local, out, lse, sel_idx,
-                       sel_cnt, workspace, ws_bytes, stream, nullptr);
+    return decode_impl(shape, q, q_sig, k_sig, K, V, seq_lens, m_per_seq, m, n_sink, n_local, nullptr, out, lse,
+                       sel_idx, sel_cnt, workspace, ws_bytes, stream, nullptr);
+}
+
+ha_status hash_attn_decode_ex(const ha_shape* shape, const void* q, const uint32_t* q_sig, const uint32_t* k_sig,
+                              const void* K, const void* V, const int32_t* seq_lens, const int32_t* m_per_seq,
+                              int32_t m, int32_t n_sink, int32_t n_local, const ha_select_opts* opts, float* out,
+                              float* lse, int32_t* sel_idx, int32_t* sel_cnt, void* workspace, size_t ws_bytes,
+                              void* stream) {
+    return decode_impl(shape, q, q_sig, k_sig, K, V, seq_lens, m_per_seq, m, n_sink, n_local, opts, out, lse,
+                       sel_idx, sel_cnt, workspace, ws_bytes, stream, nullptr);
 }
 
 ha_status hash_attn_decode_timed(const ha_shape* shape, const void* q, const uint32_t* q_sig,
@@ -416,8 +446,8 @@ ha_status hash_attn_decode_timed(const ha_shape* shape, const void* q, const uin
     if (events == nullptr) return fail(HA_ERR_INVALID_ARG, "events is NULL");
     for (int i = 0; i < 4; ++i)
         if (events[i] == nullptr) return fail(HA_ERR_INVALID_ARG, "events[%d] is NULL", i);
-    return decode_impl(shape, q, q_sig, k_sig, K, V, seq_lens, m_per_seq, m, n_sink, n_local, out, lse, sel_idx,
-                       sel_cnt, workspace, ws_bytes, stream, events);
+    return decode_impl(shape, q, q_sig, k_sig, K, V, seq_lens, m_per_seq, m, n_sink, n_local, nullptr, out, lse,
+                       sel_idx, sel_cnt, workspace, ws_bytes, stream, events);
 }
 
 ha_status hash_attn_score(const ha_shape* shape, const uint32_t* q_sig, const uint32_t* k_sig,
@@ -450,12 +480,13 @@ ha_status hash_attn_score(const ha_shape* shape, const uint32_t* q_sig, const ui
     return HA_OK;
 }
 
-ha_status hash_attn_select(const ha_shape* shape, const uint32_t* q_sig, const uint32_t* k_sig,
-                           const int32_t* seq_lens, const int32_t* m_per_seq, int32_t m, int32_t n_sink,
-                           int32_t n_local, int32_t* sel_idx, int32_t* sel_cnt, void* workspace, size_t ws_bytes,
-                           void* stream) {
+ha_status hash_attn_select_ex(const ha_shape* shape, const uint32_t* q_sig, const uint32_t* k_sig,
+                              const int32_t* seq_lens, const int32_t* m_per_seq, int32_t m, int32_t n_sink,
+                              int32_t n_local, const ha_select_opts* opts, int32_t* sel_idx, int32_t* sel_cnt,
+                              void* workspace, size_t ws_bytes, void* stream) {
     HA_TRY(check_shape(shape));
     HA_TRY(check_window(m, n_sink, n_local));
+    HA_TRY(check_opts(opts));
     HA_TRY(check_codes(shape, q_sig, k_sig));
     if (seq_lens == nullptr || sel_idx == nullptr || sel_cnt == nullptr)
         return fail(HA_ERR_INVALID_ARG, "seq_lens, sel_idx and sel_cnt must not be NULL");
@@ -466,10 +497,11 @@ ha_status hash_attn_select(const ha_shape* shape, const uint32_t* q_sig, const u
     const Views v = views(lay, workspace);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int bhkv = shape->batch * shape->h_kv;
-    HA_LAUNCH(launch_score(score_params(shape, lay, v, q_sig, k_sig, seq_lens, m_per_seq, m, true), bhkv, st), "SCORE launch");
-    HA_LAUNCH(launch_select(select_params(shape, lay, v, q_sig, k_sig, seq_lens, n_sink, n_local),
-                            bhkv, st),
-              "TOPK launch");
+    ScoreParams sp = score_params(shape, lay, v, q_sig, k_sig, seq_lens, m_per_seq, m, true);
+    SelectParams tp = select_params(shape, lay, v, q_sig, k_sig, seq_lens, n_sink, n_local);
+    apply_opts(opts, n_sink, n_local, &sp, &tp);
+    HA_LAUNCH(launch_score(sp, bhkv, st), "SCORE launch");
+    HA_LAUNCH(launch_select(tp, bhkv, st), "TOPK launch");
     CompactParams cp{};
     cp.seq_lens = seq_lens;
     cp.Hq = shape->h_q;
@@ -484,6 +516,14 @@ ha_status hash_attn_select(const ha_shape* shape, const uint32_t* q_sig, const u
     cp.err = v.err;
     HA_LAUNCH(launch_compact(cp, shape->batch * shape->h_q, st), "compaction launch");
     return HA_OK;
+}
+
+ha_status hash_attn_select(const ha_shape* shape, const uint32_t* q_sig, const uint32_t* k_sig,
+                           const int32_t* seq_lens, const int32_t* m_per_seq, int32_t m, int32_t n_sink,
+                           int32_t n_local, int32_t* sel_idx, int32_t* sel_cnt, void* workspace, size_t ws_bytes,
+                           void* stream) {
+    return hash_attn_select_ex(shape, q_sig, k_sig, seq_lens, m_per_seq, m, n_sink, n_local, nullptr, sel_idx,
+                               sel_cnt, workspace, ws_bytes, stream);
 }
 
 ha_status hash_attn_gather_att(const ha_shape* shape, const void* q, const void* K, const void* V,

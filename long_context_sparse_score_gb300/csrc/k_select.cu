@@ -67,9 +67,28 @@ __device__ __forceinline__ uint32_t field(uint32_t w01, uint32_t w23, int e) {
     return (e & 1) ? (w >> 16) : (w & 0xffffu);
 }
 
+// Tokens of [a, z) at distance t from qs, counted by the whole warp (every lane
+// gets the total); 8 loads in flight per lane.
+__device__ __forceinline__ int count_at(const uint32_t* __restrict__ row, int a, int z, uint32_t qs, int t) {
+    const int lane = threadIdx.x & 31;
+    int c = 0;
+    for (int i0 = a; i0 < z; i0 += 256) {
+        uint32_t cd[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = i0 + 32 * u + lane;
+            cd[u] = (i < z) ? __ldg(row + i) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) c += (i0 + 32 * u + lane < z && __popc(qs ^ cd[u]) == t) ? 1 : 0;
+    }
+    return __reduce_add_sync(0xffffffffu, c);
+}
+
 // ---------------------------------------------------------------- SCORE
 
-template <int TPT, bool WRITE_DIST>
+// VARIANTS: per-head budgets / exclusive windows compiled in (launched only when asked for).
+template <int TPT, bool WRITE_DIST, bool VARIANTS>
 __global__ void __launch_bounds__(kScoreThreads, 5) k_score(const ScoreParams p) {
     constexpr int C = kScoreThreads * TPT;
     constexpr int SC = 32 * TPT;
@@ -165,10 +184,24 @@ __global__ void __launch_bounds__(kScoreThreads, 5) k_score(const ScoreParams p)
             mb = min(max(mb, 0), p.m);
         }
     }
-    const int k = min(mb, n);  // tokens taken by score
+    const int wlo = min(p.n_sink, n), whi = max(0, n - p.n_local);
+    const int wmid = max(whi, wlo);         // windows: [0, wlo) and [wmid, n)
+    const int nwin = wlo + (n - wmid);
     for (int e = warp; e < p.G; e += kWarps) {
         const int64_t h = head0 + e;
         const uint32_t* H = p.chunk_hist + h * p.nchunks * HA_NBINS;
+        const int excl = VARIANTS ? p.excl : 0;
+        int mh = mb;
+        if (VARIANTS && p.m_per_head != nullptr) {
+            mh = p.m_per_head[h];
+            if (mh < 0 || mh > p.m) {
+                if (lane == 0) flag_error(p.err, HA_DEVERR_BUDGET);
+                mh = min(max(mh, 0), p.m);
+            }
+        }
+        // tokens taken by score: from all n, or (exclusive windows) from those outside the windows
+        const int k = excl ? min(mh, n - nwin) : min(mh, n);
+        const uint32_t qs = excl ? p.q_sig[h] : 0u;  // needed for the window tokens only
         // bins 0..31 (bin 32 is implied: the cumulative count reaches n there)
         uint32_t tot = 0;
         for (int c0b = 0; c0b < nch; c0b += 8) {
@@ -177,6 +210,20 @@ __global__ void __launch_bounds__(kScoreThreads, 5) k_score(const ScoreParams p)
             for (int u = 0; u < 8; ++u) v[u] = (c0b + u < nch) ? __ldcg(H + (c0b + u) * HA_NBINS + lane) : 0u;
 #pragma unroll
             for (int u = 0; u < 8; ++u) tot += v[u];
+        }
+        if (excl) {
+            // the window tokens leave the ranking: their distance counts come off the totals
+            // (this warp's slice of the CTA's histogram storage, free after the chunk pass)
+            uint32_t* wh = &hist[0][0][0] + warp * HA_NBINS;
+            for (int u = lane; u < HA_NBINS; u += 32) wh[u] = 0u;
+            __syncwarp();
+            for (int i = lane; i < nwin; i += 32) {
+                const int tok = (i < wlo) ? i : wmid + (i - wlo);
+                atomicAdd(&wh[__popc(qs ^ __ldg(row + tok))], 1u);
+            }
+            __syncwarp();
+            tot -= wh[lane];
+            __syncwarp();
         }
         uint32_t incl = tot;
 #pragma unroll
@@ -191,7 +238,22 @@ __global__ void __launch_bounds__(kScoreThreads, 5) k_score(const ScoreParams p)
         int carry = 0;  // tied tokens in the chunks before
         for (int base = 0; base < nch; base += 32) {
             const int cc = base + lane;
-            const int v = (cc < nch) ? (int)__ldcg(H + cc * HA_NBINS + t) : 0;
+            int v = (cc < nch) ? (int)__ldcg(H + cc * HA_NBINS + t) : 0;
+            if (excl) {
+                // ties inside the windows are not ties of the ranking
+                const int cb = cc * C, ce = min(n, cb + C);
+                const int sa = cb, sz = min(ce, wlo), la = max(cb, wmid), lz = ce;
+                unsigned pend = __ballot_sync(0xffffffffu, cc < nch && (sz > sa || lz > la));
+                while (pend != 0u) {
+                    const int j = __ffs(pend) - 1;
+                    pend &= pend - 1u;
+                    const int cnt = count_at(row, __shfl_sync(0xffffffffu, sa, j), __shfl_sync(0xffffffffu, sz, j),
+                                             qs, t) +
+                                    count_at(row, __shfl_sync(0xffffffffu, la, j), __shfl_sync(0xffffffffu, lz, j),
+                                             qs, t);
+                    if (lane == j) v -= cnt;
+                }
+            }
             int in = v;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -260,7 +322,8 @@ __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
 // whole warp calls this together to rank ties across lanes). `codes` are the
 // lane's codes in the shared tile.
 __device__ __noinline__ uint32_t lane_mask_slow(const uint32_t* codes, uint32_t qs, int t, int mode,
-                                                int qw, int lbase, int tpt, int n, int wlo, int whi) {
+                                                int qw, int lbase, int tpt, int n, int wlo, int whi,
+                                                int excl) {
     const int teff = (mode == 1) ? t : t - 1;
     uint32_t m = 0u, tie = 0u;
     for (int j = 0; j < tpt; ++j) {
@@ -270,7 +333,7 @@ __device__ __noinline__ uint32_t lane_mask_slow(const uint32_t* codes, uint32_t 
         const bool inw = (i < wlo) || (i >= whi);
         const bool take = (mode == 2) ? (d < t) : (d <= teff);
         if (inw || take) m |= 1u << j;
-        if (d == t) tie |= 1u << j;
+        if (d == t && !(excl && inw)) tie |= 1u << j;  // with exclusive windows a window token is never a tie
     }
     if (mode == 2) {
         const uint32_t c = (uint32_t)__popc(tie);
@@ -293,9 +356,10 @@ __device__ __noinline__ uint32_t lane_mask_slow(const uint32_t* codes, uint32_t 
 //   mode 2: the first qw tied tokens of the sub-chunk (token order) are taken
 template <int TPT>
 __device__ __forceinline__ uint32_t lane_mask(const uint32_t (&code)[TPT], const uint32_t* tile_row, uint32_t qs,
-                                              int t, int mode, int qw, int lbase, int n, int wlo, int whi) {
+                                              int t, int mode, int qw, int lbase, int n, int excl, int wlo,
+                                              int whi) {
     const bool edge = (lbase < wlo) || (lbase + TPT > whi) || (lbase + TPT > n);
-    if (edge || mode == 2) return lane_mask_slow(tile_row, qs, t, mode, qw, lbase, TPT, n, wlo, whi);
+    if (edge || mode == 2) return lane_mask_slow(tile_row, qs, t, mode, qw, lbase, TPT, n, wlo, whi, excl);
     const int teff = (mode == 1) ? t : t - 1;
     uint32_t m = 0u;
 #pragma unroll
@@ -363,7 +427,8 @@ __global__ void __launch_bounds__(kScoreThreads, 4) k_select(const SelectParams 
                     uint32_t cnt = 0;
 #pragma unroll
                     for (int j = 0; j < TPT; ++j)
-                        cnt += (lbase + j < n && (int)__popc(qs[e] ^ code[j]) == t[e]) ? 1u : 0u;
+                        cnt += (lbase + j < n && (int)__popc(qs[e] ^ code[j]) == t[e] &&
+                                !(p.excl && (lbase + j < wlo || lbase + j >= whi))) ? 1u : 0u;
                     cnt = __reduce_add_sync(0xffffffffu, cnt);
                     if (lane == 0) s_wt[e][warp] = (int)cnt;
                 }
@@ -385,7 +450,7 @@ __global__ void __launch_bounds__(kScoreThreads, 4) k_select(const SelectParams 
         uint32_t c01 = 0u, c23 = 0u;  // per-lane counts, 16-bit fields
 #pragma unroll
         for (int e = 0; e < kMaxHeadsPerPass; ++e) {
-            msk[e] = (e < nh) ? lane_mask<TPT>(code, &s_codes[warp][lane][0], qs[e], t[e], mode[e], qw[e], lbase, n,
+            msk[e] = (e < nh) ? lane_mask<TPT>(code, &s_codes[warp][lane][0], qs[e], t[e], mode[e], qw[e], lbase, n, p.excl,
                                                  wlo, whi)
                                : 0u;
             const uint32_t c = (uint32_t)__popc(msk[e]);
@@ -498,14 +563,14 @@ __global__ void __launch_bounds__(64) k_hist(const HistParams p) {
     p.hist[(int64_t)head * HA_NBINS + u] = s;
 }
 
-template <bool WD>
+template <bool WD, bool VAR>
 cudaError_t launch_score_t(const ScoreParams& p, int batch_hkv, cudaStream_t st) {
     const dim3 grid((unsigned)batch_hkv * (unsigned)p.nchunks);
     switch (p.chunk / kScoreThreads) {
-        case 4: k_score<4, WD><<<grid, kScoreThreads, 0, st>>>(p); break;
-        case 8: k_score<8, WD><<<grid, kScoreThreads, 0, st>>>(p); break;
-        case 16: k_score<16, WD><<<grid, kScoreThreads, 0, st>>>(p); break;
-        case 32: k_score<32, WD><<<grid, kScoreThreads, 0, st>>>(p); break;
+        case 4: k_score<4, WD, VAR><<<grid, kScoreThreads, 0, st>>>(p); break;
+        case 8: k_score<8, WD, VAR><<<grid, kScoreThreads, 0, st>>>(p); break;
+        case 16: k_score<16, WD, VAR><<<grid, kScoreThreads, 0, st>>>(p); break;
+        case 32: k_score<32, WD, VAR><<<grid, kScoreThreads, 0, st>>>(p); break;
         default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
@@ -514,7 +579,10 @@ cudaError_t launch_score_t(const ScoreParams& p, int batch_hkv, cudaStream_t st)
 }  // namespace
 
 cudaError_t launch_score(const ScoreParams& p, int batch_hkv, cudaStream_t st) {
-    return p.dist != nullptr ? launch_score_t<true>(p, batch_hkv, st) : launch_score_t<false>(p, batch_hkv, st);
+    // the distance-writing entry point computes no thresholds, so it needs no variants
+    if (p.dist != nullptr) return launch_score_t<true, false>(p, batch_hkv, st);
+    if (p.excl || p.m_per_head != nullptr) return launch_score_t<false, true>(p, batch_hkv, st);
+    return launch_score_t<false, false>(p, batch_hkv, st);
 }
 
 cudaError_t launch_select(const SelectParams& p, int batch_hkv, cudaStream_t st, bool pdl) {

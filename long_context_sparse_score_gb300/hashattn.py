@@ -37,13 +37,28 @@ HA_NOALLOC_SCRATCH_BYTES = 16 << 20
 # Entry points declared in include/hashattn.h (checked by the tests).
 EXPORTED = [
     "hash_attn_workspace_size", "hash_attn_workspace_init", "hash_attn_select_capacity",
-    "hash_attn_decode", "hash_attn_decode_timed", "hash_attn_score", "hash_attn_select",
+    "hash_attn_decode", "hash_attn_decode_ex", "hash_attn_decode_timed", "hash_attn_score", "hash_attn_select",
+    "hash_attn_select_ex",
     "hash_attn_gather_att", "hash_attn_gather_att_noalloc", "hash_attn_merge", "hash_attn_merge_n",
     "hash_attn_encode_queries", "hash_attn_encode_keys", "hash_attn_topk_exact_workspace_size",
     "hash_attn_topk_exact", "hash_attn_recall",
     "hash_attn_device_status",
     "hash_attn_status_string", "hash_attn_last_error",
 ]
+
+
+class HASelectOpts(ctypes.Structure):
+    """Mirror of ``ha_select_opts``."""
+
+    _fields_ = [("m_per_head", ctypes.c_void_p), ("exclusive_windows", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 3)]
+
+
+def select_opts(m_per_head=None, exclusive_windows=False) -> HASelectOpts:
+    o = HASelectOpts()
+    o.m_per_head = _ptr(m_per_head)
+    o.exclusive_windows = 1 if exclusive_windows else 0
+    return o
 
 
 class HAShape(ctypes.Structure):
@@ -89,6 +104,9 @@ def lib() -> ctypes.CDLL:
     L.hash_attn_select_capacity.restype = _I32
     dec = [SP, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _P, _P, _SZ, _P]
     L.hash_attn_decode.argtypes = dec
+    OP = ctypes.POINTER(HASelectOpts)
+    L.hash_attn_decode_ex.argtypes = dec[:11] + [OP] + dec[11:]
+    L.hash_attn_select_ex.argtypes = [SP, _P, _P, _P, _P, _I32, _I32, _I32, OP, _P, _P, _P, _SZ, _P]
     L.hash_attn_decode_timed.argtypes = dec + [ctypes.POINTER(_P)]
     L.hash_attn_score.argtypes = [SP, _P, _P, _P, _P, _P, _P, _SZ, _P]
     L.hash_attn_select.argtypes = [SP, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _SZ, _P]
@@ -204,6 +222,16 @@ def hash_attn_decode(shape, q, q_sig, k_sig, K, V, seq_lens, m_per_seq, m, n_sin
                                   _stream(stream)))
 
 
+def hash_attn_decode_ex(shape, q, q_sig, k_sig, K, V, seq_lens, m_per_seq, m, n_sink, n_local, opts,
+                        out, lse, sel_idx=None, sel_cnt=None, *, workspace, stream=None) -> None:
+    """``opts``: an HASelectOpts (see ``select_opts``) or None."""
+    ws, nb = _ws(workspace)
+    _check(lib().hash_attn_decode_ex(ctypes.byref(shape), _ptr(q), _ptr(q_sig), _ptr(k_sig), _ptr(K), _ptr(V),
+                                     _ptr(seq_lens), _ptr(m_per_seq), m, n_sink, n_local,
+                                     None if opts is None else ctypes.byref(opts), _ptr(out), _ptr(lse),
+                                     _ptr(sel_idx), _ptr(sel_cnt), ws, nb, _stream(stream)))
+
+
 def hash_attn_decode_timed(shape, q, q_sig, k_sig, K, V, seq_lens, m_per_seq, m, n_sink, n_local,
                            out, lse, events, sel_idx=None, sel_cnt=None, *, workspace,
                            stream=None) -> None:
@@ -229,6 +257,15 @@ def hash_attn_select(shape, q_sig, k_sig, seq_lens, m_per_seq, m, n_sink, n_loca
     _check(lib().hash_attn_select(ctypes.byref(shape), _ptr(q_sig), _ptr(k_sig), _ptr(seq_lens),
                                   _ptr(m_per_seq), m, n_sink, n_local, _ptr(sel_idx), _ptr(sel_cnt),
                                   ws, nb, _stream(stream)))
+
+
+def hash_attn_select_ex(shape, q_sig, k_sig, seq_lens, m_per_seq, m, n_sink, n_local, opts, sel_idx, sel_cnt,
+                        *, workspace, stream=None) -> None:
+    ws, nb = _ws(workspace)
+    _check(lib().hash_attn_select_ex(ctypes.byref(shape), _ptr(q_sig), _ptr(k_sig), _ptr(seq_lens),
+                                     _ptr(m_per_seq), m, n_sink, n_local,
+                                     None if opts is None else ctypes.byref(opts), _ptr(sel_idx), _ptr(sel_cnt),
+                                     ws, nb, _stream(stream)))
 
 
 def hash_attn_gather_att(shape, q, K, V, seq_lens, idx, idx_cap, cnt, out, lse, *, workspace,

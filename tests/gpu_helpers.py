@@ -26,8 +26,10 @@ def workspace(shape, m, n_sink, n_local, device="cuda"):
     return ws
 
 
-def run_decode(w, *, m=None, m_per_seq="workload", sel=True, K=None, V=None, ws=None, dense=False):
-    """Decode a workload through the C ABI; returns a dict of outputs and the device status."""
+def run_decode(w, *, m=None, m_per_seq="workload", sel=True, K=None, V=None, ws=None, dense=False,
+               exclusive=False, m_per_head=None):
+    """Decode a workload through the C ABI; returns a dict of outputs and the device status.
+    ``exclusive`` / ``m_per_head`` go through hash_attn_decode_ex."""
     H = ha()
     K = w.K if K is None else K
     V = w.V if V is None else V
@@ -46,8 +48,13 @@ def run_decode(w, *, m=None, m_per_seq="workload", sel=True, K=None, V=None, ws=
     if sel and not (m >= K.shape[2] and mps is None):
         sel_idx = torch.full((B, Hq, max(cap, 1)), -7, dtype=torch.int32, device=w.q.device)
         sel_cnt = torch.full((B, Hq), -7, dtype=torch.int32, device=w.q.device)
-    H.hash_attn_decode(shape, w.q, q_sig, k_sig, K, V, w.seq_lens, mps, m, w.n_sink, w.n_local,
-                       out, lse, sel_idx, sel_cnt, workspace=ws)
+    if exclusive or m_per_head is not None:
+        opts = H.select_opts(m_per_head, exclusive)
+        H.hash_attn_decode_ex(shape, w.q, q_sig, k_sig, K, V, w.seq_lens, mps, m, w.n_sink, w.n_local, opts,
+                              out, lse, sel_idx, sel_cnt, workspace=ws)
+    else:
+        H.hash_attn_decode(shape, w.q, q_sig, k_sig, K, V, w.seq_lens, mps, m, w.n_sink, w.n_local,
+                           out, lse, sel_idx, sel_cnt, workspace=ws)
     st, flags = H.hash_attn_device_status(ws)
     return dict(out=out, lse=lse, sel_idx=sel_idx, sel_cnt=sel_cnt, status=st, flags=flags, ws=ws,
                 cap=cap)
@@ -56,8 +63,10 @@ def run_decode(w, *, m=None, m_per_seq="workload", sel=True, K=None, V=None, ws=
 class HostCopy:
     """Per-(batch, KV head) host copies of a workload, made on demand."""
 
-    def __init__(self, w, K=None, V=None):
+    def __init__(self, w, K=None, V=None, exclusive=False, m_per_head=None):
         self.w = w
+        self.exclusive = exclusive
+        self.mph = None if m_per_head is None else m_per_head.cpu().numpy()
         self.K = w.K if K is None else K
         self.V = w.V if V is None else V
         self.q = w.q.float().cpu().numpy()
@@ -83,14 +92,16 @@ class HostCopy:
             self._codes[key] = self.w.k_sig[bk, g].cpu().numpy().astype(np.int64)
         return self._codes[key]
 
-    def budget(self, b, m):
+    def budget(self, b, m, h=None):
+        if self.mph is not None and h is not None:
+            return int(self.mph[b, h])
         return int(self.mps[b]) if self.mps is not None else m
 
     def select(self, b, h, m):
         G = self.w.Hq // self.w.Hkv
         n = int(self.lens[b])
-        return O.selected_set(int(self.q_sig[b, h]), self.codes(b, h // G), n, self.budget(b, m),
-                              self.w.n_sink, self.w.n_local)
+        return O.selected_set(int(self.q_sig[b, h]), self.codes(b, h // G), n, self.budget(b, m, h),
+                              self.w.n_sink, self.w.n_local, exclusive=self.exclusive)
 
     def head(self, b, h, m, dense=False):
         G = self.w.Hq // self.w.Hkv
@@ -99,7 +110,8 @@ class HostCopy:
         n = int(self.lens[b])
         codes = None if dense else self.codes(b, g)
         return O.decode_head(self.q[b, h], None if dense else int(self.q_sig[b, h]), codes, Kh, Vh, n,
-                             self.budget(b, m), self.w.n_sink, self.w.n_local, dense=dense)
+                             self.budget(b, m, h), self.w.n_sink, self.w.n_local, dense=dense,
+                             exclusive=self.exclusive)
 
 
 def assert_out_close(got, ref, what=""):

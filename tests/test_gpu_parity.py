@@ -132,6 +132,59 @@ def test_windows_across_chunks_and_tie_boundary(case):
     GH.check_attention(res, hc, all_heads(w)[:4], m)
 
 
+VARIANT_CASES = [
+    # name, n_cap, lens, m, S, Lw, codes ("random" | "pool"), exclusive, per-head budgets
+    ("exclusive_random", 9000, [9000, 7001], 700, 64, 128, "random", True, False),
+    ("exclusive_tie_pool", 9000, [9000, 8500], 1200, 1500, 2500, "pool", True, False),
+    ("exclusive_quota_in_window_chunks", 5000, [5000, 4667], 900, 1000, 300, "pool", True, False),
+    ("per_head_budgets", 6000, [6000, 3001], 500, 16, 32, "random", False, True),
+    ("per_head_budgets_exclusive", 6000, [6000, 4444], 500, 300, 200, "pool", True, True),
+]
+
+
+@pytest.mark.parametrize("case", VARIANT_CASES, ids=[c[0] for c in VARIANT_CASES])
+def test_selection_variants(case):
+    """Exclusive windows (top-m over the tokens outside the windows) and per-head
+    budgets through hash_attn_decode_ex, against the oracle."""
+    name, n_cap, lens, m, S, Lw, codes, exclusive, per_head = case
+    w = W().make_gqa(23, B=2, Hq=8, Hkv=2, d=128, n_cap=n_cap, seq_lens=lens, m=m, n_sink=S, n_local=Lw,
+                     device="cuda", name=name)
+    if codes == "pool":
+        q0 = 0x0F0F0F0F
+        gen = torch.Generator(device="cuda").manual_seed(6)
+        pool = torch.tensor([q0, q0 ^ 1, q0 ^ 3, q0 ^ 0x70000000], dtype=torch.int32, device="cuda")
+        w.k_sig = pool[torch.randint(0, 4, w.k_sig.shape, generator=gen, device="cuda")].contiguous()
+        w.q_sig = torch.full_like(w.q_sig, q0)
+    mph = None
+    if per_head:
+        gen = torch.Generator(device="cuda").manual_seed(7)
+        mph = torch.randint(0, m + 1, (2, 8), generator=gen, device="cuda", dtype=torch.int32)
+        mph[0, 0], mph[1, 7] = 0, m
+    res = GH.run_decode(w, exclusive=exclusive, m_per_head=mph)
+    assert res["status"] == 0, res["flags"]
+    hc = GH.HostCopy(w, exclusive=exclusive, m_per_head=mph)
+    GH.check_selection(res, hc, all_heads(w), m)
+    GH.check_attention(res, hc, all_heads(w)[::3], m)
+    if exclusive:
+        cnt = res["sel_cnt"].cpu().numpy()
+        for b, n in enumerate(lens):
+            W_ = len(O.window_positions(n, S, Lw))
+            for h in range(8):
+                mb = int(mph[b, h]) if per_head else m
+                assert int(cnt[b, h]) == min(n, mb + W_)
+
+
+def test_per_head_budget_above_bound_is_flagged():
+    H = GH.ha()
+    w = W().make_gqa(24, B=1, Hq=4, Hkv=1, d=128, n_cap=3000, seq_lens=[3000], m=100, n_sink=4, n_local=4,
+                     device="cuda")
+    mph = torch.tensor([[100, 150, -3, 7]], dtype=torch.int32, device="cuda")
+    res = GH.run_decode(w, m_per_head=mph)
+    assert res["status"] == H.HA_ERR_DEVICE and res["flags"] & H.HA_DEVERR_BUDGET
+    hc = GH.HostCopy(w, m_per_head=torch.tensor([[100, 100, 0, 7]], dtype=torch.int32))
+    GH.check_selection(res, hc, all_heads(w), 100)
+
+
 def test_ragged_per_sequence_budget():
     lens = [4096, 9000, 1, 0, 12000, 6000]
     wl = W()
