@@ -74,10 +74,18 @@ def popcount32(x) -> np.ndarray:
 
 
 def hamming_distances(q_code, k_codes) -> np.ndarray:
-    """popcount(h_q XOR h_i) for every key code h_i (the negated SCORE)."""
-    q = np.int64(int(q_code) & 0xFFFFFFFF)
+    """popcount(h_q XOR h_i) for every key code h_i (the negated SCORE).
+
+    32-bit codes: ``q_code`` an integer, ``k_codes`` [n]. Wider codes (HashAttention
+    Sec. 5 varies the signature length): ``q_code`` [W] and ``k_codes`` [n, W]
+    32-bit words; the distance sums over the words.
+    """
     k = np.asarray(k_codes).astype(np.int64) & 0xFFFFFFFF
-    return popcount32(k ^ q)
+    if k.ndim == 1:
+        q = np.int64(int(q_code) & 0xFFFFFFFF)
+        return popcount32(k ^ q)
+    q = (np.asarray(q_code).astype(np.int64) & 0xFFFFFFFF).reshape(1, -1)
+    return popcount32(k ^ q).sum(axis=1)
 
 
 def encode(x, W) -> int:
@@ -111,9 +119,9 @@ def encode_ambiguous(x, W, eps: float = 2.0 ** -22) -> int:
     return mask
 
 
-def distance_histogram(dist) -> np.ndarray:
-    """Count of tokens at each distance 0..32."""
-    return np.bincount(np.asarray(dist, dtype=np.int64), minlength=N_BINS)[:N_BINS]
+def distance_histogram(dist, nbins: int = N_BINS) -> np.ndarray:
+    """Count of tokens at each distance 0..nbins-1 (33 bins for 32-bit codes, b + 1 for b bits)."""
+    return np.bincount(np.asarray(dist, dtype=np.int64), minlength=nbins)[:nbins]
 
 
 # ---------------------------------------------------------------------------

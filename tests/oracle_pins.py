@@ -436,6 +436,34 @@ def check_exclusive_windows(o):
         assert np.array_equal(idx, want)
 
 
+def check_wide_codes(o):
+    """Codes of W 32-bit words: the distance is the bit count of the XOR of the
+    concatenated integers (Python big ints), the histogram has 32 W + 1 bins, and
+    the selection is the brute-force rank over those distances."""
+    rng = np.random.default_rng(59)
+    for W in (2, 4, 16):
+        n = 60
+        k = rng.integers(0, 2 ** 32, (n, W))
+        if W == 2:
+            k[rng.integers(0, n, 20)] = k[0]   # repeated codes: ties
+        q = rng.integers(0, 2 ** 32, W)
+        big = lambda words: sum(int(x) << (32 * j) for j, x in enumerate(words))
+        want = [bin(big(k[i]) ^ big(q)).count("1") for i in range(n)]
+        d = o.hamming_distances(q, k)
+        assert list(d) == want
+        h = o.distance_histogram(d, 32 * W + 1)
+        assert len(h) == 32 * W + 1 and h.sum() == n and all(h[v] == want.count(v) for v in set(want))
+        m, S, L = 17, 3, 5
+        rank = _rank_bruteforce(want)
+        top = {i for i in range(n) if rank[i] < m}
+        win = set(range(S)) | set(range(n - L, n))
+        assert set(o.selected_set(q, k, n, m, S, L)) == top | win
+    # one word in the wide layout equals the 32-bit path
+    k1 = rng.integers(0, 2 ** 32, (30, 1))
+    q1 = rng.integers(0, 2 ** 32, 1)
+    assert np.array_equal(o.hamming_distances(q1, k1), o.hamming_distances(int(q1[0]), k1[:, 0]))
+
+
 def check_decode_composition(o):
     """decode_head = attend over selected_set, and decode_batch maps h to KV head h // G."""
     rng = np.random.default_rng(37)
@@ -469,7 +497,7 @@ ALL_CHECKS = [
     check_dense_vs_sdpa, check_decimal, check_weighted_sum, check_lse_bounds,
     check_lse_gradient, check_low_temperature, check_empty,
     check_merge_partition, check_merge_segments, check_encode, check_exact_topm_and_recall,
-    check_exclusive_windows, check_decode_composition,
+    check_exclusive_windows, check_wide_codes, check_decode_composition,
 ]
 
 

@@ -51,6 +51,7 @@ MUTATIONS = [
     ("exact_topm_ties_to_larger_index", "order = np.lexsort((np.arange(n), -z))  # score descending",
      "order = np.lexsort((-np.arange(n), -z))  # score descending"),
     ("recall_over_selected", "    return hit / ref.size", "    return hit / max(1, np.unique(np.asarray(selected)).size)"),
+    ("wide_distance_first_word_only", "    return popcount32(k ^ q).sum(axis=1)", "    return popcount32(k ^ q)[:, 0]"),
     ("encode_zero_sets_bit", "        if proj[j] > 0.0:", "        if proj[j] >= 0.0:"),
     ("encode_bit_order_reversed", "            code |= 1 << j", "            code |= 1 << (31 - j)"),
     ("encode_transposed_projection", "proj = np.asarray(W, dtype=np.float64) @ np.asarray(x, dtype=np.float64)",
