@@ -306,6 +306,35 @@ def measure_variants(w, shape, ws, out, lse, dev):
     st, flags = H.hash_attn_device_status(ws)
     if st != 0:
         raise RuntimeError(f"selection variants: device status {st} flags {flags:#x}")
+    # 128-bit codes (4 words per token, random) on the same cache
+    Wd = 4
+    k4 = torch.randint(-2 ** 31, 2 ** 31 - 1, (w.B, w.Hkv, w.n_cap, Wd), generator=g, device=dev,
+                       dtype=torch.int64).to(torch.int32)
+    q4 = torch.randint(-2 ** 31, 2 ** 31 - 1, (w.B, w.Hq, Wd), generator=g, device=dev,
+                       dtype=torch.int64).to(torch.int32)
+    shape4 = H.make_shape(w.q, w.K, w.V, k4)
+    opts4 = H.select_opts(None, False, Wd)
+    ws4 = torch.empty(H.hash_attn_workspace_size_ex(shape4, w.m, w.n_sink, w.n_local, opts4), dtype=torch.uint8,
+                      device=dev)
+    H.hash_attn_workspace_init(ws4)
+    call = lambda: H.hash_attn_decode_ex(shape4, w.q, q4, k4, w.K, w.V, w.seq_lens, None, w.m, w.n_sink,
+                                         w.n_local, opts4, out, lse, workspace=ws4)
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 50
+    e0.record()
+    for _ in range(reps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    st, flags = H.hash_attn_device_status(ws4)
+    if st != 0:
+        raise RuntimeError(f"128-bit codes: device status {st} flags {flags:#x}")
+    res["codes_128bit"] = {"ms_per_step": ms, "query_heads_per_s": w.B * w.Hq / (ms * 1e-3),
+                           "code_bytes": k4.numel() * 4, "note": "random 4-word codes; generic wide SCORE/TOPK"}
     return res
 
 

@@ -169,13 +169,28 @@ ha_status hash_attn_decode_timed(const ha_shape* shape, const void* q, const uin
  *                      the windows (|I| <= m + windows). 1: the top-m is taken
  *                      over the tokens outside the windows, so
  *                      |I| = min(n, m + |windows|) exactly.
+ *   code_words         W, the 32-bit words of every code: 0 or 1 (32-bit codes,
+ *                      the layout of ha_shape), 2, 4, 8 or 16 (b = 32 W bits,
+ *                      HashAttention Sec. 5 varies the signature length). Then
+ *                      q_sig is [batch, h_q, W] words, word w of token i's code
+ *                      is k_sig[b * ks_sb + g * ks_sh + i * W + w] (ks_* in
+ *                      words, rows 16-byte aligned, ks_sh >= n_cap * W), and the
+ *                      distance is summed over the words (b + 1 values). Codes
+ *                      wider than 32 bits take the default budget rules
+ *                      (m_per_head and exclusive_windows unset), and the
+ *                      workspace must come from hash_attn_workspace_size_ex.
  *   reserved           must be zero.
  */
 typedef struct {
     const int32_t* m_per_head;
     int32_t exclusive_windows;
-    int32_t reserved[3];
+    int32_t code_words;
+    int32_t reserved[2];
 } ha_select_opts;
+
+/* hash_attn_workspace_size for the given selection options (opts may be NULL). */
+ha_status hash_attn_workspace_size_ex(const ha_shape* shape, int32_t m_max, int32_t n_sink, int32_t n_local,
+                                      const ha_select_opts* opts, size_t* bytes);
 
 /*
  * hash_attn_decode with selection options (opts may be NULL: the defaults of

@@ -47,6 +47,7 @@ struct Layout {
     int rows_cap = 0;        // most rows one head attends to
     int splits = 1;          // GATHER-ATT CTAs per head
     int rows_per_split = 0;  // multiple of kTileRows
+    int nbins = HA_NBINS;    // distance bins per chunk histogram (b + 1 for b-bit codes)
     size_t off_err = 0, off_counter = 0, off_hist = 0, off_segcnt = 0, off_seg = 0, off_part = 0;
     size_t off_scnt = 0, off_meta_t = 0, off_meta_qt = 0;
     size_t total = 0;
@@ -58,7 +59,7 @@ int choose_chunk(int64_t batch_hkv, int64_t n_cap);
 // Split-K policy for GATHER-ATT.
 void choose_splits(int64_t heads, int64_t rows_cap, int* splits, int* rows_per_split);
 // Full layout; with_selection=false leaves out the chunk_hist / seg regions.
-Layout make_layout(const ha_shape& s, int64_t rows_cap, bool with_selection);
+Layout make_layout(const ha_shape& s, int64_t rows_cap, bool with_selection, int nbins = HA_NBINS);
 
 // ------------------------------------------------------------------ parameters
 
@@ -170,6 +171,27 @@ struct EncodeParams {
     int B, Hq, Hkv, G, d, n_cap, keys;
 };
 
+// SCORE/TOPK for codes of W > 1 words (b = 32 W bits, NB = b + 1 bins); the
+// output segments are those of the 32-bit path.
+struct WideParams {
+    const uint32_t* q_sig;   // [B * Hq][W]
+    const uint32_t* k_sig;   // word w of token i: b * ks_sb + g * ks_sh + i * W + w
+    int64_t ks_sb, ks_sh;
+    const int32_t* seq_lens;
+    int B, Hq, Hkv, G, n_cap, W, NB;
+    int chunk, nchunks;
+    uint32_t* chunk_hist;    // [heads][nchunks][NB]
+    uint32_t* counters;
+    uint32_t* err;
+    const int32_t* m_per_seq;
+    int m, n_sink, n_local;
+    uint32_t* score_cnt;
+    int32_t* meta_t;
+    int2* meta_qt;
+    int32_t* seg_cnt;
+    int32_t* seg_idx;
+};
+
 // Exact top-m by dot score (the comparator of the hashed selection).
 struct ExactParams {
     const void* q;
@@ -229,6 +251,8 @@ cudaError_t launch_merge_n(const MergeNParams& p, cudaStream_t st);
 cudaError_t launch_encode(const EncodeParams& p, cudaStream_t st);
 cudaError_t launch_topk_exact(const ExactParams& p, int d, int kv_bf16, cudaStream_t st);
 cudaError_t launch_recall(const RecallParams& p, cudaStream_t st);
+cudaError_t launch_score_wide(const WideParams& p, int batch_hkv, cudaStream_t st);
+cudaError_t launch_select_wide(const WideParams& p, int batch_hkv, cudaStream_t st, bool pdl);
 
 // ------------------------------------------------------------------ device helpers
 

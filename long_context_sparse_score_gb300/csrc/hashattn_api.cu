@@ -246,9 +246,59 @@ ha_status check_opts(const ha_select_opts* o) {
     if (o == nullptr) return HA_OK;
     if (o->exclusive_windows != 0 && o->exclusive_windows != 1)
         return fail(HA_ERR_INVALID_ARG, "exclusive_windows must be 0 or 1 (got %d)", o->exclusive_windows);
-    for (int i = 0; i < 3; ++i)
+    const int w = o->code_words;
+    if (w != 0 && w != 1 && w != 2 && w != 4 && w != 8 && w != 16)
+        return fail(HA_ERR_UNSUPPORTED, "code_words must be 1, 2, 4, 8 or 16 (got %d)", w);
+    if (w > 1 && (o->exclusive_windows || o->m_per_head != nullptr))
+        return fail(HA_ERR_UNSUPPORTED, "codes wider than 32 bits take the default budget rules only");
+    for (int i = 0; i < 2; ++i)
         if (o->reserved[i] != 0) return fail(HA_ERR_INVALID_ARG, "ha_select_opts.reserved must be zero");
     return HA_OK;
+}
+
+int code_words_of(const ha_select_opts* o) { return (o != nullptr && o->code_words > 1) ? o->code_words : 1; }
+
+int nbins_of(const ha_select_opts* o) { return 32 * code_words_of(o) + 1; }
+
+ha_status check_wide_codes(const ha_shape* s, const uint32_t* q_sig, const uint32_t* k_sig, int W) {
+    if (q_sig == nullptr || k_sig == nullptr) return fail(HA_ERR_INVALID_ARG, "q_sig or k_sig is NULL");
+    if (!aligned16(k_sig) || s->ks_sh % 4 != 0 || s->ks_sb % 4 != 0 || s->ks_sh < (int64_t)s->n_cap * W)
+        return fail(HA_ERR_INVALID_ARG,
+                    "wide k_sig rows must start on 16-byte boundaries and hold n_cap * code_words words");
+    return HA_OK;
+}
+
+WideParams wide_params(const ha_shape* s, const Layout& lay, const Views& v, const uint32_t* q_sig,
+                       const uint32_t* k_sig, const int32_t* seq_lens, const int32_t* m_per_seq, int32_t m,
+                       int32_t n_sink, int32_t n_local, int W) {
+    WideParams p{};
+    p.q_sig = q_sig;
+    p.k_sig = k_sig;
+    p.ks_sb = s->ks_sb;
+    p.ks_sh = s->ks_sh;
+    p.seq_lens = seq_lens;
+    p.B = s->batch;
+    p.Hq = s->h_q;
+    p.Hkv = s->h_kv;
+    p.G = s->h_q / s->h_kv;
+    p.n_cap = s->n_cap;
+    p.W = W;
+    p.NB = 32 * W + 1;
+    p.chunk = lay.chunk;
+    p.nchunks = lay.nchunks;
+    p.chunk_hist = v.chunk_hist;
+    p.counters = v.counters;
+    p.err = v.err;
+    p.m_per_seq = m_per_seq;
+    p.m = m;
+    p.n_sink = n_sink;
+    p.n_local = n_local;
+    p.score_cnt = v.score_cnt;
+    p.meta_t = v.meta_t;
+    p.meta_qt = v.meta_qt;
+    p.seg_cnt = v.seg_cnt;
+    p.seg_idx = v.seg_idx;
+    return p;
 }
 
 // The selection options into the SCORE/TOPK parameter blocks.
@@ -272,11 +322,12 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
         return fail(HA_ERR_INVALID_ARG, "q, seq_lens, out and lse must not be NULL");
     HA_TRY(check_kv(s, K, V));
     const bool dense = (m >= s->n_cap) && (m_per_seq == nullptr) && (opts == nullptr || opts->m_per_head == nullptr);
-    if (!dense) HA_TRY(check_codes(s, q_sig, k_sig));
+    const int W = code_words_of(opts);
+    if (!dense) HA_TRY(W > 1 ? check_wide_codes(s, q_sig, k_sig, W) : check_codes(s, q_sig, k_sig));
     if ((sel_idx == nullptr) != (sel_cnt == nullptr))
         return fail(HA_ERR_INVALID_ARG, "sel_idx and sel_cnt must both be given or both be NULL");
     const int64_t rows_cap = dense ? s->n_cap : rows_cap_of(s->n_cap, m, n_sink, n_local);
-    const Layout lay = make_layout(*s, rows_cap, !dense);
+    const Layout lay = make_layout(*s, rows_cap, !dense, nbins_of(opts));
     HA_TRY(check_segments(lay));
     HA_TRY(check_ws(lay, ws, ws_bytes));
     const Views v = views(lay, ws);
@@ -294,15 +345,22 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
         HA_TRY(record(events, 3, st));
         return HA_OK;
     }
-    ScoreParams sp = score_params(s, lay, v, q_sig, k_sig, seq_lens, m_per_seq, m, true);
-    SelectParams tp = select_params(s, lay, v, q_sig, k_sig, seq_lens, n_sink, n_local);
-    apply_opts(opts, n_sink, n_local, &sp, &tp);
     HA_TRY(record(events, 0, st));
-    HA_LAUNCH(launch_score(sp, bhkv, st), "SCORE launch");
-    HA_TRY(record(events, 1, st));
-    // TOPK and GATHER-ATT may start while their predecessor drains (they wait in
-    // the kernel before reading its output)
-    HA_LAUNCH(launch_select(tp, bhkv, st, true), "TOPK launch");
+    if (W > 1) {
+        const WideParams wp = wide_params(s, lay, v, q_sig, k_sig, seq_lens, m_per_seq, m, n_sink, n_local, W);
+        HA_LAUNCH(launch_score_wide(wp, bhkv, st), "SCORE launch");
+        HA_TRY(record(events, 1, st));
+        HA_LAUNCH(launch_select_wide(wp, bhkv, st, true), "TOPK launch");
+    } else {
+        ScoreParams sp = score_params(s, lay, v, q_sig, k_sig, seq_lens, m_per_seq, m, true);
+        SelectParams tp = select_params(s, lay, v, q_sig, k_sig, seq_lens, n_sink, n_local);
+        apply_opts(opts, n_sink, n_local, &sp, &tp);
+        HA_LAUNCH(launch_score(sp, bhkv, st), "SCORE launch");
+        HA_TRY(record(events, 1, st));
+        // TOPK and GATHER-ATT may start while their predecessor drains (they wait in
+        // the kernel before reading its output)
+        HA_LAUNCH(launch_select(tp, bhkv, st, true), "TOPK launch");
+    }
     HA_TRY(record(events, 2, st));
     gp.mode = kSegmented;
     HA_LAUNCH(launch_gather(gp, s->d, s->kv_dtype == HA_BF16, st, true), "GATHER-ATT launch");
@@ -354,7 +412,7 @@ void choose_splits(int64_t heads, int64_t rows_cap, int* splits, int* rows_per_s
     *rows_per_split = (int)rps;
 }
 
-Layout make_layout(const ha_shape& s, int64_t rows_cap, bool with_selection) {
+Layout make_layout(const ha_shape& s, int64_t rows_cap, bool with_selection, int nbins) {
     Layout L;
     L.heads = s.batch * s.h_q;
     L.rows_cap = (int)rows_cap;
@@ -368,8 +426,9 @@ Layout make_layout(const ha_shape& s, int64_t rows_cap, bool with_selection) {
         L.nchunks = (int)ceil_div(s.n_cap, L.chunk);
         L.seg_cap = L.chunk / kSegPerChunk;
         L.nseg = L.nchunks * kSegPerChunk;
+        L.nbins = nbins;
         L.off_hist = off;
-        off = align_up(off + (size_t)L.heads * L.nchunks * HA_NBINS * 4, 256);
+        off = align_up(off + (size_t)L.heads * L.nchunks * nbins * 4, 256);
         L.off_segcnt = off;
         off = align_up(off + (size_t)L.heads * L.nseg * 4, 256);
         L.off_seg = off;
@@ -403,6 +462,20 @@ ha_status hash_attn_workspace_size(const ha_shape* shape, int32_t m_max, int32_t
     // hash_attn_score work with any budget on the same workspace
     const int64_t rows_cap = dense ? shape->n_cap : rows_cap_of(shape->n_cap, m_max, n_sink, n_local);
     const Layout sparse = make_layout(*shape, rows_cap, true);
+    HA_TRY(check_segments(sparse));
+    *bytes = sparse.total;
+    return HA_OK;
+}
+
+ha_status hash_attn_workspace_size_ex(const ha_shape* shape, int32_t m_max, int32_t n_sink, int32_t n_local,
+                                      const ha_select_opts* opts, size_t* bytes) {
+    HA_TRY(check_shape(shape));
+    HA_TRY(check_window(m_max, n_sink, n_local));
+    HA_TRY(check_opts(opts));
+    if (bytes == nullptr) return fail(HA_ERR_INVALID_ARG, "bytes is NULL");
+    const bool dense = m_max >= shape->n_cap;
+    const int64_t rows_cap = dense ? shape->n_cap : rows_cap_of(shape->n_cap, m_max, n_sink, n_local);
+    const Layout sparse = make_layout(*shape, rows_cap, true, nbins_of(opts));
     HA_TRY(check_segments(sparse));
     *bytes = sparse.total;
     return HA_OK;
@@ -487,21 +560,28 @@ ha_status hash_attn_select_ex(const ha_shape* shape, const uint32_t* q_sig, cons
     HA_TRY(check_shape(shape));
     HA_TRY(check_window(m, n_sink, n_local));
     HA_TRY(check_opts(opts));
-    HA_TRY(check_codes(shape, q_sig, k_sig));
+    const int W = code_words_of(opts);
+    HA_TRY(W > 1 ? check_wide_codes(shape, q_sig, k_sig, W) : check_codes(shape, q_sig, k_sig));
     if (seq_lens == nullptr || sel_idx == nullptr || sel_cnt == nullptr)
         return fail(HA_ERR_INVALID_ARG, "seq_lens, sel_idx and sel_cnt must not be NULL");
     const int64_t rows_cap = rows_cap_of(shape->n_cap, m, n_sink, n_local);
-    const Layout lay = make_layout(*shape, rows_cap, true);
+    const Layout lay = make_layout(*shape, rows_cap, true, nbins_of(opts));
     HA_TRY(check_segments(lay));
     HA_TRY(check_ws(lay, workspace, ws_bytes));
     const Views v = views(lay, workspace);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int bhkv = shape->batch * shape->h_kv;
-    ScoreParams sp = score_params(shape, lay, v, q_sig, k_sig, seq_lens, m_per_seq, m, true);
-    SelectParams tp = select_params(shape, lay, v, q_sig, k_sig, seq_lens, n_sink, n_local);
-    apply_opts(opts, n_sink, n_local, &sp, &tp);
-    HA_LAUNCH(launch_score(sp, bhkv, st), "SCORE launch");
-    HA_LAUNCH(launch_select(tp, bhkv, st), "TOPK launch");
+    if (W > 1) {
+        const WideParams wp = wide_params(shape, lay, v, q_sig, k_sig, seq_lens, m_per_seq, m, n_sink, n_local, W);
+        HA_LAUNCH(launch_score_wide(wp, bhkv, st), "SCORE launch");
+        HA_LAUNCH(launch_select_wide(wp, bhkv, st, false), "TOPK launch");
+    } else {
+        ScoreParams sp = score_params(shape, lay, v, q_sig, k_sig, seq_lens, m_per_seq, m, true);
+        SelectParams tp = select_params(shape, lay, v, q_sig, k_sig, seq_lens, n_sink, n_local);
+        apply_opts(opts, n_sink, n_local, &sp, &tp);
+        HA_LAUNCH(launch_score(sp, bhkv, st), "SCORE launch");
+        HA_LAUNCH(launch_select(tp, bhkv, st), "TOPK launch");
+    }
     CompactParams cp{};
     cp.seq_lens = seq_lens;
     cp.Hq = shape->h_q;

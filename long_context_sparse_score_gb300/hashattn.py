@@ -38,7 +38,7 @@ HA_NOALLOC_SCRATCH_BYTES = 16 << 20
 EXPORTED = [
     "hash_attn_workspace_size", "hash_attn_workspace_init", "hash_attn_select_capacity",
     "hash_attn_decode", "hash_attn_decode_ex", "hash_attn_decode_timed", "hash_attn_score", "hash_attn_select",
-    "hash_attn_select_ex",
+    "hash_attn_select_ex", "hash_attn_workspace_size_ex",
     "hash_attn_gather_att", "hash_attn_gather_att_noalloc", "hash_attn_merge", "hash_attn_merge_n",
     "hash_attn_encode_queries", "hash_attn_encode_keys", "hash_attn_topk_exact_workspace_size",
     "hash_attn_topk_exact", "hash_attn_recall",
@@ -51,13 +51,14 @@ class HASelectOpts(ctypes.Structure):
     """Mirror of ``ha_select_opts``."""
 
     _fields_ = [("m_per_head", ctypes.c_void_p), ("exclusive_windows", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 3)]
+                ("code_words", ctypes.c_int32), ("reserved", ctypes.c_int32 * 2)]
 
 
-def select_opts(m_per_head=None, exclusive_windows=False) -> HASelectOpts:
+def select_opts(m_per_head=None, exclusive_windows=False, code_words=1) -> HASelectOpts:
     o = HASelectOpts()
     o.m_per_head = _ptr(m_per_head)
     o.exclusive_windows = 1 if exclusive_windows else 0
+    o.code_words = int(code_words)
     return o
 
 
@@ -107,6 +108,7 @@ def lib() -> ctypes.CDLL:
     OP = ctypes.POINTER(HASelectOpts)
     L.hash_attn_decode_ex.argtypes = dec[:11] + [OP] + dec[11:]
     L.hash_attn_select_ex.argtypes = [SP, _P, _P, _P, _P, _I32, _I32, _I32, OP, _P, _P, _P, _SZ, _P]
+    L.hash_attn_workspace_size_ex.argtypes = [SP, _I32, _I32, _I32, OP, ctypes.POINTER(_SZ)]
     L.hash_attn_decode_timed.argtypes = dec + [ctypes.POINTER(_P)]
     L.hash_attn_score.argtypes = [SP, _P, _P, _P, _P, _P, _P, _SZ, _P]
     L.hash_attn_select.argtypes = [SP, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _SZ, _P]
@@ -220,6 +222,13 @@ def hash_attn_decode(shape, q, q_sig, k_sig, K, V, seq_lens, m_per_seq, m, n_sin
                                   _ptr(V), _ptr(seq_lens), _ptr(m_per_seq), m, n_sink, n_local,
                                   _ptr(out), _ptr(lse), _ptr(sel_idx), _ptr(sel_cnt), ws, nb,
                                   _stream(stream)))
+
+
+def hash_attn_workspace_size_ex(shape, m_max: int, n_sink: int, n_local: int, opts) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().hash_attn_workspace_size_ex(ctypes.byref(shape), m_max, n_sink, n_local,
+                                             None if opts is None else ctypes.byref(opts), ctypes.byref(out)))
+    return out.value
 
 
 def hash_attn_decode_ex(shape, q, q_sig, k_sig, K, V, seq_lens, m_per_seq, m, n_sink, n_local, opts,

@@ -27,9 +27,9 @@ def workspace(shape, m, n_sink, n_local, device="cuda"):
 
 
 def run_decode(w, *, m=None, m_per_seq="workload", sel=True, K=None, V=None, ws=None, dense=False,
-               exclusive=False, m_per_head=None):
+               exclusive=False, m_per_head=None, code_words=1):
     """Decode a workload through the C ABI; returns a dict of outputs and the device status.
-    ``exclusive`` / ``m_per_head`` go through hash_attn_decode_ex."""
+    ``exclusive`` / ``m_per_head`` / ``code_words`` go through hash_attn_decode_ex."""
     H = ha()
     K = w.K if K is None else K
     V = w.V if V is None else V
@@ -38,8 +38,16 @@ def run_decode(w, *, m=None, m_per_seq="workload", sel=True, K=None, V=None, ws=
     k_sig = None if dense else w.k_sig
     q_sig = None if dense else w.q_sig
     shape = H.make_shape(w.q, K, V, w.k_sig, batch=w.B)
+    opts = None
+    if exclusive or m_per_head is not None or code_words > 1:
+        opts = H.select_opts(m_per_head, exclusive, code_words)
     if ws is None:
-        ws = workspace(shape, m, w.n_sink, w.n_local)
+        if opts is None:
+            ws = workspace(shape, m, w.n_sink, w.n_local)
+        else:
+            ws = torch.empty(H.hash_attn_workspace_size_ex(shape, m, w.n_sink, w.n_local, opts),
+                             dtype=torch.uint8, device=w.q.device)
+            H.hash_attn_workspace_init(ws)
     B, Hq, d = w.q.shape
     out = torch.full((B, Hq, d), float("nan"), dtype=torch.float32, device=w.q.device)
     lse = torch.full((B, Hq), float("nan"), dtype=torch.float32, device=w.q.device)
@@ -48,8 +56,7 @@ def run_decode(w, *, m=None, m_per_seq="workload", sel=True, K=None, V=None, ws=
     if sel and not (m >= K.shape[2] and mps is None):
         sel_idx = torch.full((B, Hq, max(cap, 1)), -7, dtype=torch.int32, device=w.q.device)
         sel_cnt = torch.full((B, Hq), -7, dtype=torch.int32, device=w.q.device)
-    if exclusive or m_per_head is not None:
-        opts = H.select_opts(m_per_head, exclusive)
+    if opts is not None:
         H.hash_attn_decode_ex(shape, w.q, q_sig, k_sig, K, V, w.seq_lens, mps, m, w.n_sink, w.n_local, opts,
                               out, lse, sel_idx, sel_cnt, workspace=ws)
     else:
@@ -92,6 +99,10 @@ class HostCopy:
             self._codes[key] = self.w.k_sig[bk, g].cpu().numpy().astype(np.int64)
         return self._codes[key]
 
+    def qcode(self, b, h):
+        """The query code: an int (32-bit codes) or its words (wider codes)."""
+        return int(self.q_sig[b, h]) if self.q_sig.ndim == 2 else self.q_sig[b, h]
+
     def budget(self, b, m, h=None):
         if self.mph is not None and h is not None:
             return int(self.mph[b, h])
@@ -100,7 +111,7 @@ class HostCopy:
     def select(self, b, h, m):
         G = self.w.Hq // self.w.Hkv
         n = int(self.lens[b])
-        return O.selected_set(int(self.q_sig[b, h]), self.codes(b, h // G), n, self.budget(b, m, h),
+        return O.selected_set(self.qcode(b, h), self.codes(b, h // G), n, self.budget(b, m, h),
                               self.w.n_sink, self.w.n_local, exclusive=self.exclusive)
 
     def head(self, b, h, m, dense=False):
@@ -109,7 +120,7 @@ class HostCopy:
         Kh, Vh = self.kv(b, g)
         n = int(self.lens[b])
         codes = None if dense else self.codes(b, g)
-        return O.decode_head(self.q[b, h], None if dense else int(self.q_sig[b, h]), codes, Kh, Vh, n,
+        return O.decode_head(self.q[b, h], None if dense else self.qcode(b, h), codes, Kh, Vh, n,
                              self.budget(b, m, h), self.w.n_sink, self.w.n_local, dense=dense,
                              exclusive=self.exclusive)
 

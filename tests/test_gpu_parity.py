@@ -174,6 +174,34 @@ def test_selection_variants(case):
                 assert int(cnt[b, h]) == min(n, mb + W_)
 
 
+@pytest.mark.parametrize("Wd,n_cap,lens,m,S,Lw,pool", [
+    (2, 9000, [9000, 7001], 700, 16, 32, False),
+    (4, 6000, [6000, 4321], 300, 64, 64, True),
+    (16, 5000, [5000, 2500], 900, 8, 8, False),
+])
+def test_wide_codes(Wd, n_cap, lens, m, S, Lw, pool):
+    """Codes of Wd 32-bit words through hash_attn_decode_ex against the oracle
+    (the distance sums over the words; b + 1 bins)."""
+    w = W().make_gqa(25, B=2, Hq=8, Hkv=2, d=128, n_cap=n_cap, seq_lens=lens, m=m, n_sink=S, n_local=Lw,
+                     device="cuda")
+    gen = torch.Generator(device="cuda").manual_seed(8 + Wd)
+    if pool:   # few distinct codes: ties across chunks
+        base = torch.randint(-2 ** 31, 2 ** 31 - 1, (5, Wd), generator=gen, device="cuda", dtype=torch.int64)
+        pick = torch.randint(0, 5, (2, 2, n_cap), generator=gen, device="cuda")
+        w.k_sig = base[pick].to(torch.int32).contiguous()
+        w.q_sig = base[torch.zeros((2, 8), dtype=torch.int64, device="cuda")].to(torch.int32).contiguous()
+    else:
+        w.k_sig = torch.randint(-2 ** 31, 2 ** 31 - 1, (2, 2, n_cap, Wd), generator=gen, device="cuda",
+                                dtype=torch.int64).to(torch.int32).contiguous()
+        w.q_sig = torch.randint(-2 ** 31, 2 ** 31 - 1, (2, 8, Wd), generator=gen, device="cuda",
+                                dtype=torch.int64).to(torch.int32).contiguous()
+    res = GH.run_decode(w, code_words=Wd)
+    assert res["status"] == 0, res["flags"]
+    hc = GH.HostCopy(w)
+    GH.check_selection(res, hc, all_heads(w), m)
+    GH.check_attention(res, hc, all_heads(w)[::3], m)
+
+
 def test_per_head_budget_above_bound_is_flagged():
     H = GH.ha()
     w = W().make_gqa(24, B=1, Hq=4, Hkv=1, d=128, n_cap=3000, seq_lens=[3000], m=100, n_sink=4, n_local=4,
