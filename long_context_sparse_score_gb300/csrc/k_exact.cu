@@ -41,18 +41,22 @@ __device__ __forceinline__ void to_float8<float>(const uint4 w, float* f) {
     f[2] = __uint_as_float(w.z); f[3] = __uint_as_float(w.w);
 }
 
-// grid: (B * Hkv, token blocks of kScoreRowsPerCta); 256 threads; dynamic
-// shared memory G * D floats (the group's queries).
-template <int D, typename KT>
-__global__ void __launch_bounds__(256) k_dot_scores(const ExactParams p) {
+// grid: (token blocks of kScoreRowsPerCta, B * Hkv): CTAs launched together
+// stream consecutive blocks of one KV head (the heads' K regions are a power of
+// two apart, which same-offset reads across heads would concentrate on few
+// memory channels); 256 threads; dynamic shared memory G * D floats.
+// GQ: the group size when it is known at compile time (4: the heads' loop
+// unrolls), else 0 (a run-time loop over p.G).
+template <int D, typename KT, int GQ>
+__global__ void __launch_bounds__(256, 4) k_dot_scores(const ExactParams p) {
     constexpr int ES = sizeof(KT);
     constexpr int NCH = D * ES / 16;  // 16-byte chunks per row
     constexpr int CPL = NCH / 4;      // chunks per lane (4 lanes per row)
     constexpr int EPC = 16 / ES;      // elements per chunk
     extern __shared__ float s_q[];    // [G][D]
-    const int bg = blockIdx.x;
+    const int bg = blockIdx.y;
     const int b = bg / p.Hkv, g = bg % p.Hkv;
-    const int n = checked_len(p.seq_lens, b, p.n_cap, p.err, blockIdx.y == 0 && g == 0 && threadIdx.x == 0);
+    const int n = checked_len(p.seq_lens, b, p.n_cap, p.err, blockIdx.x == 0 && g == 0 && threadIdx.x == 0);
     for (int i = threadIdx.x; i < p.G * D; i += blockDim.x) {
         const int hh = i / D, k = i - hh * D;
         const int64_t off = (int64_t)b * p.q_sb + (int64_t)(g * p.G + hh) * p.q_sh + k;
@@ -63,30 +67,55 @@ __global__ void __launch_bounds__(256) k_dot_scores(const ExactParams p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r = lane & 7, qt = lane >> 3;
     const char* Kb = p.K + ((int64_t)b * p.k_sb + (int64_t)g * p.k_sh) * ES;
-    const int row_end = min(n, (int)(blockIdx.y + 1) * kScoreRowsPerCta);
-    for (int row0 = blockIdx.y * kScoreRowsPerCta + warp * 8; row0 < row_end; row0 += 8 * 8) {
+    const int row_end = min(n, (int)(blockIdx.x + 1) * kScoreRowsPerCta);
+    auto load_rows = [&](int row0, uint4 (&w)[CPL]) {
         const int row = row0 + r;
-        uint4 w[CPL];
 #pragma unroll
         for (int jc = 0; jc < CPL; ++jc)
             w[jc] = (row < row_end) ? __ldg(reinterpret_cast<const uint4*>(Kb + (int64_t)row * p.k_sn * ES +
                                                                           (jc * 4 + qt) * 16))
                                     : make_uint4(0u, 0u, 0u, 0u);
-        for (int hh = 0; hh < p.G; ++hh) {
+    };
+    // each warp walks 8-row tiles; the next tile's rows load while this one is scored
+    int row0 = blockIdx.x * kScoreRowsPerCta + warp * 8;
+    uint4 wc[CPL];
+    if (row0 < row_end) load_rows(row0, wc);
+    for (; row0 < row_end; row0 += 8 * 8) {
+        uint4 wn[CPL];
+        if (row0 + 64 < row_end) load_rows(row0 + 64, wn);
+        const int row = row0 + r;
+        float f[CPL * EPC];  // this lane's elements of the row, converted once for every head
+#pragma unroll
+        for (int jc = 0; jc < CPL; ++jc) to_float8<KT>(wc[jc], f + jc * EPC);
+        const int G = GQ ? GQ : p.G;
+        auto head_score = [&](int hh) {
             const float* qh = s_q + hh * D;
-            float acc = 0.f;
+            float2 a2 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int jc = 0; jc < CPL; ++jc) {
-                float f[EPC];
-                to_float8<KT>(w[jc], f);
 #pragma unroll
-                for (int e = 0; e < EPC; ++e) acc = fmaf(qh[(jc * 4 + qt) * EPC + e], f[e], acc);
+                for (int e = 0; e < EPC; e += 4) {
+                    const float4 q4 = *reinterpret_cast<const float4*>(qh + (jc * 4 + qt) * EPC + e);
+                    a2 = __ffma2_rn(make_float2(q4.x, q4.y), make_float2(f[jc * EPC + e], f[jc * EPC + e + 1]), a2);
+                    a2 = __ffma2_rn(make_float2(q4.z, q4.w), make_float2(f[jc * EPC + e + 2], f[jc * EPC + e + 3]),
+                                    a2);
+                }
             }
+            float acc = a2.x + a2.y;
             acc += __shfl_xor_sync(0xffffffffu, acc, 8);
             acc += __shfl_xor_sync(0xffffffffu, acc, 16);
             if (qt == 0 && row < row_end)
-                p.scores[((int64_t)b * p.Hq + g * p.G + hh) * p.n_cap + row] = acc;
+                p.scores[((int64_t)b * p.Hq + g * G + hh) * p.n_cap + row] = acc;
+        };
+        if constexpr (GQ > 0) {
+#pragma unroll
+            for (int hh = 0; hh < GQ; ++hh) head_score(hh);
+        } else {
+#pragma unroll 1
+            for (int hh = 0; hh < G; ++hh) head_score(hh);
         }
+#pragma unroll
+        for (int jc = 0; jc < CPL; ++jc) wc[jc] = wn[jc];
     }
 }
 
@@ -128,6 +157,7 @@ __device__ __forceinline__ int block_excl_scan(int v, int* s_warp, int* total) {
 // One CTA (kTopkThreads) per query head.
 __global__ void __launch_bounds__(kTopkThreads) k_topk_exact(const ExactParams p) {
     __shared__ unsigned s_hist[256];
+    __shared__ unsigned s_whist[kTopkThreads / 32][256];  // per-warp bins: scores cluster, one copy would serialise
     __shared__ int s_warp[kTopkThreads / 32];
     __shared__ uint32_t s_prefix;
     __shared__ int s_need;
@@ -147,12 +177,30 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_exact(const ExactParams p
             s_prefix = 0u;
             s_need = need;
         }
+        const int warp = tid >> 5;
         for (int shift = 24; shift >= 0; shift -= 8) {
-            for (int i = tid; i < 256; i += kTopkThreads) s_hist[i] = 0u;
+            for (int i = tid; i < (kTopkThreads / 32) * 256; i += kTopkThreads) (&s_whist[0][0])[i] = 0u;
             __syncthreads();
-            for (int i = tid; i < n; i += kTopkThreads) {
-                const uint32_t key = fkey(z[i]);
-                if ((key & mask) == prefix) atomicAdd(&s_hist[(key >> shift) & 0xFFu], 1u);
+            for (int i0 = tid; i0 < n; i0 += 8 * kTopkThreads) {  // 8 loads in flight per thread
+                float v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int i = i0 + u * kTopkThreads;
+                    v[u] = (i < n) ? __ldcg(z + i) : 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const uint32_t key = fkey(v[u]);
+                    if (i0 + u * kTopkThreads < n && (key & mask) == prefix)
+                        atomicAdd(&s_whist[warp][(key >> shift) & 0xFFu], 1u);
+                }
+            }
+            __syncthreads();
+            for (int i = tid; i < 256; i += kTopkThreads) {
+                unsigned sum = 0u;
+#pragma unroll 8
+                for (int w2 = 0; w2 < kTopkThreads / 32; ++w2) sum += s_whist[w2][i];
+                s_hist[i] = sum;
             }
             __syncthreads();
             if (tid < 32) {
@@ -192,28 +240,47 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_exact(const ExactParams p
             __syncthreads();
         }
     }
-    // ---- compaction in token order: keys above T, and the first `need` keys equal to T
+    // ---- compaction in token order: keys above T, and the first `need` keys equal to T;
+    // each thread takes 8 consecutive tokens of a block of 8 * kTopkThreads
+    constexpr int kPer = 8;
     const bool all = (k >= n);
     int out_base = 0, ties_seen = 0;
-    for (int i0 = 0; i0 < n && k > 0; i0 += kTopkThreads) {
-        const int i = i0 + tid;
-        bool take = false, tie = false;
-        if (i < n) {
-            if (all) {
-                take = true;
-            } else {
-                const uint32_t key = fkey(z[i]);
-                take = key > prefix;
-                tie = key == prefix;
+    for (int i0 = 0; i0 < n && k > 0; i0 += kPer * kTopkThreads) {
+        const int ib = i0 + tid * kPer;
+        uint32_t take = 0u, tie = 0u;  // bit u: token ib + u
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            const int i = ib + u;
+            if (i < n) {
+                if (all) {
+                    take |= 1u << u;
+                } else {
+                    const uint32_t key = fkey(__ldcg(z + i));
+                    if (key > prefix) take |= 1u << u;
+                    if (key == prefix) tie |= 1u << u;
+                }
             }
         }
         int ties_total;
-        const int tie_before = block_excl_scan(tie ? 1 : 0, s_warp, &ties_total);
-        if (tie && ties_seen + tie_before < need) take = true;
+        const int tie_before = block_excl_scan(__popc(tie), s_warp, &ties_total);
+        int rank = ties_seen + tie_before;  // ties of the tokens before this thread's
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            if ((tie >> u) & 1u) {
+                if (rank < need) take |= 1u << u;
+                ++rank;
+            }
+        }
         ties_seen += ties_total;
         int taken_total;
-        const int pos = block_excl_scan(take ? 1 : 0, s_warp, &taken_total);
-        if (take && out_base + pos < p.idx_cap) dst[out_base + pos] = i;
+        int pos = out_base + block_excl_scan(__popc(take), s_warp, &taken_total);
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+            if ((take >> u) & 1u) {
+                if (pos < p.idx_cap) dst[pos] = ib + u;
+                ++pos;
+            }
+        }
         out_base += taken_total;
     }
     for (int t = k + tid; t < p.idx_cap; t += kTopkThreads) dst[t] = -1;
@@ -263,8 +330,10 @@ __global__ void __launch_bounds__(kRecallThreads) k_recall(const RecallParams p)
 
 template <int D, typename KT>
 cudaError_t launch_scores_t(const ExactParams& p, cudaStream_t st) {
-    const dim3 grid((unsigned)(p.B * p.Hkv), (unsigned)((p.n_cap + kScoreRowsPerCta - 1) / kScoreRowsPerCta));
-    k_dot_scores<D, KT><<<grid, 256, (size_t)p.G * D * sizeof(float), st>>>(p);
+    const dim3 grid((unsigned)((p.n_cap + kScoreRowsPerCta - 1) / kScoreRowsPerCta), (unsigned)(p.B * p.Hkv));
+    const size_t smem = (size_t)p.G * D * sizeof(float);
+    if (p.G == 4) k_dot_scores<D, KT, 4><<<grid, 256, smem, st>>>(p);
+    else k_dot_scores<D, KT, 0><<<grid, 256, smem, st>>>(p);
     return cudaGetLastError();
 }
 
