@@ -271,7 +271,7 @@ def measure_exact(w, shape, sel, cnt, dev):
     kv_bytes = w.B * w.Hkv * w.n_cap * w.d * w.K.element_size()
     ms = ev[0].elapsed_time(ev[1])
     del ws
-    return {"kernels": "k_dot_scores + k_topk_exact", "m": w.m, "ms": ms,
+    return {"kernels": "k_qsplit + k_dot_scores_tc + k_topk_exact", "m": w.m, "ms": ms,
             "key_read_gbs": kv_bytes / (ms * 1e-3) / 1e9,
             "recall_mean": float(rec.mean()), "recall_min": float(rec.min()),
             "recall_kernel_us": ev[1].elapsed_time(ev[2]) * 1e3,

@@ -206,6 +206,7 @@ struct ExactParams {
     int idx_cap;
     int32_t* cnt;              // [B * Hq]
     uint32_t* err;
+    uint16_t* qt;              // [B * Hkv][32][d] bf16 query tiles of the tensor-core kernel (workspace)
 };
 
 struct RecallParams {
@@ -250,6 +251,9 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t st);
 cudaError_t launch_merge_n(const MergeNParams& p, cudaStream_t st);
 cudaError_t launch_encode(const EncodeParams& p, cudaStream_t st);
 cudaError_t launch_topk_exact(const ExactParams& p, int d, int kv_bf16, cudaStream_t st);
+// Tensor-core scores (bf16 K, 3 G <= 32); *used = false leaves the scores to
+// the CUDA-core kernel (a layout TMA cannot describe).
+cudaError_t launch_scores_tc(const ExactParams& p, int d, cudaStream_t st, bool* used);
 cudaError_t launch_recall(const RecallParams& p, cudaStream_t st);
 cudaError_t launch_score_wide(const WideParams& p, int batch_hkv, cudaStream_t st);
 cudaError_t launch_select_wide(const WideParams& p, int batch_hkv, cudaStream_t st, bool pdl);

@@ -707,7 +707,8 @@ ha_status hash_attn_encode_keys(const ha_shape* shape, const void* K, const floa
 ha_status hash_attn_topk_exact_workspace_size(const ha_shape* shape, size_t* bytes) {
     HA_TRY(check_shape(shape));
     if (bytes == nullptr) return fail(HA_ERR_INVALID_ARG, "bytes is NULL");
-    *bytes = 256 + align_up((size_t)shape->batch * shape->h_q * (size_t)shape->n_cap * sizeof(float), 256);
+    *bytes = 256 + align_up((size_t)shape->batch * shape->h_q * (size_t)shape->n_cap * sizeof(float), 1024) +
+             (size_t)shape->batch * shape->h_kv * 32 * (size_t)shape->d * sizeof(uint16_t);
     return HA_OK;
 }
 
@@ -744,6 +745,8 @@ ha_status hash_attn_topk_exact(const ha_shape* shape, const void* q, const void*
     p.m = m;
     p.err = static_cast<uint32_t*>(workspace);
     p.scores = reinterpret_cast<float*>(static_cast<char*>(workspace) + 256);
+    p.qt = reinterpret_cast<uint16_t*>(static_cast<char*>(workspace) + 256 +
+                                       align_up((size_t)shape->batch * shape->h_q * (size_t)shape->n_cap * sizeof(float), 1024));
     p.idx = idx;
     p.idx_cap = idx_cap;
     p.cnt = cnt;

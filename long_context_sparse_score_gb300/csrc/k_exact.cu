@@ -340,12 +340,17 @@ cudaError_t launch_scores_t(const ExactParams& p, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_topk_exact(const ExactParams& p, int d, int kv_bf16, cudaStream_t st) {
-    cudaError_t e = cudaErrorInvalidValue;
-    if (d == 128 && kv_bf16) e = launch_scores_t<128, __nv_bfloat16>(p, st);
-    if (d == 64 && kv_bf16) e = launch_scores_t<64, __nv_bfloat16>(p, st);
-    if (d == 128 && !kv_bf16) e = launch_scores_t<128, float>(p, st);
-    if (d == 64 && !kv_bf16) e = launch_scores_t<64, float>(p, st);
+    bool tc = false;
+    cudaError_t e = kv_bf16 ? launch_scores_tc(p, d, st, &tc) : cudaSuccess;
     if (e != cudaSuccess) return e;
+    if (!tc) {
+        e = cudaErrorInvalidValue;
+        if (d == 128 && kv_bf16) e = launch_scores_t<128, __nv_bfloat16>(p, st);
+        if (d == 64 && kv_bf16) e = launch_scores_t<64, __nv_bfloat16>(p, st);
+        if (d == 128 && !kv_bf16) e = launch_scores_t<128, float>(p, st);
+        if (d == 64 && !kv_bf16) e = launch_scores_t<64, float>(p, st);
+        if (e != cudaSuccess) return e;
+    }
     k_topk_exact<<<p.B * p.Hq, kTopkThreads, 0, st>>>(p);
     return cudaGetLastError();
 }

@@ -514,6 +514,89 @@ def test_topk_exact_ties_take_smaller_indices():
         assert int(cnt[0, h]) == 300 and torch.equal(idx[0, h].cpu(), torch.arange(300, dtype=torch.int32))
 
 
+def _exact_call(H, shape, q, K, seq_lens, m, B, Hq, n_cap):
+    """Run the exact comparator; returns (scores [B, Hq, n_cap] from the
+    workspace, idx, cnt). The scores follow the 256-byte error word."""
+    ws = torch.empty(H.hash_attn_topk_exact_workspace_size(shape), dtype=torch.uint8, device="cuda")
+    cap = min(m, n_cap)
+    idx = torch.full((B, Hq, cap), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.full((B, Hq), -7, dtype=torch.int32, device="cuda")
+    H.hash_attn_topk_exact(shape, q, K, seq_lens, m, idx, cnt, workspace=ws)
+    st, flags = H.hash_attn_device_status(ws)
+    assert st == 0, flags
+    z = ws[256:256 + B * Hq * n_cap * 4].view(torch.float32).view(B, Hq, n_cap)
+    return z.cpu(), idx.cpu().numpy(), cnt.cpu().numpy()
+
+
+# (Hq, Hkv, d, q dtype, kv dtype): groups of 1, 4, 8 and 10 heads take the
+# tensor-core kernel for bf16 keys (3 G <= 32 columns), 16 heads and float32
+# keys the CUDA-core one
+EXACT_SHAPES = [(8, 2, 128, torch.float32, torch.bfloat16), (8, 8, 64, torch.float32, torch.bfloat16),
+                (16, 2, 128, torch.float32, torch.bfloat16), (20, 2, 64, torch.bfloat16, torch.bfloat16),
+                (32, 2, 128, torch.float32, torch.bfloat16), (8, 2, 128, torch.float32, torch.float32)]
+
+
+@pytest.mark.parametrize("Hq,Hkv,d,q_dtype,kv_dtype", EXACT_SHAPES)
+def test_exact_scores_one_hot_keys_are_exact(Hq, Hkv, d, q_dtype, kv_dtype):
+    """Keys with one non-zero entry, a power of two, make every score a single
+    product: z[b, h, i] = 2^e_i q[b, h, j_i] exactly, in any summation order, so
+    the scores must match bit for bit (this pins the dimension order, the head
+    order and, for a float32 query, the split of q into three bf16 parts). Equal
+    scores recur, so the top-m also checks that ties go to the smaller index."""
+    H = GH.ha()
+    B, n_cap, lens, m = 2, 1000, [1000, 333], 150
+    g_ = torch.Generator().manual_seed(31)
+    q = torch.randn((B, Hq, d), generator=g_).to(q_dtype)
+    i = torch.arange(n_cap)
+    scale = torch.pow(2.0, (i % 5).double() - 2.0)
+    K = torch.zeros((B, Hkv, n_cap, d), dtype=torch.float64)
+    col = torch.empty((B, Hkv, n_cap), dtype=torch.int64)
+    for b in range(B):
+        for g in range(Hkv):
+            col[b, g] = (7 * i + 3 * g + b) % d
+            K[b, g, i, col[b, g]] = scale
+    Kd, qd = K.to(kv_dtype).cuda(), q.cuda()
+    V = torch.zeros_like(Kd)
+    seq = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    shape = H.make_shape(qd, Kd, V)
+    z, idx, cnt = _exact_call(H, shape, qd, Kd, seq, m, B, Hq, n_cap)
+    G = Hq // Hkv
+    q64 = q.double()
+    for b, n in enumerate(lens):
+        for h in range(Hq):
+            want = (q64[b, h, col[b, h // G, :n]] * scale[:n]).float()
+            assert torch.equal(z[b, h, :n], want), (b, h)
+            assert int(cnt[b, h]) == min(m, n)
+            ref = O.top_m_by_dot(q64[b, h].numpy(), K[b, h // G].numpy(), n, m)
+            assert np.array_equal(idx[b, h, :min(m, n)], ref), (b, h)
+
+
+@pytest.mark.parametrize("Hq,Hkv,d,q_dtype,kv_dtype", EXACT_SHAPES)
+def test_exact_scores_within_float32_bound(Hq, Hkv, d, q_dtype, kv_dtype):
+    """Random keys and queries: every score within d 2^-22 sum_k |q_k k_ik| of the
+    float64 dot product (the band the selection check uses), and the top-m inside
+    the oracle's band."""
+    H = GH.ha()
+    lens, m = [3000, 2222], 300
+    w = W().make_gqa(23, B=2, Hq=Hq, Hkv=Hkv, d=d, n_cap=3000, seq_lens=lens, m=m, n_sink=0, n_local=0,
+                     device="cuda", kv_dtype=kv_dtype)
+    q = w.q.to(q_dtype)
+    shape = H.make_shape(q, w.K, w.V, w.k_sig)
+    z, idx, cnt = _exact_call(H, shape, q, w.K, w.seq_lens, m, 2, Hq, 3000)
+    qn, Kn = q.double().cpu().numpy(), w.K.double().cpu().numpy()
+    G = Hq // Hkv
+    for b, n in enumerate(lens):
+        for h in range(Hq):
+            Kh = Kn[b, h // G, :n]
+            exact = O.dot_scores(qn[b, h], Kh, n)
+            bound = d * 2.0 ** -22 * (np.abs(Kh) @ np.abs(qn[b, h]))
+            assert np.all(np.abs(z[b, h, :n].double().numpy() - exact) <= bound), (b, h)
+            k = min(m, n)
+            assert int(cnt[b, h]) == k
+            sure, band = O.top_m_band(qn[b, h], Kn[b, h // G], n, m)
+            assert set(sure) <= set(idx[b, h, :k]) <= set(sure) | set(band), (b, h)
+
+
 def test_device_errors_are_flagged_not_faulted():
     H = GH.ha()
     w = W().make_gqa(16, B=3, Hq=4, Hkv=2, d=128, n_cap=2000, seq_lens=[2000, 1500, 2000], m=100,
