@@ -207,6 +207,7 @@ struct ExactParams {
     int32_t* cnt;              // [B * Hq]
     uint32_t* err;
     uint16_t* qt;              // [B * Hkv][32][d] bf16 query tiles of the tensor-core kernel (workspace)
+    int bitmap_words;          // top-m: words of each token bitmap in shared memory (0: no fast path)
 };
 
 struct RecallParams {

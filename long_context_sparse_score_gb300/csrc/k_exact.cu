@@ -3,12 +3,19 @@
 // HashAttention: Semantic Sparsity for Faster Inference, Sec. 5 measures the
 // hashed selection against the oracle top-k by attention score. Here:
 //   k_dot_scores   z[head, i] = <q[b, h], k_i> (float32) for every cached token
-//                  i < n; one read of a KV head's rows serves its G query heads
-//                  (4 lanes share a row, 16-byte loads, q in shared memory).
-//   k_topk_exact   per head, the min(m, n) largest z (ties: smaller index):
-//                  radix select over order-preserving 32-bit keys, 8 bits per
-//                  pass, then one compaction pass in token order writes the
-//                  ascending list (-1 padded).
+//                  i < n on the CUDA cores, for the keys the tensor-core kernel
+//                  does not take (float32 keys, more than 10 query heads per
+//                  KV head); one read of a KV head's rows serves its G query
+//                  heads (4 lanes share a row, 16-byte loads, q in shared
+//                  memory).
+//   k_topk_exact   per head, the min(m, n) largest z (ties: smaller index),
+//                  by radix select over order-preserving 32-bit keys: a
+//                  threshold from a 1/16 sample admits a few thousand
+//                  candidates into shared memory in one pass over the
+//                  scores, the exact select runs on those, and a token bitmap
+//                  gives the ascending list (-1 padded); when the estimate
+//                  misses, four 8-bit passes over all scores and a compaction
+//                  pass in token order.
 //   k_recall       per head, |selected & reference| / |reference|: the
 //                  reference list is staged in shared memory in tiles and every
 //                  selected index is looked up by binary search.
@@ -20,7 +27,11 @@ namespace ha {
 namespace {
 
 constexpr int kScoreRowsPerCta = 1024;
-constexpr int kTopkThreads = 1024;
+constexpr int kTopkThreads = 512;
+constexpr int kCandCap = 10240;        // candidate tokens held in shared memory
+constexpr int kSampleCap = 8192;       // sampled scores (in the candidate key array)
+constexpr int kTieCap = 1024;          // tokens equal to the k-th largest key, fast path
+constexpr int kBitmapTokens = 1 << 18; // fast path up to this n_cap (a bitmap of n_cap bits)
 constexpr int kRecallThreads = 256;
 constexpr int kRecallTile = 8192;
 
@@ -154,134 +165,333 @@ __device__ __forceinline__ int block_excl_scan(int v, int* s_warp, int* total) {
     return before;
 }
 
-// One CTA (kTopkThreads) per query head.
+// Warp 0 of the block: given the histogram of the keys still in play (those
+// whose resolved high bits equal `prefix`), find the bin of the need-th
+// largest and publish the extended prefix and the count still needed in it.
+__device__ __forceinline__ void pick_bin(const unsigned* s_hist, int need, uint32_t prefix, int shift,
+                                         uint32_t* s_prefix, int* s_need) {
+    const int lane = threadIdx.x & 31;
+    unsigned c[8], sum = 0u;  // lane l holds bins 255 - 8l ... 248 - 8l
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        c[u] = s_hist[255 - 8 * lane - u];
+        sum += c[u];
+    }
+    unsigned incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    unsigned above = incl - sum;  // keys in the bins above this lane's
+    const unsigned hit = __ballot_sync(0xffffffffu, above < (unsigned)need && (unsigned)need <= incl);
+    if (lane == __ffs(hit) - 1) {
+        int bin = 255 - 8 * lane;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if (above + c[u] >= (unsigned)need) {
+                bin = 255 - 8 * lane - u;
+                break;
+            }
+            above += c[u];
+        }
+        *s_prefix = prefix | ((uint32_t)bin << shift);
+        *s_need = need - (int)above;
+    }
+}
+
+// Radix select over keys[0, cnt) in shared memory: resolves `passes` 8-bit
+// digits (from the top) of the need-th largest key. With 4 passes, prefix is
+// that key and need the number of keys equal to it among the largest `need`;
+// with fewer, prefix has its low bits zero and at least `need` keys are >= it.
+// Lanes with equal digits are merged (match_any) before the shared atomics:
+// scores cluster in few high-order bins.
+__device__ void smem_radix_select(const uint32_t* keys, int cnt, int need, int passes, unsigned* s_hist,
+                                  uint32_t* s_prefix, int* s_need, uint32_t& prefix_out, int& need_out) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    uint32_t prefix = 0u, mask = 0u;
+    if (tid == 0) {
+        *s_prefix = 0u;
+        *s_need = need;
+    }
+    for (int pass = 0; pass < passes; ++pass) {
+        const int shift = 24 - 8 * pass;
+        for (int i = tid; i < 256; i += blockDim.x) s_hist[i] = 0u;
+        __syncthreads();
+        for (int i0 = 0; i0 < cnt; i0 += 8 * blockDim.x) {  // 8 keys per thread loaded before counting
+            uint32_t kv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = i0 + u * blockDim.x + tid;
+                kv[u] = (i < cnt) ? keys[i] : 0u;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = i0 + u * blockDim.x + tid;
+                const bool in = i < cnt && (kv[u] & mask) == prefix;
+                const unsigned bin = in ? (kv[u] >> shift) & 0xFFu : 256u;
+                const unsigned peers = __match_any_sync(0xffffffffu, bin);
+                if (in && lane == __ffs(peers) - 1) atomicAdd(&s_hist[bin], (unsigned)__popc(peers));
+            }
+        }
+        __syncthreads();
+        if (tid < 32) pick_bin(s_hist, need, prefix, shift, s_prefix, s_need);
+        __syncthreads();
+        prefix = *s_prefix;
+        need = *s_need;
+        mask |= 0xFFu << shift;
+        __syncthreads();
+    }
+    prefix_out = prefix;
+    need_out = need;
+}
+
+// Ascending output of the selected tokens of one block of up to 32 consecutive
+// tokens per thread: take/tie bit u = token ib + u. Ties are taken in token
+// order while fewer than `need` have been taken; out_base and ties_seen
+// advance by the block's totals (uniform across the block).
+__device__ __forceinline__ void emit_block(uint32_t take, uint32_t tie, int ib, int need, int* s_warp,
+                                           int32_t* dst, int idx_cap, int& out_base, int& ties_seen) {
+    int ties_total;
+    const int tie_before = block_excl_scan(__popc(tie), s_warp, &ties_total);
+    int rank = ties_seen + tie_before;  // ties of the tokens before this thread's
+    for (uint32_t t = tie; t != 0u; t &= t - 1u) {
+        if (rank < need) take |= t & (0u - t);
+        ++rank;
+    }
+    ties_seen += ties_total;
+    int taken_total;
+    int pos = out_base + block_excl_scan(__popc(take), s_warp, &taken_total);
+    for (uint32_t t = take; t != 0u; t &= t - 1u) {
+        if (pos < idx_cap) dst[pos] = ib + __ffs(t) - 1;
+        ++pos;
+    }
+    out_base += taken_total;
+}
+
+// One CTA (kTopkThreads) per query head: the k = min(m, n) largest scores.
+//  fast path (n within the bitmap capacity): a 16-bit threshold T16 from a
+//   1/16 sample (8 consecutive tokens out of every 128, so the sample costs
+//   1/16 of the sectors) with the target rank raised well past k's share; one
+//   pass collects every token with key >= T16 into shared memory; when their
+//   count lies in [k, kCandCap] the exact k-th largest key is among them
+//   (at least k keys are >= T16), so the exact radix select runs on the
+//   candidates alone; the tokens above the k-th key and the smallest-index
+//   tokens equal to it are marked in a token bitmap, which is written out in
+//   token order.
+//  Ties beyond kTieCap (degenerate inputs) take the general path.
+//  otherwise: radix select over all n scores (four passes of 8 bits) and a
+//   compaction pass in token order.
 __global__ void __launch_bounds__(kTopkThreads) k_topk_exact(const ExactParams p) {
+    extern __shared__ uint32_t s_dyn[];
+    uint32_t* s_ckey = s_dyn;                              // [kCandCap] (the sample first)
+    int* s_cidx = reinterpret_cast<int*>(s_dyn + kCandCap);  // [kCandCap]
+    uint32_t* s_sel = s_dyn + 2 * kCandCap;                // [bitmap_words]
+    int* s_tlist = reinterpret_cast<int*>(s_sel + p.bitmap_words);  // [kTieCap]
     __shared__ unsigned s_hist[256];
-    __shared__ unsigned s_whist[kTopkThreads / 32][256];  // per-warp bins: scores cluster, one copy would serialise
     __shared__ int s_warp[kTopkThreads / 32];
     __shared__ uint32_t s_prefix;
     __shared__ int s_need;
+    __shared__ int s_ccount, s_tcount;
     const int head = blockIdx.x;
     const int b = head / p.Hq;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31;
     const int n = checked_len(p.seq_lens, b, p.n_cap, nullptr, false);
     const int k = max(0, min(p.m, n));
     const float* z = p.scores + (int64_t)head * p.n_cap;
     int32_t* dst = p.idx + (int64_t)head * p.idx_cap;
+    int out_base = 0;
 
-    // ---- radix select: the k-th largest key T, and how many keys equal to T to take
-    uint32_t prefix = 0u, mask = 0u;
-    int need = k;
-    if (k > 0 && k < n) {
-        if (tid == 0) {  // kept if no bin matches (cannot happen for finite keys; the count check flags it)
-            s_prefix = 0u;
-            s_need = need;
+    if (k > 0 && k >= n) {  // every token
+        for (int i = tid; i < n; i += kTopkThreads)
+            if (i < p.idx_cap) dst[i] = i;
+        out_base = n;
+    } else if (k > 0) {
+        bool fast = p.bitmap_words > 0 && n <= 32 * p.bitmap_words;
+        uint32_t t16 = 0u;
+        if (fast) {
+            // ---- sample: blocks of 8 tokens, one every 8 * step tokens
+            const int step = (n + kSampleCap - 9) / (kSampleCap - 8);
+            const int nb = (n + 8 * step - 1) / (8 * step);
+            const int ns = min(nb * 8, (nb - 1) * 8 + (n - (nb - 1) * 8 * step));
+            {
+                constexpr int kPerThread = kSampleCap / kTopkThreads;  // all loads in flight at once
+                float v[kPerThread];
+#pragma unroll
+                for (int u = 0; u < kPerThread; ++u) {
+                    const int s = tid + u * kTopkThreads;
+                    v[u] = (s < ns) ? __ldcg(z + (int64_t)(s >> 3) * 8 * step + (s & 7)) : 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < kPerThread; ++u) {
+                    const int s = tid + u * kTopkThreads;
+                    if (s < ns) s_ckey[s] = fkey(v[u]);
+                }
+            }
+            const float share = (float)k * (float)ns / (float)n;  // k's expected rank in the sample
+            const int r = min(ns, (int)ceilf(1.25f * share + 4.f * sqrtf(share) + 8.f));
+            fast = (float)r * ((float)n / (float)ns) <= 0.8f * (float)kCandCap;
+            __syncthreads();
+            if (fast) {
+                int unused;
+                smem_radix_select(s_ckey, ns, r, 2, s_hist, &s_prefix, &s_need, t16, unused);
+                // ---- candidates: every token with key >= t16
+                if (tid == 0) {
+                    s_ccount = 0;
+                    s_tcount = 0;
+                }
+                __syncthreads();
+                constexpr int kInFlight = 16;  // loads per thread in flight (64 KB per SM at 2 CTAs)
+                for (int i0 = 0; i0 < n; i0 += kInFlight * kTopkThreads) {
+                    float v[kInFlight];
+#pragma unroll
+                    for (int u = 0; u < kInFlight; ++u) {
+                        const int i = i0 + u * kTopkThreads + tid;
+                        v[u] = (i < n) ? __ldcg(z + i) : 0.f;
+                    }
+                    uint32_t tk = 0u;  // bit u: token i0 + u * kTopkThreads + tid is a candidate
+#pragma unroll
+                    for (int u = 0; u < kInFlight; ++u)
+                        if (i0 + u * kTopkThreads + tid < n && fkey(v[u]) >= t16) tk |= 1u << u;
+                    // one slot reservation per warp: inclusive scan of the lanes' counts
+                    const int c = __popc(tk);
+                    int incl = c;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (lane >= o) incl += y;
+                    }
+                    int wbase = 0;
+                    if (lane == 31 && incl > 0) wbase = atomicAdd(&s_ccount, incl);
+                    int pos = __shfl_sync(0xffffffffu, wbase, 31) + incl - c;
+#pragma unroll
+                    for (int u = 0; u < kInFlight; ++u) {
+                        if ((tk >> u) & 1u) {
+                            if (pos < kCandCap) {
+                                s_ckey[pos] = fkey(v[u]);
+                                s_cidx[pos] = i0 + u * kTopkThreads + tid;
+                            }
+                            ++pos;
+                        }
+                    }
+                }
+                __syncthreads();
+                const int cc = s_ccount;
+                fast = cc >= k && cc <= kCandCap;
+                if (fast) {
+                    // ---- exact k-th largest among the candidates, then the bitmap
+                    uint32_t kth;
+                    int need;
+                    smem_radix_select(s_ckey, cc, k, 4, s_hist, &s_prefix, &s_need, kth, need);
+                    const int nw = (n + 31) >> 5;
+                    for (int w = tid; w < nw; w += kTopkThreads) s_sel[w] = 0u;
+                    __syncthreads();
+                    for (int c = tid; c < cc; c += kTopkThreads) {
+                        const uint32_t key = s_ckey[c];
+                        const int i = s_cidx[c];
+                        if (key > kth) {
+                            atomicOr(&s_sel[i >> 5], 1u << (i & 31));
+                        } else if (key == kth) {
+                            const int t = atomicAdd(&s_tcount, 1);
+                            if (t < kTieCap) s_tlist[t] = i;
+                        }
+                    }
+                    __syncthreads();
+                    const int tc = s_tcount;
+                    fast = tc <= kTieCap;
+                    if (fast) {
+                        // the `need` smallest indices among the ties: rank by counting
+                        for (int j = tid; j < tc; j += kTopkThreads) {
+                            const int i = s_tlist[j];
+                            int rank = 0;
+                            if (need < tc)
+                                for (int l = 0; l < tc; ++l) rank += (s_tlist[l] < i) ? 1 : 0;
+                            if (rank < need) atomicOr(&s_sel[i >> 5], 1u << (i & 31));
+                        }
+                        __syncthreads();
+                        // 8 consecutive bitmap words (256 tokens) per thread, in token order
+                        for (int w0 = 0; w0 < nw; w0 += 8 * kTopkThreads) {
+                            const int wb = w0 + 8 * tid;
+                            uint32_t wv[8];
+                            if (wb + 8 <= nw) {
+                                const uint4 a = *reinterpret_cast<const uint4*>(s_sel + wb);
+                                const uint4 c = *reinterpret_cast<const uint4*>(s_sel + wb + 4);
+                                wv[0] = a.x; wv[1] = a.y; wv[2] = a.z; wv[3] = a.w;
+                                wv[4] = c.x; wv[5] = c.y; wv[6] = c.z; wv[7] = c.w;
+                            } else {
+#pragma unroll
+                                for (int u = 0; u < 8; ++u) wv[u] = (wb + u < nw) ? s_sel[wb + u] : 0u;
+                            }
+                            int mine = 0;
+#pragma unroll
+                            for (int u = 0; u < 8; ++u) mine += __popc(wv[u]);
+                            int total;
+                            int pos = out_base + block_excl_scan(mine, s_warp, &total);
+#pragma unroll
+                            for (int u = 0; u < 8; ++u)
+                                for (uint32_t t = wv[u]; t != 0u; t &= t - 1u) {
+                                    if (pos < p.idx_cap) dst[pos] = (wb + u) * 32 + __ffs(t) - 1;
+                                    ++pos;
+                                }
+                            out_base += total;
+                        }
+                    }
+                }
+            }
         }
-        const int warp = tid >> 5;
-        for (int shift = 24; shift >= 0; shift -= 8) {
-            for (int i = tid; i < (kTopkThreads / 32) * 256; i += kTopkThreads) (&s_whist[0][0])[i] = 0u;
-            __syncthreads();
-            for (int i0 = tid; i0 < n; i0 += 8 * kTopkThreads) {  // 8 loads in flight per thread
-                float v[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int i = i0 + u * kTopkThreads;
-                    v[u] = (i < n) ? __ldcg(z + i) : 0.f;
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const uint32_t key = fkey(v[u]);
-                    if (i0 + u * kTopkThreads < n && (key & mask) == prefix)
-                        atomicAdd(&s_whist[warp][(key >> shift) & 0xFFu], 1u);
-                }
+        if (!fast) {
+            // ---- radix select over all n scores, then a compaction pass
+            uint32_t prefix = 0u, mask = 0u;
+            int need = k;
+            if (tid == 0) {
+                s_prefix = 0u;
+                s_need = need;
             }
-            __syncthreads();
-            for (int i = tid; i < 256; i += kTopkThreads) {
-                unsigned sum = 0u;
-#pragma unroll 8
-                for (int w2 = 0; w2 < kTopkThreads / 32; ++w2) sum += s_whist[w2][i];
-                s_hist[i] = sum;
-            }
-            __syncthreads();
-            if (tid < 32) {
-                // bins from the top: lane l holds bins 255 - 8l ... 248 - 8l
-                unsigned c[8], sum = 0u;
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    c[u] = s_hist[255 - 8 * tid - u];
-                    sum += c[u];
-                }
-                unsigned incl = sum;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (tid >= o) incl += y;
-                }
-                unsigned above = incl - sum;  // keys in the bins above this lane's
-                const unsigned hit = __ballot_sync(0xffffffffu, above < (unsigned)need && (unsigned)need <= incl);
-                if (tid == __ffs(hit) - 1) {
-                    int bin = 255 - 8 * tid;
+            for (int shift = 24; shift >= 0; shift -= 8) {
+                for (int i = tid; i < 256; i += kTopkThreads) s_hist[i] = 0u;
+                __syncthreads();
+                for (int i0 = 0; i0 < n; i0 += 8 * kTopkThreads) {  // 8 loads in flight per thread
+                    float v[8];
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
-                        if (above + c[u] >= (unsigned)need) {
-                            bin = 255 - 8 * tid - u;
-                            break;
-                        }
-                        above += c[u];
+                        const int i = i0 + u * kTopkThreads + tid;
+                        v[u] = (i < n) ? __ldcg(z + i) : 0.f;
                     }
-                    s_prefix = prefix | ((uint32_t)bin << shift);
-                    s_need = need - (int)above;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const uint32_t key = fkey(v[u]);
+                        const bool in = i0 + u * kTopkThreads + tid < n && (key & mask) == prefix;
+                        const unsigned bin = in ? (key >> shift) & 0xFFu : 256u;
+                        const unsigned peers = __match_any_sync(0xffffffffu, bin);
+                        if (in && lane == __ffs(peers) - 1) atomicAdd(&s_hist[bin], (unsigned)__popc(peers));
+                    }
                 }
+                __syncthreads();
+                if (tid < 32) pick_bin(s_hist, need, prefix, shift, &s_prefix, &s_need);
+                __syncthreads();
+                prefix = s_prefix;
+                need = s_need;
+                mask |= 0xFFu << shift;
+                __syncthreads();
             }
-            __syncthreads();
-            prefix = s_prefix;
-            need = s_need;
-            mask |= 0xFFu << shift;
-            __syncthreads();
-        }
-    }
-    // ---- compaction in token order: keys above T, and the first `need` keys equal to T;
-    // each thread takes 8 consecutive tokens of a block of 8 * kTopkThreads
-    constexpr int kPer = 8;
-    const bool all = (k >= n);
-    int out_base = 0, ties_seen = 0;
-    for (int i0 = 0; i0 < n && k > 0; i0 += kPer * kTopkThreads) {
-        const int ib = i0 + tid * kPer;
-        uint32_t take = 0u, tie = 0u;  // bit u: token ib + u
+            // each thread takes 8 consecutive tokens of a block of 8 * kTopkThreads
+            constexpr int kPer = 8;
+            int ties_seen = 0;
+            for (int i0 = 0; i0 < n; i0 += kPer * kTopkThreads) {
+                const int ib = i0 + tid * kPer;
+                uint32_t take = 0u, tie = 0u;  // bit u: token ib + u
 #pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-            const int i = ib + u;
-            if (i < n) {
-                if (all) {
-                    take |= 1u << u;
-                } else {
-                    const uint32_t key = fkey(__ldcg(z + i));
-                    if (key > prefix) take |= 1u << u;
-                    if (key == prefix) tie |= 1u << u;
+                for (int u = 0; u < kPer; ++u) {
+                    const int i = ib + u;
+                    if (i < n) {
+                        const uint32_t key = fkey(__ldcg(z + i));
+                        if (key > prefix) take |= 1u << u;
+                        if (key == prefix) tie |= 1u << u;
+                    }
                 }
+                emit_block(take, tie, ib, need, s_warp, dst, p.idx_cap, out_base, ties_seen);
             }
         }
-        int ties_total;
-        const int tie_before = block_excl_scan(__popc(tie), s_warp, &ties_total);
-        int rank = ties_seen + tie_before;  // ties of the tokens before this thread's
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-            if ((tie >> u) & 1u) {
-                if (rank < need) take |= 1u << u;
-                ++rank;
-            }
-        }
-        ties_seen += ties_total;
-        int taken_total;
-        int pos = out_base + block_excl_scan(__popc(take), s_warp, &taken_total);
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-            if ((take >> u) & 1u) {
-                if (pos < p.idx_cap) dst[pos] = ib + u;
-                ++pos;
-            }
-        }
-        out_base += taken_total;
     }
     for (int t = k + tid; t < p.idx_cap; t += kTopkThreads) dst[t] = -1;
     if (tid == 0) {
@@ -351,7 +561,12 @@ cudaError_t launch_topk_exact(const ExactParams& p, int d, int kv_bf16, cudaStre
         if (d == 64 && !kv_bf16) e = launch_scores_t<64, float>(p, st);
         if (e != cudaSuccess) return e;
     }
-    k_topk_exact<<<p.B * p.Hq, kTopkThreads, 0, st>>>(p);
+    ExactParams q = p;
+    q.bitmap_words = p.n_cap <= kBitmapTokens ? (p.n_cap + 31) / 32 : 0;
+    const size_t smem = (size_t)(2 * kCandCap + q.bitmap_words + kTieCap) * sizeof(uint32_t);
+    e = cudaFuncSetAttribute(k_topk_exact, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k_topk_exact<<<p.B * p.Hq, kTopkThreads, smem, st>>>(q);
     return cudaGetLastError();
 }
 

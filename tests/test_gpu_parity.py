@@ -597,6 +597,46 @@ def test_exact_scores_within_float32_bound(Hq, Hkv, d, q_dtype, kv_dtype):
             assert set(sure) <= set(idx[b, h, :k]) <= set(sure) | set(band), (b, h)
 
 
+@pytest.mark.parametrize("n_cap,pattern", [(131072, "sampled_high"), (131072, "sampled_low"),
+                                            (131072, "random"), (300000, "random")])
+def test_topk_exact_at_length(n_cap, pattern):
+    """The top-m at full context length. The selection estimates its threshold
+    from blocks of 8 tokens out of every 136 (n = 131072); keys whose scores are
+    large exactly on those tokens (or exactly off them) make the estimate miss
+    in both directions, and 300000 tokens exceed the bitmap, so the general
+    radix path is checked at length too. One-hot keys with two scales give exact
+    scores; random keys are checked against the oracle's float32 band."""
+    H = GH.ha()
+    B, Hq, Hkv, d, m = 1, 4, 1, 64, 4096
+    g_ = torch.Generator().manual_seed(37)
+    if pattern == "random":
+        K = torch.randn((B, Hkv, n_cap, d), generator=g_).to(torch.bfloat16)
+        q = torch.randn((B, Hq, d), generator=g_)
+    else:
+        i = torch.arange(n_cap)
+        on = (i % 136) < 8
+        big = on if pattern == "sampled_high" else ~on
+        scale = torch.where(big, 8.0, 0.125).double() * torch.pow(2.0, (i % 3).double())   # exact products
+        K = torch.zeros((B, Hkv, n_cap, d), dtype=torch.float64)
+        K[0, 0, i, (5 * i) % d] = scale
+        K = K.to(torch.bfloat16)
+        q = torch.rand((B, Hq, d), generator=g_) + 0.5      # positive: the scale decides the order
+    Kd, qd = K.cuda(), q.cuda()
+    seq = torch.tensor([n_cap], dtype=torch.int32, device="cuda")
+    shape = H.make_shape(qd, Kd, torch.zeros_like(Kd))
+    z, idx, cnt = _exact_call(H, shape, qd, Kd, seq, m, B, Hq, n_cap)
+    qn, Kn = q.double().numpy(), K.double().numpy()
+    for h in range(Hq):
+        assert int(cnt[0, h]) == m
+        got = idx[0, h, :m]
+        assert np.all(np.diff(got) > 0)
+        if pattern == "random":
+            sure, band = O.top_m_band(qn[0, h], Kn[0, 0], n_cap, m)
+            assert set(sure) <= set(got) <= set(sure) | set(band), h
+        else:
+            assert np.array_equal(got, O.top_m_by_dot(qn[0, h], Kn[0, 0], n_cap, m)), h
+
+
 def test_device_errors_are_flagged_not_faulted():
     H = GH.ha()
     w = W().make_gqa(16, B=3, Hq=4, Hkv=2, d=128, n_cap=2000, seq_lens=[2000, 1500, 2000], m=100,
