@@ -324,8 +324,12 @@ ha_status hash_attn_encode_keys(const ha_shape* shape, const void* K, const floa
  *   cnt      int32 [batch, h_q]
  *   workspace >= hash_attn_topk_exact_workspace_size bytes, 256-byte aligned
  *            (no zeroing needed: every call clears its first word, the device
- *            error word read by hash_attn_device_status; the scores of all
- *            heads live after it)
+ *            error word read by hash_attn_device_status; the scores z of all
+ *            heads follow at byte offset 256 as float32 [batch, h_q, n_cap]
+ *            (entries i < seq_lens[b] written), then scratch query tiles)
+ * bf16 keys with h_q / h_kv <= 10 are scored on the tensor cores (an fp32 q as
+ * three bf16 parts that sum to it exactly, float32 accumulation); other shapes on
+ * the CUDA cores; both give float32 scores.
  * Errors: HA_ERR_INVALID_ARG / HA_ERR_UNSUPPORTED / HA_ERR_WORKSPACE before
  * anything is enqueued; bad seq_lens are flagged in the error word.
  */
