@@ -20,6 +20,8 @@ Everything is NumPy in float64 (signature work in Python/NumPy integers), one
       (``top_m_by_dot``) through its recall (``recall``).
     - Sec. 4.1: the signature is ReLU(sign(.)) of a projection of q or k
       (``encode``; bit j set iff projection j is positive).
+    - Sec. 5 (latency setup): the map as an MLP d -> 128 -> 128 -> 32
+      (``encode_mlp``: ReLU hidden layers with biases, a reading).
     - "Token-level sparsity still needs a careful kernel" (Sec. 4.4, budget
       accounting): the retrieval budget m is joined by the first and the most
       recent tokens of the context.
@@ -115,6 +117,55 @@ def encode_ambiguous(x, W, eps: float = 2.0 ** -22) -> int:
     mask = 0
     for j in range(32):
         if abs(proj[j]) <= bound[j]:
+            mask |= 1 << j
+    return mask
+
+
+def mlp_forward(x, W1, b1, W2, b2, W3, b3):
+    """F(x) = W3 relu(W2 relu(W1 x + b1) + b2) + b3 in float64, with the hidden
+    values (h1, h2) it passes through.
+
+    HashAttention, Sec. 5 (latency setup) runs the signature map F as an MLP
+    d -> 128 -> 128 -> 32. The pages give the widths only; the plainest reading
+    is two hidden layers with biases and a ReLU after each (the signature itself
+    is ReLU(sign(.)) of the last layer, Sec. 4.1).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    h1 = np.maximum(np.asarray(W1, np.float64) @ x + np.asarray(b1, np.float64), 0.0)
+    h2 = np.maximum(np.asarray(W2, np.float64) @ h1 + np.asarray(b2, np.float64), 0.0)
+    f = np.asarray(W3, np.float64) @ h2 + np.asarray(b3, np.float64)
+    return f, h1, h2
+
+
+def encode_mlp(x, W1, b1, W2, b2, W3, b3) -> int:
+    """32-bit code of x under the MLP map: bit j is 1 iff F_j(x) > 0 (0 maps to
+    bit 0), decided in float64."""
+    f, _, _ = mlp_forward(x, W1, b1, W2, b2, W3, b3)
+    code = 0
+    for j in range(32):
+        if f[j] > 0.0:
+            code |= 1 << j
+    return code
+
+
+def encode_mlp_ambiguous(x, W1, b1, W2, b2, W3, b3, eps: float = 2.0 ** -23) -> int:
+    """Bits of ``encode_mlp`` that float32 evaluation may decide either way.
+
+    One float32 layer y = W h + b over K inputs, in any summation order, is off
+    by at most (K + 1) eps (|W| |h| + |b|), with eps twice the unit roundoff; an
+    error e in its input adds |W| e, and ReLU does not enlarge an error. The
+    bound is carried through the three layers (using |h| + e for the float32
+    hidden values); bit j is ambiguous when |F_j| is within it."""
+    W1, W2, W3 = (np.asarray(w, np.float64) for w in (W1, W2, W3))
+    b1, b2, b3 = (np.asarray(b, np.float64) for b in (b1, b2, b3))
+    x = np.asarray(x, dtype=np.float64)
+    f, h1, h2 = mlp_forward(x, W1, b1, W2, b2, W3, b3)
+    e1 = (W1.shape[1] + 1) * eps * (np.abs(W1) @ np.abs(x) + np.abs(b1))
+    e2 = (W2.shape[1] + 1) * eps * (np.abs(W2) @ (h1 + e1) + np.abs(b2)) + np.abs(W2) @ e1
+    e3 = (W3.shape[1] + 1) * eps * (np.abs(W3) @ (h2 + e2) + np.abs(b3)) + np.abs(W3) @ e2
+    mask = 0
+    for j in range(32):
+        if abs(f[j]) <= e3[j]:
             mask |= 1 << j
     return mask
 

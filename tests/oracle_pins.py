@@ -380,6 +380,35 @@ def check_encode(o):
     assert o.encode_ambiguous(xz, Wz) == 1 << 5
 
 
+def check_encode_mlp(o):
+    """MLP map codes: a worked 2 -> 3 -> 3 -> 32 example in which both ReLUs clip
+    a value and one output is exactly 0 (bit 0, the only ambiguous bit); identity
+    hidden layers on non-negative inputs reduce to the sign projection; zero
+    weights leave the bits of the last bias."""
+    W1 = np.array([[1.0, -1.0], [2.0, 0.0], [-1.0, 0.0]])
+    b1 = np.array([0.0, -1.0, 1.0])          # W1 x + b1 = (2, 5, -2) -> h1 = (2, 5, 0)
+    W2 = np.array([[1.0, 0.0, 1.0], [-1.0, 1.0, 0.0], [0.0, 0.0, 1.0]])
+    b2 = np.array([-3.0, 0.0, 1.0])          # W2 h1 + b2 = (-1, 3, 1) -> h2 = (0, 3, 1)
+    W3 = np.array([[1.0, (-1.0) ** j, 1.0] for j in range(32)])
+    b3 = np.array([j - 16.0 for j in range(32)])  # F_j = 3 (-1)^j + j - 15
+    x = np.array([3.0, 1.0])
+    # F_j > 0: even j >= 14 and odd j >= 19; F_12 = 0
+    assert o.encode_mlp(x, W1, b1, W2, b2, W3, b3) == 0xFFFD4000
+    assert o.encode_mlp_ambiguous(x, W1, b1, W2, b2, W3, b3) == 1 << 12
+    rng = np.random.default_rng(53)
+    d = 24
+    I = np.eye(d)
+    for _ in range(10):
+        Wp = rng.standard_normal((32, d))
+        v = np.abs(rng.standard_normal(d))
+        z = np.zeros(d)
+        assert o.encode_mlp(v, I, z, I, z, Wp, np.zeros(32)) == o.encode(v, Wp)
+    bz = rng.standard_normal(32)
+    H = 16
+    assert o.encode_mlp(rng.standard_normal(d), np.zeros((H, d)), np.zeros(H), np.zeros((H, H)), np.zeros(H),
+                        np.zeros((32, H)), bz) == sum(1 << j for j in range(32) if bz[j] > 0)
+
+
 def check_exact_topm_and_recall(o):
     """Exact top-m by dot score against an O(n^2) rank, ties by index, m >= n; the
     rounding band brackets the boundary; recall on worked examples."""
@@ -496,7 +525,7 @@ ALL_CHECKS = [
     check_topm_bruteforce, check_topm_ties, check_windows, check_budget,
     check_dense_vs_sdpa, check_decimal, check_weighted_sum, check_lse_bounds,
     check_lse_gradient, check_low_temperature, check_empty,
-    check_merge_partition, check_merge_segments, check_encode, check_exact_topm_and_recall,
+    check_merge_partition, check_merge_segments, check_encode, check_encode_mlp, check_exact_topm_and_recall,
     check_exclusive_windows, check_wide_codes, check_decode_composition,
 ]
 

@@ -54,6 +54,13 @@ MUTATIONS = [
     ("wide_distance_first_word_only", "    return popcount32(k ^ q).sum(axis=1)", "    return popcount32(k ^ q)[:, 0]"),
     ("encode_zero_sets_bit", "        if proj[j] > 0.0:", "        if proj[j] >= 0.0:"),
     ("encode_bit_order_reversed", "            code |= 1 << j", "            code |= 1 << (31 - j)"),
+    ("mlp_first_relu_dropped", "h1 = np.maximum(np.asarray(W1, np.float64) @ x + np.asarray(b1, np.float64), 0.0)",
+     "h1 = np.asarray(W1, np.float64) @ x + np.asarray(b1, np.float64)"),
+    ("mlp_second_relu_dropped", "h2 = np.maximum(np.asarray(W2, np.float64) @ h1 + np.asarray(b2, np.float64), 0.0)",
+     "h2 = np.asarray(W2, np.float64) @ h1 + np.asarray(b2, np.float64)"),
+    ("mlp_second_bias_dropped", "@ h1 + np.asarray(b2, np.float64), 0.0)", "@ h1, 0.0)"),
+    ("mlp_second_layer_transposed", "np.asarray(W2, np.float64) @ h1", "np.asarray(W2, np.float64).T @ h1"),
+    ("mlp_zero_sets_bit", "        if f[j] > 0.0:", "        if f[j] >= 0.0:"),
     ("encode_transposed_projection", "proj = np.asarray(W, dtype=np.float64) @ np.asarray(x, dtype=np.float64)",
      "proj = np.asarray(x, dtype=np.float64) @ np.asarray(W, dtype=np.float64)[:, :1].repeat(32, axis=1)"),
 ]
