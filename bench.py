@@ -210,19 +210,26 @@ def measure_merge_n(dev, peak):
 
 
 def measure_encode(w, shape, dev):
-    """Sign-projection codes of the step's queries (B x Hq vectors) and of one
-    appended key per (sequence, KV head), at the bench shape."""
+    """Codes of the step's queries (B x Hq vectors) and of one appended key per
+    (sequence, KV head), at the bench shape: sign projection (k_encode) and the
+    MLP map d -> 128 -> 128 -> 32 with random weights (k_encode_mlp)."""
     import torch
     from long_context_sparse_score_gb300 import hashattn as H
+    from long_context_sparse_score_gb300 import workloads as WL
     g = torch.Generator(device=dev).manual_seed(78)
     W = torch.randn((w.Hkv, 32, w.d), generator=g, device=dev)
+    wts = WL.mlp_weights(78, w.Hkv, w.d, 128, device=dev)
+    mw = H.mlp(*wts)
     q_sig = torch.empty_like(w.q_sig)
     k_sig = w.k_sig.clone()
     pos = (w.seq_lens - 1).to(torch.int32)
     reps = 50
-    graphs = []
-    for call in (lambda: H.hash_attn_encode_queries(shape, w.q, W, q_sig),
-                 lambda: H.hash_attn_encode_keys(shape, w.K, W, pos, k_sig)):
+    calls = {"queries_us": lambda: H.hash_attn_encode_queries(shape, w.q, W, q_sig),
+             "keys_us": lambda: H.hash_attn_encode_keys(shape, w.K, W, pos, k_sig),
+             "queries_mlp_us": lambda: H.hash_attn_encode_queries_mlp(shape, w.q, mw, q_sig),
+             "keys_mlp_us": lambda: H.hash_attn_encode_keys_mlp(shape, w.K, mw, pos, k_sig)}
+    graphs = {}
+    for name, call in calls.items():
         for _ in range(3):
             call()
         torch.cuda.synchronize()
@@ -230,21 +237,63 @@ def measure_encode(w, shape, dev):
         with torch.cuda.graph(gr):
             for _ in range(reps):
                 call()
-        graphs.append(gr)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-    for gr in graphs:
+        graphs[name] = gr
+    res = {"kernels": "k_encode, k_encode_mlp", "query_vectors": w.B * w.Hq, "key_vectors": w.B * w.Hkv,
+           "d": w.d, "mlp": f"{w.d} -> 128 -> 128 -> 32 (random weights)"}
+    for name, gr in graphs.items():
         gr.replay()
-    torch.cuda.synchronize()
-    ev[0].record()
-    graphs[0].replay()
-    ev[1].record()
-    graphs[1].replay()
-    ev[2].record()
-    torch.cuda.synchronize()
-    return {"kernel": "k_encode", "query_vectors": w.B * w.Hq, "key_vectors": w.B * w.Hkv, "d": w.d,
-            "queries_us": ev[0].elapsed_time(ev[1]) * 1e3 / reps, "keys_us": ev[1].elapsed_time(ev[2]) * 1e3 / reps,
-            "bound": "latency (32 x d GEMV per vector)", "timing": "CUDA graph of 50 launches"}
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        gr.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        res[name] = e0.elapsed_time(e1) * 1e3 / reps
+    res.update({"bound": "latency (small GEMVs per vector)", "timing": "CUDA graph of 50 launches"})
+    return res
 
+
+def measure_mapped(w, shape, dev):
+    """The decode step from raw queries (hash_attn_decode_mapped): the map writes
+    each sequence's appended-token key code and the query codes ahead of SCORE
+    (HashAttention's T_map in T = T_map + T_scan + T_TOPK + T_att), for the sign
+    projection and the MLP map. Codes and outputs go to buffers of their own."""
+    import torch
+    from long_context_sparse_score_gb300 import hashattn as H
+    from long_context_sparse_score_gb300 import workloads as WL
+    g = torch.Generator(device=dev).manual_seed(80)
+    W = torch.randn((w.Hkv, 32, w.d), generator=g, device=dev)
+    wts = WL.mlp_weights(80, w.Hkv, w.d, 128, device=dev)
+    mw = H.mlp(*wts)
+    k_sig = w.k_sig.clone()
+    q_sig = torch.empty_like(w.q_sig)
+    pos = (w.seq_lens - 1).to(torch.int32)
+    out = torch.empty((w.B, w.Hq, w.d), dtype=torch.float32, device=dev)
+    lse = torch.empty((w.B, w.Hq), dtype=torch.float32, device=dev)
+    shape_m = H.make_shape(w.q, w.K, w.V, k_sig)
+    ws = torch.empty(H.hash_attn_workspace_size(shape_m, w.m, w.n_sink, w.n_local), dtype=torch.uint8, device=dev)
+    H.hash_attn_workspace_init(ws)
+    res = {}
+    for name, map_ in (("sign_projection", H.sign_map(W)), ("mlp_128_128_32", H.mlp_map(mw))):
+        call = lambda: H.hash_attn_decode_mapped(shape_m, w.q, map_, pos, q_sig, k_sig, w.K, w.V, w.seq_lens,
+                                                 None, w.m, w.n_sink, w.n_local, None, out, lse, workspace=ws)
+        for _ in range(5):
+            call()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 100
+        e0.record()
+        for _ in range(reps):
+            call()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        res[name] = {"ms_per_step": ms, "query_heads_per_s": w.B * w.Hq / (ms * 1e-3)}
+    st, flags = H.hash_attn_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"mapped decode: device status {st} flags {flags:#x}")
+    res["note"] = "map kernels + SCORE + TOPK + GATHER-ATT per step; one appended token per sequence"
+    return res
 
 def measure_exact(w, shape, sel, cnt, dev):
     """The exact comparator on the bench workload: top-m (m = the decode budget)
@@ -565,7 +614,8 @@ def run_ours(args, world, rank, local):
         "clocks": clocks,
         "next": {"merge_n": measure_merge_n(dev, peak), "encode": measure_encode(w, shape, dev),
                  "exact_topk": measure_exact(w, shape, sel, cnt, dev),
-                 "selection_variants": measure_variants(w, shape, ws, dev)},
+                 "selection_variants": measure_variants(w, shape, ws, dev),
+                 "mapped_decode": measure_mapped(w, shape, dev)},
     }
     if not args.no_cpu_baseline:
         cpu_s, cpu_heads, res = run_cpu_oracle(w, args.cpu_heads)

@@ -314,6 +314,63 @@ ha_status hash_attn_encode_keys(const ha_shape* shape, const void* K, const floa
                                 uint32_t* k_sig, uint32_t* dev_flags, void* stream);
 
 /*
+ * The signature map as an MLP (HashAttention Sec. 5 runs the map as
+ * d -> 128 -> 128 -> 32; the widths are given, the rest is the plainest
+ * reading): per KV head g, F(x) = W3 relu(W2 relu(W1 x + b1) + b2) + b3 and
+ * bit j of the code is 1 iff F_j(x) > 0. All float32, contiguous, device:
+ *   W1 [h_kv, hidden, d], b1 [h_kv, hidden], W2 [h_kv, hidden, hidden],
+ *   b2 [h_kv, hidden], W3 [h_kv, 32, hidden], b3 [h_kv, 32];
+ *   hidden is 32, 64 or 128; W1, W2 and W3 are 16-byte aligned; reserved is 0.
+ * Layers accumulate in float32 over their inputs in order.
+ */
+typedef struct {
+    const float* W1;
+    const float* b1;
+    const float* W2;
+    const float* b2;
+    const float* W3;
+    const float* b3;
+    int32_t hidden;
+    int32_t reserved;
+} ha_mlp;
+
+/* hash_attn_encode_queries / hash_attn_encode_keys with the MLP map (same
+ * arguments otherwise). Errors: HA_ERR_INVALID_ARG / HA_ERR_UNSUPPORTED (shape,
+ * NULL pointers, hidden width, alignment) before anything is enqueued. */
+ha_status hash_attn_encode_queries_mlp(const ha_shape* shape, const void* q, const ha_mlp* mlp, uint32_t* q_sig,
+                                       void* stream);
+ha_status hash_attn_encode_keys_mlp(const ha_shape* shape, const void* K, const ha_mlp* mlp, const int32_t* pos,
+                                    uint32_t* k_sig, uint32_t* dev_flags, void* stream);
+
+/*
+ * One decode step with the signature map run ahead of SCORE (HashAttention's
+ * cost model: T = T_map + T_scan + T_TOPK + T_att). First the code of every
+ * sequence's appended token, k_sig[b, g, pos[b]] (pos == NULL: no token is
+ * appended; positions outside [0, n_cap) are skipped and flagged in dev_flags
+ * as for hash_attn_encode_keys), then the query codes q_sig[b, h], both by the
+ * map, then the path of hash_attn_decode_ex reading them.
+ *   map     exactly one of W (sign projection float32 [h_kv, 32, d], as for
+ *           hash_attn_encode_queries) and mlp non-NULL
+ *   q_sig   uint32 [batch, h_q] contiguous, device (written)
+ *   k_sig   key codes per shape (read; the appended tokens' codes written)
+ *   the rest as hash_attn_decode_ex; the map writes 32-bit codes, so
+ *           opts->code_words must be 0 or 1.
+ * Errors: as hash_attn_decode_ex, plus HA_ERR_INVALID_ARG / HA_ERR_UNSUPPORTED
+ * for the map, all before anything is enqueued.
+ */
+typedef struct {
+    const float* W;
+    const ha_mlp* mlp;
+} ha_map;
+
+ha_status hash_attn_decode_mapped(const ha_shape* shape, const void* q, const ha_map* map, const int32_t* pos,
+                                  uint32_t* q_sig, uint32_t* k_sig, const void* K, const void* V,
+                                  const int32_t* seq_lens, const int32_t* m_per_seq, int32_t m, int32_t n_sink,
+                                  int32_t n_local, const ha_select_opts* opts, float* out, float* lse,
+                                  int32_t* sel_idx, int32_t* sel_cnt, void* workspace, size_t ws_bytes,
+                                  uint32_t* dev_flags, void* stream);
+
+/*
  * The exact comparator of the hashed selection (HashAttention Sec. 5 measures
  * against the top-k by attention score): for every (b, h), the k = min(m, n)
  * tokens with the largest z_i = <q[b, h], K[b, h / G, i]> (float32, i < n =

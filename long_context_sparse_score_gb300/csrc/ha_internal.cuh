@@ -169,6 +169,9 @@ struct EncodeParams {
     const int32_t* pos;      // keys only
     uint32_t* flags;         // optional (keys): HA_DEVERR_INDEX for a position outside [0, n_cap)
     int B, Hq, Hkv, G, d, n_cap, keys;
+    // MLP map (k_encode_mlp): per KV head W1 [hidden][d], W2 [hidden][hidden], W3 [32][hidden]
+    const float *W1, *b1, *W2, *b2, *W3, *b3;
+    int hidden;
 };
 
 // SCORE/TOPK for codes of W > 1 words (b = 32 W bits, NB = b + 1 bins); the
@@ -251,6 +254,7 @@ cudaError_t launch_gather(const GatherParams& p, int d, int kv_bf16, cudaStream_
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t st);
 cudaError_t launch_merge_n(const MergeNParams& p, cudaStream_t st);
 cudaError_t launch_encode(const EncodeParams& p, cudaStream_t st);
+cudaError_t launch_encode_mlp(const EncodeParams& p, cudaStream_t st);
 cudaError_t launch_topk_exact(const ExactParams& p, int d, int kv_bf16, cudaStream_t st);
 // Tensor-core scores (bf16 K, 3 G <= 32); *used = false leaves the scores to
 // the CUDA-core kernel (a layout TMA cannot describe).

@@ -310,11 +310,18 @@ void apply_opts(const ha_select_opts* o, int32_t n_sink, int32_t n_local, ScoreP
     tp->excl = sp->excl;
 }
 
+// The signature map run ahead of SCORE (hash_attn_decode_mapped): the appended
+// tokens' key codes (optional) and the step's query codes.
+struct MapStep {
+    EncodeParams queries, keys;
+    bool mlp = false, with_keys = false;
+};
+
 ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, const uint32_t* k_sig,
                       const void* K, const void* V, const int32_t* seq_lens, const int32_t* m_per_seq,
                       int32_t m, int32_t n_sink, int32_t n_local, const ha_select_opts* opts, float* out,
                       float* lse, int32_t* sel_idx, int32_t* sel_cnt, void* ws, size_t ws_bytes, void* stream,
-                      void* const* events) {
+                      void* const* events, const MapStep* map = nullptr) {
     HA_TRY(check_shape(s));
     HA_TRY(check_window(m, n_sink, n_local));
     HA_TRY(check_opts(opts));
@@ -334,6 +341,12 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int bhkv = s->batch * s->h_kv;
     const int heads = s->batch * s->h_q;
+    if (map != nullptr) {  // every check has passed: nothing was enqueued before this point
+        if (map->with_keys)
+            HA_LAUNCH(map->mlp ? launch_encode_mlp(map->keys, st) : launch_encode(map->keys, st), "key map launch");
+        HA_LAUNCH(map->mlp ? launch_encode_mlp(map->queries, st) : launch_encode(map->queries, st),
+                  "query map launch");
+    }
 
     GatherParams gp = gather_params(s, lay, v, q, K, V, seq_lens, out, lse);
     if (dense) {
@@ -381,6 +394,68 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
         HA_LAUNCH(launch_compact(cp, heads, st), "compaction launch");
     }
     return HA_OK;
+}
+
+EncodeParams query_encode_params(const ha_shape* shape, const void* q, uint32_t* q_sig) {
+    EncodeParams p{};
+    p.x = q;
+    p.x_bf16 = shape->q_dtype == HA_BF16;
+    p.x_sb = shape->q_sb;
+    p.x_sh = shape->q_sh;
+    p.codes = q_sig;
+    p.B = shape->batch;
+    p.Hq = shape->h_q;
+    p.Hkv = shape->h_kv;
+    p.G = shape->h_q / shape->h_kv;
+    p.d = shape->d;
+    p.n_cap = shape->n_cap;
+    p.keys = 0;
+    return p;
+}
+
+EncodeParams key_encode_params(const ha_shape* shape, const void* K, const int32_t* pos, uint32_t* k_sig,
+                               uint32_t* dev_flags) {
+    EncodeParams p{};
+    p.x = K;
+    p.x_bf16 = shape->kv_dtype == HA_BF16;
+    p.x_sb = shape->k_sb;
+    p.x_sh = shape->k_sh;
+    p.x_sn = shape->k_sn;
+    p.codes = k_sig;
+    p.c_sb = shape->ks_sb;
+    p.c_sh = shape->ks_sh;
+    p.pos = pos;
+    p.flags = dev_flags;
+    p.B = shape->batch;
+    p.Hq = shape->h_q;
+    p.Hkv = shape->h_kv;
+    p.G = shape->h_q / shape->h_kv;
+    p.d = shape->d;
+    p.n_cap = shape->n_cap;
+    p.keys = 1;
+    return p;
+}
+
+ha_status check_mlp(const ha_mlp* mlp) {
+    if (mlp->W1 == nullptr || mlp->b1 == nullptr || mlp->W2 == nullptr || mlp->b2 == nullptr ||
+        mlp->W3 == nullptr || mlp->b3 == nullptr)
+        return fail(HA_ERR_INVALID_ARG, "every MLP weight and bias must be given");
+    if (mlp->hidden != 32 && mlp->hidden != 64 && mlp->hidden != 128)
+        return fail(HA_ERR_UNSUPPORTED, "MLP hidden width must be 32, 64 or 128 (got %d)", mlp->hidden);
+    if (!aligned16(mlp->W1) || !aligned16(mlp->W2) || !aligned16(mlp->W3))
+        return fail(HA_ERR_INVALID_ARG, "MLP weight matrices must be 16-byte aligned");
+    if (mlp->reserved != 0) return fail(HA_ERR_INVALID_ARG, "ha_mlp.reserved must be zero");
+    return HA_OK;
+}
+
+void set_mlp(EncodeParams* p, const ha_mlp* mlp) {
+    p->W1 = mlp->W1;
+    p->b1 = mlp->b1;
+    p->W2 = mlp->W2;
+    p->b2 = mlp->b2;
+    p->W3 = mlp->W3;
+    p->b3 = mlp->b3;
+    p->hidden = mlp->hidden;
 }
 
 }  // namespace
@@ -658,20 +733,8 @@ ha_status hash_attn_encode_queries(const ha_shape* shape, const void* q, const f
     HA_TRY(check_shape(shape));
     if (q == nullptr || W == nullptr || q_sig == nullptr)
         return fail(HA_ERR_INVALID_ARG, "q, W and q_sig must not be NULL");
-    EncodeParams p{};
-    p.x = q;
-    p.x_bf16 = shape->q_dtype == HA_BF16;
-    p.x_sb = shape->q_sb;
-    p.x_sh = shape->q_sh;
+    EncodeParams p = query_encode_params(shape, q, q_sig);
     p.W = W;
-    p.codes = q_sig;
-    p.B = shape->batch;
-    p.Hq = shape->h_q;
-    p.Hkv = shape->h_kv;
-    p.G = shape->h_q / shape->h_kv;
-    p.d = shape->d;
-    p.n_cap = shape->n_cap;
-    p.keys = 0;
     HA_LAUNCH(launch_encode(p, static_cast<cudaStream_t>(stream)), "query encode launch");
     return HA_OK;
 }
@@ -681,27 +744,65 @@ ha_status hash_attn_encode_keys(const ha_shape* shape, const void* K, const floa
     HA_TRY(check_shape(shape));
     if (K == nullptr || W == nullptr || pos == nullptr || k_sig == nullptr)
         return fail(HA_ERR_INVALID_ARG, "K, W, pos and k_sig must not be NULL");
-    EncodeParams p{};
-    p.x = K;
-    p.x_bf16 = shape->kv_dtype == HA_BF16;
-    p.x_sb = shape->k_sb;
-    p.x_sh = shape->k_sh;
-    p.x_sn = shape->k_sn;
+    EncodeParams p = key_encode_params(shape, K, pos, k_sig, dev_flags);
     p.W = W;
-    p.codes = k_sig;
-    p.c_sb = shape->ks_sb;
-    p.c_sh = shape->ks_sh;
-    p.pos = pos;
-    p.flags = dev_flags;
-    p.B = shape->batch;
-    p.Hq = shape->h_q;
-    p.Hkv = shape->h_kv;
-    p.G = shape->h_q / shape->h_kv;
-    p.d = shape->d;
-    p.n_cap = shape->n_cap;
-    p.keys = 1;
     HA_LAUNCH(launch_encode(p, static_cast<cudaStream_t>(stream)), "key encode launch");
     return HA_OK;
+}
+
+ha_status hash_attn_encode_queries_mlp(const ha_shape* shape, const void* q, const ha_mlp* mlp, uint32_t* q_sig,
+                                       void* stream) {
+    HA_TRY(check_shape(shape));
+    if (q == nullptr || mlp == nullptr || q_sig == nullptr)
+        return fail(HA_ERR_INVALID_ARG, "q, mlp and q_sig must not be NULL");
+    HA_TRY(check_mlp(mlp));
+    EncodeParams p = query_encode_params(shape, q, q_sig);
+    set_mlp(&p, mlp);
+    HA_LAUNCH(launch_encode_mlp(p, static_cast<cudaStream_t>(stream)), "query MLP encode launch");
+    return HA_OK;
+}
+
+ha_status hash_attn_encode_keys_mlp(const ha_shape* shape, const void* K, const ha_mlp* mlp, const int32_t* pos,
+                                    uint32_t* k_sig, uint32_t* dev_flags, void* stream) {
+    HA_TRY(check_shape(shape));
+    if (K == nullptr || mlp == nullptr || pos == nullptr || k_sig == nullptr)
+        return fail(HA_ERR_INVALID_ARG, "K, mlp, pos and k_sig must not be NULL");
+    HA_TRY(check_mlp(mlp));
+    EncodeParams p = key_encode_params(shape, K, pos, k_sig, dev_flags);
+    set_mlp(&p, mlp);
+    HA_LAUNCH(launch_encode_mlp(p, static_cast<cudaStream_t>(stream)), "key MLP encode launch");
+    return HA_OK;
+}
+
+ha_status hash_attn_decode_mapped(const ha_shape* shape, const void* q, const ha_map* map, const int32_t* pos,
+                                  uint32_t* q_sig, uint32_t* k_sig, const void* K, const void* V,
+                                  const int32_t* seq_lens, const int32_t* m_per_seq, int32_t m, int32_t n_sink,
+                                  int32_t n_local, const ha_select_opts* opts, float* out, float* lse,
+                                  int32_t* sel_idx, int32_t* sel_cnt, void* workspace, size_t ws_bytes,
+                                  uint32_t* dev_flags, void* stream) {
+    HA_TRY(check_shape(shape));
+    HA_TRY(check_opts(opts));
+    if (map == nullptr || (map->W == nullptr) == (map->mlp == nullptr))
+        return fail(HA_ERR_INVALID_ARG, "exactly one of map->W and map->mlp must be given");
+    if (map->mlp != nullptr) HA_TRY(check_mlp(map->mlp));
+    if (code_words_of(opts) > 1)
+        return fail(HA_ERR_UNSUPPORTED, "the map writes 32-bit codes (opts->code_words must be 0 or 1)");
+    HA_TRY(check_codes(shape, q_sig, k_sig));
+    if (q == nullptr || K == nullptr) return fail(HA_ERR_INVALID_ARG, "q and K must not be NULL");
+    MapStep ms;
+    ms.mlp = map->mlp != nullptr;
+    ms.with_keys = pos != nullptr;
+    ms.queries = query_encode_params(shape, q, q_sig);
+    ms.keys = key_encode_params(shape, K, pos, k_sig, dev_flags);
+    if (ms.mlp) {
+        set_mlp(&ms.queries, map->mlp);
+        set_mlp(&ms.keys, map->mlp);
+    } else {
+        ms.queries.W = map->W;
+        ms.keys.W = map->W;
+    }
+    return decode_impl(shape, q, q_sig, k_sig, K, V, seq_lens, m_per_seq, m, n_sink, n_local, opts, out, lse,
+                       sel_idx, sel_cnt, workspace, ws_bytes, stream, nullptr, &ms);
 }
 
 ha_status hash_attn_topk_exact_workspace_size(const ha_shape* shape, size_t* bytes) {

@@ -40,7 +40,8 @@ EXPORTED = [
     "hash_attn_decode", "hash_attn_decode_ex", "hash_attn_decode_timed", "hash_attn_score", "hash_attn_select",
     "hash_attn_select_ex", "hash_attn_workspace_size_ex",
     "hash_attn_gather_att", "hash_attn_gather_att_noalloc", "hash_attn_merge", "hash_attn_merge_n",
-    "hash_attn_encode_queries", "hash_attn_encode_keys", "hash_attn_topk_exact_workspace_size",
+    "hash_attn_encode_queries", "hash_attn_encode_keys", "hash_attn_encode_queries_mlp",
+    "hash_attn_encode_keys_mlp", "hash_attn_decode_mapped", "hash_attn_topk_exact_workspace_size",
     "hash_attn_topk_exact", "hash_attn_recall",
     "hash_attn_device_status",
     "hash_attn_status_string", "hash_attn_last_error",
@@ -60,6 +61,42 @@ def select_opts(m_per_head=None, exclusive_windows=False, code_words=1) -> HASel
     o.exclusive_windows = 1 if exclusive_windows else 0
     o.code_words = int(code_words)
     return o
+
+
+class HAMlp(ctypes.Structure):
+    """Mirror of ``ha_mlp`` (the MLP signature map's weights, device pointers)."""
+
+    _fields_ = [("W1", ctypes.c_void_p), ("b1", ctypes.c_void_p), ("W2", ctypes.c_void_p),
+                ("b2", ctypes.c_void_p), ("W3", ctypes.c_void_p), ("b3", ctypes.c_void_p),
+                ("hidden", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+def mlp(W1, b1, W2, b2, W3, b3) -> HAMlp:
+    """HAMlp over float32 device tensors W1 [h_kv, H, d], b1 [h_kv, H], W2 [h_kv, H, H],
+    b2 [h_kv, H], W3 [h_kv, 32, H], b3 [h_kv, 32]. The struct holds raw pointers:
+    keep the tensors alive while it is used."""
+    m = HAMlp()
+    m.W1, m.b1, m.W2, m.b2, m.W3, m.b3 = (_ptr(t) for t in (W1, b1, W2, b2, W3, b3))
+    m.hidden = int(W1.shape[1])
+    return m
+
+
+class HAMap(ctypes.Structure):
+    """Mirror of ``ha_map``: exactly one of W (sign projection) and mlp."""
+
+    _fields_ = [("W", ctypes.c_void_p), ("mlp", ctypes.POINTER(HAMlp))]
+
+
+def sign_map(W) -> HAMap:
+    m = HAMap()
+    m.W = _ptr(W)
+    return m
+
+
+def mlp_map(weights: HAMlp) -> HAMap:
+    m = HAMap()
+    m.mlp = ctypes.pointer(weights)
+    return m
 
 
 class HAShape(ctypes.Structure):
@@ -118,6 +155,10 @@ def lib() -> ctypes.CDLL:
     L.hash_attn_merge_n.argtypes = [_P, ctypes.c_int64, _P, ctypes.c_int64, _I32, _P, _P, _I32, _I32, _P]
     L.hash_attn_encode_queries.argtypes = [SP, _P, _P, _P, _P]
     L.hash_attn_encode_keys.argtypes = [SP, _P, _P, _P, _P, _P, _P]
+    L.hash_attn_encode_queries_mlp.argtypes = [SP, _P, ctypes.POINTER(HAMlp), _P, _P]
+    L.hash_attn_encode_keys_mlp.argtypes = [SP, _P, ctypes.POINTER(HAMlp), _P, _P, _P, _P]
+    L.hash_attn_decode_mapped.argtypes = [SP, _P, ctypes.POINTER(HAMap), _P, _P, _P, _P, _P, _P, _P, _I32, _I32,
+                                          _I32, OP, _P, _P, _P, _P, _P, _SZ, _P, _P]
     L.hash_attn_topk_exact_workspace_size.argtypes = [SP, ctypes.POINTER(_SZ)]
     L.hash_attn_topk_exact.argtypes = [SP, _P, _P, _P, _I32, _P, _I32, _P, _P, _SZ, _P]
     L.hash_attn_recall.argtypes = [_P, _P, _I32, _P, _P, _I32, _I32, _P, _P]
@@ -318,6 +359,30 @@ def hash_attn_encode_keys(shape, K, W, pos, k_sig, dev_flags=None, stream=None) 
     """k_sig[b, g, pos[b]] = code of K[b, g, pos[b]] under W[g], for pos[b] in [0, n_cap)."""
     _check(lib().hash_attn_encode_keys(ctypes.byref(shape), _ptr(K), _ptr(W), _ptr(pos), _ptr(k_sig),
                                        _ptr(dev_flags), _stream(stream)))
+
+
+def hash_attn_encode_queries_mlp(shape, q, weights: HAMlp, q_sig, stream=None) -> None:
+    """q_sig[b, h] = code of q[b, h] under the MLP map of KV head h / G."""
+    _check(lib().hash_attn_encode_queries_mlp(ctypes.byref(shape), _ptr(q), ctypes.byref(weights), _ptr(q_sig),
+                                              _stream(stream)))
+
+
+def hash_attn_encode_keys_mlp(shape, K, weights: HAMlp, pos, k_sig, dev_flags=None, stream=None) -> None:
+    """k_sig[b, g, pos[b]] = code of K[b, g, pos[b]] under the MLP map of KV head g."""
+    _check(lib().hash_attn_encode_keys_mlp(ctypes.byref(shape), _ptr(K), ctypes.byref(weights), _ptr(pos),
+                                           _ptr(k_sig), _ptr(dev_flags), _stream(stream)))
+
+
+def hash_attn_decode_mapped(shape, q, map_, pos, q_sig, k_sig, K, V, seq_lens, m_per_seq, m, n_sink, n_local,
+                            opts, out, lse, sel_idx=None, sel_cnt=None, *, workspace, dev_flags=None,
+                            stream=None) -> None:
+    """One decode step with the signature map (``sign_map`` / ``mlp_map``) ahead of SCORE."""
+    ws, nb = _ws(workspace)
+    _check(lib().hash_attn_decode_mapped(ctypes.byref(shape), _ptr(q), ctypes.byref(map_), _ptr(pos), _ptr(q_sig),
+                                         _ptr(k_sig), _ptr(K), _ptr(V), _ptr(seq_lens), _ptr(m_per_seq), m,
+                                         n_sink, n_local, None if opts is None else ctypes.byref(opts), _ptr(out),
+                                         _ptr(lse), _ptr(sel_idx), _ptr(sel_cnt), ws, nb, _ptr(dev_flags),
+                                         _stream(stream)))
 
 
 def hash_attn_topk_exact_workspace_size(shape) -> int:

@@ -81,6 +81,20 @@ def _gen(cfg: int, sub: int, device) -> torch.Generator:
     return g
 
 
+def mlp_weights(cfg: int, Hkv: int, d: int, hidden: int = 128, device="cpu"):
+    """Random weights for the MLP signature map d -> hidden -> hidden -> 32 per KV
+    head, float32: W ~ N(0, 1/fan_in), biases ~ N(0, 0.1^2). Returns
+    (W1 [Hkv, H, d], b1 [Hkv, H], W2 [Hkv, H, H], b2 [Hkv, H], W3 [Hkv, 32, H], b3 [Hkv, 32])."""
+    g = _gen(cfg, 7, device)
+    shapes = [((Hkv, hidden, d), d), ((Hkv, hidden), 0), ((Hkv, hidden, hidden), hidden), ((Hkv, hidden), 0),
+              ((Hkv, N_BITS, hidden), hidden), ((Hkv, N_BITS), 0)]
+    out = []
+    for shp, fan_in in shapes:
+        t = torch.randn(shp, generator=g, device=device, dtype=torch.float32)
+        out.append(t / fan_in ** 0.5 if fan_in else 0.1 * t)
+    return tuple(out)
+
+
 def pack_bits(bits: torch.Tensor) -> torch.Tensor:
     """[..., 32] bool -> int32 word with bit j (LSB = 0) = bits[..., j]."""
     w = torch.arange(N_BITS, device=bits.device, dtype=torch.int64)

@@ -458,6 +458,119 @@ def test_encode_queries_and_keys(d, q_dtype):
     assert int(flags.item()) & H.HA_DEVERR_INDEX
 
 
+@pytest.mark.parametrize("d,q_dtype,hidden", [(128, torch.float32, 128), (64, torch.bfloat16, 64),
+                                              (128, torch.bfloat16, 32)])
+def test_encode_mlp_queries_and_keys(d, q_dtype, hidden):
+    """MLP-map codes against the oracle: every bit outside the float32 error bound
+    of the three layers must match; appended keys land at their positions only;
+    20 query vectors per KV head leave a ragged last CTA."""
+    H = GH.ha()
+    B, Hq, Hkv, n_cap = 5, 8, 2, 64
+    gen = torch.Generator(device="cuda").manual_seed(61 + d + hidden)
+    q = torch.randn((B, Hq, d), generator=gen, device="cuda").to(q_dtype)
+    K = torch.randn((B, Hkv, n_cap, d), generator=gen, device="cuda").to(torch.bfloat16)
+    wts = W().mlp_weights(29, Hkv, d, hidden, device="cuda")
+    mw = H.mlp(*wts)
+    k_sig = torch.full((B, Hkv, n_cap), 0x5A5A5A5A, dtype=torch.int32, device="cuda")
+    shape = H.make_shape(q, K, torch.zeros_like(K), k_sig)
+    q_sig = torch.zeros((B, Hq), dtype=torch.int32, device="cuda")
+    H.hash_attn_encode_queries_mlp(shape, q, mw, q_sig)
+    pos_l = [17, -1, n_cap - 1, 0, 40]
+    pos = torch.tensor(pos_l, dtype=torch.int32, device="cuda")
+    flags = torch.zeros(1, dtype=torch.int32, device="cuda")
+    before = k_sig.clone()
+    H.hash_attn_encode_keys_mlp(shape, K, mw, pos, k_sig, flags)
+    torch.cuda.synchronize()
+    wn = [t.double().cpu().numpy() for t in wts]
+    qn, Kn = q.double().cpu().numpy(), K.double().cpu().numpy()
+    G = Hq // Hkv
+    got_q = q_sig.cpu().numpy().astype(np.int64) & 0xFFFFFFFF
+    for b in range(B):
+        for h in range(Hq):
+            args = [t[h // G] for t in wn]
+            ref, amb = O.encode_mlp(qn[b, h], *args), O.encode_mlp_ambiguous(qn[b, h], *args)
+            assert (int(got_q[b, h]) ^ ref) & ~amb & 0xFFFFFFFF == 0, (b, h, hex(int(got_q[b, h])), hex(ref))
+    got_k = k_sig.cpu().numpy().astype(np.int64) & 0xFFFFFFFF
+    exp_k = before.cpu().numpy().astype(np.int64) & 0xFFFFFFFF
+    for b, p_ in enumerate(pos_l):
+        for g in range(Hkv):
+            if p_ < 0:
+                continue
+            args = [t[g] for t in wn]
+            ref, amb = O.encode_mlp(Kn[b, g, p_], *args), O.encode_mlp_ambiguous(Kn[b, g, p_], *args)
+            assert (int(got_k[b, g, p_]) ^ ref) & ~amb & 0xFFFFFFFF == 0, (b, g)
+            exp_k[b, g, p_] = got_k[b, g, p_]
+    assert np.array_equal(got_k, exp_k), "codes outside the appended positions changed"
+    assert int(flags.item()) & H.HA_DEVERR_INDEX
+
+
+@pytest.mark.parametrize("kind", ["sign", "mlp"])
+def test_decode_mapped_runs_the_map_ahead_of_score(kind):
+    """One decode step from raw q: the map writes the appended tokens' key codes
+    and the query codes (as the stand-alone encoders give them, and matching the
+    oracle's unambiguous bits), and the rest of the step equals
+    hash_attn_decode on those codes, bit for bit."""
+    import copy
+    H = GH.ha()
+    w = W().make_gqa(41, B=3, Hq=8, Hkv=2, d=128, n_cap=4000, seq_lens=[4000, 3001, 1234], m=300, n_sink=16,
+                     n_local=32, device="cuda")
+    pos = (w.seq_lens - 1).to(torch.int32)
+    k_sig = w.k_sig.clone()
+    for b, p_ in enumerate(pos.tolist()):
+        k_sig[b, :, p_] = 0x5A5A5A5A            # stale: the map must rewrite it
+    stale = k_sig.clone()
+    gen = torch.Generator(device="cuda").manual_seed(43)
+    if kind == "sign":
+        Wp = torch.randn((2, 32, 128), generator=gen, device="cuda")
+        map_ = H.sign_map(Wp)
+    else:
+        wts = W().mlp_weights(31, 2, 128, 128, device="cuda")
+        mw = H.mlp(*wts)
+        map_ = H.mlp_map(mw)
+    shape = H.make_shape(w.q, w.K, w.V, k_sig)
+    ws = GH.workspace(shape, w.m, w.n_sink, w.n_local)
+    B, Hq, d = w.q.shape
+    q_sig = torch.zeros((B, Hq), dtype=torch.int32, device="cuda")
+    out = torch.full((B, Hq, d), float("nan"), device="cuda")
+    lse = torch.full((B, Hq), float("nan"), device="cuda")
+    cap = H.hash_attn_select_capacity(4000, w.m, w.n_sink, w.n_local)
+    sel_idx = torch.full((B, Hq, cap), -7, dtype=torch.int32, device="cuda")
+    sel_cnt = torch.full((B, Hq), -7, dtype=torch.int32, device="cuda")
+    H.hash_attn_decode_mapped(shape, w.q, map_, pos, q_sig, k_sig, w.K, w.V, w.seq_lens, None, w.m, w.n_sink,
+                              w.n_local, None, out, lse, sel_idx, sel_cnt, workspace=ws)
+    st, flags = H.hash_attn_device_status(ws)
+    assert st == 0, flags
+    q_ref = torch.zeros_like(q_sig)
+    k_ref = stale.clone()
+    if kind == "sign":
+        H.hash_attn_encode_queries(shape, w.q, Wp, q_ref)
+        H.hash_attn_encode_keys(shape, w.K, Wp, pos, k_ref)
+    else:
+        H.hash_attn_encode_queries_mlp(shape, w.q, mw, q_ref)
+        H.hash_attn_encode_keys_mlp(shape, w.K, mw, pos, k_ref)
+    torch.cuda.synchronize()
+    assert torch.equal(q_sig, q_ref) and torch.equal(k_sig, k_ref)
+    changed = (k_sig != stale).nonzero().tolist()
+    assert all(i == pos[b].item() for b, _, i in changed)
+    Kn = w.K.double().cpu().numpy()
+    for b, p_ in enumerate(pos.tolist()):     # the appended keys against the oracle
+        for g in range(2):
+            x = Kn[b, g, p_]
+            if kind == "sign":
+                Wn = Wp[g].double().cpu().numpy()
+                ref, amb = O.encode(x, Wn), O.encode_ambiguous(x, Wn)
+            else:
+                args = [t[g].double().cpu().numpy() for t in wts]
+                ref, amb = O.encode_mlp(x, *args), O.encode_mlp_ambiguous(x, *args)
+            assert (int(k_sig[b, g, p_].item()) & 0xFFFFFFFF ^ ref) & ~amb & 0xFFFFFFFF == 0, (b, g)
+    w2 = copy.copy(w)
+    w2.q_sig, w2.k_sig = q_sig, k_sig
+    res = GH.run_decode(w2)
+    assert res["status"] == 0
+    assert torch.equal(res["out"], out) and torch.equal(res["lse"], lse)
+    assert torch.equal(res["sel_cnt"], sel_cnt) and torch.equal(res["sel_idx"], sel_idx)
+
+
 @pytest.mark.parametrize("d,kv_dtype,m", [(128, torch.bfloat16, 100), (128, torch.bfloat16, 2500),
                                            (64, torch.float32, 37), (128, torch.bfloat16, 5000)])
 def test_topk_exact_and_recall(d, kv_dtype, m):

@@ -131,6 +131,45 @@ def test_other_entry_points_reject_bad_arguments(ha):
                                     None, 1024, 1 << 40, None, events) == ha.HA_ERR_INVALID_ARG
 
 
+def test_map_entry_points_reject_bad_arguments(ha):
+    """The MLP encoders and the mapped decode check the map before anything is
+    enqueued (every call here fails its checks, so no device is touched)."""
+    L = ha.lib()
+    s = _shape(ha)
+    sp = ctypes.byref(s)
+    good = ha.HAMlp(512, 512, 512, 512, 512, 512, 128, 0)
+    assert L.hash_attn_encode_queries_mlp(sp, 512, None, 512, None) == ha.HA_ERR_INVALID_ARG
+    for bad, status in ((ha.HAMlp(512, 512, 512, 512, 512, 512, 96, 0), ha.HA_ERR_UNSUPPORTED),
+                        (ha.HAMlp(512, 512, 520, 512, 512, 512, 128, 0), ha.HA_ERR_INVALID_ARG),  # W2 unaligned
+                        (ha.HAMlp(512, None, 512, 512, 512, 512, 128, 0), ha.HA_ERR_INVALID_ARG),
+                        (ha.HAMlp(512, 512, 512, 512, 512, 512, 128, 1), ha.HA_ERR_INVALID_ARG)):
+        assert L.hash_attn_encode_queries_mlp(sp, 512, ctypes.byref(bad), 512, None) == status
+        assert L.hash_attn_encode_keys_mlp(sp, 512, ctypes.byref(bad), 512, 512, None, None) == status
+    assert L.hash_attn_encode_keys_mlp(sp, 512, ctypes.byref(good), None, 512, None, None) == ha.HA_ERR_INVALID_ARG
+
+    def mapped(map_, opts=None, ws_bytes=1024, q_sig=512):
+        return L.hash_attn_decode_mapped(sp, 512, map_, None, q_sig, 512, 512, 512, 512, None, 8, 0, 0, opts,
+                                         512, 512, None, None, 1024, ws_bytes, None, None)
+    assert mapped(None) == ha.HA_ERR_INVALID_ARG
+    both = ha.HAMap()
+    both.W = 512
+    both.mlp = ctypes.pointer(good)
+    assert mapped(ctypes.byref(both)) == ha.HA_ERR_INVALID_ARG                     # both maps given
+    assert mapped(ctypes.byref(ha.HAMap())) == ha.HA_ERR_INVALID_ARG               # neither
+    wide = ha.select_opts(code_words=4)
+    assert mapped(ctypes.byref(_w512(ha)), ctypes.byref(wide)) == ha.HA_ERR_UNSUPPORTED
+    assert mapped(ctypes.byref(_w512(ha)), q_sig=None) == ha.HA_ERR_INVALID_ARG     # no q_sig
+    assert mapped(ctypes.byref(_w512(ha))) == ha.HA_ERR_WORKSPACE                  # 1 KB workspace
+    bad_mlp = ha.HAMlp(512, 512, 512, 512, 512, 512, 48, 0)
+    assert mapped(ctypes.byref(ha.mlp_map(bad_mlp))) == ha.HA_ERR_UNSUPPORTED
+
+
+def _w512(ha):
+    m = ha.HAMap()
+    m.W = 512
+    return m
+
+
 def test_status_strings(ha):
     for code in range(0, -7, -1):
         assert ha.status_string(code) not in ("", "unknown status")
