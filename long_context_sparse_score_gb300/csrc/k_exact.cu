@@ -269,6 +269,138 @@ __device__ __forceinline__ void emit_block(uint32_t take, uint32_t tie, int ib, 
     out_base += taken_total;
 }
 
+constexpr int kOffBins = 2 * kTopkThreads;   // 16-bit prefixes below the largest, one histogram pass
+constexpr int kVec = 4;                      // float4 loads per thread per batch of the candidate pass
+
+// Block-wide maximum (every thread gets it).
+__device__ __forceinline__ uint32_t block_max_u32(uint32_t v, uint32_t* s_red) {
+    v = __reduce_max_sync(0xffffffffu, v);
+    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    uint32_t m = 0u;
+#pragma unroll
+    for (int w = 0; w < kTopkThreads / 32; ++w) m = max(m, s_red[w]);
+    __syncthreads();
+    return m;
+}
+
+// The 16-bit prefix of the need-th largest of keys[0, cnt) (shared memory) from
+// one histogram of off = top16 - (key >> 16) over kOffBins bins, top16 being the
+// prefix of the largest key. Returns false (block-uniform) when that key lies
+// kOffBins or more prefixes below the largest; else its prefix p16, its rank
+// among the keys of its prefix (1-based) and their count.
+__device__ bool select16_onepass(const uint32_t* keys, int cnt, int need, uint32_t top16, unsigned* s_bins,
+                                 int* s_warp, int* s_res, uint32_t& p16, int& rank_in, int& bin_cnt) {
+    const int tid = threadIdx.x;
+    if (tid == 0) s_res[0] = -1;
+    for (int i = tid; i < kOffBins; i += kTopkThreads) s_bins[i] = 0u;
+    __syncthreads();
+    for (int i = tid; i < cnt; i += kTopkThreads) {
+        const uint32_t off = top16 - (keys[i] >> 16);
+        if (off < (uint32_t)kOffBins) atomicAdd(&s_bins[off], 1u);
+    }
+    __syncthreads();
+    const int c0 = (int)s_bins[2 * tid], c1 = (int)s_bins[2 * tid + 1];
+    int total;
+    const int before = block_excl_scan(c0 + c1, s_warp, &total);  // keys with larger prefixes
+    if (before < need && need <= before + c0 + c1) {
+        const bool first = need <= before + c0;
+        s_res[0] = first ? 2 * tid : 2 * tid + 1;
+        s_res[1] = need - (first ? before : before + c0);
+        s_res[2] = first ? c0 : c1;
+    }
+    __syncthreads();
+    const int bin = s_res[0];
+    p16 = top16 - (uint32_t)bin;
+    rank_in = s_res[1];
+    bin_cnt = s_res[2];
+    __syncthreads();
+    return bin >= 0;
+}
+
+// Exact need-th largest of keys[0, cnt) and the number of keys equal to it among
+// the largest `need`: one prefix histogram, then a rank by counting inside the
+// one 16-bit prefix that holds it (its keys gathered into s_list). False
+// (block-uniform) when the prefix lies out of the histogram's reach or holds more
+// than kTieCap keys.
+__device__ bool bin_select(const uint32_t* keys, int cnt, int need, uint32_t top16, unsigned* s_bins, int* s_warp,
+                           int* s_res, uint32_t* s_list, int* s_lcount, uint32_t* s_prefix, int* s_need,
+                           uint32_t& kth, int& need_out) {
+    const int tid = threadIdx.x;
+    uint32_t p16;
+    int rank_in, bc;
+    if (!select16_onepass(keys, cnt, need, top16, s_bins, s_warp, s_res, p16, rank_in, bc)) return false;
+    if (bc > kTieCap) return false;
+    if (tid == 0) *s_lcount = 0;
+    __syncthreads();
+    for (int i = tid; i < cnt; i += kTopkThreads) {
+        const uint32_t key = keys[i];
+        if ((key >> 16) == p16) s_list[atomicAdd(s_lcount, 1)] = key;
+    }
+    __syncthreads();
+    for (int j = tid; j < bc; j += kTopkThreads) {
+        const uint32_t x = s_list[j];
+        int gt = 0, eq = 0;
+        for (int l = 0; l < bc; ++l) {
+            const uint32_t y = s_list[l];
+            gt += (y > x) ? 1 : 0;
+            eq += (y == x) ? 1 : 0;
+        }
+        if (gt < rank_in && rank_in <= gt + eq) {  // every such thread holds the same key
+            *s_prefix = x;
+            *s_need = rank_in - gt;
+        }
+    }
+    __syncthreads();
+    kth = *s_prefix;
+    need_out = *s_need;
+    __syncthreads();
+    return true;
+}
+
+__device__ __forceinline__ float f4_comp(const float4& v, int c) {
+    return c == 0 ? v.x : (c == 1 ? v.y : (c == 2 ? v.z : v.w));
+}
+
+__device__ __forceinline__ void load_f4(const float4* z4, int n4, int base, float4 (&b)[kVec]) {
+#pragma unroll
+    for (int u = 0; u < kVec; ++u) {
+        const int i4 = base + u * kTopkThreads + threadIdx.x;
+        b[u] = (i4 < n4) ? __ldcg(z4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+// Append the tokens flagged in tk (bit e: value val(e), token idx(e)) to the
+// candidate arrays: one slot reservation per warp (inclusive scan of the lanes'
+// counts); cmax tracks the largest appended key.
+template <int NB, typename ValF, typename IdxF>
+__device__ __forceinline__ void append_candidates(uint32_t tk, ValF val, IdxF idx, int* s_ccount, uint32_t* s_ckey,
+                                                  int* s_cidx, uint32_t& cmax) {
+    const int lane = threadIdx.x & 31;
+    const int c = __popc(tk);
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    int wbase = 0;
+    if (lane == 31 && incl > 0) wbase = atomicAdd(s_ccount, incl);
+    int pos = __shfl_sync(0xffffffffu, wbase, 31) + incl - c;
+#pragma unroll
+    for (int e = 0; e < NB; ++e) {
+        if ((tk >> e) & 1u) {
+            const uint32_t key = fkey(val(e));
+            cmax = max(cmax, key);
+            if (pos < kCandCap) {
+                s_ckey[pos] = key;
+                s_cidx[pos] = idx(e);
+            }
+            ++pos;
+        }
+    }
+}
+
 // One CTA (kTopkThreads) per query head: the k = min(m, n) largest scores.
 //  fast path (n within the bitmap capacity): a 16-bit threshold T16 from a
 //   1/16 sample (8 consecutive tokens out of every 128, so the sample costs
@@ -292,7 +424,10 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_exact(const ExactParams p
     __shared__ int s_warp[kTopkThreads / 32];
     __shared__ uint32_t s_prefix;
     __shared__ int s_need;
-    __shared__ int s_ccount, s_tcount;
+    __shared__ int s_ccount, s_tcount, s_lcount;
+    __shared__ unsigned s_bins[kOffBins];
+    __shared__ uint32_t s_red[kTopkThreads / 32];
+    __shared__ int s_res[3];
     const int head = blockIdx.x;
     const int b = head / p.Hq;
     const int tid = threadIdx.x, lane = tid & 31;
@@ -308,12 +443,17 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_exact(const ExactParams p
         out_base = n;
     } else if (k > 0) {
         bool fast = p.bitmap_words > 0 && n <= 32 * p.bitmap_words;
-        uint32_t t16 = 0u;
         if (fast) {
-            // ---- sample: blocks of 8 tokens, one every 8 * step tokens
+            // ---- sample: blocks of 8 tokens, one every 8 * step tokens. The first
+            // batch of the candidate pass loads with it (it needs no threshold).
             const int step = (n + kSampleCap - 9) / (kSampleCap - 8);
             const int nb = (n + 8 * step - 1) / (8 * step);
             const int ns = min(nb * 8, (nb - 1) * 8 + (n - (nb - 1) * 8 * step));
+            const int n4 = ((p.n_cap & 3) == 0) ? (n >> 2) : 0;  // float4 part (16-byte aligned rows)
+            const float4* z4 = reinterpret_cast<const float4*>(z);
+            float4 cur[kVec];
+            load_f4(z4, n4, 0, cur);
+            uint32_t smax = 0u;
             {
                 constexpr int kPerThread = kSampleCap / kTopkThreads;  // all loads in flight at once
                 float v[kPerThread];
@@ -325,64 +465,81 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk_exact(const ExactParams p
 #pragma unroll
                 for (int u = 0; u < kPerThread; ++u) {
                     const int s = tid + u * kTopkThreads;
-                    if (s < ns) s_ckey[s] = fkey(v[u]);
+                    if (s < ns) {
+                        const uint32_t key = fkey(v[u]);
+                        s_ckey[s] = key;
+                        smax = max(smax, key);
+                    }
                 }
             }
+            smax = block_max_u32(smax, s_red);
             const float share = (float)k * (float)ns / (float)n;  // k's expected rank in the sample
             const int r = min(ns, (int)ceilf(1.25f * share + 4.f * sqrtf(share) + 8.f));
             fast = (float)r * ((float)n / (float)ns) <= 0.8f * (float)kCandCap;
-            __syncthreads();
             if (fast) {
-                int unused;
-                smem_radix_select(s_ckey, ns, r, 2, s_hist, &s_prefix, &s_need, t16, unused);
+                uint32_t t16;
+                {
+                    uint32_t p16;
+                    int rank_in, bc;
+                    if (select16_onepass(s_ckey, ns, r, smax >> 16, s_bins, s_warp, s_res, p16, rank_in, bc)) {
+                        t16 = p16 << 16;
+                    } else {
+                        int unused;
+                        smem_radix_select(s_ckey, ns, r, 2, s_hist, &s_prefix, &s_need, t16, unused);
+                    }
+                }
                 // ---- candidates: every token with key >= t16
                 if (tid == 0) {
                     s_ccount = 0;
                     s_tcount = 0;
                 }
                 __syncthreads();
-                constexpr int kInFlight = 16;  // loads per thread in flight (64 KB per SM at 2 CTAs)
-                for (int i0 = 0; i0 < n; i0 += kInFlight * kTopkThreads) {
+                uint32_t cmax = 0u;
+                for (int base = 0; base < n4; base += kVec * kTopkThreads) {  // the next batch loads meanwhile
+                    float4 nxt[kVec];
+                    if (base + kVec * kTopkThreads < n4) load_f4(z4, n4, base + kVec * kTopkThreads, nxt);
+                    uint32_t tk = 0u;  // bit 4u + c: element c of float4 base + u * kTopkThreads + tid
+#pragma unroll
+                    for (int u = 0; u < kVec; ++u) {
+                        const bool in = base + u * kTopkThreads + tid < n4;
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            if (in && fkey(f4_comp(cur[u], c)) >= t16) tk |= 1u << (4 * u + c);
+                    }
+                    append_candidates<4 * kVec>(
+                        tk, [&](int e) { return f4_comp(cur[e >> 2], e & 3); },
+                        [&](int e) { return 4 * (base + (e >> 2) * kTopkThreads + tid) + (e & 3); }, &s_ccount, s_ckey,
+                        s_cidx, cmax);
+#pragma unroll
+                    for (int u = 0; u < kVec; ++u) cur[u] = nxt[u];
+                }
+                constexpr int kInFlight = 16;  // the tokens past the float4 part (all when rows are unaligned)
+                for (int i0 = 4 * n4; i0 < n; i0 += kInFlight * kTopkThreads) {
                     float v[kInFlight];
 #pragma unroll
                     for (int u = 0; u < kInFlight; ++u) {
                         const int i = i0 + u * kTopkThreads + tid;
                         v[u] = (i < n) ? __ldcg(z + i) : 0.f;
                     }
-                    uint32_t tk = 0u;  // bit u: token i0 + u * kTopkThreads + tid is a candidate
+                    uint32_t tk = 0u;  // bit u: token i0 + u * kTopkThreads + tid
 #pragma unroll
                     for (int u = 0; u < kInFlight; ++u)
                         if (i0 + u * kTopkThreads + tid < n && fkey(v[u]) >= t16) tk |= 1u << u;
-                    // one slot reservation per warp: inclusive scan of the lanes' counts
-                    const int c = __popc(tk);
-                    int incl = c;
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                        if (lane >= o) incl += y;
-                    }
-                    int wbase = 0;
-                    if (lane == 31 && incl > 0) wbase = atomicAdd(&s_ccount, incl);
-                    int pos = __shfl_sync(0xffffffffu, wbase, 31) + incl - c;
-#pragma unroll
-                    for (int u = 0; u < kInFlight; ++u) {
-                        if ((tk >> u) & 1u) {
-                            if (pos < kCandCap) {
-                                s_ckey[pos] = fkey(v[u]);
-                                s_cidx[pos] = i0 + u * kTopkThreads + tid;
-                            }
-                            ++pos;
-                        }
-                    }
+                    append_candidates<kInFlight>(
+                        tk, [&](int e) { return v[e]; }, [&](int e) { return i0 + e * kTopkThreads + tid; },
+                        &s_ccount, s_ckey, s_cidx, cmax);
                 }
                 __syncthreads();
+                cmax = block_max_u32(cmax, s_red);
                 const int cc = s_ccount;
                 fast = cc >= k && cc <= kCandCap;
                 if (fast) {
                     // ---- exact k-th largest among the candidates, then the bitmap
                     uint32_t kth;
                     int need;
-                    smem_radix_select(s_ckey, cc, k, 4, s_hist, &s_prefix, &s_need, kth, need);
+                    if (!bin_select(s_ckey, cc, k, cmax >> 16, s_bins, s_warp, s_res,
+                                    reinterpret_cast<uint32_t*>(s_tlist), &s_lcount, &s_prefix, &s_need, kth, need))
+                        smem_radix_select(s_ckey, cc, k, 4, s_hist, &s_prefix, &s_need, kth, need);
                     const int nw = (n + 31) >> 5;
                     for (int w = tid; w < nw; w += kTopkThreads) s_sel[w] = 0u;
                     __syncthreads();
