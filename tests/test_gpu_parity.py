@@ -711,13 +711,17 @@ def test_exact_scores_within_float32_bound(Hq, Hkv, d, q_dtype, kv_dtype):
 
 
 @pytest.mark.parametrize("n_cap,pattern", [(131072, "sampled_high"), (131072, "sampled_low"),
-                                            (131072, "random"), (300000, "random")])
+                                            (131072, "random"), (300000, "random"), (131072, "outliers"),
+                                            (131072, "clustered")])
 def test_topk_exact_at_length(n_cap, pattern):
     """The top-m at full context length. The selection estimates its threshold
     from blocks of 8 tokens out of every 136 (n = 131072); keys whose scores are
     large exactly on those tokens (or exactly off them) make the estimate miss
     in both directions, and 300000 tokens exceed the bitmap, so the general
-    radix path is checked at length too. One-hot keys with two scales give exact
+    radix path is checked at length too. A few huge keys put the largest score
+    far above the rest (past the reach of the one-pass 16-bit histograms), and
+    clustered scores put thousands of tokens in the k-th key's 16-bit prefix,
+    so the shared-memory radix fallbacks run as well. One-hot keys give exact
     scores; random keys are checked against the oracle's float32 band."""
     H = GH.ha()
     B, Hq, Hkv, d, m = 1, 4, 1, 64, 4096
@@ -725,6 +729,28 @@ def test_topk_exact_at_length(n_cap, pattern):
     if pattern == "random":
         K = torch.randn((B, Hkv, n_cap, d), generator=g_).to(torch.bfloat16)
         q = torch.randn((B, Hq, d), generator=g_)
+    elif pattern == "outliers":
+        # exact one-hot scores, three of them 2^60 times larger than the rest
+        i = torch.arange(n_cap)
+        K = torch.zeros((B, Hkv, n_cap, d), dtype=torch.float64)
+        K[0, 0, i, (5 * i) % d] = torch.pow(2.0, (i % 3).double())
+        K[0, 0, [5, 70000, 131000]] *= 2.0 ** 60
+        K = K.to(torch.bfloat16)
+        q = torch.rand((B, Hq, d), generator=g_) + 0.5
+    elif pattern == "clustered":
+        # exact scores q[c] * 2^e with q[c] = 1 + c / 4096, tokens spread over four groups by a
+        # fixed permutation: 3000 spread over 16 prefixes, then 2500 in one prefix (where the
+        # 4096th lies: more than the 1024 keys the in-prefix rank takes), then 3000 over 6
+        # prefixes (where the sampled threshold lies: about 6500 candidates), then the rest
+        i = torch.arange(n_cap)
+        grp = (i * 7919) % n_cap
+        e = torch.where(grp < 3000, 4 + grp % 8, torch.where(grp < 5500, torch.full_like(i, 2),
+                        torch.where(grp < 8500, -1 - grp % 3, torch.full_like(i, -8))))
+        col = torch.where((grp >= 3000) & (grp < 5500), i % 32, i % 64)
+        K = torch.zeros((B, Hkv, n_cap, d), dtype=torch.float64)
+        K[0, 0, i, col] = torch.pow(2.0, e.double())
+        K = K.to(torch.bfloat16)
+        q = (1.0 + torch.arange(d, dtype=torch.float64) / 4096.0).float().expand(B, Hq, d).contiguous()
     else:
         i = torch.arange(n_cap)
         on = (i % 136) < 8
