@@ -504,8 +504,8 @@ def test_encode_mlp_queries_and_keys(d, q_dtype, hidden):
     assert int(flags.item()) & H.HA_DEVERR_INDEX
 
 
-@pytest.mark.parametrize("kind", ["sign", "mlp"])
-def test_decode_mapped_runs_the_map_ahead_of_score(kind):
+@pytest.mark.parametrize("kind,exclusive", [("sign", False), ("mlp", False), ("mlp", True)])
+def test_decode_mapped_runs_the_map_ahead_of_score(kind, exclusive):
     """One decode step from raw q: the map writes the appended tokens' key codes
     and the query codes (as the stand-alone encoders give them, and matching the
     oracle's unambiguous bits), and the rest of the step equals
@@ -536,8 +536,9 @@ def test_decode_mapped_runs_the_map_ahead_of_score(kind):
     cap = H.hash_attn_select_capacity(4000, w.m, w.n_sink, w.n_local)
     sel_idx = torch.full((B, Hq, cap), -7, dtype=torch.int32, device="cuda")
     sel_cnt = torch.full((B, Hq), -7, dtype=torch.int32, device="cuda")
+    opts = H.select_opts(None, True) if exclusive else None
     H.hash_attn_decode_mapped(shape, w.q, map_, pos, q_sig, k_sig, w.K, w.V, w.seq_lens, None, w.m, w.n_sink,
-                              w.n_local, None, out, lse, sel_idx, sel_cnt, workspace=ws)
+                              w.n_local, opts, out, lse, sel_idx, sel_cnt, workspace=ws)
     st, flags = H.hash_attn_device_status(ws)
     assert st == 0, flags
     q_ref = torch.zeros_like(q_sig)
@@ -565,7 +566,7 @@ def test_decode_mapped_runs_the_map_ahead_of_score(kind):
             assert (int(k_sig[b, g, p_].item()) & 0xFFFFFFFF ^ ref) & ~amb & 0xFFFFFFFF == 0, (b, g)
     w2 = copy.copy(w)
     w2.q_sig, w2.k_sig = q_sig, k_sig
-    res = GH.run_decode(w2)
+    res = GH.run_decode(w2, exclusive=exclusive)
     assert res["status"] == 0
     assert torch.equal(res["out"], out) and torch.equal(res["lse"], lse)
     assert torch.equal(res["sel_cnt"], sel_cnt) and torch.equal(res["sel_idx"], sel_idx)
@@ -682,6 +683,49 @@ def test_exact_scores_one_hot_keys_are_exact(Hq, Hkv, d, q_dtype, kv_dtype):
             assert int(cnt[b, h]) == min(m, n)
             ref = O.top_m_by_dot(q64[b, h].numpy(), K[b, h // G].numpy(), n, m)
             assert np.array_equal(idx[b, h, :min(m, n)], ref), (b, h)
+
+
+@pytest.mark.parametrize("n_cap,lens,shared", [(100, [100, 37], False), (8, [8, 5], False),
+                                              (700, [700, 640], True)])
+def test_exact_scores_small_and_shared_caches(n_cap, lens, shared):
+    """Caches shorter than one 128-row tile (the tile reads past n_cap as zeros
+    and nothing past n is written), and one cache shared by every batch entry
+    (batch stride 0): one-hot keys make the scores exact."""
+    H = GH.ha()
+    B, Hq, Hkv, d, m = 2, 8, 2, 128, 20
+    g_ = torch.Generator().manual_seed(41)
+    q = torch.randn((B, Hq, d), generator=g_)
+    i = torch.arange(n_cap)
+    Bk = 1 if shared else B
+    K = torch.zeros((Bk, Hkv, n_cap, d), dtype=torch.float64)
+    col = torch.empty((Bk, Hkv, n_cap), dtype=torch.int64)
+    for b in range(Bk):
+        for g in range(Hkv):
+            col[b, g] = (3 * i + 5 * g + b) % d
+            K[b, g, i, col[b, g]] = torch.pow(2.0, (i % 4).double() - 1.0)
+    Kd, qd = K.to(torch.bfloat16).cuda(), q.cuda()
+    seq = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    shape = H.make_shape(qd, Kd, torch.zeros_like(Kd))
+    assert (shape.k_sb == 0) == shared
+    ws = torch.full((H.hash_attn_topk_exact_workspace_size(shape),), 0x7F, dtype=torch.uint8, device="cuda")
+    cap = min(m, n_cap)
+    idx = torch.full((B, Hq, cap), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.full((B, Hq), -7, dtype=torch.int32, device="cuda")
+    H.hash_attn_topk_exact(shape, qd, Kd, seq, m, idx, cnt, workspace=ws)
+    st, flags = H.hash_attn_device_status(ws)
+    assert st == 0, flags
+    z = ws[256:256 + B * Hq * n_cap * 4].view(torch.float32).view(B, Hq, n_cap).cpu()
+    untouched = torch.full((1,), 0x7F7F7F7F, dtype=torch.int32).view(torch.float32)
+    G = Hq // Hkv
+    for b, n in enumerate(lens):
+        bk = 0 if shared else b
+        for h in range(Hq):
+            want = (q.double()[b, h, col[bk, h // G, :n]] * torch.pow(2.0, (i[:n] % 4).double() - 1.0)).float()
+            assert torch.equal(z[b, h, :n], want), (b, h)
+            assert torch.all(z[b, h, n:].view(torch.int32) == untouched.view(torch.int32)), (b, h)
+            ref = O.top_m_by_dot(q.double()[b, h].numpy(), K[bk, h // G].numpy(), n, m)
+            assert int(cnt[b, h]) == min(m, n)
+            assert np.array_equal(idx[b, h, :min(m, n)].cpu().numpy(), ref), (b, h)
 
 
 @pytest.mark.parametrize("Hq,Hkv,d,q_dtype,kv_dtype", EXACT_SHAPES)
