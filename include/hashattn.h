@@ -109,6 +109,34 @@ ha_status hash_attn_workspace_size(const ha_shape* shape, int32_t m_max, int32_t
 ha_status hash_attn_workspace_init(void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * Bytes of the device staging buffer hash_attn_decode_host needs for this shape
+ * (the step's q, q codes, sequence lengths, budgets, out and lse).
+ */
+ha_status hash_attn_host_staging_size(const ha_shape* shape, size_t* bytes);
+
+/*
+ * hash_attn_decode with the step's inputs and results in HOST memory (pinned
+ * memory makes the copies asynchronous): one cudaMemcpyAsync per input into
+ * `staging`, the path, then one per result back, all enqueued on `stream`; the
+ * results are in out_host / lse_host once the stream has reached them. The
+ * cache (k_sig, K, V) and the workspace stay on the device.
+ *   q_host        contiguous [batch, h_q, d] of shape->q_dtype (shape's q strides
+ *                 are ignored: the staged copy is contiguous)
+ *   q_sig_host    [batch, h_q] uint32 (may be NULL only for the dense path)
+ *   seq_lens_host [batch] int32; m_per_seq_host [batch] int32 or NULL
+ *   out_host      [batch, h_q, d] float32, lse_host [batch, h_q] float32
+ *   staging       device, >= hash_attn_host_staging_size bytes, 256-byte aligned
+ *   the rest as hash_attn_decode (no selected-index output).
+ * Errors: every check of hash_attn_decode, and the staging size, before the
+ * first copy is enqueued; HA_ERR_CUDA if a copy or launch fails.
+ */
+ha_status hash_attn_decode_host(const ha_shape* shape, const void* q_host, const uint32_t* q_sig_host,
+                                const int32_t* seq_lens_host, const int32_t* m_per_seq_host, const uint32_t* k_sig,
+                                const void* K, const void* V, int32_t m, int32_t n_sink, int32_t n_local,
+                                float* out_host, float* lse_host, void* staging, size_t staging_bytes,
+                                void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * Capacity of the per-head selected-index list for (n_cap, m, n_sink, n_local):
  * min(n_cap, m + n_sink + n_local) (HashAttention Sec. 4.4: the budget plus the
  * fixed positions bounds the number of reads). n_cap when m >= n_cap.

@@ -321,7 +321,7 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
                       const void* K, const void* V, const int32_t* seq_lens, const int32_t* m_per_seq,
                       int32_t m, int32_t n_sink, int32_t n_local, const ha_select_opts* opts, float* out,
                       float* lse, int32_t* sel_idx, int32_t* sel_cnt, void* ws, size_t ws_bytes, void* stream,
-                      void* const* events, const MapStep* map = nullptr) {
+                      void* const* events, const MapStep* map = nullptr, bool check_only = false) {
     HA_TRY(check_shape(s));
     HA_TRY(check_window(m, n_sink, n_local));
     HA_TRY(check_opts(opts));
@@ -337,6 +337,7 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
     const Layout lay = make_layout(*s, rows_cap, !dense, nbins_of(opts));
     HA_TRY(check_segments(lay));
     HA_TRY(check_ws(lay, ws, ws_bytes));
+    if (check_only) return HA_OK;
     const Views v = views(lay, ws);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int bhkv = s->batch * s->h_kv;
@@ -456,6 +457,37 @@ void set_mlp(EncodeParams* p, const ha_mlp* mlp) {
     p->W3 = mlp->W3;
     p->b3 = mlp->b3;
     p->hidden = mlp->hidden;
+}
+
+// Device staging of hash_attn_decode_host: q, q_sig, seq_lens, m_per_seq, out,
+// lse, each region 256-byte aligned.
+struct Staging {
+    size_t q = 0, q_sig = 0, seq = 0, mps = 0, out = 0, lse = 0, total = 0;
+    size_t q_bytes = 0, sig_bytes = 0, seq_bytes = 0, out_bytes = 0, lse_bytes = 0;
+};
+
+Staging staging_layout(const ha_shape* s) {
+    Staging L;
+    const size_t heads = (size_t)s->batch * s->h_q;
+    L.q_bytes = heads * s->d * (s->q_dtype == HA_F32 ? 4 : 2);
+    L.sig_bytes = heads * sizeof(uint32_t);
+    L.seq_bytes = (size_t)s->batch * sizeof(int32_t);
+    L.out_bytes = heads * s->d * sizeof(float);
+    L.lse_bytes = heads * sizeof(float);
+    size_t off = 0;
+    L.q = off;
+    off = align_up(off + L.q_bytes, 256);
+    L.q_sig = off;
+    off = align_up(off + L.sig_bytes, 256);
+    L.seq = off;
+    off = align_up(off + L.seq_bytes, 256);
+    L.mps = off;
+    off = align_up(off + L.seq_bytes, 256);
+    L.out = off;
+    off = align_up(off + L.out_bytes, 256);
+    L.lse = off;
+    L.total = align_up(off + L.lse_bytes, 256);
+    return L;
 }
 
 }  // namespace
@@ -771,6 +803,61 @@ ha_status hash_attn_encode_keys_mlp(const ha_shape* shape, const void* K, const 
     EncodeParams p = key_encode_params(shape, K, pos, k_sig, dev_flags);
     set_mlp(&p, mlp);
     HA_LAUNCH(launch_encode_mlp(p, static_cast<cudaStream_t>(stream)), "key MLP encode launch");
+    return HA_OK;
+}
+
+ha_status hash_attn_host_staging_size(const ha_shape* shape, size_t* bytes) {
+    HA_TRY(check_shape(shape));
+    if (bytes == nullptr) return fail(HA_ERR_INVALID_ARG, "bytes is NULL");
+    *bytes = staging_layout(shape).total;
+    return HA_OK;
+}
+
+ha_status hash_attn_decode_host(const ha_shape* shape, const void* q_host, const uint32_t* q_sig_host,
+                                const int32_t* seq_lens_host, const int32_t* m_per_seq_host, const uint32_t* k_sig,
+                                const void* K, const void* V, int32_t m, int32_t n_sink, int32_t n_local,
+                                float* out_host, float* lse_host, void* staging, size_t staging_bytes,
+                                void* workspace, size_t ws_bytes, void* stream) {
+    HA_TRY(check_shape(shape));
+    if (q_host == nullptr || seq_lens_host == nullptr || out_host == nullptr || lse_host == nullptr)
+        return fail(HA_ERR_INVALID_ARG, "q_host, seq_lens_host, out_host and lse_host must not be NULL");
+    const Staging L = staging_layout(shape);
+    if (staging == nullptr || (reinterpret_cast<uintptr_t>(staging) & 255u) != 0 || staging_bytes < L.total)
+        return fail(HA_ERR_WORKSPACE, "staging must be 256-byte aligned and hold %zu bytes", L.total);
+    ha_shape s = *shape;  // the staged q is contiguous
+    s.q_sh = shape->d;
+    s.q_sb = (int64_t)shape->h_q * shape->d;
+    char* sb = static_cast<char*>(staging);
+    void* q_d = sb + L.q;
+    uint32_t* sig_d = q_sig_host != nullptr ? reinterpret_cast<uint32_t*>(sb + L.q_sig) : nullptr;
+    int32_t* seq_d = reinterpret_cast<int32_t*>(sb + L.seq);
+    int32_t* mps_d = m_per_seq_host != nullptr ? reinterpret_cast<int32_t*>(sb + L.mps) : nullptr;
+    float* out_d = reinterpret_cast<float*>(sb + L.out);
+    float* lse_d = reinterpret_cast<float*>(sb + L.lse);
+    // every check of the decode runs before the first copy is enqueued
+    HA_TRY(decode_impl(&s, q_d, sig_d, k_sig, K, V, seq_d, mps_d, m, n_sink, n_local, nullptr, out_d, lse_d,
+                       nullptr, nullptr, workspace, ws_bytes, stream, nullptr, nullptr, true));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    struct Copy {
+        void* dst;
+        const void* src;
+        size_t bytes;
+        cudaMemcpyKind kind;
+    };
+    const Copy in[4] = {{q_d, q_host, L.q_bytes, cudaMemcpyHostToDevice},
+                        {sig_d, q_sig_host, L.sig_bytes, cudaMemcpyHostToDevice},
+                        {seq_d, seq_lens_host, L.seq_bytes, cudaMemcpyHostToDevice},
+                        {mps_d, m_per_seq_host, L.seq_bytes, cudaMemcpyHostToDevice}};
+    for (const Copy& c : in) {  // one asynchronous copy per input
+        if (c.dst == nullptr) continue;
+        const cudaError_t e = cudaMemcpyAsync(c.dst, c.src, c.bytes, c.kind, st);
+        if (e != cudaSuccess) return cuda_fail(e, "input copy to the device");
+    }
+    HA_TRY(decode_impl(&s, q_d, sig_d, k_sig, K, V, seq_d, mps_d, m, n_sink, n_local, nullptr, out_d, lse_d,
+                       nullptr, nullptr, workspace, ws_bytes, stream, nullptr));
+    cudaError_t e = cudaMemcpyAsync(out_host, out_d, L.out_bytes, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(lse_host, lse_d, L.lse_bytes, cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return cuda_fail(e, "result copy to the host");
     return HA_OK;
 }
 

@@ -37,7 +37,8 @@ HA_NOALLOC_SCRATCH_BYTES = 16 << 20
 # Entry points declared in include/hashattn.h (checked by the tests).
 EXPORTED = [
     "hash_attn_workspace_size", "hash_attn_workspace_init", "hash_attn_select_capacity",
-    "hash_attn_decode", "hash_attn_decode_ex", "hash_attn_decode_timed", "hash_attn_score", "hash_attn_select",
+    "hash_attn_decode", "hash_attn_decode_ex", "hash_attn_decode_timed", "hash_attn_decode_host",
+    "hash_attn_host_staging_size", "hash_attn_score", "hash_attn_select",
     "hash_attn_select_ex", "hash_attn_workspace_size_ex",
     "hash_attn_gather_att", "hash_attn_gather_att_noalloc", "hash_attn_merge", "hash_attn_merge_n",
     "hash_attn_encode_queries", "hash_attn_encode_keys", "hash_attn_encode_queries_mlp",
@@ -147,6 +148,9 @@ def lib() -> ctypes.CDLL:
     L.hash_attn_select_ex.argtypes = [SP, _P, _P, _P, _P, _I32, _I32, _I32, OP, _P, _P, _P, _SZ, _P]
     L.hash_attn_workspace_size_ex.argtypes = [SP, _I32, _I32, _I32, OP, ctypes.POINTER(_SZ)]
     L.hash_attn_decode_timed.argtypes = dec + [ctypes.POINTER(_P)]
+    L.hash_attn_host_staging_size.argtypes = [SP, ctypes.POINTER(_SZ)]
+    L.hash_attn_decode_host.argtypes = [SP, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _SZ, _P, _SZ,
+                                        _P]
     L.hash_attn_score.argtypes = [SP, _P, _P, _P, _P, _P, _P, _SZ, _P]
     L.hash_attn_select.argtypes = [SP, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _SZ, _P]
     L.hash_attn_gather_att.argtypes = [SP, _P, _P, _P, _P, _P, _I32, _P, _P, _P, _P, _SZ, _P]
@@ -263,6 +267,24 @@ def hash_attn_decode(shape, q, q_sig, k_sig, K, V, seq_lens, m_per_seq, m, n_sin
                                   _ptr(V), _ptr(seq_lens), _ptr(m_per_seq), m, n_sink, n_local,
                                   _ptr(out), _ptr(lse), _ptr(sel_idx), _ptr(sel_cnt), ws, nb,
                                   _stream(stream)))
+
+
+def hash_attn_host_staging_size(shape) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().hash_attn_host_staging_size(ctypes.byref(shape), ctypes.byref(out)))
+    return out.value
+
+
+def hash_attn_decode_host(shape, q_host, q_sig_host, seq_lens_host, m_per_seq_host, k_sig, K, V, m, n_sink, n_local,
+                          out_host, lse_host, *, staging, workspace, stream=None) -> None:
+    """hash_attn_decode with q / q_sig / seq_lens / m_per_seq and out / lse in host
+    memory (pinned tensors or raw addresses), staged through the device buffer
+    ``staging`` (hash_attn_host_staging_size bytes)."""
+    ws, nb = _ws(workspace)
+    sp, sn = _ws(staging)
+    _check(lib().hash_attn_decode_host(ctypes.byref(shape), _ptr(q_host), _ptr(q_sig_host), _ptr(seq_lens_host),
+                                       _ptr(m_per_seq_host), _ptr(k_sig), _ptr(K), _ptr(V), m, n_sink, n_local,
+                                       _ptr(out_host), _ptr(lse_host), sp, sn, ws, nb, _stream(stream)))
 
 
 def hash_attn_workspace_size_ex(shape, m_max: int, n_sink: int, n_local: int, opts) -> int:

@@ -458,6 +458,36 @@ def test_encode_queries_and_keys(d, q_dtype):
     assert int(flags.item()) & H.HA_DEVERR_INDEX
 
 
+@pytest.mark.parametrize("mode", ["sparse", "budgets", "dense"])
+def test_decode_host_buffers_equal_device_decode(mode):
+    """hash_attn_decode_host (inputs and results in pinned host memory) gives the
+    outputs of hash_attn_decode on device copies of the same inputs, bit for bit,
+    for the sparse path, per-sequence budgets and the dense path (no codes)."""
+    H = GH.ha()
+    w = W().make_gqa(47, B=3, Hq=8, Hkv=2, d=128, n_cap=3000, seq_lens=[3000, 1999, 2500], m=200, n_sink=16,
+                     n_local=16, device="cuda", m_per_seq=[200, 150, 64] if mode == "budgets" else None)
+    m = 4000 if mode == "dense" else w.m
+    res = GH.run_decode(w, m=m, sel=False, dense=(mode == "dense"))
+    assert res["status"] == 0
+    q_strided = torch.empty((3, 8, 256), dtype=w.q.dtype, device="cuda")[:, :, :128]
+    q_strided.copy_(w.q)                         # the host call ignores the shape's q strides
+    shape = H.make_shape(q_strided, w.K, w.V, w.k_sig)
+    ws = GH.workspace(shape, m, w.n_sink, w.n_local)
+    staging = torch.empty(H.hash_attn_host_staging_size(shape), dtype=torch.uint8, device="cuda")
+    pin = lambda t: t.cpu().contiguous().pin_memory()
+    q_h, sig_h, sl_h = pin(w.q), pin(w.q_sig), pin(w.seq_lens)
+    mps_h = pin(w.m_per_seq) if w.m_per_seq is not None else None
+    out_h = torch.full((3, 8, 128), float("nan")).pin_memory()
+    lse_h = torch.full((3, 8), float("nan")).pin_memory()
+    H.hash_attn_decode_host(shape, q_h, None if mode == "dense" else sig_h, sl_h, mps_h,
+                            None if mode == "dense" else w.k_sig, w.K, w.V, m, w.n_sink, w.n_local, out_h, lse_h,
+                            staging=staging, workspace=ws)
+    torch.cuda.current_stream().synchronize()
+    st, flags = H.hash_attn_device_status(ws)
+    assert st == 0, flags
+    assert torch.equal(out_h, res["out"].cpu()) and torch.equal(lse_h, res["lse"].cpu())
+
+
 @pytest.mark.parametrize("d,q_dtype,hidden", [(128, torch.float32, 128), (64, torch.bfloat16, 64),
                                               (128, torch.bfloat16, 32)])
 def test_encode_mlp_queries_and_keys(d, q_dtype, hidden):

@@ -164,6 +164,27 @@ def test_map_entry_points_reject_bad_arguments(ha):
     assert mapped(ctypes.byref(ha.mlp_map(bad_mlp))) == ha.HA_ERR_UNSUPPORTED
 
 
+def test_host_buffer_decode_checks_before_any_copy(ha):
+    """hash_attn_decode_host runs the staging check and every check of the
+    decode before it enqueues its first copy (no device is touched here)."""
+    L = ha.lib()
+    s = _shape(ha)
+    sp = ctypes.byref(s)
+    need = ctypes.c_size_t(0)
+    assert L.hash_attn_host_staging_size(sp, ctypes.byref(need)) == ha.HA_OK and need.value > 0
+
+    def call(q=512, seq=512, out=512, staging=1024, st_bytes=None, ws_bytes=1024, m=8):
+        return L.hash_attn_decode_host(sp, q, 512, seq, None, 512, 512, 512, m, 0, 0, out, 512, staging,
+                                       need.value if st_bytes is None else st_bytes, 1024, ws_bytes, None)
+    assert call(q=None) == ha.HA_ERR_INVALID_ARG
+    assert call(seq=None) == ha.HA_ERR_INVALID_ARG
+    assert call(out=None) == ha.HA_ERR_INVALID_ARG
+    assert call(staging=1024 + 16) == ha.HA_ERR_WORKSPACE              # unaligned staging
+    assert call(st_bytes=need.value - 1) == ha.HA_ERR_WORKSPACE        # staging too small
+    assert call() == ha.HA_ERR_WORKSPACE                                # the decode's own workspace check
+    assert call(m=-1) == ha.HA_ERR_INVALID_ARG
+
+
 def _w512(ha):
     m = ha.HAMap()
     m.W = 512
