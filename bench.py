@@ -688,7 +688,7 @@ def run_ours(args, world, rank, local):
                  "selection_variants": measure_variants(w, shape, ws, dev),
                  "mapped_decode": measure_mapped(w, shape, dev)},
     }
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and world == 1:  # the CPU baseline: rank 0 of a one-GPU run only
         cpu_s, cpu_heads, res, cores = run_cpu_oracle(w, args.cpu_heads)
         o = out.cpu().numpy()
         lz = lse.cpu().numpy()
