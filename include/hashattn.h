@@ -424,6 +424,15 @@ ha_status hash_attn_topk_exact(const ha_shape* shape, const void* q, const void*
                                size_t ws_bytes, void* stream);
 
 /*
+ * hash_attn_topk_exact with three CUDA events (cudaEvent_t as void*, all
+ * non-NULL, created by the caller) recorded on `stream` before the scores,
+ * between the scores and the top-m, and after the top-m.
+ */
+ha_status hash_attn_topk_exact_timed(const ha_shape* shape, const void* q, const void* K, const int32_t* seq_lens,
+                                     int32_t m, int32_t* idx, int32_t idx_cap, int32_t* cnt, void* workspace,
+                                     size_t ws_bytes, void* stream, void* const* events);
+
+/*
  * Recall of one selection against a reference, per head:
  * recall[h] = |sel_h & ref_h| / |ref_h| (1 for an empty reference), with sel_h =
  * sel_idx[h, 0..sel_cnt[h]) and ref_h = ref_idx[h, 0..ref_cnt[h]) ascending

@@ -255,7 +255,9 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t st);
 cudaError_t launch_merge_n(const MergeNParams& p, cudaStream_t st);
 cudaError_t launch_encode(const EncodeParams& p, cudaStream_t st);
 cudaError_t launch_encode_mlp(const EncodeParams& p, cudaStream_t st);
-cudaError_t launch_topk_exact(const ExactParams& p, int d, int kv_bf16, cudaStream_t st);
+// The exact comparator: every score (tensor cores or CUDA cores), then the top-m.
+cudaError_t launch_exact_scores(const ExactParams& p, int d, int kv_bf16, cudaStream_t st);
+cudaError_t launch_exact_topm(const ExactParams& p, cudaStream_t st);
 // Tensor-core scores (bf16 K, 3 G <= 32); *used = false leaves the scores to
 // the CUDA-core kernel (a layout TMA cannot describe).
 cudaError_t launch_scores_tc(const ExactParams& p, int d, cudaStream_t st, bool* used);

@@ -903,6 +903,13 @@ ha_status hash_attn_topk_exact_workspace_size(const ha_shape* shape, size_t* byt
 ha_status hash_attn_topk_exact(const ha_shape* shape, const void* q, const void* K, const int32_t* seq_lens,
                                int32_t m, int32_t* idx, int32_t idx_cap, int32_t* cnt, void* workspace,
                                size_t ws_bytes, void* stream) {
+    return hash_attn_topk_exact_timed(shape, q, K, seq_lens, m, idx, idx_cap, cnt, workspace, ws_bytes, stream,
+                                      nullptr);
+}
+
+ha_status hash_attn_topk_exact_timed(const ha_shape* shape, const void* q, const void* K, const int32_t* seq_lens,
+                                     int32_t m, int32_t* idx, int32_t idx_cap, int32_t* cnt, void* workspace,
+                                     size_t ws_bytes, void* stream, void* const* events) {
     HA_TRY(check_shape(shape));
     if (q == nullptr || seq_lens == nullptr || idx == nullptr || cnt == nullptr)
         return fail(HA_ERR_INVALID_ARG, "q, seq_lens, idx and cnt must not be NULL");
@@ -939,10 +946,17 @@ ha_status hash_attn_topk_exact(const ha_shape* shape, const void* q, const void*
     p.idx_cap = idx_cap;
     p.cnt = cnt;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (events != nullptr)
+        for (int i = 0; i < 3; ++i)
+            if (events[i] == nullptr) return fail(HA_ERR_INVALID_ARG, "events[%d] is NULL", i);
     // every call starts with a clean error word (the rest of the workspace is scratch)
     const cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(uint32_t), st);
     if (e != cudaSuccess) return cuda_fail(e, "clearing the error word");
-    HA_LAUNCH(launch_topk_exact(p, shape->d, shape->kv_dtype == HA_BF16, st), "exact top-k launch");
+    HA_TRY(record(events, 0, st));
+    HA_LAUNCH(launch_exact_scores(p, shape->d, shape->kv_dtype == HA_BF16, st), "exact score launch");
+    HA_TRY(record(events, 1, st));
+    HA_LAUNCH(launch_exact_topm(p, st), "exact top-m launch");
+    HA_TRY(record(events, 2, st));
     return HA_OK;
 }
 

@@ -706,18 +706,20 @@ cudaError_t launch_scores_t(const ExactParams& p, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_topk_exact(const ExactParams& p, int d, int kv_bf16, cudaStream_t st) {
+cudaError_t launch_exact_scores(const ExactParams& p, int d, int kv_bf16, cudaStream_t st) {
     bool tc = false;
     cudaError_t e = kv_bf16 ? launch_scores_tc(p, d, st, &tc) : cudaSuccess;
-    if (e != cudaSuccess) return e;
-    if (!tc) {
-        e = cudaErrorInvalidValue;
-        if (d == 128 && kv_bf16) e = launch_scores_t<128, __nv_bfloat16>(p, st);
-        if (d == 64 && kv_bf16) e = launch_scores_t<64, __nv_bfloat16>(p, st);
-        if (d == 128 && !kv_bf16) e = launch_scores_t<128, float>(p, st);
-        if (d == 64 && !kv_bf16) e = launch_scores_t<64, float>(p, st);
-        if (e != cudaSuccess) return e;
-    }
+    if (e != cudaSuccess || tc) return e;
+    e = cudaErrorInvalidValue;
+    if (d == 128 && kv_bf16) e = launch_scores_t<128, __nv_bfloat16>(p, st);
+    if (d == 64 && kv_bf16) e = launch_scores_t<64, __nv_bfloat16>(p, st);
+    if (d == 128 && !kv_bf16) e = launch_scores_t<128, float>(p, st);
+    if (d == 64 && !kv_bf16) e = launch_scores_t<64, float>(p, st);
+    return e;
+}
+
+cudaError_t launch_exact_topm(const ExactParams& p, cudaStream_t st) {
+    cudaError_t e;
     ExactParams q = p;
     q.bitmap_words = p.n_cap <= kBitmapTokens ? (p.n_cap + 31) / 32 : 0;
     const size_t smem = (size_t)(2 * kCandCap + q.bitmap_words + kTieCap) * sizeof(uint32_t);

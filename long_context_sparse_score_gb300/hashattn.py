@@ -43,7 +43,7 @@ EXPORTED = [
     "hash_attn_gather_att", "hash_attn_gather_att_noalloc", "hash_attn_merge", "hash_attn_merge_n",
     "hash_attn_encode_queries", "hash_attn_encode_keys", "hash_attn_encode_queries_mlp",
     "hash_attn_encode_keys_mlp", "hash_attn_decode_mapped", "hash_attn_topk_exact_workspace_size",
-    "hash_attn_topk_exact", "hash_attn_recall",
+    "hash_attn_topk_exact", "hash_attn_topk_exact_timed", "hash_attn_recall",
     "hash_attn_device_status",
     "hash_attn_status_string", "hash_attn_last_error",
 ]
@@ -165,6 +165,7 @@ def lib() -> ctypes.CDLL:
                                           _I32, OP, _P, _P, _P, _P, _P, _SZ, _P, _P]
     L.hash_attn_topk_exact_workspace_size.argtypes = [SP, ctypes.POINTER(_SZ)]
     L.hash_attn_topk_exact.argtypes = [SP, _P, _P, _P, _I32, _P, _I32, _P, _P, _SZ, _P]
+    L.hash_attn_topk_exact_timed.argtypes = [SP, _P, _P, _P, _I32, _P, _I32, _P, _P, _SZ, _P, ctypes.POINTER(_P)]
     L.hash_attn_recall.argtypes = [_P, _P, _I32, _P, _P, _I32, _I32, _P, _P]
     L.hash_attn_device_status.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_uint32)]
     L.hash_attn_status_string.argtypes = [_I32]
@@ -418,6 +419,15 @@ def hash_attn_topk_exact(shape, q, K, seq_lens, m, idx, cnt, *, workspace, strea
     ws, nb = _ws(workspace)
     _check(lib().hash_attn_topk_exact(ctypes.byref(shape), _ptr(q), _ptr(K), _ptr(seq_lens), m, _ptr(idx),
                                       idx.shape[-1], _ptr(cnt), ws, nb, _stream(stream)))
+
+
+def hash_attn_topk_exact_timed(shape, q, K, seq_lens, m, idx, cnt, events, *, workspace, stream=None) -> None:
+    """hash_attn_topk_exact with ``events``: three torch.cuda.Event(enable_timing=True),
+    recorded before the scores, between the scores and the top-m, and after."""
+    ws, nb = _ws(workspace)
+    arr = (_P * 3)(*[e.cuda_event for e in events])
+    _check(lib().hash_attn_topk_exact_timed(ctypes.byref(shape), _ptr(q), _ptr(K), _ptr(seq_lens), m, _ptr(idx),
+                                            idx.shape[-1], _ptr(cnt), ws, nb, _stream(stream), arr))
 
 
 def hash_attn_recall(sel_idx, sel_cnt, ref_idx, ref_cnt, recall, stream=None) -> None:

@@ -643,6 +643,30 @@ def test_topk_exact_and_recall(d, kv_dtype, m):
             assert abs(float(rec[b * 8 + h]) - want) < 1e-6
 
 
+def test_topk_exact_timed_equals_untimed():
+    """The events variant records its three events and returns the same selection."""
+    H = GH.ha()
+    w = W().make_gqa(24, B=2, Hq=8, Hkv=2, d=128, n_cap=5000, seq_lens=[5000, 4100], m=256, n_sink=0,
+                     n_local=0, device="cuda")
+    shape = H.make_shape(w.q, w.K, w.V, w.k_sig)
+    ws = torch.empty(H.hash_attn_topk_exact_workspace_size(shape), dtype=torch.uint8, device="cuda")
+    outs = []
+    for timed in (False, True):
+        idx = torch.full((2, 8, 256), -7, dtype=torch.int32, device="cuda")
+        cnt = torch.full((2, 8), -7, dtype=torch.int32, device="cuda")
+        if timed:
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            for e in ev:
+                e.record()
+            H.hash_attn_topk_exact_timed(shape, w.q, w.K, w.seq_lens, 256, idx, cnt, ev, workspace=ws)
+        else:
+            H.hash_attn_topk_exact(shape, w.q, w.K, w.seq_lens, 256, idx, cnt, workspace=ws)
+        torch.cuda.synchronize()
+        outs.append((idx.cpu(), cnt.cpu()))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    assert ev[0].elapsed_time(ev[1]) > 0 and ev[1].elapsed_time(ev[2]) > 0
+
+
 def test_topk_exact_ties_take_smaller_indices():
     H = GH.ha()
     w = W().make_gqa(22, B=1, Hq=4, Hkv=1, d=128, n_cap=2048, seq_lens=[2048], m=64, n_sink=0, n_local=0,

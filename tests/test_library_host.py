@@ -126,6 +126,9 @@ def test_other_entry_points_reject_bad_arguments(ha):
     assert L.hash_attn_merge_n(None, 0, None, 0, 2, None, None, 0, 128, None) == ha.HA_OK  # nothing to do
     assert L.hash_attn_device_status(None, None, None) == ha.HA_ERR_WORKSPACE
     assert L.hash_attn_workspace_init(None, 16, None) == ha.HA_ERR_WORKSPACE
+    ev3 = (ctypes.c_void_p * 3)(512, None, 512)
+    assert L.hash_attn_topk_exact_timed(sp, 512, 512, 512, 8, 512, 8, 512, 1 << 20, 1 << 40, None,
+                                        ev3) == ha.HA_ERR_INVALID_ARG          # events[1] is NULL
     events = (ctypes.c_void_p * 4)(None, None, None, None)
     assert L.hash_attn_decode_timed(sp, 512, 512, 512, 512, 512, 512, None, 8, 0, 0, 512, 512, None,
                                     None, 1024, 1 << 40, None, events) == ha.HA_ERR_INVALID_ARG
