@@ -412,7 +412,7 @@ ha_status hash_attn_decode_mapped(const ha_shape* shape, const void* q, const ha
  *            error word read by hash_attn_device_status; the scores z of all
  *            heads follow at byte offset 256 as float32 [batch, h_q, n_cap]
  *            (entries i < seq_lens[b] written), then scratch query tiles)
- * bf16 keys with h_q / h_kv <= 10 are scored on the tensor cores (an fp32 q as
+ * bf16 keys with h_q / h_kv <= 21 are scored on the tensor cores (an fp32 q as
  * three bf16 parts that sum to it exactly, float32 accumulation); other shapes on
  * the CUDA cores; both give float32 scores.
  * Errors: HA_ERR_INVALID_ARG / HA_ERR_UNSUPPORTED / HA_ERR_WORKSPACE before

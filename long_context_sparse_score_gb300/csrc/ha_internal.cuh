@@ -209,7 +209,7 @@ struct ExactParams {
     int idx_cap;
     int32_t* cnt;              // [B * Hq]
     uint32_t* err;
-    uint16_t* qt;              // [B * Hkv][32][d] bf16 query tiles of the tensor-core kernel (workspace)
+    uint16_t* qt;              // [B * Hkv][64][d] bf16 query tiles of the tensor-core kernel (workspace)
     int bitmap_words;          // top-m: words of each token bitmap in shared memory (0: no fast path)
 };
 
@@ -258,7 +258,7 @@ cudaError_t launch_encode_mlp(const EncodeParams& p, cudaStream_t st);
 // The exact comparator: every score (tensor cores or CUDA cores), then the top-m.
 cudaError_t launch_exact_scores(const ExactParams& p, int d, int kv_bf16, cudaStream_t st);
 cudaError_t launch_exact_topm(const ExactParams& p, cudaStream_t st);
-// Tensor-core scores (bf16 K, 3 G <= 32); *used = false leaves the scores to
+// Tensor-core scores (bf16 K, 3 G <= 64); *used = false leaves the scores to
 // the CUDA-core kernel (a layout TMA cannot describe).
 cudaError_t launch_scores_tc(const ExactParams& p, int d, cudaStream_t st, bool* used);
 cudaError_t launch_recall(const RecallParams& p, cudaStream_t st);

@@ -896,7 +896,7 @@ ha_status hash_attn_topk_exact_workspace_size(const ha_shape* shape, size_t* byt
     HA_TRY(check_shape(shape));
     if (bytes == nullptr) return fail(HA_ERR_INVALID_ARG, "bytes is NULL");
     *bytes = 256 + align_up((size_t)shape->batch * shape->h_q * (size_t)shape->n_cap * sizeof(float), 1024) +
-             (size_t)shape->batch * shape->h_kv * 32 * (size_t)shape->d * sizeof(uint16_t);
+             (size_t)shape->batch * shape->h_kv * 64 * (size_t)shape->d * sizeof(uint16_t);
     return HA_OK;
 }
 

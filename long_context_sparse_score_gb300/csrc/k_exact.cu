@@ -4,7 +4,7 @@
 // hashed selection against the oracle top-k by attention score. Here:
 //   k_dot_scores   z[head, i] = <q[b, h], k_i> (float32) for every cached token
 //                  i < n on the CUDA cores, for the keys the tensor-core kernel
-//                  does not take (float32 keys, more than 10 query heads per
+//                  does not take (float32 keys, more than 21 query heads per
 //                  KV head); one read of a KV head's rows serves its G query
 //                  heads (4 lanes share a row, 16-byte loads, q in shared
 //                  memory).

@@ -45,11 +45,11 @@ struct TcCfg {
     static constexpr int kStage = kA + kB;       // a multiple of 1024 (swizzle atoms stay aligned)
     static constexpr int kStages = (kTcSmemBudget / kStage) < 8 ? (kTcSmemBudget / kStage) : 8;
     static constexpr int kSpans = D / 64;        // 128-byte swizzle spans of a row
-    static constexpr uint32_t kTmemCols = (2 * NCOL <= 32) ? 32u : 64u;
+    static constexpr uint32_t kTmemCols = (2 * NCOL <= 32) ? 32u : ((2 * NCOL <= 64) ? 64u : 128u);
     static constexpr int kBarBytes = 8 * (2 * kStages + 5) + 16;
     static constexpr size_t kSmem = 1024 + (size_t)kStages * kStage + kBarBytes;
     static_assert(kStage % 1024 == 0, "stages must keep 1024-byte alignment");
-    static_assert(NCOL % 16 == 0 && NCOL <= 32, "N of the MMA");
+    static_assert(NCOL % 16 == 0 && NCOL <= 64, "N of the MMA");
 };
 
 // kind::f16 instruction descriptor: float32 accumulator, bf16 A and B, both
@@ -391,10 +391,20 @@ cudaError_t launch_tc_t(const ExactParams& p, cudaStream_t st, bool* used) {
 
 cudaError_t launch_scores_tc(const ExactParams& p, int d, cudaStream_t st, bool* used) {
     *used = false;
-    if (p.qt == nullptr || 3 * p.G > 32) return cudaSuccess;
-    const bool n16 = 3 * p.G <= 16;
-    if (d == 128) return n16 ? launch_tc_t<128, 16>(p, st, used) : launch_tc_t<128, 32>(p, st, used);
-    if (d == 64) return n16 ? launch_tc_t<64, 16>(p, st, used) : launch_tc_t<64, 32>(p, st, used);
+    if (p.qt == nullptr || 3 * p.G > 64) return cudaSuccess;
+    const int ncol = (3 * p.G + 15) / 16 * 16;  // three parts per query head, in units of 16 columns
+    if (d == 128) {
+        if (ncol == 16) return launch_tc_t<128, 16>(p, st, used);
+        if (ncol == 32) return launch_tc_t<128, 32>(p, st, used);
+        if (ncol == 48) return launch_tc_t<128, 48>(p, st, used);
+        return launch_tc_t<128, 64>(p, st, used);
+    }
+    if (d == 64) {
+        if (ncol == 16) return launch_tc_t<64, 16>(p, st, used);
+        if (ncol == 32) return launch_tc_t<64, 32>(p, st, used);
+        if (ncol == 48) return launch_tc_t<64, 48>(p, st, used);
+        return launch_tc_t<64, 64>(p, st, used);
+    }
     return cudaSuccess;
 }
 

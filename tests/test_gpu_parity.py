@@ -696,12 +696,13 @@ def _exact_call(H, shape, q, K, seq_lens, m, B, Hq, n_cap):
     return z.cpu(), idx.cpu().numpy(), cnt.cpu().numpy()
 
 
-# (Hq, Hkv, d, q dtype, kv dtype): groups of 1, 4, 8 and 10 heads take the
-# tensor-core kernel for bf16 keys (3 G <= 32 columns), 16 heads and float32
-# keys the CUDA-core one
+# (Hq, Hkv, d, q dtype, kv dtype): groups of 1, 4, 8, 10, 16 and 21 heads take
+# the tensor-core kernel for bf16 keys (3 G <= 64 columns: N = 16, 32, 48, 64),
+# 24 heads and float32 keys the CUDA-core one
 EXACT_SHAPES = [(8, 2, 128, torch.float32, torch.bfloat16), (8, 8, 64, torch.float32, torch.bfloat16),
                 (16, 2, 128, torch.float32, torch.bfloat16), (20, 2, 64, torch.bfloat16, torch.bfloat16),
-                (32, 2, 128, torch.float32, torch.bfloat16), (8, 2, 128, torch.float32, torch.float32)]
+                (32, 2, 128, torch.float32, torch.bfloat16), (21, 1, 64, torch.float32, torch.bfloat16),
+                (24, 1, 128, torch.float32, torch.bfloat16), (8, 2, 128, torch.float32, torch.float32)]
 
 
 @pytest.mark.parametrize("Hq,Hkv,d,q_dtype,kv_dtype", EXACT_SHAPES)
