@@ -427,6 +427,8 @@ ha_status hash_attn_topk_exact(const ha_shape* shape, const void* q, const void*
  * hash_attn_topk_exact with three CUDA events (cudaEvent_t as void*, all
  * non-NULL, created by the caller) recorded on `stream` before the scores,
  * between the scores and the top-m, and after the top-m.
+ * Errors: those of hash_attn_topk_exact, and HA_ERR_INVALID_ARG for a NULL
+ * event, all before anything is enqueued.
  */
 ha_status hash_attn_topk_exact_timed(const ha_shape* shape, const void* q, const void* K, const int32_t* seq_lens,
                                      int32_t m, int32_t* idx, int32_t idx_cap, int32_t* cnt, void* workspace,
