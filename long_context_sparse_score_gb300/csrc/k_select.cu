@@ -375,11 +375,32 @@ __global__ void __launch_bounds__(kScoreThreads, 4) k_select(const SelectParams 
     __shared__ __align__(16) uint32_t s_codes[kWarps][32][TPT + 4];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int c = blockIdx.x % p.nchunks;
-    const int bg = blockIdx.x / p.nchunks;
+    // Chunks holding the windows take the out-of-line path and run several times
+    // longer, so they come first in the grid instead of trailing it: CTA i < W
+    // takes the first chunk of pair i (W = B * Hkv pairs), W <= i < 2W the last
+    // chunk pair i - W uses, and the rest the remaining chunks of each pair.
+    const int W = p.B * p.Hkv;
+    const int i = blockIdx.x;
+    int bg, c;
+    if (i < W) {
+        bg = i;
+    } else if (p.nchunks >= 2 && i < 2 * W) {
+        bg = i - W;
+    } else {
+        bg = (i - 2 * W) / (p.nchunks - 2);
+    }
     const int b = bg / p.Hkv, g = bg % p.Hkv;
     const int n = checked_len(p.seq_lens, b, p.n_cap, p.err, false);
     const int nch = (n + C - 1) / C;
+    const int last = nch - 1;                  // the chunk holding the local window
+    if (i < W) {
+        c = 0;
+    } else if (p.nchunks >= 2 && i < 2 * W) {
+        c = last >= 1 ? last : p.nchunks - 1;  // a one-chunk sequence: an idle CTA
+    } else {
+        c = 1 + (i - 2 * W) % (p.nchunks - 2);
+        if (last >= 1 && c >= last) ++c;      // skip the chunk the second group took
+    }
     if (c >= nch) return;
 
     const int wlo = min(p.n_sink, n);          // sink window [0, wlo)
