@@ -50,3 +50,27 @@ def test_single_process_throughput():
     sys.path.insert(0, ROOT)
     import bench
     assert bench.throughput(1, 512, 2000, 640.0) == 512 * 2000 / 0.64
+
+
+def test_cpu_oracle_pool_matches_direct_calls():
+    """The CPU baseline's process pool (spawn workers reading each (sequence, KV
+    head) pair from shared memory) returns what the oracle returns when called
+    directly, and reports the worker count as its cores."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+
+    import bench
+    from long_context_sparse_score_gb300 import workloads as W
+    from oracle import hashattn_oracle as O
+    w = W.make_gqa(5, B=2, Hq=8, Hkv=2, d=64, n_cap=2048, seq_lens=[2048, 1500], m=100, n_sink=8,
+                   n_local=16, device="cpu")
+    secs, done, res, cores = bench.run_cpu_oracle(w, 12)
+    assert done == 12 and len(res) == 12 and secs > 0
+    assert cores == len(os.sched_getaffinity(0))
+    q = w.q.float().numpy().astype(np.float64)
+    for (b, h), (idx, _, out, lse) in res.items():
+        g = h // 4
+        want = O.decode_head(q[b, h], int(w.q_sig[b, h]),
+                             w.k_sig[b, g].numpy().astype(np.int64), w.K[b, g].float().numpy(),
+                             w.V[b, g].float().numpy(), int(w.seq_lens[b]), w.m, w.n_sink, w.n_local)
+        assert np.array_equal(idx, want[0]) and np.array_equal(out, want[2]) and lse == want[3], (b, h)
