@@ -287,11 +287,14 @@ ha_status hash_attn_gather_att(const ha_shape* shape, const void* q, const void*
  * Shapes whose scratch would exceed HA_NOALLOC_SCRATCH_BYTES are rejected with
  * HA_ERR_WORKSPACE before anything is enqueued (the scratch holds
  * 256 + 4 * batch * h_q plus 4 * batch * h_q * splits * (d + 2) bytes, rounded).
- * The first call on a device looks up the array's device address and clears it
- * (a synchronous memset); make that first call before any stream capture. All
- * calls share the one array, which keeps the last call's contents: calls that
- * overlap on the GPU (other streams, other host threads) race and must not be
- * issued. Other arguments, layouts and errors as hash_attn_gather_att.
+ * The first call on a device (with that device current) looks up the array's
+ * device address once; the array itself starts zeroed when the library loads.
+ * Every call first clears the error word and the split counters with one
+ * cudaMemsetAsync on `stream`, so a call never depends on what an earlier call
+ * left behind. All calls share the one array, which keeps the last call's
+ * contents: calls that overlap on the GPU (other streams, other host threads)
+ * race and must not be issued. Other arguments, layouts and errors as
+ * hash_attn_gather_att.
  */
 #define HA_NOALLOC_SCRATCH_BYTES (16u << 20)
 ha_status hash_attn_gather_att_noalloc(const ha_shape* shape, const void* q, const void* K,

@@ -24,6 +24,7 @@ constexpr int kSegPerChunk = kScoreThreads / 32;  // TOPK writes one segment per
 constexpr int kMaxSegments = 4096;        // segments per head (bounds GATHER-ATT's prefix table)
 constexpr int64_t kMaxCap = int64_t(1) << 24;  // largest n_cap accepted
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per pipeline wait
+constexpr int kClMax = 8;                 // fused SCORE+TOPK: most CTAs per cluster (portable size)
 
 // ------------------------------------------------------------------ workspace
 //
@@ -40,6 +41,8 @@ constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per pipeline 
 // meta_qt    int2  [heads][nchunks]       per chunk: (tie quota left, ties in chunk)
 struct Layout {
     int heads = 0;
+    bool fused = false;      // selection by the cluster kernel: flat lists instead of segments
+    int cl = 0, rmax = 0;    // its cluster size and most tokens per CTA
     int chunk = 0;           // tokens per SCORE/TOPK chunk (0: no selection regions)
     int nchunks = 0;
     int seg_cap = 0;         // tokens per TOPK segment (chunk / kSegPerChunk)
@@ -50,6 +53,7 @@ struct Layout {
     int nbins = HA_NBINS;    // distance bins per chunk histogram (b + 1 for b-bit codes)
     size_t off_err = 0, off_counter = 0, off_hist = 0, off_segcnt = 0, off_seg = 0, off_part = 0;
     size_t off_scnt = 0, off_meta_t = 0, off_meta_qt = 0;
+    size_t off_list = 0, off_lcnt = 0;  // fused: flat lists [heads][rows_cap] and their counts [heads]
     size_t total = 0;
 };
 
@@ -58,8 +62,23 @@ struct Layout {
 int choose_chunk(int64_t batch_hkv, int64_t n_cap);
 // Split-K policy for GATHER-ATT.
 void choose_splits(int64_t heads, int64_t rows_cap, int* splits, int* rows_per_split);
-// Full layout; with_selection=false leaves out the chunk_hist / seg regions.
-Layout make_layout(const ha_shape& s, int64_t rows_cap, bool with_selection, int nbins = HA_NBINS);
+// Fused SCORE+TOPK plan for a shape (32-bit codes, at most 4 query heads per
+// KV head, and a per-CTA token range whose packed distances fit in shared
+// memory); ok = false leaves the shape to the two-kernel path.
+struct ClPlan {
+    bool ok = false;
+    int cl = 1;      // CTAs per cluster, one cluster per (batch entry, KV head)
+    int rmax = 0;    // tokens per CTA: 32 per thread of a 256-, 512- or 1024-thread CTA
+};
+ClPlan cl_plan(const ha_shape& s, int code_words);
+// Dynamic shared memory of the fused kernel for a per-CTA range of rmax tokens
+// (the packed distances).
+size_t cl_select_smem(int rmax);
+// Full layout; with_selection=false leaves out the selection regions. With a
+// fused plan the selection regions are the flat lists; otherwise the chunk
+// histograms, segments and threshold metadata of the two-kernel path.
+Layout make_layout(const ha_shape& s, int64_t rows_cap, bool with_selection, int nbins = HA_NBINS,
+                   int code_words = 1);
 
 // ------------------------------------------------------------------ parameters
 
@@ -99,6 +118,24 @@ struct SelectParams {
     int excl;                // window tokens are never ties (exclusive windows)
     int32_t* seg_cnt;        // [heads][nseg]
     int32_t* seg_idx;        // [heads][nseg * seg_cap]
+    uint32_t* err;
+};
+
+// Fused SCORE+TOPK (k_select_cl): one cluster of `CL` CTAs per (batch entry, KV head).
+struct ClSelectParams {
+    const uint32_t* q_sig;   // [B * Hq]
+    const uint32_t* k_sig;
+    int64_t ks_sb, ks_sh;
+    const int32_t* seq_lens;
+    const int32_t* m_per_seq;    // [B] or null
+    const int32_t* m_per_head;   // [B * Hq] or null (overrides m_per_seq)
+    int m, n_sink, n_local, excl;
+    int B, Hq, Hkv, G, n_cap;
+    int CL, rmax;
+    int32_t* list;           // [B * Hq][cap] selected tokens, ascending
+    int cap;
+    int32_t* cnt;            // [B * Hq]
+    int pad;                 // 1: list[cnt .. cap) = -1
     uint32_t* err;
 };
 
@@ -248,6 +285,7 @@ cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem
 // Launchers (each returns cudaGetLastError() of its launch).
 cudaError_t launch_score(const ScoreParams& p, int batch_hkv, cudaStream_t st);
 cudaError_t launch_select(const SelectParams& p, int batch_hkv, cudaStream_t st, bool pdl = false);
+cudaError_t launch_select_cl(const ClSelectParams& p, int batch_hkv, cudaStream_t st);
 cudaError_t launch_compact(const CompactParams& p, int heads, cudaStream_t st);
 cudaError_t launch_hist(const HistParams& p, int heads, cudaStream_t st);
 cudaError_t launch_gather(const GatherParams& p, int d, int kv_bf16, cudaStream_t st, bool pdl = false);

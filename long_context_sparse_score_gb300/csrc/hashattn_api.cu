@@ -92,7 +92,7 @@ ha_status check_ws(const Layout& lay, void* ws, size_t ws_bytes) {
 }
 
 ha_status check_segments(const Layout& lay) {
-    if (lay.nseg > kMaxSegments)
+    if (!lay.fused && lay.nseg > kMaxSegments)
         return fail(HA_ERR_UNSUPPORTED, "n_cap too large for this batch: %d selection segments per head (limit %d)",
                     lay.nseg, kMaxSegments);
     return HA_OK;
@@ -118,19 +118,24 @@ struct Views {
     uint32_t* score_cnt;
     int32_t* meta_t;
     int2* meta_qt;
+    int32_t* list;
+    int32_t* lcnt;
 };
 
 Views views(const Layout& lay, void* ws) {
     Views v;
+    const bool seg = lay.chunk && !lay.fused;
     v.err = at<uint32_t>(ws, lay.off_err);
     v.counters = at<uint32_t>(ws, lay.off_counter);
     v.chunk_hist = lay.chunk ? at<uint32_t>(ws, lay.off_hist) : nullptr;
-    v.seg_cnt = lay.chunk ? at<int32_t>(ws, lay.off_segcnt) : nullptr;
-    v.seg_idx = lay.chunk ? at<int32_t>(ws, lay.off_seg) : nullptr;
+    v.seg_cnt = seg ? at<int32_t>(ws, lay.off_segcnt) : nullptr;
+    v.seg_idx = seg ? at<int32_t>(ws, lay.off_seg) : nullptr;
     v.part = at<float>(ws, lay.off_part);
     v.score_cnt = lay.chunk ? at<uint32_t>(ws, lay.off_scnt) : nullptr;
     v.meta_t = lay.chunk ? at<int32_t>(ws, lay.off_meta_t) : nullptr;
     v.meta_qt = lay.chunk ? at<int2>(ws, lay.off_meta_qt) : nullptr;
+    v.list = lay.fused ? at<int32_t>(ws, lay.off_list) : nullptr;
+    v.lcnt = lay.fused ? at<int32_t>(ws, lay.off_lcnt) : nullptr;
     return v;
 }
 
@@ -310,6 +315,38 @@ void apply_opts(const ha_select_opts* o, int32_t n_sink, int32_t n_local, ScoreP
     tp->excl = sp->excl;
 }
 
+// Parameters of the fused SCORE+TOPK kernel; the lists go to `list` (stride cap).
+ClSelectParams cl_params(const ha_shape* s, const Layout& lay, const Views& v, const uint32_t* q_sig,
+                         const uint32_t* k_sig, const int32_t* seq_lens, const int32_t* m_per_seq, int32_t m,
+                         int32_t n_sink, int32_t n_local, const ha_select_opts* o, int32_t* list, int32_t* cnt,
+                         int pad) {
+    ClSelectParams p{};
+    p.q_sig = q_sig;
+    p.k_sig = k_sig;
+    p.ks_sb = s->ks_sb;
+    p.ks_sh = s->ks_sh;
+    p.seq_lens = seq_lens;
+    p.m_per_seq = m_per_seq;
+    p.m_per_head = o ? o->m_per_head : nullptr;
+    p.m = m;
+    p.n_sink = n_sink;
+    p.n_local = n_local;
+    p.excl = o ? o->exclusive_windows : 0;
+    p.B = s->batch;
+    p.Hq = s->h_q;
+    p.Hkv = s->h_kv;
+    p.G = s->h_q / s->h_kv;
+    p.n_cap = s->n_cap;
+    p.CL = lay.cl;
+    p.rmax = lay.rmax;
+    p.list = list;
+    p.cap = lay.rows_cap;
+    p.cnt = cnt;
+    p.pad = pad;
+    p.err = v.err;
+    return p;
+}
+
 // The signature map run ahead of SCORE (hash_attn_decode_mapped): the appended
 // tokens' key codes (optional) and the step's query codes.
 struct MapStep {
@@ -334,7 +371,7 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
     if ((sel_idx == nullptr) != (sel_cnt == nullptr))
         return fail(HA_ERR_INVALID_ARG, "sel_idx and sel_cnt must both be given or both be NULL");
     const int64_t rows_cap = dense ? s->n_cap : rows_cap_of(s->n_cap, m, n_sink, n_local);
-    const Layout lay = make_layout(*s, rows_cap, !dense, nbins_of(opts));
+    const Layout lay = make_layout(*s, rows_cap, !dense, nbins_of(opts), W);
     HA_TRY(check_segments(lay));
     HA_TRY(check_ws(lay, ws, ws_bytes));
     if (check_only) return HA_OK;
@@ -360,6 +397,24 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
         return HA_OK;
     }
     HA_TRY(record(events, 0, st));
+    if (lay.fused) {
+        // SCORE and TOPK in one cluster kernel writing flat ascending lists: into the
+        // caller's sel_idx (padded with -1) when given, else into the workspace
+        const bool to_caller = sel_idx != nullptr;
+        const ClSelectParams cp = cl_params(s, lay, v, q_sig, k_sig, seq_lens, m_per_seq, m, n_sink, n_local, opts,
+                                            to_caller ? sel_idx : v.list, to_caller ? sel_cnt : v.lcnt,
+                                            to_caller ? 1 : 0);
+        HA_LAUNCH(launch_select_cl(cp, bhkv, st), "SCORE+TOPK launch");
+        HA_TRY(record(events, 1, st));
+        HA_TRY(record(events, 2, st));
+        gp.mode = kList;
+        gp.list_idx = cp.list;
+        gp.list_cnt = cp.cnt;
+        gp.list_cap = cp.cap;
+        HA_LAUNCH(launch_gather(gp, s->d, s->kv_dtype == HA_BF16, st, true), "GATHER-ATT launch");
+        HA_TRY(record(events, 3, st));
+        return HA_OK;
+    }
     if (W > 1) {
         const WideParams wp = wide_params(s, lay, v, q_sig, k_sig, seq_lens, m_per_seq, m, n_sink, n_local, W);
         HA_LAUNCH(launch_score_wide(wp, bhkv, st), "SCORE launch");
@@ -496,9 +551,36 @@ Staging staging_layout(const ha_shape* s) {
 
 int choose_chunk(int64_t batch_hkv, int64_t n_cap) {
     // kScoreThreads * TPT with TPT in {32, 16, 8, 4} (the instantiated kernels)
+    int chunk = kScoreThreads * 4;
     for (int tpt = 32; tpt > 4; tpt >>= 1)
-        if (batch_hkv * ceil_div(n_cap, (int64_t)kScoreThreads * tpt) >= kTargetCtas) return kScoreThreads * tpt;
-    return kScoreThreads * 4;
+        if (batch_hkv * ceil_div(n_cap, (int64_t)kScoreThreads * tpt) >= kTargetCtas) {
+            chunk = kScoreThreads * tpt;
+            break;
+        }
+    // a long single sequence: larger chunks keep the segments per head within
+    // GATHER-ATT's prefix table
+    while (chunk < kScoreThreads * 32 && ceil_div(n_cap, chunk) * kSegPerChunk > kMaxSegments) chunk *= 2;
+    return chunk;
+}
+
+ClPlan cl_plan(const ha_shape& s, int code_words) {
+    ClPlan P;
+    const int G = s.h_q / s.h_kv;
+    if (code_words > 1 || G > kMaxHeadsPerPass) return P;
+    // the smallest per-CTA range (32 tokens per thread of a 256-, 512- or 1024-thread
+    // CTA) whose cluster covers n_cap with at most kClMax CTAs
+    for (int nt = 256; nt <= 1024; nt *= 2) {
+        const int64_t range = 32 * (int64_t)nt;
+        int cl = 1;
+        while ((int64_t)cl * range < s.n_cap) cl *= 2;
+        if (cl <= kClMax) {
+            P.ok = true;
+            P.cl = cl;
+            P.rmax = (int)range;
+            return P;
+        }
+    }
+    return P;
 }
 
 void choose_splits(int64_t heads, int64_t rows_cap, int* splits, int* rows_per_split) {
@@ -519,7 +601,7 @@ void choose_splits(int64_t heads, int64_t rows_cap, int* splits, int* rows_per_s
     *rows_per_split = (int)rps;
 }
 
-Layout make_layout(const ha_shape& s, int64_t rows_cap, bool with_selection, int nbins) {
+Layout make_layout(const ha_shape& s, int64_t rows_cap, bool with_selection, int nbins, int code_words) {
     Layout L;
     L.heads = s.batch * s.h_q;
     L.rows_cap = (int)rows_cap;
@@ -529,23 +611,37 @@ Layout make_layout(const ha_shape& s, int64_t rows_cap, bool with_selection, int
     L.off_counter = off;
     off = align_up(off + (size_t)L.heads * 4, 256);
     if (with_selection) {
+        // the self-resetting SCORE counters and the threshold metadata come first,
+        // at offsets that do not depend on the code width, so one workspace sized
+        // for the largest use can serve calls with different options
         L.chunk = choose_chunk((int64_t)s.batch * s.h_kv, s.n_cap);
         L.nchunks = (int)ceil_div(s.n_cap, L.chunk);
         L.seg_cap = L.chunk / kSegPerChunk;
         L.nseg = L.nchunks * kSegPerChunk;
         L.nbins = nbins;
-        L.off_hist = off;
-        off = align_up(off + (size_t)L.heads * L.nchunks * nbins * 4, 256);
-        L.off_segcnt = off;
-        off = align_up(off + (size_t)L.heads * L.nseg * 4, 256);
-        L.off_seg = off;
-        off = align_up(off + (size_t)L.heads * L.nseg * L.seg_cap * 4, 256);
         L.off_scnt = off;
         off = align_up(off + (size_t)s.batch * s.h_kv * 4, 256);
         L.off_meta_t = off;
         off = align_up(off + (size_t)L.heads * 4, 256);
         L.off_meta_qt = off;
         off = align_up(off + (size_t)L.heads * L.nchunks * 8, 256);
+        L.off_hist = off;
+        off = align_up(off + (size_t)L.heads * L.nchunks * nbins * 4, 256);
+        const ClPlan P = cl_plan(s, code_words);
+        if (P.ok) {
+            L.fused = true;
+            L.cl = P.cl;
+            L.rmax = P.rmax;
+            L.off_list = off;
+            off = align_up(off + (size_t)L.heads * (size_t)rows_cap * 4, 256);
+            L.off_lcnt = off;
+            off = align_up(off + (size_t)L.heads * 4, 256);
+        } else {
+            L.off_segcnt = off;
+            off = align_up(off + (size_t)L.heads * L.nseg * 4, 256);
+            L.off_seg = off;
+            off = align_up(off + (size_t)L.heads * L.nseg * L.seg_cap * 4, 256);
+        }
     }
     L.off_part = off;
     off = align_up(off + (size_t)L.heads * L.splits * (s.d + 2) * 4, 256);
@@ -582,7 +678,7 @@ ha_status hash_attn_workspace_size_ex(const ha_shape* shape, int32_t m_max, int3
     if (bytes == nullptr) return fail(HA_ERR_INVALID_ARG, "bytes is NULL");
     const bool dense = m_max >= shape->n_cap;
     const int64_t rows_cap = dense ? shape->n_cap : rows_cap_of(shape->n_cap, m_max, n_sink, n_local);
-    const Layout sparse = make_layout(*shape, rows_cap, true, nbins_of(opts));
+    const Layout sparse = make_layout(*shape, rows_cap, true, nbins_of(opts), code_words_of(opts));
     HA_TRY(check_segments(sparse));
     *bytes = sparse.total;
     return HA_OK;
@@ -672,12 +768,18 @@ ha_status hash_attn_select_ex(const ha_shape* shape, const uint32_t* q_sig, cons
     if (seq_lens == nullptr || sel_idx == nullptr || sel_cnt == nullptr)
         return fail(HA_ERR_INVALID_ARG, "seq_lens, sel_idx and sel_cnt must not be NULL");
     const int64_t rows_cap = rows_cap_of(shape->n_cap, m, n_sink, n_local);
-    const Layout lay = make_layout(*shape, rows_cap, true, nbins_of(opts));
+    const Layout lay = make_layout(*shape, rows_cap, true, nbins_of(opts), W);
     HA_TRY(check_segments(lay));
     HA_TRY(check_ws(lay, workspace, ws_bytes));
     const Views v = views(lay, workspace);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int bhkv = shape->batch * shape->h_kv;
+    if (lay.fused) {
+        const ClSelectParams cp = cl_params(shape, lay, v, q_sig, k_sig, seq_lens, m_per_seq, m, n_sink, n_local,
+                                            opts, sel_idx, sel_cnt, 1);
+        HA_LAUNCH(launch_select_cl(cp, bhkv, st), "SCORE+TOPK launch");
+        return HA_OK;
+    }
     if (W > 1) {
         const WideParams wp = wide_params(shape, lay, v, q_sig, k_sig, seq_lens, m_per_seq, m, n_sink, n_local, W);
         HA_LAUNCH(launch_score_wide(wp, bhkv, st), "SCORE launch");
@@ -1021,8 +1123,10 @@ constexpr int kNoallocMaxDevices = 128;
 std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[kNoallocMaxDevices] = {};
 
-// Device address of the scratch on the current device; the first call per
-// device looks it up and clears the array.
+// Device address of the scratch on the current device, looked up once per
+// device (with that device current). The array needs no clearing at set-up: a
+// module's __device__ variables start zeroed when the module loads, and every
+// call clears what it relies on in stream order.
 ha_status noalloc_scratch(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1034,8 +1138,6 @@ ha_status noalloc_scratch(void** out) {
         void* ptr = nullptr;
         e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
         if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the built-in scratch");
-        e = cudaMemset(ptr, 0, HA_NOALLOC_SCRATCH_BYTES);
-        if (e != cudaSuccess) return cuda_fail(e, "clearing the built-in scratch");
         g_noalloc_ptr[dev] = ptr;
     }
     *out = g_noalloc_ptr[dev];
@@ -1065,10 +1167,11 @@ extern "C" ha_status hash_attn_gather_att_noalloc(const ha_shape* shape, const v
     void* ws = nullptr;
     HA_TRY(noalloc_scratch(&ws));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // the error word starts clean for every call; the counters are left at zero by
-    // the previous call (and by the clearing at set-up)
-    cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(uint32_t), st);
-    if (e != cudaSuccess) return cuda_fail(e, "clearing the error word");
+    // every call clears the error word and the split-K arrival counters on the
+    // caller's stream (the partials that follow them are overwritten before they
+    // are read), so nothing left by an earlier call can leak into this one
+    cudaError_t e = cudaMemsetAsync(ws, 0, lay.off_part, st);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the error word and counters");
     const Views v = views(lay, ws);
     GatherParams gp = gather_params(shape, lay, v, q, K, V, seq_lens, out, lse);
     gp.mode = kList;
