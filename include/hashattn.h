@@ -260,6 +260,24 @@ ha_status hash_attn_select_ex(const ha_shape* shape, const uint32_t* q_sig, cons
                               void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * The selection plan the library takes for a shape (host-only: no device call,
+ * no allocation). It depends only on the shape and the code width, so it also
+ * fixes the layout that hash_attn_workspace_size(_ex) sizes.
+ *   code_words  words per code (1 = the 32-bit codes of HashAttention Eq. (2))
+ *   fused       1: SCORE and TOPK run as one thread-block-cluster kernel (32-bit
+ *               codes, at most 4 query heads per KV head, n_cap within 8 CTAs of
+ *               8192, 16384 or 32768 tokens); 0: as two kernels
+ *   cluster     CTAs per (batch entry, KV head) of the fused kernel (0 if not fused)
+ *   range       tokens per CTA of the fused kernel (0 if not fused)
+ *   chunk       tokens per CTA of the two-kernel SCORE/TOPK (also used by
+ *               hash_attn_score whatever `fused` says)
+ * Any output pointer may be NULL. HA_ERR_INVALID_ARG / HA_ERR_UNSUPPORTED as
+ * hash_attn_workspace_size for a bad shape or code width.
+ */
+ha_status hash_attn_selection_plan(const ha_shape* shape, int32_t code_words, int32_t* fused,
+                                   int32_t* cluster, int32_t* range, int32_t* chunk);
+
+/*
  * GATHER-ATT + merge over caller-given index lists (page size 1, read in place):
  *   idx  [batch, h_q, idx_cap] int32 token indices (any order, no duplicates
  *        expected; each must lie in [0, seq_lens[b]) or it is skipped and

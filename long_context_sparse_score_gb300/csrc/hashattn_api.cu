@@ -684,6 +684,19 @@ ha_status hash_attn_workspace_size_ex(const ha_shape* shape, int32_t m_max, int3
     return HA_OK;
 }
 
+ha_status hash_attn_selection_plan(const ha_shape* shape, int32_t code_words, int32_t* fused, int32_t* cluster,
+                                   int32_t* range, int32_t* chunk) {
+    HA_TRY(check_shape(shape));
+    if (code_words != 1 && code_words != 2 && code_words != 4 && code_words != 8 && code_words != 16)
+        return fail(HA_ERR_UNSUPPORTED, "code_words must be 1, 2, 4, 8 or 16 (got %d)", code_words);
+    const ClPlan P = cl_plan(*shape, code_words);
+    if (fused) *fused = P.ok ? 1 : 0;
+    if (cluster) *cluster = P.ok ? P.cl : 0;
+    if (range) *range = P.ok ? P.rmax : 0;
+    if (chunk) *chunk = choose_chunk((int64_t)shape->batch * shape->h_kv, shape->n_cap);
+    return HA_OK;
+}
+
 ha_status hash_attn_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
     if (workspace == nullptr) return fail(HA_ERR_WORKSPACE, "workspace is NULL");
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)

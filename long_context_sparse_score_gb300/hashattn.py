@@ -39,7 +39,7 @@ EXPORTED = [
     "hash_attn_workspace_size", "hash_attn_workspace_init", "hash_attn_select_capacity",
     "hash_attn_decode", "hash_attn_decode_ex", "hash_attn_decode_timed", "hash_attn_decode_host",
     "hash_attn_host_staging_size", "hash_attn_score", "hash_attn_select",
-    "hash_attn_select_ex", "hash_attn_workspace_size_ex",
+    "hash_attn_select_ex", "hash_attn_workspace_size_ex", "hash_attn_selection_plan",
     "hash_attn_gather_att", "hash_attn_gather_att_noalloc", "hash_attn_merge", "hash_attn_merge_n",
     "hash_attn_encode_queries", "hash_attn_encode_keys", "hash_attn_encode_queries_mlp",
     "hash_attn_encode_keys_mlp", "hash_attn_decode_mapped", "hash_attn_topk_exact_workspace_size",
@@ -148,6 +148,8 @@ def lib() -> ctypes.CDLL:
     L.hash_attn_select_ex.argtypes = [SP, _P, _P, _P, _P, _I32, _I32, _I32, OP, _P, _P, _P, _SZ, _P]
     L.hash_attn_workspace_size_ex.argtypes = [SP, _I32, _I32, _I32, OP, ctypes.POINTER(_SZ)]
     L.hash_attn_decode_timed.argtypes = dec + [ctypes.POINTER(_P)]
+    IP = ctypes.POINTER(_I32)
+    L.hash_attn_selection_plan.argtypes = [SP, _I32, IP, IP, IP, IP]
     L.hash_attn_host_staging_size.argtypes = [SP, ctypes.POINTER(_SZ)]
     L.hash_attn_decode_host.argtypes = [SP, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _SZ, _P, _SZ,
                                         _P]
@@ -293,6 +295,13 @@ def hash_attn_workspace_size_ex(shape, m_max: int, n_sink: int, n_local: int, op
     _check(lib().hash_attn_workspace_size_ex(ctypes.byref(shape), m_max, n_sink, n_local,
                                              None if opts is None else ctypes.byref(opts), ctypes.byref(out)))
     return out.value
+
+
+def hash_attn_selection_plan(shape, code_words: int = 1) -> dict:
+    """{"fused", "cluster", "range", "chunk"}: the selection path the library takes for a shape."""
+    v = [ctypes.c_int32(0) for _ in range(4)]
+    _check(lib().hash_attn_selection_plan(ctypes.byref(shape), int(code_words), *(ctypes.byref(x) for x in v)))
+    return dict(zip(("fused", "cluster", "range", "chunk"), (x.value for x in v)))
 
 
 def hash_attn_decode_ex(shape, q, q_sig, k_sig, K, V, seq_lens, m_per_seq, m, n_sink, n_local, opts,

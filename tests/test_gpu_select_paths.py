@@ -1,0 +1,241 @@
+"""Every selection kernel instantiation the library launches, against the oracle.
+
+The fused SCORE+TOPK kernel comes in three CTA sizes (8,192 / 16,384 / 32,768
+tokens per CTA) and runs with clusters of 1, 2, 4 or 8 CTAs per (sequence, KV
+head); the two-kernel path (more than four query heads per KV head, codes wider
+than 32 bits, or a context beyond eight CTAs of 32,768 tokens) has SCORE/TOPK
+instantiations for 4, 8, 16 and 32 tokens per thread. Each case asserts which
+plan the shape takes (hash_attn_selection_plan) and then compares the selected
+sets bit for bit and the attention within tolerance on the selected heads.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gpu_helpers as GH
+from oracle import hashattn_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from long_context_sparse_score_gb300 import _build
+    _build.build()
+    from long_context_sparse_score_gb300 import hashattn
+    hashattn.lib()
+
+
+def W():
+    from long_context_sparse_score_gb300 import workloads
+    return workloads
+
+
+def _codes(w, kind, seed):
+    """Replace the workload's codes: 'random' keeps the projection codes, 'pool'
+    draws from a few codes near the query (the threshold bin holds thousands of
+    ties), 'far' makes every key the complement of every query (all distances 32)."""
+    if kind == "random":
+        return
+    q0 = 0x0F0F0F0F
+    if kind == "pool":
+        gen = torch.Generator(device="cuda").manual_seed(seed)
+        pool = torch.tensor([q0, q0 ^ 1, q0 ^ 3, q0 ^ 0x70000000, q0 ^ 0x0000FFFF], dtype=torch.int32,
+                            device="cuda")
+        w.k_sig = pool[torch.randint(0, 5, w.k_sig.shape, generator=gen, device="cuda")].contiguous()
+    elif kind == "far":
+        w.k_sig = torch.full_like(w.k_sig, ~q0)
+    w.q_sig = torch.full_like(w.q_sig, q0)
+
+
+def _check(w, heads, *, exclusive=False, m_per_head=None, code_words=1, att_heads=4):
+    res = GH.run_decode(w, exclusive=exclusive, m_per_head=m_per_head, code_words=code_words)
+    assert res["status"] == 0, hex(res["flags"])
+    hc = GH.HostCopy(w, exclusive=exclusive, m_per_head=m_per_head)
+    GH.check_selection(res, hc, heads, w.m)
+    GH.check_attention(res, hc, heads[:att_heads], w.m)
+    return res
+
+
+def _plan(w, code_words=1):
+    H = GH.ha()
+    return H.hash_attn_selection_plan(H.make_shape(w.q, w.K, w.V, w.k_sig), code_words)
+
+
+# ---------------------------------------------------------------- fused kernel: every (range, cluster)
+
+FUSED = [
+    # name, B, Hq, Hkv, n_cap, lens, m, S, Lw, codes, expected (range, cluster)
+    ("r8k_cl1", 2, 8, 2, 8192, [8192, 5000], 300, 16, 64, "pool", (8192, 1)),
+    ("r8k_cl2_ragged", 2, 4, 1, 12000, [12000, 7000], 700, 40, 500, "random", (8192, 2)),
+    ("r8k_cl4_g3", 1, 3, 1, 30000, [30000], 2000, 128, 128, "pool", (8192, 4)),
+    ("r8k_cl8_g2", 2, 4, 2, 60000, [60000, 33333], 1500, 9000, 9000, "pool", (8192, 8)),
+    ("r8k_cl8_g1", 1, 1, 1, 65536, [65535], 4000, 7, 20000, "random", (8192, 8)),
+    ("r16k_cl8", 1, 4, 1, 100000, [100000], 3000, 128, 256, "pool", (16384, 8)),
+    ("r16k_cl8_short_seq", 2, 4, 1, 131072, [131072, 3000], 4096, 128, 256, "random", (16384, 8)),
+    ("r32k_cl8", 1, 4, 1, 200000, [200000], 6000, 128, 256, "pool", (32768, 8)),
+    ("r32k_cl8_windows_span_ranks", 1, 4, 1, 262144, [250000], 5000, 70000, 40000, "pool", (32768, 8)),
+    ("all_distances_32", 1, 4, 1, 20000, [20000], 900, 16, 16, "far", (8192, 4)),
+    ("budget_zero_windows_only", 1, 4, 1, 20000, [20000], 0, 9000, 100, "pool", (8192, 4)),
+]
+
+
+@pytest.mark.parametrize("case", FUSED, ids=[c[0] for c in FUSED])
+def test_fused_selection(case):
+    name, B, Hq, Hkv, n_cap, lens, m, S, Lw, codes, want = case
+    w = W().make_gqa(31, B=B, Hq=Hq, Hkv=Hkv, d=128, n_cap=n_cap, seq_lens=lens, m=m, n_sink=S, n_local=Lw,
+                     device="cuda", name=name)
+    _codes(w, codes, 41)
+    plan = _plan(w)
+    assert plan["fused"] == 1 and (plan["range"], plan["cluster"]) == want, plan
+    heads = [(b, h) for b in range(B) for h in range(Hq)]
+    _check(w, heads)
+
+
+FUSED_VARIANTS = [
+    # name, n_cap, lens, m, S, Lw, codes, exclusive, per-head budgets
+    ("exclusive_quota_across_ranks", 60000, [60000, 41000], 3000, 9000, 12000, "pool", True, False),
+    ("per_head_budgets_cl8", 60000, [60000, 20000], 2500, 64, 128, "random", False, True),
+    ("exclusive_per_head_cl8_r16k", 100000, [100000, 77777], 3000, 128, 20000, "pool", True, True),
+]
+
+
+@pytest.mark.parametrize("case", FUSED_VARIANTS, ids=[c[0] for c in FUSED_VARIANTS])
+def test_fused_selection_variants(case):
+    """Exclusive windows and per-head budgets where the windows and the tie
+    boundary fall in different CTAs of the cluster."""
+    name, n_cap, lens, m, S, Lw, codes, exclusive, per_head = case
+    w = W().make_gqa(32, B=2, Hq=4, Hkv=1, d=128, n_cap=n_cap, seq_lens=lens, m=m, n_sink=S, n_local=Lw,
+                     device="cuda", name=name)
+    _codes(w, codes, 42)
+    assert _plan(w)["cluster"] == 8
+    mph = None
+    if per_head:
+        gen = torch.Generator(device="cuda").manual_seed(9)
+        mph = torch.randint(0, m + 1, (2, 4), generator=gen, device="cuda", dtype=torch.int32)
+        mph[0, 0], mph[1, 3] = 0, m
+    res = _check(w, [(b, h) for b in range(2) for h in range(4)], exclusive=exclusive, m_per_head=mph)
+    if exclusive:
+        cnt = res["sel_cnt"].cpu().numpy()
+        for b, n in enumerate(lens):
+            nw = len(O.window_positions(n, S, Lw))
+            for h in range(4):
+                mb = int(mph[b, h]) if per_head else m
+                assert int(cnt[b, h]) == min(n, mb + nw)
+
+
+def test_fused_select_entry_point_pads_and_matches_decode():
+    H = GH.ha()
+    w = W().make_gqa(33, B=2, Hq=4, Hkv=1, d=128, n_cap=60000, seq_lens=[60000, 100], m=2000, n_sink=64,
+                     n_local=64, device="cuda")
+    shape = H.make_shape(w.q, w.K, w.V, w.k_sig)
+    ws = GH.workspace(shape, w.m, w.n_sink, w.n_local)
+    cap = H.hash_attn_select_capacity(60000, 2000, 64, 64)
+    sel = torch.full((2, 4, cap), 77, dtype=torch.int32, device="cuda")
+    cnt = torch.full((2, 4), 77, dtype=torch.int32, device="cuda")
+    H.hash_attn_select(shape, w.q_sig, w.k_sig, w.seq_lens, None, 2000, 64, 64, sel, cnt, workspace=ws)
+    res = {"sel_idx": sel, "sel_cnt": cnt, "cap": cap}
+    GH.check_selection(res, GH.HostCopy(w), [(b, h) for b in range(2) for h in range(4)], 2000)
+    dec = GH.run_decode(w)
+    assert torch.equal(dec["sel_idx"], sel) and torch.equal(dec["sel_cnt"], cnt)
+
+
+# ---------------------------------------------------------------- two-kernel path: every TPT
+
+TWO_KERNEL = [
+    # name, B, Hq, Hkv, n_cap, lens, m, S, Lw, codes, expected chunk
+    ("g8_tpt4", 2, 64, 8, 10000, [10000, 6000], 500, 32, 64, "pool", 1024),
+    ("g8_tpt8", 2, 64, 8, 40000, [40000, 25000], 1200, 128, 128, "random", 2048),
+    ("g8_tpt16", 2, 64, 8, 80000, [80000, 79999], 2500, 128, 256, "pool", 4096),
+    ("g8_tpt32", 2, 64, 8, 150000, [150000, 99999], 4096, 128, 256, "random", 8192),
+    ("g4_beyond_fused_range", 1, 4, 1, 300000, [299000], 8000, 128, 256, "pool", 1024),
+]
+
+
+def _sample(B, Hq, k, seed):
+    rng = np.random.default_rng(seed)
+    heads = [(b, h) for b in range(B) for h in range(Hq)]
+    pick = rng.choice(len(heads), size=min(k, len(heads)), replace=False)
+    return sorted(heads[i] for i in pick)
+
+
+@pytest.mark.parametrize("case", TWO_KERNEL, ids=[c[0] for c in TWO_KERNEL])
+def test_two_kernel_selection(case):
+    name, B, Hq, Hkv, n_cap, lens, m, S, Lw, codes, chunk = case
+    w = W().make_gqa(34, B=B, Hq=Hq, Hkv=Hkv, d=128, n_cap=n_cap, seq_lens=lens, m=m, n_sink=S, n_local=Lw,
+                     device="cuda", name=name)
+    _codes(w, codes, 43)
+    plan = _plan(w)
+    assert plan["fused"] == 0 and plan["chunk"] == chunk, plan
+    _check(w, _sample(B, Hq, 12, 1))
+
+
+@pytest.mark.parametrize("chunk,exclusive", [(8192, True), (2048, True), (8192, False)])
+def test_two_kernel_variants(chunk, exclusive):
+    """Exclusive windows and per-head budgets on the two-kernel path (eight query
+    heads per KV head), at the largest and a small chunk."""
+    n_cap = 150000 if chunk == 8192 else 40000
+    w = W().make_gqa(35, B=2, Hq=64, Hkv=8, d=128, n_cap=n_cap, seq_lens=[n_cap, n_cap - 1234], m=2000,
+                     n_sink=3000, n_local=5000, device="cuda")
+    _codes(w, "pool", 44)
+    assert _plan(w)["chunk"] == chunk
+    gen = torch.Generator(device="cuda").manual_seed(10)
+    mph = torch.randint(0, 2001, (2, 64), generator=gen, device="cuda", dtype=torch.int32)
+    _check(w, _sample(2, 64, 10, 2), exclusive=exclusive, m_per_head=mph)
+
+
+@pytest.mark.parametrize("Wd", [2, 4, 16])
+def test_wide_codes_at_the_largest_chunk(Wd):
+    """Codes of Wd words at the 8,192-token chunk (the shape of the bench's
+    128-bit measurement), random codes."""
+    B, Hq, Hkv, n_cap = 2, 32, 8, 160000
+    w = W().make_gqa(36, B=B, Hq=Hq, Hkv=Hkv, d=128, n_cap=n_cap, seq_lens=[n_cap, 150001], m=4096,
+                     n_sink=128, n_local=256, device="cuda")
+    gen = torch.Generator(device="cuda").manual_seed(20 + Wd)
+    w.k_sig = torch.randint(-2 ** 31, 2 ** 31 - 1, (B, Hkv, n_cap, Wd), generator=gen, device="cuda",
+                            dtype=torch.int64).to(torch.int32).contiguous()
+    w.q_sig = torch.randint(-2 ** 31, 2 ** 31 - 1, (B, Hq, Wd), generator=gen, device="cuda",
+                            dtype=torch.int64).to(torch.int32).contiguous()
+    plan = _plan(w, Wd)
+    assert plan["fused"] == 0 and plan["chunk"] == 8192
+    _check(w, _sample(B, Hq, 8, 3), code_words=Wd)
+
+
+@pytest.mark.parametrize("n_cap,B,Hkv,chunk", [(10000, 2, 2, 1024), (40000, 2, 8, 2048), (80000, 2, 8, 4096),
+                                                (150000, 2, 8, 8192)])
+def test_score_entry_point_every_chunk(n_cap, B, Hkv, chunk):
+    """hash_attn_score (distances and histograms) at each SCORE instantiation."""
+    H = GH.ha()
+    Hq = 4 * Hkv
+    w = W().make_gqa(37, B=B, Hq=Hq, Hkv=Hkv, d=128, n_cap=n_cap, seq_lens=[n_cap, n_cap // 2 + 3], m=64,
+                     n_sink=0, n_local=0, device="cuda")
+    shape = H.make_shape(w.q, w.K, w.V, w.k_sig)
+    assert H.hash_attn_selection_plan(shape)["chunk"] == chunk
+    ws = GH.workspace(shape, w.m, 0, 0)
+    dist = torch.full((B, Hq, n_cap), 255, dtype=torch.uint8, device="cuda")
+    hist = torch.zeros((B, Hq, 33), dtype=torch.int32, device="cuda")
+    H.hash_attn_score(shape, w.q_sig, w.k_sig, w.seq_lens, dist, hist, workspace=ws)
+    torch.cuda.synchronize()
+    dist = dist.cpu().numpy()
+    hist = hist.cpu().numpy()
+    qs = w.q_sig.cpu().numpy()
+    lens = w.seq_lens.cpu().numpy()
+    for b, h in _sample(B, Hq, 6, 4):
+        n = int(lens[b])
+        ref = O.hamming_distances(int(qs[b, h]), w.k_sig[b, h // 4, :n].cpu().numpy())
+        assert np.array_equal(dist[b, h, :n], ref)
+        assert np.all(dist[b, h, n:] == 255)
+        assert np.array_equal(hist[b, h], O.distance_histogram(ref))
+
+
+def test_single_sequence_of_two_million_tokens():
+    """One (sequence, KV head) of 2^21 tokens: beyond the fused kernel's range,
+    the two-kernel path with its chunk raised so the segments fit."""
+    n = 1 << 21
+    w = W().make_gqa(38, B=1, Hq=4, Hkv=1, d=128, n_cap=n, seq_lens=[n], m=65536, n_sink=128, n_local=256,
+                     device="cuda")
+    plan = _plan(w)
+    assert plan["fused"] == 0 and (n + plan["chunk"] - 1) // plan["chunk"] * 8 <= 4096
+    _check(w, [(0, h) for h in range(4)], att_heads=2)

@@ -67,6 +67,42 @@ def test_workspace_size_and_capacity(ha):
     assert _ws_size(ha, _shape(ha), m=4096)[1] >= nbytes
 
 
+def _plan(ha, B, Hq, Hkv, n_cap, code_words=1):
+    s = _shape(ha, batch=B, h_q=Hq, h_kv=Hkv, n_cap=n_cap, q_sb=Hq * 128, k_sb=Hkv * n_cap * 128,
+               k_sh=n_cap * 128, v_sb=Hkv * n_cap * 128, v_sh=n_cap * 128, ks_sb=Hkv * n_cap, ks_sh=n_cap)
+    return ha.hash_attn_selection_plan(s, code_words)
+
+
+def test_selection_plan_of_the_workloads(ha):
+    """The five workloads take the fused kernel; more than four query heads per KV
+    head, wider codes, or a context beyond eight CTAs take the two-kernel path."""
+    # name: (B, Hq, Hkv, n_cap) -> (range, cluster)
+    fused = {"tiny": ((1, 1, 1, 1024), (8192, 1)), "gqa32k": ((1, 32, 8, 32768), (8192, 4)),
+             "batch16_128k": ((16, 32, 8, 131072), (16384, 8)), "shared_doc": ((32, 32, 8, 61440), (8192, 8)),
+             "ragged": ((64, 32, 8, 65536), (8192, 8)), "256k": ((1, 4, 1, 262144), (32768, 8))}
+    for name, (shape, want) in fused.items():
+        p = _plan(ha, *shape)
+        assert p["fused"] == 1 and (p["range"], p["cluster"]) == want, (name, p)
+    assert _plan(ha, 2, 64, 8, 131072)["fused"] == 0                 # eight query heads per KV head
+    assert _plan(ha, 16, 32, 8, 131072, code_words=4)["fused"] == 0  # 128-bit codes
+    assert _plan(ha, 1, 4, 1, 262145)["fused"] == 0                  # beyond 8 x 32,768 tokens
+    # a single long sequence keeps the two-kernel path within its segment table
+    for n in (1 << 21, 1 << 22):
+        p = _plan(ha, 1, 4, 1, n)
+        assert p["fused"] == 0 and -(-n // p["chunk"]) * 8 <= 4096, (n, p)
+    with pytest.raises(ha.HashAttnError):
+        _plan(ha, 1, 4, 1, 4096, code_words=3)
+
+
+def test_fused_workspace_is_sized_by_the_budget_not_the_context(ha):
+    """With the fused kernel the token lists take heads x (m + n_sink + n_local) ints,
+    not heads x n_cap: at the 16 x 131,072-token shape well under 100 MB."""
+    s = _shape(ha, batch=16, h_q=32, h_kv=8, n_cap=131072, q_sb=32 * 128, k_sb=8 * 131072 * 128,
+               k_sh=131072 * 128, v_sb=8 * 131072 * 128, v_sh=131072 * 128, ks_sb=8 * 131072, ks_sh=131072)
+    st, nbytes = _ws_size(ha, s, m=4096, S=128, L=256)
+    assert st == ha.HA_OK and nbytes < 100 * 2 ** 20, nbytes
+
+
 @pytest.mark.parametrize("field,value,status", [
     ("d", 96, -2), ("d", 256, -2), ("h_q", 7, -1), ("h_kv", 0, -1), ("batch", 0, -1),
     ("n_cap", 0, -1), ("kv_dtype", 5, -2), ("q_dtype", -1, -2), ("k_sn", 0, -1), ("q_sh", -3, -1),
