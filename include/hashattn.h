@@ -265,8 +265,8 @@ ha_status hash_attn_select_ex(const ha_shape* shape, const uint32_t* q_sig, cons
  * fixes the layout that hash_attn_workspace_size(_ex) sizes.
  *   code_words  words per code (1 = the 32-bit codes of HashAttention Eq. (2))
  *   fused       1: SCORE and TOPK run as one thread-block-cluster kernel (32-bit
- *               codes, at most 4 query heads per KV head, n_cap within 8 CTAs of
- *               8192, 16384 or 32768 tokens); 0: as two kernels
+ *               codes, at most 4 query heads per KV head, n_cap within 16 CTAs
+ *               of 8192, 16384 or 32768 tokens); 0: as two kernels
  *   cluster     CTAs per (batch entry, KV head) of the fused kernel (0 if not fused)
  *   range       tokens per CTA of the fused kernel (0 if not fused)
  *   chunk       tokens per CTA of the two-kernel SCORE/TOPK (also used by

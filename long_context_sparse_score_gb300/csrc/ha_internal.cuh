@@ -24,7 +24,8 @@ constexpr int kSegPerChunk = kScoreThreads / 32;  // TOPK writes one segment per
 constexpr int kMaxSegments = 4096;        // segments per head (bounds GATHER-ATT's prefix table)
 constexpr int64_t kMaxCap = int64_t(1) << 24;  // largest n_cap accepted
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per pipeline wait
-constexpr int kClMax = 8;                 // fused SCORE+TOPK: most CTAs per cluster (portable size)
+constexpr int kClMax = 16;                // fused SCORE+TOPK: most CTAs per cluster (16 needs the non-portable opt-in)
+constexpr int kSMs = 152;                 // SMs of a GB300
 
 // ------------------------------------------------------------------ workspace
 //
@@ -68,7 +69,7 @@ void choose_splits(int64_t heads, int64_t rows_cap, int* splits, int* rows_per_s
 struct ClPlan {
     bool ok = false;
     int cl = 1;      // CTAs per cluster, one cluster per (batch entry, KV head)
-    int rmax = 0;    // tokens per CTA: 32 per thread of a 256-, 512- or 1024-thread CTA
+    int rmax = 0;    // tokens per CTA: 8192, 16384 or 32768
 };
 ClPlan cl_plan(const ha_shape& s, int code_words);
 // Dynamic shared memory of the fused kernel for a per-CTA range of rmax tokens

@@ -404,13 +404,14 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
         const ClSelectParams cp = cl_params(s, lay, v, q_sig, k_sig, seq_lens, m_per_seq, m, n_sink, n_local, opts,
                                             to_caller ? sel_idx : v.list, to_caller ? sel_cnt : v.lcnt,
                                             to_caller ? 1 : 0);
-        HA_LAUNCH(launch_select_cl(cp, bhkv, st), "SCORE+TOPK launch");
-        HA_TRY(record(events, 1, st));
-        HA_TRY(record(events, 2, st));
         gp.mode = kList;
         gp.list_idx = cp.list;
         gp.list_cnt = cp.cnt;
         gp.list_cap = cp.cap;
+        HA_LAUNCH(launch_select_cl(cp, bhkv, st), "SCORE+TOPK launch");
+        HA_TRY(record(events, 1, st));
+        HA_TRY(record(events, 2, st));
+        // GATHER-ATT may start while the selection drains (it waits in the kernel)
         HA_LAUNCH(launch_gather(gp, s->d, s->kv_dtype == HA_BF16, st, true), "GATHER-ATT launch");
         HA_TRY(record(events, 3, st));
         return HA_OK;
@@ -567,19 +568,24 @@ ClPlan cl_plan(const ha_shape& s, int code_words) {
     ClPlan P;
     const int G = s.h_q / s.h_kv;
     if (code_words > 1 || G > kMaxHeadsPerPass) return P;
-    // the smallest per-CTA range (32 tokens per thread of a 256-, 512- or 1024-thread
-    // CTA) whose cluster covers n_cap with at most kClMax CTAs
-    for (int nt = 256; nt <= 1024; nt *= 2) {
-        const int64_t range = 32 * (int64_t)nt;
+    const int64_t pairs = (int64_t)s.batch * s.h_kv;
+    auto cluster_of = [&](int64_t range) {
         int cl = 1;
         while ((int64_t)cl * range < s.n_cap) cl *= 2;
-        if (cl <= kClMax) {
-            P.ok = true;
-            P.cl = cl;
-            P.rmax = (int)range;
-            return P;
-        }
-    }
+        return cl;
+    };
+    auto take = [&](int range, int cl) {
+        P.ok = true;
+        P.cl = cl;
+        P.rmax = range;
+        return P;
+    };
+    // 16,384-token CTAs (512 threads, two per SM) with up to 8 per cluster; 8,192
+    // (256 threads) where that leaves fewer CTAs than SMs; 32,768 for contexts
+    // beyond 8 x 16,384 tokens, with up to 16 per cluster
+    const int c16 = cluster_of(16384), c8 = cluster_of(8192), c32 = cluster_of(32768);
+    if (c16 <= 8) return (pairs * c16 < kSMs && c8 <= 8) ? take(8192, c8) : take(16384, c16);
+    if (c32 <= kClMax) return take(32768, c32);
     return P;
 }
 

@@ -73,6 +73,19 @@ __device__ __forceinline__ float load_q(const void* q, int64_t off, int bf16) {
     return reinterpret_cast<const float*>(q)[off];
 }
 
+// acc + q.lo * k.lo + q.hi * k.hi for two bf16 pairs: the products of bf16
+// operands are exact in fp32 and each add rounds once, as in an fp32 FMA.
+__device__ __forceinline__ float fma_bf16x2(uint32_t q2, uint32_t k2, float acc) {
+    asm("{\n\t.reg .b16 ql, qh, kl, kh;\n\t"
+        "mov.b32 {ql, qh}, %1;\n\t"
+        "mov.b32 {kl, kh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, ql, kl, %0;\n\t"
+        "fma.rn.f32.bf16 %0, qh, kh, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(q2), "r"(k2));
+    return acc;
+}
+
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
 template <int N>
@@ -101,7 +114,11 @@ __device__ __forceinline__ int token_at(const GatherParams& p, int pp, int n, co
 
 // Five CTAs per SM for rows of up to 256 bytes (20 warps of copy pipelines);
 // the 512-byte-row instantiation keeps three to avoid spills.
-template <int D, typename KT>
+// QREG: bf16 query and bf16 K/V; each lane keeps the query elements of its
+// dims as packed bf16 in registers and forms q.k with bf16 x bf16 -> fp32 FMAs
+// straight from the K chunk (no query reads from shared memory, no K
+// conversion); the score is scaled once per row.
+template <int D, typename KT, bool QREG>
 __global__ void __launch_bounds__(kGatherThreads, (D * sizeof(KT) <= 256) ? 5 : 3)
     k_gather_att(const GatherParams p) {
     using C = Cfg<D, KT>;
@@ -127,10 +144,25 @@ __global__ void __launch_bounds__(kGatherThreads, (D * sizeof(KT) <= 256) ? 5 : 
     const int n = checked_len(p.seq_lens, b, p.n_cap, p.err, report);
     const int nused = (p.mode == kSegmented) ? (n + p.seg_cap - 1) / p.seg_cap : 0;
 
-    // ---- the scaled query (an input: read before waiting for TOPK's output)
+    // ---- the query (an input: read before waiting for TOPK's output)
+    const int r = lane & 7, qt = lane >> 3;
+    constexpr int QW = QREG ? D / 8 : 1;   // packed bf16 pairs of this lane's D / 4 dims
+    uint32_t qreg[QW];
     {
         const int64_t qoff = (int64_t)b * p.q_sb + (int64_t)(g * p.G + hh) * p.q_sh;
-        for (int dd = tid; dd < D; dd += kGatherThreads) s_q[dd] = load_q(p.q, qoff + dd, p.q_bf16) * p.qscale;
+        if constexpr (QREG) {
+            // chunk jc of the lane holds dims (jc * 4 + qt) * 8 .. + 7
+            const uint16_t* qh16 = reinterpret_cast<const uint16_t*>(p.q) + qoff;
+#pragma unroll
+            for (int jc = 0; jc < QW / 4; ++jc)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int dim = (jc * 4 + qt) * 8 + 2 * u;
+                    qreg[jc * 4 + u] = (uint32_t)qh16[dim] | ((uint32_t)qh16[dim + 1] << 16);
+                }
+        } else {
+            for (int dd = tid; dd < D; dd += kGatherThreads) s_q[dd] = load_q(p.q, qoff + dd, p.q_bf16) * p.qscale;
+        }
     }
     pdl_launch_dependents();
     pdl_wait();
@@ -230,7 +262,6 @@ __global__ void __launch_bounds__(kGatherThreads, (D * sizeof(KT) <= 256) ? 5 : 
         }
     };
 
-    const int r = lane & 7, qt = lane >> 3;
     float2 ov[C::DPL / 2];
 #pragma unroll
     for (int i = 0; i < C::DPL / 2; ++i) ov[i] = make_float2(0.f, 0.f);
@@ -253,24 +284,37 @@ __global__ void __launch_bounds__(kGatherThreads, (D * sizeof(KT) <= 256) ? 5 : 
 
         float part = 0.f;
         if (tok >= 0) {
-            float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+            if constexpr (QREG) {
+                float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int jc = 0; jc < C::CPL; ++jc) {
-                const uint4 w = *reinterpret_cast<const uint4*>(kr + (jc * 4 + qt) * 16);
-                float f[C::EPC];
-                chunk_to_float<KT>(w, f);
-#pragma unroll
-                for (int e = 0; e < C::EPC; e += 4) {
-                    const float4 q4 = *reinterpret_cast<const float4*>(s_q + (jc * 4 + qt) * C::EPC + e);
-                    a0 = __ffma2_rn(make_float2(q4.x, q4.y), make_float2(f[e], f[e + 1]), a0);
-                    a1 = __ffma2_rn(make_float2(q4.z, q4.w), make_float2(f[e + 2], f[e + 3]), a1);
+                for (int jc = 0; jc < C::CPL; ++jc) {
+                    const uint4 w = *reinterpret_cast<const uint4*>(kr + (jc * 4 + qt) * 16);
+                    a[0] = fma_bf16x2(qreg[jc * 4 + 0], w.x, a[0]);
+                    a[1] = fma_bf16x2(qreg[jc * 4 + 1], w.y, a[1]);
+                    a[2] = fma_bf16x2(qreg[jc * 4 + 2], w.z, a[2]);
+                    a[3] = fma_bf16x2(qreg[jc * 4 + 3], w.w, a[3]);
                 }
+                part = (a[0] + a[1]) + (a[2] + a[3]);
+            } else {
+                float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int jc = 0; jc < C::CPL; ++jc) {
+                    const uint4 w = *reinterpret_cast<const uint4*>(kr + (jc * 4 + qt) * 16);
+                    float f[C::EPC];
+                    chunk_to_float<KT>(w, f);
+#pragma unroll
+                    for (int e = 0; e < C::EPC; e += 4) {
+                        const float4 q4 = *reinterpret_cast<const float4*>(s_q + (jc * 4 + qt) * C::EPC + e);
+                        a0 = __ffma2_rn(make_float2(q4.x, q4.y), make_float2(f[e], f[e + 1]), a0);
+                        a1 = __ffma2_rn(make_float2(q4.z, q4.w), make_float2(f[e + 2], f[e + 3]), a1);
+                    }
+                }
+                part = (a0.x + a0.y) + (a1.x + a1.y);
             }
-            part = (a0.x + a0.y) + (a1.x + a1.y);
         }
         part += __shfl_xor_sync(0xffffffffu, part, 8);
         part += __shfl_xor_sync(0xffffffffu, part, 16);
-        const float sc = (tok >= 0) ? part : -CUDART_INF_F;
+        const float sc = (tok >= 0) ? (QREG ? part * p.qscale : part) : -CUDART_INF_F;
         float mx = sc;
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
@@ -417,24 +461,26 @@ __global__ void __launch_bounds__(256) k_merge(const MergeParams p) {
     if (lane == 0) p.lse[row] = empty ? -CUDART_INF_F : M + logf(S);
 }
 
-template <int D, typename KT>
+template <int D, typename KT, bool QREG>
 cudaError_t launch_gather_t(const GatherParams& p, cudaStream_t st, bool pdl) {
     using C = Cfg<D, KT>;
     const size_t smem = (size_t)C::OFF_TOKL + (size_t)(p.rows_per_split + p.nseg + 1) * sizeof(int);
-    cudaError_t e = cudaFuncSetAttribute(k_gather_att<D, KT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(k_gather_att<D, KT, QREG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)(p.B * p.Hq) * (unsigned)p.splits;
-    return launch_ex(k_gather_att<D, KT>, dim3(grid), dim3(kGatherThreads), smem, st, pdl, p);
+    return launch_ex(k_gather_att<D, KT, QREG>, dim3(grid), dim3(kGatherThreads), smem, st, pdl, p);
 }
 
 }  // namespace
 
 cudaError_t launch_gather(const GatherParams& p, int d, int kv_bf16, cudaStream_t st, bool pdl) {
-    if (d == 128 && kv_bf16) return launch_gather_t<128, __nv_bfloat16>(p, st, pdl);
-    if (d == 64 && kv_bf16) return launch_gather_t<64, __nv_bfloat16>(p, st, pdl);
-    if (d == 128 && !kv_bf16) return launch_gather_t<128, float>(p, st, pdl);
-    if (d == 64 && !kv_bf16) return launch_gather_t<64, float>(p, st, pdl);
+    if (d == 128 && kv_bf16 && p.q_bf16) return launch_gather_t<128, __nv_bfloat16, true>(p, st, pdl);
+    if (d == 64 && kv_bf16 && p.q_bf16) return launch_gather_t<64, __nv_bfloat16, true>(p, st, pdl);
+    if (d == 128 && kv_bf16) return launch_gather_t<128, __nv_bfloat16, false>(p, st, pdl);
+    if (d == 64 && kv_bf16) return launch_gather_t<64, __nv_bfloat16, false>(p, st, pdl);
+    if (d == 128 && !kv_bf16) return launch_gather_t<128, float, false>(p, st, pdl);
+    if (d == 64 && !kv_bf16) return launch_gather_t<64, float, false>(p, st, pdl);
     return cudaErrorInvalidValue;
 }
 

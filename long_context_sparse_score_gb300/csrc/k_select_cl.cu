@@ -7,31 +7,32 @@
 // of a KV head's codes serves all its query heads (Nectar Sec. 3, GQA sharing).
 //
 // Decomposition. The CL CTAs of a cluster split the n tokens of one (batch
-// entry b, KV head g) into contiguous ranges of R = 32 NT tokens (NT threads per
-// CTA; rank r owns [r R, min(n, (r + 1) R))). A CTA keeps its intermediates on
-// chip:
-//   phase 1  every code of the range is read once (16-byte loads, 512 contiguous
-//            bytes per warp instruction, four rounds in flight per thread); per
-//            token the distances to the (up to four) query heads are computed
-//            once, kept as one packed word (head e in byte e) in shared memory
-//            and counted into a 33-bin histogram per head (shared-memory columns
-//            indexed by lane).
+// entry b, KV head g) into contiguous ranges of R = 8192 LB tokens (rank r owns
+// [r R, min(n, (r + 1) R))); R is chosen so that the whole grid is resident at
+// once where it can be (every SM streams codes at the same time instead of in
+// waves that finish together).
+//   phase 1  every code of the range is read once (16-byte streaming loads, 512
+//            contiguous bytes per warp instruction, four rounds in flight per
+//            thread); per token the distances to the (up to four) query heads
+//            are computed once, written as one packed word (head e in byte e) to
+//            a buffer in token order that stays in L2, and counted into a 33-bin
+//            histogram per head (shared-memory columns indexed by lane).
 //   meta     after a cluster barrier every CTA reads the cluster's histograms
 //            through distributed shared memory and derives, per head, the
 //            threshold bin t (smallest t whose cumulative count reaches k), the
-//            number of tied tokens (distance t) still to take, and how many of
-//            those fall to this CTA: none (mode 0), all (mode 1) or the first q
-//            in token order (mode 2, one CTA per head at most).
-//   masks    warp w owns tokens [w 1024, (w + 1) 1024) of the range and lane l
-//            of it the 32 tokens of block 32 w + l; the lane builds its
-//            selection mask for all heads at once with byte-wise compares of the
-//            packed distances (no further popcounts); windows and the sequence
+//            number of tied tokens (distance t) still to take, how many of those
+//            fall to each CTA (none, all, or the first q in token order: at most
+//            one CTA per head takes part of its ties) and so how many tokens each
+//            CTA selects, which fixes this CTA's first output position.
+//   masks    warp w owns 1024 LB consecutive tokens of the range and each lane LB
+//            consecutive 32-token blocks, one 128-byte line of packed distances
+//            each; a lane builds its selection masks for all heads at once with
+//            byte-wise compares (no further popcounts); windows and the sequence
 //            end enter as bit ranges; in the boundary CTA the tied tokens are
 //            ranked across warps and lanes.
-//   output   after a second cluster barrier each CTA knows the selected count
-//            of the ranks before it, so it writes its tokens straight into one
-//            flat ascending list per query head; rank 0 writes the count (and,
-//            when asked, pads the list with -1).
+//   output   the lane writes its tokens straight into one flat ascending list per
+//            query head and drops each distance line from L2 without writing it
+//            back; rank 0 writes the count (and, when asked, pads the list with -1).
 #include <cooperative_groups.h>
 
 #include "ha_internal.cuh"
@@ -41,7 +42,6 @@ namespace cg = cooperative_groups;
 namespace ha {
 namespace {
 
-constexpr int kPadWords = 36;            // shared pitch of a 32-token lane block (32 words + 4 pad)
 
 __device__ __forceinline__ uint32_t warp_sum_u(uint32_t v) {
 #pragma unroll
@@ -69,6 +69,8 @@ __device__ __forceinline__ uint32_t half_field(uint32_t w01, uint32_t w23, int e
     const uint32_t w = (e < 2) ? w01 : w23;
     return (e & 1) ? (w >> 16) : (w & 0xffffu);
 }
+
+constexpr int kBlockWords = 36;  // shared words per 32-token block of packed distances
 
 // Bits [0, k) set, k clamped to [0, 32].
 __device__ __forceinline__ uint32_t low_bits(int k) {
@@ -107,20 +109,6 @@ __device__ __forceinline__ uint32_t thresh_word(const int (&T)[4], int nh) {
     return w;
 }
 
-// The 32 packed distance words of this lane's block (the warp's blocks are 32 w .. 32 w + 31).
-__device__ __forceinline__ void load_block(const uint32_t* sD, int warp, uint32_t (&D)[32]) {
-    const int lane = threadIdx.x & 31;
-    const uint4* src = reinterpret_cast<const uint4*>(sD + (warp * 32 + lane) * kPadWords);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const uint4 v = src[j];
-        D[4 * j + 0] = v.x;
-        D[4 * j + 1] = v.y;
-        D[4 * j + 2] = v.z;
-        D[4 * j + 3] = v.w;
-    }
-}
-
 // Keep the first q set bits of x (q >= 0).
 __device__ __forceinline__ uint32_t first_bits(uint32_t x, int q) {
     uint32_t keep = 0u;
@@ -133,24 +121,29 @@ __device__ __forceinline__ uint32_t first_bits(uint32_t x, int q) {
     return keep;
 }
 
-// NT threads per CTA; a CTA covers R = 32 NT tokens: warp w owns the 1024
-// consecutive tokens [w 1024, (w + 1) 1024) of the range and lane l of it the 32
-// tokens of block 32 w + l.
-template <int NT>
-__global__ void __launch_bounds__(NT, 1024 / NT) k_select_cl(const ClSelectParams p) {
+// A CTA of NT threads covers R = 32 NT LB tokens of one (batch entry, KV head):
+// warp w owns [w 1024 LB, (w + 1) 1024 LB) of the range and lane l of it the LB
+// consecutive 32-token blocks from w 1024 LB + 32 LB l. The packed distances of
+// the range stay in shared memory, 36 words per 32-token block (the 4 spare words
+// keep both the phase-1 stores and the per-lane block reads free of bank conflicts).
+template <int NT, int LB>
+__global__ void __launch_bounds__(NT, (NT >= 1024 || LB > 1) ? 1 : 1024 / NT) k_select_cl(const ClSelectParams p) {
     constexpr int NW = NT / 32;
-    constexpr int R = 32 * NT;
+    constexpr int R = 32 * NT * LB;
     constexpr int NR = R / (4 * NT);   // phase-1 rounds of 4 tokens per thread
     constexpr int U = 4;               // rounds of codes in flight per thread
-    extern __shared__ __align__(16) uint32_t sD[];  // [R / 32][kPadWords] packed distances
+    extern __shared__ __align__(16) uint32_t sD[];  // [R / 32][kBlockWords]
     __shared__ uint32_t hist[HA_NBINS][2][32];      // lane columns; heads 2k, 2k+1 in 16-bit fields
-    // Read by the whole cluster: per head, the histogram of this CTA's tokens and
-    // of the two window parts of its range (the sink part is a prefix of the
-    // range, the local part a suffix); entry 33 of a window histogram holds its
-    // token count.
+    // Per head, the histogram of this CTA's tokens and of the two window parts of
+    // its range (the sink part is a prefix of the range, the local part a suffix)
     __shared__ uint32_t s_hc[4][HA_NBINS + 3];
     __shared__ uint32_t s_hp[4][HA_NBINS + 3];
     __shared__ uint32_t s_hs[4][HA_NBINS + 3];
+    // Read by the whole cluster: the same three as exclusive prefix sums,
+    // c[u] = tokens at distances below u, u = 0 .. 33 (c[33] = all of them)
+    __shared__ uint32_t s_ca[4][HA_NBINS + 3];
+    __shared__ uint32_t s_cp[4][HA_NBINS + 3];
+    __shared__ uint32_t s_cs[4][HA_NBINS + 3];
     __shared__ int s_wt[4][NW];                     // ties per warp (the head's boundary CTA)
     __shared__ int s_wc[4][NW];                     // selected tokens per warp
     __shared__ int s_t[4], s_mode[4], s_q[4], s_base[4], s_all[4], s_cnt[4];
@@ -199,8 +192,8 @@ __global__ void __launch_bounds__(NT, 1024 / NT) k_select_cl(const ClSelectParam
             return c;
         };
         auto compute = [&](const uint4 c4, int k) {
-            const int o = k * 4 * NT + 4 * tid;  // offset in the range
-            const int i = lo + o;
+            const int i = lo + k * 4 * NT + 4 * tid;
+            if (i >= hi) return;
             const uint32_t code[4] = {c4.x, c4.y, c4.z, c4.w};
             uint32_t pk[4];
 #pragma unroll
@@ -218,7 +211,8 @@ __global__ void __launch_bounds__(NT, 1024 / NT) k_select_cl(const ClSelectParam
                 }
                 pk[j] = w;
             }
-            *reinterpret_cast<uint4*>(sD + (o >> 5) * kPadWords + (o & 31)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            const int o = i - lo;  // 4-aligned: the four words stay in one block
+            *reinterpret_cast<uint4*>(sD + (o >> 5) * kBlockWords + (o & 31)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         };
 #pragma unroll
         for (int k = 0; k < NR + U; ++k) {
@@ -226,7 +220,7 @@ __global__ void __launch_bounds__(NT, 1024 / NT) k_select_cl(const ClSelectParam
             if (k < NR) v[k % U] = load(k);
         }
     }
-    __syncthreads();
+    __syncthreads();  // the range's distances are in shared memory
     // lane columns -> this CTA's histogram
     for (int u = warp; u < HA_NBINS; u += NW) {
         const uint32_t s01 = warp_sum_u(hist[u][0][lane]);
@@ -239,18 +233,33 @@ __global__ void __launch_bounds__(NT, 1024 / NT) k_select_cl(const ClSelectParam
         const int na = max(0, a1 - a0), nb = max(0, b1 - b0);
         for (int x = tid; x < na + nb; x += NT) {
             const int o = (x < na ? a0 + x : b0 + (x - na)) - lo;
-            const uint32_t w = sD[(o >> 5) * kPadWords + (o & 31)];
+            const uint32_t w = sD[(o >> 5) * kBlockWords + (o & 31)];
             uint32_t(*hw)[HA_NBINS + 3] = (x < na) ? s_hp : s_hs;
 #pragma unroll
             for (int e = 0; e < 4; ++e)
                 if (e < nh) atomicAdd(&hw[e][(w >> (8 * e)) & 0xffu], 1u);
         }
-        if (tid < nh) {
-            s_hp[tid][HA_NBINS] = (uint32_t)na;
-            s_hs[tid][HA_NBINS] = (uint32_t)nb;
+    }
+    __syncthreads();
+    // exclusive prefix sums over the 33 bins, one warp per (head, histogram)
+    for (int job = warp; job < 3 * nh; job += NW) {
+        const int e = job % nh, which = job / nh;
+        const uint32_t* hsrc = (which == 0) ? s_hc[e] : (which == 1 ? s_hp[e] : s_hs[e]);
+        uint32_t* cdst = (which == 0) ? s_ca[e] : (which == 1 ? s_cp[e] : s_cs[e]);
+        const uint32_t v = hsrc[lane];
+        uint32_t x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        cdst[lane] = x - v;
+        if (lane == 31) {
+            cdst[32] = x;
+            cdst[33] = x + hsrc[32];
         }
     }
-    cluster.sync();  // every CTA's histograms are complete and visible to the cluster
+    cluster.sync();  // every CTA's prefix sums are complete and visible to the cluster
 
     // ---------------------------------------------------------------- meta
     // Per head: the threshold bin t and the ties still to take over the whole
@@ -283,27 +292,21 @@ __global__ void __launch_bounds__(NT, 1024 / NT) k_select_cl(const ClSelectParam
         }
         const int nwin = wlo + (n - wmid);
         const int k = p.excl ? min(mb, n - nwin) : min(mb, n);
-        // bin `lane` of every rank, all loads in flight together (bin 32 is implied by the total)
-        uint32_t hr[kClMax], np[kClMax], ns[kClMax];
+        // bin `lane` summed over the cluster, every load in flight together (bin 32
+        // is implied by the total)
+        uint32_t tot = 0u;
 #pragma unroll
         for (int r = 0; r < kClMax; ++r) {
-            hr[r] = np[r] = ns[r] = 0u;
             if (r < CL) {
-                hr[r] = cluster.map_shared_rank(&s_hc[e][0], r)[lane];
-                np[r] = cluster.map_shared_rank(&s_hp[e][0], r)[HA_NBINS];
-                ns[r] = cluster.map_shared_rank(&s_hs[e][0], r)[HA_NBINS];
+                const uint32_t* ca = cluster.map_shared_rank(&s_ca[e][0], r);
+                tot += ca[lane + 1] - ca[lane];
+                if (p.excl) {
+                    const uint32_t* cp = cluster.map_shared_rank(&s_cp[e][0], r);
+                    const uint32_t* cs = cluster.map_shared_rank(&s_cs[e][0], r);
+                    tot -= (cp[lane + 1] - cp[lane]) + (cs[lane + 1] - cs[lane]);
+                }
             }
         }
-        uint32_t tot = 0u;
-        if (p.excl) {
-#pragma unroll
-            for (int r = 0; r < kClMax; ++r) {
-                if (r < CL && np[r] + ns[r] != 0u)
-                    tot -= cluster.map_shared_rank(&s_hp[e][0], r)[lane] + cluster.map_shared_rank(&s_hs[e][0], r)[lane];
-            }
-        }
-#pragma unroll
-        for (int r = 0; r < kClMax; ++r) tot += hr[r];
         uint32_t incl = tot;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -313,47 +316,41 @@ __global__ void __launch_bounds__(NT, 1024 / NT) k_select_cl(const ClSelectParam
         const unsigned reach = __ballot_sync(0xffffffffu, incl >= (uint32_t)k);
         const int t = reach ? (__ffs(reach) - 1) : 32;
         const uint32_t below = __shfl_sync(0xffffffffu, incl, (t == 0 ? 0 : t - 1) & 31);
-        int left = k - (t == 0 ? 0 : (int)below);  // ties still to take, in token order
-        int base = 0, all = 0, my_q = 0, my_T = 0, my_cnt = 0;
-#pragma unroll
-        for (int r = 0; r < kClMax; ++r) {
-            if (r < CL) {
-                const uint32_t* hc = cluster.map_shared_rank(&s_hc[e][0], r);
-                const int A = (int)warp_sum_u(lane < t ? hr[r] : 0u);
-                int T = (t < 32) ? (int)__shfl_sync(0xffffffffu, hr[r], t) : (int)hc[32];
-                int Pl = 0, Pt = 0, Sl = 0, St = 0;
-                if (np[r] + ns[r] != 0u) {
-                    const uint32_t* hp = cluster.map_shared_rank(&s_hp[e][0], r);
-                    const uint32_t* hs = cluster.map_shared_rank(&s_hs[e][0], r);
-                    const uint32_t pv = hp[lane], sv = hs[lane];
-                    Pl = (int)warp_sum_u(lane < t ? pv : 0u);
-                    Sl = (int)warp_sum_u(lane < t ? sv : 0u);
-                    Pt = (t < 32) ? (int)__shfl_sync(0xffffffffu, pv, t) : (int)hp[32];
-                    St = (t < 32) ? (int)__shfl_sync(0xffffffffu, sv, t) : (int)hs[32];
-                }
-                if (p.excl) T -= Pt + St;
-                const int qr = min(max(left, 0), T);
-                left -= T;
-                int c;
-                if (p.excl) {
-                    c = (A - Pl - Sl) + qr + (int)np[r] + (int)ns[r];
-                } else {
-                    c = A + ((int)np[r] - Pl) + ((int)ns[r] - Sl) + qr - min(qr, Pt) - max(0, qr - (T - St));
-                }
-                if (r < rank) base += c;
-                if (r == rank) {
-                    my_q = qr;
-                    my_T = T;
-                    my_cnt = c;
-                }
-                all += c;
-            }
+        const int rq = k - (t == 0 ? 0 : (int)below);  // ties to take over the whole sequence, in token order
+        // lane r: rank r's counts at t, its share of the ties and its selected tokens
+        int A = 0, T = 0, Pl = 0, Pt = 0, NP = 0, Sl = 0, St = 0, NS = 0;
+        if (lane < CL) {
+            const uint32_t* ca = cluster.map_shared_rank(&s_ca[e][0], lane);
+            const uint32_t* cp = cluster.map_shared_rank(&s_cp[e][0], lane);
+            const uint32_t* cs = cluster.map_shared_rank(&s_cs[e][0], lane);
+            A = (int)ca[t];
+            T = (int)ca[t + 1] - A;
+            Pl = (int)cp[t];
+            Pt = (int)cp[t + 1] - Pl;
+            NP = (int)cp[HA_NBINS];
+            Sl = (int)cs[t];
+            St = (int)cs[t + 1] - Sl;
+            NS = (int)cs[HA_NBINS];
         }
+        if (p.excl) T -= Pt + St;
+        int tsum;
+        const int qr = min(max(rq - warp_excl_scan(T, &tsum), 0), T);
+        int c = 0;
+        if (lane < CL) {
+            c = p.excl ? (A - Pl - Sl) + qr + NP + NS
+                       : A + (NP - Pl) + (NS - Sl) + qr - min(qr, Pt) - max(0, qr - (T - St));
+        }
+        int all;
+        const int base = warp_excl_scan(c, &all);
+        const int my_q = __shfl_sync(0xffffffffu, qr, rank & 31);
+        const int my_T = __shfl_sync(0xffffffffu, T, rank & 31);
+        const int my_base = __shfl_sync(0xffffffffu, base, rank & 31);
+        const int my_cnt = __shfl_sync(0xffffffffu, c, rank & 31);
         if (lane == 0) {
             s_t[e] = t;
             s_q[e] = my_q;
             s_mode[e] = (my_q <= 0) ? 0 : (my_q >= my_T ? 1 : 2);
-            s_base[e] = base;
+            s_base[e] = my_base;
             s_all[e] = all;
             s_cnt[e] = my_cnt;
         }
@@ -362,9 +359,8 @@ __global__ void __launch_bounds__(NT, 1024 / NT) k_select_cl(const ClSelectParam
     __syncthreads();
 
     // ---------------------------------------------------------------- selection masks
-    int mode[4];
+    int mode[4], T[4], Tm1[4];
     bool any2 = false;
-    int Tm1[4], T[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
         T[e] = (e < nh) ? s_t[e] : 0;
@@ -372,50 +368,96 @@ __global__ void __launch_bounds__(NT, 1024 / NT) k_select_cl(const ClSelectParam
         mode[e] = (e < nh) ? s_mode[e] : 0;
         any2 = any2 || mode[e] == 2;
     }
-    const int lbase = lo + (warp * 32 + lane) * 32;  // this lane's 32 tokens
-    const uint32_t win = low_bits(wlo - lbase) | ~low_bits(wmid - lbase);
-    const uint32_t valid = low_bits(n - lbase);
-    uint32_t msk[4];
-    {
+    const uint32_t TLT = thresh_word(Tm1, nh), TLE = thresh_word(T, nh);
+    const int lane0 = lo + warp * 1024 * LB + lane * 32 * LB;  // this lane's first token
+    // masks of block k of this lane: lt (distance < t), le (distance <= t), the
+    // windows and the valid tokens; false when the block lies past the sequence
+    auto block = [&](int k, uint32_t (&lt)[4], uint32_t (&le)[4], uint32_t& win, uint32_t& valid) {
+        const int lb = lane0 + 32 * k;
+        valid = low_bits(n - lb);
+        win = low_bits(wlo - lb) | ~low_bits(wmid - lb);
+        if (valid == 0u) return false;
         uint32_t D[32];
-        load_block(sD, warp, D);
-        uint32_t lt[4], le[4];
-        le_masks(D, thresh_word(Tm1, nh), lt);
-        le_masks(D, thresh_word(T, nh), le);
+        const uint4* src = reinterpret_cast<const uint4*>(sD + ((lb - lo) >> 5) * kBlockWords);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) msk[e] = (mode[e] == 1) ? le[e] : lt[e];
-        if (any2) {
-            // the boundary CTA of a head: its tied tokens, ranked in token order
-            uint32_t eq[4];
+        for (int j = 0; j < 8; ++j) {
+            const uint4 v = src[j];
+            D[4 * j + 0] = v.x;
+            D[4 * j + 1] = v.y;
+            D[4 * j + 2] = v.z;
+            D[4 * j + 3] = v.w;
+        }
+        le_masks(D, TLT, lt);
+        le_masks(D, TLE, le);
+        return true;
+    };
+    // tied tokens (distance t) of a block that may be taken
+    auto ties = [&](int e, const uint32_t (&lt)[4], const uint32_t (&le)[4], uint32_t win, uint32_t valid) {
+        uint32_t eq = le[e] & ~lt[e] & valid;
+        if (p.excl) eq &= ~win;
+        return eq;
+    };
+    int qrem[4] = {0, 0, 0, 0};  // ties this lane still takes (the head's boundary CTA)
+    if (any2) {
+        int tl[4] = {0, 0, 0, 0};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                eq[e] = 0u;
-                if (mode[e] == 2) {
-                    eq[e] = le[e] & ~lt[e] & valid;
-                    if (p.excl) eq[e] &= ~win;
-                    const uint32_t c = warp_sum_u((uint32_t)__popc(eq[e]));
-                    if (lane == 0) s_wt[e][warp] = (int)c;
-                }
+        for (int k = 0; k < LB; ++k) {
+            uint32_t lt[4], le[4], win, valid;
+            if (!block(k, lt, le, win, valid)) continue;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (mode[e] == 2) tl[e] += __popc(ties(e, lt, le, win, valid));
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (mode[e] == 2) {
+                int tot;
+                qrem[e] = -warp_excl_scan(tl[e], &tot);
+                if (lane == 0) s_wt[e][warp] = tot;
             }
-            __syncthreads();
+        }
+        __syncthreads();
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (mode[e] == 2) {
+                int qw = s_q[e];
+                for (int w2 = 0; w2 < warp; ++w2) qw -= s_wt[e][w2];
+                qrem[e] += qw;
+            }
+        }
+    }
+    // the final mask of head e for a block, taking this lane's ties in token order
+    auto final_mask = [&](int e, const uint32_t (&lt)[4], const uint32_t (&le)[4], uint32_t win, uint32_t valid,
+                          int (&q)[4]) {
+        uint32_t m = (mode[e] == 1) ? le[e] : lt[e];
+        if (mode[e] == 2) {
+            const uint32_t take = first_bits(ties(e, lt, le, win, valid), q[e]);
+            q[e] -= __popc(take);
+            m |= take;
+        }
+        return (m | win) & valid;
+    };
+    // final masks of the lane's blocks, kept for the output
+    uint32_t keep[LB][4];
+    int cnt[4] = {0, 0, 0, 0};
+    {
+        int q[4] = {qrem[0], qrem[1], qrem[2], qrem[3]};
+#pragma unroll
+        for (int k = 0; k < LB; ++k) {
+            uint32_t lt[4], le[4], win, valid;
+            const bool any = block(k, lt, le, win, valid);
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                if (mode[e] == 2) {
-                    int qw = s_q[e];
-                    for (int w2 = 0; w2 < warp; ++w2) qw -= s_wt[e][w2];
-                    int tot;
-                    const int ex = warp_excl_scan(__popc(eq[e]), &tot);
-                    msk[e] |= first_bits(eq[e], qw - ex);
-                }
+                keep[k][e] = (any && e < nh) ? final_mask(e, lt, le, win, valid, q) : 0u;
+                cnt[e] += __popc(keep[k][e]);
             }
         }
     }
     int pos[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        msk[e] = (e < nh) ? ((msk[e] | win) & valid) : 0u;
         int tot;
-        pos[e] = warp_excl_scan(__popc(msk[e]), &tot);
+        pos[e] = warp_excl_scan(cnt[e], &tot);
         if (lane == 0) s_wc[e][warp] = tot;
     }
     __syncthreads();
@@ -425,31 +467,39 @@ __global__ void __launch_bounds__(NT, 1024 / NT) k_select_cl(const ClSelectParam
         if (mine != s_cnt[tid]) flag_error(p.err, HA_DEVERR_STATE);  // the masks disagree with the counts
     }
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
+    for (int e = 0; e < 4; ++e) {
+        pos[e] += s_base[e];
         for (int w2 = 0; w2 < warp; ++w2) pos[e] += s_wc[e][w2];
+    }
 
     // ---------------------------------------------------------------- output
     const int cap = p.cap;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        if (e < nh) {
-            uint32_t m = msk[e];
-            int at = s_base[e] + pos[e];
-            int32_t* dst = p.list + (int64_t)(head0 + e) * cap;
-            if (at + __popc(m) > cap) {
-                flag_error(p.err, HA_DEVERR_STATE);
-                m = 0u;
-            }
-            if (__popc(m) >= 8) {
-                // dense (window) lanes: independent stores instead of a serial bit walk
+    for (int k = 0; k < LB; ++k) {
+        const int lb = lane0 + 32 * k;
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if ((m >> j) & 1u) dst[at + __popc(m & ((1u << j) - 1u))] = lbase + j;
-            } else {
-                while (m != 0u) {
-                    const int j = __ffs(m) - 1;
-                    m &= m - 1u;
-                    dst[at++] = lbase + j;
+        for (int e = 0; e < 4; ++e) {
+            if (e < nh) {
+                uint32_t m = keep[k][e];
+                int32_t* dst = p.list + (int64_t)(head0 + e) * cap;
+                const int at = pos[e];
+                pos[e] += __popc(m);
+                if (at + __popc(m) > cap) {
+                    flag_error(p.err, HA_DEVERR_STATE);
+                    m = 0u;
+                }
+                if (__popc(m) >= 8) {
+                    // dense (window) blocks: independent stores instead of a serial bit walk
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if ((m >> j) & 1u) dst[at + __popc(m & ((1u << j) - 1u))] = lb + j;
+                } else {
+                    int a = at;
+                    while (m != 0u) {
+                        const int j = __ffs(m) - 1;
+                        m &= m - 1u;
+                        dst[a++] = lb + j;
+                    }
                 }
             }
         }
@@ -471,20 +521,14 @@ __global__ void __launch_bounds__(NT, 1024 / NT) k_select_cl(const ClSelectParam
     cluster.barrier_wait();  // no CTA leaves while another may still read its shared memory
 }
 
-}  // namespace
-
-size_t cl_select_smem(int rmax) { return (size_t)(rmax / 32) * kPadWords * 4; }
-
-template <int NT>
+template <int NT, int LB>
 cudaError_t launch_cl_t(const ClSelectParams& p, int batch_hkv, cudaStream_t st) {
-    const size_t smem = cl_select_smem(32 * NT);
-    static int s_smem_set = 0;
-    if ((int)smem > s_smem_set) {
-        const cudaError_t e =
-            cudaFuncSetAttribute(k_select_cl<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        s_smem_set = (int)smem;
-    }
+    const size_t smem = cl_select_smem(32 * NT * LB);
+    // function attributes belong to the current device's context: set them on every launch
+    cudaError_t e = cudaFuncSetAttribute(k_select_cl<NT, LB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess && p.CL > 8)
+        e = cudaFuncSetAttribute(k_select_cl<NT, LB>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)batch_hkv * (unsigned)p.CL);
     cfg.blockDim = dim3(NT);
@@ -497,14 +541,18 @@ cudaError_t launch_cl_t(const ClSelectParams& p, int batch_hkv, cudaStream_t st)
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_select_cl<NT>, p);
+    return cudaLaunchKernelEx(&cfg, k_select_cl<NT, LB>, p);
 }
+
+}  // namespace
+
+size_t cl_select_smem(int rmax) { return (size_t)(rmax / 32) * kBlockWords * 4; }
 
 cudaError_t launch_select_cl(const ClSelectParams& p, int batch_hkv, cudaStream_t st) {
     switch (p.rmax) {
-        case 32 * 256: return launch_cl_t<256>(p, batch_hkv, st);
-        case 32 * 512: return launch_cl_t<512>(p, batch_hkv, st);
-        case 32 * 1024: return launch_cl_t<1024>(p, batch_hkv, st);
+        case 8192: return launch_cl_t<256, 1>(p, batch_hkv, st);
+        case 16384: return launch_cl_t<512, 1>(p, batch_hkv, st);
+        case 32768: return launch_cl_t<512, 2>(p, batch_hkv, st);
         default: return cudaErrorInvalidValue;
     }
 }
