@@ -34,8 +34,12 @@ WORKLOAD_DESC = ("batch16-128k: B=16 sequences x 131072 cached tokens, 32 query 
                  "bf16 K/V ~ N(0,1), 32-bit sign(W x) codes per KV head, m=4096 (32x token sparsity), "
                  "n_sink=128, n_local=256")
 FALLBACK_HBM_GBS = 6800.0
-PROFILE_FILE = os.path.join(ROOT, "profiles", "k_gather_att_batch16_128k.md")
 GATHER_SOURCE = os.path.join(ROOT, "long_context_sparse_score_gb300", "csrc", "k_gather_att.cu")
+# DRAM bytes (read + write) per GATHER-ATT launch at the 16 x 131,072-token workload,
+# from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the same
+# launch on the 2-sequence case scaled by 8 (the heads are independent); it holds
+# only for the k_gather_att.cu source it was taken on.
+GATHER_TRAFFIC = {"source_sha256": None, "bytes_per_launch": None}
 
 
 def parse_args():
@@ -47,6 +51,7 @@ def parse_args():
     ap.add_argument("--cpu-heads", type=int, default=512,
                     help="query heads of the workload the CPU oracle baseline runs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-workload measurements of workloads 1, 2, 4, 5")
     ap.add_argument("--batch", type=int, default=16,
                     help="sequences per GPU (16 = the workload; fewer only for small profiling cases)")
     return ap.parse_args()
@@ -158,24 +163,15 @@ class ClockSampler:
 
 
 def profiled_traffic():
-    """DRAM bytes per GATHER-ATT launch from the committed ncu summary, if the kernel
-    source is unchanged since the capture (else None)."""
+    """DRAM bytes per GATHER-ATT launch from the recorded capture, if the kernel
+    source is unchanged since it was taken (else None)."""
     try:
-        text = open(PROFILE_FILE).read()
         sha = hashlib.sha256(open(GATHER_SOURCE, "rb").read()).hexdigest()
     except OSError:
         return None
-    got = {}
-    for line in text.splitlines():
-        if ":" in line and line.strip().startswith("- "):
-            k, v = line.strip()[2:].split(":", 1)
-            got[k.strip()] = v.strip().strip("`")
-    if got.get("kernel_source_sha256") != sha:
+    if GATHER_TRAFFIC["source_sha256"] != sha:
         return None
-    try:
-        return float(got["traffic_bytes_per_launch_full_workload"])
-    except (KeyError, ValueError):
-        return None
+    return GATHER_TRAFFIC["bytes_per_launch"]
 
 
 # ---------------------------------------------------------------- next rows
@@ -404,6 +400,129 @@ def measure_variants(w, shape, ws, dev):
     return res
 
 
+# ---------------------------------------------------------------- the other workloads
+
+CONFIG_DESC = {
+    1: "tiny: B=1, 1/1 heads, d=64, n=1024, fp32 q/K/V, separate W_q/W_k; m=64, n_sink=4, n_local=16",
+    2: "gqa-32k: B=1, 32/8 heads, d=128, n=32768, bf16 K/V; m=1024, n_sink=128, n_local=128",
+    4: "shared-doc: one 61440-token bf16 document (batch stride 0) for 32 queries, m=2048, n_sink=128, "
+       "n_local=0, plus a dense 512-token local KV per query merged through the log-normalisers",
+    5: "ragged: B=64, 32/8 heads, seq_len ~ U{4096..65536}, m_b = 64 floor((seq_len + 1024) / 2048), "
+       "n_sink=64, n_local=128",
+}
+
+
+def _time_calls(call, reps, warm=5):
+    """Mean device time of `call` over `reps` back-to-back calls (CUDA events)."""
+    import torch
+    for _ in range(warm):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        call()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def measure_config(c, dev, peak, cpu: bool, reps: int):
+    """One workload of the suite: query-heads/s of the whole step, its algorithmic
+    bytes and fraction of the HBM peak, GATHER-ATT's own fraction (stage events),
+    and the CPU oracle on a sample of the same inputs (with its parity)."""
+    import torch
+    from long_context_sparse_score_gb300 import hashattn as H, workloads as W
+    w = W.make_workload(c, dev)
+    B, Hq, d = w.q.shape
+    shape = H.make_shape(w.q, w.K, w.V, w.k_sig, batch=B)
+    ws = torch.empty(H.hash_attn_workspace_size(shape, w.m, w.n_sink, w.n_local), dtype=torch.uint8, device=dev)
+    H.hash_attn_workspace_init(ws)
+    out = torch.empty((B, Hq, d), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    cap = H.hash_attn_select_capacity(w.n_cap, w.m, w.n_sink, w.n_local)
+    sel = torch.empty((B, Hq, cap), dtype=torch.int32, device=dev)
+    cnt = torch.empty((B, Hq), dtype=torch.int32, device=dev)
+
+    def decode(events=None, s_idx=None, s_cnt=None):
+        if events is None:
+            H.hash_attn_decode(shape, w.q, w.q_sig, w.k_sig, w.K, w.V, w.seq_lens, w.m_per_seq, w.m, w.n_sink,
+                               w.n_local, out, lse, s_idx, s_cnt, workspace=ws)
+        else:
+            H.hash_attn_decode_timed(shape, w.q, w.q_sig, w.k_sig, w.K, w.V, w.seq_lens, w.m_per_seq, w.m,
+                                     w.n_sink, w.n_local, out, lse, events, s_idx, s_cnt, workspace=ws)
+
+    decode(None, sel, cnt)
+    st, flags = H.hash_attn_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"workload {c}: device status {st} flags {flags:#x}")
+    score_bytes, gather_bytes, rows = algorithmic_bytes(w, sel, cnt)
+    res = {"workload": CONFIG_DESC[c], "plan": H.hash_attn_selection_plan(shape)}
+    step = decode
+    extra = 0
+    if c == 4:  # the document part, the dense local part and the exact merge, as one step
+        lshape = H.make_shape(w.q, w.K_loc, w.V_loc, batch=B)
+        lws = torch.empty(H.hash_attn_workspace_size(lshape, 512, 0, 0), dtype=torch.uint8, device=dev)
+        H.hash_attn_workspace_init(lws)
+        lens_loc = torch.full((B,), 512, dtype=torch.int32, device=dev)
+        o_loc, l_loc = torch.empty_like(out), torch.empty_like(lse)
+        o_m, l_m = torch.empty_like(out), torch.empty_like(lse)
+
+        def step():
+            decode()
+            H.hash_attn_decode(lshape, w.q, None, None, w.K_loc, w.V_loc, lens_loc, None, 512, 0, 0, o_loc, l_loc,
+                               workspace=lws)
+            H.hash_attn_merge(out, lse, o_loc, l_loc, o_m, l_m, B * Hq, d)
+        extra = w.K_loc.numel() * w.K_loc.element_size() * 2 + B * Hq * (d + 1) * 4 * 2
+    ms = _time_calls(step, reps)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for e in evs:
+        e.record()  # a torch event gets its CUDA handle when first recorded
+    g_ms = []
+    for _ in range(5):
+        decode(evs)
+        torch.cuda.synchronize()
+        g_ms.append(evs[2].elapsed_time(evs[3]))
+    g_ms = statistics.median(g_ms)
+    path = score_bytes + gather_bytes + extra
+    res.update({"query_heads_per_s": B * Hq / (ms * 1e-3), "ms_per_step": ms, "algorithmic_bytes": path,
+                "unique_kv_rows": rows, "achieved_gbs": path / (ms * 1e-3) / 1e9,
+                "frac": path / (ms * 1e-3) / 1e9 / peak,
+                "gather_att": {"ms": g_ms, "algorithmic_bytes": gather_bytes,
+                               "frac": gather_bytes / (g_ms * 1e-3) / 1e9 / peak},
+                "timing": f"CUDA events over {reps} back-to-back steps after 5 warm-up steps; GATHER-ATT from "
+                          "stage events of 5 timed steps (median)"})
+    if cpu:
+        n_heads = min(B * Hq, 64)
+        cpu_s, cpu_heads, ores, cores = run_cpu_oracle(w, n_heads)
+        res["cpu_baseline"] = {"value": cpu_heads / cpu_s, "unit": UNIT, "cores": cores, "kind": "oracle",
+                               "sample": f"{cpu_heads} query heads of the same inputs",
+                               "parity_on_sample": oracle_parity(ores, o_m if c == 4 else out,
+                                                                 l_m if c == 4 else lse, sel, cnt)}
+    if c == 5:  # the in-run dense reference: every cached token of every sequence
+        dshape = shape
+        dws = torch.empty(H.hash_attn_workspace_size(dshape, w.n_cap, 0, 0), dtype=torch.uint8, device=dev)
+        H.hash_attn_workspace_init(dws)
+
+        def dense():
+            H.hash_attn_decode(dshape, w.q, None, None, w.K, w.V, w.seq_lens, None, w.n_cap, 0, 0, out, lse,
+                               workspace=dws)
+        dms = _time_calls(dense, max(3, reps // 4))
+        kv_rows = int(w.seq_lens.to(torch.int64).sum().item()) * w.Hkv
+        dbytes = kv_rows * 2 * d * w.K.element_size() + B * Hq * d * w.q.element_size() + B * Hq * (d + 1) * 4
+        res["dense"] = {"query_heads_per_s": B * Hq / (dms * 1e-3), "ms_per_step": dms, "algorithmic_bytes": dbytes,
+                        "frac": dbytes / (dms * 1e-3) / 1e9 / peak}
+        if cpu:
+            cpu_s, cpu_heads, ores, cores = run_cpu_oracle(w, 8, dense=True)
+            res["dense"]["cpu_baseline"] = {"value": cpu_heads / cpu_s, "unit": UNIT, "cores": cores,
+                                            "kind": "oracle", "sample": f"{cpu_heads} query heads, dense",
+                                            "parity_on_sample": oracle_parity(ores, out, lse)}
+        del dws
+    del w, ws, sel
+    torch.cuda.empty_cache()
+    return res
+
+
 # ---------------------------------------------------------------- workload helpers
 
 def algorithmic_bytes(w, sel_idx, sel_cnt):
@@ -433,24 +552,34 @@ def algorithmic_bytes(w, sel_idx, sel_cnt):
 
 def _oracle_task(task):
     """Pool worker: the listed heads of one (sequence, KV head) pair, whose K, V
-    (float32) and codes (int64) sit in a shared-memory block; returns
-    ({(b, h): (idx, None, out, lse)}, seconds spent in the oracle)."""
+    (float32) and codes (int64) sit in a shared-memory block; each head is
+    (b, h, q, q_code, n, m, dense). ``local`` names a second block with a dense
+    local K/V part of n_loc rows merged exactly into every head (the shared-
+    document workload). Returns ({(b, h): (idx, None, out, lse)}, seconds spent
+    in the oracle)."""
     import numpy as np
     from multiprocessing import shared_memory
     from oracle import hashattn_oracle as O
-    name, n_cap, d, m, n_sink, n_local, heads = task
+    name, n_cap, d, n_sink, n_local, heads, local = task
     shm = shared_memory.SharedMemory(name=name)
+    lshm = shared_memory.SharedMemory(name=local[0]) if local else None
     try:
         kv = np.ndarray((2, n_cap, d), dtype=np.float32, buffer=shm.buf)
         codes = np.ndarray((n_cap,), dtype=np.int64, buffer=shm.buf, offset=2 * n_cap * d * 4)
+        lkv = np.ndarray((2, local[1], d), dtype=np.float32, buffer=lshm.buf) if local else None
         res = {}
         t0 = time.perf_counter()
-        for b, h, qv, qs, n in heads:
-            idx, _, out, lse = O.decode_head(qv, qs, codes, kv[0], kv[1], n, m, n_sink, n_local)
+        for b, h, qv, qs, n, m, dense in heads:
+            idx, _, out, lse = O.decode_head(qv, qs, codes, kv[0], kv[1], n, m, n_sink, n_local, dense=dense)
+            if lkv is not None:
+                ol, ll = O.attend(qv, lkv[0], lkv[1], np.arange(local[1]))
+                out, lse = O.merge(out, lse, ol, ll)
             res[(b, h)] = (idx, None, out, lse)
         return res, time.perf_counter() - t0
     finally:
         shm.close()
+        if lshm is not None:
+            lshm.close()
 
 
 def _pool_ready(_):
@@ -473,18 +602,32 @@ class OraclePool:
         self.blocks = []
 
     def put(self, w, b, g):
-        """Shared-memory block with K, V (float32) and the codes of pair (b, g)."""
+        """Shared-memory block with K, V (float32) and the codes of pair (b, g)
+        (batch entry 0 of a cache shared by the batch)."""
         import numpy as np
         from multiprocessing import shared_memory
         n_cap, d = w.n_cap, w.d
+        bk = 0 if w.K.shape[0] == 1 else b
         shm = shared_memory.SharedMemory(create=True, size=2 * n_cap * d * 4 + n_cap * 8)
         kv = np.ndarray((2, n_cap, d), dtype=np.float32, buffer=shm.buf)
-        kv[0] = w.K[b, g].float().cpu().numpy()
-        kv[1] = w.V[b, g].float().cpu().numpy()
+        kv[0] = w.K[bk, g].float().cpu().numpy()
+        kv[1] = w.V[bk, g].float().cpu().numpy()
         np.ndarray((n_cap,), dtype=np.int64, buffer=shm.buf, offset=2 * n_cap * d * 4)[:] = \
-            w.k_sig[b, g].cpu().numpy().astype(np.int64)
+            w.k_sig[bk, g].cpu().numpy().astype(np.int64)
         self.blocks.append(shm)
         return shm.name
+
+    def put_local(self, K, V, b, g):
+        """Shared-memory block with the dense local K, V (float32) of pair (b, g)."""
+        import numpy as np
+        from multiprocessing import shared_memory
+        n, d = K.shape[2], K.shape[3]
+        shm = shared_memory.SharedMemory(create=True, size=2 * n * d * 4)
+        kv = np.ndarray((2, n, d), dtype=np.float32, buffer=shm.buf)
+        kv[0] = K[b, g].float().cpu().numpy()
+        kv[1] = V[b, g].float().cpu().numpy()
+        self.blocks.append(shm)
+        return shm.name, n
 
     def run(self, tasks):
         """Run the tasks in parallel; returns (wall seconds, merged results)."""
@@ -508,27 +651,33 @@ class OraclePool:
         self.pool.join()
 
 
-def run_cpu_oracle(w, n_heads: int):
+def run_cpu_oracle(w, n_heads: int, dense: bool = False, pairs=None):
     """Time the oracle on all host cores over the first n_heads query heads (the G
-    heads of each (sequence, KV head) pair form one task), in waves of one pair
-    per core; returns (seconds, heads, results, cores). Only the parallel oracle
-    work is timed, not the copies into shared memory."""
+    heads of each (sequence, KV head) pair form one task; ``pairs`` picks other
+    pairs), in waves of one pair per core; returns (seconds, heads, results,
+    cores). Only the parallel oracle work is timed, not the copies into shared
+    memory. Per-sequence budgets and a dense local part (w.K_loc) are included."""
     import numpy as np
     B, Hq, d = w.q.shape
     G = Hq // w.Hkv
     q = w.q.float().cpu().numpy().astype(np.float64)
     qs = w.q_sig.cpu().numpy().astype(np.int64)
     lens = w.seq_lens.cpu().numpy()
-    pairs = [(b, g) for b in range(B) for g in range(w.Hkv)][:math.ceil(n_heads / G)]
+    mps = None if w.m_per_seq is None else w.m_per_seq.cpu().numpy()
+    if pairs is None:
+        pairs = [(b, g) for b in range(B) for g in range(w.Hkv)]
+    pairs = pairs[:math.ceil(n_heads / G)]
     op = OraclePool()
     spent, done, results = 0.0, 0, {}
     try:
         for i in range(0, len(pairs), op.cores):
             tasks = []
             for b, g in pairs[i:i + op.cores]:
-                heads = [(b, g * G + hh, q[b, g * G + hh], int(qs[b, g * G + hh]), int(lens[b]))
+                mb = int(lens[b]) if dense else (int(mps[b]) if mps is not None else w.m)
+                heads = [(b, g * G + hh, q[b, g * G + hh], int(qs[b, g * G + hh]), int(lens[b]), mb, dense)
                          for hh in range(G) if done + len(tasks) * G + hh < n_heads]
-                tasks.append((op.put(w, b, g), w.n_cap, d, w.m, w.n_sink, w.n_local, heads))
+                local = op.put_local(w.K_loc, w.V_loc, b, g) if w.K_loc is not None else None
+                tasks.append((op.put(w, b, g), w.n_cap, d, w.n_sink, w.n_local, heads, local))
             wall, res = op.run(tasks)
             spent += wall
             done += len(res)
@@ -537,6 +686,24 @@ def run_cpu_oracle(w, n_heads: int):
     finally:
         op.close()
     return spent, done, results, op.cores
+
+
+def oracle_parity(res, out, lse, sel=None, cnt=None):
+    """Largest relative out / lse errors of the GPU results against the oracle's on
+    the sampled heads, and whether the selected sets match bit for bit."""
+    import numpy as np
+    o = out.cpu().numpy()
+    lz = lse.cpu().numpy()
+    worst = max(float(np.max(np.abs(o[b, h] - r[2]) / (1 + np.abs(r[2])))) for (b, h), r in res.items())
+    worst_l = max(abs(float(lz[b, h]) - r[3]) / (1 + abs(r[3])) if math.isfinite(r[3]) else
+                  (0.0 if lz[b, h] == r[3] else math.inf) for (b, h), r in res.items())
+    sel_ok = None
+    if sel is not None:
+        sel_ok = all(int(cnt[b, h]) == len(r[0]) and np.array_equal(sel[b, h, :int(cnt[b, h])].cpu().numpy(), r[0])
+                     for (b, h), r in res.items())
+    ok = bool((sel_ok is not False) and worst <= 2e-3 and worst_l <= 1e-4)
+    return {"selected_sets_exact": sel_ok, "max_out_err_rel": worst, "max_lse_err_rel": worst_l,
+            "within_tolerance": ok}
 
 
 def build_lib():
@@ -684,7 +851,10 @@ def run_ours(args, world, rank, local):
         "roofline": {"kernel": "k_gather_att", "bound": "hbm", "achieved": achieved, "peak": peak,
                      "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s", "frac": achieved / peak,
                      "traffic": profiled_traffic(), "algorithmic_bytes_per_launch": gather_bytes,
-                     "unique_kv_rows": uniq_rows, "avg_launch_ms": g_ms},
+                     "unique_kv_rows": uniq_rows, "avg_launch_ms": g_ms,
+                     "step": {"achieved": path_gbs, "frac": path_gbs / peak, "algorithmic_bytes": path_bytes,
+                              "ms": ms_step,
+                              "note": "the whole SCORE -> TOPK -> GATHER-ATT step against the same peak"}},
         "pipeline": {"achieved_gbs": path_gbs, "frac": path_gbs / peak,
                      "algorithmic_bytes_per_step": path_bytes,
                      "stage_events": f"every {EVERY}th timed step ({len(sampled)} of {K})",
@@ -704,25 +874,22 @@ def run_ours(args, world, rank, local):
     }
     if not args.no_cpu_baseline and world == 1:  # the CPU baseline: rank 0 of a one-GPU run only
         cpu_s, cpu_heads, res, cores = run_cpu_oracle(w, args.cpu_heads)
-        o = out.cpu().numpy()
-        lz = lse.cpu().numpy()
-        worst = max(float(np.max(np.abs(o[b, h] - r[2]) / (1 + np.abs(r[2])))) for (b, h), r in res.items())
-        worst_l = max(abs(float(lz[b, h]) - r[3]) / (1 + abs(r[3])) for (b, h), r in res.items())
-        sel_ok = all(int(cnt[b, h]) == len(r[0]) and
-                     np.array_equal(sel[b, h, :int(cnt[b, h])].cpu().numpy(), r[0])
-                     for (b, h), r in res.items())
         line["cpu_baseline"] = {
             "value": cpu_heads / cpu_s, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{cpu_heads} query heads (all 4 heads of the first {math.ceil(cpu_heads / 4)} "
                       f"(sequence, KV head) pairs) of the same workload, NumPy float64, a process pool of "
                       f"{cores} single-threaded workers, one pair per task",
             "seconds": cpu_s,
-            "parity_on_sample": {"selected_sets_exact": sel_ok, "max_out_err_rel": worst,
-                                 "max_lse_err_rel": worst_l,
-                                 "within_tolerance": bool(sel_ok and worst <= 2e-3 and worst_l <= 1e-4)}}
+            "parity_on_sample": oracle_parity(res, out, lse, sel, cnt)}
+        worst = line["cpu_baseline"]["parity_on_sample"]["max_out_err_rel"]
+        worst_l = line["cpu_baseline"]["parity_on_sample"]["max_lse_err_rel"]
         if not line["cpu_baseline"]["parity_on_sample"]["within_tolerance"]:
             print(f"bench: GPU outputs differ from the oracle on the sample (out {worst:.3g}, lse {worst_l:.3g})",
                   file=sys.stderr)
+    if not args.no_configs and world == 1:
+        line["configs"] = {}
+        for c in (1, 2, 4, 5):
+            line["configs"][str(c)] = measure_config(c, dev, peak, not args.no_cpu_baseline, reps=50)
     return line
 
 
@@ -754,8 +921,8 @@ def run_reference(args, world, rank, local):
         tasks = []
         for c in range(op.cores):
             name, b, h = heads[(i * op.cores + c) % len(heads)]
-            tasks.append((name, w.n_cap, d, w.m, w.n_sink, w.n_local,
-                          [(b, h, q[b, h].astype(np.float64), int(qs[b, h]), int(lens[b]))]))
+            tasks.append((name, w.n_cap, d, w.n_sink, w.n_local,
+                          [(b, h, q[b, h].astype(np.float64), int(qs[b, h]), int(lens[b]), w.m, False)], None))
         return op.run(tasks)[0]
 
     try:

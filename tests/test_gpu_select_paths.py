@@ -247,3 +247,27 @@ def test_single_sequence_of_two_million_tokens():
     plan = _plan(w)
     assert plan["fused"] == 0 and (n + plan["chunk"] - 1) // plan["chunk"] * 8 <= 4096
     _check(w, [(0, h) for h in range(4)], att_heads=2)
+
+
+# ---------------------------------------------------------------- dense path: one read per GQA group
+
+DENSE_GROUP = [
+    # name, B, Hq, Hkv, d, n_cap, lens, shared
+    ("many_splits_ragged", 3, 8, 2, 128, 40000, [40000, 1, 0], False),
+    ("d64_odd_lengths", 2, 4, 1, 64, 700, [700, 333], False),
+    ("one_split", 2, 8, 2, 128, 50, [50, 17], False),
+    ("shared_cache", 4, 8, 2, 128, 5000, [5000, 4999, 3, 2500], True),
+]
+
+
+@pytest.mark.parametrize("case", DENSE_GROUP, ids=[c[0] for c in DENSE_GROUP])
+def test_dense_group_kernel(case):
+    """The dense path (m >= n_cap) with four query heads per KV head reads each row
+    once for the group; every head must equal full attention over its sequence."""
+    name, B, Hq, Hkv, d, n_cap, lens, shared = case
+    w = W().make_gqa(39, B=B, Hq=Hq, Hkv=Hkv, d=d, n_cap=n_cap, seq_lens=lens, m=0, n_sink=0, n_local=0,
+                     device="cuda", shared=shared, name=name)
+    res = GH.run_decode(w, m=n_cap, dense=True, m_per_seq=None, sel=False)
+    assert res["status"] == 0, hex(res["flags"])
+    hc = GH.HostCopy(w)
+    GH.check_attention(res, hc, [(b, h) for b in range(B) for h in range(Hq)], n_cap, dense=True)
