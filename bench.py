@@ -52,6 +52,8 @@ def parse_args():
                     help="query heads of the workload the CPU oracle baseline runs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-workload measurements of workloads 1, 2, 4, 5")
+    ap.add_argument("--only-config", type=int, choices=[1, 2, 4, 5], default=None,
+                    help="measure only this workload (for profiling) and print its object")
     ap.add_argument("--batch", type=int, default=16,
                     help="sequences per GPU (16 = the workload; fewer only for small profiling cases)")
     return ap.parse_args()
@@ -949,6 +951,14 @@ def run_reference(args, world, rank, local):
 
 def main():
     args = parse_args()
+    if args.only_config is not None:
+        import torch
+        torch.cuda.set_device(0)
+        build_lib()
+        peak, _ = hbm_peak()
+        print(json.dumps(measure_config(args.only_config, torch.device("cuda", 0), peak, not args.no_cpu_baseline,
+                                        reps=max(1, args.steps))), flush=True)
+        return
     world, rank, local = dist_setup()
     if args.impl == "reference":
         line = run_reference(args, world, rank, local)

@@ -264,18 +264,20 @@ ha_status hash_attn_select_ex(const ha_shape* shape, const uint32_t* q_sig, cons
  * no allocation). It depends only on the shape and the code width, so it also
  * fixes the layout that hash_attn_workspace_size(_ex) sizes.
  *   code_words  words per code (1 = the 32-bit codes of HashAttention Eq. (2))
- *   fused       1: SCORE and TOPK run as one thread-block-cluster kernel (32-bit
- *               codes, at most 4 query heads per KV head, n_cap within 16 CTAs
- *               of 8192, 16384 or 32768 tokens); 0: as two kernels
- *   cluster     CTAs per (batch entry, KV head) of the fused kernel (0 if not fused)
- *   range       tokens per CTA of the fused kernel (0 if not fused)
+ *   fused       1: each distance is computed once (32-bit codes, at most 4 query
+ *               heads per KV head): a scan kernel writes the packed distances
+ *               and per-range histograms, an emit kernel writes the lists;
+ *               0: the two-kernel path that recomputes the distances in TOPK
+ *   ranges      CTAs of 8192 tokens per (batch entry, KV head) of the fused
+ *               kernels (0 if not fused)
+ *   range       8192 (tokens per fused CTA), 0 if not fused
  *   chunk       tokens per CTA of the two-kernel SCORE/TOPK (also used by
  *               hash_attn_score whatever `fused` says)
  * Any output pointer may be NULL. HA_ERR_INVALID_ARG / HA_ERR_UNSUPPORTED as
  * hash_attn_workspace_size for a bad shape or code width.
  */
 ha_status hash_attn_selection_plan(const ha_shape* shape, int32_t code_words, int32_t* fused,
-                                   int32_t* cluster, int32_t* range, int32_t* chunk);
+                                   int32_t* ranges, int32_t* range, int32_t* chunk);
 
 /*
  * GATHER-ATT + merge over caller-given index lists (page size 1, read in place):

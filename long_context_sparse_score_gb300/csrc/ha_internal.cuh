@@ -24,7 +24,6 @@ constexpr int kSegPerChunk = kScoreThreads / 32;  // TOPK writes one segment per
 constexpr int kMaxSegments = 4096;        // segments per head (bounds GATHER-ATT's prefix table)
 constexpr int64_t kMaxCap = int64_t(1) << 24;  // largest n_cap accepted
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per pipeline wait
-constexpr int kClMax = 16;                // fused SCORE+TOPK: most CTAs per cluster (16 needs the non-portable opt-in)
 constexpr int kSMs = 152;                 // SMs of a GB300
 
 // ------------------------------------------------------------------ workspace
@@ -42,8 +41,8 @@ constexpr int kSMs = 152;                 // SMs of a GB300
 // meta_qt    int2  [heads][nchunks]       per chunk: (tie quota left, ties in chunk)
 struct Layout {
     int heads = 0;
-    bool fused = false;      // selection by the cluster kernel: flat lists instead of segments
-    int cl = 0, rmax = 0;    // its cluster size and most tokens per CTA
+    bool fused = false;      // fused selection: flat lists instead of segments
+    int nranges = 0;         // fused: ranges of 8192 tokens per (batch entry, KV head)
     int chunk = 0;           // tokens per SCORE/TOPK chunk (0: no selection regions)
     int nchunks = 0;
     int seg_cap = 0;         // tokens per TOPK segment (chunk / kSegPerChunk)
@@ -55,6 +54,12 @@ struct Layout {
     size_t off_err = 0, off_counter = 0, off_hist = 0, off_segcnt = 0, off_seg = 0, off_part = 0;
     size_t off_scnt = 0, off_meta_t = 0, off_meta_qt = 0;
     size_t off_list = 0, off_lcnt = 0;  // fused: flat lists [heads][rows_cap] and their counts [heads]
+    size_t off_dist = 0;                // fused: packed distances [batch * h_kv][d_sp]
+    size_t off_rh = 0;                  // fused: per range, 3 x 4 prefix-summed histograms of 36 words
+    size_t off_meta_r = 0;              // fused: per (pair, range, head) int4 {first position, ties taken, ties, count}
+    size_t off_meta_tt = 0;             // fused: per (pair, head) int2 {t, total}
+    size_t off_tot = 0;                 // fused: per (pair, head) 36-word distance histogram (zero at rest)
+    int64_t d_sp = 0;                   // fused: words per row of the distance buffer
     size_t total = 0;
 };
 
@@ -63,18 +68,12 @@ struct Layout {
 int choose_chunk(int64_t batch_hkv, int64_t n_cap);
 // Split-K policy for GATHER-ATT.
 void choose_splits(int64_t heads, int64_t rows_cap, int* splits, int* rows_per_split);
-// Fused SCORE+TOPK plan for a shape (32-bit codes, at most 4 query heads per
-// KV head, and a per-CTA token range whose packed distances fit in shared
-// memory); ok = false leaves the shape to the two-kernel path.
-struct ClPlan {
-    bool ok = false;
-    int cl = 1;      // CTAs per cluster, one cluster per (batch entry, KV head)
-    int rmax = 0;    // tokens per CTA: 8192, 16384 or 32768
-};
-ClPlan cl_plan(const ha_shape& s, int code_words);
-// Dynamic shared memory of the fused kernel for a per-CTA range of rmax tokens
-// (the packed distances).
-size_t cl_select_smem(int rmax);
+// SCORE and TOPK with one popcount per (token, query head) (k_sel_scan +
+// k_sel_emit) take 32-bit codes with at most 4 query heads per KV head; other
+// shapes take the two-kernel path that recomputes the distances.
+bool fused_selection(const ha_shape& s, int code_words);
+// Ranges of 8192 tokens (one CTA each) per (batch entry, KV head) of the fused path.
+int fused_ranges(int n_cap);
 // Full layout; with_selection=false leaves out the selection regions. With a
 // fused plan the selection regions are the flat lists; otherwise the chunk
 // histograms, segments and threshold metadata of the two-kernel path.
@@ -122,8 +121,9 @@ struct SelectParams {
     uint32_t* err;
 };
 
-// Fused SCORE+TOPK (k_select_cl): one cluster of `CL` CTAs per (batch entry, KV head).
-struct ClSelectParams {
+// Fused SCORE+TOPK (k_sel_scan, k_sel_emit): one CTA per range of 8192 tokens of
+// a (batch entry, KV head) in each kernel.
+struct FusedSelParams {
     const uint32_t* q_sig;   // [B * Hq]
     const uint32_t* k_sig;
     int64_t ks_sb, ks_sh;
@@ -132,7 +132,14 @@ struct ClSelectParams {
     const int32_t* m_per_head;   // [B * Hq] or null (overrides m_per_seq)
     int m, n_sink, n_local, excl;
     int B, Hq, Hkv, G, n_cap;
-    int CL, rmax;
+    int nranges;             // ranges per (batch entry, KV head)
+    uint32_t* dist;          // [B * Hkv][d_sp] packed distances (head e in byte e), token order
+    int64_t d_sp;
+    uint32_t* rh;            // [B * Hkv][nranges][3][4][36] prefix-summed histograms
+    uint32_t* arrive;        // [B * Hkv] arrival counters of k_sel_scan (self-resetting)
+    uint32_t* tot;           // [B * Hkv][4][36] per-sequence distance histograms (summed, then cleared)
+    int4* meta_r;            // [B * Hkv][nranges][4]
+    int2* meta_t;            // [B * Hkv][4]
     int32_t* list;           // [B * Hq][cap] selected tokens, ascending
     int cap;
     int32_t* cnt;            // [B * Hq]
@@ -286,7 +293,7 @@ cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem
 // Launchers (each returns cudaGetLastError() of its launch).
 cudaError_t launch_score(const ScoreParams& p, int batch_hkv, cudaStream_t st);
 cudaError_t launch_select(const SelectParams& p, int batch_hkv, cudaStream_t st, bool pdl = false);
-cudaError_t launch_select_cl(const ClSelectParams& p, int batch_hkv, cudaStream_t st);
+cudaError_t launch_select_fused(const FusedSelParams& p, int batch_hkv, cudaStream_t st);
 cudaError_t launch_compact(const CompactParams& p, int heads, cudaStream_t st);
 cudaError_t launch_hist(const HistParams& p, int heads, cudaStream_t st);
 cudaError_t launch_gather(const GatherParams& p, int d, int kv_bf16, cudaStream_t st, bool pdl = false);

@@ -315,12 +315,12 @@ void apply_opts(const ha_select_opts* o, int32_t n_sink, int32_t n_local, ScoreP
     tp->excl = sp->excl;
 }
 
-// Parameters of the fused SCORE+TOPK kernel; the lists go to `list` (stride cap).
-ClSelectParams cl_params(const ha_shape* s, const Layout& lay, const Views& v, const uint32_t* q_sig,
-                         const uint32_t* k_sig, const int32_t* seq_lens, const int32_t* m_per_seq, int32_t m,
-                         int32_t n_sink, int32_t n_local, const ha_select_opts* o, int32_t* list, int32_t* cnt,
-                         int pad) {
-    ClSelectParams p{};
+// Parameters of the fused SCORE+TOPK kernels; the lists go to `list` (stride cap).
+FusedSelParams fused_params(const ha_shape* s, const Layout& lay, void* ws, const Views& v, const uint32_t* q_sig,
+                            const uint32_t* k_sig, const int32_t* seq_lens, const int32_t* m_per_seq, int32_t m,
+                            int32_t n_sink, int32_t n_local, const ha_select_opts* o, int32_t* list, int32_t* cnt,
+                            int pad) {
+    FusedSelParams p{};
     p.q_sig = q_sig;
     p.k_sig = k_sig;
     p.ks_sb = s->ks_sb;
@@ -337,8 +337,14 @@ ClSelectParams cl_params(const ha_shape* s, const Layout& lay, const Views& v, c
     p.Hkv = s->h_kv;
     p.G = s->h_q / s->h_kv;
     p.n_cap = s->n_cap;
-    p.CL = lay.cl;
-    p.rmax = lay.rmax;
+    p.nranges = lay.nranges;
+    p.dist = at<uint32_t>(ws, lay.off_dist);
+    p.d_sp = lay.d_sp;
+    p.rh = at<uint32_t>(ws, lay.off_rh);
+    p.arrive = v.score_cnt;
+    p.meta_r = at<int4>(ws, lay.off_meta_r);
+    p.meta_t = at<int2>(ws, lay.off_meta_tt);
+    p.tot = at<uint32_t>(ws, lay.off_tot);
     p.list = list;
     p.cap = lay.rows_cap;
     p.cnt = cnt;
@@ -401,14 +407,14 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
         // SCORE and TOPK in one cluster kernel writing flat ascending lists: into the
         // caller's sel_idx (padded with -1) when given, else into the workspace
         const bool to_caller = sel_idx != nullptr;
-        const ClSelectParams cp = cl_params(s, lay, v, q_sig, k_sig, seq_lens, m_per_seq, m, n_sink, n_local, opts,
-                                            to_caller ? sel_idx : v.list, to_caller ? sel_cnt : v.lcnt,
-                                            to_caller ? 1 : 0);
+        const FusedSelParams cp = fused_params(s, lay, ws, v, q_sig, k_sig, seq_lens, m_per_seq, m, n_sink, n_local,
+                                               opts, to_caller ? sel_idx : v.list, to_caller ? sel_cnt : v.lcnt,
+                                               to_caller ? 1 : 0);
         gp.mode = kList;
         gp.list_idx = cp.list;
         gp.list_cnt = cp.cnt;
         gp.list_cap = cp.cap;
-        HA_LAUNCH(launch_select_cl(cp, bhkv, st), "SCORE+TOPK launch");
+        HA_LAUNCH(launch_select_fused(cp, bhkv, st), "SCORE+TOPK launch");
         HA_TRY(record(events, 1, st));
         HA_TRY(record(events, 2, st));
         // GATHER-ATT may start while the selection drains (it waits in the kernel)
@@ -564,29 +570,8 @@ int choose_chunk(int64_t batch_hkv, int64_t n_cap) {
     return chunk;
 }
 
-ClPlan cl_plan(const ha_shape& s, int code_words) {
-    ClPlan P;
-    const int G = s.h_q / s.h_kv;
-    if (code_words > 1 || G > kMaxHeadsPerPass) return P;
-    const int64_t pairs = (int64_t)s.batch * s.h_kv;
-    auto cluster_of = [&](int64_t range) {
-        int cl = 1;
-        while ((int64_t)cl * range < s.n_cap) cl *= 2;
-        return cl;
-    };
-    auto take = [&](int range, int cl) {
-        P.ok = true;
-        P.cl = cl;
-        P.rmax = range;
-        return P;
-    };
-    // 16,384-token CTAs (512 threads, two per SM) with up to 8 per cluster; 8,192
-    // (256 threads) where that leaves fewer CTAs than SMs; 32,768 for contexts
-    // beyond 8 x 16,384 tokens, with up to 16 per cluster
-    const int c16 = cluster_of(16384), c8 = cluster_of(8192), c32 = cluster_of(32768);
-    if (c16 <= 8) return (pairs * c16 < kSMs && c8 <= 8) ? take(8192, c8) : take(16384, c16);
-    if (c32 <= kClMax) return take(32768, c32);
-    return P;
+bool fused_selection(const ha_shape& s, int code_words) {
+    return code_words <= 1 && s.h_q / s.h_kv <= kMaxHeadsPerPass;
 }
 
 void choose_splits(int64_t heads, int64_t rows_cap, int* splits, int* rows_per_split) {
@@ -633,15 +618,25 @@ Layout make_layout(const ha_shape& s, int64_t rows_cap, bool with_selection, int
         off = align_up(off + (size_t)L.heads * L.nchunks * 8, 256);
         L.off_hist = off;
         off = align_up(off + (size_t)L.heads * L.nchunks * nbins * 4, 256);
-        const ClPlan P = cl_plan(s, code_words);
-        if (P.ok) {
+        if (fused_selection(s, code_words)) {
+            const int64_t pairs = (int64_t)s.batch * s.h_kv;
             L.fused = true;
-            L.cl = P.cl;
-            L.rmax = P.rmax;
+            L.nranges = fused_ranges(s.n_cap);
+            L.d_sp = ceil_div(s.n_cap, 64) * 64;
             L.off_list = off;
             off = align_up(off + (size_t)L.heads * (size_t)rows_cap * 4, 256);
             L.off_lcnt = off;
             off = align_up(off + (size_t)L.heads * 4, 256);
+            L.off_dist = off;
+            off = align_up(off + (size_t)pairs * (size_t)L.d_sp * 4, 256);
+            L.off_rh = off;
+            off = align_up(off + (size_t)pairs * L.nranges * 3 * 4 * 36 * 4, 256);
+            L.off_meta_r = off;
+            off = align_up(off + (size_t)pairs * L.nranges * 4 * 16, 256);
+            L.off_meta_tt = off;
+            off = align_up(off + (size_t)pairs * 4 * 8, 256);
+            L.off_tot = off;
+            off = align_up(off + (size_t)pairs * 4 * 36 * 4, 256);
         } else {
             L.off_segcnt = off;
             off = align_up(off + (size_t)L.heads * L.nseg * 4, 256);
@@ -690,15 +685,15 @@ ha_status hash_attn_workspace_size_ex(const ha_shape* shape, int32_t m_max, int3
     return HA_OK;
 }
 
-ha_status hash_attn_selection_plan(const ha_shape* shape, int32_t code_words, int32_t* fused, int32_t* cluster,
+ha_status hash_attn_selection_plan(const ha_shape* shape, int32_t code_words, int32_t* fused, int32_t* ranges,
                                    int32_t* range, int32_t* chunk) {
     HA_TRY(check_shape(shape));
     if (code_words != 1 && code_words != 2 && code_words != 4 && code_words != 8 && code_words != 16)
         return fail(HA_ERR_UNSUPPORTED, "code_words must be 1, 2, 4, 8 or 16 (got %d)", code_words);
-    const ClPlan P = cl_plan(*shape, code_words);
-    if (fused) *fused = P.ok ? 1 : 0;
-    if (cluster) *cluster = P.ok ? P.cl : 0;
-    if (range) *range = P.ok ? P.rmax : 0;
+    const bool f = fused_selection(*shape, code_words);
+    if (fused) *fused = f ? 1 : 0;
+    if (ranges) *ranges = f ? fused_ranges(shape->n_cap) : 0;
+    if (range) *range = f ? 8192 : 0;
     if (chunk) *chunk = choose_chunk((int64_t)shape->batch * shape->h_kv, shape->n_cap);
     return HA_OK;
 }
@@ -794,9 +789,9 @@ ha_status hash_attn_select_ex(const ha_shape* shape, const uint32_t* q_sig, cons
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int bhkv = shape->batch * shape->h_kv;
     if (lay.fused) {
-        const ClSelectParams cp = cl_params(shape, lay, v, q_sig, k_sig, seq_lens, m_per_seq, m, n_sink, n_local,
-                                            opts, sel_idx, sel_cnt, 1);
-        HA_LAUNCH(launch_select_cl(cp, bhkv, st), "SCORE+TOPK launch");
+        const FusedSelParams cp = fused_params(shape, lay, workspace, v, q_sig, k_sig, seq_lens, m_per_seq, m, n_sink,
+                                               n_local, opts, sel_idx, sel_cnt, 1);
+        HA_LAUNCH(launch_select_fused(cp, bhkv, st), "SCORE+TOPK launch");
         return HA_OK;
     }
     if (W > 1) {

@@ -298,10 +298,10 @@ def hash_attn_workspace_size_ex(shape, m_max: int, n_sink: int, n_local: int, op
 
 
 def hash_attn_selection_plan(shape, code_words: int = 1) -> dict:
-    """{"fused", "cluster", "range", "chunk"}: the selection path the library takes for a shape."""
+    """{"fused", "ranges", "range", "chunk"}: the selection path the library takes for a shape."""
     v = [ctypes.c_int32(0) for _ in range(4)]
     _check(lib().hash_attn_selection_plan(ctypes.byref(shape), int(code_words), *(ctypes.byref(x) for x in v)))
-    return dict(zip(("fused", "cluster", "range", "chunk"), (x.value for x in v)))
+    return dict(zip(("fused", "ranges", "range", "chunk"), (x.value for x in v)))
 
 
 def hash_attn_decode_ex(shape, q, q_sig, k_sig, K, V, seq_lens, m_per_seq, m, n_sink, n_local, opts,

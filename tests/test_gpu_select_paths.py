@@ -1,12 +1,14 @@
 """Every selection kernel instantiation the library launches, against the oracle.
 
-The fused SCORE+TOPK kernel comes in three CTA sizes (8,192 / 16,384 / 32,768
-tokens per CTA) and runs with clusters of 1, 2, 4, 8 or 16 CTAs per (sequence,
-KV head); the two-kernel path (more than four query heads per KV head, codes
-wider than 32 bits, or a context beyond 16 CTAs of 32,768 tokens) has SCORE/TOPK
-instantiations for 4, 8, 16 and 32 tokens per thread. Each case asserts which
-plan the shape takes (hash_attn_selection_plan) and then compares the selected
-sets bit for bit and the attention within tolerance on the selected heads.
+The fused selection (32-bit codes, at most four query heads per KV head) runs a
+scan kernel and an emit kernel over ranges of 8,192 tokens, with the ranges of
+a sequence combined by the scan's last CTA; the cases vary the number of
+ranges, where the windows and the tie boundary fall among them, and the
+budget rules. The two-kernel path (more than four query heads per KV head or
+codes wider than 32 bits) has SCORE/TOPK instantiations for 4, 8, 16 and 32
+tokens per thread. Each case asserts which plan the shape takes
+(hash_attn_selection_plan) and then compares the selected sets bit for bit and
+the attention within tolerance on the selected heads.
 """
 import numpy as np
 import pytest
@@ -64,38 +66,33 @@ def _plan(w, code_words=1):
     return H.hash_attn_selection_plan(H.make_shape(w.q, w.K, w.V, w.k_sig), code_words)
 
 
-# ---------------------------------------------------------------- fused kernel: every (range, cluster)
+# ---------------------------------------------------------------- fused selection: ranges, windows, ties
 
 FUSED = [
-    # name, B, Hq, Hkv, n_cap, lens, m, S, Lw, codes, expected (range, cluster)
-    ("r8k_cl1", 2, 8, 2, 8192, [8192, 5000], 300, 16, 64, "pool", (8192, 1)),
-    ("r8k_cl2_ragged", 2, 4, 1, 12000, [12000, 7000], 700, 40, 500, "random", (8192, 2)),
-    ("r8k_cl4_g3", 1, 3, 1, 30000, [30000], 2000, 128, 128, "pool", (8192, 4)),
-    ("r8k_cl8_g2", 2, 4, 2, 60000, [60000, 33333], 1500, 9000, 9000, "pool", (8192, 8)),
-    ("r8k_cl8_g1", 1, 1, 1, 65536, [65535], 4000, 7, 20000, "random", (8192, 8)),
-    ("r16k_cl1_wide_grid", 40, 8, 8, 16000, [16000 - 7 * i for i in range(40)], 1000, 16, 32, "random",
-     (16384, 1)),
-    ("r16k_cl2_wide_grid", 20, 8, 8, 30000, [30000] * 10 + [1, 0] + [29000] * 8, 1000, 16, 32, "pool",
-     (16384, 2)),
-    ("r16k_cl4_wide_grid", 16, 16, 8, 40000, [40000] * 8 + [30000] * 8, 1200, 128, 256, "random", (16384, 4)),
-    ("r16k_cl8_wide_grid", 5, 32, 8, 70000, [70000, 5, 69999, 0, 40000], 2000, 64, 128, "pool", (16384, 8)),
-    ("r16k_cl8_short_seq", 20, 4, 1, 131072, [131072, 3000] * 10, 4096, 128, 256, "random", (16384, 8)),
-    ("r32k_cl8", 1, 4, 1, 200000, [200000], 6000, 128, 256, "pool", (32768, 8)),
-    ("r32k_cl8_windows_span_ranks", 1, 4, 1, 262144, [250000], 5000, 70000, 40000, "pool", (32768, 8)),
-    ("r32k_cl16", 1, 2, 1, 524288, [524288], 16000, 128, 256, "pool", (32768, 16)),
-    ("all_distances_32", 1, 4, 1, 20000, [20000], 900, 16, 16, "far", (8192, 4)),
-    ("budget_zero_windows_only", 1, 4, 1, 20000, [20000], 0, 9000, 100, "pool", (8192, 4)),
+    # name, B, Hq, Hkv, n_cap, lens, m, S, Lw, codes
+    ("one_range", 2, 8, 2, 8192, [8192, 5000], 300, 16, 64, "pool"),
+    ("two_ranges_ragged", 2, 4, 1, 12000, [12000, 7000], 700, 40, 500, "random"),
+    ("four_ranges_g3", 1, 3, 1, 30000, [30000], 2000, 128, 128, "pool"),
+    ("windows_span_ranges_g2", 2, 4, 2, 60000, [60000, 33333], 1500, 9000, 9000, "pool"),
+    ("g1_long_local_window", 1, 1, 1, 65536, [65535], 4000, 7, 20000, "random"),
+    ("many_pairs_ragged", 40, 8, 8, 16000, [16000 - 7 * i for i in range(40)], 1000, 16, 32, "random"),
+    ("empty_and_one_token", 20, 8, 8, 30000, [30000] * 10 + [1, 0] + [29000] * 8, 1000, 16, 32, "pool"),
+    ("sixteen_ranges", 5, 32, 8, 131072, [131072, 5, 131071, 0, 70000], 4096, 128, 256, "pool"),
+    ("windows_span_ranges_long", 1, 4, 1, 262144, [250000], 5000, 70000, 40000, "pool"),
+    ("sixty_four_ranges", 1, 2, 1, 524288, [524288], 16000, 128, 256, "pool"),
+    ("all_distances_32", 1, 4, 1, 20000, [20000], 900, 16, 16, "far"),
+    ("budget_zero_windows_only", 1, 4, 1, 20000, [20000], 0, 9000, 100, "pool"),
 ]
 
 
 @pytest.mark.parametrize("case", FUSED, ids=[c[0] for c in FUSED])
 def test_fused_selection(case):
-    name, B, Hq, Hkv, n_cap, lens, m, S, Lw, codes, want = case
+    name, B, Hq, Hkv, n_cap, lens, m, S, Lw, codes = case
     w = W().make_gqa(31, B=B, Hq=Hq, Hkv=Hkv, d=128, n_cap=n_cap, seq_lens=lens, m=m, n_sink=S, n_local=Lw,
                      device="cuda", name=name)
     _codes(w, codes, 41)
     plan = _plan(w)
-    assert plan["fused"] == 1 and (plan["range"], plan["cluster"]) == want, plan
+    assert plan["fused"] == 1 and plan["ranges"] == -(-n_cap // 8192), plan
     heads = [(b, h) for b in range(B) for h in range(Hq)]
     if len(heads) > 16:
         heads = _sample(B, Hq, 16, 5)
@@ -113,12 +110,12 @@ FUSED_VARIANTS = [
 @pytest.mark.parametrize("case", FUSED_VARIANTS, ids=[c[0] for c in FUSED_VARIANTS])
 def test_fused_selection_variants(case):
     """Exclusive windows and per-head budgets where the windows and the tie
-    boundary fall in different CTAs of the cluster."""
+    boundary fall in different ranges."""
     name, n_cap, lens, m, S, Lw, codes, exclusive, per_head = case
     w = W().make_gqa(32, B=2, Hq=4, Hkv=1, d=128, n_cap=n_cap, seq_lens=lens, m=m, n_sink=S, n_local=Lw,
                      device="cuda", name=name)
     _codes(w, codes, 42)
-    assert _plan(w)["cluster"] >= 8
+    assert _plan(w)["ranges"] >= 8
     mph = None
     if per_head:
         gen = torch.Generator(device="cuda").manual_seed(9)
@@ -158,7 +155,6 @@ TWO_KERNEL = [
     ("g8_tpt8", 2, 64, 8, 40000, [40000, 25000], 1200, 128, 128, "random", 2048),
     ("g8_tpt16", 2, 64, 8, 80000, [80000, 79999], 2500, 128, 256, "pool", 4096),
     ("g8_tpt32", 2, 64, 8, 150000, [150000, 99999], 4096, 128, 256, "random", 8192),
-    ("g4_beyond_fused_range", 1, 4, 1, 600000, [599000], 8000, 128, 256, "pool", 2048),
 ]
 
 
@@ -239,14 +235,25 @@ def test_score_entry_point_every_chunk(n_cap, B, Hkv, chunk):
 
 
 def test_single_sequence_of_two_million_tokens():
-    """One (sequence, KV head) of 2^21 tokens: beyond the fused kernel's range,
-    the two-kernel path with its chunk raised so the segments fit."""
+    """One (sequence, KV head) of 2^21 tokens with four query heads: 256 ranges of
+    the fused selection."""
     n = 1 << 21
     w = W().make_gqa(38, B=1, Hq=4, Hkv=1, d=128, n_cap=n, seq_lens=[n], m=65536, n_sink=128, n_local=256,
                      device="cuda")
     plan = _plan(w)
-    assert plan["fused"] == 0 and (n + plan["chunk"] - 1) // plan["chunk"] * 8 <= 4096
+    assert plan["fused"] == 1 and plan["ranges"] == 256
     _check(w, [(0, h) for h in range(4)], att_heads=2)
+
+
+def test_single_sequence_two_kernel_path_long():
+    """One (sequence, KV head) of 2^21 tokens with eight query heads: the two-kernel
+    path with its chunk raised so the segments fit GATHER-ATT's table."""
+    n = 1 << 21
+    w = W().make_gqa(40, B=1, Hq=8, Hkv=1, d=128, n_cap=n, seq_lens=[n - 5], m=30000, n_sink=128, n_local=256,
+                     device="cuda")
+    plan = _plan(w)
+    assert plan["fused"] == 0 and (n + plan["chunk"] - 1) // plan["chunk"] * 8 <= 4096
+    _check(w, [(0, h) for h in range(0, 8, 3)], att_heads=2)
 
 
 # ---------------------------------------------------------------- dense path: one read per GQA group

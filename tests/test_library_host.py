@@ -74,23 +74,20 @@ def _plan(ha, B, Hq, Hkv, n_cap, code_words=1):
 
 
 def test_selection_plan_of_the_workloads(ha):
-    """The five workloads take the fused kernel; more than four query heads per KV
-    head, wider codes, or a context beyond 16 CTAs of 32,768 tokens take the
+    """32-bit codes with at most four query heads per KV head take the fused
+    selection (each distance computed once, one CTA per 8,192 tokens) at any
+    context length; more query heads per KV head or wider codes take the
     two-kernel path."""
-    # name: (B, Hq, Hkv, n_cap) -> (range, cluster)
-    fused = {"tiny": ((1, 1, 1, 1024), (8192, 1)), "gqa32k": ((1, 32, 8, 32768), (8192, 4)),
-             "batch16_128k": ((16, 32, 8, 131072), (16384, 8)), "shared_doc": ((32, 32, 8, 61440), (16384, 4)),
-             "ragged": ((64, 32, 8, 65536), (16384, 4)), "256k": ((1, 4, 1, 262144), (32768, 8)),
-             "512k": ((1, 4, 1, 524288), (32768, 16))}
-    for name, (shape, want) in fused.items():
+    for name, shape in {"tiny": (1, 1, 1, 1024), "gqa32k": (1, 32, 8, 32768), "batch16_128k": (16, 32, 8, 131072),
+                        "shared_doc": (32, 32, 8, 61440), "ragged": (64, 32, 8, 65536),
+                        "2m": (1, 4, 1, 1 << 21)}.items():
         p = _plan(ha, *shape)
-        assert p["fused"] == 1 and (p["range"], p["cluster"]) == want, (name, p)
+        assert p["fused"] == 1 and p["range"] == 8192 and p["ranges"] == -(-shape[3] // 8192), (name, p)
     assert _plan(ha, 2, 64, 8, 131072)["fused"] == 0                 # eight query heads per KV head
     assert _plan(ha, 16, 32, 8, 131072, code_words=4)["fused"] == 0  # 128-bit codes
-    assert _plan(ha, 1, 4, 1, 524289)["fused"] == 0                  # beyond 16 x 32,768 tokens
-    # a single long sequence keeps the two-kernel path within its segment table
+    # a single long sequence on the two-kernel path keeps within its segment table
     for n in (1 << 21, 1 << 22):
-        p = _plan(ha, 1, 4, 1, n)
+        p = _plan(ha, 1, 8, 1, n)
         assert p["fused"] == 0 and -(-n // p["chunk"]) * 8 <= 4096, (n, p)
     with pytest.raises(ha.HashAttnError):
         _plan(ha, 1, 4, 1, 4096, code_words=3)
