@@ -39,7 +39,8 @@ GATHER_SOURCE = os.path.join(ROOT, "long_context_sparse_score_gb300", "csrc", "k
 # from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the same
 # launch on the 2-sequence case scaled by 8 (the heads are independent); it holds
 # only for the k_gather_att.cu source it was taken on.
-GATHER_TRAFFIC = {"source_sha256": None, "bytes_per_launch": None}
+GATHER_TRAFFIC = {"source_sha256": "c922252848d06b11e6751d82737340a10cd4954d7c3761c20fb9824257352a66",
+                  "bytes_per_launch": 8 * (132475648 + 2883840)}
 
 
 def parse_args():
