@@ -34,13 +34,13 @@ WORKLOAD_DESC = ("batch16-128k: B=16 sequences x 131072 cached tokens, 32 query 
                  "bf16 K/V ~ N(0,1), 32-bit sign(W x) codes per KV head, m=4096 (32x token sparsity), "
                  "n_sink=128, n_local=256")
 FALLBACK_HBM_GBS = 6800.0
-GATHER_SOURCE = os.path.join(ROOT, "long_context_sparse_score_gb300", "csrc", "k_gather_att.cu")
-# DRAM bytes (read + write) per GATHER-ATT launch at the 16 x 131,072-token workload,
-# from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the same
-# launch on the 2-sequence case scaled by 8 (the heads are independent); it holds
-# only for the k_gather_att.cu source it was taken on.
-GATHER_TRAFFIC = {"source_sha256": "c922252848d06b11e6751d82737340a10cd4954d7c3761c20fb9824257352a66",
-                  "bytes_per_launch": 8 * (132475648 + 2883840)}
+GATHER_SOURCE = os.path.join(ROOT, "long_context_sparse_score_gb300", "csrc", "k_group_att.cu")
+# DRAM bytes (read + write) per launch of the step's attention kernel (k_group_att:
+# TOPK's masks and GATHER-ATT per GQA group) at the 16 x 131,072-token workload, from
+# one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the same launch
+# on the 2-sequence case scaled by 8 (the sequences are independent); it holds only
+# for the k_group_att.cu source it was taken on.
+GATHER_TRAFFIC = {"source_sha256": "", "bytes_per_launch": None}
 
 
 def parse_args():
@@ -166,8 +166,8 @@ class ClockSampler:
 
 
 def profiled_traffic():
-    """DRAM bytes per GATHER-ATT launch from the recorded capture, if the kernel
-    source is unchanged since it was taken (else None)."""
+    """DRAM bytes per launch of the attention kernel from the recorded capture, if
+    the kernel source is unchanged since it was taken (else None)."""
     try:
         sha = hashlib.sha256(open(GATHER_SOURCE, "rb").read()).hexdigest()
     except OSError:
@@ -851,7 +851,7 @@ def run_ours(args, world, rank, local):
                    "seq_len": w.n_cap, "parallelism": f"replicas x{world} (independent batches)",
                    "l2": "no flush: inputs larger than L2 (8.6 GB KV + 67 MB codes per GPU; "
                          f"{path_bytes / 1e9:.2f} GB algorithmic reads per step > 126 MB L2)"},
-        "roofline": {"kernel": "k_gather_att", "bound": "hbm", "achieved": achieved, "peak": peak,
+        "roofline": {"kernel": "k_group_att", "bound": "hbm", "achieved": achieved, "peak": peak,
                      "peak_kind": f"{peak_kind} hbm_gbs", "unit": "GB/s", "frac": achieved / peak,
                      "traffic": profiled_traffic(), "algorithmic_bytes_per_launch": gather_bytes,
                      "unique_kv_rows": uniq_rows, "avg_launch_ms": g_ms,
@@ -862,8 +862,11 @@ def run_ours(args, world, rank, local):
                      "algorithmic_bytes_per_step": path_bytes,
                      "stage_events": f"every {EVERY}th timed step ({len(sampled)} of {K})",
                      "stage_ms": {"score": statistics.mean(t_score), "topk": statistics.mean(t_topk),
-                                  "gather_att": g_ms}},
-        "gpu_launches": 3 * K,
+                                  "gather_att": g_ms},
+                     "stages": "score = k_sel_scan (SCORE and the TOPK threshold of every range); "
+                               "gather_att = k_group_att (TOPK's masks and GATHER-ATT per GQA group); "
+                               "topk = the events between them"},
+        "gpu_launches": 2 * K,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps,
                 "note": "per step: one hash_attn_decode_host call (q, q_sig, seq_lens host->device from pinned "

@@ -163,6 +163,15 @@ int32_t hash_attn_select_capacity(int32_t n_cap, int32_t m, int32_t n_sink, int3
  *              int32 receives |I|. Both NULL to skip. Ignored by the dense path.
  *   workspace  >= hash_attn_workspace_size(shape, m, n_sink, n_local) bytes,
  *              256-byte aligned, zeroed once before first use.
+ * Kernels: with 32-bit codes, at most 4 query heads per KV head, a bf16 query,
+ * bf16 K/V, d in {64, 128} and sel_idx NULL, two kernels run: the selection scan
+ * (SCORE and every range's share of TOPK), then one kernel per GQA group that
+ * builds each head's selection mask from the codes and attends over the union
+ * of the group's rows (each row read once per group; K/V must then be finite,
+ * since a row of one head's set is multiplied by weight 0 into the others').
+ * The scan may start while the previous kernel in the stream drains: it waits
+ * for it before writing workspace state. Otherwise the selection writes per-head
+ * lists (or sel_idx) and GATHER-ATT runs per query head.
  * Errors: HA_ERR_INVALID_ARG, HA_ERR_UNSUPPORTED, HA_ERR_WORKSPACE before
  * launch; HA_ERR_CUDA on a failed launch.
  */

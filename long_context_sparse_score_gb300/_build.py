@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_PATH = os.path.join(PKG_DIR, "libhashattn.so")
 
-SOURCES = ["hashattn_api.cu", "k_select.cu", "k_select_fused.cu", "k_gather_att.cu", "k_merge.cu", "k_encode.cu", "k_exact.cu",
+SOURCES = ["hashattn_api.cu", "k_select.cu", "k_select_fused.cu", "k_gather_att.cu", "k_group_att.cu", "k_merge.cu", "k_encode.cu", "k_exact.cu",
            "k_exact_tc.cu", "k_wide.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]

@@ -25,6 +25,7 @@ constexpr int kMaxSegments = 4096;        // segments per head (bounds GATHER-AT
 constexpr int64_t kMaxCap = int64_t(1) << 24;  // largest n_cap accepted
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per pipeline wait
 constexpr int kSMs = 152;                 // SMs of a GB300
+constexpr int kFusedRange = 8192;         // tokens per range of the fused selection (one CTA each)
 
 // ------------------------------------------------------------------ workspace
 //
@@ -193,6 +194,16 @@ struct GatherParams {
     float qscale;            // log2(e) / sqrt(d)
 };
 
+// k_group_att: the selection masks of a GQA group and GATHER-ATT over the union
+// of its query heads' rows. `sel` carries the scan's metadata (its lists are
+// not used), `att` the query, cache, outputs and the partials [heads][nranges][d + 2]
+// (the arrival counters are indexed by (batch entry, KV head)).
+struct GroupAttParams {
+    FusedSelParams sel;
+    GatherParams att;
+    int nsplit;              // CTAs per range, each taking a contiguous part of the union's chunks
+};
+
 struct MergeParams {
     const float* out_a; const float* lse_a;
     const float* out_b; const float* lse_b;
@@ -294,10 +305,19 @@ cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem
 cudaError_t launch_score(const ScoreParams& p, int batch_hkv, cudaStream_t st);
 cudaError_t launch_select(const SelectParams& p, int batch_hkv, cudaStream_t st, bool pdl = false);
 cudaError_t launch_select_fused(const FusedSelParams& p, int batch_hkv, cudaStream_t st);
+// k_sel_scan alone (the threshold metadata, no lists); write_dist = false leaves
+// out the packed distances (their consumer recomputes them from the codes);
+// pdl = true lets its counting overlap the previous kernel in the stream.
+cudaError_t launch_sel_scan(const FusedSelParams& p, int batch_hkv, cudaStream_t st, bool write_dist, bool pdl);
 cudaError_t launch_compact(const CompactParams& p, int heads, cudaStream_t st);
 cudaError_t launch_hist(const HistParams& p, int heads, cudaStream_t st);
 cudaError_t launch_gather(const GatherParams& p, int d, int kv_bf16, cudaStream_t st, bool pdl = false);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t st);
+// bf16 query and K/V, d in {64, 128}, at most 4 query heads per KV head.
+bool group_att_supported(int d, int kv_bf16, int q_bf16, int G);
+// CTAs per range of k_group_att for (batch entry, KV head) pairs x ranges.
+int group_splits(int64_t pair_ranges);
+cudaError_t launch_group_att(const GroupAttParams& p, int d, int batch_hkv, cudaStream_t st, bool pdl);
 cudaError_t launch_merge_n(const MergeNParams& p, cudaStream_t st);
 cudaError_t launch_encode(const EncodeParams& p, cudaStream_t st);
 cudaError_t launch_encode_mlp(const EncodeParams& p, cudaStream_t st);

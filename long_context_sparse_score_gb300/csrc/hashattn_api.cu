@@ -1,6 +1,7 @@
 // C ABI of the sparse-decode library: argument checks, workspace layout and the
 // stream-ordered launch sequence SCORE -> TOPK -> GATHER-ATT (+ merge).
 // Every check that the host can make happens before anything is enqueued.
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -403,6 +404,25 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
         return HA_OK;
     }
     HA_TRY(record(events, 0, st));
+    if (lay.fused && sel_idx == nullptr &&
+        group_att_supported(s->d, s->kv_dtype == HA_BF16, s->q_dtype == HA_BF16, s->h_q / s->h_kv) &&
+        s->k_sn < (int64_t(1) << 30) && s->v_sn < (int64_t(1) << 30)) {
+        // the scan's thresholds, then one kernel per GQA group that builds the masks
+        // in place and attends over the union of the group's rows
+        GroupAttParams ga{};
+        ga.sel = fused_params(s, lay, ws, v, q_sig, k_sig, seq_lens, m_per_seq, m, n_sink, n_local, opts, v.list,
+                              v.lcnt, 0);
+        ga.att = gp;
+        ga.nsplit = group_splits((int64_t)bhkv * lay.nranges);
+        // the scan's counting may overlap the previous call's last kernel (not the
+        // map kernels, whose codes it reads)
+        HA_LAUNCH(launch_sel_scan(ga.sel, bhkv, st, false, map == nullptr), "SCORE+TOPK launch");
+        HA_TRY(record(events, 1, st));
+        HA_TRY(record(events, 2, st));
+        HA_LAUNCH(launch_group_att(ga, s->d, bhkv, st, true), "GATHER-ATT launch");
+        HA_TRY(record(events, 3, st));
+        return HA_OK;
+    }
     if (lay.fused) {
         // SCORE and TOPK in one cluster kernel writing flat ascending lists: into the
         // caller's sel_idx (padded with -1) when given, else into the workspace
@@ -644,8 +664,12 @@ Layout make_layout(const ha_shape& s, int64_t rows_cap, bool with_selection, int
             off = align_up(off + (size_t)L.heads * L.nseg * L.seg_cap * 4, 256);
         }
     }
+    // split-K partials; the group kernel keeps one per (head, range) of the fused plan
+    const int psplits =
+        L.fused ? std::max<int64_t>(L.splits, (int64_t)L.nranges * group_splits((int64_t)s.batch * s.h_kv * L.nranges))
+                : L.splits;
     L.off_part = off;
-    off = align_up(off + (size_t)L.heads * L.splits * (s.d + 2) * 4, 256);
+    off = align_up(off + (size_t)L.heads * psplits * (s.d + 2) * 4, 256);
     L.total = off;
     return L;
 }

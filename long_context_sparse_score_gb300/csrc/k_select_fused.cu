@@ -28,91 +28,16 @@
 //               into the flat lists and drops the line from L2 without writing it
 //               back to memory.
 #include "ha_internal.cuh"
+#include "sel_common.cuh"
 
 namespace ha {
 namespace {
 
 constexpr int kSelThreads = 256;
-constexpr int kSelRange = 32 * kSelThreads;  // tokens per CTA
+constexpr int kSelRange = kFusedRange;      // tokens per CTA (32 per thread)
+static_assert(kSelRange == 32 * kSelThreads, "one 32-token lane block per thread");
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kCum = HA_NBINS + 3;           // entries of a published prefix-sum array (0 .. 33 used)
-
-__device__ __forceinline__ uint32_t warp_sum_u(uint32_t v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
-__device__ __forceinline__ int warp_excl_scan(int v, int* total) {
-    const int lane = threadIdx.x & 31;
-    int x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-    }
-    *total = __shfl_sync(0xffffffffu, x, 31);
-    return x - v;
-}
-
-__device__ __forceinline__ void red_add_shared(uint32_t addr, uint32_t v) {
-    asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ uint32_t half_field(uint32_t w01, uint32_t w23, int e) {
-    const uint32_t w = (e < 2) ? w01 : w23;
-    return (e & 1) ? (w >> 16) : (w & 0xffffu);
-}
-
-// Bits [0, k) set, k clamped to [0, 32].
-__device__ __forceinline__ uint32_t low_bits(int k) {
-    return k <= 0 ? 0u : (k >= 32 ? 0xffffffffu : ((1u << k) - 1u));
-}
-
-// Per-head masks over a lane block of 32 tokens: bit j of m[e] is set iff byte e
-// of D[j] is at most byte e of the threshold word, where TE holds 0x80 + T_e in
-// byte e (T_e in [-1, 32]; distances are at most 32, so no byte borrows from its
-// neighbour and bit 7 of byte e of TE - D[j] is set exactly when D_e <= T_e).
-__device__ __forceinline__ void le_masks(const uint32_t (&D)[32], uint32_t TE, uint32_t (&m)[4]) {
-    uint32_t X[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint32_t x = 0u;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) x |= ((TE - D[8 * q + j]) & 0x80808080u) >> (7 - j);
-        X[q] = x;  // byte e: tokens 8q .. 8q+7 of head e
-    }
-    // 4 x 4 byte transpose: byte q of m[e] = byte e of X[q]
-    const uint32_t a = __byte_perm(X[0], X[1], 0x5140);
-    const uint32_t c = __byte_perm(X[0], X[1], 0x7362);
-    const uint32_t bb = __byte_perm(X[2], X[3], 0x5140);
-    const uint32_t dd = __byte_perm(X[2], X[3], 0x7362);
-    m[0] = __byte_perm(a, bb, 0x5410);
-    m[1] = __byte_perm(a, bb, 0x7632);
-    m[2] = __byte_perm(c, dd, 0x5410);
-    m[3] = __byte_perm(c, dd, 0x7632);
-}
-
-// Threshold word: byte e = 0x80 + T_e for heads e < nh, 0x7F (select nothing) above.
-__device__ __forceinline__ uint32_t thresh_word(const int (&T)[4], int nh) {
-    uint32_t w = 0u;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) w |= (uint32_t)((e < nh) ? (0x80 + T[e]) : 0x7F) << (8 * e);
-    return w;
-}
-
-// Keep the first q set bits of x (q >= 0).
-__device__ __forceinline__ uint32_t first_bits(uint32_t x, int q) {
-    uint32_t keep = 0u;
-    while (x != 0u && q > 0) {
-        const uint32_t low = x & (0u - x);
-        keep |= low;
-        x ^= low;
-        --q;
-    }
-    return keep;
-}
-
 
 // Budget of head h (per-head budgets override per-sequence ones, which override m;
 // out-of-range budgets are clamped and flagged).
@@ -135,6 +60,10 @@ __device__ __forceinline__ int head_budget(const FusedSelParams& p, int b, int64
     return mb;
 }
 
+// WD: write the packed distances for k_sel_emit; without them the window parts
+// are recounted from the codes and the codes are read with the default cache
+// policy (a later kernel reads them again).
+template <bool WD>
 __global__ void __launch_bounds__(kSelThreads, 4) k_sel_scan(const FusedSelParams p) {
     constexpr int NT = kSelThreads, R = kSelRange;
     constexpr int NR = R / (4 * NT);   // rounds of 4 tokens per thread
@@ -171,12 +100,13 @@ __global__ void __launch_bounds__(kSelThreads, 4) k_sel_scan(const FusedSelParam
             const int i = lo + k * 4 * NT + 4 * tid;
             uint4 c;
             if (i + 4 <= hi) {
-                c = __ldcs(reinterpret_cast<const uint4*>(row + i));  // read once: evict first
+                // with the distances written, the codes are read once: evict first
+                c = WD ? __ldcs(reinterpret_cast<const uint4*>(row + i)) : *reinterpret_cast<const uint4*>(row + i);
             } else {
-                c.x = (i < hi) ? __ldcs(row + i) : 0u;
-                c.y = (i + 1 < hi) ? __ldcs(row + i + 1) : 0u;
-                c.z = (i + 2 < hi) ? __ldcs(row + i + 2) : 0u;
-                c.w = (i + 3 < hi) ? __ldcs(row + i + 3) : 0u;
+                c.x = (i < hi) ? row[i] : 0u;
+                c.y = (i + 1 < hi) ? row[i + 1] : 0u;
+                c.z = (i + 2 < hi) ? row[i + 2] : 0u;
+                c.w = (i + 3 < hi) ? row[i + 3] : 0u;
             }
             return c;
         };
@@ -201,7 +131,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) k_sel_scan(const FusedSelParam
                 pk[j] = w;
             }
             // i is a multiple of 4 below n <= n_cap <= d_sp: the four words stay in the row
-            *reinterpret_cast<uint4*>(drow + i) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            if constexpr (WD) *reinterpret_cast<uint4*>(drow + i) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         };
 #pragma unroll
         for (int k = 0; k < NR + U; ++k) {
@@ -209,6 +139,12 @@ __global__ void __launch_bounds__(kSelThreads, 4) k_sel_scan(const FusedSelParam
             if (k < NR) v[k % U] = load(k);
         }
     }
+    // Launched with programmatic dependent launch, the counting above may overlap
+    // the previous kernel in the stream; everything below writes state that the
+    // previous call's kernels may still read (published sums, totals, shares),
+    // so wait for it here (every kernel of the library waits for its own
+    // predecessor before it completes, so this orders the calls).
+    pdl_wait();
     __syncthreads();  // the range's distances are written and visible to this CTA
     for (int u = warp; u < HA_NBINS; u += kSelWarps) {
         const uint32_t s01 = warp_sum_u(hist[u][0][lane]);
@@ -219,8 +155,18 @@ __global__ void __launch_bounds__(kSelThreads, 4) k_sel_scan(const FusedSelParam
         // the window parts of this range: [lo, min(hi, wlo)) and [max(lo, wmid), hi)
         const int a0 = lo, a1 = min(hi, wlo), b0 = max(lo, wmid), b1 = hi;
         const int na = max(0, a1 - a0), nb = max(0, b1 - b0);
+        const uint32_t* crow = p.k_sig + (int64_t)b * p.ks_sb + (int64_t)g * p.ks_sh;
         for (int x = tid; x < na + nb; x += NT) {
-            const uint32_t w = drow[x < na ? a0 + x : b0 + (x - na)];
+            const int i = x < na ? a0 + x : b0 + (x - na);
+            uint32_t w = 0u;
+            if constexpr (WD) {
+                w = drow[i];
+            } else {
+                const uint32_t c = crow[i];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (e < nh) w |= (uint32_t)__popc(qs[e] ^ c) << (8 * e);
+            }
             const int which = (x < na) ? 1 : 2;
 #pragma unroll
             for (int e = 0; e < 4; ++e)
@@ -491,10 +437,16 @@ int fused_ranges(int n_cap) { return (n_cap + kSelRange - 1) / kSelRange; }
 
 cudaError_t launch_select_fused(const FusedSelParams& p, int batch_hkv, cudaStream_t st) {
     const dim3 grid((unsigned)batch_hkv * (unsigned)p.nranges);
-    k_sel_scan<<<grid, kSelThreads, 0, st>>>(p);
+    k_sel_scan<true><<<grid, kSelThreads, 0, st>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_ex(k_sel_emit, grid, dim3(kSelThreads), 0, st, true, p);
+}
+
+cudaError_t launch_sel_scan(const FusedSelParams& p, int batch_hkv, cudaStream_t st, bool write_dist, bool pdl) {
+    const dim3 grid((unsigned)batch_hkv * (unsigned)p.nranges);
+    if (write_dist) return launch_ex(k_sel_scan<true>, grid, dim3(kSelThreads), 0, st, pdl, p);
+    return launch_ex(k_sel_scan<false>, grid, dim3(kSelThreads), 0, st, pdl, p);
 }
 
 }  // namespace ha
