@@ -62,13 +62,14 @@ __device__ __forceinline__ int head_budget(const FusedSelParams& p, int b, int64
 
 // WD: write the packed distances for k_sel_emit; without them the window parts
 // are recounted from the codes and the codes are read with the default cache
-// policy (a later kernel reads them again).
-template <bool WD>
+// policy (a later kernel reads them again). NHT: query heads per KV head known
+// at compile time (4), or 0 for the runtime value p.G (1 to 4).
+template <bool WD, int NHT>
 __global__ void __launch_bounds__(kSelThreads, 4) k_sel_scan(const FusedSelParams p) {
     constexpr int NT = kSelThreads, R = kSelRange;
     constexpr int NR = R / (4 * NT);   // rounds of 4 tokens per thread
     constexpr int U = 4;               // rounds of codes in flight per thread
-    __shared__ uint32_t hist[HA_NBINS][2][32];      // lane columns; heads 2k, 2k+1 in 16-bit fields
+    __shared__ __align__(16) uint32_t hist[HA_NBINS][2][32];  // lane columns; heads 2k, 2k+1 in 16-bit fields
     __shared__ uint32_t s_h[3][4][HA_NBINS + 3];    // per head: all tokens, sink part, local part
     __shared__ int s_last;
 
@@ -79,7 +80,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) k_sel_scan(const FusedSelParam
     const int lo = min(n, range * R);
     const int hi = min(n, lo + R);
     const int head0 = b * p.Hq + g * p.G;
-    const int nh = p.G;  // at most 4 (checked on the host)
+    const int nh = NHT > 0 ? NHT : p.G;  // at most 4 (checked on the host)
     const int wlo = min(p.n_sink, n);                   // sink window [0, wlo)
     const int wmid = max(max(0, n - p.n_local), wlo);   // local window [wmid, n)
     uint32_t* drow = p.dist + (int64_t)pair * p.d_sp;
@@ -110,25 +111,34 @@ __global__ void __launch_bounds__(kSelThreads, 4) k_sel_scan(const FusedSelParam
             }
             return c;
         };
+        // one token: its distances to the heads into the histogram columns, packed
+        auto count = [&](uint32_t code) {
+            uint32_t w = 0u;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (NHT > 0 ? e < NHT : e < nh) {
+                    const uint32_t d = (uint32_t)__popc(qs[e] ^ code);
+                    red_add_shared(col + (d * 2 + (e >> 1)) * 128u, 1u << (16 * (e & 1)));
+                    w |= d << (8 * e);
+                }
+            }
+            return w;
+        };
         auto compute = [&](const uint4 c4, int k) {
             const int i = lo + k * 4 * NT + 4 * tid;
-            if (i >= hi) return;
-            const uint32_t code[4] = {c4.x, c4.y, c4.z, c4.w};
-            uint32_t pk[4];
+            uint32_t pk[4] = {0u, 0u, 0u, 0u};
+            if (i + 4 <= hi) {  // four whole tokens: no per-token checks
+                pk[0] = count(c4.x);
+                pk[1] = count(c4.y);
+                pk[2] = count(c4.z);
+                pk[3] = count(c4.w);
+            } else if (i < hi) {
+                const uint32_t code[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                uint32_t w = 0u;
-                if (i + j < hi) {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        if (e < nh) {
-                            const uint32_t d = (uint32_t)__popc(qs[e] ^ code[j]);
-                            red_add_shared(col + (d * 2 + (e >> 1)) * 128u, 1u << (16 * (e & 1)));
-                            w |= d << (8 * e);
-                        }
-                    }
-                }
-                pk[j] = w;
+                for (int j = 0; j < 4; ++j)
+                    if (i + j < hi) pk[j] = count(code[j]);
+            } else {
+                return;
             }
             // i is a multiple of 4 below n <= n_cap <= d_sp: the four words stay in the row
             if constexpr (WD) *reinterpret_cast<uint4*>(drow + i) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -146,10 +156,31 @@ __global__ void __launch_bounds__(kSelThreads, 4) k_sel_scan(const FusedSelParam
     // predecessor before it completes, so this orders the calls).
     pdl_wait();
     __syncthreads();  // the range's distances are written and visible to this CTA
-    for (int u = warp; u < HA_NBINS; u += kSelWarps) {
-        const uint32_t s01 = warp_sum_u(hist[u][0][lane]);
-        const uint32_t s23 = warp_sum_u(hist[u][1][lane]);
-        if (lane < 4) s_h[0][lane][u] = (lane < nh) ? half_field(s01, s23, lane) : 0u;
+    {
+        // every (bin, head pair) row of 32 lane columns: 4 threads x 8 columns, then
+        // 2 shuffles (bins 0-31); bin 32 by warp 0, 16 lanes x 2 columns per pair.
+        // The 16-bit fields hold at most 8192 counts: no carries between heads.
+        const int r = tid >> 2, q = tid & 3;
+        const uint4* rp = reinterpret_cast<const uint4*>(&hist[0][0][0] + r * 32 + q * 8);
+        const uint4 x0 = rp[0], x1 = rp[1];
+        uint32_t v = (x0.x + x0.y) + (x0.z + x0.w) + (x1.x + x1.y) + (x1.z + x1.w);
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        if (q == 0) {
+            s_h[0][2 * (r & 1)][r >> 1] = v & 0xffffu;
+            s_h[0][2 * (r & 1) + 1][r >> 1] = v >> 16;
+        }
+        if (warp == 0) {
+            const int pr = lane >> 4;
+            const uint2 y = *reinterpret_cast<const uint2*>(&hist[HA_NBINS - 1][pr][(lane & 15) * 2]);
+            uint32_t t = y.x + y.y;
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+            if ((lane & 15) == 0) {
+                s_h[0][2 * pr][HA_NBINS - 1] = t & 0xffffu;
+                s_h[0][2 * pr + 1][HA_NBINS - 1] = t >> 16;
+            }
+        }
     }
     {
         // the window parts of this range: [lo, min(hi, wlo)) and [max(lo, wmid), hi)
@@ -437,7 +468,10 @@ int fused_ranges(int n_cap) { return (n_cap + kSelRange - 1) / kSelRange; }
 
 cudaError_t launch_select_fused(const FusedSelParams& p, int batch_hkv, cudaStream_t st) {
     const dim3 grid((unsigned)batch_hkv * (unsigned)p.nranges);
-    k_sel_scan<true><<<grid, kSelThreads, 0, st>>>(p);
+    if (p.G == 4)
+        k_sel_scan<true, 4><<<grid, kSelThreads, 0, st>>>(p);
+    else
+        k_sel_scan<true, 0><<<grid, kSelThreads, 0, st>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_ex(k_sel_emit, grid, dim3(kSelThreads), 0, st, true, p);
@@ -445,8 +479,12 @@ cudaError_t launch_select_fused(const FusedSelParams& p, int batch_hkv, cudaStre
 
 cudaError_t launch_sel_scan(const FusedSelParams& p, int batch_hkv, cudaStream_t st, bool write_dist, bool pdl) {
     const dim3 grid((unsigned)batch_hkv * (unsigned)p.nranges);
-    if (write_dist) return launch_ex(k_sel_scan<true>, grid, dim3(kSelThreads), 0, st, pdl, p);
-    return launch_ex(k_sel_scan<false>, grid, dim3(kSelThreads), 0, st, pdl, p);
+    if (p.G == 4) {
+        if (write_dist) return launch_ex(k_sel_scan<true, 4>, grid, dim3(kSelThreads), 0, st, pdl, p);
+        return launch_ex(k_sel_scan<false, 4>, grid, dim3(kSelThreads), 0, st, pdl, p);
+    }
+    if (write_dist) return launch_ex(k_sel_scan<true, 0>, grid, dim3(kSelThreads), 0, st, pdl, p);
+    return launch_ex(k_sel_scan<false, 0>, grid, dim3(kSelThreads), 0, st, pdl, p);
 }
 
 }  // namespace ha
