@@ -103,7 +103,8 @@ ha_status hash_attn_workspace_size(const ha_shape* shape, int32_t m_max, int32_t
 
 /*
  * Zero a workspace (enqueued on `stream`). A workspace must be zeroed once
- * before its first use; every call leaves its counters back at zero.
+ * before its first use; every call leaves its counters back at zero. After a
+ * call that raised HA_DEVERR_TIMEOUT or HA_DEVERR_STATE, zero it again.
  * The workspace pointer must be 256-byte aligned.
  */
 ha_status hash_attn_workspace_init(void* workspace, size_t ws_bytes, void* stream);

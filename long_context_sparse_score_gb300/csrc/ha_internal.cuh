@@ -60,6 +60,7 @@ struct Layout {
     size_t off_meta_r = 0;              // fused: per (pair, range, head) int4 {first position, ties taken, ties, count}
     size_t off_meta_tt = 0;             // fused: per (pair, head) int2 {t, total}
     size_t off_tot = 0;                 // fused: per (pair, head) 36-word distance histogram (zero at rest)
+    size_t off_ready = 0;               // fused: per pair, shares-complete flag (zero at rest)
     int64_t d_sp = 0;                   // fused: words per row of the distance buffer
     size_t total = 0;
 };
@@ -141,6 +142,8 @@ struct FusedSelParams {
     uint32_t* tot;           // [B * Hkv][4][36] per-sequence distance histograms (summed, then cleared)
     int4* meta_r;            // [B * Hkv][nranges][4]
     int2* meta_t;            // [B * Hkv][4]
+    uint32_t* ready;         // [B * Hkv] or null: set to 1 once a pair's shares are written
+                             // (k_group_att waits on it and resets it)
     int32_t* list;           // [B * Hq][cap] selected tokens, ascending
     int cap;
     int32_t* cnt;            // [B * Hq]

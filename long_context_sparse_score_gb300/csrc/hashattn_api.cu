@@ -412,6 +412,7 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
         GroupAttParams ga{};
         ga.sel = fused_params(s, lay, ws, v, q_sig, k_sig, seq_lens, m_per_seq, m, n_sink, n_local, opts, v.list,
                               v.lcnt, 0);
+        ga.sel.ready = at<uint32_t>(ws, lay.off_ready);
         ga.att = gp;
         ga.nsplit = group_splits((int64_t)bhkv * lay.nranges);
         // the scan's counting may overlap the previous call's last kernel (not the
@@ -657,6 +658,8 @@ Layout make_layout(const ha_shape& s, int64_t rows_cap, bool with_selection, int
             off = align_up(off + (size_t)pairs * 4 * 8, 256);
             L.off_tot = off;
             off = align_up(off + (size_t)pairs * 4 * 36 * 4, 256);
+            L.off_ready = off;
+            off = align_up(off + (size_t)pairs * 4, 256);
         } else {
             L.off_segcnt = off;
             off = align_up(off + (size_t)L.heads * L.nseg * 4, 256);

@@ -167,7 +167,36 @@ __global__ void __launch_bounds__(kGT, GCfg<D, ST>::MINB) k_group_att(const Grou
         }
     }
     pdl_launch_dependents();
-    pdl_wait();  // the scan's thresholds and shares
+    // The scan's thresholds and shares of this pair: its last CTA sets ready[pair]
+    // after writing them, so the pairs that are done start while the scan drains.
+    // Every scan CTA is resident before this grid starts (programmatic launch), so
+    // the flag comes; the wait is bounded all the same.
+    __shared__ int s_go;
+    if (p.ready != nullptr) {
+        if (tid == 0) {
+            int ok = 0;
+            const unsigned long long t0 = global_ns();
+            for (uint32_t it = 0;; ++it) {
+                uint32_t v;
+                asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p.ready + pair) : "memory");
+                if (v != 0u) {
+                    ok = 1;
+                    break;
+                }
+                if ((it & 15u) == 15u && global_ns() - t0 > kWaitLimitNs) break;
+                __nanosleep(200);
+            }
+            if (!ok) flag_error(p.err, HA_DEVERR_TIMEOUT);
+            s_go = ok;
+        }
+        __syncthreads();
+        if (!s_go) {
+            pdl_wait();
+            return;
+        }
+    } else {
+        pdl_wait();
+    }
 
     // ---- 1. masks
     int T[4], Tsel[4], qv[4], expect[4], mode[4];
@@ -179,8 +208,8 @@ __global__ void __launch_bounds__(kGT, GCfg<D, ST>::MINB) k_group_att(const Grou
         expect[e] = 0;
         mode[e] = 0;
         if (e < nh && lo < n) {
-            const int2 mt = p.meta_t[pair * 4 + e];
-            const int4 m4 = p.meta_r[((int64_t)pair * p.nranges + range) * 4 + e];
+            const int2 mt = __ldcg(p.meta_t + pair * 4 + e);
+            const int4 m4 = __ldcg(p.meta_r + ((int64_t)pair * p.nranges + range) * 4 + e);
             T[e] = mt.x;
             qv[e] = m4.y;
             expect[e] = m4.w;
@@ -463,6 +492,9 @@ __global__ void __launch_bounds__(kGT, GCfg<D, ST>::MINB) k_group_att(const Grou
         __syncwarp();  // the stage is read before it is refilled
     }
     wait_group<0>();
+    // the whole scan grid has completed long before: this orders the next kernel
+    // in the stream after it
+    pdl_wait();
 
     // ---- 3. combine the warps, then the ranges
 #pragma unroll
@@ -523,7 +555,10 @@ __global__ void __launch_bounds__(kGT, GCfg<D, ST>::MINB) k_group_att(const Grou
             }
         }
     }
-    if (nparts == 1) return;
+    if (nparts == 1) {
+        if (tid == 0 && p.ready != nullptr) p.ready[pair] = 0u;
+        return;
+    }
 
     __syncthreads();  // every partial store of this CTA precedes thread 0's fence
     if (tid == 0) {
@@ -555,7 +590,10 @@ __global__ void __launch_bounds__(kGT, GCfg<D, ST>::MINB) k_group_att(const Grou
         a.out[head * D + dd] = (Ls > 0.f) ? O / Ls : 0.f;
         if (dd == 0) a.lse[head] = (Ls > 0.f) ? (M + log2f(Ls)) * kLn2 : -CUDART_INF_F;
     }
-    if (tid == 0) a.counters[pair] = 0u;
+    if (tid == 0) {
+        a.counters[pair] = 0u;
+        if (p.ready != nullptr) p.ready[pair] = 0u;
+    }
 }
 
 template <int D, int ST>

@@ -74,8 +74,10 @@ __global__ void __launch_bounds__(kSelThreads, 4) k_sel_scan(const FusedSelParam
     __shared__ int s_last;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int pair = blockIdx.x / p.nranges, range = blockIdx.x % p.nranges;
-    const int b = pair / p.Hkv, g = pair % p.Hkv;
+    // CTA order: batch entry fastest, then range, then KV head, so that the pairs of
+    // one KV head complete together (and a cache shared by the batch is read once)
+    const int b = blockIdx.x % p.B, range = (blockIdx.x / p.B) % p.nranges, g = blockIdx.x / (p.B * p.nranges);
+    const int pair = b * p.Hkv + g;
     const int n = checked_len(p.seq_lens, b, p.n_cap, p.err, range == 0 && g == 0 && tid == 0);
     const int lo = min(n, range * R);
     const int hi = min(n, lo + R);
@@ -310,9 +312,15 @@ __global__ void __launch_bounds__(kSelThreads, 4) k_sel_scan(const FusedSelParam
         }
         if (lane == 0) p.meta_t[pair * 4 + e] = make_int2(t, carry);
     }
-    __syncthreads();  // every warp has read the totals
+    __syncthreads();  // every warp has read the totals and written its shares
     for (int x = tid; x < 4 * kCum; x += NT) tot_g[x] = 0u;
-    if (tid == 0) p.arrive[pair] = 0u;
+    if (tid == 0) {
+        p.arrive[pair] = 0u;
+        if (p.ready != nullptr) {  // the shares of this pair are complete
+            __threadfence();
+            asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.ready + pair), "r"(1u) : "memory");
+        }
+    }
 }
 
 __global__ void __launch_bounds__(kSelThreads, 4) k_sel_emit(const FusedSelParams p) {
