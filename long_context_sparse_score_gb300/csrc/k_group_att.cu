@@ -230,10 +230,11 @@ __global__ void __launch_bounds__(kGT, GCfg<D, ST>::MINB) k_group_att(const Grou
             uint32_t Dw[32];
             if (valid == 0xffffffffu) {
                 // lb + 32 <= n <= n_cap and lb is a multiple of 32: whole 16-byte loads in the row
+                // the codes' last read: streaming (evict first)
                 const uint4* src = reinterpret_cast<const uint4*>(crow + lb);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const uint4 v = src[j];
+                    const uint4 v = __ldcs(src + j);
                     Dw[4 * j + 0] = v.x;
                     Dw[4 * j + 1] = v.y;
                     Dw[4 * j + 2] = v.z;
