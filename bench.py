@@ -38,9 +38,11 @@ GATHER_SOURCE = os.path.join(ROOT, "long_context_sparse_score_gb300", "csrc", "k
 # DRAM bytes (read + write) per launch of the step's attention kernel (k_group_att:
 # TOPK's masks and GATHER-ATT per GQA group) at the 16 x 131,072-token workload, from
 # one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the same launch
-# on the 2-sequence case scaled by 8 (the sequences are independent); it holds only
-# for the k_group_att.cu source it was taken on.
-GATHER_TRAFFIC = {"source_sha256": "", "bytes_per_launch": None}
+# on the 2-sequence case scaled by 8 (the sequences are independent); ncu starts the
+# launch with a cold L2, so the kernel's second read of the codes comes from DRAM.
+# It holds only for the k_group_att.cu source it was taken on.
+GATHER_TRAFFIC = {"source_sha256": "93946070433be616c405ec8bc7ae7cd4d1287bdb2b4ddbf67bdc43487284c467",
+                  "bytes_per_launch": 8 * (139243776 + 3377152)}
 
 
 def parse_args():
