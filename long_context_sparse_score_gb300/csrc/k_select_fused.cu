@@ -65,7 +65,7 @@ __device__ __forceinline__ int head_budget(const FusedSelParams& p, int b, int64
 // policy (a later kernel reads them again). NHT: query heads per KV head known
 // at compile time (4), or 0 for the runtime value p.G (1 to 4).
 template <bool WD, int NHT>
-__global__ void __launch_bounds__(kSelThreads, 4) k_sel_scan(const FusedSelParams p) {
+__global__ void __launch_bounds__(kSelThreads, WD ? 5 : 8) k_sel_scan(const FusedSelParams p) {
     constexpr int NT = kSelThreads, R = kSelRange;
     constexpr int NR = R / (4 * NT);   // rounds of 4 tokens per thread
     constexpr int U = 4;               // rounds of codes in flight per thread
