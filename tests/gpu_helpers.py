@@ -158,3 +158,21 @@ def check_attention(res, hc, heads, m, dense=False):
         _, _, ref_out, ref_lse = hc.head(b, h, m, dense=dense)
         assert_out_close(out[b, h], ref_out, f"out (b={b}, h={h})")
         assert_lse_close(float(lse[b, h]), ref_lse, f"lse (b={b}, h={h})")
+
+
+def check_decode_step_path(w, res_sel, hc, heads, m, ws=None):
+    """The decode call without selection outputs (the path the bench times: the
+    selection scan, then the GQA-group kernel when the shape allows it) on the same
+    workload: against the oracle on ``heads`` and against ``res_sel`` (the call that
+    also returned the selection) on every head."""
+    grp = run_decode(w, m=m, sel=False, ws=ws)
+    assert grp["status"] == 0, hex(grp["flags"])
+    check_attention(grp, hc, heads, m)
+    go, ro = grp["out"].cpu().numpy(), res_sel["out"].cpu().numpy()
+    assert np.all(np.isfinite(go)), "non-finite output"
+    assert_out_close(go, ro, "decode step vs the call with selection outputs")
+    gl, rl = grp["lse"].cpu().numpy(), res_sel["lse"].cpu().numpy()
+    fin = np.isfinite(rl)
+    assert np.array_equal(np.isfinite(gl), fin)
+    assert np.all(np.abs(gl[fin] - rl[fin]) <= 2 * LSE_ATOL * (1 + np.abs(rl[fin])))
+    return grp

@@ -917,6 +917,7 @@ def test_workload2_gqa_32k_full():
     hc = GH.HostCopy(w)
     GH.check_selection(res, hc, all_heads(w), w.m)
     GH.check_attention(res, hc, all_heads(w), w.m)
+    GH.check_decode_step_path(w, res, hc, all_heads(w), w.m, ws=res["ws"])
 
 
 def _sample_heads(w, k, seed):
@@ -940,6 +941,8 @@ def test_workload3_batch16_128k_sampled():
     idx = res["sel_idx"].cpu().numpy()
     assert np.all(np.diff(idx[:, :, :4096], axis=-1) > 0)
     assert np.all(idx[:, :, :128] == np.arange(128))
+    # the path the bench times, in its launch configuration (full grid, same workspace)
+    GH.check_decode_step_path(w, res, hc, heads[:12], w.m, ws=res["ws"])
     del w, res
 
 
@@ -962,6 +965,7 @@ def test_workload4_shared_document_full():
     hc = GH.HostCopy(w)
     heads = _sample_heads(w, 16, 4)
     GH.check_selection(doc, hc, heads, w.m)
+    GH.check_decode_step_path(w, doc, hc, heads[:8], w.m, ws=doc["ws"])
     q = w.q.float().cpu().numpy()
     for b, h in heads[:8]:
         _, _, od, ld = hc.head(b, h, w.m)
@@ -981,6 +985,7 @@ def test_workload5_ragged_full_sparse_and_dense():
     heads = _sample_heads(w, 24, 5)
     GH.check_selection(res, hc, heads, w.m)
     GH.check_attention(res, hc, heads[:12], w.m)
+    GH.check_decode_step_path(w, res, hc, heads[:12], w.m, ws=res["ws"])
     dense = GH.run_decode(w, m=w.n_cap, m_per_seq=None, dense=True, sel=False)
     assert dense["status"] == 0
     GH.check_attention(dense, hc, heads[:6], w.n_cap, dense=True)
