@@ -56,9 +56,16 @@ struct GCfg {
     static constexpr int STAGE = 2 * kCR * PITCH;      // K rows, then V rows
     static constexpr int RING = kGW * ST * STAGE;
     static constexpr int KS = D / 16;                  // k-steps of K Q^T, m-tiles of V^T P^T
-    static constexpr int OFF_HB = RING;                // int [kGW][ST][kCR] head bits of the ring's rows
-    static constexpr int BYTES = OFF_HB + kGW * ST * kCR * 4;
     static constexpr int MINB = (ST >= 3) ? 2 : 3;     // CTAs per SM
+    static constexpr int OFF_HB = RING;                // int [kGW][ST][kCR] head bits of the ring's rows
+    static constexpr int OFF_LST = OFF_HB + kGW * ST * kCR * 4;  // uint32 [LCAP] the list's first entries
+    // what the shared memory of an SM leaves a CTA beside MINB - 1 others (228 KB,
+    // 1 KB reserved per CTA, the static arrays), in 16-entry chunks
+    static constexpr int SMEM_CTA = (228 * 1024) / MINB - 1024 - 1024;
+    static constexpr int LCAP_FIT = ((SMEM_CTA - OFF_LST) / 4) / kCR * kCR;
+    static constexpr int LCAP = LCAP_FIT < kFusedRange ? LCAP_FIT : kFusedRange;
+    static constexpr int BYTES = OFF_LST + LCAP * 4;
+    static_assert(LCAP >= kCR, "room for a list chunk in shared memory");
     // combine area (reuses the ring): o [kGW][4][D], m [kGW][4], l [kGW][4]
     static_assert((kGW * 4 * D + 2 * kGW * 4) * 4 <= RING, "combine fits in the ring");
     static_assert(RPI * 2 * NCH == 32, "whole rows per copy instruction");
@@ -124,6 +131,7 @@ __global__ void __launch_bounds__(kGT, GCfg<D, ST>::MINB) k_group_att(const Grou
     const GatherParams& a = gp.att;
     extern __shared__ __align__(128) unsigned char smem[];
     int* s_hb = reinterpret_cast<int*>(smem + C::OFF_HB);
+    uint32_t* s_lst = reinterpret_cast<uint32_t*>(smem + C::OFF_LST);
     __shared__ int s_wt[kIt][4][kGW];   // ties per (iteration, head, warp)
     __shared__ int s_wc[kIt][4][kGW];   // selected tokens per (iteration, head, warp)
     __shared__ int s_wu[kIt][kGW];      // union rows per (iteration, warp)
@@ -313,9 +321,10 @@ __global__ void __launch_bounds__(kGT, GCfg<D, ST>::MINB) k_group_att(const Grou
         if (lane == 0) s_wu[it][warp] = tot;
     }
     __syncthreads();
-    // The list lives in the distance buffer's row of this (batch entry, KV head), at
-    // the range's offset: the range holds at least as many tokens as list entries,
-    // and range * 8192 + (tokens of the range) <= n <= n_cap <= d_sp.
+    // The list's first LCAP entries live in shared memory, the rest in the distance
+    // buffer's row of this (batch entry, KV head), at the range's offset: the range
+    // holds at least as many tokens as list entries, and
+    // range * 8192 + (tokens of the range) <= n <= n_cap <= d_sp.
     // Split `split` of S takes chunks [c0, c1) of the range's union and writes only
     // their entries (the splits of a range write disjoint parts of the list).
     uint32_t* lst = p.dist + (int64_t)pair * p.d_sp + (int64_t)range * kFusedRange;
@@ -341,7 +350,11 @@ __global__ void __launch_bounds__(kGT, GCfg<D, ST>::MINB) k_group_att(const Grou
                 uint32_t hb = 0u;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) hb |= ((msk[it][e] >> bit) & 1u) << e;
-                lst[pos] = (uint32_t)(off0 + bit) | (hb << 16);
+                const uint32_t v = (uint32_t)(off0 + bit) | (hb << 16);
+                if (pos < C::LCAP)
+                    s_lst[pos] = v;
+                else
+                    lst[pos] = v;
             }
             ++pos;
         }
@@ -379,7 +392,8 @@ __global__ void __launch_bounds__(kGT, GCfg<D, ST>::MINB) k_group_att(const Grou
     // first token with no head bits (its rows are read and then masked out)
     auto entry = [&](int k) -> uint32_t {
         const int pos = (c0 + warp + k * kGW) * kCR + lane;
-        return (lane < kCR && k < ncw && pos < U) ? lst[pos] : 0u;
+        if (lane >= kCR || k >= ncw || pos >= U) return 0u;
+        return pos < C::LCAP ? s_lst[pos] : lst[pos];
     };
     auto issue = [&](int k, uint32_t ent) {
         const int slot = k % ST;
