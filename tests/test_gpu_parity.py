@@ -211,6 +211,10 @@ def test_per_head_budget_above_bound_is_flagged():
     assert res["status"] == H.HA_ERR_DEVICE and res["flags"] & H.HA_DEVERR_BUDGET
     hc = GH.HostCopy(w, m_per_head=torch.tensor([[100, 100, 0, 7]], dtype=torch.int32))
     GH.check_selection(res, hc, all_heads(w), 100)
+    # the decode step without selection outputs clamps and flags the same way
+    grp = GH.run_decode(w, m_per_head=mph, sel=False)
+    assert grp["status"] == H.HA_ERR_DEVICE and grp["flags"] & H.HA_DEVERR_BUDGET
+    GH.check_attention(grp, hc, all_heads(w), 100)
 
 
 def test_ragged_per_sequence_budget():
@@ -886,6 +890,11 @@ def test_device_errors_are_flagged_not_faulted():
     assert torch.all(res["sel_cnt"][1:] == 0)
     hc = GH.HostCopy(w)
     GH.check_attention(res, hc, [(0, h) for h in range(4)], w.m)
+    # the same on the decode step without selection outputs (scan + group kernel)
+    grp = GH.run_decode(w, sel=False)
+    assert grp["status"] == H.HA_ERR_DEVICE and grp["flags"] & H.HA_DEVERR_SEQLEN
+    assert torch.all(grp["lse"][1:].isneginf()) and torch.all(grp["out"][1:] == 0)
+    GH.check_attention(grp, hc, [(0, h) for h in range(4)], w.m)
     # a per-sequence budget above the bound is clamped and flagged
     w.seq_lens = torch.tensor([2000, 1500, 2000], dtype=torch.int32, device="cuda")
     w.m_per_seq = torch.tensor([100, 150, 50], dtype=torch.int32, device="cuda")
@@ -893,6 +902,10 @@ def test_device_errors_are_flagged_not_faulted():
     assert res["status"] == H.HA_ERR_DEVICE and res["flags"] & H.HA_DEVERR_BUDGET
     assert int(res["sel_cnt"][1, 0]) == len(O.selected_set(int(w.q_sig[1, 0]),
                                                               w.k_sig[1, 0].cpu().numpy(), 1500, 100, 4, 4))
+    grp = GH.run_decode(w, m=100, sel=False)
+    assert grp["status"] == H.HA_ERR_DEVICE and grp["flags"] & H.HA_DEVERR_BUDGET
+    w.m_per_seq = torch.tensor([100, 100, 50], dtype=torch.int32, device="cuda")  # as clamped
+    GH.check_attention(grp, GH.HostCopy(w), [(b, h) for b in range(3) for h in range(4)], 100)
     # the next call on the same workspace reports clean
     w.m_per_seq = None
     res = GH.run_decode(w, ws=res["ws"])
