@@ -36,13 +36,13 @@ WORKLOAD_DESC = ("batch16-128k: B=16 sequences x 131072 cached tokens, 32 query 
 FALLBACK_HBM_GBS = 6800.0
 GATHER_SOURCE = os.path.join(ROOT, "long_context_sparse_score_gb300", "csrc", "k_group_att.cu")
 # DRAM bytes (read + write) per launch of the step's attention kernel (k_group_att:
-# TOPK's masks and GATHER-ATT per GQA group) at the 16 x 131,072-token workload, from
-# one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum) of the same launch
-# on the 2-sequence case scaled by 8 (the sequences are independent); ncu starts the
-# launch with a cold L2, so the kernel's second read of the codes comes from DRAM.
-# It holds only for the k_group_att.cu source it was taken on.
+# TOPK's masks and GATHER-ATT per GQA group) at the 16 x 131,072-token workload,
+# from one ncu capture of a full-size launch inside this program's own loop
+# (dram__bytes_read.sum + dram__bytes_write.sum, one pass, --cache-control none, so
+# the L2 holds what the step left there: the codes the scan has just read). It
+# holds only for the k_group_att.cu source it was taken on.
 GATHER_TRAFFIC = {"source_sha256": "c22f458a150a947a4b79bc2181854272a59bc65c06a70c8da7cf124bf36eb399",
-                  "bytes_per_launch": 8 * (139237120 + 2468352)}
+                  "bytes_per_launch": 1057629696 + 2438912}
 
 
 def parse_args():
