@@ -8,28 +8,34 @@
 // Estimation of Cached-Token Attention via Regression, Eqs. (3.4)-(3.5): partial
 // results over disjoint token ranges merge exactly through their log-normalisers.
 //
-// k_group_att: one CTA (4 warps) per (batch entry, KV head, range of 8,192
-// tokens), run after k_sel_scan, which has fixed every head's threshold bin t
-// and each range's share of the ties.
+// k_group_att: one CTA (4 warps, three per SM) per (batch entry, KV head, range
+// of 8,192 tokens), run after k_sel_scan, which has fixed every head's threshold
+// bin t and each range's share of the ties. A CTA starts as soon as the scan's
+// last CTA of its (batch entry, KV head) has set the pair's ready flag.
 //  1. Masks. Each thread recomputes the distances of two 32-token lane blocks
-//     from the codes (one popcount per token and head) and builds every head's
-//     mask with byte-wise compares against t - 1 and t (as k_sel_emit does), ranks
-//     the ties of a head's boundary range in token order, adds the windows, and
-//     checks each head's count against the scan's. The masks, their union and the
-//     union's prefix counts stay in shared memory.
-//  2. Attention. The union of the group's rows is cut into chunks of 16; warp w
-//     takes chunks w, w + 4, ... and runs its own three-stage ring of 16-byte
-//     asynchronous copies (a K row and its V row per chunk row, each read once for
-//     the whole group). Per chunk, S = K Q^T (16 rows x 8 head columns, heads
-//     beyond the group zero) and O^T += V^T P^T are mma.sync m16n8k16 products
-//     with bf16 operands and fp32 accumulation: the products of bf16 values are
-//     exact, P is passed as two bf16 parts (p = hi + lo, relative error below
-//     2^-16) so P.V keeps fp32 accuracy. A row outside a head's own set gets score
-//     -inf for that head: each head attends over exactly its own rows. The softmax
-//     is online in base 2 per (warp, head).
+//     from the codes (one popcount per token and head; the codes' last read) and
+//     builds every head's mask with one byte-wise compare pass against a per-head
+//     threshold word (t - 1, or t for a head that takes its whole bin t here; a
+//     second pass at t only in a head's boundary range, whose ties are ranked in
+//     token order), adds the windows, and checks each head's count against the
+//     scan's. The union of the heads' masks becomes a list in token order, one word
+//     per row (offset in the range | head bits << 16): its first entries in shared
+//     memory, the rest in the workspace.
+//  2. Attention. The union is cut into chunks of 16 rows; warp w takes chunks
+//     w, w + 4, ... and runs its own two-stage ring of 16-byte asynchronous copies
+//     (a K row and its V row per chunk row, each read once for the whole group,
+//     with an L2 evict-first policy). Per chunk, S = K Q^T (16 rows x 8 head
+//     columns, heads beyond the group zero) and O^T += V^T P^T are mma.sync
+//     m16n8k16 products with bf16 operands and fp32 accumulation: the products of
+//     bf16 values are exact, P is passed as two bf16 parts (p = hi + lo, relative
+//     error below 2^-16) so P.V keeps fp32 accuracy. A row outside a head's own set
+//     gets score -inf for that head: each head attends over exactly its own rows.
+//     The softmax is online in base 2 per (warp, head).
 //  3. The warps combine in shared memory into the range's partial (max, sum, o)
 //     per head; the last CTA of a (batch entry, KV head) to arrive merges the
 //     ranges of its heads (an arrival counter decides; nothing waits).
+// When the grid would not give every SM a CTA, two CTAs share a range, each with
+// a contiguous half of its chunks (both build the masks).
 // K/V must be finite: a row selected by one head of the group is also multiplied
 // (by weight zero) into the other heads' P.V.
 #include "ha_internal.cuh"
