@@ -871,8 +871,8 @@ def run_ours(args, world, rank, local):
         "gpu_launches": 2 * K,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps,
-                "note": "per step: one hash_attn_decode_host call (q, q_sig, seq_lens host->device from pinned "
-                        "memory, one copy each; decode; out and lse device->host, one copy each), then a stream "
+                "note": "per step: one hash_attn_decode_host call (q, q_sig, seq_lens host->device from one "
+                        "pinned buffer in one copy; decode; out and lse device->host in one copy), then a stream "
                         "sync; KV cache and key codes are device-resident state"},
         "clocks": clocks,
         "next": {"merge_n": measure_merge_n(dev, peak), "encode": measure_encode(w, shape, dev),

@@ -117,10 +117,14 @@ ha_status hash_attn_host_staging_size(const ha_shape* shape, size_t* bytes);
 
 /*
  * hash_attn_decode with the step's inputs and results in HOST memory (pinned
- * memory makes the copies asynchronous): one cudaMemcpyAsync per input into
- * `staging`, the path, then one per result back, all enqueued on `stream`; the
+ * memory makes the copies asynchronous): the inputs are copied into `staging`,
+ * the path runs, the results are copied back, all enqueued on `stream`; the
  * results are in out_host / lse_host once the stream has reached them. The
- * cache (k_sig, K, V) and the workspace stay on the device.
+ * cache (k_sig, K, V) and the workspace stay on the device. Copies: one per
+ * input, except that inputs which follow each other directly in host memory
+ * in the staging order (q, q_sig, seq_lens, m_per_seq; each staged at the next
+ * 16-byte boundary) move in one copy, and so do out and lse when lse_host
+ * follows out_host directly and out's size is a multiple of 16 bytes.
  *   q_host        contiguous [batch, h_q, d] of shape->q_dtype (shape's q strides
  *                 are ignored: the staged copy is contiguous)
  *   q_sig_host    [batch, h_q] uint32 (may be NULL only for the dense path)

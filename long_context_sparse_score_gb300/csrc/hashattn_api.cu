@@ -542,8 +542,9 @@ void set_mlp(EncodeParams* p, const ha_mlp* mlp) {
     p->hidden = mlp->hidden;
 }
 
-// Device staging of hash_attn_decode_host: q, q_sig, seq_lens, m_per_seq, out,
-// lse, each region 256-byte aligned.
+// Device staging of hash_attn_decode_host: q, q_sig, seq_lens, m_per_seq (each
+// 16-byte aligned, packed), then out (256-byte aligned) and lse (16-byte aligned):
+// host buffers laid out the same way move in one copy each way.
 struct Staging {
     size_t q = 0, q_sig = 0, seq = 0, mps = 0, out = 0, lse = 0, total = 0;
     size_t q_bytes = 0, sig_bytes = 0, seq_bytes = 0, out_bytes = 0, lse_bytes = 0;
@@ -559,15 +560,15 @@ Staging staging_layout(const ha_shape* s) {
     L.lse_bytes = heads * sizeof(float);
     size_t off = 0;
     L.q = off;
-    off = align_up(off + L.q_bytes, 256);
+    off = align_up(off + L.q_bytes, 16);
     L.q_sig = off;
-    off = align_up(off + L.sig_bytes, 256);
+    off = align_up(off + L.sig_bytes, 16);
     L.seq = off;
-    off = align_up(off + L.seq_bytes, 256);
+    off = align_up(off + L.seq_bytes, 16);
     L.mps = off;
     off = align_up(off + L.seq_bytes, 256);
     L.out = off;
-    off = align_up(off + L.out_bytes, 256);
+    off = align_up(off + L.out_bytes, 16);
     L.lse = off;
     L.total = align_up(off + L.lse_bytes, 256);
     return L;
@@ -991,15 +992,38 @@ ha_status hash_attn_decode_host(const ha_shape* shape, const void* q_host, const
                         {sig_d, q_sig_host, L.sig_bytes, cudaMemcpyHostToDevice},
                         {seq_d, seq_lens_host, L.seq_bytes, cudaMemcpyHostToDevice},
                         {mps_d, m_per_seq_host, L.seq_bytes, cudaMemcpyHostToDevice}};
-    for (const Copy& c : in) {  // one asynchronous copy per input
+    // one asynchronous copy per run of inputs that are adjacent both on the host and
+    // in the staging buffer (an input following the previous one directly in both)
+    const Copy* run = nullptr;
+    size_t run_bytes = 0;
+    auto flush = [&]() -> ha_status {
+        if (run == nullptr) return HA_OK;
+        const cudaError_t e = cudaMemcpyAsync(run->dst, run->src, run_bytes, cudaMemcpyHostToDevice, st);
+        run = nullptr;
+        return e == cudaSuccess ? HA_OK : cuda_fail(e, "input copy to the device");
+    };
+    for (const Copy& c : in) {
         if (c.dst == nullptr) continue;
-        const cudaError_t e = cudaMemcpyAsync(c.dst, c.src, c.bytes, c.kind, st);
-        if (e != cudaSuccess) return cuda_fail(e, "input copy to the device");
+        if (run != nullptr && static_cast<const char*>(run->src) + run_bytes == static_cast<const char*>(c.src) &&
+            static_cast<char*>(run->dst) + run_bytes == static_cast<char*>(c.dst)) {
+            run_bytes += c.bytes;
+            continue;
+        }
+        HA_TRY(flush());
+        run = &c;
+        run_bytes = c.bytes;
     }
+    HA_TRY(flush());
     HA_TRY(decode_impl(&s, q_d, sig_d, k_sig, K, V, seq_d, mps_d, m, n_sink, n_local, nullptr, out_d, lse_d,
                        nullptr, nullptr, workspace, ws_bytes, stream, nullptr));
-    cudaError_t e = cudaMemcpyAsync(out_host, out_d, L.out_bytes, cudaMemcpyDeviceToHost, st);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(lse_host, lse_d, L.lse_bytes, cudaMemcpyDeviceToHost, st);
+    cudaError_t e;
+    if (reinterpret_cast<char*>(out_host) + L.out_bytes == reinterpret_cast<char*>(lse_host) &&
+        L.out + L.out_bytes == L.lse) {
+        e = cudaMemcpyAsync(out_host, out_d, L.out_bytes + L.lse_bytes, cudaMemcpyDeviceToHost, st);
+    } else {
+        e = cudaMemcpyAsync(out_host, out_d, L.out_bytes, cudaMemcpyDeviceToHost, st);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(lse_host, lse_d, L.lse_bytes, cudaMemcpyDeviceToHost, st);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "result copy to the host");
     return HA_OK;
 }

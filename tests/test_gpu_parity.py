@@ -462,11 +462,13 @@ def test_encode_queries_and_keys(d, q_dtype):
     assert int(flags.item()) & H.HA_DEVERR_INDEX
 
 
-@pytest.mark.parametrize("mode", ["sparse", "budgets", "dense"])
+@pytest.mark.parametrize("mode", ["sparse", "budgets", "dense", "packed"])
 def test_decode_host_buffers_equal_device_decode(mode):
     """hash_attn_decode_host (inputs and results in pinned host memory) gives the
     outputs of hash_attn_decode on device copies of the same inputs, bit for bit,
-    for the sparse path, per-sequence budgets and the dense path (no codes)."""
+    for the sparse path, per-sequence budgets and the dense path (no codes); in
+    "packed" the inputs sit back to back in one host buffer at the staging offsets
+    (merged copies) and out / lse in another."""
     H = GH.ha()
     w = W().make_gqa(47, B=3, Hq=8, Hkv=2, d=128, n_cap=3000, seq_lens=[3000, 1999, 2500], m=200, n_sink=16,
                      n_local=16, device="cuda", m_per_seq=[200, 150, 64] if mode == "budgets" else None)
@@ -483,6 +485,17 @@ def test_decode_host_buffers_equal_device_decode(mode):
     mps_h = pin(w.m_per_seq) if w.m_per_seq is not None else None
     out_h = torch.full((3, 8, 128), float("nan")).pin_memory()
     lse_h = torch.full((3, 8), float("nan")).pin_memory()
+    if mode == "packed":
+        # q (6,144 bytes), q_sig (96 bytes) and seq_lens (12 bytes) back to back: the
+        # first two and the lengths follow each other at 16-byte staging boundaries
+        qb, sb = w.q.numel() * 2, w.q_sig.numel() * 4
+        buf = torch.empty(qb + sb + 12, dtype=torch.uint8).pin_memory()
+        buf[:qb].copy_(w.q.cpu().contiguous().view(torch.uint8).view(-1))
+        buf[qb:qb + sb].copy_(w.q_sig.cpu().contiguous().view(torch.uint8).view(-1))
+        buf[qb + sb:].copy_(w.seq_lens.cpu().contiguous().view(torch.uint8).view(-1))
+        q_h, sig_h, sl_h = buf[:qb], buf[qb:qb + sb], buf[qb + sb:]
+        res_buf = torch.full((3 * 8 * 128 + 3 * 8,), float("nan")).pin_memory()
+        out_h, lse_h = res_buf[:3 * 8 * 128].view(3, 8, 128), res_buf[3 * 8 * 128:].view(3, 8)
     H.hash_attn_decode_host(shape, q_h, None if mode == "dense" else sig_h, sl_h, mps_h,
                             None if mode == "dense" else w.k_sig, w.K, w.V, m, w.n_sink, w.n_local, out_h, lse_h,
                             staging=staging, workspace=ws)
