@@ -800,8 +800,9 @@ def run_ours(args, world, rank, local):
     value = throughput(world, B * Hq, K, elapsed_ms)
 
     # e2e: per-step query inputs from pinned host memory, results back to the host,
-    # through the C-ABI call that takes host buffers (hash_attn_decode_host: one
-    # host->device copy per input, the path, one device->host copy per result, all
+    # through the C-ABI call that takes host buffers (hash_attn_decode_host: the
+    # inputs sit back to back in one pinned buffer and move in one host->device
+    # copy, the path runs, out and lse come back in one device->host copy, all
     # enqueued by the library); its arguments are marshalled once.
     qn, qsn, sln = w.q.numel() * w.q.element_size(), w.q_sig.numel() * 4, w.seq_lens.numel() * 4
     in_h = torch.empty(qn + qsn + sln, dtype=torch.uint8).pin_memory()
