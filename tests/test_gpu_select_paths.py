@@ -242,7 +242,9 @@ def test_single_sequence_of_two_million_tokens():
                      device="cuda")
     plan = _plan(w)
     assert plan["fused"] == 1 and plan["ranges"] == 256
-    _check(w, [(0, h) for h in range(4)], att_heads=2)
+    res = _check(w, [(0, h) for h in range(4)], att_heads=2)
+    # the decode step without selection outputs: 256 ranges merged per head
+    GH.check_decode_step_path(w, res, GH.HostCopy(w), [(0, 0), (0, 3)], w.m, ws=res["ws"])
 
 
 def test_single_sequence_two_kernel_path_long():
