@@ -160,12 +160,12 @@ def check_attention(res, hc, heads, m, dense=False):
         assert_lse_close(float(lse[b, h]), ref_lse, f"lse (b={b}, h={h})")
 
 
-def check_decode_step_path(w, res_sel, hc, heads, m, ws=None):
+def check_decode_step_path(w, res_sel, hc, heads, m, ws=None, K=None, V=None):
     """The decode call without selection outputs (the path the bench times: the
     selection scan, then the GQA-group kernel when the shape allows it) on the same
     workload: against the oracle on ``heads`` and against ``res_sel`` (the call that
     also returned the selection) on every head."""
-    grp = run_decode(w, m=m, sel=False, ws=ws)
+    grp = run_decode(w, m=m, sel=False, ws=ws, K=K, V=V)
     assert grp["status"] == 0, hex(grp["flags"])
     check_attention(grp, hc, heads, m)
     go, ro = grp["out"].cpu().numpy(), res_sel["out"].cpu().numpy()

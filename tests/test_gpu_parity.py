@@ -66,6 +66,8 @@ def test_small_shapes(case):
     hc = GH.HostCopy(w)
     GH.check_selection(res, hc, all_heads(w), m)
     GH.check_attention(res, hc, all_heads(w), m)
+    # the decode step without selection outputs (the group kernel where it applies)
+    GH.check_decode_step_path(w, res, hc, all_heads(w), m, ws=res["ws"])
 
 
 def test_tie_heavy_codes():
@@ -83,6 +85,7 @@ def test_tie_heavy_codes():
     hc = GH.HostCopy(w)
     GH.check_selection(res, hc, all_heads(w), w.m)
     GH.check_attention(res, hc, all_heads(w), w.m)
+    GH.check_decode_step_path(w, res, hc, all_heads(w), w.m, ws=res["ws"])
 
 
 def test_all_codes_equal_take_first_m():
@@ -130,6 +133,7 @@ def test_windows_across_chunks_and_tie_boundary(case):
     hc = GH.HostCopy(w)
     GH.check_selection(res, hc, all_heads(w), m)
     GH.check_attention(res, hc, all_heads(w)[:4], m)
+    GH.check_decode_step_path(w, res, hc, all_heads(w)[:4], m, ws=res["ws"])
 
 
 VARIANT_CASES = [
@@ -260,6 +264,7 @@ def test_strided_views():
     hc = GH.HostCopy(base, K=K, V=V)
     GH.check_selection(res, hc, all_heads(base), base.m)
     GH.check_attention(res, hc, all_heads(base), base.m)
+    GH.check_decode_step_path(base, res, hc, all_heads(base), base.m, ws=res["ws"], K=K, V=V)
 
 
 def test_dense_path_equals_full_attention():
