@@ -176,7 +176,10 @@ int32_t hash_attn_select_capacity(int32_t n_cap, int32_t m, int32_t n_sink, int3
  * since a row of one head's set is multiplied by weight 0 into the others').
  * The scan may start while the previous kernel in the stream drains: it waits
  * for it before writing workspace state. Otherwise the selection writes per-head
- * lists (or sel_idx) and GATHER-ATT runs per query head.
+ * lists (or sel_idx) and GATHER-ATT runs per query head. The dense path runs one
+ * kernel: per GQA group on the same shapes (each row read once per group; its
+ * copies may start while the previous kernel drains, its results are written
+ * after it), else per query head.
  * Errors: HA_ERR_INVALID_ARG, HA_ERR_UNSUPPORTED, HA_ERR_WORKSPACE before
  * launch; HA_ERR_CUDA on a failed launch.
  */

@@ -79,8 +79,9 @@ int fused_ranges(int n_cap);
 // Full layout; with_selection=false leaves out the selection regions. With a
 // fused plan the selection regions are the flat lists; otherwise the chunk
 // histograms, segments and threshold metadata of the two-kernel path.
+// dense_parts: room for the partials of the dense path on the group kernel.
 Layout make_layout(const ha_shape& s, int64_t rows_cap, bool with_selection, int nbins = HA_NBINS,
-                   int code_words = 1);
+                   int code_words = 1, bool dense_parts = false);
 
 // ------------------------------------------------------------------ parameters
 
@@ -321,6 +322,11 @@ bool group_att_supported(int d, int kv_bf16, int q_bf16, int G);
 // CTAs per range of k_group_att for (batch entry, KV head) pairs x ranges.
 int group_splits(int64_t pair_ranges);
 cudaError_t launch_group_att(const GroupAttParams& p, int d, int batch_hkv, cudaStream_t st, bool pdl);
+// The dense path on the same kernel: every token of the sequence for every head
+// of the group, ranges of 8192 tokens cut into group_dense_splits spans (p.sel
+// needs only the shape fields, seq_lens, nranges and err; p.sel.ready null).
+int group_dense_splits(int64_t batch_hkv, int n_cap);
+cudaError_t launch_group_dense(const GroupAttParams& p, int d, int batch_hkv, cudaStream_t st, bool pdl);
 cudaError_t launch_merge_n(const MergeNParams& p, cudaStream_t st);
 cudaError_t launch_encode(const EncodeParams& p, cudaStream_t st);
 cudaError_t launch_encode_mlp(const EncodeParams& p, cudaStream_t st);

@@ -354,6 +354,28 @@ FusedSelParams fused_params(const ha_shape* s, const Layout& lay, void* ws, cons
     return p;
 }
 
+// The dense path runs on the group kernel for the shapes it takes (element
+// strides of K/V rows below 2^30).
+bool dense_group(const ha_shape& s) {
+    return group_att_supported(s.d, s.kv_dtype == HA_BF16, s.q_dtype == HA_BF16, s.h_q / s.h_kv) &&
+           s.k_sn < (int64_t(1) << 30) && s.v_sn < (int64_t(1) << 30);
+}
+
+// The group kernel's parameters on the dense path: the shape, the lengths and the
+// error word; no codes, budgets or selection buffers.
+FusedSelParams dense_sel_params(const ha_shape* s, const Views& v, const int32_t* seq_lens) {
+    FusedSelParams p{};
+    p.seq_lens = seq_lens;
+    p.B = s->batch;
+    p.Hq = s->h_q;
+    p.Hkv = s->h_kv;
+    p.G = s->h_q / s->h_kv;
+    p.n_cap = s->n_cap;
+    p.nranges = fused_ranges(s->n_cap);
+    p.err = v.err;
+    return p;
+}
+
 // The signature map run ahead of SCORE (hash_attn_decode_mapped): the appended
 // tokens' key codes (optional) and the step's query codes.
 struct MapStep {
@@ -378,7 +400,7 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
     if ((sel_idx == nullptr) != (sel_cnt == nullptr))
         return fail(HA_ERR_INVALID_ARG, "sel_idx and sel_cnt must both be given or both be NULL");
     const int64_t rows_cap = dense ? s->n_cap : rows_cap_of(s->n_cap, m, n_sink, n_local);
-    const Layout lay = make_layout(*s, rows_cap, !dense, nbins_of(opts), W);
+    const Layout lay = make_layout(*s, rows_cap, !dense, nbins_of(opts), W, dense);
     HA_TRY(check_segments(lay));
     HA_TRY(check_ws(lay, ws, ws_bytes));
     if (check_only) return HA_OK;
@@ -398,8 +420,18 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
         HA_TRY(record(events, 0, st));
         HA_TRY(record(events, 1, st));
         HA_TRY(record(events, 2, st));
-        gp.mode = kIdentity;
-        HA_LAUNCH(launch_gather(gp, s->d, s->kv_dtype == HA_BF16, st), "GATHER-ATT launch");
+        if (dense_group(*s)) {
+            // one CTA per (batch entry, KV head, span of a range): each K/V row once
+            // for the whole group
+            GroupAttParams ga{};
+            ga.sel = dense_sel_params(s, v, seq_lens);
+            ga.att = gp;
+            ga.nsplit = group_dense_splits(bhkv, s->n_cap);
+            HA_LAUNCH(launch_group_dense(ga, s->d, bhkv, st, true), "GATHER-ATT launch");
+        } else {
+            gp.mode = kIdentity;
+            HA_LAUNCH(launch_gather(gp, s->d, s->kv_dtype == HA_BF16, st), "GATHER-ATT launch");
+        }
         HA_TRY(record(events, 3, st));
         return HA_OK;
     }
@@ -614,7 +646,8 @@ void choose_splits(int64_t heads, int64_t rows_cap, int* splits, int* rows_per_s
     *rows_per_split = (int)rps;
 }
 
-Layout make_layout(const ha_shape& s, int64_t rows_cap, bool with_selection, int nbins, int code_words) {
+Layout make_layout(const ha_shape& s, int64_t rows_cap, bool with_selection, int nbins, int code_words,
+                   bool dense_parts) {
     Layout L;
     L.heads = s.batch * s.h_q;
     L.rows_cap = (int)rows_cap;
@@ -668,10 +701,13 @@ Layout make_layout(const ha_shape& s, int64_t rows_cap, bool with_selection, int
             off = align_up(off + (size_t)L.heads * L.nseg * L.seg_cap * 4, 256);
         }
     }
-    // split-K partials; the group kernel keeps one per (head, range) of the fused plan
-    const int psplits =
-        L.fused ? std::max<int64_t>(L.splits, (int64_t)L.nranges * group_splits((int64_t)s.batch * s.h_kv * L.nranges))
-                : L.splits;
+    // split-K partials; the group kernel keeps one per (head, range, split) of the
+    // fused plan, or per (head, range, span) on the dense path
+    const int64_t pairs = (int64_t)s.batch * s.h_kv;
+    int64_t psplits = L.splits;
+    if (L.fused) psplits = std::max<int64_t>(psplits, (int64_t)L.nranges * group_splits(pairs * L.nranges));
+    if (dense_parts && dense_group(s))
+        psplits = std::max<int64_t>(psplits, (int64_t)fused_ranges(s.n_cap) * group_dense_splits(pairs, s.n_cap));
     L.off_part = off;
     off = align_up(off + (size_t)L.heads * psplits * (s.d + 2) * 4, 256);
     L.total = off;
@@ -693,7 +729,7 @@ ha_status hash_attn_workspace_size(const ha_shape* shape, int32_t m_max, int32_t
     // the selection regions are always included so that hash_attn_select and
     // hash_attn_score work with any budget on the same workspace
     const int64_t rows_cap = dense ? shape->n_cap : rows_cap_of(shape->n_cap, m_max, n_sink, n_local);
-    const Layout sparse = make_layout(*shape, rows_cap, true);
+    const Layout sparse = make_layout(*shape, rows_cap, true, HA_NBINS, 1, dense);
     HA_TRY(check_segments(sparse));
     *bytes = sparse.total;
     return HA_OK;
@@ -707,7 +743,7 @@ ha_status hash_attn_workspace_size_ex(const ha_shape* shape, int32_t m_max, int3
     if (bytes == nullptr) return fail(HA_ERR_INVALID_ARG, "bytes is NULL");
     const bool dense = m_max >= shape->n_cap;
     const int64_t rows_cap = dense ? shape->n_cap : rows_cap_of(shape->n_cap, m_max, n_sink, n_local);
-    const Layout sparse = make_layout(*shape, rows_cap, true, nbins_of(opts), code_words_of(opts));
+    const Layout sparse = make_layout(*shape, rows_cap, true, nbins_of(opts), code_words_of(opts), dense);
     HA_TRY(check_segments(sparse));
     *bytes = sparse.total;
     return HA_OK;

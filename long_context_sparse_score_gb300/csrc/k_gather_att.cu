@@ -440,232 +440,6 @@ __global__ void __launch_bounds__(kGatherThreads, (D * sizeof(KT) <= 256) ? 5 : 
     if (tid == 0) p.counters[head] = 0u;
 }
 
-// Dense GATHER-ATT for a GQA group (bf16 query and K/V, four query heads per KV
-// head): one CTA per (batch entry, KV head, split of the rows) with one warp per
-// query head. All 128 threads copy each stage of 32 K and V rows once into a
-// shared ring of three stages (16-byte cp.async), and the four warps read them
-// from there, so every cached row costs one memory request instead of one per
-// query head. Per warp the arithmetic is that of k_gather_att (query as packed
-// bf16 in registers, fp32 online softmax in base 2); splits merge as there.
-template <int D>
-__global__ void __launch_bounds__(kGatherThreads, 4) k_gather_group(const GatherParams p) {
-    using C = Cfg<D, __nv_bfloat16>;
-    constexpr int T = 32;                        // rows per stage
-    constexpr int P = 3;                         // stages
-    constexpr int STAGE = 2 * T * C::PITCH;      // K rows, then V rows
-    constexpr int QW = D / 8;
-    extern __shared__ __align__(128) unsigned char smem[];
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    int lin = blockIdx.x;
-    const int split = lin % p.splits;
-    lin /= p.splits;
-    const int b = lin % p.B;
-    const int g = lin / p.B;
-    const int head = b * p.Hq + g * p.G + warp;  // this warp's query head
-    const int n = checked_len(p.seq_lens, b, p.n_cap, p.err, split == 0 && g == 0 && tid == 0);
-    const int r0 = split * p.rows_per_split;
-    const int nrows = max(0, min(n, r0 + p.rows_per_split) - r0);
-    const int r = lane & 7, qt = lane >> 3;
-
-    uint32_t qreg[QW];
-    {
-        const uint16_t* qh16 = reinterpret_cast<const uint16_t*>(p.q) + (int64_t)b * p.q_sb +
-                               (int64_t)(g * p.G + warp) * p.q_sh;
-#pragma unroll
-        for (int jc = 0; jc < QW / 4; ++jc)
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int dim = (jc * 4 + qt) * 8 + 2 * u;
-                qreg[jc * 4 + u] = (uint32_t)qh16[dim] | ((uint32_t)qh16[dim + 1] << 16);
-            }
-    }
-    pdl_launch_dependents();
-    pdl_wait();
-
-    const char* Kb = p.K + ((int64_t)b * p.k_sb + (int64_t)g * p.k_sh) * C::ES;
-    const char* Vb = p.V + ((int64_t)b * p.v_sb + (int64_t)g * p.v_sh) * C::ES;
-    const int64_t kstep = p.k_sn * C::ES, vstep = p.v_sn * C::ES;
-    const int nst = (nrows + T - 1) / T;
-    auto issue = [&](int k) {
-        unsigned char* stg = smem + (k % P) * STAGE;
-#pragma unroll
-        for (int it = tid; it < T * 2 * C::NCH; it += kGatherThreads) {
-            const int row = it / (2 * C::NCH);
-            const int rem = it - row * (2 * C::NCH);
-            const int isv = rem >= C::NCH ? 1 : 0;
-            const int ch = rem - isv * C::NCH;
-            const int rr = k * T + row;
-            if (rr < nrows) {
-                const int64_t tok = r0 + rr;
-                const char* src = (isv ? Vb + tok * vstep : Kb + tok * kstep) + ch * 16;
-                cp_async16(smem_addr(stg + (isv * T + row) * C::PITCH + ch * 16), src);
-            }
-        }
-    };
-
-    float2 ov[C::DPL / 2];
-#pragma unroll
-    for (int i = 0; i < C::DPL / 2; ++i) ov[i] = make_float2(0.f, 0.f);
-    float mrun = -CUDART_INF_F, lrun = 0.f;
-#pragma unroll
-    for (int k = 0; k < P - 1; ++k) {
-        if (k < nst) issue(k);
-        cp_async_commit();
-    }
-    for (int k = 0; k < nst; ++k) {
-        if (k + P - 1 < nst) issue(k + P - 1);
-        cp_async_commit();
-        cp_async_wait<P - 1>();
-        __syncthreads();  // stage k has landed, from every thread's copies
-        const unsigned char* stg = smem + (k % P) * STAGE;
-#pragma unroll
-        for (int sub = 0; sub < T / 8; ++sub) {
-            const int rr = k * T + sub * 8 + r;
-            const bool ok = rr < nrows;
-            const unsigned char* kr = stg + (sub * 8 + r) * C::PITCH;
-            const unsigned char* vr = kr + T * C::PITCH;
-            float part = 0.f;
-            if (ok) {
-                float a[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int jc = 0; jc < C::CPL; ++jc) {
-                    const uint4 w = *reinterpret_cast<const uint4*>(kr + (jc * 4 + qt) * 16);
-                    a[0] = fma_bf16x2(qreg[jc * 4 + 0], w.x, a[0]);
-                    a[1] = fma_bf16x2(qreg[jc * 4 + 1], w.y, a[1]);
-                    a[2] = fma_bf16x2(qreg[jc * 4 + 2], w.z, a[2]);
-                    a[3] = fma_bf16x2(qreg[jc * 4 + 3], w.w, a[3]);
-                }
-                part = (a[0] + a[1]) + (a[2] + a[3]);
-            }
-            part += __shfl_xor_sync(0xffffffffu, part, 8);
-            part += __shfl_xor_sync(0xffffffffu, part, 16);
-            const float sc = ok ? part * p.qscale : -CUDART_INF_F;
-            float mx = sc;
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-            const float mnew = fmaxf(mrun, mx);
-            if (mnew != -CUDART_INF_F) {
-                if (mnew > mrun) {
-                    const float alpha = exp2f(mrun - mnew);
-                    lrun *= alpha;
-#pragma unroll
-                    for (int i = 0; i < C::DPL / 2; ++i) ov[i] = __fmul2_rn(ov[i], make_float2(alpha, alpha));
-                    mrun = mnew;
-                }
-                const float pr = exp2f(sc - mnew);
-                float ps = pr;
-                ps += __shfl_xor_sync(0xffffffffu, ps, 1);
-                ps += __shfl_xor_sync(0xffffffffu, ps, 2);
-                ps += __shfl_xor_sync(0xffffffffu, ps, 4);
-                lrun += ps;
-                if (ok) {
-                    const float2 pp2 = make_float2(pr, pr);
-#pragma unroll
-                    for (int jc = 0; jc < C::CPL; ++jc) {
-                        const uint4 w = *reinterpret_cast<const uint4*>(vr + (jc * 4 + qt) * 16);
-                        float f[C::EPC];
-                        chunk_to_float<__nv_bfloat16>(w, f);
-#pragma unroll
-                        for (int e = 0; e < C::EPC; e += 2)
-                            ov[(jc * C::EPC + e) / 2] =
-                                __ffma2_rn(pp2, make_float2(f[e], f[e + 1]), ov[(jc * C::EPC + e) / 2]);
-                    }
-                }
-            }
-        }
-        __syncthreads();  // every warp is done with stage k before it is refilled
-    }
-    cp_async_wait<0>();
-
-    // ---- per warp: sum the 8 row lanes of each dim group (lanes r == 0 hold the sums)
-#pragma unroll
-    for (int i = 0; i < C::DPL / 2; ++i) {
-#pragma unroll
-        for (int o = 1; o < 8; o <<= 1) {
-            ov[i].x += __shfl_xor_sync(0xffffffffu, ov[i].x, o);
-            ov[i].y += __shfl_xor_sync(0xffffffffu, ov[i].y, o);
-        }
-    }
-    constexpr float kLn2 = 0.69314718055994530942f;
-    if (p.splits == 1) {
-        if (r == 0) {
-            const float inv = (lrun > 0.f) ? 1.f / lrun : 0.f;
-#pragma unroll
-            for (int jc = 0; jc < C::CPL; ++jc) {
-                const int dim0 = (jc * 4 + qt) * C::EPC;
-#pragma unroll
-                for (int e = 0; e < C::EPC; e += 2) {
-                    p.out[(int64_t)head * D + dim0 + e] = ov[(jc * C::EPC + e) / 2].x * inv;
-                    p.out[(int64_t)head * D + dim0 + e + 1] = ov[(jc * C::EPC + e) / 2].y * inv;
-                }
-            }
-        }
-        if (lane == 0) p.lse[head] = (lrun > 0.f) ? (mrun + log2f(lrun)) * kLn2 : -CUDART_INF_F;
-        return;
-    }
-    float* pt = p.part + ((int64_t)head * p.splits + split) * (D + 2);
-    if (r == 0) {
-#pragma unroll
-        for (int jc = 0; jc < C::CPL; ++jc) {
-            const int dim0 = (jc * 4 + qt) * C::EPC;
-#pragma unroll
-            for (int e = 0; e < C::EPC; e += 2) {
-                pt[2 + dim0 + e] = ov[(jc * C::EPC + e) / 2].x;
-                pt[2 + dim0 + e + 1] = ov[(jc * C::EPC + e) / 2].y;
-            }
-        }
-    }
-    if (lane == 0) {
-        pt[0] = mrun;
-        pt[1] = lrun;
-    }
-    __syncwarp();  // every partial store of this warp precedes lane 0's fence
-    unsigned last = 0u;
-    if (lane == 0) {
-        __threadfence();
-        const unsigned prev = atomicAdd(&p.counters[head], 1u);
-        if (prev >= (unsigned)p.splits) flag_error(p.err, HA_DEVERR_STATE);
-        last = (prev == (unsigned)(p.splits - 1)) ? 1u : 0u;
-    }
-    if (__shfl_sync(0xffffffffu, last, 0) == 0u) return;
-    __threadfence();
-    const float* ph = p.part + (int64_t)head * p.splits * (D + 2);
-    float M = -CUDART_INF_F;
-    for (int sp = 0; sp < p.splits; ++sp) M = fmaxf(M, __ldcg(ph + (int64_t)sp * (D + 2)));
-    float Ls = 0.f, O[D / 32];
-#pragma unroll
-    for (int i = 0; i < D / 32; ++i) O[i] = 0.f;
-    if (M != -CUDART_INF_F) {
-        for (int sp = 0; sp < p.splits; ++sp) {
-            const float ms = __ldcg(ph + (int64_t)sp * (D + 2));
-            if (ms != -CUDART_INF_F) {
-                const float sc = exp2f(ms - M);
-                Ls += __ldcg(ph + (int64_t)sp * (D + 2) + 1) * sc;
-#pragma unroll
-                for (int i = 0; i < D / 32; ++i) O[i] += __ldcg(ph + (int64_t)sp * (D + 2) + 2 + i * 32 + lane) * sc;
-            }
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < D / 32; ++i) p.out[(int64_t)head * D + i * 32 + lane] = (Ls > 0.f) ? O[i] / Ls : 0.f;
-    if (lane == 0) {
-        p.lse[head] = (Ls > 0.f) ? (M + log2f(Ls)) * kLn2 : -CUDART_INF_F;
-        p.counters[head] = 0u;
-    }
-}
-
-template <int D>
-cudaError_t launch_group_t(const GatherParams& p, cudaStream_t st, bool pdl) {
-    using C = Cfg<D, __nv_bfloat16>;
-    const size_t smem = (size_t)3 * 2 * 32 * C::PITCH;
-    cudaError_t e = cudaFuncSetAttribute(k_gather_group<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)(p.B * p.Hkv) * (unsigned)p.splits;
-    return launch_ex(k_gather_group<D>, dim3(grid), dim3(kGatherThreads), smem, st, pdl, p);
-}
-
 // Exact merge of two partial attentions (Nectar Eq. (3.4)); one warp per row.
 __global__ void __launch_bounds__(256) k_merge(const MergeParams p) {
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -701,11 +475,6 @@ cudaError_t launch_gather_t(const GatherParams& p, cudaStream_t st, bool pdl) {
 }  // namespace
 
 cudaError_t launch_gather(const GatherParams& p, int d, int kv_bf16, cudaStream_t st, bool pdl) {
-    // every row for every query head (the dense path): one read of each row per GQA group of four
-    if (p.mode == kIdentity && p.G == 4 && kv_bf16 && p.q_bf16) {
-        if (d == 128) return launch_group_t<128>(p, st, pdl);
-        if (d == 64) return launch_group_t<64>(p, st, pdl);
-    }
     if (d == 128 && kv_bf16 && p.q_bf16) return launch_gather_t<128, __nv_bfloat16, true>(p, st, pdl);
     if (d == 64 && kv_bf16 && p.q_bf16) return launch_gather_t<64, __nv_bfloat16, true>(p, st, pdl);
     if (d == 128 && kv_bf16) return launch_gather_t<128, __nv_bfloat16, false>(p, st, pdl);

@@ -38,6 +38,10 @@
 // a contiguous half of its chunks (both build the masks).
 // K/V must be finite: a row selected by one head of the group is also multiplied
 // (by weight zero) into the other heads' P.V.
+// The dense path (I = every token; HashAttention Sec. 4 with m >= n) runs the
+// same kernel without step 1: a range's tokens are its rows, all heads' bits
+// set, cut into spans of chunks (group_dense_splits CTAs per range), and no scan
+// precedes it.
 #include "ha_internal.cuh"
 #include "sel_common.cuh"
 
@@ -130,7 +134,9 @@ __device__ __forceinline__ void commit_group() { asm volatile("cp.async.commit_g
 template <int N>
 __device__ __forceinline__ void wait_group() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-template <int D, int ST>
+// DENSE: every token of the range is a row of every head of the group (no codes,
+// no scan, no masks); the rows of a range are cut into contiguous spans of chunks.
+template <int D, int ST, bool DENSE>
 __global__ void __launch_bounds__(kGT, GCfg<D, ST>::MINB) k_group_att(const GroupAttParams gp) {
     using C = GCfg<D, ST>;
     const FusedSelParams& p = gp.sel;
@@ -167,7 +173,7 @@ __global__ void __launch_bounds__(kGT, GCfg<D, ST>::MINB) k_group_att(const Grou
     // (b0) and 8 + 2 (lane % 4) + {0, 1} (b1) of every 16-dim k-step
     uint32_t qs[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) qs[e] = (e < nh) ? p.q_sig[head0 + e] : 0u;
+    for (int e = 0; e < 4; ++e) qs[e] = (!DENSE && e < nh) ? p.q_sig[head0 + e] : 0u;
     uint32_t qb[C::KS][2];
     {
         const int hq = lane >> 2, qq = lane & 3;
@@ -186,7 +192,10 @@ __global__ void __launch_bounds__(kGT, GCfg<D, ST>::MINB) k_group_att(const Grou
     // Every scan CTA is resident before this grid starts (programmatic launch), so
     // the flag comes; the wait is bounded all the same.
     __shared__ int s_go;
-    if (p.ready != nullptr) {
+    if (DENSE) {
+        // nothing to wait for before the copies: the inputs are the caller's, and the
+        // partials and counters are written after the wait below
+    } else if (p.ready != nullptr) {
         if (tid == 0) {
             int ok = 0;
             const unsigned long long t0 = global_ns();
@@ -213,7 +222,13 @@ __global__ void __launch_bounds__(kGT, GCfg<D, ST>::MINB) k_group_att(const Grou
     }
 
     // ---- 1. masks
-    int T[4], Tsel[4], qv[4], expect[4], mode[4];
+    uint32_t msk[kIt][4], uni[kIt];
+    int uex[kIt], expect[4];
+    int U = 0;
+    if constexpr (DENSE) {
+        U = max(0, min(n - lo, kFusedRange));  // the range's tokens, in order
+    } else {
+    int T[4], Tsel[4], qv[4], mode[4];
     bool any2 = false;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -233,7 +248,7 @@ __global__ void __launch_bounds__(kGT, GCfg<D, ST>::MINB) k_group_att(const Grou
         any2 = any2 || mode[e] == 2;
     }
     const uint32_t* crow = p.k_sig + (int64_t)b * p.ks_sb + (int64_t)g * p.ks_sh;
-    uint32_t msk[kIt][4], eqm[kIt][4], validv[kIt], winv[kIt];
+    uint32_t eqm[kIt][4], validv[kIt], winv[kIt];
 #pragma unroll
     for (int it = 0; it < kIt; ++it) {
         const int lb = lo + (it * kGT + tid) * 32;  // this thread's lane block
@@ -308,8 +323,6 @@ __global__ void __launch_bounds__(kGT, GCfg<D, ST>::MINB) k_group_att(const Grou
     }
     // ---- the union of the heads' masks: its rows go to a list in token order,
     // entry = offset in the range | head bits << 16
-    uint32_t uni[kIt];
-    int uex[kIt];
 #pragma unroll
     for (int it = 0; it < kIt; ++it) {
         uint32_t u = 0u;
@@ -333,12 +346,13 @@ __global__ void __launch_bounds__(kGT, GCfg<D, ST>::MINB) k_group_att(const Grou
     // range * 8192 + (tokens of the range) <= n <= n_cap <= d_sp.
     // Split `split` of S takes chunks [c0, c1) of the range's union and writes only
     // their entries (the splits of a range write disjoint parts of the list).
-    uint32_t* lst = p.dist + (int64_t)pair * p.d_sp + (int64_t)range * kFusedRange;
-    int U = 0;
     for (int i2 = 0; i2 < kIt; ++i2)
         for (int w2 = 0; w2 < kGW; ++w2) U += s_wu[i2][w2];
+    }
+    uint32_t* lst = p.dist + (int64_t)pair * p.d_sp + (int64_t)range * kFusedRange;
     const int nch = (U + kCR - 1) / kCR;
     const int c0 = (int)((int64_t)split * nch / S), c1 = (int)((int64_t)(split + 1) * nch / S);
+    if constexpr (!DENSE) {
     const int p0 = c0 * kCR, p1 = min(U, c1 * kCR);
 #pragma unroll
     for (int it = 0; it < kIt; ++it) {
@@ -374,6 +388,7 @@ __global__ void __launch_bounds__(kGT, GCfg<D, ST>::MINB) k_group_att(const Grou
             if (e == tid && mine != expect[e]) flag_error(p.err, HA_DEVERR_STATE);  // masks disagree with the scan
     }
     __syncthreads();  // the list is written (block-scope visibility)
+    }
 
     // ---- 2. attention over the union, per warp
     const int ncw = (c1 - c0 > warp) ? (c1 - c0 - warp + kGW - 1) / kGW : 0;
@@ -399,6 +414,7 @@ __global__ void __launch_bounds__(kGT, GCfg<D, ST>::MINB) k_group_att(const Grou
     auto entry = [&](int k) -> uint32_t {
         const int pos = (c0 + warp + k * kGW) * kCR + lane;
         if (lane >= kCR || k >= ncw || pos >= U) return 0u;
+        if constexpr (DENSE) return (uint32_t)pos | (((1u << nh) - 1u) << 16);
         return pos < C::LCAP ? s_lst[pos] : lst[pos];
     };
     auto issue = [&](int k, uint32_t ent) {
@@ -514,7 +530,8 @@ __global__ void __launch_bounds__(kGT, GCfg<D, ST>::MINB) k_group_att(const Grou
     }
     wait_group<0>();
     // the whole scan grid has completed long before: this orders the next kernel
-    // in the stream after it
+    // in the stream after it (dense: the previous kernel in the stream is done with
+    // the partials and counters before this CTA writes them)
     pdl_wait();
 
     // ---- 3. combine the warps, then the ranges
@@ -617,13 +634,14 @@ __global__ void __launch_bounds__(kGT, GCfg<D, ST>::MINB) k_group_att(const Grou
     }
 }
 
-template <int D, int ST>
+template <int D, int ST, bool DENSE>
 cudaError_t launch_group_t(const GroupAttParams& p, int batch_hkv, cudaStream_t st, bool pdl) {
     using C = GCfg<D, ST>;
-    cudaError_t e = cudaFuncSetAttribute(k_group_att<D, ST>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES);
+    cudaError_t e =
+        cudaFuncSetAttribute(k_group_att<D, ST, DENSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)batch_hkv * (unsigned)p.sel.nranges * (unsigned)p.nsplit;
-    return launch_ex(k_group_att<D, ST>, dim3(grid), dim3(kGT), (size_t)C::BYTES, st, pdl, p);
+    return launch_ex(k_group_att<D, ST, DENSE>, dim3(grid), dim3(kGT), (size_t)C::BYTES, st, pdl, p);
 }
 
 }  // namespace
@@ -640,8 +658,26 @@ bool group_att_supported(int d, int kv_bf16, int q_bf16, int G) {
 
 cudaError_t launch_group_att(const GroupAttParams& p, int d, int batch_hkv, cudaStream_t st, bool pdl) {
     if (p.nsplit < 1) return cudaErrorInvalidValue;
-    if (d == 128) return launch_group_t<128, 2>(p, batch_hkv, st, pdl);
-    if (d == 64) return launch_group_t<64, 2>(p, batch_hkv, st, pdl);
+    if (d == 128) return launch_group_t<128, 2, false>(p, batch_hkv, st, pdl);
+    if (d == 64) return launch_group_t<64, 2, false>(p, batch_hkv, st, pdl);
+    return cudaErrorInvalidValue;
+}
+
+int group_dense_splits(int64_t batch_hkv, int n_cap) {
+    // spans of about 2,048 rows; fewer per range when a head would get more than
+    // 64 partials, more while the grid would not give each SM two CTAs
+    const int64_t nr = fused_ranges(n_cap);
+    const int r = std::min(n_cap, kFusedRange);
+    int s = std::max(1, r / 2048);
+    while (s > 1 && nr * s > 64) s /= 2;
+    while (s < 16 && batch_hkv * nr * s < 2 * kSMs && r / (2 * s) >= 256) s *= 2;
+    return s;
+}
+
+cudaError_t launch_group_dense(const GroupAttParams& p, int d, int batch_hkv, cudaStream_t st, bool pdl) {
+    if (p.nsplit < 1 || p.sel.ready != nullptr) return cudaErrorInvalidValue;
+    if (d == 128) return launch_group_t<128, 2, true>(p, batch_hkv, st, pdl);
+    if (d == 64) return launch_group_t<64, 2, true>(p, batch_hkv, st, pdl);
     return cudaErrorInvalidValue;
 }
 

@@ -261,21 +261,33 @@ def test_single_sequence_two_kernel_path_long():
 # ---------------------------------------------------------------- dense path: one read per GQA group
 
 DENSE_GROUP = [
-    # name, B, Hq, Hkv, d, n_cap, lens, shared
-    ("many_splits_ragged", 3, 8, 2, 128, 40000, [40000, 1, 0], False),
-    ("d64_odd_lengths", 2, 4, 1, 64, 700, [700, 333], False),
-    ("one_split", 2, 8, 2, 128, 50, [50, 17], False),
-    ("shared_cache", 4, 8, 2, 128, 5000, [5000, 4999, 3, 2500], True),
+    # name, B, Hq, Hkv, d, n_cap, lens, shared, kv dtype
+    ("many_splits_ragged", 3, 8, 2, 128, 40000, [40000, 1, 0], False, "bf16"),
+    ("d64_odd_lengths", 2, 4, 1, 64, 700, [700, 333], False, "bf16"),
+    ("one_split", 2, 8, 2, 128, 50, [50, 17], False, "bf16"),
+    ("shared_cache", 4, 8, 2, 128, 5000, [5000, 4999, 3, 2500], True, "bf16"),
+    # one, two and three query heads per KV head; range boundaries and ragged tails
+    ("g1_two_ranges", 2, 4, 4, 128, 9000, [9000, 8193], False, "bf16"),
+    ("g2_d64_three_ranges", 2, 4, 2, 64, 17000, [17000, 123], False, "bf16"),
+    ("g3_ragged_tail", 1, 6, 2, 128, 20000, [19999], False, "bf16"),
+    # spans of 2,048 rows over 16 ranges of a long sequence (64 partials per head)
+    ("long_sequence", 4, 8, 2, 128, 131072, [131072, 131071, 65536, 8191], False, "bf16"),
+    # float32 K/V: the per-head kernel
+    ("fp32_per_head", 2, 8, 2, 64, 3000, [3000, 1500], False, "f32"),
 ]
 
 
 @pytest.mark.parametrize("case", DENSE_GROUP, ids=[c[0] for c in DENSE_GROUP])
 def test_dense_group_kernel(case):
-    """The dense path (m >= n_cap) with four query heads per KV head reads each row
-    once for the group; every head must equal full attention over its sequence."""
-    name, B, Hq, Hkv, d, n_cap, lens, shared = case
+    """The dense path (m >= n_cap) reads each row once for the GQA group on
+    bf16 K/V (1 to 4 query heads per KV head); every head must equal full
+    attention over its sequence."""
+    name, B, Hq, Hkv, d, n_cap, lens, shared, kvd = case
     w = W().make_gqa(39, B=B, Hq=Hq, Hkv=Hkv, d=d, n_cap=n_cap, seq_lens=lens, m=0, n_sink=0, n_local=0,
-                     device="cuda", shared=shared, name=name)
+                     device="cuda", shared=shared, name=name,
+                     kv_dtype=torch.bfloat16 if kvd == "bf16" else torch.float32)
+    if kvd == "f32":
+        w.q = w.q.float()
     res = GH.run_decode(w, m=n_cap, dense=True, m_per_seq=None, sel=False)
     assert res["status"] == 0, hex(res["flags"])
     hc = GH.HostCopy(w)
