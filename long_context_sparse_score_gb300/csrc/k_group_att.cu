@@ -35,7 +35,8 @@
 //     per head; the last CTA of a (batch entry, KV head) to arrive merges the
 //     ranges of its heads (an arrival counter decides; nothing waits).
 // When the grid would not give every SM a CTA, two CTAs share a range, each with
-// a contiguous half of its chunks (both build the masks).
+// a contiguous half of its chunks (both build the masks), and each CTA has eight
+// warps (one CTA per SM, the whole list in shared memory).
 // K/V must be finite: a row selected by one head of the group is also multiplied
 // (by weight zero) into the other heads' P.V.
 // The dense path (I = every token; HashAttention Sec. 4 with m >= n) runs the
@@ -50,25 +51,27 @@
 namespace ha {
 namespace {
 
-constexpr int kGT = 128;                 // threads per CTA
-constexpr int kGW = kGT / 32;            // warps
 constexpr int kLB = kFusedRange / 32;    // lane blocks of 32 tokens per range
-constexpr int kIt = kLB / kGT;           // lane blocks per thread
 constexpr int kCR = 16;                  // union rows per warp chunk
-static_assert(kLB % kGT == 0, "whole lane blocks per thread");
 
-template <int D, int ST>
+// NW warps per CTA: 4 (three CTAs per SM) or 8 (one CTA per SM, for grids that
+// give no SM a second CTA: half the serial mask work and chunks per warp)
+template <int D, int ST, int NW>
 struct GCfg {
+    static constexpr int GW = NW;                      // warps
+    static constexpr int GT = 32 * NW;                 // threads
+    static constexpr int IT = kLB / GT;                // lane blocks per thread
+    static_assert(kLB % GT == 0, "whole lane blocks per thread");
     static constexpr int RB = 2 * D;                   // bytes of a bf16 row
     static constexpr int PITCH = RB + 16;              // 8 rows of an ldmatrix land on distinct banks
     static constexpr int NCH = RB / 16;                // 16-byte chunks per row
     static constexpr int RPI = 32 / (2 * NCH);         // chunk rows per copy instruction of the warp
     static constexpr int STAGE = 2 * kCR * PITCH;      // K rows, then V rows
-    static constexpr int RING = kGW * ST * STAGE;
+    static constexpr int RING = GW * ST * STAGE;
     static constexpr int KS = D / 16;                  // k-steps of K Q^T, m-tiles of V^T P^T
-    static constexpr int MINB = (ST >= 3) ? 2 : 3;     // CTAs per SM
-    static constexpr int OFF_HB = RING;                // int [kGW][ST][kCR] head bits of the ring's rows
-    static constexpr int OFF_LST = OFF_HB + kGW * ST * kCR * 4;  // uint32 [LCAP] the list's first entries
+    static constexpr int MINB = (NW > 4) ? 1 : ((ST >= 3) ? 2 : 3);  // CTAs per SM
+    static constexpr int OFF_HB = RING;                // int [GW][ST][kCR] head bits of the ring's rows
+    static constexpr int OFF_LST = OFF_HB + GW * ST * kCR * 4;  // uint32 [LCAP] the list's first entries
     // what the shared memory of an SM leaves a CTA beside MINB - 1 others (228 KB,
     // 1 KB reserved per CTA, the static arrays), in 16-entry chunks
     static constexpr int SMEM_CTA = (228 * 1024) / MINB - 1024 - 1024;
@@ -76,8 +79,8 @@ struct GCfg {
     static constexpr int LCAP = LCAP_FIT < kFusedRange ? LCAP_FIT : kFusedRange;
     static constexpr int BYTES = OFF_LST + LCAP * 4;
     static_assert(LCAP >= kCR, "room for a list chunk in shared memory");
-    // combine area (reuses the ring): o [kGW][4][D], m [kGW][4], l [kGW][4]
-    static_assert((kGW * 4 * D + 2 * kGW * 4) * 4 <= RING, "combine fits in the ring");
+    // combine area (reuses the ring): o [GW][4][D], m [GW][4], l [GW][4]
+    static_assert((GW * 4 * D + 2 * GW * 4) * 4 <= RING, "combine fits in the ring");
     static_assert(RPI * 2 * NCH == 32, "whole rows per copy instruction");
 };
 
@@ -136,9 +139,10 @@ __device__ __forceinline__ void wait_group() { asm volatile("cp.async.wait_group
 
 // DENSE: every token of the range is a row of every head of the group (no codes,
 // no scan, no masks); the rows of a range are cut into contiguous spans of chunks.
-template <int D, int ST, bool DENSE>
-__global__ void __launch_bounds__(kGT, GCfg<D, ST>::MINB) k_group_att(const GroupAttParams gp) {
-    using C = GCfg<D, ST>;
+template <int D, int ST, bool DENSE, int NW>
+__global__ void __launch_bounds__(32 * NW, GCfg<D, ST, NW>::MINB) k_group_att(const GroupAttParams gp) {
+    using C = GCfg<D, ST, NW>;
+    constexpr int kGT = C::GT, kGW = C::GW, kIt = C::IT;
     const FusedSelParams& p = gp.sel;
     const GatherParams& a = gp.att;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -634,14 +638,14 @@ __global__ void __launch_bounds__(kGT, GCfg<D, ST>::MINB) k_group_att(const Grou
     }
 }
 
-template <int D, int ST, bool DENSE>
+template <int D, int ST, bool DENSE, int NW>
 cudaError_t launch_group_t(const GroupAttParams& p, int batch_hkv, cudaStream_t st, bool pdl) {
-    using C = GCfg<D, ST>;
+    using C = GCfg<D, ST, NW>;
     cudaError_t e =
-        cudaFuncSetAttribute(k_group_att<D, ST, DENSE>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES);
+        cudaFuncSetAttribute(k_group_att<D, ST, DENSE, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::BYTES);
     if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)batch_hkv * (unsigned)p.sel.nranges * (unsigned)p.nsplit;
-    return launch_ex(k_group_att<D, ST, DENSE>, dim3(grid), dim3(kGT), (size_t)C::BYTES, st, pdl, p);
+    return launch_ex(k_group_att<D, ST, DENSE, NW>, dim3(grid), dim3(C::GT), (size_t)C::BYTES, st, pdl, p);
 }
 
 }  // namespace
@@ -658,8 +662,12 @@ bool group_att_supported(int d, int kv_bf16, int q_bf16, int G) {
 
 cudaError_t launch_group_att(const GroupAttParams& p, int d, int batch_hkv, cudaStream_t st, bool pdl) {
     if (p.nsplit < 1) return cudaErrorInvalidValue;
-    if (d == 128) return launch_group_t<128, 2, false>(p, batch_hkv, st, pdl);
-    if (d == 64) return launch_group_t<64, 2, false>(p, batch_hkv, st, pdl);
+    // eight warps per CTA when the grid leaves SMs without a CTA
+    const bool wide = (int64_t)batch_hkv * p.sel.nranges * p.nsplit < kSMs;
+    if (d == 128) return wide ? launch_group_t<128, 2, false, 8>(p, batch_hkv, st, pdl)
+                              : launch_group_t<128, 2, false, 4>(p, batch_hkv, st, pdl);
+    if (d == 64) return wide ? launch_group_t<64, 2, false, 8>(p, batch_hkv, st, pdl)
+                             : launch_group_t<64, 2, false, 4>(p, batch_hkv, st, pdl);
     return cudaErrorInvalidValue;
 }
 
@@ -676,8 +684,8 @@ int group_dense_splits(int64_t batch_hkv, int n_cap) {
 
 cudaError_t launch_group_dense(const GroupAttParams& p, int d, int batch_hkv, cudaStream_t st, bool pdl) {
     if (p.nsplit < 1 || p.sel.ready != nullptr) return cudaErrorInvalidValue;
-    if (d == 128) return launch_group_t<128, 2, true>(p, batch_hkv, st, pdl);
-    if (d == 64) return launch_group_t<64, 2, true>(p, batch_hkv, st, pdl);
+    if (d == 128) return launch_group_t<128, 2, true, 4>(p, batch_hkv, st, pdl);
+    if (d == 64) return launch_group_t<64, 2, true, 4>(p, batch_hkv, st, pdl);
     return cudaErrorInvalidValue;
 }
 
