@@ -21,8 +21,14 @@
  * Conventions shared by every entry point:
  *  - All tensor pointers are DEVICE pointers unless stated; the caller owns every
  *    buffer. The library allocates no device memory and keeps no global state
- *    other than a thread-local last-error string and the fixed scratch array of
- *    hash_attn_gather_att_noalloc.
+ *    other than a thread-local last-error string, the fixed scratch array of
+ *    hash_attn_gather_att_noalloc and a process-wide call count (the tag a
+ *    decode call's selection writes into its workspace's ready flags, so that a
+ *    kernel of the next call, which may start before this one's have finished,
+ *    never takes this call's flags for its own).
+ *  - A workspace sized for the largest use serves calls of any smaller budget,
+ *    any window, option or path on its shape in turn (one stream at a time):
+ *    what must be zero between calls sits at offsets fixed by the shape.
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *    stream). All work is enqueued on it; no call synchronises except
  *    hash_attn_device_status and hash_attn_workspace_init's caller-visible copy.

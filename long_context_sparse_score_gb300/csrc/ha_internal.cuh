@@ -30,14 +30,17 @@ constexpr int kFusedRange = 8192;         // tokens per range of the fused selec
 // ------------------------------------------------------------------ workspace
 //
 // [0, 256)                 error word (uint32) + padding
-// counters   uint32[heads]  split-K arrival counters of GATHER-ATT (self-resetting)
+// zero between calls (self-resetting), at offsets fixed by the shape:
+// counters   uint32[heads]  split-K arrival counters of GATHER-ATT
+// score_cnt  uint32[batch*h_kv]          SCORE arrival counters
+// tot, ready                             fused selection totals and ready flags
+// scratch (its layout depends on the budget, the options and the path):
 // chunk_hist uint32[heads][nchunks][33]  SCORE histogram of every chunk
 // seg_cnt    int32 [heads][nseg]         selected tokens of every segment (one
 //                                          per warp sub-chunk of seg_cap tokens)
 // seg_idx    int32 [heads][nseg*seg_cap] selected token indices, segment s's
 //                                          entries at [s*seg_cap, s*seg_cap + seg_cnt)
 // part       float [heads][splits][2 + d] split-K partials (max, sum, o[d])
-// score_cnt  uint32[batch*h_kv]          SCORE arrival counters (self-resetting)
 // meta_t     int32 [heads]                threshold bin t of every head
 // meta_qt    int2  [heads][nchunks]       per chunk: (tie quota left, ties in chunk)
 struct Layout {
@@ -143,8 +146,9 @@ struct FusedSelParams {
     uint32_t* tot;           // [B * Hkv][4][36] per-sequence distance histograms (summed, then cleared)
     int4* meta_r;            // [B * Hkv][nranges][4]
     int2* meta_t;            // [B * Hkv][4]
-    uint32_t* ready;         // [B * Hkv] or null: set to 1 once a pair's shares are written
-                             // (k_group_att waits on it and resets it)
+    uint32_t* ready;         // [B * Hkv] or null: set to `epoch` once a pair's shares are
+                             // written (k_group_att waits for that value and resets it)
+    uint32_t epoch;          // nonzero tag of the call (a flag left by an earlier call differs)
     int32_t* list;           // [B * Hq][cap] selected tokens, ascending
     int cap;
     int32_t* cnt;            // [B * Hq]

@@ -2,6 +2,7 @@
 // stream-ordered launch sequence SCORE -> TOPK -> GATHER-ATT (+ merge).
 // Every check that the host can make happens before anything is enqueued.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -132,7 +133,7 @@ Views views(const Layout& lay, void* ws) {
     v.seg_cnt = seg ? at<int32_t>(ws, lay.off_segcnt) : nullptr;
     v.seg_idx = seg ? at<int32_t>(ws, lay.off_seg) : nullptr;
     v.part = at<float>(ws, lay.off_part);
-    v.score_cnt = lay.chunk ? at<uint32_t>(ws, lay.off_scnt) : nullptr;
+    v.score_cnt = at<uint32_t>(ws, lay.off_scnt);
     v.meta_t = lay.chunk ? at<int32_t>(ws, lay.off_meta_t) : nullptr;
     v.meta_qt = lay.chunk ? at<int2>(ws, lay.off_meta_qt) : nullptr;
     v.list = lay.fused ? at<int32_t>(ws, lay.off_list) : nullptr;
@@ -354,6 +355,16 @@ FusedSelParams fused_params(const ha_shape* s, const Layout& lay, void* ws, cons
     return p;
 }
 
+// The tag of a call's selection ready flags: nonzero, different from the tags of
+// the calls before it (a process-wide count; it wraps after 2^32 - 1 calls, long
+// after any flag of an earlier call has been reset).
+uint32_t next_call_tag() {
+    static std::atomic<uint32_t> count{0};
+    uint32_t t = count.fetch_add(1u, std::memory_order_relaxed) + 1u;
+    if (t == 0u) t = count.fetch_add(1u, std::memory_order_relaxed) + 1u;
+    return t;
+}
+
 // The dense path runs on the group kernel for the shapes it takes (element
 // strides of K/V rows below 2^30).
 bool dense_group(const ha_shape& s) {
@@ -445,6 +456,7 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
         ga.sel = fused_params(s, lay, ws, v, q_sig, k_sig, seq_lens, m_per_seq, m, n_sink, n_local, opts, v.list,
                               v.lcnt, 0);
         ga.sel.ready = at<uint32_t>(ws, lay.off_ready);
+        ga.sel.epoch = next_call_tag();
         ga.att = gp;
         ga.nsplit = group_splits((int64_t)bhkv * lay.nranges);
         // the scan's counting may overlap the previous call's last kernel (not the
@@ -654,19 +666,26 @@ Layout make_layout(const ha_shape& s, int64_t rows_cap, bool with_selection, int
     choose_splits(L.heads, rows_cap, &L.splits, &L.rows_per_split);
     size_t off = 256;  // error word + padding
     L.off_err = 0;
-    L.off_counter = off;
+    // What must be zero between calls comes first, at offsets that depend on the
+    // shape alone: calls with other budgets, code widths or options, the dense
+    // path and the entry points with given lists lay out the scratch after it
+    // differently, so one workspace serves all of them in turn.
+    const int64_t pairs = (int64_t)s.batch * s.h_kv;
+    L.off_counter = off;  // GATHER-ATT split-K arrival counters, per head
     off = align_up(off + (size_t)L.heads * 4, 256);
+    L.off_scnt = off;     // SCORE arrival counters, per (batch entry, KV head)
+    off = align_up(off + (size_t)pairs * 4, 256);
+    L.off_tot = off;      // fused: per (pair, head) 36-word distance histogram
+    off = align_up(off + (size_t)pairs * 4 * 36 * 4, 256);
+    L.off_ready = off;    // fused: per pair, shares-complete flag
+    off = align_up(off + (size_t)pairs * 4, 256);
+    // scratch: written by every call before it reads it
     if (with_selection) {
-        // the self-resetting SCORE counters and the threshold metadata come first,
-        // at offsets that do not depend on the code width, so one workspace sized
-        // for the largest use can serve calls with different options
-        L.chunk = choose_chunk((int64_t)s.batch * s.h_kv, s.n_cap);
+        L.chunk = choose_chunk(pairs, s.n_cap);
         L.nchunks = (int)ceil_div(s.n_cap, L.chunk);
         L.seg_cap = L.chunk / kSegPerChunk;
         L.nseg = L.nchunks * kSegPerChunk;
         L.nbins = nbins;
-        L.off_scnt = off;
-        off = align_up(off + (size_t)s.batch * s.h_kv * 4, 256);
         L.off_meta_t = off;
         off = align_up(off + (size_t)L.heads * 4, 256);
         L.off_meta_qt = off;
@@ -674,7 +693,6 @@ Layout make_layout(const ha_shape& s, int64_t rows_cap, bool with_selection, int
         L.off_hist = off;
         off = align_up(off + (size_t)L.heads * L.nchunks * nbins * 4, 256);
         if (fused_selection(s, code_words)) {
-            const int64_t pairs = (int64_t)s.batch * s.h_kv;
             L.fused = true;
             L.nranges = fused_ranges(s.n_cap);
             L.d_sp = ceil_div(s.n_cap, 64) * 64;
@@ -690,10 +708,6 @@ Layout make_layout(const ha_shape& s, int64_t rows_cap, bool with_selection, int
             off = align_up(off + (size_t)pairs * L.nranges * 4 * 16, 256);
             L.off_meta_tt = off;
             off = align_up(off + (size_t)pairs * 4 * 8, 256);
-            L.off_tot = off;
-            off = align_up(off + (size_t)pairs * 4 * 36 * 4, 256);
-            L.off_ready = off;
-            off = align_up(off + (size_t)pairs * 4, 256);
         } else {
             L.off_segcnt = off;
             off = align_up(off + (size_t)L.heads * L.nseg * 4, 256);
@@ -703,7 +717,6 @@ Layout make_layout(const ha_shape& s, int64_t rows_cap, bool with_selection, int
     }
     // split-K partials; the group kernel keeps one per (head, range, split) of the
     // fused plan, or per (head, range, span) on the dense path
-    const int64_t pairs = (int64_t)s.batch * s.h_kv;
     int64_t psplits = L.splits;
     if (L.fused) psplits = std::max<int64_t>(psplits, (int64_t)L.nranges * group_splits(pairs * L.nranges));
     if (dense_parts && dense_group(s))

@@ -102,7 +102,13 @@ __device__ __forceinline__ int token_at(const GatherParams& p, int pp, int n, co
             const int mid = (lo + hi + 1) >> 1;
             if (pre[mid] <= pp) lo = mid; else hi = mid - 1;
         }
-        return seg[(int64_t)lo * p.seg_cap + (pp - pre[lo])];
+        // TOPK's own entries: outside [0, n) only if the workspace was disturbed
+        const int tok = seg[(int64_t)lo * p.seg_cap + (pp - pre[lo])];
+        if (tok < 0 || tok >= n) {
+            flag_error(p.err, HA_DEVERR_STATE);
+            return -1;
+        }
+        return tok;
     }
     const int tok = lst[pp];
     if (tok < 0 || tok >= n) {
@@ -189,6 +195,10 @@ __global__ void __launch_bounds__(kGatherThreads, (D * sizeof(KT) <= 256) ? 5 : 
                 for (int k = 0; k < 4; ++k) {
                     const int cc = base + 32 * k + lane;
                     v4[k] = (cc < nused) ? cnt[cc] : 0;
+                    if (v4[k] < 0 || v4[k] > p.seg_cap) {  // a disturbed workspace: stay in the segment
+                        flag_error(p.err, HA_DEVERR_STATE);
+                        v4[k] = min(max(v4[k], 0), p.seg_cap);
+                    }
                 }
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {

@@ -11,7 +11,8 @@
 // k_group_att: one CTA (4 warps, three per SM) per (batch entry, KV head, range
 // of 8,192 tokens), run after k_sel_scan, which has fixed every head's threshold
 // bin t and each range's share of the ties. A CTA starts as soon as the scan's
-// last CTA of its (batch entry, KV head) has set the pair's ready flag.
+// last CTA of its (batch entry, KV head) has set the pair's ready flag to the
+// call's tag (a nonzero number no earlier call used).
 //  1. Masks. Each thread recomputes the distances of two 32-token lane blocks
 //     from the codes (one popcount per token and head; the codes' last read) and
 //     builds every head's mask with one byte-wise compare pass against a per-head
@@ -192,9 +193,12 @@ __global__ void __launch_bounds__(32 * NW, GCfg<D, ST, NW>::MINB) k_group_att(co
     }
     pdl_launch_dependents();
     // The scan's thresholds and shares of this pair: its last CTA sets ready[pair]
-    // after writing them, so the pairs that are done start while the scan drains.
-    // Every scan CTA is resident before this grid starts (programmatic launch), so
-    // the flag comes; the wait is bounded all the same.
+    // to this call's tag after writing them, so the pairs that are done start while
+    // the scan drains. This grid may start while the previous call's group kernel
+    // still runs (each kernel lets the next one start early), whose pairs' flags
+    // hold that call's tag until its last CTAs reset them: only this call's tag
+    // counts. Every scan CTA is resident before this grid starts (programmatic
+    // launch), so the flag comes; the wait is bounded all the same.
     __shared__ int s_go;
     if (DENSE) {
         // nothing to wait for before the copies: the inputs are the caller's, and the
@@ -206,7 +210,7 @@ __global__ void __launch_bounds__(32 * NW, GCfg<D, ST, NW>::MINB) k_group_att(co
             for (uint32_t it = 0;; ++it) {
                 uint32_t v;
                 asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p.ready + pair) : "memory");
-                if (v != 0u) {
+                if (v == p.epoch) {
                     ok = 1;
                     break;
                 }
@@ -423,6 +427,12 @@ __global__ void __launch_bounds__(32 * NW, GCfg<D, ST, NW>::MINB) k_group_att(co
     };
     auto issue = [&](int k, uint32_t ent) {
         const int slot = k % ST;
+        // a row outside the sequence only if the workspace was disturbed: never read
+        // it (the range's first row instead, with no head bits)
+        if (lo + (int)(ent & 0xffffu) >= n) {
+            flag_error(p.err, HA_DEVERR_STATE);
+            ent = 0u;
+        }
         if (lane < kCR) whb[slot * kCR + lane] = (int)(ent >> 16);
         const int tok = lo + (int)(ent & 0xffffu);
         const uint32_t sbase = smem_addr(ring + slot * C::STAGE) + cdst;

@@ -316,9 +316,9 @@ __global__ void __launch_bounds__(kSelThreads, WD ? 5 : 8) k_sel_scan(const Fuse
     for (int x = tid; x < 4 * kCum; x += NT) tot_g[x] = 0u;
     if (tid == 0) {
         p.arrive[pair] = 0u;
-        if (p.ready != nullptr) {  // the shares of this pair are complete
+        if (p.ready != nullptr) {  // the shares of this pair are complete: this call's tag
             __threadfence();
-            asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.ready + pair), "r"(1u) : "memory");
+            asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.ready + pair), "r"(p.epoch) : "memory");
         }
     }
 }
@@ -436,7 +436,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) k_sel_emit(const FusedSelParam
             for (int w2 = 0; w2 < warp; ++w2) at += s_wc[e][w2];
             uint32_t m = msk[e];
             int32_t* dst = p.list + (int64_t)(head0 + e) * cap;
-            if (at + __popc(m) > cap) {
+            if (at < 0 || at + __popc(m) > cap) {
                 flag_error(p.err, HA_DEVERR_STATE);
                 m = 0u;
             }

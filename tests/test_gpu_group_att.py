@@ -103,3 +103,85 @@ def test_group_path_batch16_slice():
     w = W().make_gqa(3, B=2, Hq=32, Hkv=8, d=128, n_cap=131072, seq_lens=131072, m=4096, n_sink=128,
                      n_local=256, device="cuda", name="batch2-128k")
     _both(w, _sample(2, 32, 16, 7))
+
+
+# ---------------------------------------------------------------- calls back to back
+
+BACK_TO_BACK = [
+    # name, B, n (32 / 8 heads, d = 128): one CTA per SM or less, and several waves
+    ("one_sequence_32k", 1, 32768),
+    ("four_sequences_40000", 4, 40000),
+    ("eight_sequences_128k", 8, 131072),
+]
+
+
+@pytest.mark.parametrize("case", BACK_TO_BACK, ids=[c[0] for c in BACK_TO_BACK])
+def test_back_to_back_calls_with_different_inputs(case):
+    """Calls on one stream and one workspace issued with nothing between them (no
+    host synchronisation, no other kernel), each with inputs and a budget of its
+    own, as successive layers of a model make them; the decode step (selection
+    scan + group kernel), the path that also returns the selection and the dense
+    path interleaved. Each kernel lets the next one start early, so a call's
+    kernels run beside the previous call's: every output, log-normaliser and
+    selection must equal, bit for bit, those of the same call made alone, and
+    the calls alone meet the oracle on sampled heads."""
+    name, B, n = case
+    H = GH.ha()
+    wl = [W().make_gqa(50 + k, B=B, Hq=32, Hkv=8, d=128, n_cap=n, seq_lens=n, m=(1024, 2048, 700)[k],
+                       n_sink=128, n_local=(128, 256, 0)[k], device="cuda", name=f"{name}_{k}")
+          for k in range(3)]
+    shape = H.make_shape(wl[0].q, wl[0].K, wl[0].V, wl[0].k_sig, batch=B)
+    # one workspace for every call, sized for the largest use (the dense path)
+    ws = GH.workspace(shape, n, 0, 0)
+    caps = [H.hash_attn_select_capacity(n, w.m, w.n_sink, w.n_local) for w in wl]
+
+    def buffers(k):
+        return {"out": torch.full((B, 32, 128), float("nan"), device="cuda"),
+                "lse": torch.full((B, 32), float("nan"), device="cuda"),
+                "idx": torch.full((B, 32, caps[k]), -7, dtype=torch.int32, device="cuda"),
+                "cnt": torch.full((B, 32), -7, dtype=torch.int32, device="cuda")}
+
+    def call(k, mode, bf):
+        w = wl[k]
+        if mode == "dense":
+            H.hash_attn_decode(shape, w.q, None, None, w.K, w.V, w.seq_lens, None, n, 0, 0, bf["out"], bf["lse"],
+                               workspace=ws)
+        elif mode == "sel":
+            H.hash_attn_decode(shape, w.q, w.q_sig, w.k_sig, w.K, w.V, w.seq_lens, None, w.m, w.n_sink,
+                               w.n_local, bf["out"], bf["lse"], bf["idx"], bf["cnt"], workspace=ws)
+        else:
+            H.hash_attn_decode(shape, w.q, w.q_sig, w.k_sig, w.K, w.V, w.seq_lens, None, w.m, w.n_sink,
+                               w.n_local, bf["out"], bf["lse"], workspace=ws)
+
+    kinds = [(k, "group") for k in range(3)] + [(k, "sel") for k in range(3)] + [(1, "dense")]
+    alone = {}
+    for k, mode in kinds:
+        bf = buffers(k)
+        call(k, mode, bf)
+        torch.cuda.synchronize()
+        alone[(k, mode)] = bf
+    seq = [(0, "group"), (1, "group"), (2, "group"), (0, "group"), (1, "dense"), (2, "group"), (1, "group"),
+           (0, "sel"), (2, "group"), (1, "sel"), (0, "group"), (2, "sel"), (1, "group"), (0, "group")]
+    bufs = [buffers(k) for k, _ in seq]
+    torch.cuda.synchronize()
+    for (k, mode), bf in zip(seq, bufs):  # nothing else enters the stream between the calls
+        call(k, mode, bf)
+    torch.cuda.synchronize()
+    st, flags = H.hash_attn_device_status(ws)
+    assert st == 0, hex(flags)
+    for i, ((k, mode), bf) in enumerate(zip(seq, bufs)):
+        ref = alone[(k, mode)]
+        what = f"call {i} (workload {k}, {mode})"
+        assert torch.equal(bf["out"], ref["out"]), f"{what}: output differs from the call alone"
+        assert torch.equal(bf["lse"], ref["lse"]), f"{what}: lse differs from the call alone"
+        if mode == "sel":
+            assert torch.equal(bf["idx"], ref["idx"]) and torch.equal(bf["cnt"], ref["cnt"]), what
+    heads = [(b, h) for b in range(min(B, 2)) for h in (0, 5, 18, 31)]
+    for k in range(3):
+        w = wl[k]
+        hc = GH.HostCopy(w)
+        for mode in ("group", "sel"):
+            GH.check_attention(alone[(k, mode)], hc, heads, w.m)
+        sel = {"sel_idx": alone[(k, "sel")]["idx"], "sel_cnt": alone[(k, "sel")]["cnt"], "cap": caps[k]}
+        GH.check_selection(sel, hc, heads, w.m)
+    GH.check_attention(alone[(1, "dense")], GH.HostCopy(wl[1]), heads, n, dense=True)
