@@ -192,6 +192,44 @@ __global__ void __launch_bounds__(32 * NW, GCfg<D, ST, NW>::MINB) k_group_att(co
         }
     }
     pdl_launch_dependents();
+    // The packed distances of lane block `it` of this thread (head e in byte e): the
+    // codes and the query codes alone. With eight warps (small grids, where the
+    // wait is on the critical path) the first block's come before the wait; with
+    // four, the registers are kept for the attention loop.
+    const uint32_t* crow = p.k_sig + (int64_t)b * p.ks_sb + (int64_t)g * p.ks_sh;
+    auto distances = [&](int it, uint32_t (&Dw)[32]) {
+        const int lb = lo + (it * kGT + tid) * 32;
+        const uint32_t valid = low_bits(n - lb);
+        if (valid == 0u) return;
+        if (valid == 0xffffffffu) {
+            // lb + 32 <= n <= n_cap and lb is a multiple of 32: whole 16-byte loads in the row
+            // the codes' last read: streaming (evict first)
+            const uint4* src = reinterpret_cast<const uint4*>(crow + lb);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint4 v = __ldcs(src + j);
+                Dw[4 * j + 0] = v.x;
+                Dw[4 * j + 1] = v.y;
+                Dw[4 * j + 2] = v.z;
+                Dw[4 * j + 3] = v.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) Dw[j] = ((valid >> j) & 1u) ? crow[lb + j] : 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const uint32_t c = Dw[j];
+            uint32_t w = 0u;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (e < nh) w |= (uint32_t)__popc(qs[e] ^ c) << (8 * e);
+            Dw[j] = w;
+        }
+    };
+    constexpr bool kEarly = !DENSE && NW > 4;
+    uint32_t D0[32];
+    if constexpr (kEarly) distances(0, D0);
     // The scan's thresholds and shares of this pair: its last CTA sets ready[pair]
     // to this call's tag after writing them, so the pairs that are done start while
     // the scan drains. This grid may start while the previous call's group kernel
@@ -255,7 +293,6 @@ __global__ void __launch_bounds__(32 * NW, GCfg<D, ST, NW>::MINB) k_group_att(co
         Tsel[e] = (mode[e] == 1) ? T[e] : T[e] - 1;  // all of bin t, or only below it
         any2 = any2 || mode[e] == 2;
     }
-    const uint32_t* crow = p.k_sig + (int64_t)b * p.ks_sb + (int64_t)g * p.ks_sh;
     uint32_t eqm[kIt][4], validv[kIt], winv[kIt];
 #pragma unroll
     for (int it = 0; it < kIt; ++it) {
@@ -265,30 +302,11 @@ __global__ void __launch_bounds__(32 * NW, GCfg<D, ST, NW>::MINB) k_group_att(co
         uint32_t m1[4] = {0u, 0u, 0u, 0u}, le[4] = {0u, 0u, 0u, 0u};
         if (valid != 0u) {
             uint32_t Dw[32];
-            if (valid == 0xffffffffu) {
-                // lb + 32 <= n <= n_cap and lb is a multiple of 32: whole 16-byte loads in the row
-                // the codes' last read: streaming (evict first)
-                const uint4* src = reinterpret_cast<const uint4*>(crow + lb);
+            if (kEarly && it == 0) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint4 v = __ldcs(src + j);
-                    Dw[4 * j + 0] = v.x;
-                    Dw[4 * j + 1] = v.y;
-                    Dw[4 * j + 2] = v.z;
-                    Dw[4 * j + 3] = v.w;
-                }
+                for (int j = 0; j < 32; ++j) Dw[j] = D0[j];
             } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) Dw[j] = ((valid >> j) & 1u) ? crow[lb + j] : 0u;
-            }
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const uint32_t c = Dw[j];
-                uint32_t w = 0u;
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    if (e < nh) w |= (uint32_t)__popc(qs[e] ^ c) << (8 * e);
-                Dw[j] = w;
+                distances(it, Dw);
             }
             le_masks(Dw, thresh_word(Tsel, nh), m1);
             if (any2) le_masks(Dw, thresh_word(T, nh), le);  // the ties of a boundary range

@@ -151,12 +151,6 @@ __global__ void __launch_bounds__(kSelThreads, WD ? 5 : 8) k_sel_scan(const Fuse
             if (k < NR) v[k % U] = load(k);
         }
     }
-    // Launched with programmatic dependent launch, the counting above may overlap
-    // the previous kernel in the stream; everything below writes state that the
-    // previous call's kernels may still read (published sums, totals, shares),
-    // so wait for it here (every kernel of the library waits for its own
-    // predecessor before it completes, so this orders the calls).
-    pdl_wait();
     __syncthreads();  // the range's distances are written and visible to this CTA
     {
         // every (bin, head pair) row of 32 lane columns: 4 threads x 8 columns, then
@@ -206,6 +200,13 @@ __global__ void __launch_bounds__(kSelThreads, WD ? 5 : 8) k_sel_scan(const Fuse
                 if (e < nh) atomicAdd(&s_h[which][e][(w >> (8 * e)) & 0xffu], 1u);
         }
     }
+    // Launched with programmatic dependent launch, everything above (reads of the
+    // codes, this CTA's shared memory) may overlap the previous kernel in the
+    // stream; everything below writes state that the previous call's kernels may
+    // still read (published sums, totals, shares), so wait for it here (every
+    // kernel of the library waits for its own predecessor before it completes, so
+    // this orders the calls).
+    pdl_wait();
     __syncthreads();
     // exclusive prefix sums over the 33 bins, one warp per (head, histogram), published
     uint32_t* pub = p.rh + ((int64_t)pair * p.nranges + range) * (3 * 4 * kCum);
