@@ -41,8 +41,8 @@ GATHER_SOURCE = os.path.join(ROOT, "long_context_sparse_score_gb300", "csrc", "k
 # (dram__bytes_read.sum + dram__bytes_write.sum, one pass, --cache-control none, so
 # the L2 holds what the step left there: the codes the scan has just read). It
 # holds only for the k_group_att.cu source it was taken on.
-GATHER_TRAFFIC = {"source_sha256": "c22f458a150a947a4b79bc2181854272a59bc65c06a70c8da7cf124bf36eb399",
-                  "bytes_per_launch": 1057629696 + 2438912}
+GATHER_TRAFFIC = {"source_sha256": "4b8879846acc3f6ea2a58169e1c7db9a5933eb3b90c90a720afa6704c869b9b2",
+                  "bytes_per_launch": 1053973504 + 1976832}
 
 
 def parse_args():
