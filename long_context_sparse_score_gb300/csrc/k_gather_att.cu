@@ -432,16 +432,19 @@ __global__ void __launch_bounds__(kGatherThreads, (D * sizeof(KT) <= 256) ? 5 : 
     for (int dd = tid; dd < D; dd += kGatherThreads) {
         const float* pt = p.part + (int64_t)head * p.splits * (D + 2);
         float M = -CUDART_INF_F;
+#pragma unroll 8
         for (int s = 0; s < p.splits; ++s) M = fmaxf(M, __ldcg(pt + (int64_t)s * (D + 2)));
         float Ls = 0.f, O = 0.f;
         if (M != -CUDART_INF_F) {
+            // loads that depend on no branch, so the splits' loads are in flight together
+#pragma unroll 8
             for (int s = 0; s < p.splits; ++s) {
-                const float ms = __ldcg(pt + (int64_t)s * (D + 2));
-                if (ms != -CUDART_INF_F) {
-                    const float sc = exp2f(ms - M);
-                    Ls += __ldcg(pt + (int64_t)s * (D + 2) + 1) * sc;
-                    O += __ldcg(pt + (int64_t)s * (D + 2) + 2 + dd) * sc;
-                }
+                const float* ps = pt + (int64_t)s * (D + 2);
+                const float ms = __ldcg(ps), ls = __ldcg(ps + 1), os = __ldcg(ps + 2 + dd);
+                const bool live = ms != -CUDART_INF_F;  // an empty split adds nothing
+                const float sc = exp2f((live ? ms : M) - M);
+                Ls += live ? ls * sc : 0.f;
+                O += live ? os * sc : 0.f;
             }
         }
         p.out[(int64_t)head * D + dd] = (Ls > 0.f) ? O / Ls : 0.f;
