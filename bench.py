@@ -41,8 +41,8 @@ GATHER_SOURCE = os.path.join(ROOT, "long_context_sparse_score_gb300", "csrc", "k
 # (dram__bytes_read.sum + dram__bytes_write.sum, one pass, --cache-control none, so
 # the L2 holds what the step left there: the codes the scan has just read). It
 # holds only for the k_group_att.cu source it was taken on.
-GATHER_TRAFFIC = {"source_sha256": "4b8879846acc3f6ea2a58169e1c7db9a5933eb3b90c90a720afa6704c869b9b2",
-                  "bytes_per_launch": 1053973504 + 1976832}
+GATHER_TRAFFIC = {"source_sha256": "bb43ed1e3b708de1ffb4ebca79cb485f2163bd3031ffce031d3ccf45db243a67",
+                  "bytes_per_launch": 1053678080 + 2058240}
 
 
 def parse_args():
