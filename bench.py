@@ -40,8 +40,9 @@ GATHER_SOURCE = os.path.join(ROOT, "long_context_sparse_score_gb300", "csrc", "k
 # from one ncu capture of a full-size launch inside this program's own loop
 # (dram__bytes_read.sum + dram__bytes_write.sum, one pass, --cache-control none, so
 # the L2 holds what the step left there: the codes the scan has just read). It
-# holds only for the k_group_att.cu source it was taken on.
-GATHER_TRAFFIC = {"source_sha256": "bb43ed1e3b708de1ffb4ebca79cb485f2163bd3031ffce031d3ccf45db243a67",
+# holds only for the k_group_att.cu code it was taken on: the key hashes the
+# source without its comments and blank lines (source_code_key).
+GATHER_TRAFFIC = {"code_sha256": "974bc7f183965b3fa96b7dd06c6b095c3bae2c31a95dc765692e5e281ba33201",
                   "bytes_per_launch": 1053678080 + 2058240}
 
 
@@ -167,14 +168,26 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(win)}
 
 
+def source_code_key(path):
+    """SHA-256 of a C++/CUDA source's code: every line cut at its first '//',
+    trailing blanks and empty lines dropped (a comment edit keeps the key)."""
+    lines = []
+    with open(path, encoding="utf-8") as f:
+        for line in f:
+            code = line.split("//", 1)[0].rstrip()
+            if code:
+                lines.append(code)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()
+
+
 def profiled_traffic():
     """DRAM bytes per launch of the attention kernel from the recorded capture, if
-    the kernel source is unchanged since it was taken (else None)."""
+    the kernel's code is unchanged since it was taken (else None)."""
     try:
-        sha = hashlib.sha256(open(GATHER_SOURCE, "rb").read()).hexdigest()
+        key = source_code_key(GATHER_SOURCE)
     except OSError:
         return None
-    if GATHER_TRAFFIC["source_sha256"] != sha:
+    if GATHER_TRAFFIC["code_sha256"] != key:
         return None
     return GATHER_TRAFFIC["bytes_per_launch"]
 

@@ -34,10 +34,12 @@
 //     The softmax is online in base 2 per (warp, head).
 //  3. The warps combine in shared memory into the range's partial (max, sum, o)
 //     per head; the last CTA of a (batch entry, KV head) to arrive merges the
-//     ranges of its heads (an arrival counter decides; nothing waits).
+//     ranges of its heads (an arrival counter decides; nothing waits), with each
+//     head's maximum and part weights found once, in shared memory.
 // When the grid would not give every SM a CTA, two CTAs share a range, each with
 // a contiguous half of its chunks (both build the masks), and each CTA has eight
-// warps (one CTA per SM, the whole list in shared memory).
+// warps with three-stage rings (one CTA per SM; the list's first 5,248 entries
+// in shared memory for d = 128, all of them for d = 64).
 // K/V must be finite: a row selected by one head of the group is also multiplied
 // (by weight zero) into the other heads' P.V.
 // The dense path (I = every token; HashAttention Sec. 4 with m >= n) runs the

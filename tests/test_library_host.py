@@ -241,3 +241,16 @@ def test_product_path_fails_loudly_without_the_library(ha, monkeypatch, tmp_path
     monkeypatch.setattr(hashattn, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         hashattn.lib()
+
+
+def test_bench_traffic_key_ignores_comments(tmp_path):
+    """The bench's recorded DRAM traffic stays valid across comment edits of the
+    kernel source and lapses on any code change."""
+    import bench
+    src = tmp_path / "k.cu"
+    src.write_text("// header\n__global__ void k(int* p) {  // a kernel\n    p[0] = 1;\n}\n")
+    key = bench.source_code_key(str(src))
+    src.write_text("// another header\n\n__global__ void k(int* p) {  // the same kernel\n    p[0] = 1;\n}\n")
+    assert bench.source_code_key(str(src)) == key
+    src.write_text("// header\n__global__ void k(int* p) {\n    p[0] = 2;\n}\n")
+    assert bench.source_code_key(str(src)) != key
