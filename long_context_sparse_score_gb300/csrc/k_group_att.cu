@@ -643,71 +643,73 @@ __global__ void __launch_bounds__(32 * NW, GCfg<D, ST, NW>::MINB) k_group_att(co
     if (!s_last) return;
     __threadfence();
     // Merge the pair's parts per head (Nectar Eq. (3.4)). One warp per head finds
-    // the head's maximum and each part's weight 2^(m_r - M) once (in the ring's
-    // shared memory, free again), then every (head, dim) reads only the parts'
-    // outputs: loads that depend on no branch, all in flight together.
-    float* s_w = reinterpret_cast<float*>(smem);  // [nh][nparts] weights, then M [4], L [4]
-    if ((nh * nparts + 8) * 4 <= C::RING) {
-        float* s_ml = s_w + nh * nparts;
-        if (warp < nh) {
-            const float* ph = a.part + (int64_t)(head0 + warp) * nparts * (D + 2);
-            float M = -CUDART_INF_F;
-            for (int r = lane; r < nparts; r += 32) M = fmaxf(M, __ldcg(ph + (int64_t)r * (D + 2)));
+    // the head's maximum over all parts, then, for blocks of up to kMB parts, each
+    // part's weight 2^(m_r - M) once (in the ring's shared memory, free again), and
+    // every (head, dim) reads only the block's outputs: loads that depend on no
+    // branch, all in flight together.
+    constexpr int kMB = 64;                                // parts per block
+    constexpr int kItems = (4 * D + kGT - 1) / kGT;        // (head, dim) outputs per thread
+    static_assert((4 * kMB + 8) * 4 <= C::RING, "a block's weights fit the ring");
+    float* s_w = reinterpret_cast<float*>(smem);           // [4][kMB] weights
+    float* s_ml = s_w + 4 * kMB;                           // M [4], L [4]
+    if (warp < nh) {
+        const float* ph = a.part + (int64_t)(head0 + warp) * nparts * (D + 2);
+        float M = -CUDART_INF_F;
+        for (int r = lane; r < nparts; r += 32) M = fmaxf(M, __ldcg(ph + (int64_t)r * (D + 2)));
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-            float Ls = 0.f;
-            for (int r = lane; r < nparts; r += 32) {
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        if (lane == 0) s_ml[warp] = M;
+    }
+    float O[kItems];
+#pragma unroll
+    for (int i = 0; i < kItems; ++i) O[i] = 0.f;
+    float Ls = 0.f;  // per lane of the head's warp
+    for (int r0 = 0; r0 < nparts; r0 += kMB) {
+        const int rn = min(kMB, nparts - r0);
+        __syncthreads();  // the maxima are written; the previous block's weights are read
+        if (warp < nh) {
+            const float M = s_ml[warp];
+            const float* ph = a.part + ((int64_t)(head0 + warp) * nparts + r0) * (D + 2);
+            for (int r = lane; r < rn; r += 32) {
                 const float mr = __ldcg(ph + (int64_t)r * (D + 2)), lr = __ldcg(ph + (int64_t)r * (D + 2) + 1);
                 const float w = (mr != -CUDART_INF_F) ? exp2f(mr - M) : 0.f;  // an empty part adds nothing
-                s_w[warp * nparts + r] = w;
+                s_w[warp * kMB + r] = w;
                 Ls += (w != 0.f) ? w * lr : 0.f;
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, off);
-            if (lane == 0) {
-                s_ml[warp] = M;
-                s_ml[4 + warp] = Ls;
             }
         }
         __syncthreads();
-        for (int x = tid; x < nh * D; x += kGT) {
-            const int e = x / D, dd = x - e * D;
-            const int64_t head = head0 + e;
-            const float* po = a.part + head * nparts * (D + 2) + 2 + dd;
-            const float* we = s_w + e * nparts;
-            float O = 0.f;
+#pragma unroll
+        for (int i = 0; i < kItems; ++i) {
+            const int x = tid + i * kGT;
+            if (x < nh * D) {
+                const int e = x / D, dd = x - e * D;
+                const float* po = a.part + ((int64_t)(head0 + e) * nparts + r0) * (D + 2) + 2 + dd;
+                const float* we = s_w + e * kMB;
+                float acc = 0.f;
 #pragma unroll 8
-            for (int r = 0; r < nparts; ++r) {
-                const float w = we[r], o = __ldcg(po + (int64_t)r * (D + 2));
-                O += (w != 0.f) ? w * o : 0.f;
-            }
-            const float M = s_ml[e], Ls = s_ml[4 + e];
-            a.out[head * D + dd] = (Ls > 0.f) ? O / Ls : 0.f;
-            if (dd == 0) a.lse[head] = (Ls > 0.f) ? (M + log2f(Ls)) * kLn2 : -CUDART_INF_F;
-        }
-    } else {
-        // more parts than the shared memory holds weights for: per (head, dim)
-        for (int x = tid; x < nh * D; x += kGT) {
-            const int e = x / D, dd = x - e * D;
-            const int64_t head = head0 + e;
-            const float* ph = a.part + head * nparts * (D + 2);
-            float M = -CUDART_INF_F;
-#pragma unroll 8
-            for (int r = 0; r < nparts; ++r) M = fmaxf(M, __ldcg(ph + (int64_t)r * (D + 2)));
-            float Ls = 0.f, O = 0.f;
-            if (M != -CUDART_INF_F) {
-#pragma unroll 8
-                for (int r = 0; r < nparts; ++r) {
-                    const float* pr = ph + (int64_t)r * (D + 2);
-                    const float mr = __ldcg(pr), lr = __ldcg(pr + 1), orr = __ldcg(pr + 2 + dd);
-                    const bool live = mr != -CUDART_INF_F;
-                    const float sc = exp2f((live ? mr : M) - M);
-                    Ls += live ? lr * sc : 0.f;
-                    O += live ? orr * sc : 0.f;
+                for (int r = 0; r < rn; ++r) {
+                    const float w = we[r], o = __ldcg(po + (int64_t)r * (D + 2));
+                    acc += (w != 0.f) ? w * o : 0.f;
                 }
+                O[i] += acc;
             }
-            a.out[head * D + dd] = (Ls > 0.f) ? O / Ls : 0.f;
-            if (dd == 0) a.lse[head] = (Ls > 0.f) ? (M + log2f(Ls)) * kLn2 : -CUDART_INF_F;
+        }
+    }
+    if (warp < nh) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, off);
+        if (lane == 0) s_ml[4 + warp] = Ls;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kItems; ++i) {
+        const int x = tid + i * kGT;
+        if (x < nh * D) {
+            const int e = x / D, dd = x - e * D;
+            const int64_t head = head0 + e;
+            const float M = s_ml[e], L = s_ml[4 + e];
+            a.out[head * D + dd] = (L > 0.f) ? O[i] / L : 0.f;
+            if (dd == 0) a.lse[head] = (L > 0.f) ? (M + log2f(L)) * kLn2 : -CUDART_INF_F;
         }
     }
     if (tid == 0) {
