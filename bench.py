@@ -42,8 +42,8 @@ GATHER_SOURCE = os.path.join(ROOT, "long_context_sparse_score_gb300", "csrc", "k
 # the L2 holds what the step left there: the codes the scan has just read). It
 # holds only for the k_group_att.cu code it was taken on: the key hashes the
 # source without its comments and blank lines (source_code_key).
-GATHER_TRAFFIC = {"code_sha256": "974bc7f183965b3fa96b7dd06c6b095c3bae2c31a95dc765692e5e281ba33201",
-                  "bytes_per_launch": 1053678080 + 2058240}
+GATHER_TRAFFIC = {"code_sha256": "e5080d56c74eea376bc1676919e0a0235d6a6250ff4bbb8adf0371f5f447985a",
+                  "bytes_per_launch": 1052332800 + 2016256}
 
 
 def parse_args():
