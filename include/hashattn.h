@@ -174,8 +174,10 @@ int32_t hash_attn_select_capacity(int32_t n_cap, int32_t m, int32_t n_sink, int3
  *              int32 receives |I|. Both NULL to skip. Ignored by the dense path.
  *   workspace  >= hash_attn_workspace_size(shape, m, n_sink, n_local) bytes,
  *              256-byte aligned, zeroed once before first use.
- * Kernels: with 32-bit codes, at most 4 query heads per KV head, a bf16 query,
- * bf16 K/V, d in {64, 128} and sel_idx NULL, two kernels run: the selection scan
+ * Kernels: with 32-bit codes, a bf16 query, bf16 K/V, d in {64, 128} and sel_idx
+ * NULL, two kernels run (more than 4 query heads per KV head are split into
+ * groups of at most 4, each run as a KV head of its own that reads the same
+ * codes and rows): the selection scan
  * (SCORE and every range's share of TOPK), then one kernel per GQA group that
  * builds each head's selection mask from the codes and attends over the union
  * of the group's rows (each row read once per group; K/V must then be finite,

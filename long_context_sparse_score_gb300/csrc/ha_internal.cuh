@@ -138,6 +138,7 @@ struct FusedSelParams {
     const int32_t* m_per_head;   // [B * Hq] or null (overrides m_per_seq)
     int m, n_sink, n_local, excl;
     int B, Hq, Hkv, G, n_cap;
+    int kv_div;              // query-head groups per KV head: group g reads the codes of KV head g / kv_div
     int nranges;             // ranges per (batch entry, KV head)
     uint32_t* dist;          // [B * Hkv][d_sp] packed distances (head e in byte e), token order
     int64_t d_sp;
@@ -184,6 +185,7 @@ struct GatherParams {
     int64_t k_sb, k_sh, k_sn, v_sb, v_sh, v_sn;  // elements
     const int32_t* seq_lens;
     int B, Hq, Hkv, G, n_cap;
+    int kv_div;              // query-head groups per KV head: group g reads KV head g / kv_div
     int mode;
     // kSegmented
     const int32_t* seg_cnt;

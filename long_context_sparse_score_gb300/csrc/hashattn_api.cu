@@ -214,6 +214,7 @@ GatherParams gather_params(const ha_shape* s, const Layout& lay, const Views& v,
     p.Hq = s->h_q;
     p.Hkv = s->h_kv;
     p.G = s->h_q / s->h_kv;
+    p.kv_div = 1;
     p.n_cap = s->n_cap;
     p.mode = kIdentity;
     p.seg_cap = lay.seg_cap;
@@ -338,6 +339,7 @@ FusedSelParams fused_params(const ha_shape* s, const Layout& lay, void* ws, cons
     p.Hq = s->h_q;
     p.Hkv = s->h_kv;
     p.G = s->h_q / s->h_kv;
+    p.kv_div = 1;
     p.n_cap = s->n_cap;
     p.nranges = lay.nranges;
     p.dist = at<uint32_t>(ws, lay.off_dist);
@@ -365,6 +367,28 @@ uint32_t next_call_tag() {
     return t;
 }
 
+// Query-head groups per KV head for the fused selection, the group kernel and the
+// dense group path, which take at most kMaxHeadsPerPass query heads per KV head:
+// with G = h_q / h_kv above that, each KV head's heads are split into k groups of
+// G / k (the smallest such k; G itself when nothing smaller divides G), which run
+// as k virtual KV heads that read the same codes and rows (kv_div = k). Wider codes
+// keep the two-kernel path, which takes any G (1).
+int kv_split(const ha_shape& s, int code_words) {
+    const int G = s.h_q / s.h_kv;
+    if (code_words != 1 || G <= kMaxHeadsPerPass) return 1;
+    for (int k = (G + kMaxHeadsPerPass - 1) / kMaxHeadsPerPass; k < G; ++k)
+        if (G % k == 0) return k;
+    return G;
+}
+
+// The shape with k virtual KV heads per KV head (the strides stay those of the
+// real heads; the kernels divide a virtual head by kv_div).
+ha_shape virtual_shape(const ha_shape& s, int k) {
+    ha_shape v = s;
+    v.h_kv = s.h_kv * k;
+    return v;
+}
+
 // The dense path runs on the group kernel for the shapes it takes (element
 // strides of K/V rows below 2^30).
 bool dense_group(const ha_shape& s) {
@@ -381,6 +405,7 @@ FusedSelParams dense_sel_params(const ha_shape* s, const Views& v, const int32_t
     p.Hq = s->h_q;
     p.Hkv = s->h_kv;
     p.G = s->h_q / s->h_kv;
+    p.kv_div = 1;
     p.n_cap = s->n_cap;
     p.nranges = fused_ranges(s->n_cap);
     p.err = v.err;
@@ -407,6 +432,11 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
     HA_TRY(check_kv(s, K, V));
     const bool dense = (m >= s->n_cap) && (m_per_seq == nullptr) && (opts == nullptr || opts->m_per_head == nullptr);
     const int W = code_words_of(opts);
+    // more than kMaxHeadsPerPass query heads per KV head: virtual KV heads (the
+    // checks above ran on the caller's shape; strides and pointers are the same)
+    const int kdiv = kv_split(*s, W);
+    const ha_shape vshape = virtual_shape(*s, kdiv);
+    s = &vshape;
     if (!dense) HA_TRY(W > 1 ? check_wide_codes(s, q_sig, k_sig, W) : check_codes(s, q_sig, k_sig));
     if ((sel_idx == nullptr) != (sel_cnt == nullptr))
         return fail(HA_ERR_INVALID_ARG, "sel_idx and sel_cnt must both be given or both be NULL");
@@ -427,6 +457,7 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
     }
 
     GatherParams gp = gather_params(s, lay, v, q, K, V, seq_lens, out, lse);
+    gp.kv_div = kdiv;
     if (dense) {
         HA_TRY(record(events, 0, st));
         HA_TRY(record(events, 1, st));
@@ -436,6 +467,7 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
             // for the whole group
             GroupAttParams ga{};
             ga.sel = dense_sel_params(s, v, seq_lens);
+            ga.sel.kv_div = kdiv;
             ga.att = gp;
             ga.nsplit = group_dense_splits(bhkv, s->n_cap);
             HA_LAUNCH(launch_group_dense(ga, s->d, bhkv, st, true), "GATHER-ATT launch");
@@ -455,6 +487,7 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
         GroupAttParams ga{};
         ga.sel = fused_params(s, lay, ws, v, q_sig, k_sig, seq_lens, m_per_seq, m, n_sink, n_local, opts, v.list,
                               v.lcnt, 0);
+        ga.sel.kv_div = kdiv;
         ga.sel.ready = at<uint32_t>(ws, lay.off_ready);
         ga.sel.epoch = next_call_tag();
         ga.att = gp;
@@ -472,9 +505,9 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
         // SCORE and TOPK in one cluster kernel writing flat ascending lists: into the
         // caller's sel_idx (padded with -1) when given, else into the workspace
         const bool to_caller = sel_idx != nullptr;
-        const FusedSelParams cp = fused_params(s, lay, ws, v, q_sig, k_sig, seq_lens, m_per_seq, m, n_sink, n_local,
-                                               opts, to_caller ? sel_idx : v.list, to_caller ? sel_cnt : v.lcnt,
-                                               to_caller ? 1 : 0);
+        FusedSelParams cp = fused_params(s, lay, ws, v, q_sig, k_sig, seq_lens, m_per_seq, m, n_sink, n_local, opts,
+                                         to_caller ? sel_idx : v.list, to_caller ? sel_cnt : v.lcnt, to_caller ? 1 : 0);
+        cp.kv_div = kdiv;
         gp.mode = kList;
         gp.list_idx = cp.list;
         gp.list_cnt = cp.cnt;
@@ -727,6 +760,19 @@ Layout make_layout(const ha_shape& s, int64_t rows_cap, bool with_selection, int
     return L;
 }
 
+// The layout a workspace is sized for: the largest that a call on this shape makes
+// (the decode on virtual KV heads when G exceeds kMaxHeadsPerPass, the selection
+// and SCORE entry points on the caller's shape, whose two-kernel path takes any G).
+Layout workspace_layout(const ha_shape& s, int64_t rows_cap, int nbins, int code_words, bool dense) {
+    const int k = kv_split(s, code_words);
+    Layout L = make_layout(virtual_shape(s, k), rows_cap, true, nbins, code_words, dense);
+    if (k > 1) {
+        const Layout r = make_layout(s, rows_cap, true, nbins, code_words, dense);
+        L.total = std::max(L.total, r.total);
+    }
+    return L;
+}
+
 }  // namespace ha
 
 using namespace ha;
@@ -742,7 +788,7 @@ ha_status hash_attn_workspace_size(const ha_shape* shape, int32_t m_max, int32_t
     // the selection regions are always included so that hash_attn_select and
     // hash_attn_score work with any budget on the same workspace
     const int64_t rows_cap = dense ? shape->n_cap : rows_cap_of(shape->n_cap, m_max, n_sink, n_local);
-    const Layout sparse = make_layout(*shape, rows_cap, true, HA_NBINS, 1, dense);
+    const Layout sparse = workspace_layout(*shape, rows_cap, HA_NBINS, 1, dense);
     HA_TRY(check_segments(sparse));
     *bytes = sparse.total;
     return HA_OK;
@@ -756,7 +802,7 @@ ha_status hash_attn_workspace_size_ex(const ha_shape* shape, int32_t m_max, int3
     if (bytes == nullptr) return fail(HA_ERR_INVALID_ARG, "bytes is NULL");
     const bool dense = m_max >= shape->n_cap;
     const int64_t rows_cap = dense ? shape->n_cap : rows_cap_of(shape->n_cap, m_max, n_sink, n_local);
-    const Layout sparse = make_layout(*shape, rows_cap, true, nbins_of(opts), code_words_of(opts), dense);
+    const Layout sparse = workspace_layout(*shape, rows_cap, nbins_of(opts), code_words_of(opts), dense);
     HA_TRY(check_segments(sparse));
     *bytes = sparse.total;
     return HA_OK;
@@ -767,7 +813,7 @@ ha_status hash_attn_selection_plan(const ha_shape* shape, int32_t code_words, in
     HA_TRY(check_shape(shape));
     if (code_words != 1 && code_words != 2 && code_words != 4 && code_words != 8 && code_words != 16)
         return fail(HA_ERR_UNSUPPORTED, "code_words must be 1, 2, 4, 8 or 16 (got %d)", code_words);
-    const bool f = fused_selection(*shape, code_words);
+    const bool f = fused_selection(virtual_shape(*shape, kv_split(*shape, code_words)), code_words);
     if (fused) *fused = f ? 1 : 0;
     if (ranges) *ranges = f ? fused_ranges(shape->n_cap) : 0;
     if (range) *range = f ? 8192 : 0;

@@ -1,11 +1,12 @@
 """Every selection kernel instantiation the library launches, against the oracle.
 
-The fused selection (32-bit codes, at most four query heads per KV head) runs a
-scan kernel and an emit kernel over ranges of 8,192 tokens, with the ranges of
-a sequence combined by the scan's last CTA; the cases vary the number of
-ranges, where the windows and the tie boundary fall among them, and the
-budget rules. The two-kernel path (more than four query heads per KV head or
-codes wider than 32 bits) has SCORE/TOPK instantiations for 4, 8, 16 and 32
+The fused selection (32-bit codes; more than four query heads per KV head run as
+virtual groups of at most four) runs a scan kernel and an emit kernel over
+ranges of 8,192 tokens, with the ranges of a sequence combined by the scan's
+last CTA; the cases vary the number of ranges, where the windows and the tie
+boundary fall among them, and the budget rules. The two-kernel path (codes
+wider than 32 bits in the decode; the selection entry point with more than four
+query heads per KV head) has SCORE/TOPK instantiations for 4, 8, 16 and 32
 tokens per thread. Each case asserts which plan the shape takes
 (hash_attn_selection_plan) and then compares the selected sets bit for bit and
 the attention within tolerance on the selected heads.
@@ -59,6 +60,33 @@ def _check(w, heads, *, exclusive=False, m_per_head=None, code_words=1, att_head
     GH.check_selection(res, hc, heads, w.m)
     GH.check_attention(res, hc, heads[:att_heads], w.m)
     return res
+
+
+def _check_two_kernel(w, heads, *, exclusive=False, m_per_head=None, att_heads=4):
+    """The selection entry point (the two-kernel SCORE/TOPK on the caller's shape,
+    which takes any number of query heads per KV head) and GATHER-ATT on its lists,
+    against the oracle."""
+    H = GH.ha()
+    shape = H.make_shape(w.q, w.K, w.V, w.k_sig, batch=w.B)
+    opts = H.select_opts(m_per_head, exclusive, 1) if (exclusive or m_per_head is not None) else None
+    ws = torch.empty(H.hash_attn_workspace_size_ex(shape, w.m, w.n_sink, w.n_local, opts), dtype=torch.uint8,
+                     device="cuda")
+    H.hash_attn_workspace_init(ws)
+    B, Hq, d = w.q.shape
+    cap = H.hash_attn_select_capacity(w.n_cap, w.m, w.n_sink, w.n_local)
+    idx = torch.full((B, Hq, cap), -7, dtype=torch.int32, device="cuda")
+    cnt = torch.full((B, Hq), -7, dtype=torch.int32, device="cuda")
+    H.hash_attn_select_ex(shape, w.q_sig, w.k_sig, w.seq_lens, w.m_per_seq, w.m, w.n_sink, w.n_local, opts, idx,
+                          cnt, workspace=ws)
+    out = torch.full((B, Hq, d), float("nan"), device="cuda")
+    lse = torch.full((B, Hq), float("nan"), device="cuda")
+    H.hash_attn_gather_att(shape, w.q, w.K, w.V, w.seq_lens, idx, cap, cnt, out, lse, workspace=ws)
+    st, flags = H.hash_attn_device_status(ws)
+    assert st == 0, hex(flags)
+    res = dict(out=out, lse=lse, sel_idx=idx, sel_cnt=cnt, cap=cap)
+    hc = GH.HostCopy(w, exclusive=exclusive, m_per_head=m_per_head)
+    GH.check_selection(res, hc, heads, w.m)
+    GH.check_attention(res, hc, heads[:att_heads], w.m)
 
 
 def _plan(w, code_words=1):
@@ -148,6 +176,10 @@ def test_fused_select_entry_point_pads_and_matches_decode():
 
 
 # ---------------------------------------------------------------- two-kernel path: every TPT
+# Eight query heads per KV head: the selection entry point takes the two-kernel
+# path (its chunk, hence its tokens per thread, set by the shape); the decode runs
+# two virtual groups of four per KV head on the fused selection and the group
+# kernel. Both against the oracle.
 
 TWO_KERNEL = [
     # name, B, Hq, Hkv, n_cap, lens, m, S, Lw, codes, expected chunk
@@ -172,14 +204,18 @@ def test_two_kernel_selection(case):
                      device="cuda", name=name)
     _codes(w, codes, 43)
     plan = _plan(w)
-    assert plan["fused"] == 0 and plan["chunk"] == chunk, plan
-    _check(w, _sample(B, Hq, 12, 1))
+    assert plan["fused"] == 1 and plan["chunk"] == chunk, plan
+    heads = _sample(B, Hq, 12, 1)
+    _check_two_kernel(w, heads)
+    res = _check(w, heads)
+    GH.check_decode_step_path(w, res, GH.HostCopy(w), heads[:4], w.m, ws=res["ws"])
 
 
 @pytest.mark.parametrize("chunk,exclusive", [(8192, True), (2048, True), (8192, False)])
 def test_two_kernel_variants(chunk, exclusive):
     """Exclusive windows and per-head budgets on the two-kernel path (eight query
-    heads per KV head), at the largest and a small chunk."""
+    heads per KV head), at the largest and a small chunk, and on the decode's
+    virtual groups of four."""
     n_cap = 150000 if chunk == 8192 else 40000
     w = W().make_gqa(35, B=2, Hq=64, Hkv=8, d=128, n_cap=n_cap, seq_lens=[n_cap, n_cap - 1234], m=2000,
                      n_sink=3000, n_local=5000, device="cuda")
@@ -187,7 +223,9 @@ def test_two_kernel_variants(chunk, exclusive):
     assert _plan(w)["chunk"] == chunk
     gen = torch.Generator(device="cuda").manual_seed(10)
     mph = torch.randint(0, 2001, (2, 64), generator=gen, device="cuda", dtype=torch.int32)
-    _check(w, _sample(2, 64, 10, 2), exclusive=exclusive, m_per_head=mph)
+    heads = _sample(2, 64, 10, 2)
+    _check_two_kernel(w, heads, exclusive=exclusive, m_per_head=mph)
+    _check(w, heads, exclusive=exclusive, m_per_head=mph)
 
 
 @pytest.mark.parametrize("Wd", [2, 4, 16])
@@ -249,13 +287,17 @@ def test_single_sequence_of_two_million_tokens():
 
 def test_single_sequence_two_kernel_path_long():
     """One (sequence, KV head) of 2^21 tokens with eight query heads: the two-kernel
-    path with its chunk raised so the segments fit GATHER-ATT's table."""
+    path with its chunk raised so the segments fit GATHER-ATT's table, and the
+    decode's two virtual groups of four over 256 ranges."""
     n = 1 << 21
     w = W().make_gqa(40, B=1, Hq=8, Hkv=1, d=128, n_cap=n, seq_lens=[n - 5], m=30000, n_sink=128, n_local=256,
                      device="cuda")
     plan = _plan(w)
-    assert plan["fused"] == 0 and (n + plan["chunk"] - 1) // plan["chunk"] * 8 <= 4096
-    _check(w, [(0, h) for h in range(0, 8, 3)], att_heads=2)
+    assert plan["fused"] == 1 and (n + plan["chunk"] - 1) // plan["chunk"] * 8 <= 4096
+    heads = [(0, h) for h in range(0, 8, 3)]
+    _check_two_kernel(w, heads, att_heads=2)
+    res = _check(w, heads, att_heads=2)
+    GH.check_decode_step_path(w, res, GH.HostCopy(w), heads[:2], w.m, ws=res["ws"])
 
 
 # ---------------------------------------------------------------- dense path: one read per GQA group

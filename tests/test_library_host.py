@@ -74,21 +74,26 @@ def _plan(ha, B, Hq, Hkv, n_cap, code_words=1):
 
 
 def test_selection_plan_of_the_workloads(ha):
-    """32-bit codes with at most four query heads per KV head take the fused
-    selection (each distance computed once, one CTA per 8,192 tokens) at any
-    context length; more query heads per KV head or wider codes take the
-    two-kernel path."""
+    """32-bit codes take the fused selection (each distance computed once, one CTA
+    per 8,192 tokens) at any context length: with more than four query heads per
+    KV head the decode splits each KV head's heads into groups of at most four
+    (virtual KV heads reading the same codes and rows). Wider codes take the
+    two-kernel path, as does the selection entry point for more than four heads
+    per KV head (the plan's chunk is that path's)."""
     for name, shape in {"tiny": (1, 1, 1, 1024), "gqa32k": (1, 32, 8, 32768), "batch16_128k": (16, 32, 8, 131072),
                         "shared_doc": (32, 32, 8, 61440), "ragged": (64, 32, 8, 65536),
                         "2m": (1, 4, 1, 1 << 21)}.items():
         p = _plan(ha, *shape)
         assert p["fused"] == 1 and p["range"] == 8192 and p["ranges"] == -(-shape[3] // 8192), (name, p)
-    assert _plan(ha, 2, 64, 8, 131072)["fused"] == 0                 # eight query heads per KV head
+    # 5, 6, 7, 8, 12 and 16 query heads per KV head: virtual groups of at most four
+    for Hq in (40, 48, 56, 64, 96, 128):
+        p = _plan(ha, 2, Hq, 8, 131072)
+        assert p["fused"] == 1 and p["ranges"] == 16, (Hq, p)
     assert _plan(ha, 16, 32, 8, 131072, code_words=4)["fused"] == 0  # 128-bit codes
     # a single long sequence on the two-kernel path keeps within its segment table
     for n in (1 << 21, 1 << 22):
         p = _plan(ha, 1, 8, 1, n)
-        assert p["fused"] == 0 and -(-n // p["chunk"]) * 8 <= 4096, (n, p)
+        assert -(-n // p["chunk"]) * 8 <= 4096, (n, p)
     with pytest.raises(ha.HashAttnError):
         _plan(ha, 1, 4, 1, 4096, code_words=3)
 
