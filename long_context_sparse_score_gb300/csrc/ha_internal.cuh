@@ -138,7 +138,7 @@ struct FusedSelParams {
     const int32_t* m_per_head;   // [B * Hq] or null (overrides m_per_seq)
     int m, n_sink, n_local, excl;
     int B, Hq, Hkv, G, n_cap;
-    int kv_div;              // query-head groups per KV head: group g reads the codes of KV head g / kv_div
+    uint32_t kv_mul;         // query-head groups per KV head k: group g reads KV head kv_head(g, kv_mul)
     int nranges;             // ranges per (batch entry, KV head)
     uint32_t* dist;          // [B * Hkv][d_sp] packed distances (head e in byte e), token order
     int64_t d_sp;
@@ -185,7 +185,7 @@ struct GatherParams {
     int64_t k_sb, k_sh, k_sn, v_sb, v_sh, v_sn;  // elements
     const int32_t* seq_lens;
     int B, Hq, Hkv, G, n_cap;
-    int kv_div;              // query-head groups per KV head: group g reads KV head g / kv_div
+    uint32_t kv_mul;         // query-head groups per KV head k: group g reads KV head kv_head(g, kv_mul)
     int mode;
     // kSegmented
     const int32_t* seg_cnt;
@@ -346,9 +346,22 @@ cudaError_t launch_recall(const RecallParams& p, cudaStream_t st);
 cudaError_t launch_score_wide(const WideParams& p, int batch_hkv, cudaStream_t st);
 cudaError_t launch_select_wide(const WideParams& p, int batch_hkv, cudaStream_t st, bool pdl);
 
+// Query-head groups per KV head: group g of k per KV head reads KV head g / k. The
+// kernels divide by a multiply-high with kv_magic(k) = ceil(2^32 / k), exact for
+// every g below 2^28 (the error of the reciprocal is below k <= 16 parts in 2^32);
+// 0 stands for k = 1.
+inline uint32_t kv_magic(int k) {
+    return k <= 1 ? 0u : (uint32_t)((0x100000000ull + (uint64_t)k - 1u) / (uint64_t)k);
+}
+
 // ------------------------------------------------------------------ device helpers
 
 #ifdef __CUDACC__
+
+// The KV head of query-head group g (kv_mul = kv_magic(groups per KV head)).
+__device__ __forceinline__ int kv_head(int g, uint32_t kv_mul) {
+    return kv_mul != 0u ? (int)__umulhi((uint32_t)g, kv_mul) : g;
+}
 
 __device__ __forceinline__ void flag_error(uint32_t* err, uint32_t f) {
     if (err) atomicOr(err, f);

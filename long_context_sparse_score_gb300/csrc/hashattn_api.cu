@@ -214,7 +214,7 @@ GatherParams gather_params(const ha_shape* s, const Layout& lay, const Views& v,
     p.Hq = s->h_q;
     p.Hkv = s->h_kv;
     p.G = s->h_q / s->h_kv;
-    p.kv_div = 1;
+    p.kv_mul = 0u;
     p.n_cap = s->n_cap;
     p.mode = kIdentity;
     p.seg_cap = lay.seg_cap;
@@ -339,7 +339,7 @@ FusedSelParams fused_params(const ha_shape* s, const Layout& lay, void* ws, cons
     p.Hq = s->h_q;
     p.Hkv = s->h_kv;
     p.G = s->h_q / s->h_kv;
-    p.kv_div = 1;
+    p.kv_mul = 0u;
     p.n_cap = s->n_cap;
     p.nranges = lay.nranges;
     p.dist = at<uint32_t>(ws, lay.off_dist);
@@ -371,7 +371,7 @@ uint32_t next_call_tag() {
 // dense group path, which take at most kMaxHeadsPerPass query heads per KV head:
 // with G = h_q / h_kv above that, each KV head's heads are split into k groups of
 // G / k (the smallest such k; G itself when nothing smaller divides G), which run
-// as k virtual KV heads that read the same codes and rows (kv_div = k). A grid so
+// as k virtual KV heads that read the same codes and rows (kv_magic(k)). A grid so
 // small that even twice its CTAs leave SMs idle splits four heads into two groups
 // of two: twice the CTAs, each with half the masks and rows. Wider codes keep the
 // two-kernel path, which takes any G (1).
@@ -386,7 +386,7 @@ int kv_split(const ha_shape& s, int code_words) {
 }
 
 // The shape with k virtual KV heads per KV head (the strides stay those of the
-// real heads; the kernels divide a virtual head by kv_div).
+// real heads; the kernels map a virtual head g to the real head g / k).
 ha_shape virtual_shape(const ha_shape& s, int k) {
     ha_shape v = s;
     v.h_kv = s.h_kv * k;
@@ -409,7 +409,7 @@ FusedSelParams dense_sel_params(const ha_shape* s, const Views& v, const int32_t
     p.Hq = s->h_q;
     p.Hkv = s->h_kv;
     p.G = s->h_q / s->h_kv;
-    p.kv_div = 1;
+    p.kv_mul = 0u;
     p.n_cap = s->n_cap;
     p.nranges = fused_ranges(s->n_cap);
     p.err = v.err;
@@ -461,7 +461,7 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
     }
 
     GatherParams gp = gather_params(s, lay, v, q, K, V, seq_lens, out, lse);
-    gp.kv_div = kdiv;
+    gp.kv_mul = kv_magic(kdiv);
     if (dense) {
         HA_TRY(record(events, 0, st));
         HA_TRY(record(events, 1, st));
@@ -471,7 +471,7 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
             // for the whole group
             GroupAttParams ga{};
             ga.sel = dense_sel_params(s, v, seq_lens);
-            ga.sel.kv_div = kdiv;
+            ga.sel.kv_mul = kv_magic(kdiv);
             ga.att = gp;
             ga.nsplit = group_dense_splits(bhkv, s->n_cap);
             HA_LAUNCH(launch_group_dense(ga, s->d, bhkv, st, true), "GATHER-ATT launch");
@@ -491,7 +491,7 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
         GroupAttParams ga{};
         ga.sel = fused_params(s, lay, ws, v, q_sig, k_sig, seq_lens, m_per_seq, m, n_sink, n_local, opts, v.list,
                               v.lcnt, 0);
-        ga.sel.kv_div = kdiv;
+        ga.sel.kv_mul = kv_magic(kdiv);
         ga.sel.ready = at<uint32_t>(ws, lay.off_ready);
         ga.sel.epoch = next_call_tag();
         ga.att = gp;
@@ -511,7 +511,7 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
         const bool to_caller = sel_idx != nullptr;
         FusedSelParams cp = fused_params(s, lay, ws, v, q_sig, k_sig, seq_lens, m_per_seq, m, n_sink, n_local, opts,
                                          to_caller ? sel_idx : v.list, to_caller ? sel_cnt : v.lcnt, to_caller ? 1 : 0);
-        cp.kv_div = kdiv;
+        cp.kv_mul = kv_magic(kdiv);
         gp.mode = kList;
         gp.list_idx = cp.list;
         gp.list_cnt = cp.cnt;

@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(kGatherThreads, (D * sizeof(KT) <= 256) ? 5 : 
     __syncthreads();
 
     // ---- per-warp pipeline over 8-row tiles
-    const int gk = g / p.kv_div;  // the KV head of this query-head group
+    const int gk = kv_head(g, p.kv_mul);  // the KV head of this query-head group
     const char* Kb = p.K + ((int64_t)b * p.k_sb + (int64_t)gk * p.k_sh) * C::ES;
     const char* Vb = p.V + ((int64_t)b * p.v_sb + (int64_t)gk * p.v_sh) * C::ES;
     const int64_t kstep = p.k_sn * C::ES, vstep = p.v_sn * C::ES;

@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(32 * NW, GCfg<D, ST, NW>::MINB) k_group_att(co
     // codes and the query codes alone. With eight warps (small grids, where the
     // wait is on the critical path) the first block's come before the wait; with
     // four, the registers are kept for the attention loop.
-    const uint32_t* crow = p.k_sig + (int64_t)b * p.ks_sb + (int64_t)(g / p.kv_div) * p.ks_sh;
+    const uint32_t* crow = p.k_sig + (int64_t)b * p.ks_sb + (int64_t)kv_head(g, p.kv_mul) * p.ks_sh;
     auto distances = [&](int it, uint32_t (&Dw)[32]) {
         const int lb = lo + (it * kGT + tid) * 32;
         const uint32_t valid = low_bits(n - lb);
@@ -428,7 +428,7 @@ __global__ void __launch_bounds__(32 * NW, GCfg<D, ST, NW>::MINB) k_group_att(co
     const int rem = lane - sub * (2 * C::NCH);
     const int isv = rem >= C::NCH ? 1 : 0;
     const int ch = rem - isv * C::NCH;
-    const int gk = g / a.kv_div;  // the KV head of this query-head group
+    const int gk = kv_head(g, a.kv_mul);  // the KV head of this query-head group
     const char* cbase = (isv ? a.V + ((int64_t)b * a.v_sb + (int64_t)gk * a.v_sh) * 2
                              : a.K + ((int64_t)b * a.k_sb + (int64_t)gk * a.k_sh) * 2) + ch * 16;
     const int cstep = (int)(isv ? a.v_sn * 2 : a.k_sn * 2);  // < 2^31 (checked on the host)

@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(kSelThreads, WD ? 5 : 8) k_sel_scan(const Fuse
     __syncthreads();
 
     {
-        const uint32_t* row = p.k_sig + (int64_t)b * p.ks_sb + (int64_t)(g / p.kv_div) * p.ks_sh;
+        const uint32_t* row = p.k_sig + (int64_t)b * p.ks_sb + (int64_t)kv_head(g, p.kv_mul) * p.ks_sh;
         const uint32_t col = smem_addr(&hist[0][0][lane]);
         uint4 v[U];
         auto load = [&](int k) {
@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(kSelThreads, WD ? 5 : 8) k_sel_scan(const Fuse
         // the window parts of this range: [lo, min(hi, wlo)) and [max(lo, wmid), hi)
         const int a0 = lo, a1 = min(hi, wlo), b0 = max(lo, wmid), b1 = hi;
         const int na = max(0, a1 - a0), nb = max(0, b1 - b0);
-        const uint32_t* crow = p.k_sig + (int64_t)b * p.ks_sb + (int64_t)(g / p.kv_div) * p.ks_sh;
+        const uint32_t* crow = p.k_sig + (int64_t)b * p.ks_sb + (int64_t)kv_head(g, p.kv_mul) * p.ks_sh;
         for (int x = tid; x < na + nb; x += NT) {
             const int i = x < na ? a0 + x : b0 + (x - na);
             uint32_t w = 0u;
