@@ -42,8 +42,8 @@ GATHER_SOURCE = os.path.join(ROOT, "long_context_sparse_score_gb300", "csrc", "k
 # the L2 holds what the step left there: the codes the scan has just read). It
 # holds only for the k_group_att.cu code it was taken on: the key hashes the
 # source without its comments and blank lines (source_code_key).
-GATHER_TRAFFIC = {"code_sha256": "e5080d56c74eea376bc1676919e0a0235d6a6250ff4bbb8adf0371f5f447985a",
-                  "bytes_per_launch": 1052332800 + 2016256}
+GATHER_TRAFFIC = {"code_sha256": "0aede477ef3530a324cf8285dde27c61c2f99bffbb0b4720226aafc160136e01",
+                  "bytes_per_launch": 1054095360 + 2036224}
 
 
 def parse_args():
