@@ -372,17 +372,21 @@ uint32_t next_call_tag() {
 // with G = h_q / h_kv above that, each KV head's heads are split into k groups of
 // G / k (the smallest such k; G itself when nothing smaller divides G), which run
 // as k virtual KV heads that read the same codes and rows (kv_magic(k)). A grid so
-// small that even twice its CTAs leave SMs idle splits four heads into two groups
-// of two: twice the CTAs, each with half the masks and rows. Wider codes keep the
-// two-kernel path, which takes any G (1).
+// small that even twice its CTAs leave SMs idle splits groups of four heads once
+// more, into two of two: twice the CTAs, each with half the masks and rows. Wider
+// codes keep the two-kernel path, which takes any G (1).
 int kv_split(const ha_shape& s, int code_words) {
     const int G = s.h_q / s.h_kv;
     if (code_words != 1) return 1;
-    if (G == kMaxHeadsPerPass && (int64_t)s.batch * s.h_kv * fused_ranges(s.n_cap) * 4 < kSMs) return 2;
-    if (G <= kMaxHeadsPerPass) return 1;
-    for (int k = (G + kMaxHeadsPerPass - 1) / kMaxHeadsPerPass; k < G; ++k)
-        if (G % k == 0) return k;
-    return G;
+    int k = G;
+    for (int c = (G + kMaxHeadsPerPass - 1) / kMaxHeadsPerPass; c < G; ++c)
+        if (G % c == 0) {
+            k = c;
+            break;
+        }
+    if (G <= kMaxHeadsPerPass) k = 1;
+    if (G / k == kMaxHeadsPerPass && (int64_t)s.batch * s.h_kv * k * fused_ranges(s.n_cap) * 4 < kSMs) k *= 2;
+    return k;
 }
 
 // The shape with k virtual KV heads per KV head (the strides stay those of the
