@@ -289,15 +289,17 @@ ha_status hash_attn_select_ex(const ha_shape* shape, const uint32_t* q_sig, cons
  * no allocation). It depends only on the shape and the code width, so it also
  * fixes the layout that hash_attn_workspace_size(_ex) sizes.
  *   code_words  words per code (1 = the 32-bit codes of HashAttention Eq. (2))
- *   fused       1: each distance is computed once (32-bit codes, at most 4 query
- *               heads per KV head): a scan kernel writes the packed distances
- *               and per-range histograms, an emit kernel writes the lists;
+ *   fused       1: the decode computes each distance once (32-bit codes; a KV
+ *               head with more than 4 query heads runs as groups of at most 4):
+ *               a scan kernel writes per-range histograms, then the group kernel
+ *               (or, with selection outputs, an emit kernel) builds the masks;
  *               0: the two-kernel path that recomputes the distances in TOPK
- *   ranges      CTAs of 8192 tokens per (batch entry, KV head) of the fused
- *               kernels (0 if not fused)
+ *   ranges      CTAs of 8192 tokens per (batch entry, KV head group) of the
+ *               fused kernels (0 if not fused)
  *   range       8192 (tokens per fused CTA), 0 if not fused
- *   chunk       tokens per CTA of the two-kernel SCORE/TOPK (also used by
- *               hash_attn_score whatever `fused` says)
+ *   chunk       tokens per CTA of the two-kernel SCORE/TOPK (used by
+ *               hash_attn_score, and by hash_attn_select for more than 4 query
+ *               heads per KV head, whatever `fused` says)
  * Any output pointer may be NULL. HA_ERR_INVALID_ARG / HA_ERR_UNSUPPORTED as
  * hash_attn_workspace_size for a bad shape or code width.
  */
