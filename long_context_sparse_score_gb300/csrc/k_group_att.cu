@@ -169,6 +169,10 @@ __global__ void __launch_bounds__(32 * NW, GCfg<D, ST, NW>::MINB) k_group_att(co
     const int g = lin / p.nranges;
     const int pair = b * p.Hkv + g;
     const int n = checked_len(p.seq_lens, b, p.n_cap, p.err, range == 0 && g == 0 && split == 0 && tid == 0);
+    // ranges past the sequence's end hold no rows: their CTAs leave at once, and
+    // the pair's parts are those of the live ranges (range 0 always runs)
+    const int live = max(1, (n + kFusedRange - 1) / kFusedRange);
+    if (range >= live) return;
     const int lo = range * kFusedRange;
     const int head0 = b * p.Hq + g * p.G;
     const int nh = p.G;  // at most 4 (checked on the host)
@@ -597,7 +601,8 @@ __global__ void __launch_bounds__(32 * NW, GCfg<D, ST, NW>::MINB) k_group_att(co
     }
     __syncthreads();
     constexpr float kLn2 = 0.69314718055994530942f;
-    const int nparts = p.nranges * S;  // partials per head
+    const int nparts = p.nranges * S;  // partials per head (the stride of a head's parts)
+    const int nlive = live * S;        // the parts this pair's live ranges write
     for (int x = tid; x < nh * D; x += kGT) {
         const int e = x / D, dd = x - e * D;
         float M = -CUDART_INF_F;
@@ -616,7 +621,7 @@ __global__ void __launch_bounds__(32 * NW, GCfg<D, ST, NW>::MINB) k_group_att(co
             }
         }
         const int64_t head = head0 + e;
-        if (nparts == 1) {
+        if (nlive == 1) {
             a.out[head * D + dd] = (Ls > 0.f) ? O / Ls : 0.f;
             if (dd == 0) a.lse[head] = (Ls > 0.f) ? (M + log2f(Ls)) * kLn2 : -CUDART_INF_F;
         } else {
@@ -628,7 +633,7 @@ __global__ void __launch_bounds__(32 * NW, GCfg<D, ST, NW>::MINB) k_group_att(co
             }
         }
     }
-    if (nparts == 1) {
+    if (nlive == 1) {
         if (tid == 0 && p.ready != nullptr) p.ready[pair] = 0u;
         return;
     }
@@ -637,8 +642,8 @@ __global__ void __launch_bounds__(32 * NW, GCfg<D, ST, NW>::MINB) k_group_att(co
     if (tid == 0) {
         __threadfence();
         const unsigned prev = atomicAdd(&a.counters[pair], 1u);
-        if (prev >= (unsigned)nparts) flag_error(p.err, HA_DEVERR_STATE);
-        s_last = (prev == (unsigned)(nparts - 1)) ? 1 : 0;
+        if (prev >= (unsigned)nlive) flag_error(p.err, HA_DEVERR_STATE);
+        s_last = (prev == (unsigned)(nlive - 1)) ? 1 : 0;
     }
     __syncthreads();
     if (!s_last) return;
@@ -656,7 +661,7 @@ __global__ void __launch_bounds__(32 * NW, GCfg<D, ST, NW>::MINB) k_group_att(co
     if (warp < nh) {
         const float* ph = a.part + (int64_t)(head0 + warp) * nparts * (D + 2);
         float M = -CUDART_INF_F;
-        for (int r = lane; r < nparts; r += 32) M = fmaxf(M, __ldcg(ph + (int64_t)r * (D + 2)));
+        for (int r = lane; r < nlive; r += 32) M = fmaxf(M, __ldcg(ph + (int64_t)r * (D + 2)));
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
         if (lane == 0) s_ml[warp] = M;
@@ -665,8 +670,8 @@ __global__ void __launch_bounds__(32 * NW, GCfg<D, ST, NW>::MINB) k_group_att(co
 #pragma unroll
     for (int i = 0; i < kItems; ++i) O[i] = 0.f;
     float Ls = 0.f;  // per lane of the head's warp
-    for (int r0 = 0; r0 < nparts; r0 += kMB) {
-        const int rn = min(kMB, nparts - r0);
+    for (int r0 = 0; r0 < nlive; r0 += kMB) {
+        const int rn = min(kMB, nlive - r0);
         __syncthreads();  // the maxima are written; the previous block's weights are read
         if (warp < nh) {
             const float M = s_ml[warp];

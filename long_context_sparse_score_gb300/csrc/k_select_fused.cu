@@ -79,6 +79,9 @@ __global__ void __launch_bounds__(kSelThreads, WD ? 5 : 8) k_sel_scan(const Fuse
     const int b = blockIdx.x % p.B, range = (blockIdx.x / p.B) % p.nranges, g = blockIdx.x / (p.B * p.nranges);
     const int pair = b * p.Hkv + g;
     const int n = checked_len(p.seq_lens, b, p.n_cap, p.err, range == 0 && g == 0 && tid == 0);
+    // ranges past the sequence's end hold no tokens: they leave at once, and the
+    // pair's last CTA counts only the live ones (range 0 always runs)
+    if (range > 0 && range * R >= n) return;
     const int lo = min(n, range * R);
     const int hi = min(n, lo + R);
     const int head0 = b * p.Hq + g * p.G;
@@ -241,9 +244,10 @@ __global__ void __launch_bounds__(kSelThreads, WD ? 5 : 8) k_sel_scan(const Fuse
     __syncthreads();  // every store of this CTA precedes thread 0's fence
     if (tid == 0) {
         __threadfence();
+        const unsigned live = (unsigned)max(1, (n + R - 1) / R);  // the ranges that arrive
         const unsigned prev = atomicAdd(&p.arrive[pair], 1u);
-        if (prev >= (unsigned)p.nranges) flag_error(p.err, HA_DEVERR_STATE);
-        s_last = (prev == (unsigned)(p.nranges - 1)) ? 1 : 0;
+        if (prev >= live) flag_error(p.err, HA_DEVERR_STATE);
+        s_last = (prev == live - 1u) ? 1 : 0;
     }
     __syncthreads();
     if (!s_last) return;
