@@ -42,8 +42,8 @@ GATHER_SOURCE = os.path.join(ROOT, "long_context_sparse_score_gb300", "csrc", "k
 # the L2 holds what the step left there: the codes the scan has just read). It
 # holds only for the k_group_att.cu code it was taken on: the key hashes the
 # source without its comments and blank lines (source_code_key).
-GATHER_TRAFFIC = {"code_sha256": "0aede477ef3530a324cf8285dde27c61c2f99bffbb0b4720226aafc160136e01",
-                  "bytes_per_launch": 1054095360 + 2036224}
+GATHER_TRAFFIC = {"code_sha256": "407cada68f4b930cd0abe71f571b88364600fe2413c933ce1c655f1b59091117",
+                  "bytes_per_launch": 1052510720 + 1956352}
 
 
 def parse_args():
