@@ -556,15 +556,17 @@ def test_encode_mlp_queries_and_keys(d, q_dtype, hidden):
     assert int(flags.item()) & H.HA_DEVERR_INDEX
 
 
-@pytest.mark.parametrize("kind,exclusive", [("sign", False), ("mlp", False), ("mlp", True)])
-def test_decode_mapped_runs_the_map_ahead_of_score(kind, exclusive):
+@pytest.mark.parametrize("kind,exclusive,Hq", [("sign", False, 8), ("mlp", False, 8), ("mlp", True, 8),
+                                               ("sign", False, 16)])
+def test_decode_mapped_runs_the_map_ahead_of_score(kind, exclusive, Hq):
     """One decode step from raw q: the map writes the appended tokens' key codes
     and the query codes (as the stand-alone encoders give them, and matching the
     oracle's unambiguous bits), and the rest of the step equals
-    hash_attn_decode on those codes, bit for bit."""
+    hash_attn_decode on those codes, bit for bit (four and eight query heads per
+    KV head: groups of two, and of four, per KV head on this small grid)."""
     import copy
     H = GH.ha()
-    w = W().make_gqa(41, B=3, Hq=8, Hkv=2, d=128, n_cap=4000, seq_lens=[4000, 3001, 1234], m=300, n_sink=16,
+    w = W().make_gqa(41, B=3, Hq=Hq, Hkv=2, d=128, n_cap=4000, seq_lens=[4000, 3001, 1234], m=300, n_sink=16,
                      n_local=32, device="cuda")
     pos = (w.seq_lens - 1).to(torch.int32)
     k_sig = w.k_sig.clone()
