@@ -307,6 +307,35 @@ ha_status hash_attn_selection_plan(const ha_shape* shape, int32_t code_words, in
                                    int32_t* ranges, int32_t* range, int32_t* chunk);
 
 /*
+ * The kernels hash_attn_decode_ex (and hash_attn_decode, hash_attn_decode_host)
+ * runs for this shape, budget and options; nothing is launched and no pointer is
+ * read. HashAttention Sec. 4 defines what every path computes; they differ only
+ * in how:
+ *   HA_PATH_DENSE_GROUP  m >= n_cap with no smaller budget: every token, one CTA
+ *                        per (batch entry, KV head group, span of a range)
+ *   HA_PATH_DENSE_HEADS  the same on the per-head GATHER-ATT, for what the
+ *                        group kernel does not take (an fp32 query or cache,
+ *                        d other than 64 or 128)
+ *   HA_PATH_GROUP        the SCORE/TOPK scan, then one kernel per (batch entry,
+ *                        KV head group, range) over the union of the group's rows
+ *   HA_PATH_FUSED_LISTS  selection outputs requested: one SCORE/TOPK kernel
+ *                        writing the lists, then the per-head GATHER-ATT
+ *   HA_PATH_TWO_KERNEL   code_words > 1: SCORE, TOPK and the per-head GATHER-ATT
+ * with_selection: nonzero when sel_idx / sel_cnt will be given. m_per_seq only
+ * matters for being NULL or not. Errors as hash_attn_workspace_size for a bad
+ * shape or options; HA_ERR_INVALID_ARG for m < 0 or a NULL path.
+ */
+enum {
+    HA_PATH_DENSE_GROUP = 1,
+    HA_PATH_DENSE_HEADS = 2,
+    HA_PATH_GROUP = 3,
+    HA_PATH_FUSED_LISTS = 4,
+    HA_PATH_TWO_KERNEL = 5
+};
+ha_status hash_attn_decode_path(const ha_shape* shape, int32_t m, const int32_t* m_per_seq,
+                                const ha_select_opts* opts, int32_t with_selection, int32_t* path);
+
+/*
  * GATHER-ATT + merge over caller-given index lists (page size 1, read in place):
  *   idx  [batch, h_q, idx_cap] int32 token indices (any order, no duplicates
  *        expected; each must lie in [0, seq_lens[b]) or it is skipped and

@@ -420,6 +420,25 @@ FusedSelParams dense_sel_params(const ha_shape* s, const Views& v, const int32_t
     return p;
 }
 
+// The kernels a decode call runs (hash_attn_decode_path reports what decode_impl
+// takes): the budget and options and whether the selection is returned. *kdiv:
+// virtual KV heads per real one.
+int decode_path(const ha_shape& s, int32_t m, const int32_t* m_per_seq, const ha_select_opts* opts, bool with_sel,
+                int* kdiv) {
+    const bool dense = (m >= s.n_cap) && (m_per_seq == nullptr) && (opts == nullptr || opts->m_per_head == nullptr);
+    const int W = code_words_of(opts);
+    // more than kMaxHeadsPerPass query heads per KV head: virtual KV heads
+    *kdiv = kv_split(s, W);
+    const ha_shape v = virtual_shape(s, *kdiv);
+    if (dense) return dense_group(v) ? HA_PATH_DENSE_GROUP : HA_PATH_DENSE_HEADS;
+    const bool fused = fused_selection(v, W);
+    if (fused && !with_sel &&
+        group_att_supported(v.d, v.kv_dtype == HA_BF16, v.q_dtype == HA_BF16, v.h_q / v.h_kv) &&
+        v.k_sn < (int64_t(1) << 30) && v.v_sn < (int64_t(1) << 30))
+        return HA_PATH_GROUP;
+    return fused ? HA_PATH_FUSED_LISTS : HA_PATH_TWO_KERNEL;
+}
+
 // The signature map run ahead of SCORE (hash_attn_decode_mapped): the appended
 // tokens' key codes (optional) and the step's query codes.
 struct MapStep {
@@ -438,11 +457,12 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
     if (q == nullptr || seq_lens == nullptr || out == nullptr || lse == nullptr)
         return fail(HA_ERR_INVALID_ARG, "q, seq_lens, out and lse must not be NULL");
     HA_TRY(check_kv(s, K, V));
-    const bool dense = (m >= s->n_cap) && (m_per_seq == nullptr) && (opts == nullptr || opts->m_per_head == nullptr);
+    int kdiv = 1;
+    const int path = decode_path(*s, m, m_per_seq, opts, sel_idx != nullptr, &kdiv);
+    const bool dense = path == HA_PATH_DENSE_GROUP || path == HA_PATH_DENSE_HEADS;
     const int W = code_words_of(opts);
-    // more than kMaxHeadsPerPass query heads per KV head: virtual KV heads (the
-    // checks above ran on the caller's shape; strides and pointers are the same)
-    const int kdiv = kv_split(*s, W);
+    // with virtual KV heads the checks above ran on the caller's shape; strides and
+    // pointers are the same
     const ha_shape vshape = virtual_shape(*s, kdiv);
     s = &vshape;
     if (!dense) HA_TRY(W > 1 ? check_wide_codes(s, q_sig, k_sig, W) : check_codes(s, q_sig, k_sig));
@@ -470,7 +490,7 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
         HA_TRY(record(events, 0, st));
         HA_TRY(record(events, 1, st));
         HA_TRY(record(events, 2, st));
-        if (dense_group(*s)) {
+        if (path == HA_PATH_DENSE_GROUP) {
             // one CTA per (batch entry, KV head, span of a range): each K/V row once
             // for the whole group
             GroupAttParams ga{};
@@ -487,9 +507,7 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
         return HA_OK;
     }
     HA_TRY(record(events, 0, st));
-    if (lay.fused && sel_idx == nullptr &&
-        group_att_supported(s->d, s->kv_dtype == HA_BF16, s->q_dtype == HA_BF16, s->h_q / s->h_kv) &&
-        s->k_sn < (int64_t(1) << 30) && s->v_sn < (int64_t(1) << 30)) {
+    if (path == HA_PATH_GROUP) {
         // the scan's thresholds, then one kernel per GQA group that builds the masks
         // in place and attends over the union of the group's rows
         GroupAttParams ga{};
@@ -509,7 +527,7 @@ ha_status decode_impl(const ha_shape* s, const void* q, const uint32_t* q_sig, c
         HA_TRY(record(events, 3, st));
         return HA_OK;
     }
-    if (lay.fused) {
+    if (path == HA_PATH_FUSED_LISTS) {
         // SCORE and TOPK in one cluster kernel writing flat ascending lists: into the
         // caller's sel_idx (padded with -1) when given, else into the workspace
         const bool to_caller = sel_idx != nullptr;
@@ -826,6 +844,17 @@ ha_status hash_attn_selection_plan(const ha_shape* shape, int32_t code_words, in
     if (ranges) *ranges = f ? fused_ranges(shape->n_cap) : 0;
     if (range) *range = f ? 8192 : 0;
     if (chunk) *chunk = choose_chunk((int64_t)shape->batch * shape->h_kv, shape->n_cap);
+    return HA_OK;
+}
+
+ha_status hash_attn_decode_path(const ha_shape* shape, int32_t m, const int32_t* m_per_seq,
+                                const ha_select_opts* opts, int32_t with_selection, int32_t* path) {
+    HA_TRY(check_shape(shape));
+    HA_TRY(check_opts(opts));
+    if (m < 0) return fail(HA_ERR_INVALID_ARG, "m must be >= 0 (got %d)", m);
+    if (path == nullptr) return fail(HA_ERR_INVALID_ARG, "path is NULL");
+    int kdiv = 1;
+    *path = decode_path(*shape, m, m_per_seq, opts, with_selection != 0, &kdiv);
     return HA_OK;
 }
 

@@ -39,7 +39,7 @@ EXPORTED = [
     "hash_attn_workspace_size", "hash_attn_workspace_init", "hash_attn_select_capacity",
     "hash_attn_decode", "hash_attn_decode_ex", "hash_attn_decode_timed", "hash_attn_decode_host",
     "hash_attn_host_staging_size", "hash_attn_score", "hash_attn_select",
-    "hash_attn_select_ex", "hash_attn_workspace_size_ex", "hash_attn_selection_plan",
+    "hash_attn_select_ex", "hash_attn_workspace_size_ex", "hash_attn_selection_plan", "hash_attn_decode_path",
     "hash_attn_gather_att", "hash_attn_gather_att_noalloc", "hash_attn_merge", "hash_attn_merge_n",
     "hash_attn_encode_queries", "hash_attn_encode_keys", "hash_attn_encode_queries_mlp",
     "hash_attn_encode_keys_mlp", "hash_attn_decode_mapped", "hash_attn_topk_exact_workspace_size",
@@ -150,6 +150,7 @@ def lib() -> ctypes.CDLL:
     L.hash_attn_decode_timed.argtypes = dec + [ctypes.POINTER(_P)]
     IP = ctypes.POINTER(_I32)
     L.hash_attn_selection_plan.argtypes = [SP, _I32, IP, IP, IP, IP]
+    L.hash_attn_decode_path.argtypes = [SP, _I32, _P, OP, _I32, IP]
     L.hash_attn_host_staging_size.argtypes = [SP, ctypes.POINTER(_SZ)]
     L.hash_attn_decode_host.argtypes = [SP, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P, _SZ, _P, _SZ,
                                         _P]
@@ -302,6 +303,19 @@ def hash_attn_selection_plan(shape, code_words: int = 1) -> dict:
     v = [ctypes.c_int32(0) for _ in range(4)]
     _check(lib().hash_attn_selection_plan(ctypes.byref(shape), int(code_words), *(ctypes.byref(x) for x in v)))
     return dict(zip(("fused", "ranges", "range", "chunk"), (x.value for x in v)))
+
+
+# decode paths (hash_attn_decode_path)
+PATHS = {1: "dense_group", 2: "dense_heads", 3: "group", 4: "fused_lists", 5: "two_kernel"}
+
+
+def hash_attn_decode_path(shape, m: int, m_per_seq=None, opts=None, with_selection: bool = False) -> str:
+    """The kernels a decode call with this shape, budget and options runs (a name of PATHS)."""
+    out = ctypes.c_int32(0)
+    _check(lib().hash_attn_decode_path(ctypes.byref(shape), int(m), _ptr(m_per_seq),
+                                       None if opts is None else ctypes.byref(opts), 1 if with_selection else 0,
+                                       ctypes.byref(out)))
+    return PATHS[out.value]
 
 
 def hash_attn_decode_ex(shape, q, q_sig, k_sig, K, V, seq_lens, m_per_seq, m, n_sink, n_local, opts,

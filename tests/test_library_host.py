@@ -98,6 +98,36 @@ def test_selection_plan_of_the_workloads(ha):
         _plan(ha, 1, 4, 1, 4096, code_words=3)
 
 
+def test_decode_path_reports_the_kernels(ha):
+    """hash_attn_decode_path (host only: nothing is launched). The batch-16 128K
+    shape and the shared 61,440-token document take the GQA-group kernel; with
+    selection outputs the fused lists; 128-bit codes the two-kernel path; m >=
+    n_cap the dense group kernel, or the per-head one for an fp32 cache; a
+    per-sequence budget keeps the selection even at m = n_cap."""
+    n = 131072
+    s = _shape(ha, batch=16, h_q=32, h_kv=8, n_cap=n, q_sb=32 * 128, k_sb=8 * n * 128, k_sh=n * 128,
+               v_sb=8 * n * 128, v_sh=n * 128, ks_sb=8 * n, ks_sh=n)
+    P = ha.hash_attn_decode_path
+    assert P(s, 4096) == "group"
+    assert P(s, 4096, with_selection=True) == "fused_lists"
+    assert P(s, 4096, opts=ha.select_opts(None, False, 4)) == "two_kernel"
+    assert P(s, n) == "dense_group"
+    assert P(s, n, m_per_seq=1 << 20) == "group"
+    s32 = _shape(ha, batch=16, h_q=32, h_kv=8, n_cap=n, q_sb=32 * 128, k_sb=8 * n * 128, k_sh=n * 128,
+                 v_sb=8 * n * 128, v_sh=n * 128, ks_sb=8 * n, ks_sh=n, kv_dtype=ha.HA_F32)
+    assert P(s32, n) == "dense_heads"
+    nd = 61440
+    doc = _shape(ha, batch=32, h_q=32, h_kv=8, n_cap=nd, q_sb=32 * 128, k_sb=0, k_sh=nd * 128, v_sb=0,
+                 v_sh=nd * 128, ks_sb=0, ks_sh=nd)
+    assert P(doc, 2048) == "group"
+    # eight query heads per KV head: virtual groups of four on the group kernel
+    s8 = _shape(ha, batch=2, h_q=64, h_kv=8, n_cap=n, q_sb=64 * 128, k_sb=8 * n * 128, k_sh=n * 128,
+                v_sb=8 * n * 128, v_sh=n * 128, ks_sb=8 * n, ks_sh=n)
+    assert P(s8, 4096) == "group"
+    with pytest.raises(ha.HashAttnError):
+        P(s, -1)
+
+
 def test_fused_workspace_is_sized_by_the_budget_not_the_context(ha):
     """With the fused kernel the token lists take heads x (m + n_sink + n_local) ints,
     not heads x n_cap: at the 16 x 131,072-token shape well under 100 MB."""
